@@ -1,0 +1,142 @@
+"""Plain fp64 CPU oracle for jagged attention -- TEST INFRASTRUCTURE ONLY.
+
+Only ``tests/``, the smoke check in ``__graft_entry__`` and the CPU-baseline leg
+of ``bench.py`` may import this package.  The product path (the CUDA library
+``libjfa`` and its Python binding) never imports, links or calls it, and the
+two share no code: the arithmetic lives in ``jfa_oracle.c`` (plain loops in
+double precision, one (sequence, head) pair at a time) and this module only
+marshals numpy arrays into it.
+
+Sources for the definitions (restated in ``jfa_oracle.c``):
+Meta GEM MFU co-design write-up (piletech.kr/articles/112134), details
+section: jagged-input bullet, Jagged Flash Attention bullet (attention directly
+on variable-length tensors; self / cross / asymmetric-QKV patterns) and the
+Generalized Dot-Product Attention bullet (non-softmax activation).  The
+library fixes that activation to SiLU(u)/L with L the sequence length.
+
+Every oracle function here has independent pins in ``tests/test_oracle_pins.py``
+(50-digit brute force, finite differences, padded dense attention through
+torch autograd, closed forms and invariants).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "jfa_oracle.c")
+_LIB_DIR = os.path.join(_HERE, "_build")
+_LIB = os.path.join(_LIB_DIR, "libjfa_oracle.so")
+
+ACT_SOFTMAX = 0
+ACT_SILU_OVER_LEN = 1
+
+_ERRORS = {1: "bad arguments", 2: "bad offsets", 3: "out of memory"}
+
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile the C oracle with gcc (OpenMP, -O3, portable flags) and return its path."""
+    os.makedirs(_LIB_DIR, exist_ok=True)
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + ".tmp%d" % os.getpid()
+        cmd = ["gcc", "-O3", "-std=c11", "-fopenmp", "-fPIC", "-shared", _SRC, "-o", tmp, "-lm"]
+        subprocess.run(cmd, check=True)
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(build())
+            i64p = ctypes.POINTER(ctypes.c_int64)
+            dp = ctypes.POINTER(ctypes.c_double)
+            common = [ctypes.c_int64, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, i64p, i64p,
+                      dp, dp, dp]
+            lib.oracle_fwd.argtypes = common + [ctypes.c_double, ctypes.c_int32, ctypes.c_int32,
+                                                dp, dp]
+            lib.oracle_fwd.restype = ctypes.c_int
+            lib.oracle_bwd.argtypes = common + [dp, ctypes.c_double, ctypes.c_int32,
+                                                ctypes.c_int32, dp, dp, dp]
+            lib.oracle_bwd.restype = ctypes.c_int
+            _lib = lib
+    return _lib
+
+
+def _f64(a):
+    return np.ascontiguousarray(np.asarray(a, dtype=np.float64))
+
+
+def _i64(a):
+    return np.ascontiguousarray(np.asarray(a, dtype=np.int64))
+
+
+def _ptr(a, ctype):
+    return a.ctypes.data_as(ctypes.POINTER(ctype))
+
+
+def _shapes(q, k, v, offs_q, offs_k):
+    if q.ndim != 3 or k.ndim != 3 or v.ndim != 3:
+        raise ValueError("q, k, v must be [T, H, D]")
+    B = offs_q.shape[0] - 1
+    if offs_k.shape[0] != B + 1 or B < 0:
+        raise ValueError("offs_q and offs_k must both have B+1 entries")
+    Tq, H, Dqk = q.shape
+    Tk, Hk, Dk = k.shape
+    if Hk != H or Dk != Dqk or v.shape[0] != Tk or v.shape[1] != H:
+        raise ValueError("inconsistent q/k/v shapes")
+    if B >= 0 and (offs_q[-1] != Tq or offs_k[-1] != Tk):
+        raise ValueError("offsets must end at the row counts")
+    return B, Tq, Tk, H, Dqk, v.shape[2]
+
+
+def fwd(q, k, v, offs_q, offs_k=None, scale=None, causal=False, act=ACT_SOFTMAX):
+    """Forward pass.  q [Tq,H,Dqk], k [Tk,H,Dqk], v [Tk,H,Dv]; returns (o [Tq,H,Dv], lse [Tq,H])."""
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    offs_q = _i64(offs_q)
+    offs_k = offs_q if offs_k is None else _i64(offs_k)
+    B, Tq, Tk, H, Dqk, Dv = _shapes(q, k, v, offs_q, offs_k)
+    if scale is None:
+        scale = 1.0 / np.sqrt(Dqk)
+    o = np.zeros((Tq, H, Dv), dtype=np.float64)
+    lse = np.zeros((Tq, H), dtype=np.float64)
+    lib = _load()
+    dp = ctypes.c_double
+    rc = lib.oracle_fwd(B, H, Dqk, Dv, _ptr(offs_q, ctypes.c_int64), _ptr(offs_k, ctypes.c_int64),
+                        _ptr(q, dp), _ptr(k, dp), _ptr(v, dp), float(scale), int(bool(causal)),
+                        int(act), _ptr(o, dp), _ptr(lse, dp))
+    if rc:
+        raise ValueError("oracle_fwd: " + _ERRORS.get(rc, str(rc)))
+    return o, lse
+
+
+def bwd(q, k, v, dout, offs_q, offs_k=None, scale=None, causal=False, act=ACT_SOFTMAX):
+    """Backward pass.  Returns (dq, dk, dv) with the shapes of q, k, v."""
+    q, k, v, dout = _f64(q), _f64(k), _f64(v), _f64(dout)
+    offs_q = _i64(offs_q)
+    offs_k = offs_q if offs_k is None else _i64(offs_k)
+    B, Tq, Tk, H, Dqk, Dv = _shapes(q, k, v, offs_q, offs_k)
+    if dout.shape != (Tq, H, Dv):
+        raise ValueError("dout must be [Tq, H, Dv]")
+    if scale is None:
+        scale = 1.0 / np.sqrt(Dqk)
+    dq = np.zeros_like(q)
+    dk = np.zeros_like(k)
+    dv = np.zeros_like(v)
+    lib = _load()
+    dp = ctypes.c_double
+    rc = lib.oracle_bwd(B, H, Dqk, Dv, _ptr(offs_q, ctypes.c_int64), _ptr(offs_k, ctypes.c_int64),
+                        _ptr(q, dp), _ptr(k, dp), _ptr(v, dp), _ptr(dout, dp), float(scale),
+                        int(bool(causal)), int(act), _ptr(dq, dp), _ptr(dk, dp), _ptr(dv, dp))
+    if rc:
+        raise ValueError("oracle_bwd: " + _ERRORS.get(rc, str(rc)))
+    return dq, dk, dv
+

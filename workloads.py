@@ -1,0 +1,144 @@
+"""Seeded synthetic jagged-attention workloads, shared by the tests and the benchmark.
+
+This module holds no attention arithmetic: it only draws sequence lengths and
+input values, builds offsets, and counts FLOPs and bytes.  Both the CUDA path
+and the CPU oracle receive the arrays it returns.
+
+The pages this library follows measure on production ads traffic, which is not
+public; these seeded batches stand in for it.  Lengths come from
+``numpy.random.default_rng(seed)`` in a fixed draw order, so the sizes
+reproduce exactly; values are i.i.d. N(0, 1) drawn with a seeded
+``torch.Generator`` in the order Q, K, V, dO, then cast to the compute dtype.
+
+Workloads (named by what they are):
+
+``tiny``    B=4 self-attention, lengths {1, 7, 33, 64}, H=2, D=32, fp32, softmax.
+``d64``     B=256 self-attention, lengths uniform in [1, 512], H=4, D=64, bf16, softmax.
+``causal``  B=1024 causal self-attention over long user histories, lengths
+            lognormal(5.5, 0.8) rounded and clipped to [1, 2048], H=8, D=128, bf16.
+``cross``   B=512 asymmetric-QKV cross-attention, query lengths uniform in [1, 64],
+            key lengths uniform in [1, 4096], H=4, Dqk=128, Dv=64, bf16, softmax.
+``gdpa``    B=256 causal non-softmax attention P = SiLU(QK^T/sqrt(D))/L, lengths uniform
+            in [256, 4096], H=8, D=128, bf16.
+"""
+from __future__ import annotations
+
+import dataclasses
+import math
+
+import numpy as np
+import torch
+
+ACT_SOFTMAX = 0
+ACT_SILU_OVER_LEN = 1
+
+
+@dataclasses.dataclass(frozen=True)
+class Workload:
+    name: str
+    batch: int
+    heads: int
+    dim_qk: int
+    dim_v: int
+    causal: bool
+    act: int
+    dtype: torch.dtype
+    cross: bool
+
+    @property
+    def scale(self) -> float:
+        return 1.0 / math.sqrt(self.dim_qk)
+
+
+WORKLOADS = {
+    "tiny": Workload("tiny", 4, 2, 32, 32, False, ACT_SOFTMAX, torch.float32, False),
+    "d64": Workload("d64", 256, 4, 64, 64, False, ACT_SOFTMAX, torch.bfloat16, False),
+    "causal": Workload("causal", 1024, 8, 128, 128, True, ACT_SOFTMAX, torch.bfloat16, False),
+    "cross": Workload("cross", 512, 4, 128, 64, False, ACT_SOFTMAX, torch.bfloat16, True),
+    "gdpa": Workload("gdpa", 256, 8, 128, 128, True, ACT_SILU_OVER_LEN, torch.bfloat16, False),
+}
+
+
+def lengths(name: str, seed: int = 0):
+    """Per-sequence (query, key) lengths of a named workload, as int64 numpy arrays."""
+    rng = np.random.default_rng(seed)
+    if name == "tiny":
+        lq = np.array([1, 7, 33, 64], dtype=np.int64)
+        return lq, lq.copy()
+    if name == "d64":
+        lq = rng.integers(1, 512, 256, endpoint=True).astype(np.int64)
+        return lq, lq.copy()
+    if name == "causal":
+        lq = np.clip(np.rint(rng.lognormal(5.5, 0.8, 1024)), 1, 2048).astype(np.int64)
+        return lq, lq.copy()
+    if name == "cross":
+        lq = rng.integers(1, 64, 512, endpoint=True).astype(np.int64)
+        lk = rng.integers(1, 4096, 512, endpoint=True).astype(np.int64)
+        return lq, lk
+    if name == "gdpa":
+        lq = rng.integers(256, 4096, 256, endpoint=True).astype(np.int64)
+        return lq, lq.copy()
+    raise KeyError(name)
+
+
+def offsets(lens) -> np.ndarray:
+    """Exclusive prefix sum of the lengths, int64 [B+1]."""
+    lens = np.asarray(lens, dtype=np.int64)
+    out = np.zeros(lens.shape[0] + 1, dtype=np.int64)
+    np.cumsum(lens, out=out[1:])
+    return out
+
+
+def values(tq: int, tk: int, heads: int, dim_qk: int, dim_v: int, dtype: torch.dtype,
+           seed: int = 0, device="cpu"):
+    """Q [tq,H,Dqk], K [tk,H,Dqk], V [tk,H,Dv], dO [tq,H,Dv], N(0,1), drawn in that order."""
+    g = torch.Generator(device=device).manual_seed(seed)
+    shapes = [(tq, heads, dim_qk), (tk, heads, dim_qk), (tk, heads, dim_v), (tq, heads, dim_v)]
+    out = []
+    for s in shapes:
+        t = torch.randn(s, generator=g, dtype=torch.float32, device=device)
+        out.append(t.to(dtype))
+    return tuple(out)
+
+
+def make_batch(w: Workload, lq=None, lk=None, seed: int = 0, device="cpu"):
+    """A full input batch for workload ``w`` (or for explicit lengths, if given)."""
+    if lq is None:
+        lq, lk = lengths(w.name, seed)
+    lq = np.asarray(lq, dtype=np.int64)
+    lk = lq.copy() if lk is None else np.asarray(lk, dtype=np.int64)
+    oq, ok = offsets(lq), offsets(lk)
+    q, k, v, do = values(int(oq[-1]), int(ok[-1]), w.heads, w.dim_qk, w.dim_v, w.dtype, seed, device)
+    return dict(lq=lq, lk=lk, offs_q=oq, offs_k=ok, q=q, k=k, v=v, do=do)
+
+
+def valid_pairs(lq, lk, causal: bool) -> float:
+    """Number of (query, key) pairs that take part in attention, per head."""
+    lq = np.asarray(lq, dtype=np.float64)
+    lk = np.asarray(lk, dtype=np.float64)
+    if causal:
+        return float(np.sum(lq * (lq + 1) / 2))
+    return float(np.sum(lq * lk))
+
+
+def useful_flops(w: Workload, lq, lk):
+    """(forward, backward) useful FLOPs: no padding, no masked area, no recompute.
+
+    Forward: QK^T and PV, 2*P*H*(Dqk+Dv).  Backward: S recompute, dV, dP, dQ and
+    dK, 2*P*H*(3*Dqk+2*Dv).  P = valid pairs per head.
+    """
+    p = valid_pairs(lq, lk, w.causal)
+    return 2.0 * p * w.heads * (w.dim_qk + w.dim_v), 2.0 * p * w.heads * (3 * w.dim_qk + 2 * w.dim_v)
+
+
+def algorithmic_bytes(w: Workload, tq: int, tk: int):
+    """(forward, backward) minimum HBM bytes the method must move.
+
+    Forward reads Q, K, V and writes O and the fp32 log-sum-exp.  Backward reads
+    Q, K, V, O, dO and the log-sum-exp, writes dQ, dK, dV and the fp32 row term D.
+    """
+    e = torch.tensor([], dtype=w.dtype).element_size()
+    H, dq, dv = w.heads, w.dim_qk, w.dim_v
+    fwd = e * H * (tq * dq + tk * dq + tk * dv + tq * dv) + 4 * H * tq
+    bwd = e * H * (2 * tq * dq + 2 * tk * dq + 2 * tk * dv + 2 * tq * dv) + 8 * H * tq
+    return fwd, bwd
