@@ -1,0 +1,429 @@
+#!/usr/bin/env python3
+"""Benchmark of the jagged attention hot path: one step = forward + backward of one batch.
+
+Default workload: B=256 jagged self-attention, lengths uniform in [1, 512], H=4, D=64,
+bf16 inputs with fp32 accumulation, softmax, non-causal.  Metric: useful (unpadded)
+attention TFLOP/s of forward + backward; also reported as a fraction of the measured
+dense BF16 peak.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+Prints one JSON line (rank 0).  Under torchrun each rank runs an independent replica of
+the workload on its own GPU (the path has no cross-sequence exchange), timing is the
+maximum over ranks, and the value is the aggregate over all ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+import workloads  # noqa: E402
+
+METRIC = "useful (unpadded) attention TFLOP/s fwd+bwd on 1 GB300; % of dense BF16 peak"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+L2_FLUSH_BYTES = 256 << 20
+KERNEL_SOURCES = {"fwd": "tc_fwd.cu", "bwd_dkdv": "tc_bwd.cu", "bwd_dq": "tc_bwd.cu",
+                  "bwd_d": "simt.cu", "schedule": "sched.cu"}
+
+
+def log(*a):
+    print(*a, file=sys.stderr, flush=True)
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        out = {}
+        for key in ("hbm_gbs", "bf16_tflops", "bf16_tflops_sustained"):
+            val = d.get(key)
+            if isinstance(val, dict):
+                val = val.get("value")
+            out[key] = float(val)
+        return out, "measured"
+    except Exception:
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_flops_bytes(w, lq, lk, tq, tk):
+    """Algorithmic FLOPs and bytes of one launch of each kernel kind.
+
+    fwd:  QK^T and PV over the valid pairs; reads Q, K, V, writes O and lse.
+    dkdv: S^T and dP^T recompute, dV and dK products; reads Q, K, V, dO, lse, D, writes dK, dV.
+    dq:   S and dP recompute, dQ product; reads Q, K, V, dO, lse, D, writes dQ.
+    """
+    P = workloads.valid_pairs(lq, lk, w.causal)
+    H, dq, dv = w.heads, w.dim_qk, w.dim_v
+    e = 2 if w.dtype == torch.bfloat16 else 4
+    sm = w.act == workloads.ACT_SOFTMAX
+    rowb = 8 * H * tq if sm else 0
+    return {
+        "fwd": (2 * P * H * (dq + dv), e * H * (tq * dq + tk * dq + tk * dv + tq * dv) + (4 * H * tq if sm else 0)),
+        "bwd_dkdv": (2 * P * H * (2 * dq + 2 * dv),
+                     e * H * (tq * dq + tk * dq + tk * dv + tq * dv + tk * dq + tk * dv) + rowb),
+        "bwd_dq": (2 * P * H * (2 * dq + dv),
+                   e * H * (tq * dq + tk * dq + tk * dv + tq * dv + tq * dq) + rowb),
+        "bwd_d": (2 * H * tq * dv, e * H * 2 * tq * dv + 4 * H * tq),
+        "schedule": (0, 8 * (len(lq) + 1) * 2),
+    }
+
+
+def file_sha(name):
+    p = os.path.join(ROOT, "jagged_attention_recsys_gb300", "csrc", name)
+    try:
+        return hashlib.sha256(open(p, "rb").read()).hexdigest()[:16]
+    except OSError:
+        return None
+
+
+def measured_traffic(kind, workload):
+    """DRAM bytes per launch from a committed ncu capture, if the kernel source is unchanged."""
+    try:
+        d = json.load(open(os.path.join(ROOT, "profiles", "traffic.json")))
+        ent = d[workload][kind]
+    except Exception:
+        return None
+    if ent.get("source_sha") != file_sha(KERNEL_SOURCES.get(kind, "")):
+        return None
+    return ent.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index):
+        self.proc = None
+        self.dev = device_index
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.dev), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except Exception:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self):
+        if not getattr(self, "lines", None):
+            return None
+        sm, mx = [], []
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = set()
+        for l in self.lines:
+            parts = [x.strip() for x in l.split(",")]
+            if len(parts) < 6:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, val in zip(names, parts[2:6]):
+                if val.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+# ----------------------------------------------------------------------------- our arm
+def gpu_step_fn(jfa, w, d, ws):
+    q, k, v, do, oq, ok = d["q"], d["k"], d["v"], d["do"], d["oq"], d["ok"]
+    o, lse, dq, dk, dv = d["o"], d["lse"], d["dq"], d["dk"], d["dv"]
+    sc = w.scale
+    if w.act == workloads.ACT_SILU_OVER_LEN:
+        def step():
+            jfa.jfa_gdpa_fwd(q, k, v, oq, ok, scale=sc, causal=w.causal, o=o, ws=ws)
+            jfa.jfa_gdpa_bwd(q, k, v, do, oq, ok, scale=sc, causal=w.causal, dq=dq, dk=dk, dv=dv,
+                             ws=ws)
+    elif w.cross:
+        def step():
+            jfa.jfa_cross_fwd(q, k, v, oq, ok, scale=sc, o=o, lse=lse, ws=ws)
+            jfa.jfa_cross_bwd(q, k, v, o, lse, do, oq, ok, scale=sc, dq=dq, dk=dk, dv=dv, ws=ws)
+    else:
+        def step():
+            jfa.jfa_fwd(q, k, v, oq, scale=sc, causal=w.causal, o=o, lse=lse, ws=ws)
+            jfa.jfa_bwd(q, k, v, o, lse, do, oq, scale=sc, causal=w.causal, dq=dq, dk=dk, dv=dv,
+                        ws=ws)
+    return step
+
+
+def cpu_baseline(w, lq, lk, budget_s=12.0, seed=0):
+    """The fp64 oracle, as it stands, on a bounded seeded sample of the workload's sequences."""
+    import oracle
+
+    cores = len(os.sched_getaffinity(0))
+    os.environ.setdefault("OMP_NUM_THREADS", str(cores))
+    rng = np.random.default_rng(seed + 7)
+    order = rng.permutation(len(lq))
+    per_flop = 1.0 / (1.0e9 * cores)  # assumed ~1 GFLOP/s per core for plain fp64 loops
+    chosen, est = [], 0.0
+    for b in order:
+        f, g = workloads.useful_flops(w, [lq[b]], [lk[b]])
+        chosen.append(int(b))
+        est += (f + g) * per_flop
+        if est >= budget_s:
+            break
+    slq = [int(lq[b]) for b in chosen]
+    slk = [int(lk[b]) for b in chosen]
+    oq, ok = workloads.offsets(slq), workloads.offsets(slk)
+    q, k, v, do = workloads.values(int(oq[-1]), int(ok[-1]), w.heads, w.dim_qk, w.dim_v,
+                                   w.dtype, seed=seed)
+    f64 = lambda t: t.to(torch.float64).numpy()
+    q, k, v, do = f64(q), f64(k), f64(v), f64(do)
+    oracle.build()
+    t0 = time.perf_counter()
+    oracle.fwd(q, k, v, oq, ok, scale=w.scale, causal=w.causal, act=w.act)
+    oracle.bwd(q, k, v, do, oq, ok, scale=w.scale, causal=w.causal, act=w.act)
+    dt = time.perf_counter() - t0
+    f, g = workloads.useful_flops(w, slq, slk)
+    return {"value": (f + g) / dt / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+            "seconds": dt,
+            "sample": "%d of %d sequences (seeded), fp64 forward+backward, %.3g useful GFLOP"
+                      % (len(chosen), len(lq), (f + g) / 1e9)}
+
+
+def run_ours(args):
+    world, rank, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    import jagged_attention_recsys_gb300 as jfa
+
+    jfa.lib()
+    w = workloads.WORKLOADS[args.workload]
+    lq, lk = workloads.lengths(w.name, seed=0)
+    batch = workloads.make_batch(w, lq, lk, seed=0, device=dev)
+    d = dict(q=batch["q"], k=batch["k"], v=batch["v"], do=batch["do"],
+             oq=torch.as_tensor(batch["offs_q"], device=dev),
+             ok=torch.as_tensor(batch["offs_k"], device=dev))
+    tq, tk = d["q"].shape[0], d["k"].shape[0]
+    d["o"] = torch.empty(tq, w.heads, w.dim_v, dtype=w.dtype, device=dev)
+    d["lse"] = torch.empty(tq, w.heads, dtype=torch.float32, device=dev)
+    d["dq"] = torch.empty_like(d["q"])
+    d["dk"] = torch.empty_like(d["k"])
+    d["dv"] = torch.empty_like(d["v"])
+    p = jfa.params_for(d["q"], d["k"], d["v"], d["oq"], w.scale, w.causal)
+    ws = jfa.workspace(p, dev)
+    step = gpu_step_fn(jfa, w, d, ws)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    fwd_f, bwd_f = workloads.useful_flops(w, lq, lk)
+    step_flops = fwd_f + bwd_f
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    st = jfa.jfa_status_check(ws)
+    if st != 0:
+        raise RuntimeError("device status after warm-up: %s" % jfa.status_string(st))
+
+    stream = torch.cuda.current_stream()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    jfa.jfa_profile_reset()
+    jfa.jfa_profile_enable(True)
+    with ClockSampler(local) as clk:
+        for i in range(args.steps):
+            flush.fill_(float(i))  # evicts the inputs from L2 between timed steps
+            starts[i].record(stream)
+            step()
+            ends[i].record(stream)
+        torch.cuda.synchronize()
+    jfa.jfa_profile_enable(False)
+    ms_total = sum(s.elapsed_time(e) for s, e in zip(starts, ends))
+    if world > 1:
+        t = torch.tensor([ms_total], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms_total = float(t.item())
+        torch.distributed.barrier()
+    prof = {k: jfa.jfa_profile_read(k) for k in jfa.KERNEL_KINDS}
+    launches = sum(n for n, _ in prof.values())
+    ms_per_step = ms_total / args.steps
+    value = world * step_flops / (ms_per_step * 1e-3) / 1e12
+
+    # roofline of the dominant kernel
+    pk, peak_src = peaks()
+    per_kernel = kernel_flops_bytes(w, lq, lk, tq, tk)
+    kind = max(prof, key=lambda k: prof[k][1])
+    n_launch, kms = prof[kind]
+    avg_s = kms / max(n_launch, 1) * 1e-3
+    kf, kb = per_kernel[kind]
+    ridge = pk["bf16_tflops"] * 1e12 / (pk["hbm_gbs"] * 1e9)
+    bound = "tensor" if kb == 0 or kf / kb >= ridge else "hbm"
+    if bound == "tensor":
+        achieved, peak, unit = kf / avg_s / 1e12, pk["bf16_tflops"], "TFLOP/s"
+    else:
+        achieved, peak, unit = kb / avg_s / 1e9, pk["hbm_gbs"], "GB/s"
+    roof = {"kernel": kind, "bound": bound, "achieved": round(achieved, 2), "peak": peak,
+            "unit": unit, "frac": round(achieved / peak, 4), "peak_source": peak_src,
+            "traffic": measured_traffic(kind, w.name),
+            "algorithmic_flops_per_launch": kf, "algorithmic_bytes_per_launch": kb,
+            "avg_launch_ms": round(kms / max(n_launch, 1), 5)}
+    kernels = {k: {"launches": n, "ms_per_launch": round(ms / max(n, 1), 5),
+                   "share": round(ms / max(sum(x for _, x in prof.values()), 1e-12), 4)}
+               for k, (n, ms) in prof.items() if n}
+
+    # end to end through the public API with pinned host buffers
+    e2e = e2e_measure(jfa, w, batch, d, ws, p, args, dev, step_flops, world)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(w, lq, lk)
+
+    line = {
+        "metric": METRIC, "value": round(value, 3), "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16"
+        if w.dtype == torch.bfloat16 else "f32", "data": "synthetic (seeded, no padding)",
+        "frac_of_bf16_peak": round(value / world / pk["bf16_tflops"], 4),
+        "config": {"workload": w.name, "batch": w.batch, "heads": w.heads, "dim_qk": w.dim_qk,
+                   "dim_v": w.dim_v, "causal": w.causal,
+                   "activation": "softmax" if w.act == 0 else "silu_over_len",
+                   "cross": w.cross, "total_q": tq, "total_k": tk,
+                   "useful_gflop_fwd": round(fwd_f / 1e9, 3),
+                   "useful_gflop_bwd": round(bwd_f / 1e9, 3),
+                   "l2": "flushed between timed steps (256 MiB write)",
+                   "parallelism": "replicas" if world > 1 else "single"},
+        "roofline": roof, "kernels": kernels, "gpu_launches": launches,
+        "e2e": e2e, "cpu_baseline": cpu, "clocks": clk.summary(),
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+def e2e_measure(jfa, w, batch, d, ws, p, args, dev, step_flops, world):
+    names_in = ["q", "k", "v", "do"]
+    host = {n: batch[n].to("cpu").pin_memory() for n in names_in}
+    host_oq = torch.as_tensor(batch["offs_q"]).pin_memory()
+    host_ok = torch.as_tensor(batch["offs_k"]).pin_memory()
+    outs = ["o", "dq", "dk", "dv"]
+    host_out = {n: torch.empty(d[n].shape, dtype=d[n].dtype).pin_memory() for n in outs}
+    dd = dict(d)
+    step = gpu_step_fn(jfa, w, dd, ws)
+    h2d = sum(t.numel() * t.element_size() for t in host.values()) + \
+        host_oq.numel() * 8 + host_ok.numel() * 8
+    d2h = sum(d[n].numel() * d[n].element_size() for n in outs)
+
+    def one():
+        for n in names_in:
+            dd[n].copy_(host[n], non_blocking=True)
+        dd["oq"].copy_(host_oq, non_blocking=True)
+        dd["ok"].copy_(host_ok, non_blocking=True)
+        step()
+        for n in outs:
+            host_out[n].copy_(dd[n], non_blocking=True)
+        torch.cuda.current_stream().synchronize()
+
+    for _ in range(max(1, args.warmup)):
+        one()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        one()
+    dt = time.perf_counter() - t0
+    if world > 1:
+        t = torch.tensor([dt], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        dt = float(t.item())
+    return {"value": round(world * step_flops * args.steps / dt / 1e12, 3), "unit": "TFLOP/s",
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+            "ms_per_step": round(dt / args.steps * 1e3, 4)}
+
+
+# ----------------------------------------------------------------------------- reference arm
+def run_reference(args):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return
+    w = workloads.WORKLOADS[args.workload]
+    lq, lk = workloads.lengths(w.name, seed=0)
+    budget = max(2.0, 150.0 / max(args.steps + args.warmup, 1))
+    for _ in range(args.warmup):
+        cpu_baseline(w, lq, lk, budget_s=budget)
+    vals, secs = [], 0.0
+    res = None
+    for _ in range(args.steps):
+        res = cpu_baseline(w, lq, lk, budget_s=budget)
+        vals.append(res["value"])
+        secs += res["seconds"]
+    value = statistics.median(vals)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(secs / max(args.steps, 1) * 1e3, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
+        "config": {"workload": w.name, "batch": w.batch, "heads": w.heads, "dim_qk": w.dim_qk,
+                   "dim_v": w.dim_v, "causal": w.causal},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": res["cores"],
+                         "kind": "oracle", "sample": res["sample"]},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="d64", choices=sorted(workloads.WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        log("note: warm-up raised to 3 steps (minimum)")
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,185 @@
+/*
+ * jfa.h -- C ABI of libjfa, Jagged Flash Attention for one NVIDIA GB300 (sm_103a).
+ *
+ * Source of the method.  Meta GEM MFU co-design write-up
+ * (piletech.kr/articles/112134), "상세 정리" (details) section:
+ *   - jagged-input bullet: per-request sequences have different lengths, and
+ *     padding them wastes up to half of the attention compute; the attention
+ *     patterns are self, cross, pooled multi-head and asymmetric QKV;
+ *   - Jagged Flash Attention bullet: attention that works directly on the
+ *     variable-length tensors, masks by subtraction instead of -inf fill, and
+ *     parallelises the backward pass without atomic operations;
+ *   - Generalized Dot-Product Attention bullet: the same pipeline for
+ *     non-softmax activations, with software tile scheduling over jagged
+ *     tensors.
+ * The pages give no formulas; the ones below are the plain definitions.
+ *
+ * Jagged tensors.  B sequences are concatenated without padding.  Sequence b
+ * owns query rows offs_q[b] .. offs_q[b+1]-1 and key/value rows
+ * offs_k[b] .. offs_k[b+1]-1.  Offsets are int64 [B+1] in DEVICE memory,
+ * offs[0] == 0, non-decreasing, offs[B] == total rows.
+ *
+ * Layouts (row-major, contiguous, every pointer 16-byte aligned):
+ *   Q  [T_q, H, Dqk]   K [T_k, H, Dqk]   V [T_k, H, Dv]
+ *   O  [T_q, H, Dv]    dO [T_q, H, Dv]   lse [T_q, H] fp32 (natural log)
+ *   dQ/dK/dV have the shapes of Q/K/V.  Values are fp32 or bf16 (params.dtype),
+ *   lse is always fp32.
+ *
+ * Math, per sequence b and head h (i < Lq_b query rows, j < Lk_b key rows):
+ *   s_ij = scale * <q_i, k_j>; valid pairs: j < Lk_b, and j <= i when causal.
+ *   softmax:  P_ij = exp(s_ij - lse_i) over the valid j, o_i = sum_j P_ij v_j,
+ *             lse_i = log sum_{valid j} exp(s_ij).  A row with no valid key
+ *             (cross-attention with Lk_b == 0) gets o_i = 0, lse_i = -inf.
+ *   SiLU/L:   P_ij = SiLU(s_ij) / Lq_b over the valid j, o_i = sum_j P_ij v_j.
+ *   Backward: the analytic gradients of a loss whose gradient w.r.t. O is dO.
+ *
+ * Ownership and threading.  The caller owns every buffer.  The library never
+ * allocates device memory on these paths and keeps no per-call state; its
+ * only scratch is the caller's workspace (size from jfa_workspace_size).
+ * One workspace must not be used by two calls that may run concurrently.
+ *
+ * Asynchrony and errors.  Every compute call only enqueues work on `stream`
+ * (NULL = the legacy default stream) and returns.  Argument errors are
+ * detected on the host before anything is launched, and returned.  Errors
+ * found on the device (offsets that are not a valid jagged layout) are
+ * written to a status word inside the workspace; the affected call then
+ * computes nothing and leaves its outputs untouched.  jfa_status_check()
+ * synchronises the stream and returns that word.  The library never aborts,
+ * traps or prints.
+ */
+#ifndef JFA_H_
+#define JFA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same object as cudaStream_t; declared here so this header needs no CUDA headers. */
+typedef struct CUstream_st* jfa_stream_t;
+
+typedef enum {
+  JFA_OK = 0,
+  JFA_ERR_INVALID_ARG = 1, /* null pointer, bad size, misaligned pointer */
+  JFA_ERR_UNSUPPORTED = 2, /* valid request this build does not implement */
+  JFA_ERR_WORKSPACE = 3,   /* workspace missing, misaligned or too small */
+  JFA_ERR_BAD_OFFSETS = 4, /* (device) offsets are not a jagged layout of the given totals */
+  JFA_ERR_TIMEOUT = 5,     /* (device) a bounded wait inside a kernel gave up */
+  JFA_ERR_CUDA = 6         /* a CUDA runtime or driver call failed */
+} jfa_status;
+
+typedef enum { JFA_F32 = 0, JFA_BF16 = 1 } jfa_dtype;
+
+typedef struct {
+  int64_t batch;   /* B >= 0 */
+  int64_t total_q; /* T_q = offs_q[B] */
+  int64_t total_k; /* T_k = offs_k[B]; equal to total_q for self-attention */
+  int32_t heads;   /* H >= 1 */
+  int32_t dim_qk;  /* Dqk: bf16 supports 64 and 128; fp32 supports 1..128 */
+  int32_t dim_v;   /* Dv:  bf16 supports 64 and 128; fp32 supports 1..128 */
+  float scale;     /* score scale, normally 1/sqrt(Dqk) */
+  int32_t causal;  /* 1: key j visible to query i only if j <= i (self-attention only) */
+  int32_t dtype;   /* jfa_dtype of Q, K, V, O, dO, dQ, dK, dV */
+} jfa_params;
+
+/*
+ * Bytes of device workspace the calls below need for these params (work lists
+ * of the jagged tile scheduler, the backward row term D, the status word).
+ * Any call may be given a larger workspace.  Depends on batch, total_q,
+ * total_k and heads only.  Returns 0 for a null pointer.
+ */
+size_t jfa_workspace_size(const jfa_params* p);
+
+/*
+ * Softmax self-attention forward (Jagged Flash Attention bullet).  One offsets
+ * array serves queries and keys (total_k must equal total_q).  Writes O and lse.
+ * Causal masking is allowed.
+ */
+jfa_status jfa_fwd(const jfa_params* p, const void* q, const void* k, const void* v,
+                   const int64_t* offs, void* o, float* lse, void* ws, size_t ws_bytes,
+                   jfa_stream_t stream);
+
+/*
+ * Softmax self-attention backward, without atomics (Jagged Flash Attention
+ * bullet): a key-tile-major pass writes dK and dV, a query-tile-major pass
+ * writes dQ, each output element is written exactly once.  o and lse are the
+ * outputs of jfa_fwd on the same inputs; dout is dL/dO.
+ */
+jfa_status jfa_bwd(const jfa_params* p, const void* q, const void* k, const void* v,
+                   const void* o, const float* lse, const void* dout, const int64_t* offs,
+                   void* dq, void* dk, void* dv, void* ws, size_t ws_bytes,
+                   jfa_stream_t stream);
+
+/*
+ * Softmax cross-attention forward with independent query and key offsets and
+ * possibly Dv != Dqk (jagged-input bullet: cross and asymmetric-QKV patterns).
+ * Causal must be 0.  A sequence with Lk_b == 0 yields o = 0 and lse = -inf.
+ */
+jfa_status jfa_cross_fwd(const jfa_params* p, const void* q, const void* k, const void* v,
+                         const int64_t* offs_q, const int64_t* offs_k, void* o, float* lse,
+                         void* ws, size_t ws_bytes, jfa_stream_t stream);
+
+/* Backward of jfa_cross_fwd; same passes as jfa_bwd. */
+jfa_status jfa_cross_bwd(const jfa_params* p, const void* q, const void* k, const void* v,
+                         const void* o, const float* lse, const void* dout,
+                         const int64_t* offs_q, const int64_t* offs_k, void* dq, void* dk,
+                         void* dv, void* ws, size_t ws_bytes, jfa_stream_t stream);
+
+/*
+ * Non-softmax (Generalized Dot-Product Attention bullet) forward:
+ * P_ij = SiLU(s_ij) / Lq_b on the valid pairs, O = P V.  No lse is produced.
+ * Pass the same pointer as offs_q and offs_k for self-attention; causal is
+ * allowed only then (Lq_b == Lk_b is checked on the device).
+ */
+jfa_status jfa_gdpa_fwd(const jfa_params* p, const void* q, const void* k, const void* v,
+                        const int64_t* offs_q, const int64_t* offs_k, void* o, void* ws,
+                        size_t ws_bytes, jfa_stream_t stream);
+
+/* Backward of jfa_gdpa_fwd (no D term, no lse); same two atomic-free passes. */
+jfa_status jfa_gdpa_bwd(const jfa_params* p, const void* q, const void* k, const void* v,
+                        const void* dout, const int64_t* offs_q, const int64_t* offs_k,
+                        void* dq, void* dk, void* dv, void* ws, size_t ws_bytes,
+                        jfa_stream_t stream);
+
+/*
+ * Synchronises `stream`, then returns the device status word of the last
+ * call that used `ws` (JFA_OK, JFA_ERR_BAD_OFFSETS or JFA_ERR_TIMEOUT), or
+ * JFA_ERR_CUDA if the synchronisation itself failed.
+ */
+jfa_status jfa_status_check(const void* ws, jfa_stream_t stream);
+
+/* Static, human-readable name of a status code. */
+const char* jfa_status_string(jfa_status s);
+
+/*
+ * Kernel timing, for benchmarks.  While enabled, every kernel the library
+ * launches is bracketed by CUDA events recorded on its launch stream.
+ * jfa_profile_read synchronises those events and returns, for kernel kind
+ * `kind` (a JFA_KERNEL_* value), the number of launches and their summed
+ * device time in milliseconds since the last reset.  Not thread-safe.
+ */
+enum {
+  JFA_KERNEL_SCHEDULE = 0, /* jagged tile scheduler: offsets -> heavy-first work lists */
+  JFA_KERNEL_FWD = 1,      /* forward tile loop */
+  JFA_KERNEL_BWD_D = 2,    /* backward row term D = rowsum(dO * O) */
+  JFA_KERNEL_BWD_DKDV = 3, /* key-tile-major dK/dV pass */
+  JFA_KERNEL_BWD_DQ = 4,   /* query-tile-major dQ pass */
+  JFA_KERNEL_KINDS = 5
+};
+jfa_status jfa_profile_enable(int on);
+jfa_status jfa_profile_reset(void);
+jfa_status jfa_profile_read(int kind, int64_t* launches, double* total_ms);
+
+/*
+ * Which kernel family serves a request with these params: 1 = tcgen05/TMA
+ * tensor-core kernels (bf16), 0 = CUDA-core fp32 kernels, -1 = unsupported.
+ */
+int jfa_path_for(const jfa_params* p);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* JFA_H_ */

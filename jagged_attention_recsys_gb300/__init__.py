@@ -1,0 +1,260 @@
+"""Python binding of libjfa (Jagged Flash Attention for GB300): argument marshalling only.
+
+Every function here has the name of the C entry point it calls (see
+``include/jfa.h``) and forwards torch CUDA tensors as raw device pointers on
+the current CUDA stream.  No attention arithmetic happens in Python and there
+is no fallback: if the compiled library is missing or no CUDA device is
+present, the calls raise.
+
+Build the library with ``python -m jagged_attention_recsys_gb300.build``.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "_build", "libjfa.so")
+
+JFA_OK = 0
+JFA_ERR_INVALID_ARG = 1
+JFA_ERR_UNSUPPORTED = 2
+JFA_ERR_WORKSPACE = 3
+JFA_ERR_BAD_OFFSETS = 4
+JFA_ERR_TIMEOUT = 5
+JFA_ERR_CUDA = 6
+
+JFA_F32 = 0
+JFA_BF16 = 1
+
+KERNEL_KINDS = {"schedule": 0, "fwd": 1, "bwd_d": 2, "bwd_dkdv": 3, "bwd_dq": 4}
+
+# Every symbol include/jfa.h declares.
+EXPORTS = ("jfa_workspace_size", "jfa_fwd", "jfa_bwd", "jfa_cross_fwd", "jfa_cross_bwd",
+           "jfa_gdpa_fwd", "jfa_gdpa_bwd", "jfa_status_check", "jfa_status_string",
+           "jfa_profile_enable", "jfa_profile_reset", "jfa_profile_read", "jfa_path_for")
+
+
+class JfaError(RuntimeError):
+    def __init__(self, code, where):
+        self.code = code
+        super().__init__("%s: %s (status %d)" % (where, status_string(code), code))
+
+
+class jfa_params(ctypes.Structure):
+    _fields_ = [("batch", ctypes.c_int64), ("total_q", ctypes.c_int64),
+                ("total_k", ctypes.c_int64), ("heads", ctypes.c_int32),
+                ("dim_qk", ctypes.c_int32), ("dim_v", ctypes.c_int32),
+                ("scale", ctypes.c_float), ("causal", ctypes.c_int32),
+                ("dtype", ctypes.c_int32)]
+
+
+_lib = None
+
+
+def lib():
+    """The loaded libjfa (ctypes.CDLL); raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError("libjfa is not built (%s missing); run "
+                               "`python -m jagged_attention_recsys_gb300.build`" % LIB_PATH)
+        L = ctypes.CDLL(LIB_PATH)
+        vp, i64p, fp = ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p
+        P = ctypes.POINTER(jfa_params)
+        sz = ctypes.c_size_t
+        L.jfa_workspace_size.argtypes = [P]
+        L.jfa_workspace_size.restype = sz
+        L.jfa_path_for.argtypes = [P]
+        L.jfa_path_for.restype = ctypes.c_int
+        L.jfa_fwd.argtypes = [P, vp, vp, vp, i64p, vp, fp, vp, sz, vp]
+        L.jfa_bwd.argtypes = [P, vp, vp, vp, vp, fp, vp, i64p, vp, vp, vp, vp, sz, vp]
+        L.jfa_cross_fwd.argtypes = [P, vp, vp, vp, i64p, i64p, vp, fp, vp, sz, vp]
+        L.jfa_cross_bwd.argtypes = [P, vp, vp, vp, vp, fp, vp, i64p, i64p, vp, vp, vp, vp, sz, vp]
+        L.jfa_gdpa_fwd.argtypes = [P, vp, vp, vp, i64p, i64p, vp, vp, sz, vp]
+        L.jfa_gdpa_bwd.argtypes = [P, vp, vp, vp, vp, i64p, i64p, vp, vp, vp, vp, sz, vp]
+        for f in ("jfa_fwd", "jfa_bwd", "jfa_cross_fwd", "jfa_cross_bwd", "jfa_gdpa_fwd",
+                  "jfa_gdpa_bwd"):
+            getattr(L, f).restype = ctypes.c_int
+        L.jfa_status_check.argtypes = [vp, vp]
+        L.jfa_status_check.restype = ctypes.c_int
+        L.jfa_status_string.argtypes = [ctypes.c_int]
+        L.jfa_status_string.restype = ctypes.c_char_p
+        L.jfa_profile_enable.argtypes = [ctypes.c_int]
+        L.jfa_profile_enable.restype = ctypes.c_int
+        L.jfa_profile_reset.argtypes = []
+        L.jfa_profile_reset.restype = ctypes.c_int
+        L.jfa_profile_read.argtypes = [ctypes.c_int, ctypes.POINTER(ctypes.c_int64),
+                                       ctypes.POINTER(ctypes.c_double)]
+        L.jfa_profile_read.restype = ctypes.c_int
+        _lib = L
+    return _lib
+
+
+def status_string(code: int) -> str:
+    return lib().jfa_status_string(int(code)).decode()
+
+
+def _check(code, where):
+    if code != JFA_OK:
+        raise JfaError(code, where)
+
+
+def _dtype_code(t: torch.dtype) -> int:
+    if t == torch.float32:
+        return JFA_F32
+    if t == torch.bfloat16:
+        return JFA_BF16
+    raise TypeError("libjfa takes fp32 or bf16 tensors, got %s" % t)
+
+
+def make_params(batch, total_q, total_k, heads, dim_qk, dim_v, dtype, scale=None, causal=False):
+    if scale is None:
+        scale = 1.0 / math.sqrt(dim_qk)
+    return jfa_params(int(batch), int(total_q), int(total_k), int(heads), int(dim_qk),
+                      int(dim_v), float(scale), int(bool(causal)), _dtype_code(dtype))
+
+
+def params_for(q, k, v, offs_q, scale=None, causal=False):
+    return make_params(offs_q.numel() - 1, q.shape[0], k.shape[0], q.shape[1], q.shape[2],
+                       v.shape[2], q.dtype, scale, causal)
+
+
+def jfa_workspace_size(p: jfa_params) -> int:
+    return int(lib().jfa_workspace_size(ctypes.byref(p)))
+
+
+def jfa_path_for(p: jfa_params) -> int:
+    return int(lib().jfa_path_for(ctypes.byref(p)))
+
+
+def workspace(p: jfa_params, device="cuda") -> torch.Tensor:
+    """A device workspace large enough for every call with these params."""
+    return torch.empty(max(jfa_workspace_size(p), 256), dtype=torch.uint8, device=device)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _prep(q, k, v, offs_q, offs_k, ws, scale, causal):
+    for t in (q, k, v):
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError("q, k, v must be contiguous CUDA tensors")
+    if offs_q.dtype != torch.int64 or not offs_q.is_cuda:
+        raise ValueError("offsets must be int64 CUDA tensors")
+    if offs_k is not None and (offs_k.dtype != torch.int64 or not offs_k.is_cuda):
+        raise ValueError("offsets must be int64 CUDA tensors")
+    p = params_for(q, k, v, offs_q, scale, causal)
+    if ws is None:
+        ws = workspace(p, q.device)
+    return p, ws
+
+
+def jfa_fwd(q, k, v, offs, *, scale=None, causal=False, o=None, lse=None, ws=None, stream=None):
+    """Softmax self-attention forward; returns (o, lse)."""
+    p, ws = _prep(q, k, v, offs, None, ws, scale, causal)
+    if o is None:
+        o = torch.empty(q.shape[0], q.shape[1], v.shape[2], dtype=q.dtype, device=q.device)
+    if lse is None:
+        lse = torch.empty(q.shape[0], q.shape[1], dtype=torch.float32, device=q.device)
+    _check(lib().jfa_fwd(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(offs), _ptr(o),
+                         _ptr(lse), _ptr(ws), ws.numel(), _stream(stream)), "jfa_fwd")
+    return o, lse
+
+
+def jfa_bwd(q, k, v, o, lse, dout, offs, *, scale=None, causal=False, dq=None, dk=None,
+            dv=None, ws=None, stream=None):
+    """Softmax self-attention backward; returns (dq, dk, dv)."""
+    p, ws = _prep(q, k, v, offs, None, ws, scale, causal)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    _check(lib().jfa_bwd(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse),
+                         _ptr(dout), _ptr(offs), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(ws),
+                         ws.numel(), _stream(stream)), "jfa_bwd")
+    return dq, dk, dv
+
+
+def jfa_cross_fwd(q, k, v, offs_q, offs_k, *, scale=None, o=None, lse=None, ws=None,
+                  stream=None):
+    """Softmax cross-attention forward (independent key offsets); returns (o, lse)."""
+    p, ws = _prep(q, k, v, offs_q, offs_k, ws, scale, False)
+    if o is None:
+        o = torch.empty(q.shape[0], q.shape[1], v.shape[2], dtype=q.dtype, device=q.device)
+    if lse is None:
+        lse = torch.empty(q.shape[0], q.shape[1], dtype=torch.float32, device=q.device)
+    _check(lib().jfa_cross_fwd(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(offs_q),
+                               _ptr(offs_k), _ptr(o), _ptr(lse), _ptr(ws), ws.numel(),
+                               _stream(stream)), "jfa_cross_fwd")
+    return o, lse
+
+
+def jfa_cross_bwd(q, k, v, o, lse, dout, offs_q, offs_k, *, scale=None, dq=None, dk=None,
+                  dv=None, ws=None, stream=None):
+    """Backward of jfa_cross_fwd; returns (dq, dk, dv)."""
+    p, ws = _prep(q, k, v, offs_q, offs_k, ws, scale, False)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    _check(lib().jfa_cross_bwd(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse),
+                               _ptr(dout), _ptr(offs_q), _ptr(offs_k), _ptr(dq), _ptr(dk),
+                               _ptr(dv), _ptr(ws), ws.numel(), _stream(stream)), "jfa_cross_bwd")
+    return dq, dk, dv
+
+
+def jfa_gdpa_fwd(q, k, v, offs_q, offs_k=None, *, scale=None, causal=False, o=None, ws=None,
+                 stream=None):
+    """SiLU(s)/L attention forward; returns o.  offs_k=None means self-attention."""
+    offs_k = offs_q if offs_k is None else offs_k
+    p, ws = _prep(q, k, v, offs_q, offs_k, ws, scale, causal)
+    if o is None:
+        o = torch.empty(q.shape[0], q.shape[1], v.shape[2], dtype=q.dtype, device=q.device)
+    _check(lib().jfa_gdpa_fwd(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(offs_q),
+                              _ptr(offs_k), _ptr(o), _ptr(ws), ws.numel(), _stream(stream)),
+           "jfa_gdpa_fwd")
+    return o
+
+
+def jfa_gdpa_bwd(q, k, v, dout, offs_q, offs_k=None, *, scale=None, causal=False, dq=None,
+                 dk=None, dv=None, ws=None, stream=None):
+    """Backward of jfa_gdpa_fwd; returns (dq, dk, dv)."""
+    offs_k = offs_q if offs_k is None else offs_k
+    p, ws = _prep(q, k, v, offs_q, offs_k, ws, scale, causal)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    _check(lib().jfa_gdpa_bwd(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(dout),
+                              _ptr(offs_q), _ptr(offs_k), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(ws),
+                              ws.numel(), _stream(stream)), "jfa_gdpa_bwd")
+    return dq, dk, dv
+
+
+def jfa_status_check(ws, stream=None) -> int:
+    """Synchronises the stream and returns the device status word of the last call on ``ws``."""
+    return int(lib().jfa_status_check(_ptr(ws), _stream(stream)))
+
+
+def jfa_profile_enable(on: bool = True):
+    _check(lib().jfa_profile_enable(int(bool(on))), "jfa_profile_enable")
+
+
+def jfa_profile_reset():
+    _check(lib().jfa_profile_reset(), "jfa_profile_reset")
+
+
+def jfa_profile_read(kind: str):
+    """(launches, total_ms) of one kernel kind since the last reset."""
+    n = ctypes.c_int64(0)
+    ms = ctypes.c_double(0.0)
+    _check(lib().jfa_profile_read(KERNEL_KINDS[kind], ctypes.byref(n), ctypes.byref(ms)),
+           "jfa_profile_read")
+    return int(n.value), float(ms.value)

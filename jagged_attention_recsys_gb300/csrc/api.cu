@@ -1,0 +1,351 @@
+// C ABI of libjfa: argument validation, workspace carve-up, kernel dispatch,
+// status reporting and optional per-kernel event timing.  See include/jfa.h.
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <mutex>
+#include <vector>
+
+#include "internal.h"
+#include "tc.h"
+
+namespace jfa {
+
+int num_sms() {
+  static int cache[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+  if (cache[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+      n = 148;
+    cache[dev] = n;
+  }
+  return cache[dev];
+}
+
+static size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+size_t workspace_layout(int64_t batch, int64_t total_q, int64_t total_k, int heads, void* base,
+                        Workspace* out) {
+  char* b = (char*)base;
+  size_t off = 0;
+  Workspace w{};
+  w.hdr = (WsHeader*)(b + off);
+  off = align_up(off + sizeof(WsHeader), 256);
+  w.q_prefix = (int*)(b + off);
+  off = align_up(off + sizeof(int) * (size_t)(batch + 1), 256);
+  w.k_prefix = (int*)(b + off);
+  off = align_up(off + sizeof(int) * (size_t)(batch + 1), 256);
+  w.max_items_q = (int64_t)heads * (total_q / kMinTile + batch + 1);
+  w.list_q = (WorkItem*)(b + off);
+  off = align_up(off + sizeof(WorkItem) * (size_t)w.max_items_q, 256);
+  w.max_items_k = (int64_t)heads * (total_k / kMinTile + batch + 1);
+  w.list_k = (WorkItem*)(b + off);
+  off = align_up(off + sizeof(WorkItem) * (size_t)w.max_items_k, 256);
+  w.drow = (float*)(b + off);
+  off = align_up(off + sizeof(float) * (size_t)total_q * (size_t)heads, 256);
+  if (out) *out = w;
+  return off;
+}
+
+// ---------------------------------------------------------------------------
+// Kernel timing (benchmarks only)
+// ---------------------------------------------------------------------------
+namespace {
+struct Prof {
+  bool on = false;
+  std::vector<cudaEvent_t> pool;
+  struct Pending { int kind; cudaEvent_t a, b; };
+  std::vector<Pending> pending;
+  int64_t launches[JFA_KERNEL_KINDS] = {0};
+  double ms[JFA_KERNEL_KINDS] = {0};
+};
+Prof& prof() {
+  static Prof p;
+  return p;
+}
+cudaEvent_t take_event() {
+  Prof& P = prof();
+  if (!P.pool.empty()) {
+    cudaEvent_t e = P.pool.back();
+    P.pool.pop_back();
+    return e;
+  }
+  cudaEvent_t e = nullptr;
+  if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+  return e;
+}
+jfa_status drain() {
+  Prof& P = prof();
+  jfa_status st = JFA_OK;
+  for (auto& x : P.pending) {
+    float t = 0.f;
+    if (cudaEventSynchronize(x.b) != cudaSuccess || cudaEventElapsedTime(&t, x.a, x.b) != cudaSuccess)
+      st = JFA_ERR_CUDA;
+    P.launches[x.kind] += 1;
+    P.ms[x.kind] += t;
+    P.pool.push_back(x.a);
+    P.pool.push_back(x.b);
+  }
+  P.pending.clear();
+  return st;
+}
+
+// Records events around one launch when profiling is on.
+struct Timed {
+  int kind;
+  cudaStream_t s;
+  cudaEvent_t a = nullptr, b = nullptr;
+  Timed(int k, cudaStream_t st) : kind(k), s(st) {
+    if (!prof().on) return;
+    if (prof().pending.size() > 65536) drain();
+    a = take_event();
+    b = take_event();
+    if (a) cudaEventRecord(a, s);
+  }
+  ~Timed() {
+    if (!a || !b) return;
+    cudaEventRecord(b, s);
+    prof().pending.push_back({kind, a, b});
+  }
+};
+
+inline jfa_status cu(cudaError_t e) { return e == cudaSuccess ? JFA_OK : JFA_ERR_CUDA; }
+
+bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+
+enum class Kind { Self, Cross, Gdpa };
+
+jfa_status check_params(const jfa_params* p, Kind kind) {
+  if (!p) return JFA_ERR_INVALID_ARG;
+  if (p->batch < 0 || p->total_q < 0 || p->total_k < 0 || p->heads < 1) return JFA_ERR_INVALID_ARG;
+  if (p->dim_qk < 1 || p->dim_v < 1) return JFA_ERR_INVALID_ARG;
+  if (p->dtype != JFA_F32 && p->dtype != JFA_BF16) return JFA_ERR_INVALID_ARG;
+  if (!(p->scale == p->scale) || p->scale == INFINITY || p->scale == -INFINITY)
+    return JFA_ERR_INVALID_ARG;
+  if (p->causal != 0 && p->causal != 1) return JFA_ERR_INVALID_ARG;
+  if (p->batch == 0 && (p->total_q != 0 || p->total_k != 0)) return JFA_ERR_INVALID_ARG;
+  if (p->total_q > ((int64_t)1 << 31) || p->total_k > ((int64_t)1 << 31)) return JFA_ERR_UNSUPPORTED;
+  if (kind == Kind::Self && p->total_k != p->total_q) return JFA_ERR_INVALID_ARG;
+  if (kind == Kind::Cross && p->causal) return JFA_ERR_UNSUPPORTED;
+  if (kind == Kind::Gdpa && p->causal && p->total_k != p->total_q) return JFA_ERR_INVALID_ARG;
+  if (jfa_path_for(p) < 0) return JFA_ERR_UNSUPPORTED;
+  return JFA_OK;
+}
+
+jfa_status check_ptrs(std::initializer_list<const void*> ptrs) {
+  for (const void* x : ptrs)
+    if (!x || !aligned16(x)) return JFA_ERR_INVALID_ARG;
+  return JFA_OK;
+}
+
+jfa_status prepare(const jfa_params* p, void* ws, size_t ws_bytes, Workspace* w) {
+  if (!ws || ((uintptr_t)ws & 255u) != 0) return JFA_ERR_WORKSPACE;
+  size_t need = workspace_layout(p->batch, p->total_q, p->total_k, p->heads, ws, w);
+  if (ws_bytes < need) return JFA_ERR_WORKSPACE;
+  return JFA_OK;
+}
+
+Problem make_problem(const jfa_params* p, const int64_t* oq, const int64_t* ok, int act) {
+  Problem r;
+  r.offs_q = oq;
+  r.offs_k = ok;
+  r.batch = p->batch;
+  r.total_q = p->total_q;
+  r.total_k = p->total_k;
+  r.heads = p->heads;
+  r.dim_qk = p->dim_qk;
+  r.dim_v = p->dim_v;
+  r.scale = p->scale;
+  r.causal = p->causal;
+  r.act = act;
+  return r;
+}
+
+// An empty batch still resets the status word so jfa_status_check reports it.
+jfa_status empty_call(const Workspace& w, cudaStream_t s) {
+  return cu(cudaMemsetAsync(w.hdr, 0, sizeof(WsHeader), s));
+}
+
+jfa_status run_fwd(const jfa_params* p, Kind kind, int act, const void* q, const void* k,
+                   const void* v, const int64_t* oq, const int64_t* ok, void* o, float* lse,
+                   void* ws, size_t ws_bytes, cudaStream_t s) {
+  jfa_status st = check_params(p, kind);
+  if (st != JFA_OK) return st;
+  if ((st = check_ptrs({oq, ok})) != JFA_OK) return st;
+  if (p->batch > 0 && p->total_q > 0) {
+    if ((st = check_ptrs({q, o})) != JFA_OK) return st;
+    if (act == kActSoftmax && (st = check_ptrs({lse})) != JFA_OK) return st;
+  }
+  if (p->total_k > 0 && (st = check_ptrs({k, v})) != JFA_OK) return st;
+  Workspace w;
+  if ((st = prepare(p, ws, ws_bytes, &w)) != JFA_OK) return st;
+  if (p->batch == 0) return empty_call(w, s);
+  Problem pr = make_problem(p, oq, ok, act);
+  const int path = jfa_path_for(p);
+  SchedConfig sc = path == 1 ? tc_fwd_sched(pr) : kSimtSched;
+  sc.build_q = 1;
+  sc.build_k = 0;
+  sc.self_attention = (kind == Kind::Self) || p->causal;
+  {
+    Timed t(JFA_KERNEL_SCHEDULE, s);
+    if ((st = cu(launch_schedule(pr, w, sc, s))) != JFA_OK) return st;
+  }
+  Timed t(JFA_KERNEL_FWD, s);
+  if (path == 1) return cu(launch_tc_fwd(pr, q, k, v, o, lse, w, s));
+  return cu(launch_simt_fwd(pr, p->dtype, q, k, v, o, lse, w, s));
+}
+
+jfa_status run_bwd(const jfa_params* p, Kind kind, int act, const void* q, const void* k,
+                   const void* v, const void* o, const float* lse, const void* dout,
+                   const int64_t* oq, const int64_t* ok, void* dq, void* dk, void* dv, void* ws,
+                   size_t ws_bytes, cudaStream_t s) {
+  jfa_status st = check_params(p, kind);
+  if (st != JFA_OK) return st;
+  if ((st = check_ptrs({oq, ok})) != JFA_OK) return st;
+  if (p->batch > 0 && p->total_q > 0) {
+    if ((st = check_ptrs({q, dout, dq})) != JFA_OK) return st;
+    if (act == kActSoftmax && (st = check_ptrs({o, lse})) != JFA_OK) return st;
+  }
+  if (p->total_k > 0 && (st = check_ptrs({k, v, dk, dv})) != JFA_OK) return st;
+  Workspace w;
+  if ((st = prepare(p, ws, ws_bytes, &w)) != JFA_OK) return st;
+  if (p->batch == 0) return empty_call(w, s);
+  Problem pr = make_problem(p, oq, ok, act);
+  const int path = jfa_path_for(p);
+  SchedConfig sc = path == 1 ? tc_bwd_sched(pr) : kSimtSched;
+  sc.build_q = 1;
+  sc.build_k = 1;
+  sc.self_attention = (kind == Kind::Self) || p->causal;
+  {
+    Timed t(JFA_KERNEL_SCHEDULE, s);
+    if ((st = cu(launch_schedule(pr, w, sc, s))) != JFA_OK) return st;
+  }
+  if (act == kActSoftmax) {
+    Timed t(JFA_KERNEL_BWD_D, s);
+    if ((st = cu(launch_bwd_rowterm(pr, p->dtype, o, dout, w, s))) != JFA_OK) return st;
+  }
+  {
+    Timed t(JFA_KERNEL_BWD_DKDV, s);
+    if (path == 1)
+      st = cu(launch_tc_dkdv(pr, q, k, v, lse, dout, dk, dv, w, s));
+    else
+      st = cu(launch_simt_dkdv(pr, p->dtype, q, k, v, lse, dout, dk, dv, w, s));
+    if (st != JFA_OK) return st;
+  }
+  Timed t(JFA_KERNEL_BWD_DQ, s);
+  if (path == 1) return cu(launch_tc_dq(pr, q, k, v, lse, dout, dq, w, s));
+  return cu(launch_simt_dq(pr, p->dtype, q, k, v, lse, dout, dq, w, s));
+}
+
+}  // namespace
+}  // namespace jfa
+
+using namespace jfa;
+
+extern "C" {
+
+size_t jfa_workspace_size(const jfa_params* p) {
+  if (!p || p->batch < 0 || p->total_q < 0 || p->total_k < 0 || p->heads < 1) return 0;
+  return workspace_layout(p->batch, p->total_q, p->total_k, p->heads, nullptr, nullptr);
+}
+
+int jfa_path_for(const jfa_params* p) {
+  if (!p) return -1;
+  if (p->dim_qk < 1 || p->dim_v < 1 || p->dim_qk > 128 || p->dim_v > 128) return -1;
+  if (p->dtype == JFA_BF16 && tc_supports(p->dim_qk, p->dim_v)) return 1;
+  if (p->dtype == JFA_F32 || p->dtype == JFA_BF16) return 0;
+  return -1;
+}
+
+jfa_status jfa_fwd(const jfa_params* p, const void* q, const void* k, const void* v,
+                   const int64_t* offs, void* o, float* lse, void* ws, size_t ws_bytes,
+                   jfa_stream_t stream) {
+  return run_fwd(p, Kind::Self, kActSoftmax, q, k, v, offs, offs, o, lse, ws, ws_bytes,
+                 (cudaStream_t)stream);
+}
+
+jfa_status jfa_bwd(const jfa_params* p, const void* q, const void* k, const void* v,
+                   const void* o, const float* lse, const void* dout, const int64_t* offs,
+                   void* dq, void* dk, void* dv, void* ws, size_t ws_bytes,
+                   jfa_stream_t stream) {
+  return run_bwd(p, Kind::Self, kActSoftmax, q, k, v, o, lse, dout, offs, offs, dq, dk, dv, ws,
+                 ws_bytes, (cudaStream_t)stream);
+}
+
+jfa_status jfa_cross_fwd(const jfa_params* p, const void* q, const void* k, const void* v,
+                         const int64_t* offs_q, const int64_t* offs_k, void* o, float* lse,
+                         void* ws, size_t ws_bytes, jfa_stream_t stream) {
+  return run_fwd(p, Kind::Cross, kActSoftmax, q, k, v, offs_q, offs_k, o, lse, ws, ws_bytes,
+                 (cudaStream_t)stream);
+}
+
+jfa_status jfa_cross_bwd(const jfa_params* p, const void* q, const void* k, const void* v,
+                         const void* o, const float* lse, const void* dout,
+                         const int64_t* offs_q, const int64_t* offs_k, void* dq, void* dk,
+                         void* dv, void* ws, size_t ws_bytes, jfa_stream_t stream) {
+  return run_bwd(p, Kind::Cross, kActSoftmax, q, k, v, o, lse, dout, offs_q, offs_k, dq, dk, dv,
+                 ws, ws_bytes, (cudaStream_t)stream);
+}
+
+jfa_status jfa_gdpa_fwd(const jfa_params* p, const void* q, const void* k, const void* v,
+                        const int64_t* offs_q, const int64_t* offs_k, void* o, void* ws,
+                        size_t ws_bytes, jfa_stream_t stream) {
+  return run_fwd(p, Kind::Gdpa, kActSiluOverLen, q, k, v, offs_q, offs_k, o, nullptr, ws,
+                 ws_bytes, (cudaStream_t)stream);
+}
+
+jfa_status jfa_gdpa_bwd(const jfa_params* p, const void* q, const void* k, const void* v,
+                        const void* dout, const int64_t* offs_q, const int64_t* offs_k,
+                        void* dq, void* dk, void* dv, void* ws, size_t ws_bytes,
+                        jfa_stream_t stream) {
+  return run_bwd(p, Kind::Gdpa, kActSiluOverLen, q, k, v, nullptr, nullptr, dout, offs_q, offs_k,
+                 dq, dk, dv, ws, ws_bytes, (cudaStream_t)stream);
+}
+
+jfa_status jfa_status_check(const void* ws, jfa_stream_t stream) {
+  if (!ws || ((uintptr_t)ws & 255u) != 0) return JFA_ERR_WORKSPACE;
+  if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return JFA_ERR_CUDA;
+  int st = 0;
+  if (cudaMemcpy(&st, ws, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return JFA_ERR_CUDA;
+  if (st < 0 || st > JFA_ERR_CUDA) return JFA_ERR_CUDA;
+  return (jfa_status)st;
+}
+
+const char* jfa_status_string(jfa_status s) {
+  switch (s) {
+    case JFA_OK: return "ok";
+    case JFA_ERR_INVALID_ARG: return "invalid argument";
+    case JFA_ERR_UNSUPPORTED: return "unsupported configuration";
+    case JFA_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+    case JFA_ERR_BAD_OFFSETS: return "offsets are not a valid jagged layout";
+    case JFA_ERR_TIMEOUT: return "a bounded wait inside a kernel timed out";
+    case JFA_ERR_CUDA: return "CUDA error";
+  }
+  return "unknown status";
+}
+
+jfa_status jfa_profile_enable(int on) {
+  prof().on = on != 0;
+  return JFA_OK;
+}
+
+jfa_status jfa_profile_reset(void) {
+  jfa_status st = drain();
+  for (int i = 0; i < JFA_KERNEL_KINDS; ++i) {
+    prof().launches[i] = 0;
+    prof().ms[i] = 0;
+  }
+  return st;
+}
+
+jfa_status jfa_profile_read(int kind, int64_t* launches, double* total_ms) {
+  if (kind < 0 || kind >= JFA_KERNEL_KINDS || !launches || !total_ms) return JFA_ERR_INVALID_ARG;
+  jfa_status st = drain();
+  *launches = prof().launches[kind];
+  *total_ms = prof().ms[kind];
+  return st;
+}
+
+}  // extern "C"

@@ -1,0 +1,95 @@
+// Internal declarations shared by the libjfa translation units (host and device).
+// Nothing here is part of the public ABI (include/jfa.h is).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "jfa.h"
+
+namespace jfa {
+
+constexpr int kActSoftmax = 0;
+constexpr int kActSiluOverLen = 1;
+
+// Masked scores are moved down by this amount (in the log2-scaled score
+// domain) instead of being replaced by -inf: exp2 of a masked score then
+// underflows to exactly 0 once the running row maximum comes from a valid
+// key, no inf - inf can arise, and no -inf fill is needed on partial tiles
+// (the "subtraction instead of -inf masking" of the Jagged Flash Attention
+// bullet, Meta GEM MFU write-up, piletech.kr/articles/112134, details).
+// The same shift drives SiLU(u - shift) to (-)0 for the non-softmax variant.
+constexpr float kMaskShift = 1048576.0f;  // 2^20
+
+// One unit of work produced by the jagged tile scheduler.
+//   x = sequence b, y = head h, z = tile index inside the sequence,
+//   w = cost (number of inner steps the kernel will run for it).
+// Query-major lists hold q-tiles, key-major lists hold k-tiles.
+using WorkItem = int4;
+
+// Device workspace header; lives at offset 0 of the caller's workspace.
+struct WsHeader {
+  int status;  // jfa_status of the last call (device-detected errors only)
+  int n_q;     // items in the query-major list
+  int n_k;     // items in the key-major list
+  int pad[61];
+};
+
+// Everything a kernel needs to know about one request.
+struct Problem {
+  const int64_t* offs_q;
+  const int64_t* offs_k;
+  int64_t batch, total_q, total_k;
+  int heads, dim_qk, dim_v;
+  float scale;
+  int causal;
+  int act;
+};
+
+// Carve-up of the caller's workspace.
+struct Workspace {
+  WsHeader* hdr;
+  int* q_prefix;        // [B+1] q-tile prefix sums (scheduler scratch)
+  int* k_prefix;        // [B+1] k-tile prefix sums (scheduler scratch)
+  WorkItem* list_q;     // [max_items_q]
+  WorkItem* list_k;     // [max_items_k]
+  float* drow;          // [T_q * H] backward row term D
+  int64_t max_items_q, max_items_k;
+};
+
+// Smallest tile any kernel uses; bounds the number of work items.
+constexpr int kMinTile = 32;
+
+size_t workspace_layout(int64_t batch, int64_t total_q, int64_t total_k, int heads, void* base,
+                        Workspace* out);
+
+// Scheduler: validates offsets, writes the status word and builds the lists
+// requested (a q-list of tiles of q_rows rows whose inner loop steps over keys
+// in blocks of q_keys_step, and/or a k-list of tiles of k_keys keys whose
+// inner loop steps over rows in blocks of k_rows_step).
+struct SchedConfig {
+  int q_rows, q_keys_step;
+  int k_keys, k_rows_step;
+  int build_q, build_k;
+  int self_attention;  // causal or GDPA self: Lq_b must equal Lk_b
+};
+cudaError_t launch_schedule(const Problem& p, const Workspace& ws, const SchedConfig& c,
+                            cudaStream_t s);
+
+// CUDA-core kernels (fp32 arithmetic; inputs fp32 or bf16).
+extern const SchedConfig kSimtSched;
+cudaError_t launch_simt_fwd(const Problem& p, int dtype, const void* q, const void* k,
+                            const void* v, void* o, float* lse, const Workspace& ws,
+                            cudaStream_t s);
+cudaError_t launch_bwd_rowterm(const Problem& p, int dtype, const void* o, const void* dout,
+                               const Workspace& ws, cudaStream_t s);
+cudaError_t launch_simt_dkdv(const Problem& p, int dtype, const void* q, const void* k,
+                             const void* v, const float* lse, const void* dout, void* dk,
+                             void* dv, const Workspace& ws, cudaStream_t s);
+cudaError_t launch_simt_dq(const Problem& p, int dtype, const void* q, const void* k,
+                           const void* v, const float* lse, const void* dout, void* dq,
+                           const Workspace& ws, cudaStream_t s);
+
+int num_sms();
+
+}  // namespace jfa

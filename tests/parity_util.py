@@ -1,0 +1,125 @@
+"""Helpers for the GPU parity tests: run libjfa and the fp64 oracle on the same inputs."""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import oracle
+import workloads
+
+# Tolerances.  fp32 inputs: max-abs error <= 1e-5 on O, dQ, dK, dV.  bf16 inputs with fp32
+# accumulation: O max-abs <= 2e-2 and relative L2 <= 1e-2; each gradient relative L2 <= 1e-2.
+F32_ATOL = 1e-5
+BF16_O_ATOL = 2e-2
+BF16_REL_L2 = 1e-2
+
+
+def to64(t):
+    return t.detach().to("cpu", torch.float64).numpy()
+
+
+def rel_l2(got, ref):
+    den = float(np.linalg.norm(ref))
+    num = float(np.linalg.norm(got - ref))
+    return num / den if den > 0 else num
+
+
+def run_gpu(w: workloads.Workload, batch, ws=None):
+    """Forward and backward on the GPU through the C ABI binding; returns numpy fp64 dict."""
+    import jagged_attention_recsys_gb300 as jfa
+
+    dev = batch["q"].device
+    oq = torch.as_tensor(batch["offs_q"], device=dev)
+    ok = torch.as_tensor(batch["offs_k"], device=dev)
+    q, k, v, do = batch["q"], batch["k"], batch["v"], batch["do"]
+    sc = w.scale
+    if w.act == workloads.ACT_SILU_OVER_LEN:
+        o = jfa.jfa_gdpa_fwd(q, k, v, oq, ok, scale=sc, causal=w.causal, ws=ws)
+        dq, dk, dv = jfa.jfa_gdpa_bwd(q, k, v, do, oq, ok, scale=sc, causal=w.causal, ws=ws)
+        lse = None
+    elif w.cross:
+        o, lse = jfa.jfa_cross_fwd(q, k, v, oq, ok, scale=sc, ws=ws)
+        dq, dk, dv = jfa.jfa_cross_bwd(q, k, v, o, lse, do, oq, ok, scale=sc, ws=ws)
+    else:
+        o, lse = jfa.jfa_fwd(q, k, v, oq, scale=sc, causal=w.causal, ws=ws)
+        dq, dk, dv = jfa.jfa_bwd(q, k, v, o, lse, do, oq, scale=sc, causal=w.causal, ws=ws)
+    torch.cuda.synchronize()
+    return dict(o=o, lse=lse, dq=dq, dk=dk, dv=dv)
+
+
+def run_oracle(w: workloads.Workload, q, k, v, do, offs_q, offs_k):
+    o, lse = oracle.fwd(q, k, v, offs_q, offs_k, scale=w.scale, causal=w.causal, act=w.act)
+    dq, dk, dv = oracle.bwd(q, k, v, do, offs_q, offs_k, scale=w.scale, causal=w.causal,
+                            act=w.act)
+    return dict(o=o, lse=lse, dq=dq, dk=dk, dv=dv)
+
+
+def compare(w: workloads.Workload, got, ref, fp32: bool):
+    """Asserts the tolerances; returns the error figures."""
+    errs = {}
+    for name in ("o", "dq", "dk", "dv"):
+        g, r = got[name], ref[name]
+        assert np.all(np.isfinite(g)), name + " has non-finite values"
+        errs[name + "_maxabs"] = float(np.max(np.abs(g - r))) if g.size else 0.0
+        errs[name + "_rel_l2"] = rel_l2(g, r) if g.size else 0.0
+    if got.get("lse") is not None and ref.get("lse") is not None and got["lse"].size:
+        fin = np.isfinite(ref["lse"])
+        assert np.array_equal(fin, np.isfinite(got["lse"])), "lse -inf pattern differs"
+        if fin.any():
+            errs["lse_maxabs"] = float(np.max(np.abs(got["lse"][fin] - ref["lse"][fin])))
+    if fp32:
+        for name in ("o", "dq", "dk", "dv"):
+            assert errs[name + "_maxabs"] <= F32_ATOL, (name, errs)
+        if "lse_maxabs" in errs:
+            assert errs["lse_maxabs"] <= F32_ATOL, errs
+    else:
+        assert errs["o_maxabs"] <= BF16_O_ATOL, errs
+        assert errs["o_rel_l2"] <= BF16_REL_L2, errs
+        for name in ("dq", "dk", "dv"):
+            assert errs[name + "_rel_l2"] <= BF16_REL_L2, (name, errs)
+        if "lse_maxabs" in errs:
+            assert errs["lse_maxabs"] <= 2e-2, errs
+    return errs
+
+
+def full_check(w: workloads.Workload, lq, lk=None, seed=0, device="cuda"):
+    """Whole batch on GPU and in the oracle; element-by-element comparison."""
+    batch = workloads.make_batch(w, lq, lk, seed=seed, device=device)
+    got = run_gpu(w, batch)
+    got = {n: (to64(t) if t is not None else None) for n, t in got.items()}
+    q, k, v, do = (to64(batch[n]) for n in ("q", "k", "v", "do"))
+    ref = run_oracle(w, q, k, v, do, batch["offs_q"], batch["offs_k"])
+    return compare(w, got, ref, fp32=(w.dtype == torch.float32))
+
+
+def sample_indices(lq, count=6, seed=0):
+    """Longest, shortest and a few seeded random sequences."""
+    lq = np.asarray(lq)
+    order = np.argsort(lq, kind="stable")
+    pick = {int(order[-1]), int(order[0])}
+    if len(lq) > 1:
+        pick.add(int(order[-2]))
+    rng = np.random.default_rng(seed + 1)
+    while len(pick) < min(count, len(lq)):
+        pick.add(int(rng.integers(0, len(lq))))
+    return sorted(pick)
+
+
+def sampled_check(w: workloads.Workload, batch, got, idx):
+    """Compares the GPU result of a full batch with the oracle on a few whole sequences."""
+    oq, ok = batch["offs_q"], batch["offs_k"]
+    lq = [int(oq[b + 1] - oq[b]) for b in idx]
+    lk = [int(ok[b + 1] - ok[b]) for b in idx]
+    rq = np.concatenate([np.arange(oq[b], oq[b + 1]) for b in idx]).astype(np.int64)
+    rk = np.concatenate([np.arange(ok[b], ok[b + 1]) for b in idx]).astype(np.int64)
+    tq = torch.as_tensor(rq, device=batch["q"].device)
+    tk = torch.as_tensor(rk, device=batch["q"].device)
+    q, do = to64(batch["q"][tq]), to64(batch["do"][tq])
+    k, v = to64(batch["k"][tk]), to64(batch["v"][tk])
+    sub_q = workloads.offsets(lq)
+    sub_k = workloads.offsets(lk)
+    ref = run_oracle(w, q, k, v, do, sub_q, sub_k)
+    g = dict(o=to64(got["o"][tq]), dq=to64(got["dq"][tq]), dk=to64(got["dk"][tk]),
+             dv=to64(got["dv"][tk]),
+             lse=to64(got["lse"][tq]) if got.get("lse") is not None else None)
+    return compare(w, g, ref, fp32=(w.dtype == torch.float32))

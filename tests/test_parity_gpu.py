@@ -1,0 +1,167 @@
+"""GPU parity: libjfa (through its C ABI) against the fp64 CPU oracle, element by element.
+
+Small cases span several tiles and ragged tails and run the whole batch through
+the oracle; the full-size workloads run the whole batch on the GPU in the
+launch configuration the benchmark times and check sampled whole sequences.
+"""
+import numpy as np
+import pytest
+import torch
+
+import workloads
+from workloads import ACT_SILU_OVER_LEN as GD, ACT_SOFTMAX as SM, Workload
+
+from parity_util import full_check, run_gpu, sample_indices, sampled_check, to64
+
+pytestmark = pytest.mark.gpu
+
+BF16, F32 = torch.bfloat16, torch.float32
+
+
+def W(dq, dv, causal=False, act=SM, dtype=BF16, cross=False, heads=2):
+    return Workload("case", 0, heads, dq, dv, causal, act, dtype, cross)
+
+
+# ----------------------------------------------------------------------------- fp32 path
+def test_tiny_fp32_workload():
+    w = workloads.WORKLOADS["tiny"]
+    lq, lk = workloads.lengths("tiny")
+    full_check(w, lq, lk)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("act", [SM, GD])
+@pytest.mark.parametrize("dims", [(32, 32), (48, 20), (128, 64)])
+def test_fp32_self(causal, act, dims):
+    lq = [1, 7, 33, 64, 65, 130, 0, 5]
+    full_check(W(*dims, causal=causal, act=act, dtype=F32), lq)
+
+
+@pytest.mark.parametrize("act", [SM, GD])
+def test_fp32_cross(act):
+    lq = [3, 64, 1, 0, 40]
+    lk = [100, 1, 0, 7, 129]
+    full_check(W(64, 32, act=act, dtype=F32, cross=True), lq, lk)
+
+
+# ----------------------------------------------------------------------------- bf16 path
+TILE_EDGES = [1, 2, 63, 64, 65, 127, 128, 129, 255, 256, 257, 300, 511]
+
+
+@pytest.mark.parametrize("dims", [(64, 64), (128, 128), (128, 64), (64, 128)])
+@pytest.mark.parametrize("causal", [False, True])
+def test_bf16_self_softmax(dims, causal):
+    full_check(W(*dims, causal=causal), TILE_EDGES, seed=1)
+
+
+@pytest.mark.parametrize("dims", [(64, 64), (128, 128)])
+@pytest.mark.parametrize("causal", [False, True])
+def test_bf16_gdpa(dims, causal):
+    full_check(W(*dims, causal=causal, act=GD), TILE_EDGES, seed=2)
+
+
+@pytest.mark.parametrize("act", [SM, GD])
+def test_bf16_cross_asymmetric(act):
+    lq = [1, 64, 17, 63, 128, 129, 5]
+    lk = [4096, 1, 300, 129, 64, 1000, 2]
+    full_check(W(128, 64, act=act, cross=True, heads=4), lq, lk, seed=3)
+
+
+def test_bf16_zero_length_sequences():
+    full_check(W(128, 128, causal=True), [0, 130, 0, 0, 1, 0], seed=4)
+
+
+def test_cross_with_empty_key_sequences():
+    lq = [5, 70, 3]
+    lk = [0, 40, 0]
+    full_check(W(128, 64, cross=True), lq, lk, seed=5)
+    full_check(W(64, 64, cross=True, dtype=F32), lq, lk, seed=5)
+
+
+def test_single_sequence_single_row():
+    full_check(W(64, 64), [1], seed=6)
+    full_check(W(64, 64, causal=True, act=GD), [1], seed=6)
+
+
+# ----------------------------------------------------------------------------- edge cases
+def test_empty_batch():
+    import jagged_attention_recsys_gb300 as jfa
+
+    e = torch.empty(0, 2, 64, dtype=BF16, device="cuda")
+    offs = torch.zeros(1, dtype=torch.int64, device="cuda")
+    o, lse = jfa.jfa_fwd(e, e, e, offs)
+    dq, dk, dv = jfa.jfa_bwd(e, e, e, o, lse, e, offs)
+    assert o.shape == (0, 2, 64) and dq.shape == (0, 2, 64)
+
+
+def test_bad_offsets_reported_and_outputs_untouched():
+    import jagged_attention_recsys_gb300 as jfa
+
+    T, H, D = 40, 2, 64
+    q = torch.randn(T, H, D, device="cuda").to(BF16)
+    offs = torch.tensor([0, 30, 20, 40], dtype=torch.int64, device="cuda")  # not monotone
+    o = torch.full((T, H, D), 7.0, dtype=BF16, device="cuda")
+    lse = torch.zeros(T, H, device="cuda")
+    p = jfa.params_for(q, q, q, offs)
+    ws = jfa.workspace(p)
+    jfa.jfa_fwd(q, q, q, offs, o=o, lse=lse, ws=ws)
+    assert jfa.jfa_status_check(ws) == jfa.JFA_ERR_BAD_OFFSETS
+    assert torch.all(o == 7.0)
+    good = torch.tensor([0, 20, 30, 40], dtype=torch.int64, device="cuda")
+    jfa.jfa_fwd(q, q, q, good, o=o, lse=lse, ws=ws)
+    assert jfa.jfa_status_check(ws) == jfa.JFA_OK
+    last = torch.tensor([0, 20, 30, 39], dtype=torch.int64, device="cuda")  # offs[B] != T
+    jfa.jfa_fwd(q, q, q, last, o=o, lse=lse, ws=ws)
+    assert jfa.jfa_status_check(ws) == jfa.JFA_ERR_BAD_OFFSETS
+
+
+def test_causal_gdpa_needs_equal_lengths():
+    import jagged_attention_recsys_gb300 as jfa
+
+    q = torch.randn(10, 1, 64, device="cuda").to(BF16)
+    oq = torch.tensor([0, 4, 10], dtype=torch.int64, device="cuda")
+    ok = torch.tensor([0, 5, 10], dtype=torch.int64, device="cuda")
+    p = jfa.params_for(q, q, q, oq, causal=True)
+    ws = jfa.workspace(p)
+    jfa.jfa_gdpa_fwd(q, q, q, oq, ok, causal=True, ws=ws)
+    assert jfa.jfa_status_check(ws) == jfa.JFA_ERR_BAD_OFFSETS
+
+
+def test_neighbour_rows_not_overwritten():
+    """Outputs pre-filled with NaN: every row of every sequence must be written, exactly once."""
+    import jagged_attention_recsys_gb300 as jfa
+
+    w = W(128, 128, causal=True)
+    batch = workloads.make_batch(w, [129, 3, 128, 1], seed=7, device="cuda")
+    oq = torch.as_tensor(batch["offs_q"], device="cuda")
+    q, k, v, do = batch["q"], batch["k"], batch["v"], batch["do"]
+    o = torch.full_like(q, float("nan"))
+    lse = torch.full(q.shape[:2], float("nan"), device="cuda")
+    jfa.jfa_fwd(q, k, v, oq, causal=True, o=o, lse=lse)
+    dq, dk, dv = (torch.full_like(t, float("nan")) for t in (q, k, v))
+    jfa.jfa_bwd(q, k, v, o, lse, do, oq, causal=True, dq=dq, dk=dk, dv=dv)
+    torch.cuda.synchronize()
+    for t in (o, lse, dq, dk, dv):
+        assert torch.isfinite(t).all()
+
+
+def test_deterministic_bitwise():
+    w = W(128, 128, causal=True, heads=3)
+    batch = workloads.make_batch(w, [300, 17, 129, 64], seed=8, device="cuda")
+    a = run_gpu(w, batch)
+    b = run_gpu(w, batch)
+    for n in ("o", "lse", "dq", "dk", "dv"):
+        assert torch.equal(a[n], b[n]), n
+
+
+# ----------------------------------------------------------------------------- full size
+@pytest.mark.parametrize("name", ["d64", "causal", "cross", "gdpa"])
+def test_full_size_workload_sampled(name):
+    w = workloads.WORKLOADS[name]
+    batch = workloads.make_batch(w, device="cuda")
+    got = run_gpu(w, batch)
+    for t in got.values():
+        if t is not None:
+            assert torch.isfinite(t).all()
+    idx = sample_indices(batch["lq"], count=5)
+    sampled_check(w, batch, got, idx)
