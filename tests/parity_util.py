@@ -54,8 +54,14 @@ def run_oracle(w: workloads.Workload, q, k, v, do, offs_q, offs_k):
     return dict(o=o, lse=lse, dq=dq, dk=dk, dv=dv)
 
 
-def compare(w: workloads.Workload, got, ref, fp32: bool):
-    """Asserts the tolerances; returns the error figures."""
+def compare(w: workloads.Workload, got, ref, fp32: bool, strict_o: bool = False):
+    """Asserts the tolerances; returns the error figures.
+
+    The O max-abs bound of 2e-2 is stated for the named workloads, whose outputs are O(1).
+    bf16 output rounding alone is half an ulp of |o|, so for other cases (for example
+    SiLU/L cross-attention with one query and thousands of keys, |o| ~ 60) the bound is
+    scaled by max(1, max |o|).  ``strict_o`` applies the plain bound.
+    """
     errs = {}
     for name in ("o", "dq", "dk", "dv"):
         g, r = got[name], ref[name]
@@ -73,7 +79,8 @@ def compare(w: workloads.Workload, got, ref, fp32: bool):
         if "lse_maxabs" in errs:
             assert errs["lse_maxabs"] <= F32_ATOL, errs
     else:
-        assert errs["o_maxabs"] <= BF16_O_ATOL, errs
+        mag = 1.0 if strict_o else max(1.0, float(np.max(np.abs(ref["o"]))) if ref["o"].size else 1.0)
+        assert errs["o_maxabs"] <= BF16_O_ATOL * mag, errs
         assert errs["o_rel_l2"] <= BF16_REL_L2, errs
         for name in ("dq", "dk", "dv"):
             assert errs[name + "_rel_l2"] <= BF16_REL_L2, (name, errs)
@@ -82,14 +89,14 @@ def compare(w: workloads.Workload, got, ref, fp32: bool):
     return errs
 
 
-def full_check(w: workloads.Workload, lq, lk=None, seed=0, device="cuda"):
+def full_check(w: workloads.Workload, lq, lk=None, seed=0, device="cuda", strict_o=False):
     """Whole batch on GPU and in the oracle; element-by-element comparison."""
     batch = workloads.make_batch(w, lq, lk, seed=seed, device=device)
     got = run_gpu(w, batch)
     got = {n: (to64(t) if t is not None else None) for n, t in got.items()}
     q, k, v, do = (to64(batch[n]) for n in ("q", "k", "v", "do"))
     ref = run_oracle(w, q, k, v, do, batch["offs_q"], batch["offs_k"])
-    return compare(w, got, ref, fp32=(w.dtype == torch.float32))
+    return compare(w, got, ref, fp32=(w.dtype == torch.float32), strict_o=strict_o)
 
 
 def sample_indices(lq, count=6, seed=0):
@@ -105,7 +112,7 @@ def sample_indices(lq, count=6, seed=0):
     return sorted(pick)
 
 
-def sampled_check(w: workloads.Workload, batch, got, idx):
+def sampled_check(w: workloads.Workload, batch, got, idx, strict_o=True):
     """Compares the GPU result of a full batch with the oracle on a few whole sequences."""
     oq, ok = batch["offs_q"], batch["offs_k"]
     lq = [int(oq[b + 1] - oq[b]) for b in idx]
@@ -122,4 +129,4 @@ def sampled_check(w: workloads.Workload, batch, got, idx):
     g = dict(o=to64(got["o"][tq]), dq=to64(got["dq"][tq]), dk=to64(got["dk"][tk]),
              dv=to64(got["dv"][tk]),
              lse=to64(got["lse"][tq]) if got.get("lse") is not None else None)
-    return compare(w, g, ref, fp32=(w.dtype == torch.float32))
+    return compare(w, g, ref, fp32=(w.dtype == torch.float32), strict_o=strict_o)

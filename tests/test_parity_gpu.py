@@ -26,7 +26,7 @@ def W(dq, dv, causal=False, act=SM, dtype=BF16, cross=False, heads=2):
 def test_tiny_fp32_workload():
     w = workloads.WORKLOADS["tiny"]
     lq, lk = workloads.lengths("tiny")
-    full_check(w, lq, lk)
+    full_check(w, lq, lk, strict_o=True)
 
 
 @pytest.mark.parametrize("causal", [False, True])
