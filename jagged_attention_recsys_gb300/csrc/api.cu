@@ -44,7 +44,7 @@ size_t workspace_layout(int64_t batch, int64_t total_q, int64_t total_k, int hea
   w.list_k = (WorkItem*)(b + off);
   off = align_up(off + sizeof(WorkItem) * (size_t)w.max_items_k, 256);
   w.drow = (float*)(b + off);
-  off = align_up(off + sizeof(float) * (size_t)total_q * (size_t)heads, 256);
+  off = align_up(off + 2 * sizeof(float) * (size_t)total_q * (size_t)heads, 256);
   if (out) *out = w;
   return off;
 }
@@ -224,7 +224,9 @@ jfa_status run_bwd(const jfa_params* p, Kind kind, int act, const void* q, const
   }
   if (act == kActSoftmax) {
     Timed t(JFA_KERNEL_BWD_D, s);
-    if ((st = cu(launch_bwd_rowterm(pr, p->dtype, o, dout, w, s))) != JFA_OK) return st;
+    st = path == 1 ? cu(launch_tc_rowstat(pr, o, dout, lse, w, s))
+                   : cu(launch_bwd_rowterm(pr, p->dtype, o, dout, w, s));
+    if (st != JFA_OK) return st;
   }
   {
     Timed t(JFA_KERNEL_BWD_DKDV, s);

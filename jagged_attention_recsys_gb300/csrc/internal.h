@@ -53,7 +53,7 @@ struct Workspace {
   int* k_prefix;        // [B+1] k-tile prefix sums (scheduler scratch)
   WorkItem* list_q;     // [max_items_q]
   WorkItem* list_k;     // [max_items_k]
-  float* drow;          // [T_q * H] backward row term D
+  float* drow;          // [2 * T_q * H] backward row terms (layout chosen by the kernel family)
   int64_t max_items_q, max_items_k;
 };
 

@@ -10,6 +10,9 @@ SchedConfig tc_fwd_sched(const Problem& p);
 SchedConfig tc_bwd_sched(const Problem& p);
 cudaError_t launch_tc_fwd(const Problem& p, const void* q, const void* k, const void* v, void* o,
                           float* lse, const Workspace& ws, cudaStream_t s);
+// Backward row pass: head-major (lse * log2 e, D = <dO, O>) pairs in the workspace.
+cudaError_t launch_tc_rowstat(const Problem& p, const void* o, const void* dout, const float* lse,
+                              const Workspace& ws, cudaStream_t s);
 cudaError_t launch_tc_dkdv(const Problem& p, const void* q, const void* k, const void* v,
                            const float* lse, const void* dout, void* dk, void* dv,
                            const Workspace& ws, cudaStream_t s);

@@ -55,7 +55,8 @@ struct FwdLayout {
   static constexpr uint32_t V_OFF = K_OFF + 2 * K_BYTES;
   static constexpr uint32_t P_OFF = V_OFF + 2 * V_BYTES;
   static constexpr uint32_t BAR_OFF = P_OFF + 2 * P_BYTES;
-  static constexpr uint32_t SMEM = BAR_OFF + 256 + 1024;
+  // at least 120 KB so that exactly one CTA (which owns all of TMEM) fits per SM
+  static constexpr uint32_t SMEM = (BAR_OFF + 256 + 1024) > 122880u ? (BAR_OFF + 256 + 1024) : 122880u;
 };
 
 // mbarrier slots

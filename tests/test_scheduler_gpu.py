@@ -1,0 +1,119 @@
+"""The device-built jagged tile scheduler against a plain-Python statement of its rule.
+
+Rule: every (sequence b, head h, tile t) is one item; its cost is the number of inner
+steps the kernel runs for it; items are ordered by cost descending (costs of 127 and
+more share one bucket), ties by (b, t) ascending, with the H heads of one (b, t)
+adjacent.  The list is read back from the caller's workspace.
+"""
+import numpy as np
+import pytest
+import torch
+
+import workloads
+
+pytestmark = pytest.mark.gpu
+
+BUCKETS = 128
+
+
+def _align(x, a=256):
+    return (x + a - 1) // a * a
+
+
+def expected(lq, lk, H, tile, step, causal, key_major):
+    units = []
+    for b in range(len(lq)):
+        n_tiles = -(-(lk[b] if key_major else lq[b]) // tile)
+        for t in range(n_tiles):
+            if not key_major:
+                keys = min(lk[b], (t + 1) * tile) if causal else lk[b]
+                cost = -(-keys // step)
+            elif not causal:
+                cost = -(-lq[b] // step)
+            else:
+                cost = max(0, -(-lq[b] // step) - (t * tile) // step)
+            units.append((b, t, cost))
+    order = sorted(range(len(units)), key=lambda u: (-min(units[u][2], BUCKETS - 1), u))
+    out = []
+    for u in order:
+        b, t, cost = units[u]
+        for h in range(H):
+            out.append((b, h, t, cost))
+    return out
+
+
+def read_lists(ws, B, Tq, Tk, H):
+    raw = ws.cpu().numpy()
+    hdr = raw[:256].view(np.int32)
+    n_q, n_k = int(hdr[1]), int(hdr[2])
+    off = 256 + 2 * _align(4 * (B + 1))
+    max_q = H * (Tq // 32 + B + 1)
+    lq_ = raw[off:off + 16 * n_q].view(np.int32).reshape(-1, 4)
+    off2 = off + _align(16 * max_q)
+    lk_ = raw[off2:off2 + 16 * n_k].view(np.int32).reshape(-1, 4)
+    return int(hdr[0]), [tuple(x) for x in lq_], [tuple(x) for x in lk_]
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("seed", [0, 1])
+def test_tensor_core_lists(causal, seed):
+    import jagged_attention_recsys_gb300 as jfa
+
+    rng = np.random.default_rng(seed)
+    lq = rng.integers(0, 700, 37)
+    lq[3] = 0
+    lq[5] = 1
+    H = 3
+    w = workloads.Workload("s", 0, H, 64, 64, causal, 0, torch.bfloat16, False)
+    batch = workloads.make_batch(w, lq, seed=seed, device="cuda")
+    oq = torch.as_tensor(batch["offs_q"], device="cuda")
+    p = jfa.params_for(batch["q"], batch["k"], batch["v"], oq, causal=causal)
+    ws = jfa.workspace(p)
+    o, lse = jfa.jfa_fwd(batch["q"], batch["k"], batch["v"], oq, causal=causal, ws=ws)
+    st, got_q, _ = read_lists(ws, len(lq), int(oq[-1]), int(oq[-1]), H)
+    assert st == 0
+    assert got_q == expected(list(lq), list(lq), H, 128, 128, causal, False)
+    jfa.jfa_bwd(batch["q"], batch["k"], batch["v"], o, lse, batch["do"], oq, causal=causal, ws=ws)
+    st, got_q, got_k = read_lists(ws, len(lq), int(oq[-1]), int(oq[-1]), H)
+    assert st == 0
+    assert got_q == expected(list(lq), list(lq), H, 128, 64, causal, False)
+    assert got_k == expected(list(lq), list(lq), H, 128, 64, causal, True)
+
+
+def test_cuda_core_lists_cross():
+    import jagged_attention_recsys_gb300 as jfa
+
+    rng = np.random.default_rng(5)
+    lq = rng.integers(0, 90, 20)
+    lk = rng.integers(0, 300, 20)
+    H = 2
+    w = workloads.Workload("s", 0, H, 32, 32, False, 0, torch.float32, True)
+    batch = workloads.make_batch(w, lq, lk, seed=5, device="cuda")
+    oq = torch.as_tensor(batch["offs_q"], device="cuda")
+    ok = torch.as_tensor(batch["offs_k"], device="cuda")
+    p = jfa.params_for(batch["q"], batch["k"], batch["v"], oq)
+    ws = jfa.workspace(p)
+    o, lse = jfa.jfa_cross_fwd(batch["q"], batch["k"], batch["v"], oq, ok, ws=ws)
+    jfa.jfa_cross_bwd(batch["q"], batch["k"], batch["v"], o, lse, batch["do"], oq, ok, ws=ws)
+    st, got_q, got_k = read_lists(ws, len(lq), int(oq[-1]), int(ok[-1]), H)
+    assert st == 0
+    assert got_q == expected(list(lq), list(lk), H, 64, 32, False, False)
+    assert got_k == expected(list(lq), list(lk), H, 64, 32, False, True)
+
+
+def test_large_batch_many_rounds():
+    """More sequences than scheduler threads: the prefix scan runs several rounds."""
+    import jagged_attention_recsys_gb300 as jfa
+
+    rng = np.random.default_rng(9)
+    lq = rng.integers(1, 300, 2500)
+    H = 1
+    w = workloads.Workload("s", 0, H, 64, 64, True, 0, torch.bfloat16, False)
+    batch = workloads.make_batch(w, lq, seed=9, device="cuda")
+    oq = torch.as_tensor(batch["offs_q"], device="cuda")
+    p = jfa.params_for(batch["q"], batch["k"], batch["v"], oq, causal=True)
+    ws = jfa.workspace(p)
+    jfa.jfa_fwd(batch["q"], batch["k"], batch["v"], oq, causal=True, ws=ws)
+    st, got_q, _ = read_lists(ws, len(lq), int(oq[-1]), int(oq[-1]), H)
+    assert st == 0
+    assert got_q == expected(list(lq), list(lq), H, 128, 128, True, False)
