@@ -144,6 +144,31 @@ jfa_status jfa_gdpa_bwd(const jfa_params* p, const void* q, const void* k, const
                         jfa_stream_t stream);
 
 /*
+ * Allocation-free variant of jfa_fwd.  The pages describe no such call; it
+ * exists for callers that cannot allocate device memory at all -- for example
+ * a plugin running inside a host application that owns the device allocator
+ * and forbids other allocations, or a serving process that must not allocate
+ * once it has started -- and so cannot provide the workspace jfa_fwd needs.
+ *
+ * Same arguments, layouts and results as jfa_fwd, minus the workspace: the
+ * scratch (work lists and status word) lives in one 64 MiB array compiled
+ * into the library, which every GPU that loads the library holds until the
+ * process exits.  Requests whose workspace (jfa_workspace_size) would exceed
+ * 64 MiB are rejected with JFA_ERR_WORKSPACE before anything is launched.
+ * The call itself never allocates: no cudaMalloc, no cudaFree, no allocating
+ * library routine.  The first call on a device looks up the array's device
+ * address (cudaGetSymbolAddress, with that device current) and caches it;
+ * make that first call before any stream capture.  All calls share the one
+ * array, which keeps the last call's contents, so calls that may overlap on
+ * the GPU (different streams, or different host threads) race and must be
+ * serialised by the caller.  Offsets found invalid on the device make the
+ * call compute nothing, as in jfa_fwd; this variant has no status word the
+ * caller can read.
+ */
+jfa_status jfa_fwd_noalloc(const jfa_params* p, const void* q, const void* k, const void* v,
+                           const int64_t* offs, void* o, float* lse, jfa_stream_t stream);
+
+/*
  * Synchronises `stream`, then returns the device status word of the last
  * call that used `ws` (JFA_OK, JFA_ERR_BAD_OFFSETS or JFA_ERR_TIMEOUT), or
  * JFA_ERR_CUDA if the synchronisation itself failed.

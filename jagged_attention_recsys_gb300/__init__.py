@@ -35,7 +35,8 @@ KERNEL_KINDS = {"schedule": 0, "fwd": 1, "bwd_d": 2, "bwd_dkdv": 3, "bwd_dq": 4}
 # Every symbol include/jfa.h declares.
 EXPORTS = ("jfa_workspace_size", "jfa_fwd", "jfa_bwd", "jfa_cross_fwd", "jfa_cross_bwd",
            "jfa_gdpa_fwd", "jfa_gdpa_bwd", "jfa_status_check", "jfa_status_string",
-           "jfa_profile_enable", "jfa_profile_reset", "jfa_profile_read", "jfa_path_for")
+           "jfa_profile_enable", "jfa_profile_reset", "jfa_profile_read", "jfa_path_for",
+           "jfa_fwd_noalloc")
 
 
 class JfaError(RuntimeError):
@@ -79,6 +80,8 @@ def lib():
         for f in ("jfa_fwd", "jfa_bwd", "jfa_cross_fwd", "jfa_cross_bwd", "jfa_gdpa_fwd",
                   "jfa_gdpa_bwd"):
             getattr(L, f).restype = ctypes.c_int
+        L.jfa_fwd_noalloc.argtypes = [P, vp, vp, vp, i64p, vp, fp, vp]
+        L.jfa_fwd_noalloc.restype = ctypes.c_int
         L.jfa_status_check.argtypes = [vp, vp]
         L.jfa_status_check.restype = ctypes.c_int
         L.jfa_status_string.argtypes = [ctypes.c_int]
@@ -168,6 +171,22 @@ def jfa_fwd(q, k, v, offs, *, scale=None, causal=False, o=None, lse=None, ws=Non
         lse = torch.empty(q.shape[0], q.shape[1], dtype=torch.float32, device=q.device)
     _check(lib().jfa_fwd(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(offs), _ptr(o),
                          _ptr(lse), _ptr(ws), ws.numel(), _stream(stream)), "jfa_fwd")
+    return o, lse
+
+
+def jfa_fwd_noalloc(q, k, v, offs, *, scale=None, causal=False, o=None, lse=None, stream=None):
+    """jfa_fwd without a workspace (scratch in a static device array); returns (o, lse).
+
+    For callers that cannot allocate device memory; pass preallocated ``o`` and ``lse``
+    to keep the call itself free of allocations.
+    """
+    p = params_for(q, k, v, offs, scale, causal)
+    if o is None:
+        o = torch.empty(q.shape[0], q.shape[1], v.shape[2], dtype=q.dtype, device=q.device)
+    if lse is None:
+        lse = torch.empty(q.shape[0], q.shape[1], dtype=torch.float32, device=q.device)
+    _check(lib().jfa_fwd_noalloc(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(offs),
+                                 _ptr(o), _ptr(lse), _stream(stream)), "jfa_fwd_noalloc")
     return o, lse
 
 
