@@ -33,6 +33,8 @@ size_t workspace_layout(int64_t batch, int64_t total_q, int64_t total_k, int hea
   Workspace w{};
   w.hdr = (WsHeader*)(b + off);
   off = align_up(off + sizeof(WsHeader), 256);
+  w.seq = (int4*)(b + off);
+  off = align_up(off + sizeof(int4) * (size_t)batch, 256);
   w.q_prefix = (int*)(b + off);
   off = align_up(off + sizeof(int) * (size_t)(batch + 1), 256);
   w.k_prefix = (int*)(b + off);
@@ -126,7 +128,7 @@ jfa_status check_params(const jfa_params* p, Kind kind) {
     return JFA_ERR_INVALID_ARG;
   if (p->causal != 0 && p->causal != 1) return JFA_ERR_INVALID_ARG;
   if (p->batch == 0 && (p->total_q != 0 || p->total_k != 0)) return JFA_ERR_INVALID_ARG;
-  if (p->total_q > ((int64_t)1 << 31) || p->total_k > ((int64_t)1 << 31)) return JFA_ERR_UNSUPPORTED;
+  if (p->total_q > INT32_MAX || p->total_k > INT32_MAX) return JFA_ERR_UNSUPPORTED;
   if (kind == Kind::Self && p->total_k != p->total_q) return JFA_ERR_INVALID_ARG;
   if (kind == Kind::Cross && p->causal) return JFA_ERR_UNSUPPORTED;
   if (kind == Kind::Gdpa && p->causal && p->total_k != p->total_q) return JFA_ERR_INVALID_ARG;

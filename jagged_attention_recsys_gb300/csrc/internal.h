@@ -21,11 +21,24 @@ constexpr int kActSiluOverLen = 1;
 // The same shift drives SiLU(u - shift) to (-)0 for the non-softmax variant.
 constexpr float kMaskShift = 1048576.0f;  // 2^20
 
-// One unit of work produced by the jagged tile scheduler.
-//   x = sequence b, y = head h, z = tile index inside the sequence,
-//   w = cost (number of inner steps the kernel will run for it).
+// One unit of work produced by the jagged tile scheduler: (sequence b, head h,
+// tile index inside the sequence, cost = number of inner steps the kernel will
+// run for it) plus the sequence's first query / key rows and its query / key
+// lengths, so that a kernel needs a single 32-byte load per item.
 // Query-major lists hold q-tiles, key-major lists hold k-tiles.
-using WorkItem = int4;
+struct __align__(16) WorkItem {
+  int b, h, tile, cost;
+  int q0, k0, lq, lk;
+};
+
+__device__ __forceinline__ WorkItem load_item(const WorkItem* list, int i) {
+  const int4* p = reinterpret_cast<const int4*>(list + i);
+  const int4 a = __ldg(p), c = __ldg(p + 1);
+  WorkItem w;
+  w.b = a.x; w.h = a.y; w.tile = a.z; w.cost = a.w;
+  w.q0 = c.x; w.k0 = c.y; w.lq = c.z; w.lk = c.w;
+  return w;
+}
 
 // Device workspace header; lives at offset 0 of the caller's workspace.
 struct WsHeader {
@@ -49,8 +62,9 @@ struct Problem {
 // Carve-up of the caller's workspace.
 struct Workspace {
   WsHeader* hdr;
-  int* q_prefix;        // [B+1] q-tile prefix sums (scheduler scratch)
-  int* k_prefix;        // [B+1] k-tile prefix sums (scheduler scratch)
+  int4* seq;            // [B] (q0, k0, lq, lk) per sequence (scheduler scratch, large batches)
+  int* q_prefix;        // [B+1] q-tile prefix sums (scheduler scratch, large batches)
+  int* k_prefix;        // [B+1] k-tile prefix sums (scheduler scratch, large batches)
   WorkItem* list_q;     // [max_items_q]
   WorkItem* list_k;     // [max_items_k]
   float* drow;          // [2 * T_q * H] backward row terms (layout chosen by the kernel family)

@@ -8,10 +8,14 @@
 // cost (inner-loop steps); items are ordered by cost, heaviest first (the
 // longest-processing-time rule), ties by (sequence, tile) ascending, heads
 // adjacent.  Persistent CTAs then take items i, i + grid, i + 2*grid, ...
+// Each item also carries its sequence's first rows and lengths, so a kernel
+// needs one 32-byte load per item and no dependent offset lookups.
 //
 // The whole list is built by one CTA from the offsets in device memory, so a
 // call never synchronises with the host and can be captured in a CUDA graph.
-// The same kernel validates the offsets and writes the status word.
+// The same kernel validates the offsets and writes the status word.  Per-
+// sequence data and prefix sums live in shared memory for batches of up to
+// kCacheB sequences and in the workspace beyond that.
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -23,8 +27,17 @@ namespace {
 constexpr int kThreads = 1024;
 constexpr int kWarps = kThreads / 32;
 constexpr int kBuckets = 128;  // costs >= kBuckets-1 share the heaviest bucket
+constexpr int kCacheB = 4096;  // sequences cached in shared memory
 
-__device__ __forceinline__ int64_t cdiv64(int64_t a, int64_t b) { return (a + b - 1) / b; }
+struct SchedShared {
+  int warp_tot[32];
+  int hist[kBuckets], start[kBuckets], run[kBuckets];
+  int wcount[kWarps][kBuckets];
+  int4 seq[kCacheB];        // (q0, k0, lq, lk)
+  int pref[kCacheB + 1];    // tile prefix sums of the list being built
+};
+
+__device__ __forceinline__ int cdiv(int a, int b) { return (a + b - 1) / b; }
 
 // Inclusive block-wide scan of one int per thread.
 __device__ int block_inclusive_scan(int x, int* warp_tot) {
@@ -57,117 +70,117 @@ struct ListSpec {
   int step;        // keys (q-list) or rows (k-list) per inner step
 };
 
-// Number of tiles of sequence b and the cost of tile t.
-__device__ __forceinline__ int tiles_of(const ListSpec& L, int64_t lq, int64_t lk) {
-  return (int)cdiv64(L.key_major ? lk : lq, L.tile);
+__device__ __forceinline__ int tiles_of(const ListSpec& L, int lq, int lk) {
+  return cdiv(L.key_major ? lk : lq, L.tile);
 }
 
-__device__ __forceinline__ int cost_of(const ListSpec& L, int causal, int64_t lq, int64_t lk,
-                                       int t) {
-  int64_t c;
+// Inner steps the kernel runs for tile t of a sequence with lengths (lq, lk).
+__device__ __forceinline__ int cost_of(const ListSpec& L, int causal, int lq, int lk, int t) {
   if (!L.key_major) {
-    int64_t keys = causal ? min(lk, (int64_t)(t + 1) * L.tile) : lk;
-    c = cdiv64(keys, L.step);
-  } else if (!causal) {
-    c = cdiv64(lq, L.step);
-  } else {
-    // rows >= the first key of this tile, counted in whole inner steps
-    int64_t first = ((int64_t)t * L.tile) / L.step;
-    c = cdiv64(lq, L.step) - first;
-    if (c < 0) c = 0;
+    const int keys = causal ? min(lk, (t + 1) * L.tile) : lk;
+    return cdiv(keys, L.step);
   }
-  return (int)c;
+  if (!causal) return cdiv(lq, L.step);
+  // rows >= the first key of this tile, counted in whole inner steps
+  return max(0, cdiv(lq, L.step) - (t * L.tile) / L.step);
 }
 
-// Sequence owning unit u: the largest b with prefix[b] <= u.
-__device__ __forceinline__ int find_seq(const int* prefix, int64_t B, int u) {
-  int64_t lo = 0, hi = B;  // prefix[lo] <= u < prefix[hi]
+// Sequence owning unit u: the largest b with pref[b] <= u.
+__device__ __forceinline__ int find_seq(const int* pref, int B, int u) {
+  int lo = 0, hi = B;  // pref[lo] <= u < pref[hi]
   while (hi - lo > 1) {
-    int64_t mid = (lo + hi) >> 1;
-    if (prefix[mid] <= u) lo = mid; else hi = mid;
+    const int mid = (lo + hi) >> 1;
+    if (pref[mid] <= u) lo = mid; else hi = mid;
   }
-  return (int)lo;
+  return lo;
 }
 
-__device__ void build_list(const Problem& p, const ListSpec& L, int* prefix, WorkItem* list,
-                           int* n_out, int* warp_tot, int* hist, int* start, int* run,
-                           int (*wcount)[kBuckets]) {
+__device__ void build_list(const Problem& p, const ListSpec& L, const int4* seq, int* pref,
+                           WorkItem* list, int* n_out, SchedShared& sh) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int64_t B = p.batch;
-  // 1. tiles per sequence -> exclusive prefix sums in prefix[0..B]
+  const int B = (int)p.batch;
+  // 1. tiles per sequence -> exclusive prefix sums in pref[0..B]
   int carry = 0;
-  for (int64_t base = 0; base < B; base += kThreads) {
-    int64_t b = base + tid;
+  for (int base = 0; base < B; base += kThreads) {
+    const int b = base + tid;
     int cnt = 0;
-    if (b < B) {
-      int64_t lq = p.offs_q[b + 1] - p.offs_q[b];
-      int64_t lk = p.offs_k[b + 1] - p.offs_k[b];
-      cnt = tiles_of(L, lq, lk);
-    }
-    int inc = block_inclusive_scan(cnt, warp_tot);
-    if (b < B) prefix[b] = carry + inc - cnt;
-    // the last thread's inclusive value is this round's total
-    if (tid == kThreads - 1) warp_tot[0] = inc;
+    if (b < B) cnt = tiles_of(L, seq[b].z, seq[b].w);
+    const int inc = block_inclusive_scan(cnt, sh.warp_tot);
+    if (b < B) pref[b] = carry + inc - cnt;
+    if (tid == kThreads - 1) sh.warp_tot[0] = inc;  // this round's total
     __syncthreads();
-    carry += warp_tot[0];
+    carry += sh.warp_tot[0];
     __syncthreads();
   }
-  if (tid == 0) prefix[B] = carry;
+  if (tid == 0) pref[B] = carry;
   const int U = carry;
-  for (int c = tid; c < kBuckets; c += kThreads) { hist[c] = 0; run[c] = 0; }
-  for (int i = tid; i < kWarps * kBuckets; i += kThreads) (&wcount[0][0])[i] = 0;
+  for (int c = tid; c < kBuckets; c += kThreads) { sh.hist[c] = 0; sh.run[c] = 0; }
+  for (int i = tid; i < kWarps * kBuckets; i += kThreads) (&sh.wcount[0][0])[i] = 0;
   __syncthreads();
 
   // 2. histogram of buckets
   for (int u = tid; u < U; u += kThreads) {
-    int b = find_seq(prefix, B, u);
-    int t = u - prefix[b];
-    int64_t lq = p.offs_q[b + 1] - p.offs_q[b];
-    int64_t lk = p.offs_k[b + 1] - p.offs_k[b];
-    int c = min(cost_of(L, p.causal, lq, lk, t), kBuckets - 1);
-    atomicAdd(&hist[c], 1);
+    const int b = find_seq(pref, B, u);
+    const int4 s = seq[b];
+    atomicAdd(&sh.hist[min(cost_of(L, p.causal, s.z, s.w, u - pref[b]), kBuckets - 1)], 1);
   }
   __syncthreads();
   // 3. bucket starts, heaviest bucket first
-  if (tid == 0) {
-    int acc = 0;
-    for (int c = kBuckets - 1; c >= 0; --c) { start[c] = acc; acc += hist[c]; }
+  if (warp == 0) {
+    // descending exclusive scan over kBuckets counts, 4 buckets per lane
+    int v[4], sum = 0;
+#pragma unroll
+    for (int t = 0; t < 4; ++t) { v[t] = sh.hist[kBuckets - 1 - (lane * 4 + t)]; sum += v[t]; }
+    int inc = sum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, inc, o);
+      if (lane >= o) inc += y;
+    }
+    int acc = inc - sum;
+#pragma unroll
+    for (int t = 0; t < 4; ++t) { sh.start[kBuckets - 1 - (lane * 4 + t)] = acc; acc += v[t]; }
   }
   __syncthreads();
 
   // 4. stable placement, kThreads units per round
   for (int base = 0; base < U; base += kThreads) {
-    int u = base + tid;
-    bool valid = u < U;
+    const int u = base + tid;
+    const bool valid = u < U;
     int b = 0, t = 0, cost = 0, c = -1;
+    int4 s = make_int4(0, 0, 0, 0);
     if (valid) {
-      b = find_seq(prefix, B, u);
-      t = u - prefix[b];
-      int64_t lq = p.offs_q[b + 1] - p.offs_q[b];
-      int64_t lk = p.offs_k[b + 1] - p.offs_k[b];
-      cost = cost_of(L, p.causal, lq, lk, t);
+      b = find_seq(pref, B, u);
+      t = u - pref[b];
+      s = seq[b];
+      cost = cost_of(L, p.causal, s.z, s.w, t);
       c = min(cost, kBuckets - 1);
     }
-    unsigned peers = __match_any_sync(0xffffffffu, c);
-    int rank = __popc(peers & ((1u << lane) - 1u));
-    if (valid && rank == 0) wcount[warp][c] = __popc(peers);
+    const unsigned peers = __match_any_sync(0xffffffffu, c);
+    const int rank = __popc(peers & ((1u << lane) - 1u));
+    if (valid && rank == 0) sh.wcount[warp][c] = __popc(peers);
     __syncthreads();
     for (int cc = tid; cc < kBuckets; cc += kThreads) {
-      int acc = run[cc];
+      int acc = sh.run[cc];
       for (int w = 0; w < kWarps; ++w) {
-        int x = wcount[w][cc];
-        wcount[w][cc] = acc;
+        const int x = sh.wcount[w][cc];
+        sh.wcount[w][cc] = acc;
         acc += x;
       }
-      run[cc] = acc;
+      sh.run[cc] = acc;
     }
     __syncthreads();
     if (valid) {
-      int64_t pos = (int64_t)start[c] + wcount[warp][c] + rank;
-      for (int h = 0; h < p.heads; ++h) list[pos * p.heads + h] = make_int4(b, h, t, cost);
+      const int64_t pos = (int64_t)sh.start[c] + sh.wcount[warp][c] + rank;
+      for (int h = 0; h < p.heads; ++h) {
+        WorkItem w;
+        w.b = b; w.h = h; w.tile = t; w.cost = cost;
+        w.q0 = s.x; w.k0 = s.y; w.lq = s.z; w.lk = s.w;
+        list[pos * p.heads + h] = w;
+      }
     }
     __syncthreads();
-    for (int i = tid; i < kWarps * kBuckets; i += kThreads) (&wcount[0][0])[i] = 0;
+    for (int i = tid; i < kWarps * kBuckets; i += kThreads) (&sh.wcount[0][0])[i] = 0;
     __syncthreads();
   }
   if (tid == 0) *n_out = U * p.heads;
@@ -177,25 +190,30 @@ __device__ void build_list(const Problem& p, const ListSpec& L, int* prefix, Wor
 __global__ void __launch_bounds__(kThreads, 1)
 schedule_kernel(Problem p, Workspace ws, ListSpec lq_spec, ListSpec lk_spec, int build_q,
                 int build_k, int self_attention) {
-  __shared__ int warp_tot[32];
-  __shared__ int hist[kBuckets], start[kBuckets], run[kBuckets];
-  __shared__ int wcount[kWarps][kBuckets];
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  SchedShared& sh = *reinterpret_cast<SchedShared*>(smem_raw);
   const int tid = threadIdx.x;
-  const int64_t B = p.batch;
+  const int B = (int)p.batch;
+  const bool cached = B <= kCacheB;
+  int4* seq = cached ? sh.seq : ws.seq;
+  int* pref_q = cached ? sh.pref : ws.q_prefix;
+  int* pref_k = cached ? sh.pref : ws.k_prefix;
 
   // Validate: offs[0] == 0, non-decreasing, offs[B] == total; equal lengths
-  // for self-attention.
+  // for self-attention.  Record (q0, k0, lq, lk) per sequence.
   int bad = 0;
   if (tid == 0) {
     bad |= (p.offs_q[0] != 0) | (p.offs_k[0] != 0);
     bad |= (p.offs_q[B] != p.total_q) | (p.offs_k[B] != p.total_k);
   }
-  for (int64_t b = tid; b < B; b += kThreads) {
-    int64_t lq = p.offs_q[b + 1] - p.offs_q[b];
-    int64_t lk = p.offs_k[b + 1] - p.offs_k[b];
-    bad |= (lq < 0) | (lk < 0);
-    bad |= (lq > 0x3fffffffLL) | (lk > 0x3fffffffLL);
-    if (self_attention) bad |= (lq != lk);
+  for (int b = tid; b < B; b += kThreads) {
+    const int64_t q0 = p.offs_q[b], q1 = p.offs_q[b + 1];
+    const int64_t k0 = p.offs_k[b], k1 = p.offs_k[b + 1];
+    const int64_t lq = q1 - q0, lk = k1 - k0;
+    int e = (lq < 0) | (lk < 0) | (q1 > p.total_q) | (k1 > p.total_k) | (q0 < 0) | (k0 < 0);
+    if (self_attention) e |= (lq != lk);
+    bad |= e;
+    if (!e) seq[b] = make_int4((int)q0, (int)k0, (int)lq, (int)lk);
   }
   bad = __syncthreads_or(bad);
   if (bad) {
@@ -207,13 +225,11 @@ schedule_kernel(Problem p, Workspace ws, ListSpec lq_spec, ListSpec lk_spec, int
     return;
   }
   if (build_q)
-    build_list(p, lq_spec, ws.q_prefix, ws.list_q, &ws.hdr->n_q, warp_tot, hist, start, run,
-               wcount);
+    build_list(p, lq_spec, seq, pref_q, ws.list_q, &ws.hdr->n_q, sh);
   else if (tid == 0)
     ws.hdr->n_q = 0;
   if (build_k)
-    build_list(p, lk_spec, ws.k_prefix, ws.list_k, &ws.hdr->n_k, warp_tot, hist, start, run,
-               wcount);
+    build_list(p, lk_spec, seq, pref_k, ws.list_k, &ws.hdr->n_k, sh);
   else if (tid == 0)
     ws.hdr->n_k = 0;
   if (tid == 0) ws.hdr->status = JFA_OK;
@@ -225,7 +241,10 @@ cudaError_t launch_schedule(const Problem& p, const Workspace& ws, const SchedCo
                             cudaStream_t s) {
   ListSpec lq{false, c.q_rows, c.q_keys_step};
   ListSpec lk{true, c.k_keys, c.k_rows_step};
-  schedule_kernel<<<1, kThreads, 0, s>>>(p, ws, lq, lk, c.build_q, c.build_k, c.self_attention);
+  const int smem = (int)sizeof(SchedShared);
+  cudaError_t e = cudaFuncSetAttribute(schedule_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  schedule_kernel<<<1, kThreads, smem, s>>>(p, ws, lq, lk, c.build_q, c.build_k, c.self_attention);
   return cudaGetLastError();
 }
 

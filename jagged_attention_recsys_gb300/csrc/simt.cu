@@ -75,10 +75,10 @@ simt_fwd_kernel(Problem p, const T* __restrict__ q, const T* __restrict__ k,
   const float qf = q_factor(p);
   const int n = hdr->n_q;
   for (int it = blockIdx.x; it < n; it += gridDim.x) {
-    const WorkItem w = list[it];
-    const int b = w.x, h = w.y, row0 = w.z * kTileRows;
-    const int64_t q0 = p.offs_q[b], k0 = p.offs_k[b];
-    const int Lq = (int)(p.offs_q[b + 1] - q0), Lk = (int)(p.offs_k[b + 1] - k0);
+    const WorkItem w = load_item(list, it);
+    const int h = w.h, row0 = w.tile * kTileRows;
+    const int64_t q0 = w.q0, k0 = w.k0;
+    const int Lq = w.lq, Lk = w.lk;
     const float inv_len = 1.0f / (float)max(Lq, 1);
     __syncthreads();
     for (int idx = tid; idx < kTileRows * DQ; idx += kThreads) {
@@ -194,10 +194,10 @@ simt_dq_kernel(Problem p, const T* __restrict__ q, const T* __restrict__ k,
   const bool softmax = p.act == kActSoftmax;
   const int n = hdr->n_q;
   for (int it = blockIdx.x; it < n; it += gridDim.x) {
-    const WorkItem w = list[it];
-    const int b = w.x, h = w.y, row0 = w.z * kTileRows;
-    const int64_t q0 = p.offs_q[b], k0 = p.offs_k[b];
-    const int Lq = (int)(p.offs_q[b + 1] - q0), Lk = (int)(p.offs_k[b + 1] - k0);
+    const WorkItem w = load_item(list, it);
+    const int h = w.h, row0 = w.tile * kTileRows;
+    const int64_t q0 = w.q0, k0 = w.k0;
+    const int Lq = w.lq, Lk = w.lk;
     const float inv_len = 1.0f / (float)max(Lq, 1);
     __syncthreads();
     for (int idx = tid; idx < kTileRows * DQ; idx += kThreads) {
@@ -298,10 +298,10 @@ simt_dkdv_kernel(Problem p, const T* __restrict__ q, const T* __restrict__ k,
   const bool softmax = p.act == kActSoftmax;
   const int n = hdr->n_k;
   for (int it = blockIdx.x; it < n; it += gridDim.x) {
-    const WorkItem w = list[it];
-    const int b = w.x, h = w.y, key0 = w.z * kTileRows;
-    const int64_t q0 = p.offs_q[b], k0 = p.offs_k[b];
-    const int Lq = (int)(p.offs_q[b + 1] - q0), Lk = (int)(p.offs_k[b + 1] - k0);
+    const WorkItem w = load_item(list, it);
+    const int h = w.h, key0 = w.tile * kTileRows;
+    const int64_t q0 = w.q0, k0 = w.k0;
+    const int Lq = w.lq, Lk = w.lk;
     const float inv_len = 1.0f / (float)max(Lq, 1);
     __syncthreads();
     for (int idx = tid; idx < kTileRows * DQ; idx += kThreads) {

@@ -176,13 +176,15 @@ tc_dkdv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
     }
     uint32_t kv_it = 0, q_it = 0;
     bool ok = true;
+    WorkItem nxt = blockIdx.x < (unsigned)n_items ? load_item(list, blockIdx.x) : WorkItem{};
     for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
-      const WorkItem w = list[it];
-      const int n = w.w;
+      const WorkItem w = nxt;  // prefetched one item ahead
+      if (it + (int)gridDim.x < n_items) nxt = load_item(list, it + gridDim.x);
+      const int n = w.cost;
       if (n == 0) continue;
-      const int b = w.x, h = w.y, key0 = w.z * TILE;
-      const int64_t q0 = p.offs_q[b], k0 = p.offs_k[b];
-      const int Lq = (int)(p.offs_q[b + 1] - q0);
+      const int h = w.h, key0 = w.tile * TILE;
+      const int64_t q0 = w.q0, k0 = w.k0;
+      const int Lq = w.lq;
       if (lane == 0) {
         ok = mbar_wait(bar(KV_KVEMPTY), (kv_it & 1) ^ 1, abort, status);
         if (ok) {
@@ -204,6 +206,14 @@ tc_dkdv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
       for (int j = 0; j < n; ++j, ++q_it) {
         const int i0 = (qs0 + j) * STEP;
         const uint32_t st = q_it & 1, ph = (q_it >> 1) & 1;
+        // row terms of this step: issue the global loads before waiting for the stage
+        float2 rv[2];
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+          const int c = lane + 32 * t;
+          rv[t] = make_float2(0.f, 0.f);
+          if (ACT == kActSoftmax && i0 + c < Lq) rv[t] = rowstat[(int64_t)h * p.total_q + q0 + i0 + c];
+        }
         ok = mbar_wait(bar(KV_QEMPTY + st), ph ^ 1, abort, status);
         if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
         if (lane == 0) {
@@ -219,12 +229,7 @@ tc_dkdv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
         }
         float2* rs = reinterpret_cast<float2*>(smem + L::RS_OFF + st * STEP * 8);
 #pragma unroll
-        for (int t = 0; t < 2; ++t) {
-          const int c = lane + 32 * t;
-          float2 val = make_float2(0.f, 0.f);
-          if (ACT == kActSoftmax && i0 + c < Lq) val = rowstat[(int64_t)h * p.total_q + q0 + i0 + c];
-          rs[c] = val;
-        }
+        for (int t = 0; t < 2; ++t) rs[lane + 32 * t] = rv[t];
         mbar_arrive(bar(KV_RSFULL + st));
       }
     }
@@ -237,9 +242,11 @@ tc_dkdv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
       constexpr uint32_t idesc_dk = idesc_bf16(TILE, DQK, 0, 1);
       uint32_t kv_it = 0, q_it = 0, s_it = 0, p_it = 0, a_it = 0;
       bool ok = true;
+      WorkItem nxt = blockIdx.x < (unsigned)n_items ? load_item(list, blockIdx.x) : WorkItem{};
       for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
-        const WorkItem w = list[it];
-        const int n = w.w;
+        const WorkItem w = nxt;  // prefetched one item ahead
+        if (it + (int)gridDim.x < n_items) nxt = load_item(list, it + gridDim.x);
+        const int n = w.cost;
         if (n == 0) continue;
         if (!mbar_wait(bar(KV_KVFULL), kv_it & 1, abort, status)) break;
         tc_fence_after();
@@ -313,12 +320,14 @@ tc_dkdv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
     const float c_score = ACT == kActSoftmax ? p.scale * kLog2e : p.scale;
     uint32_t q_it = 0, s_it = 0, p_it = 0;
     bool ok = true;
+    WorkItem nxt = blockIdx.x < (unsigned)n_items ? load_item(list, blockIdx.x) : WorkItem{};
     for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
-      const WorkItem w = list[it];
-      const int n = w.w;
-      const int b = w.x, h = w.y, key0 = w.z * TILE;
-      const int64_t q0 = p.offs_q[b], k0 = p.offs_k[b];
-      const int Lq = (int)(p.offs_q[b + 1] - q0), Lk = (int)(p.offs_k[b + 1] - k0);
+      const WorkItem w = nxt;  // prefetched one item ahead
+      if (it + (int)gridDim.x < n_items) nxt = load_item(list, it + gridDim.x);
+      const int n = w.cost;
+      const int h = w.h, key0 = w.tile * TILE;
+      const int64_t q0 = w.q0, k0 = w.k0;
+      const int Lq = w.lq, Lk = w.lk;
       const int j = key0 + r;  // key index inside the sequence
       const float inv_len = 1.0f / (float)max(Lq, 1);
       const int qs0 = CAUSAL ? key0 / STEP : 0;
@@ -354,7 +363,7 @@ tc_dkdv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
             dp[c] = pv * (dp[c] - ld.y);
           } else {
             const float u = fmaf(sv[c], c_score, valid ? 0.f : -kMaskShift);
-            const float sg = rcp(1.f + ex2(-u * kLog2e));
+            const float sg = sigmoid_fast(u);
             sv[c] = u * sg * inv_len;
             dp[c] = dp[c] * sg * fmaf(u, 1.f - sg, 1.f) * inv_len;
           }
@@ -482,12 +491,14 @@ tc_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
       tma_prefetch_desc(&tm_v);
       uint32_t q_it = 0, k_it = 0;
       bool ok = true;
+      WorkItem nxt = blockIdx.x < (unsigned)n_items ? load_item(list, blockIdx.x) : WorkItem{};
       for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
-        const WorkItem w = list[it];
-        const int n = w.w;
+        const WorkItem w = nxt;  // prefetched one item ahead
+        if (it + (int)gridDim.x < n_items) nxt = load_item(list, it + gridDim.x);
+        const int n = w.cost;
         if (n == 0) continue;
-        const int b = w.x, h = w.y, row0 = w.z * TILE;
-        const int32_t q0 = (int32_t)p.offs_q[b], k0 = (int32_t)p.offs_k[b];
+        const int h = w.h, row0 = w.tile * TILE;
+        const int32_t q0 = w.q0, k0 = w.k0;
         if (!mbar_wait(bar(Q_QEMPTY), (q_it & 1) ^ 1, abort, status)) break;
         mbar_expect_tx(bar(Q_QFULL), L::Q_BYTES + L::O_BYTES);
 #pragma unroll
@@ -519,9 +530,11 @@ tc_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
       constexpr uint32_t idesc_dq = idesc_bf16(TILE, DQK, 0, 1);
       uint32_t q_it = 0, k_it = 0, s_it = 0, p_it = 0, a_it = 0;
       bool ok = true;
+      WorkItem nxt = blockIdx.x < (unsigned)n_items ? load_item(list, blockIdx.x) : WorkItem{};
       for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
-        const WorkItem w = list[it];
-        const int n = w.w;
+        const WorkItem w = nxt;  // prefetched one item ahead
+        if (it + (int)gridDim.x < n_items) nxt = load_item(list, it + gridDim.x);
+        const int n = w.cost;
         if (n == 0) continue;
         if (!mbar_wait(bar(Q_QFULL), q_it & 1, abort, status)) break;
         tc_fence_after();
@@ -587,12 +600,14 @@ tc_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
     const float c_score = ACT == kActSoftmax ? p.scale * kLog2e : p.scale;
     uint32_t s_it = 0, p_it = 0;
     bool ok = true;
+    WorkItem nxt = blockIdx.x < (unsigned)n_items ? load_item(list, blockIdx.x) : WorkItem{};
     for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
-      const WorkItem w = list[it];
-      const int n = w.w;
-      const int b = w.x, h = w.y, row0 = w.z * TILE;
-      const int64_t q0 = p.offs_q[b], k0 = p.offs_k[b];
-      const int Lq = (int)(p.offs_q[b + 1] - q0), Lk = (int)(p.offs_k[b + 1] - k0);
+      const WorkItem w = nxt;  // prefetched one item ahead
+      if (it + (int)gridDim.x < n_items) nxt = load_item(list, it + gridDim.x);
+      const int n = w.cost;
+      const int h = w.h, row0 = w.tile * TILE;
+      const int64_t q0 = w.q0, k0 = w.k0;
+      const int Lq = w.lq, Lk = w.lk;
       const int i = row0 + r;
       const bool row_ok = i < Lq;
       const float inv_len = 1.0f / (float)max(Lq, 1);
@@ -624,7 +639,7 @@ tc_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
             dp[c] = pv * (dp[c] - rsv.y);
           } else {
             const float u = fmaf(sv[c], c_score, valid ? 0.f : -kMaskShift);
-            const float sg = rcp(1.f + ex2(-u * kLog2e));
+            const float sg = sigmoid_fast(u);
             dp[c] = dp[c] * sg * fmaf(u, 1.f - sg, 1.f) * inv_len;
           }
         }

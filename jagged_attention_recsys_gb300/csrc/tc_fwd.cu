@@ -6,23 +6,27 @@
 // specialised warps; Generalized Dot-Product Attention bullet: the same
 // pipeline with a non-softmax activation (here SiLU(s)/L).
 //
-// One persistent CTA per SM walks the scheduler's heavy-first list of
-// (sequence, head, 128-row q-tile) items.  Warp roles:
-//   warp 0      TMA producer: Q tile once per item, K and V tiles of 128 keys
-//               into a two-stage ring, straight from the jagged [T, H*D]
+// One persistent CTA per SM walks the scheduler's heavy-first list of items;
+// an item is a PAIR of adjacent 128-row q-tiles of one (sequence, head),
+// held in two slots that share every K/V tile:
+//   warps 0..3  softmax warpgroup of slot 0, one query row per thread (TMEM lane)
+//   warps 4..7  softmax warpgroup of slot 1
+//   warp 8      TMA producer: both Q tiles once per item, K and V tiles of 128
+//               keys into an NS-stage ring, straight from the jagged [T, H*D]
 //               buffers (rows past a sequence belong to its neighbour and are
-//               masked; rows past the buffer are zero-filled by TMA).
-//   warp 1      TMEM owner and MMA issuer (one lane): S = Q K^T into one of two
-//               TMEM S buffers, then O += P V into the TMEM O accumulator; S of
-//               step j+1 is issued before PV of step j so the tensor pipe works
-//               while the softmax warps process S_j.
-//   warps 2..5  softmax warpgroup, one query row per thread (TMEM lane):
-//               tcgen05.ld of its S row, scale to log2 units, subtract a finite
-//               shift from masked columns, online max with lazy rescaling of O
-//               (only when the running max grows by more than 2^8), exp2, row
-//               sum, P as bf16 into a 128-byte-swizzled smem tile, and the
-//               epilogue O / l -> bf16, lse = (m + log2 l) ln 2.
-// TMEM: S0 cols [0,128), S1 [128,256), O [256, 256+Dv).
+//               masked; rows past the buffer are zero-filled by TMA)
+//   warp 9      TMEM owner and MMA issuer (one lane).  Per key step j it issues,
+//               slot by slot, O_s += P_s(j-1) V(j-1) and S_s(j) = Q_s K(j)^T, so
+//               the tensor pipe works on one slot while the other slot's
+//               warpgroup turns its S into P (ping-pong).
+// Softmax warpgroup, per step: tcgen05.ld of its S row, scale to log2 units,
+// subtract a finite shift from masked columns, online max with lazy rescaling
+// of O (only when the running max grows by more than 2^8), exp2, row sum,
+// and P as packed bf16 back into TMEM over the S columns; the PV product reads
+// P straight from TMEM.  Epilogue: O / l -> bf16, lse = (m + log2 l) ln 2.
+// TMEM per slot s: S (and P) at columns [256 s, 256 s + 128), O at
+// [256 s + 128, 256 s + 128 + Dv).  MMAs issued by one thread execute in
+// order, so S_s(j) overwriting P_s(j-1) is ordered after the PV that reads it.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
@@ -30,39 +34,40 @@
 #include <stdint.h>
 
 #include "tc.h"
-#include "tc_ptx.cuh"
 #include "tc_host.h"
+#include "tc_ptx.cuh"
 
 namespace jfa {
 namespace {
 using namespace tc;
 
-constexpr int BM = 128;
-constexpr int BN = 128;
-constexpr int kThreads = 192;
+constexpr int BM = 128;          // rows per slot (MMA M)
+constexpr int BN = 128;          // keys per step (MMA N of S)
+constexpr int kPair = 2 * BM;    // rows per item
+constexpr int kThreads = 320;
+constexpr int kProducerWarp = 8, kMmaWarp = 9;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleLog2 = 8.0f;
 
 template <int DQK, int DV>
 struct FwdLayout {
-  static constexpr uint32_t Q_BYTES = DQK / 64 * 16384;
+  static constexpr int NS = DQK + DV <= 128 ? 4 : (DQK + DV <= 192 ? 3 : 2);  // K/V ring stages
+  static constexpr uint32_t Q_BYTES = DQK / 64 * 16384;  // one 128-row tile
   static constexpr uint32_t K_BYTES = DQK / 64 * 16384;
   static constexpr uint32_t V_BYTES = DV / 64 * 16384;
-  static constexpr uint32_t P_BYTES = 2 * 16384;
-  static constexpr uint32_t Q_OFF = 0;
-  static constexpr uint32_t K_OFF = Q_OFF + Q_BYTES;
-  static constexpr uint32_t V_OFF = K_OFF + 2 * K_BYTES;
-  static constexpr uint32_t P_OFF = V_OFF + 2 * V_BYTES;
-  static constexpr uint32_t BAR_OFF = P_OFF + 2 * P_BYTES;
+  static constexpr uint32_t Q_OFF = 0;                    // 2 slots
+  static constexpr uint32_t K_OFF = Q_OFF + 2 * Q_BYTES;  // NS stages
+  static constexpr uint32_t V_OFF = K_OFF + NS * K_BYTES; // NS stages
+  static constexpr uint32_t BAR_OFF = V_OFF + NS * V_BYTES;
   // at least 120 KB so that exactly one CTA (which owns all of TMEM) fits per SM
   static constexpr uint32_t SMEM = (BAR_OFF + 256 + 1024) > 122880u ? (BAR_OFF + 256 + 1024) : 122880u;
 };
 
-// mbarrier slots
+// mbarrier slots (K_FULL, V_FULL, KV_EMPTY have up to 4 stages)
 enum : uint32_t {
-  B_QFULL = 0, B_QEMPTY = 1, B_KFULL = 2, B_VFULL = 4, B_KVEMPTY = 6, B_SFULL = 8,
-  B_SEMPTY = 10, B_PFULL = 12, B_PEMPTY = 14, B_OEMPTY = 16, B_COUNT = 17
+  B_QFULL = 0, B_QEMPTY = 1, B_KFULL = 2, B_VFULL = 6, B_KVEMPTY = 10, B_SFULL = 14,
+  B_PFULL = 16, B_OFULL = 18, B_OEMPTY = 20, B_COUNT = 22
 };
 
 template <int DQK, int DV, int ACT, bool CAUSAL>
@@ -72,6 +77,7 @@ tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
               __nv_bfloat16* __restrict__ out, float* __restrict__ lse, WsHeader* hdr,
               const WorkItem* __restrict__ list) {
   using L = FwdLayout<DQK, DV>;
+  constexpr int NS = L::NS;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   const uint32_t sb = smem_u32(smem);
@@ -86,161 +92,181 @@ tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
   if (threadIdx.x == 0) {
     mbar_init(bar(B_QFULL), 1);
     mbar_init(bar(B_QEMPTY), 1);
-    for (int s = 0; s < 2; ++s) {
+    for (int s = 0; s < NS; ++s) {
       mbar_init(bar(B_KFULL + s), 1);
       mbar_init(bar(B_VFULL + s), 1);
       mbar_init(bar(B_KVEMPTY + s), 1);
-      mbar_init(bar(B_SFULL + s), 1);
-      mbar_init(bar(B_SEMPTY + s), 128);
-      mbar_init(bar(B_PFULL + s), 128);
-      mbar_init(bar(B_PEMPTY + s), 1);
     }
-    mbar_init(bar(B_OEMPTY), 128);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(bar(B_SFULL + s), 1);
+      mbar_init(bar(B_PFULL + s), 128);
+      mbar_init(bar(B_OFULL + s), 1);
+      mbar_init(bar(B_OEMPTY + s), 128);
+    }
     *abort = 0;
     fence_mbar_init();
   }
-  if (warp == 1) tmem_alloc(smem_u32(tmem_slot), 512);
+  if (warp == kMmaWarp) tmem_alloc(smem_u32(tmem_slot), 512);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 0) {
+  if (warp == kProducerWarp) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
       tma_prefetch_desc(&tm_q);
       tma_prefetch_desc(&tm_k);
       tma_prefetch_desc(&tm_v);
       uint32_t kv_it = 0, q_it = 0;
-      for (int it = blockIdx.x; it < n_items; it += gridDim.x) {
-        const WorkItem w = list[it];
-        const int n = w.w;
+      bool ok = true;
+      WorkItem nxt = blockIdx.x < (unsigned)n_items ? load_item(list, blockIdx.x) : WorkItem{};
+      for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
+        const WorkItem w = nxt;  // prefetched one item ahead
+        if (it + (int)gridDim.x < n_items) nxt = load_item(list, it + gridDim.x);
+        const int n = w.cost;
         if (n == 0) continue;
-        const int b = w.x, h = w.y, row0 = w.z * BM;
-        const int32_t q0 = (int32_t)p.offs_q[b], k0 = (int32_t)p.offs_k[b];
+        const int h = w.h, row0 = w.tile * kPair;
+        const bool two = row0 + BM < w.lq;
         if (!mbar_wait(bar(B_QEMPTY), (q_it & 1) ^ 1, abort, status)) break;
-        mbar_expect_tx(bar(B_QFULL), L::Q_BYTES);
-#pragma unroll
-        for (int a = 0; a < DQK / 64; ++a)
-          tma_load_2d(sb + L::Q_OFF + a * 16384, &tm_q, h * DQK + a * 64, q0 + row0, bar(B_QFULL));
-        ++q_it;
-        bool ok = true;
-        for (int j = 0; j < n; ++j, ++kv_it) {
-          const uint32_t s = kv_it & 1, ph = (kv_it >> 1) & 1;
-          if (!mbar_wait(bar(B_KVEMPTY + s), ph ^ 1, abort, status)) { ok = false; break; }
-          mbar_expect_tx(bar(B_KFULL + s), L::K_BYTES);
+        mbar_expect_tx(bar(B_QFULL), (two ? 2u : 1u) * L::Q_BYTES);
+        for (int s = 0; s < (two ? 2 : 1); ++s) {
 #pragma unroll
           for (int a = 0; a < DQK / 64; ++a)
-            tma_load_2d(sb + L::K_OFF + s * L::K_BYTES + a * 16384, &tm_k, h * DQK + a * 64,
-                        k0 + j * BN, bar(B_KFULL + s));
-          mbar_expect_tx(bar(B_VFULL + s), L::V_BYTES);
+            tma_load_2d(sb + L::Q_OFF + s * L::Q_BYTES + a * 16384, &tm_q, h * DQK + a * 64,
+                        w.q0 + row0 + s * BM, bar(B_QFULL));
+        }
+        ++q_it;
+        for (int j = 0; j < n; ++j, ++kv_it) {
+          const uint32_t st = kv_it % NS, ph = (kv_it / NS) & 1;
+          if (!mbar_wait(bar(B_KVEMPTY + st), ph ^ 1, abort, status)) { ok = false; break; }
+          mbar_expect_tx(bar(B_KFULL + st), L::K_BYTES);
+#pragma unroll
+          for (int a = 0; a < DQK / 64; ++a)
+            tma_load_2d(sb + L::K_OFF + st * L::K_BYTES + a * 16384, &tm_k, h * DQK + a * 64,
+                        w.k0 + j * BN, bar(B_KFULL + st));
+          mbar_expect_tx(bar(B_VFULL + st), L::V_BYTES);
 #pragma unroll
           for (int a = 0; a < DV / 64; ++a)
-            tma_load_2d(sb + L::V_OFF + s * L::V_BYTES + a * 16384, &tm_v, h * DV + a * 64,
-                        k0 + j * BN, bar(B_VFULL + s));
+            tma_load_2d(sb + L::V_OFF + st * L::V_BYTES + a * 16384, &tm_v, h * DV + a * 64,
+                        w.k0 + j * BN, bar(B_VFULL + st));
         }
-        if (!ok) break;
       }
     }
     __syncwarp();
-  } else if (warp == 1) {
+  } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t idesc_s = idesc_bf16(BM, BN, 0, 0);
       constexpr uint32_t idesc_o = idesc_bf16(BM, DV, 0, 1);
-      uint32_t kv_it = 0, s_it = 0, p_it = 0, q_it = 0, o_it = 0;
+      uint32_t kv_it = 0, q_it = 0;
+      uint32_t s_cnt[2] = {0, 0}, o_cnt[2] = {0, 0};
       bool ok = true;
+      WorkItem nxt = blockIdx.x < (unsigned)n_items ? load_item(list, blockIdx.x) : WorkItem{};
       for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
-        const WorkItem w = list[it];
-        const int n = w.w;
+        const WorkItem w = nxt;
+        if (it + (int)gridDim.x < n_items) nxt = load_item(list, it + gridDim.x);
+        const int n = w.cost;
         if (n == 0) continue;
+        const int row0 = w.tile * kPair;
+        const bool two = row0 + BM < w.lq;
+        // key steps of each slot: slot 1 needs n, slot 0 one fewer on the causal diagonal
+        int ns[2];
+        ns[0] = CAUSAL ? min(n, (min(w.lk, row0 + BM) + BN - 1) / BN) : n;
+        ns[1] = two ? n : 0;
         if (!mbar_wait(bar(B_QFULL), q_it & 1, abort, status)) break;
         tc_fence_after();
-        uint32_t prev_stage = 0, prev_phase = 0;
+        uint32_t prev_st = 0;
         for (int j = 0; j <= n && ok; ++j) {
-          uint32_t cur_stage = 0, cur_phase = 0;
+          const uint32_t st = kv_it % NS;
           if (j < n) {
-            cur_stage = kv_it & 1;
-            cur_phase = (kv_it >> 1) & 1;
-            const uint32_t sbuf = s_it & 1;
-            if (!mbar_wait(bar(B_KFULL + cur_stage), cur_phase, abort, status) ||
-                !mbar_wait(bar(B_SEMPTY + sbuf), ((s_it >> 1) & 1) ^ 1, abort, status)) {
-              ok = false;
-              break;
-            }
+            if (!mbar_wait(bar(B_KFULL + st), (kv_it / NS) & 1, abort, status)) { ok = false; break; }
             tc_fence_after();
-            const uint32_t d = tmem + sbuf * 128;
+          }
+          if (j > 0 && !mbar_wait(bar(B_VFULL + prev_st), ((kv_it - 1) / NS) & 1, abort, status)) {
+            ok = false;
+            break;
+          }
 #pragma unroll
-            for (int kk = 0; kk < DQK / 16; ++kk) {
-              const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-              const uint64_t ad = sw128_desc(sb + L::Q_OFF + off, 16, 1024);
-              const uint64_t bd = sw128_desc(sb + L::K_OFF + cur_stage * L::K_BYTES + off, 16, 1024);
-              mma_bf16(d, ad, bd, idesc_s, kk > 0 ? 1u : 0u);
+          for (int s = 0; s < 2; ++s) {
+            const uint32_t s_tm = tmem + s * 256;
+            if (j > 0 && j - 1 < ns[s]) {
+              // O_s += P_s(j-1) V(j-1), P read from TMEM
+              if (!mbar_wait(bar(B_PFULL + s), (s_cnt[s] - 1) & 1, abort, status) ||
+                  (j == 1 && !mbar_wait(bar(B_OEMPTY + s), (o_cnt[s] & 1) ^ 1, abort, status))) {
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+#pragma unroll
+              for (int kk = 0; kk < BN / 16; ++kk) {
+                const uint64_t bd = sw128_desc(sb + L::V_OFF + prev_st * L::V_BYTES + kk * 2048, 16384, 1024);
+                mma_bf16_tmem_a(s_tm + 128, s_tm + kk * 8, bd, idesc_o, (j > 1 || kk > 0) ? 1u : 0u);
+              }
+              if (j == ns[s]) {
+                mma_commit(bar(B_OFULL + s));
+                ++o_cnt[s];
+              }
             }
-            mma_commit(bar(B_SFULL + sbuf));
-            if (j == n - 1) mma_commit(bar(B_QEMPTY));
-            ++s_it;
+            if (j < ns[s]) {
+              // S_s(j) = Q_s K(j)^T
+#pragma unroll
+              for (int kk = 0; kk < DQK / 16; ++kk) {
+                const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+                const uint64_t ad = sw128_desc(sb + L::Q_OFF + s * L::Q_BYTES + off, 16, 1024);
+                const uint64_t bd = sw128_desc(sb + L::K_OFF + st * L::K_BYTES + off, 16, 1024);
+                mma_bf16(s_tm, ad, bd, idesc_s, kk > 0 ? 1u : 0u);
+              }
+              mma_commit(bar(B_SFULL + s));
+              ++s_cnt[s];
+            }
+          }
+          if (!ok) break;
+          if (j == n - 1) mma_commit(bar(B_QEMPTY));
+          if (j > 0) mma_commit(bar(B_KVEMPTY + prev_st));
+          if (j < n) {
+            prev_st = st;
             ++kv_it;
           }
-          if (j > 0) {
-            const uint32_t pbuf = p_it & 1;
-            if (!mbar_wait(bar(B_PFULL + pbuf), (p_it >> 1) & 1, abort, status) ||
-                !mbar_wait(bar(B_VFULL + prev_stage), prev_phase, abort, status) ||
-                (j == 1 && !mbar_wait(bar(B_OEMPTY), (o_it & 1) ^ 1, abort, status))) {
-              ok = false;
-              break;
-            }
-            tc_fence_after();
-#pragma unroll
-            for (int kk = 0; kk < BN / 16; ++kk) {
-              const uint64_t ad = sw128_desc(sb + L::P_OFF + pbuf * L::P_BYTES + (kk >> 2) * 16384 +
-                                                 (kk & 3) * 32, 16, 1024);
-              const uint64_t bd = sw128_desc(sb + L::V_OFF + prev_stage * L::V_BYTES + kk * 2048,
-                                             16384, 1024);
-              mma_bf16(tmem + 256, ad, bd, idesc_o, (j > 1 || kk > 0) ? 1u : 0u);
-            }
-            mma_commit(bar(B_PEMPTY + pbuf));
-            mma_commit(bar(B_KVEMPTY + prev_stage));
-            ++p_it;
-          }
-          prev_stage = cur_stage;
-          prev_phase = cur_phase;
         }
         ++q_it;
-        ++o_it;
       }
     }
     __syncwarp();
   } else {
-    // ------------------------------------------------------------ softmax warpgroup
-    const int r = 32 * (warp & 3) + lane;  // TMEM lane = row of the tile
+    // ------------------------------------------------------------ softmax warpgroups
+    const int slot = warp >> 2;
+    const int r = 32 * (warp & 3) + lane;  // TMEM lane = row of the slot's tile
     const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
+    const uint32_t s_tm = tmem + slot * 256 + lane_base;
     const float c_score = ACT == kActSoftmax ? p.scale * kLog2e : p.scale;
-    uint32_t s_it = 0, p_it = 0;
+    uint32_t s_cnt = 0, o_cnt = 0;
     bool ok = true;
+    WorkItem nxt = blockIdx.x < (unsigned)n_items ? load_item(list, blockIdx.x) : WorkItem{};
     for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
-      const WorkItem w = list[it];
-      const int n = w.w;
-      const int b = w.x, h = w.y, row0 = w.z * BM;
-      const int64_t q0 = p.offs_q[b], k0 = p.offs_k[b];
-      const int Lq = (int)(p.offs_q[b + 1] - q0), Lk = (int)(p.offs_k[b + 1] - k0);
+      const WorkItem w = nxt;
+      if (it + (int)gridDim.x < n_items) nxt = load_item(list, it + gridDim.x);
+      const int n = w.cost, h = w.h;
+      const int row0 = w.tile * kPair + slot * BM;  // first row of this slot's tile
+      if (row0 >= w.lq) continue;                   // slot empty for this item
+      const int Lq = w.lq, Lk = w.lk;
+      const int ns = (slot == 0 && CAUSAL) ? min(n, (min(Lk, row0 + BM) + BN - 1) / BN) : n;
       const int i = row0 + r;
       const float inv_len = 1.0f / (float)max(Lq, 1);
       float m = -INFINITY, l = 0.f;
-      float sv[BN];
-      for (int j = 0; j < n; ++j) {
-        const uint32_t sbuf = s_it & 1;
-        if (!mbar_wait(bar(B_SFULL + sbuf), (s_it >> 1) & 1, abort, status)) { ok = false; break; }
+      for (int j = 0; j < ns; ++j) {
+        if (!mbar_wait(bar(B_SFULL + slot), s_cnt & 1, abort, status)) { ok = false; break; }
+        ++s_cnt;
         tc_fence_after();
+        float sv[BN];
 #pragma unroll
-        for (int c = 0; c < BN / 32; ++c) tmem_ld32(tmem + lane_base + sbuf * 128 + 32 * c, sv + 32 * c);
+        for (int c = 0; c < BN / 32; ++c) tmem_ld32(s_tm + 32 * c, sv + 32 * c);
         tmem_wait_ld();
-        tc_fence_before();
-        mbar_arrive(bar(B_SEMPTY + sbuf));
-        ++s_it;
         const int kb = j * BN;
         int nvalid = Lk - kb;
         if (CAUSAL) nvalid = min(nvalid, i - kb + 1);
+        float alpha = 1.f;  // rescale factor of O for this step (softmax only)
+        bool rescale = false;
         if (ACT == kActSoftmax) {
           float mt = -INFINITY;
           if (nvalid >= BN) {
@@ -256,73 +282,70 @@ tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
           if (j == 0) {
             m = mt;
           } else {
+            // lazy rescaling: move the reference max only when it grows by > 2^8
             const bool need = mt > m + kRescaleLog2;
-            if (__any_sync(0xffffffffu, need)) {
-              // O must hold PV of step j-1 before it is rescaled.
-              const uint32_t pprev = p_it - 1;
-              if (!mbar_wait(bar(B_PEMPTY + (pprev & 1)), (pprev >> 1) & 1, abort, status)) {
-                ok = false;
-                break;
-              }
-              tc_fence_after();
-              const float alpha = need ? ex2(m - mt) : 1.f;
-              float ov[32];
-#pragma unroll
-              for (int c = 0; c < DV / 32; ++c) {
-                tmem_ld32(tmem + lane_base + 256 + 32 * c, ov);
-                tmem_wait_ld();
-#pragma unroll
-                for (int t = 0; t < 32; ++t) ov[t] *= alpha;
-                tmem_st32(tmem + lane_base + 256 + 32 * c, ov);
-              }
-              tmem_wait_st();
-              l *= alpha;
-              if (need) m = mt;
+            rescale = __any_sync(0xffffffffu, need);
+            if (need) {
+              alpha = ex2(m - mt);
+              m = mt;
             }
           }
-          float rs = 0.f;
+          l *= alpha;
+        }
+        // P = exp2(s - m) (or SiLU(u)/L), packed bf16 pairs over the first 64 S columns,
+        // written 64 values at a time so the fp32 scores die as they are consumed.
+        float rs = 0.f;
 #pragma unroll
-          for (int k = 0; k < BN; ++k) { sv[k] = ex2(sv[k] - m); rs += sv[k]; }
-          l += rs;
-        } else {
+        for (int half = 0; half < 2; ++half) {
+          uint32_t pk[32];
 #pragma unroll
-          for (int k = 0; k < BN; ++k) {
-            const float u = fmaf(sv[k], c_score, k < nvalid ? 0.f : -kMaskShift);
-            const float sg = rcp(1.f + ex2(-u * kLog2e));
-            sv[k] = u * sg * inv_len;
+          for (int c = 0; c < 32; ++c) {
+            float x0 = sv[half * 64 + 2 * c], x1 = sv[half * 64 + 2 * c + 1];
+            if (ACT == kActSoftmax) {
+              x0 = ex2(x0 - m);
+              x1 = ex2(x1 - m);
+              rs += x0 + x1;
+            } else {
+              const int k0i = half * 64 + 2 * c;
+              const float u0 = fmaf(x0, c_score, k0i < nvalid ? 0.f : -kMaskShift);
+              const float u1 = fmaf(x1, c_score, k0i + 1 < nvalid ? 0.f : -kMaskShift);
+              x0 = u0 * sigmoid_fast(u0) * inv_len;
+              x1 = u1 * sigmoid_fast(u1) * inv_len;
+            }
+            pk[c] = pack_bf16(x0, x1);
+          }
+          tmem_st32(s_tm + 32 * half, reinterpret_cast<const float*>(pk));
+        }
+        if (ACT == kActSoftmax) l += rs;
+        if (rescale) {
+          // O_s already holds every PV issued before this S (in-order MMAs).
+          float ov[32];
+#pragma unroll
+          for (int c = 0; c < DV / 32; ++c) {
+            tmem_ld32(s_tm + 128 + 32 * c, ov);
+            tmem_wait_ld();
+#pragma unroll
+            for (int t = 0; t < 32; ++t) ov[t] *= alpha;
+            tmem_st32(s_tm + 128 + 32 * c, ov);
           }
         }
-        // P (bf16) into the swizzled smem tile of this buffer
-        const uint32_t pbuf = p_it & 1;
-        if (!mbar_wait(bar(B_PEMPTY + pbuf), ((p_it >> 1) & 1) ^ 1, abort, status)) { ok = false; break; }
-        const uint32_t pbase = sb + L::P_OFF + pbuf * L::P_BYTES;
-#pragma unroll
-        for (int a = 0; a < 2; ++a) {
-#pragma unroll
-          for (int ch = 0; ch < 8; ++ch) {
-            const float* x = sv + a * 64 + ch * 8;
-            st_shared_v4(pbase + a * 16384 + sw128_offset(r, ch), pack_bf16(x[0], x[1]),
-                         pack_bf16(x[2], x[3]), pack_bf16(x[4], x[5]), pack_bf16(x[6], x[7]));
-          }
-        }
-        fence_proxy_async_smem();
+        tmem_wait_st();
         tc_fence_before();
-        mbar_arrive(bar(B_PFULL + pbuf));
-        ++p_it;
+        mbar_arrive(bar(B_PFULL + slot));
       }
       if (!ok) break;
       // ---------------------------------------------------------- epilogue
       const bool row_ok = i < Lq;
-      const int64_t orow = (q0 + i) * p.heads + h;
-      if (n > 0) {
-        const uint32_t plast = p_it - 1;
-        if (!mbar_wait(bar(B_PEMPTY + (plast & 1)), (plast >> 1) & 1, abort, status)) { ok = false; break; }
+      const int64_t orow = ((int64_t)w.q0 + i) * p.heads + h;
+      if (ns > 0) {
+        if (!mbar_wait(bar(B_OFULL + slot), o_cnt & 1, abort, status)) { ok = false; break; }
+        ++o_cnt;
         tc_fence_after();
         const float norm = ACT == kActSoftmax ? (l > 0.f ? 1.f / l : 0.f) : 1.f;
         float ov[32];
 #pragma unroll
         for (int c = 0; c < DV / 32; ++c) {
-          tmem_ld32(tmem + lane_base + 256 + 32 * c, ov);
+          tmem_ld32(s_tm + 128 + 32 * c, ov);
           tmem_wait_ld();
           if (row_ok) {
             uint4* dst = reinterpret_cast<uint4*>(out + orow * DV + 32 * c);
@@ -335,7 +358,7 @@ tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
           }
         }
         tc_fence_before();
-        mbar_arrive(bar(B_OEMPTY));
+        mbar_arrive(bar(B_OEMPTY + slot));
         if (ACT == kActSoftmax && row_ok && lse != nullptr)
           lse[orow] = l > 0.f ? (m + log2f(l)) * kLn2 : -INFINITY;
       } else if (row_ok) {
@@ -349,7 +372,7 @@ tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 1) {
+  if (warp == kMmaWarp) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
@@ -384,7 +407,8 @@ bool tc_supports(int dim_qk, int dim_v) {
   return (dim_qk == 64 || dim_qk == 128) && (dim_v == 64 || dim_v == 128);
 }
 
-SchedConfig tc_fwd_sched(const Problem&) { return SchedConfig{BM, BN, BN, BM, 1, 0, 0}; }
+// Items are pairs of 128-row q-tiles; the cost is the number of 128-key steps.
+SchedConfig tc_fwd_sched(const Problem&) { return SchedConfig{kPair, BN, BN, BM, 1, 0, 0}; }
 
 cudaError_t launch_tc_fwd(const Problem& p, const void* q, const void* k, const void* v, void* o,
                           float* lse, const Workspace& ws, cudaStream_t s) {

@@ -43,15 +43,23 @@ def expected(lq, lk, H, tile, step, causal, key_major):
 
 
 def read_lists(ws, B, Tq, Tk, H):
+    """(status, q-list, k-list) from the workspace; each item is 8 int32 values."""
     raw = ws.cpu().numpy()
     hdr = raw[:256].view(np.int32)
     n_q, n_k = int(hdr[1]), int(hdr[2])
-    off = 256 + 2 * _align(4 * (B + 1))
+    off = 256 + _align(16 * B) + 2 * _align(4 * (B + 1))
     max_q = H * (Tq // 32 + B + 1)
-    lq_ = raw[off:off + 16 * n_q].view(np.int32).reshape(-1, 4)
-    off2 = off + _align(16 * max_q)
-    lk_ = raw[off2:off2 + 16 * n_k].view(np.int32).reshape(-1, 4)
+    lq_ = raw[off:off + 32 * n_q].view(np.int32).reshape(-1, 8)
+    off2 = off + _align(32 * max_q)
+    lk_ = raw[off2:off2 + 32 * n_k].view(np.int32).reshape(-1, 8)
     return int(hdr[0]), [tuple(x) for x in lq_], [tuple(x) for x in lk_]
+
+
+def with_rows(items, lq, lk):
+    """Appends (q0, k0, lq, lk) of the item's sequence, as the scheduler does."""
+    oq = np.concatenate([[0], np.cumsum(lq)])
+    ok = np.concatenate([[0], np.cumsum(lk)])
+    return [(b, h, t, c, int(oq[b]), int(ok[b]), int(lq[b]), int(lk[b])) for b, h, t, c in items]
 
 
 @pytest.mark.parametrize("causal", [False, True])
@@ -72,12 +80,12 @@ def test_tensor_core_lists(causal, seed):
     o, lse = jfa.jfa_fwd(batch["q"], batch["k"], batch["v"], oq, causal=causal, ws=ws)
     st, got_q, _ = read_lists(ws, len(lq), int(oq[-1]), int(oq[-1]), H)
     assert st == 0
-    assert got_q == expected(list(lq), list(lq), H, 128, 128, causal, False)
+    assert got_q == with_rows(expected(list(lq), list(lq), H, 256, 128, causal, False), lq, lq)
     jfa.jfa_bwd(batch["q"], batch["k"], batch["v"], o, lse, batch["do"], oq, causal=causal, ws=ws)
     st, got_q, got_k = read_lists(ws, len(lq), int(oq[-1]), int(oq[-1]), H)
     assert st == 0
-    assert got_q == expected(list(lq), list(lq), H, 128, 64, causal, False)
-    assert got_k == expected(list(lq), list(lq), H, 128, 64, causal, True)
+    assert got_q == with_rows(expected(list(lq), list(lq), H, 128, 64, causal, False), lq, lq)
+    assert got_k == with_rows(expected(list(lq), list(lq), H, 128, 64, causal, True), lq, lq)
 
 
 def test_cuda_core_lists_cross():
@@ -97,16 +105,18 @@ def test_cuda_core_lists_cross():
     jfa.jfa_cross_bwd(batch["q"], batch["k"], batch["v"], o, lse, batch["do"], oq, ok, ws=ws)
     st, got_q, got_k = read_lists(ws, len(lq), int(oq[-1]), int(ok[-1]), H)
     assert st == 0
-    assert got_q == expected(list(lq), list(lk), H, 64, 32, False, False)
-    assert got_k == expected(list(lq), list(lk), H, 64, 32, False, True)
+    assert got_q == with_rows(expected(list(lq), list(lk), H, 64, 32, False, False), lq, lk)
+    assert got_k == with_rows(expected(list(lq), list(lk), H, 64, 32, False, True), lq, lk)
 
 
-def test_large_batch_many_rounds():
-    """More sequences than scheduler threads: the prefix scan runs several rounds."""
+@pytest.mark.parametrize("nseq", [2500, 5000])
+def test_large_batch_many_rounds(nseq):
+    """More sequences than scheduler threads (several scan rounds), and more than the
+    shared-memory cache holds (per-sequence data in the workspace)."""
     import jagged_attention_recsys_gb300 as jfa
 
     rng = np.random.default_rng(9)
-    lq = rng.integers(1, 300, 2500)
+    lq = rng.integers(1, 300, nseq)
     H = 1
     w = workloads.Workload("s", 0, H, 64, 64, True, 0, torch.bfloat16, False)
     batch = workloads.make_batch(w, lq, seed=9, device="cuda")
@@ -116,4 +126,4 @@ def test_large_batch_many_rounds():
     jfa.jfa_fwd(batch["q"], batch["k"], batch["v"], oq, causal=True, ws=ws)
     st, got_q, _ = read_lists(ws, len(lq), int(oq[-1]), int(oq[-1]), H)
     assert st == 0
-    assert got_q == expected(list(lq), list(lq), H, 128, 128, True, False)
+    assert got_q == with_rows(expected(list(lq), list(lq), H, 256, 128, True, False), lq, lq)
