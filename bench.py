@@ -231,6 +231,9 @@ def run_ours(args):
     jfa.lib()
     w = workloads.WORKLOADS[args.workload]
     lq, lk = workloads.lengths(w.name, seed=0)
+    if args.max_seqs:
+        # profiling aid: the first N sequences of the workload (not a benchmark line)
+        lq, lk = lq[:args.max_seqs], lk[:args.max_seqs]
     batch = workloads.make_batch(w, lq, lk, seed=0, device=dev)
     d = dict(q=batch["q"], k=batch["k"], v=batch["v"], do=batch["do"],
              oq=torch.as_tensor(batch["offs_q"], device=dev),
@@ -324,7 +327,8 @@ def run_ours(args):
                    "useful_gflop_fwd": round(fwd_f / 1e9, 3),
                    "useful_gflop_bwd": round(bwd_f / 1e9, 3),
                    "l2": "flushed between timed steps (256 MiB write)",
-                   "parallelism": "replicas" if world > 1 else "single"},
+                   "parallelism": "replicas" if world > 1 else "single",
+                   "max_seqs": args.max_seqs or None},
         "roofline": roof, "kernels": kernels, "gpu_launches": launches,
         "e2e": e2e, "cpu_baseline": cpu, "clocks": clk.summary(),
     }
@@ -415,6 +419,8 @@ def main():
     ap.add_argument("--workload", default="d64", choices=sorted(workloads.WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--max-seqs", type=int, default=0,
+                    help="profiling aid: only the first N sequences of the workload")
     args = ap.parse_args()
     if args.warmup < 3:
         log("note: warm-up raised to 3 steps (minimum)")

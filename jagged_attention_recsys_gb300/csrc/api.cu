@@ -35,10 +35,8 @@ size_t workspace_layout(int64_t batch, int64_t total_q, int64_t total_k, int hea
   off = align_up(off + sizeof(WsHeader), 256);
   w.seq = (int4*)(b + off);
   off = align_up(off + sizeof(int4) * (size_t)batch, 256);
-  w.q_prefix = (int*)(b + off);
-  off = align_up(off + sizeof(int) * (size_t)(batch + 1), 256);
-  w.k_prefix = (int*)(b + off);
-  off = align_up(off + sizeof(int) * (size_t)(batch + 1), 256);
+  w.seq_ints = (int*)(b + off);
+  off = align_up(off + 4 * sizeof(int) * (size_t)(batch + 1), 256);
   w.max_items_q = (int64_t)heads * (total_q / kMinTile + batch + 1);
   w.list_q = (WorkItem*)(b + off);
   off = align_up(off + sizeof(WorkItem) * (size_t)w.max_items_q, 256);

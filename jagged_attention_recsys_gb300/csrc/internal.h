@@ -63,8 +63,7 @@ struct Problem {
 struct Workspace {
   WsHeader* hdr;
   int4* seq;            // [B] (q0, k0, lq, lk) per sequence (scheduler scratch, large batches)
-  int* q_prefix;        // [B+1] q-tile prefix sums (scheduler scratch, large batches)
-  int* k_prefix;        // [B+1] k-tile prefix sums (scheduler scratch, large batches)
+  int* seq_ints;        // [4 (B+1)] per-sequence scheduler arrays (scratch, large batches)
   WorkItem* list_q;     // [max_items_q]
   WorkItem* list_k;     // [max_items_k]
   float* drow;          // [2 * T_q * H] backward row terms (layout chosen by the kernel family)

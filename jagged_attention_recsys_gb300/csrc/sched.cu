@@ -4,18 +4,24 @@
 // Generalized Dot-Product Attention bullet names software tile scheduling for
 // jagged tensors, the Jagged Flash Attention bullet persistent-kernel
 // scheduling, and the Base Batch Shuffling bullet pairs heavy and light work.
-// Here every (sequence, head, tile) becomes one work item with an integer
-// cost (inner-loop steps); items are ordered by cost, heaviest first (the
-// longest-processing-time rule), ties by (sequence, tile) ascending, heads
-// adjacent.  Persistent CTAs then take items i, i + grid, i + 2*grid, ...
+//
+// Rule.  Every (sequence, head, tile) is one work item whose cost is the
+// number of inner steps the kernel runs for it.  Sequences are ordered by
+// their total cost, heaviest first (the longest-processing-time rule at
+// sequence granularity; costs are bucketed into 128 levels relative to the
+// heaviest sequence, ties by sequence index).  The tiles of one sequence are
+// contiguous, heaviest tile first, and the heads of one tile are adjacent.
+// Persistent CTAs take items i, i + grid, i + 2*grid, ...: the items that run
+// at the same time therefore belong to few sequences and share their K/V
+// tiles through L2, while the heavy sequences start first.
 // Each item also carries its sequence's first rows and lengths, so a kernel
 // needs one 32-byte load per item and no dependent offset lookups.
 //
-// The whole list is built by one CTA from the offsets in device memory, so a
-// call never synchronises with the host and can be captured in a CUDA graph.
-// The same kernel validates the offsets and writes the status word.  Per-
-// sequence data and prefix sums live in shared memory for batches of up to
-// kCacheB sequences and in the workspace beyond that.
+// The list is built by one CTA from the offsets in device memory, so a call
+// never synchronises with the host and can be captured in a CUDA graph.  The
+// same kernel validates the offsets and writes the status word.  Per-sequence
+// arrays live in shared memory for up to kCacheB sequences and in the
+// workspace beyond that.
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -26,15 +32,19 @@ namespace {
 
 constexpr int kThreads = 1024;
 constexpr int kWarps = kThreads / 32;
-constexpr int kBuckets = 128;  // costs >= kBuckets-1 share the heaviest bucket
-constexpr int kCacheB = 4096;  // sequences cached in shared memory
+constexpr int kBuckets = 128;
+constexpr int kCacheB = 4096;  // sequences whose arrays fit in shared memory
 
 struct SchedShared {
   int warp_tot[32];
   int hist[kBuckets], start[kBuckets], run[kBuckets];
   int wcount[kWarps][kBuckets];
-  int4 seq[kCacheB];        // (q0, k0, lq, lk)
-  int pref[kCacheB + 1];    // tile prefix sums of the list being built
+  int red;
+  int4 seq[kCacheB];      // (q0, k0, lq, lk)
+  int ntile[kCacheB];     // tiles of the list being built
+  int bucket[kCacheB];    // cost bucket of the sequence
+  int order[kCacheB];     // sequences in list order
+  int first[kCacheB + 1]; // first unit of the r-th sequence in list order
 };
 
 __device__ __forceinline__ int cdiv(int a, int b) { return (a + b - 1) / b; }
@@ -85,49 +95,56 @@ __device__ __forceinline__ int cost_of(const ListSpec& L, int causal, int lq, in
   return max(0, cdiv(lq, L.step) - (t * L.tile) / L.step);
 }
 
-// Sequence owning unit u: the largest b with pref[b] <= u.
-__device__ __forceinline__ int find_seq(const int* pref, int B, int u) {
-  int lo = 0, hi = B;  // pref[lo] <= u < pref[hi]
-  while (hi - lo > 1) {
-    const int mid = (lo + hi) >> 1;
-    if (pref[mid] <= u) lo = mid; else hi = mid;
-  }
-  return lo;
+// k-th tile of a sequence in list order (heaviest first): causal q-tiles grow
+// in cost with the tile index, so they are taken from the last one.
+__device__ __forceinline__ int tile_at(const ListSpec& L, int causal, int n, int k) {
+  return (causal && !L.key_major) ? n - 1 - k : k;
 }
 
-__device__ void build_list(const Problem& p, const ListSpec& L, const int4* seq, int* pref,
-                           WorkItem* list, int* n_out, SchedShared& sh) {
+struct Arrays {
+  int4* seq;
+  int* ntile;
+  int* bucket;
+  int* order;
+  int* first;
+};
+
+__device__ void build_list(const Problem& p, const ListSpec& L, const Arrays& A, WorkItem* list,
+                           int* n_out, SchedShared& sh) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int B = (int)p.batch;
-  // 1. tiles per sequence -> exclusive prefix sums in pref[0..B]
-  int carry = 0;
-  for (int base = 0; base < B; base += kThreads) {
-    const int b = base + tid;
-    int cnt = 0;
-    if (b < B) cnt = tiles_of(L, seq[b].z, seq[b].w);
-    const int inc = block_inclusive_scan(cnt, sh.warp_tot);
-    if (b < B) pref[b] = carry + inc - cnt;
-    if (tid == kThreads - 1) sh.warp_tot[0] = inc;  // this round's total
-    __syncthreads();
-    carry += sh.warp_tot[0];
-    __syncthreads();
+
+  // 1. tiles and total cost per sequence; the heaviest total
+  long long cmax = 0;
+  for (int b = tid; b < B; b += kThreads) {
+    const int4 s = A.seq[b];
+    const int n = tiles_of(L, s.z, s.w);
+    long long c = 0;
+    for (int t = 0; t < n; ++t) c += cost_of(L, p.causal, s.z, s.w, t);
+    A.ntile[b] = n;
+    A.bucket[b] = (int)min(c, (long long)0x7fffffff);  // total cost for now
+    cmax = max(cmax, c);
   }
-  if (tid == 0) pref[B] = carry;
-  const int U = carry;
+  // block max
+  for (int o = 16; o > 0; o >>= 1) cmax = max(cmax, __shfl_xor_sync(0xffffffffu, cmax, o));
+  if (tid == 0) sh.red = 0;
+  __syncthreads();
+  if (lane == 0) atomicMax(&sh.red, (int)min(cmax, (long long)0x7fffffff));
   for (int c = tid; c < kBuckets; c += kThreads) { sh.hist[c] = 0; sh.run[c] = 0; }
   for (int i = tid; i < kWarps * kBuckets; i += kThreads) (&sh.wcount[0][0])[i] = 0;
   __syncthreads();
+  const long long top = sh.red;
 
-  // 2. histogram of buckets
-  for (int u = tid; u < U; u += kThreads) {
-    const int b = find_seq(pref, B, u);
-    const int4 s = seq[b];
-    atomicAdd(&sh.hist[min(cost_of(L, p.causal, s.z, s.w, u - pref[b]), kBuckets - 1)], 1);
+  // 2. cost buckets (relative to the heaviest sequence) and their histogram
+  for (int b = tid; b < B; b += kThreads) {
+    const long long c = A.bucket[b];
+    const int k = top > 0 ? (int)(c * (kBuckets - 1) / top) : 0;
+    A.bucket[b] = k;
+    atomicAdd(&sh.hist[k], 1);
   }
   __syncthreads();
-  // 3. bucket starts, heaviest bucket first
+  // 3. bucket starts, heaviest bucket first (descending exclusive scan, 4 buckets per lane)
   if (warp == 0) {
-    // descending exclusive scan over kBuckets counts, 4 buckets per lane
     int v[4], sum = 0;
 #pragma unroll
     for (int t = 0; t < 4; ++t) { v[t] = sh.hist[kBuckets - 1 - (lane * 4 + t)]; sum += v[t]; }
@@ -143,19 +160,11 @@ __device__ void build_list(const Problem& p, const ListSpec& L, const int4* seq,
   }
   __syncthreads();
 
-  // 4. stable placement, kThreads units per round
-  for (int base = 0; base < U; base += kThreads) {
-    const int u = base + tid;
-    const bool valid = u < U;
-    int b = 0, t = 0, cost = 0, c = -1;
-    int4 s = make_int4(0, 0, 0, 0);
-    if (valid) {
-      b = find_seq(pref, B, u);
-      t = u - pref[b];
-      s = seq[b];
-      cost = cost_of(L, p.causal, s.z, s.w, t);
-      c = min(cost, kBuckets - 1);
-    }
+  // 4. stable counting sort of the sequences by bucket -> order[]
+  for (int base = 0; base < B; base += kThreads) {
+    const int b = base + tid;
+    const bool valid = b < B;
+    const int c = valid ? A.bucket[b] : -1;
     const unsigned peers = __match_any_sync(0xffffffffu, c);
     const int rank = __popc(peers & ((1u << lane) - 1u));
     if (valid && rank == 0) sh.wcount[warp][c] = __popc(peers);
@@ -170,20 +179,43 @@ __device__ void build_list(const Problem& p, const ListSpec& L, const int4* seq,
       sh.run[cc] = acc;
     }
     __syncthreads();
-    if (valid) {
-      const int64_t pos = (int64_t)sh.start[c] + sh.wcount[warp][c] + rank;
-      for (int h = 0; h < p.heads; ++h) {
-        WorkItem w;
-        w.b = b; w.h = h; w.tile = t; w.cost = cost;
-        w.q0 = s.x; w.k0 = s.y; w.lq = s.z; w.lk = s.w;
-        list[pos * p.heads + h] = w;
-      }
-    }
+    if (valid) A.order[sh.start[c] + sh.wcount[warp][c] + rank] = b;
     __syncthreads();
     for (int i = tid; i < kWarps * kBuckets; i += kThreads) (&sh.wcount[0][0])[i] = 0;
     __syncthreads();
   }
-  if (tid == 0) *n_out = U * p.heads;
+
+  // 5. first unit of every sequence in list order
+  int carry = 0;
+  for (int base = 0; base < B; base += kThreads) {
+    const int r = base + tid;
+    const int cnt = r < B ? A.ntile[A.order[r]] : 0;
+    const int inc = block_inclusive_scan(cnt, sh.warp_tot);
+    if (r < B) A.first[r] = carry + inc - cnt;
+    if (tid == kThreads - 1) sh.warp_tot[0] = inc;  // this round's total
+    __syncthreads();
+    carry += sh.warp_tot[0];
+    __syncthreads();
+  }
+
+  // 6. write the items: one thread per sequence, its tiles heaviest first
+  for (int r = tid; r < B; r += kThreads) {
+    const int b = A.order[r];
+    const int4 s = A.seq[b];
+    const int n = A.ntile[b];
+    for (int k = 0; k < n; ++k) {
+      const int t = tile_at(L, p.causal, n, k);
+      WorkItem w;
+      w.b = b; w.tile = t; w.cost = cost_of(L, p.causal, s.z, s.w, t);
+      w.q0 = s.x; w.k0 = s.y; w.lq = s.z; w.lk = s.w;
+      const int64_t pos = (int64_t)(A.first[r] + k) * p.heads;
+      for (int h = 0; h < p.heads; ++h) {
+        w.h = h;
+        list[pos + h] = w;
+      }
+    }
+  }
+  if (tid == 0) *n_out = carry * p.heads;
   __syncthreads();
 }
 
@@ -194,10 +226,13 @@ schedule_kernel(Problem p, Workspace ws, ListSpec lq_spec, ListSpec lk_spec, int
   SchedShared& sh = *reinterpret_cast<SchedShared*>(smem_raw);
   const int tid = threadIdx.x;
   const int B = (int)p.batch;
-  const bool cached = B <= kCacheB;
-  int4* seq = cached ? sh.seq : ws.seq;
-  int* pref_q = cached ? sh.pref : ws.q_prefix;
-  int* pref_k = cached ? sh.pref : ws.k_prefix;
+  Arrays A;
+  if (B <= kCacheB) {
+    A = Arrays{sh.seq, sh.ntile, sh.bucket, sh.order, sh.first};
+  } else {
+    A = Arrays{ws.seq, ws.seq_ints, ws.seq_ints + (B + 1), ws.seq_ints + 2 * (B + 1),
+               ws.seq_ints + 3 * (B + 1)};
+  }
 
   // Validate: offs[0] == 0, non-decreasing, offs[B] == total; equal lengths
   // for self-attention.  Record (q0, k0, lq, lk) per sequence.
@@ -213,7 +248,7 @@ schedule_kernel(Problem p, Workspace ws, ListSpec lq_spec, ListSpec lk_spec, int
     int e = (lq < 0) | (lk < 0) | (q1 > p.total_q) | (k1 > p.total_k) | (q0 < 0) | (k0 < 0);
     if (self_attention) e |= (lq != lk);
     bad |= e;
-    if (!e) seq[b] = make_int4((int)q0, (int)k0, (int)lq, (int)lk);
+    if (!e) A.seq[b] = make_int4((int)q0, (int)k0, (int)lq, (int)lk);
   }
   bad = __syncthreads_or(bad);
   if (bad) {
@@ -225,11 +260,11 @@ schedule_kernel(Problem p, Workspace ws, ListSpec lq_spec, ListSpec lk_spec, int
     return;
   }
   if (build_q)
-    build_list(p, lq_spec, seq, pref_q, ws.list_q, &ws.hdr->n_q, sh);
+    build_list(p, lq_spec, A, ws.list_q, &ws.hdr->n_q, sh);
   else if (tid == 0)
     ws.hdr->n_q = 0;
   if (build_k)
-    build_list(p, lk_spec, seq, pref_k, ws.list_k, &ws.hdr->n_k, sh);
+    build_list(p, lk_spec, A, ws.list_k, &ws.hdr->n_k, sh);
   else if (tid == 0)
     ws.hdr->n_k = 0;
   if (tid == 0) ws.hdr->status = JFA_OK;

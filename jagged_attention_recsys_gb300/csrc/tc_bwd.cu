@@ -85,42 +85,34 @@ __device__ __forceinline__ void store_row_bf16(__nv_bfloat16* dst, const float* 
   }
 }
 
-// Writes 64 values of one row into a 128-row x 64-column bf16 tile (one
-// 128-byte-swizzled atom column) at smem address `base`.
-__device__ __forceinline__ void store_tile_row(uint32_t base, int row, const float* x) {
-#pragma unroll
-  for (int ch = 0; ch < 8; ++ch) {
-    const float* y = x + ch * 8;
-    st_shared_v4(base + sw128_offset(row, ch), pack_bf16(y[0], y[1]), pack_bf16(y[2], y[3]),
-                 pack_bf16(y[4], y[5]), pack_bf16(y[6], y[7]));
-  }
-}
-
 // =============================================================================
 // dK / dV pass
 // =============================================================================
+// Q/dO steps are staged in an NQ-deep ring so the loads of later query steps
+// are in flight while the current ones are computed.  P^T and dS^T are written
+// back into TMEM as packed bf16 over the first 32 columns of the S^T and dP^T
+// buffers they were computed from, and the dV / dK products read them from
+// there (A operand in TMEM).
 template <int DQK, int DV>
 struct KvLayout {
+  static constexpr int NQ = 4;                            // Q/dO ring stages
   static constexpr uint32_t K_BYTES = DQK / 64 * 16384;   // 128 keys
   static constexpr uint32_t V_BYTES = DV / 64 * 16384;
   static constexpr uint32_t Q_BYTES = DQK / 64 * 8192;    // 64 rows
   static constexpr uint32_t O_BYTES = DV / 64 * 8192;
-  static constexpr uint32_t T_BYTES = 16384;              // 128 x 64 bf16
   static constexpr uint32_t K_OFF = 0;
   static constexpr uint32_t V_OFF = K_OFF + K_BYTES;
-  static constexpr uint32_t Q_OFF = V_OFF + V_BYTES;      // 2 stages
-  static constexpr uint32_t O_OFF = Q_OFF + 2 * Q_BYTES;  // 2 stages (dO)
-  static constexpr uint32_t P_OFF = O_OFF + 2 * O_BYTES;  // 2 buffers
-  static constexpr uint32_t DS_OFF = P_OFF + 2 * T_BYTES; // 2 buffers
-  static constexpr uint32_t RS_OFF = DS_OFF + 2 * T_BYTES;// 2 stages x 64 float2
-  static constexpr uint32_t BAR_OFF = RS_OFF + 2 * STEP * 8;
+  static constexpr uint32_t Q_OFF = V_OFF + V_BYTES;       // NQ stages
+  static constexpr uint32_t O_OFF = Q_OFF + NQ * Q_BYTES;  // NQ stages (dO)
+  static constexpr uint32_t RS_OFF = O_OFF + NQ * O_BYTES; // NQ stages x 64 float2
+  static constexpr uint32_t BAR_OFF = RS_OFF + NQ * STEP * 8;
   // at least 120 KB so that exactly one CTA (which owns all of TMEM) fits per SM
   static constexpr uint32_t SMEM = (BAR_OFF + 256 + 1024) > 122880u ? (BAR_OFF + 256 + 1024) : 122880u;
 };
 
 enum : uint32_t {
-  KV_KVFULL = 0, KV_KVEMPTY = 1, KV_QFULL = 2, KV_RSFULL = 4, KV_QEMPTY = 6, KV_SFULL = 8,
-  KV_SEMPTY = 10, KV_PFULL = 12, KV_PEMPTY = 14, KV_ACCEMPTY = 16, KV_COUNT = 17
+  KV_KVFULL = 0, KV_KVEMPTY = 1, KV_QFULL = 2, KV_RSFULL = 6, KV_QEMPTY = 10, KV_SFULL = 14,
+  KV_PFULL = 16, KV_ACCFULL = 18, KV_ACCEMPTY = 19, KV_COUNT = 20
 };
 
 template <int DQK, int DV, int ACT, bool CAUSAL>
@@ -131,6 +123,7 @@ tc_dkdv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
                __nv_bfloat16* __restrict__ dk, __nv_bfloat16* __restrict__ dv, WsHeader* hdr,
                const WorkItem* __restrict__ list) {
   using L = KvLayout<DQK, DV>;
+  constexpr int NQ = L::NQ;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   const uint32_t sb = smem_u32(smem);
@@ -145,15 +138,16 @@ tc_dkdv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
   if (threadIdx.x == 0) {
     mbar_init(bar(KV_KVFULL), 1);
     mbar_init(bar(KV_KVEMPTY), 1);
-    for (int s = 0; s < 2; ++s) {
+    for (int s = 0; s < NQ; ++s) {
       mbar_init(bar(KV_QFULL + s), 1);
       mbar_init(bar(KV_RSFULL + s), 32);
       mbar_init(bar(KV_QEMPTY + s), 1);
-      mbar_init(bar(KV_SFULL + s), 1);
-      mbar_init(bar(KV_SEMPTY + s), 128);
-      mbar_init(bar(KV_PFULL + s), 128);
-      mbar_init(bar(KV_PEMPTY + s), 1);
     }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(bar(KV_SFULL + s), 1);
+      mbar_init(bar(KV_PFULL + s), 128);
+    }
+    mbar_init(bar(KV_ACCFULL), 1);
     mbar_init(bar(KV_ACCEMPTY), 128);
     *abort = 0;
     fence_mbar_init();
@@ -163,7 +157,7 @@ tc_dkdv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  // TMEM columns: dK [0,128), dV [128,256), S^T [256 + 64 b), dP^T [384 + 64 b)
+  // TMEM columns: dK [0,128), dV [128,256), S^T/P^T [256 + 64 b), dP^T/dS^T [384 + 64 b)
   constexpr uint32_t T_DK = 0, T_DV = 128, T_S = 256, T_DP = 384;
 
   if (warp == 0) {
@@ -205,7 +199,7 @@ tc_dkdv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
       const int qs0 = CAUSAL ? key0 / STEP : 0;
       for (int j = 0; j < n; ++j, ++q_it) {
         const int i0 = (qs0 + j) * STEP;
-        const uint32_t st = q_it & 1, ph = (q_it >> 1) & 1;
+        const uint32_t st = q_it % NQ, ph = (q_it / NQ) & 1;
         // row terms of this step: issue the global loads before waiting for the stage
         float2 rv[2];
 #pragma unroll
@@ -240,11 +234,11 @@ tc_dkdv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
       constexpr uint32_t idesc_s = idesc_bf16(TILE, STEP, 0, 0);
       constexpr uint32_t idesc_dv = idesc_bf16(TILE, DV, 0, 1);
       constexpr uint32_t idesc_dk = idesc_bf16(TILE, DQK, 0, 1);
-      uint32_t kv_it = 0, q_it = 0, s_it = 0, p_it = 0, a_it = 0;
+      uint32_t kv_it = 0, q_it = 0, s_it = 0, a_it = 0;
       bool ok = true;
       WorkItem nxt = blockIdx.x < (unsigned)n_items ? load_item(list, blockIdx.x) : WorkItem{};
       for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
-        const WorkItem w = nxt;  // prefetched one item ahead
+        const WorkItem w = nxt;
         if (it + (int)gridDim.x < n_items) nxt = load_item(list, it + gridDim.x);
         const int n = w.cost;
         if (n == 0) continue;
@@ -254,10 +248,12 @@ tc_dkdv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
         for (int j = 0; j <= n && ok; ++j) {
           uint32_t cur_stage = 0;
           if (j < n) {
-            cur_stage = q_it & 1;
+            // S^T(j) = K Q(j)^T and dP^T(j) = V dO(j)^T into buffer j % 2.  The buffer
+            // held step j-2, whose P^T / dS^T were consumed by the dV / dK products
+            // issued (in order) before this point.
+            cur_stage = q_it % NQ;
             const uint32_t sbuf = s_it & 1;
-            if (!mbar_wait(bar(KV_QFULL + cur_stage), (q_it >> 1) & 1, abort, status) ||
-                !mbar_wait(bar(KV_SEMPTY + sbuf), ((s_it >> 1) & 1) ^ 1, abort, status)) {
+            if (!mbar_wait(bar(KV_QFULL + cur_stage), (q_it / NQ) & 1, abort, status)) {
               ok = false;
               break;
             }
@@ -282,8 +278,10 @@ tc_dkdv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
             ++q_it;
           }
           if (j > 0) {
-            const uint32_t pbuf = p_it & 1;
-            if (!mbar_wait(bar(KV_PFULL + pbuf), (p_it >> 1) & 1, abort, status) ||
+            // dV += P^T(j-1) dO(j-1), dK += dS^T(j-1) Q(j-1); A operands from TMEM
+            const uint32_t pbuf = (s_it - (j < n ? 2 : 1)) & 1;
+            const uint32_t pidx = s_it - (j < n ? 2 : 1);
+            if (!mbar_wait(bar(KV_PFULL + pbuf), (pidx >> 1) & 1, abort, status) ||
                 (j == 1 && !mbar_wait(bar(KV_ACCEMPTY), (a_it & 1) ^ 1, abort, status))) {
               ok = false;
               break;
@@ -292,19 +290,18 @@ tc_dkdv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
             const uint32_t acc = j > 1 ? 1u : 0u;
 #pragma unroll
             for (int kk = 0; kk < STEP / 16; ++kk) {
-              const uint64_t ad = sw128_desc(sb + L::P_OFF + pbuf * L::T_BYTES + kk * 32, 16, 1024);
               const uint64_t bd = sw128_desc(sb + L::O_OFF + prev_stage * L::O_BYTES + kk * 2048, 8192, 1024);
-              mma_bf16(tmem + T_DV, ad, bd, idesc_dv, (acc | (kk > 0)) ? 1u : 0u);
+              mma_bf16_tmem_a(tmem + T_DV, tmem + T_S + pbuf * STEP + kk * 8, bd, idesc_dv,
+                              (acc | (kk > 0)) ? 1u : 0u);
             }
 #pragma unroll
             for (int kk = 0; kk < STEP / 16; ++kk) {
-              const uint64_t ad = sw128_desc(sb + L::DS_OFF + pbuf * L::T_BYTES + kk * 32, 16, 1024);
               const uint64_t bd = sw128_desc(sb + L::Q_OFF + prev_stage * L::Q_BYTES + kk * 2048, 8192, 1024);
-              mma_bf16(tmem + T_DK, ad, bd, idesc_dk, (acc | (kk > 0)) ? 1u : 0u);
+              mma_bf16_tmem_a(tmem + T_DK, tmem + T_DP + pbuf * STEP + kk * 8, bd, idesc_dk,
+                              (acc | (kk > 0)) ? 1u : 0u);
             }
-            mma_commit(bar(KV_PEMPTY + pbuf));
             mma_commit(bar(KV_QEMPTY + prev_stage));
-            ++p_it;
+            if (j == n) mma_commit(bar(KV_ACCFULL));
           }
           prev_stage = cur_stage;
         }
@@ -318,15 +315,15 @@ tc_dkdv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
     const int r = 32 * (warp & 3) + lane;  // key of the tile = TMEM lane
     const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
     const float c_score = ACT == kActSoftmax ? p.scale * kLog2e : p.scale;
-    uint32_t q_it = 0, s_it = 0, p_it = 0;
+    uint32_t q_it = 0, s_it = 0, a_it = 0;
     bool ok = true;
     WorkItem nxt = blockIdx.x < (unsigned)n_items ? load_item(list, blockIdx.x) : WorkItem{};
     for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
-      const WorkItem w = nxt;  // prefetched one item ahead
+      const WorkItem w = nxt;
       if (it + (int)gridDim.x < n_items) nxt = load_item(list, it + gridDim.x);
       const int n = w.cost;
       const int h = w.h, key0 = w.tile * TILE;
-      const int64_t q0 = w.q0, k0 = w.k0;
+      const int64_t k0 = w.k0;
       const int Lq = w.lq, Lk = w.lk;
       const int j = key0 + r;  // key index inside the sequence
       const float inv_len = 1.0f / (float)max(Lq, 1);
@@ -336,53 +333,56 @@ tc_dkdv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
         if (!mbar_wait(bar(KV_SFULL + sbuf), (s_it >> 1) & 1, abort, status)) { ok = false; break; }
         tc_fence_after();
         float sv[STEP], dp[STEP];
-        tmem_ld32(tmem + lane_base + T_S + sbuf * STEP, sv);
-        tmem_ld32(tmem + lane_base + T_S + sbuf * STEP + 32, sv + 32);
-        tmem_ld32(tmem + lane_base + T_DP + sbuf * STEP, dp);
-        tmem_ld32(tmem + lane_base + T_DP + sbuf * STEP + 32, dp + 32);
+        const uint32_t s_tm = tmem + lane_base + T_S + sbuf * STEP;
+        const uint32_t p_tm = tmem + lane_base + T_DP + sbuf * STEP;
+        tmem_ld32(s_tm, sv);
+        tmem_ld32(s_tm + 32, sv + 32);
+        tmem_ld32(p_tm, dp);
+        tmem_ld32(p_tm + 32, dp + 32);
         tmem_wait_ld();
-        tc_fence_before();
-        mbar_arrive(bar(KV_SEMPTY + sbuf));
-        ++s_it;
-        const uint32_t st = q_it & 1;
-        if (!mbar_wait(bar(KV_RSFULL + st), (q_it >> 1) & 1, abort, status)) { ok = false; break; }
+        const uint32_t st = q_it % NQ;
+        if (!mbar_wait(bar(KV_RSFULL + st), (q_it / NQ) & 1, abort, status)) { ok = false; break; }
         const float2* rs = reinterpret_cast<const float2*>(smem + L::RS_OFF + st * STEP * 8);
         const int i0 = (qs0 + step) * STEP;
         // valid queries of this step for key j: i < Lq and (causal) i >= j
-        int lo = CAUSAL ? j - i0 : 0;
-        int hi = Lq - i0;
-        if (j >= Lk) hi = 0;
+        const int lo = CAUSAL ? j - i0 : 0;
+        const int hi = j < Lk ? Lq - i0 : 0;
+        uint32_t pk[STEP / 2], dk2[STEP / 2];
 #pragma unroll
-        for (int c = 0; c < STEP; ++c) {
-          const bool valid = c >= lo && c < hi;
-          if (ACT == kActSoftmax) {
-            const float2 ld = rs[c];
-            const float x = fmaf(sv[c], c_score, valid ? -ld.x : -ld.x - kMaskShift);
-            const float pv = ex2(x);
-            sv[c] = pv;
-            dp[c] = pv * (dp[c] - ld.y);
-          } else {
-            const float u = fmaf(sv[c], c_score, valid ? 0.f : -kMaskShift);
-            const float sg = sigmoid_fast(u);
-            sv[c] = u * sg * inv_len;
-            dp[c] = dp[c] * sg * fmaf(u, 1.f - sg, 1.f) * inv_len;
+        for (int c = 0; c < STEP; c += 2) {
+          float pv[2], ds[2];
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const bool valid = c + e >= lo && c + e < hi;
+            if (ACT == kActSoftmax) {
+              const float2 ld = rs[c + e];
+              const float x = fmaf(sv[c + e], c_score, valid ? -ld.x : -ld.x - kMaskShift);
+              pv[e] = ex2(x);
+              ds[e] = pv[e] * (dp[c + e] - ld.y);
+            } else {
+              const float u = fmaf(sv[c + e], c_score, valid ? 0.f : -kMaskShift);
+              const float sg = sigmoid_fast(u);
+              pv[e] = u * sg * inv_len;
+              ds[e] = dp[c + e] * sg * fmaf(u, 1.f - sg, 1.f) * inv_len;
+            }
           }
+          pk[c / 2] = pack_bf16(pv[0], pv[1]);
+          dk2[c / 2] = pack_bf16(ds[0], ds[1]);
         }
-        const uint32_t pbuf = p_it & 1;
-        if (!mbar_wait(bar(KV_PEMPTY + pbuf), ((p_it >> 1) & 1) ^ 1, abort, status)) { ok = false; break; }
-        store_tile_row(sb + L::P_OFF + pbuf * L::T_BYTES, r, sv);
-        store_tile_row(sb + L::DS_OFF + pbuf * L::T_BYTES, r, dp);
-        fence_proxy_async_smem();
-        mbar_arrive(bar(KV_PFULL + pbuf));
-        ++p_it;
+        tmem_st32(s_tm, reinterpret_cast<const float*>(pk));
+        tmem_st32(p_tm, reinterpret_cast<const float*>(dk2));
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(bar(KV_PFULL + sbuf));
+        ++s_it;
       }
       if (!ok) break;
       // ---------------------------------------------------------- epilogue
       const bool key_ok = j < Lk;
       const int64_t krow = (k0 + j) * p.heads + h;
       if (n > 0) {
-        const uint32_t plast = p_it - 1;
-        if (!mbar_wait(bar(KV_PEMPTY + (plast & 1)), (plast >> 1) & 1, abort, status)) { ok = false; break; }
+        if (!mbar_wait(bar(KV_ACCFULL), a_it & 1, abort, status)) { ok = false; break; }
+        ++a_it;
         tc_fence_after();
         float x[32];
 #pragma unroll
@@ -420,26 +420,27 @@ tc_dkdv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
 // =============================================================================
 // dQ pass
 // =============================================================================
+// K/V steps are staged in an NK-deep ring; dS is written back into TMEM as
+// packed bf16 over the first 32 columns of the dP buffer and the dQ product
+// reads it from there.
 template <int DQK, int DV>
 struct QLayout {
+  static constexpr int NK = 4;                             // K/V ring stages
   static constexpr uint32_t Q_BYTES = DQK / 64 * 16384;   // 128 rows
   static constexpr uint32_t O_BYTES = DV / 64 * 16384;
   static constexpr uint32_t K_BYTES = DQK / 64 * 8192;    // 64 keys
   static constexpr uint32_t V_BYTES = DV / 64 * 8192;
-  static constexpr uint32_t T_BYTES = 16384;              // 128 x 64 bf16
   static constexpr uint32_t Q_OFF = 0;
   static constexpr uint32_t O_OFF = Q_OFF + Q_BYTES;
-  static constexpr uint32_t K_OFF = O_OFF + O_BYTES;      // 2 stages
-  static constexpr uint32_t V_OFF = K_OFF + 2 * K_BYTES;  // 2 stages
-  static constexpr uint32_t DS_OFF = V_OFF + 2 * V_BYTES; // 2 buffers
-  static constexpr uint32_t BAR_OFF = DS_OFF + 2 * T_BYTES;
-  // at least 120 KB so that exactly one CTA (which owns all of TMEM) fits per SM
+  static constexpr uint32_t K_OFF = O_OFF + O_BYTES;       // NK stages
+  static constexpr uint32_t V_OFF = K_OFF + NK * K_BYTES;  // NK stages
+  static constexpr uint32_t BAR_OFF = V_OFF + NK * V_BYTES;
   static constexpr uint32_t SMEM = (BAR_OFF + 256 + 1024) > 122880u ? (BAR_OFF + 256 + 1024) : 122880u;
 };
 
 enum : uint32_t {
-  Q_QFULL = 0, Q_QEMPTY = 1, Q_KFULL = 2, Q_KEMPTY = 4, Q_SFULL = 6, Q_SEMPTY = 8, Q_PFULL = 10,
-  Q_PEMPTY = 12, Q_ACCEMPTY = 14, Q_COUNT = 15
+  Q_QFULL = 0, Q_QEMPTY = 1, Q_KFULL = 2, Q_KEMPTY = 6, Q_SFULL = 10, Q_PFULL = 12,
+  Q_ACCFULL = 14, Q_ACCEMPTY = 15, Q_COUNT = 16
 };
 
 template <int DQK, int DV, int ACT, bool CAUSAL>
@@ -449,6 +450,7 @@ tc_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
              const Problem p, const float2* __restrict__ rowstat, __nv_bfloat16* __restrict__ dq,
              WsHeader* hdr, const WorkItem* __restrict__ list) {
   using L = QLayout<DQK, DV>;
+  constexpr int NK = L::NK;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   const uint32_t sb = smem_u32(smem);
@@ -463,14 +465,15 @@ tc_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
   if (threadIdx.x == 0) {
     mbar_init(bar(Q_QFULL), 1);
     mbar_init(bar(Q_QEMPTY), 1);
-    for (int s = 0; s < 2; ++s) {
+    for (int s = 0; s < NK; ++s) {
       mbar_init(bar(Q_KFULL + s), 1);
       mbar_init(bar(Q_KEMPTY + s), 1);
-      mbar_init(bar(Q_SFULL + s), 1);
-      mbar_init(bar(Q_SEMPTY + s), 128);
-      mbar_init(bar(Q_PFULL + s), 128);
-      mbar_init(bar(Q_PEMPTY + s), 1);
     }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(bar(Q_SFULL + s), 1);
+      mbar_init(bar(Q_PFULL + s), 128);
+    }
+    mbar_init(bar(Q_ACCFULL), 1);
     mbar_init(bar(Q_ACCEMPTY), 128);
     *abort = 0;
     fence_mbar_init();
@@ -480,7 +483,7 @@ tc_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  // TMEM columns: dQ [0,128), S [128 + 64 b), dP [256 + 64 b)
+  // TMEM columns: dQ [0,128), S [128 + 64 b), dP/dS [256 + 64 b)
   constexpr uint32_t T_DQ = 0, T_S = 128, T_DP = 256;
 
   if (warp == 0) {
@@ -509,7 +512,7 @@ tc_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
           tma_load_2d(sb + L::O_OFF + a * 16384, &tm_do, h * DV + a * 64, q0 + row0, bar(Q_QFULL));
         ++q_it;
         for (int j = 0; j < n; ++j, ++k_it) {
-          const uint32_t st = k_it & 1, ph = (k_it >> 1) & 1;
+          const uint32_t st = k_it % NK, ph = (k_it / NK) & 1;
           if (!mbar_wait(bar(Q_KEMPTY + st), ph ^ 1, abort, status)) { ok = false; break; }
           mbar_expect_tx(bar(Q_KFULL + st), L::K_BYTES + L::V_BYTES);
 #pragma unroll
@@ -528,11 +531,11 @@ tc_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
     if (lane == 0) {
       constexpr uint32_t idesc_s = idesc_bf16(TILE, STEP, 0, 0);
       constexpr uint32_t idesc_dq = idesc_bf16(TILE, DQK, 0, 1);
-      uint32_t q_it = 0, k_it = 0, s_it = 0, p_it = 0, a_it = 0;
+      uint32_t q_it = 0, k_it = 0, s_it = 0, a_it = 0;
       bool ok = true;
       WorkItem nxt = blockIdx.x < (unsigned)n_items ? load_item(list, blockIdx.x) : WorkItem{};
       for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
-        const WorkItem w = nxt;  // prefetched one item ahead
+        const WorkItem w = nxt;
         if (it + (int)gridDim.x < n_items) nxt = load_item(list, it + gridDim.x);
         const int n = w.cost;
         if (n == 0) continue;
@@ -542,10 +545,9 @@ tc_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
         for (int j = 0; j <= n && ok; ++j) {
           uint32_t cur_stage = 0;
           if (j < n) {
-            cur_stage = k_it & 1;
+            cur_stage = k_it % NK;
             const uint32_t sbuf = s_it & 1;
-            if (!mbar_wait(bar(Q_KFULL + cur_stage), (k_it >> 1) & 1, abort, status) ||
-                !mbar_wait(bar(Q_SEMPTY + sbuf), ((s_it >> 1) & 1) ^ 1, abort, status)) {
+            if (!mbar_wait(bar(Q_KFULL + cur_stage), (k_it / NK) & 1, abort, status)) {
               ok = false;
               break;
             }
@@ -570,8 +572,10 @@ tc_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
             ++k_it;
           }
           if (j > 0) {
-            const uint32_t pbuf = p_it & 1;
-            if (!mbar_wait(bar(Q_PFULL + pbuf), (p_it >> 1) & 1, abort, status) ||
+            // dQ += dS(j-1) K(j-1), dS from TMEM
+            const uint32_t pidx = s_it - (j < n ? 2 : 1);
+            const uint32_t pbuf = pidx & 1;
+            if (!mbar_wait(bar(Q_PFULL + pbuf), (pidx >> 1) & 1, abort, status) ||
                 (j == 1 && !mbar_wait(bar(Q_ACCEMPTY), (a_it & 1) ^ 1, abort, status))) {
               ok = false;
               break;
@@ -579,13 +583,12 @@ tc_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
             tc_fence_after();
 #pragma unroll
             for (int kk = 0; kk < STEP / 16; ++kk) {
-              const uint64_t ad = sw128_desc(sb + L::DS_OFF + pbuf * L::T_BYTES + kk * 32, 16, 1024);
               const uint64_t bd = sw128_desc(sb + L::K_OFF + prev_stage * L::K_BYTES + kk * 2048, 8192, 1024);
-              mma_bf16(tmem + T_DQ, ad, bd, idesc_dq, (j > 1 || kk > 0) ? 1u : 0u);
+              mma_bf16_tmem_a(tmem + T_DQ, tmem + T_DP + pbuf * STEP + kk * 8, bd, idesc_dq,
+                              (j > 1 || kk > 0) ? 1u : 0u);
             }
-            mma_commit(bar(Q_PEMPTY + pbuf));
             mma_commit(bar(Q_KEMPTY + prev_stage));
-            ++p_it;
+            if (j == n) mma_commit(bar(Q_ACCFULL));
           }
           prev_stage = cur_stage;
         }
@@ -598,15 +601,15 @@ tc_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
     const int r = 32 * (warp & 3) + lane;  // query row of the tile = TMEM lane
     const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
     const float c_score = ACT == kActSoftmax ? p.scale * kLog2e : p.scale;
-    uint32_t s_it = 0, p_it = 0;
+    uint32_t s_it = 0, a_it = 0;
     bool ok = true;
     WorkItem nxt = blockIdx.x < (unsigned)n_items ? load_item(list, blockIdx.x) : WorkItem{};
     for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
-      const WorkItem w = nxt;  // prefetched one item ahead
+      const WorkItem w = nxt;
       if (it + (int)gridDim.x < n_items) nxt = load_item(list, it + gridDim.x);
       const int n = w.cost;
       const int h = w.h, row0 = w.tile * TILE;
-      const int64_t q0 = w.q0, k0 = w.k0;
+      const int64_t q0 = w.q0;
       const int Lq = w.lq, Lk = w.lk;
       const int i = row0 + r;
       const bool row_ok = i < Lq;
@@ -618,43 +621,46 @@ tc_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
         if (!mbar_wait(bar(Q_SFULL + sbuf), (s_it >> 1) & 1, abort, status)) { ok = false; break; }
         tc_fence_after();
         float sv[STEP], dp[STEP];
-        tmem_ld32(tmem + lane_base + T_S + sbuf * STEP, sv);
-        tmem_ld32(tmem + lane_base + T_S + sbuf * STEP + 32, sv + 32);
-        tmem_ld32(tmem + lane_base + T_DP + sbuf * STEP, dp);
-        tmem_ld32(tmem + lane_base + T_DP + sbuf * STEP + 32, dp + 32);
+        const uint32_t s_tm = tmem + lane_base + T_S + sbuf * STEP;
+        const uint32_t p_tm = tmem + lane_base + T_DP + sbuf * STEP;
+        tmem_ld32(s_tm, sv);
+        tmem_ld32(s_tm + 32, sv + 32);
+        tmem_ld32(p_tm, dp);
+        tmem_ld32(p_tm + 32, dp + 32);
         tmem_wait_ld();
-        tc_fence_before();
-        mbar_arrive(bar(Q_SEMPTY + sbuf));
-        ++s_it;
         const int kb = step * STEP;
         int nvalid = Lk - kb;
         if (CAUSAL) nvalid = min(nvalid, i - kb + 1);
         if (!row_ok) nvalid = 0;
+        uint32_t pk[STEP / 2];
 #pragma unroll
-        for (int c = 0; c < STEP; ++c) {
-          const bool valid = c < nvalid;
-          if (ACT == kActSoftmax) {
-            const float x = fmaf(sv[c], c_score, valid ? -rsv.x : -rsv.x - kMaskShift);
-            const float pv = ex2(x);
-            dp[c] = pv * (dp[c] - rsv.y);
-          } else {
-            const float u = fmaf(sv[c], c_score, valid ? 0.f : -kMaskShift);
-            const float sg = sigmoid_fast(u);
-            dp[c] = dp[c] * sg * fmaf(u, 1.f - sg, 1.f) * inv_len;
+        for (int c = 0; c < STEP; c += 2) {
+          float ds[2];
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const bool valid = c + e < nvalid;
+            if (ACT == kActSoftmax) {
+              const float x = fmaf(sv[c + e], c_score, valid ? -rsv.x : -rsv.x - kMaskShift);
+              ds[e] = ex2(x) * (dp[c + e] - rsv.y);
+            } else {
+              const float u = fmaf(sv[c + e], c_score, valid ? 0.f : -kMaskShift);
+              const float sg = sigmoid_fast(u);
+              ds[e] = dp[c + e] * sg * fmaf(u, 1.f - sg, 1.f) * inv_len;
+            }
           }
+          pk[c / 2] = pack_bf16(ds[0], ds[1]);
         }
-        const uint32_t pbuf = p_it & 1;
-        if (!mbar_wait(bar(Q_PEMPTY + pbuf), ((p_it >> 1) & 1) ^ 1, abort, status)) { ok = false; break; }
-        store_tile_row(sb + L::DS_OFF + pbuf * L::T_BYTES, r, dp);
-        fence_proxy_async_smem();
-        mbar_arrive(bar(Q_PFULL + pbuf));
-        ++p_it;
+        tmem_st32(p_tm, reinterpret_cast<const float*>(pk));
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(bar(Q_PFULL + sbuf));
+        ++s_it;
       }
       if (!ok) break;
       const int64_t orow = (q0 + i) * p.heads + h;
       if (n > 0) {
-        const uint32_t plast = p_it - 1;
-        if (!mbar_wait(bar(Q_PEMPTY + (plast & 1)), (plast >> 1) & 1, abort, status)) { ok = false; break; }
+        if (!mbar_wait(bar(Q_ACCFULL), a_it & 1, abort, status)) { ok = false; break; }
+        ++a_it;
         tc_fence_after();
         float x[32];
 #pragma unroll

@@ -1,9 +1,10 @@
 """The device-built jagged tile scheduler against a plain-Python statement of its rule.
 
 Rule: every (sequence b, head h, tile t) is one item; its cost is the number of inner
-steps the kernel runs for it; items are ordered by cost descending (costs of 127 and
-more share one bucket), ties by (b, t) ascending, with the H heads of one (b, t)
-adjacent.  The list is read back from the caller's workspace.
+steps the kernel runs for it.  Sequences are ordered by total cost, heaviest first (cost
+bucketed into 128 levels relative to the heaviest sequence, ties by b); the tiles of a
+sequence are contiguous, heaviest first; the H heads of a tile are adjacent.  The list is
+read back from the caller's workspace.
 """
 import numpy as np
 import pytest
@@ -21,24 +22,28 @@ def _align(x, a=256):
 
 
 def expected(lq, lk, H, tile, step, causal, key_major):
-    units = []
-    for b in range(len(lq)):
-        n_tiles = -(-(lk[b] if key_major else lq[b]) // tile)
-        for t in range(n_tiles):
-            if not key_major:
-                keys = min(lk[b], (t + 1) * tile) if causal else lk[b]
-                cost = -(-keys // step)
-            elif not causal:
-                cost = -(-lq[b] // step)
-            else:
-                cost = max(0, -(-lq[b] // step) - (t * tile) // step)
-            units.append((b, t, cost))
-    order = sorted(range(len(units)), key=lambda u: (-min(units[u][2], BUCKETS - 1), u))
+    """Sequences by total cost (bucketed relative to the heaviest), heaviest first, ties
+    by index; a sequence's tiles contiguous, heaviest first; heads of a tile adjacent."""
+    def cost(b, t):
+        if not key_major:
+            keys = min(lk[b], (t + 1) * tile) if causal else lk[b]
+            return -(-keys // step)
+        if not causal:
+            return -(-lq[b] // step)
+        return max(0, -(-lq[b] // step) - (t * tile) // step)
+
+    ntile = [-(-(lk[b] if key_major else lq[b]) // tile) for b in range(len(lq))]
+    total = [sum(cost(b, t) for t in range(ntile[b])) for b in range(len(lq))]
+    top = max(total) if total else 0
+    bucket = [total[b] * (BUCKETS - 1) // top if top > 0 else 0 for b in range(len(lq))]
+    order = sorted(range(len(lq)), key=lambda b: (-bucket[b], b))
     out = []
-    for u in order:
-        b, t, cost = units[u]
-        for h in range(H):
-            out.append((b, h, t, cost))
+    for b in order:
+        n = ntile[b]
+        for k in range(n):
+            t = n - 1 - k if (causal and not key_major) else k
+            for h in range(H):
+                out.append((b, h, t, cost(b, t)))
     return out
 
 
@@ -47,7 +52,7 @@ def read_lists(ws, B, Tq, Tk, H):
     raw = ws.cpu().numpy()
     hdr = raw[:256].view(np.int32)
     n_q, n_k = int(hdr[1]), int(hdr[2])
-    off = 256 + _align(16 * B) + 2 * _align(4 * (B + 1))
+    off = 256 + _align(16 * B) + _align(16 * (B + 1))
     max_q = H * (Tq // 32 + B + 1)
     lq_ = raw[off:off + 32 * n_q].view(np.int32).reshape(-1, 8)
     off2 = off + _align(32 * max_q)
