@@ -79,7 +79,7 @@ typedef struct {
   int32_t heads;   /* H >= 1 */
   int32_t dim_qk;  /* Dqk: bf16 supports 64 and 128; fp32 supports 1..128 */
   int32_t dim_v;   /* Dv:  bf16 supports 64 and 128; fp32 supports 1..128 */
-  float scale;     /* score scale, normally 1/sqrt(Dqk) */
+  float scale;     /* score scale > 0, normally 1/sqrt(Dqk) */
   int32_t causal;  /* 1: key j visible to query i only if j <= i (self-attention only) */
   int32_t dtype;   /* jfa_dtype of Q, K, V, O, dO, dQ, dK, dV */
 } jfa_params;

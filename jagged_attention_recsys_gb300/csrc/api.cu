@@ -122,8 +122,7 @@ jfa_status check_params(const jfa_params* p, Kind kind) {
   if (p->batch < 0 || p->total_q < 0 || p->total_k < 0 || p->heads < 1) return JFA_ERR_INVALID_ARG;
   if (p->dim_qk < 1 || p->dim_v < 1) return JFA_ERR_INVALID_ARG;
   if (p->dtype != JFA_F32 && p->dtype != JFA_BF16) return JFA_ERR_INVALID_ARG;
-  if (!(p->scale == p->scale) || p->scale == INFINITY || p->scale == -INFINITY)
-    return JFA_ERR_INVALID_ARG;
+  if (!(p->scale > 0.f) || p->scale == INFINITY) return JFA_ERR_INVALID_ARG;
   if (p->causal != 0 && p->causal != 1) return JFA_ERR_INVALID_ARG;
   if (p->batch == 0 && (p->total_q != 0 || p->total_k != 0)) return JFA_ERR_INVALID_ARG;
   if (p->total_q > INT32_MAX || p->total_k > INT32_MAX) return JFA_ERR_UNSUPPORTED;

@@ -95,24 +95,25 @@ __device__ __forceinline__ void store_row_bf16(__nv_bfloat16* dst, const float* 
 // there (A operand in TMEM).
 template <int DQK, int DV>
 struct KvLayout {
-  static constexpr int NQ = 4;                            // Q/dO ring stages
+  static constexpr int NKV = 2;                           // K/V tiles: current and next item
+  static constexpr int NQ = DQK + DV > 192 ? 3 : (DQK + DV > 128 ? 4 : 8);  // Q/dO ring stages
   static constexpr uint32_t K_BYTES = DQK / 64 * 16384;   // 128 keys
   static constexpr uint32_t V_BYTES = DV / 64 * 16384;
   static constexpr uint32_t Q_BYTES = DQK / 64 * 8192;    // 64 rows
   static constexpr uint32_t O_BYTES = DV / 64 * 8192;
-  static constexpr uint32_t K_OFF = 0;
-  static constexpr uint32_t V_OFF = K_OFF + K_BYTES;
-  static constexpr uint32_t Q_OFF = V_OFF + V_BYTES;       // NQ stages
+  static constexpr uint32_t K_OFF = 0;                     // NKV stages
+  static constexpr uint32_t V_OFF = K_OFF + NKV * K_BYTES; // NKV stages
+  static constexpr uint32_t Q_OFF = V_OFF + NKV * V_BYTES; // NQ stages
   static constexpr uint32_t O_OFF = Q_OFF + NQ * Q_BYTES;  // NQ stages (dO)
   static constexpr uint32_t RS_OFF = O_OFF + NQ * O_BYTES; // NQ stages x 64 float2
   static constexpr uint32_t BAR_OFF = RS_OFF + NQ * STEP * 8;
   // at least 120 KB so that exactly one CTA (which owns all of TMEM) fits per SM
-  static constexpr uint32_t SMEM = (BAR_OFF + 256 + 1024) > 122880u ? (BAR_OFF + 256 + 1024) : 122880u;
+  static constexpr uint32_t SMEM = (BAR_OFF + 512 + 1024) > 122880u ? (BAR_OFF + 512 + 1024) : 122880u;
 };
 
 enum : uint32_t {
-  KV_KVFULL = 0, KV_KVEMPTY = 1, KV_QFULL = 2, KV_RSFULL = 6, KV_QEMPTY = 10, KV_SFULL = 14,
-  KV_PFULL = 16, KV_ACCFULL = 18, KV_ACCEMPTY = 19, KV_COUNT = 20
+  KV_KVFULL = 0, KV_KVEMPTY = 2, KV_QFULL = 4, KV_RSFULL = 12, KV_QEMPTY = 20, KV_SFULL = 28,
+  KV_PFULL = 30, KV_ACCFULL = 32, KV_ACCEMPTY = 33, KV_COUNT = 34
 };
 
 template <int DQK, int DV, int ACT, bool CAUSAL>
@@ -136,8 +137,10 @@ tc_dkdv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
   const int n_items = hdr->n_k;
 
   if (threadIdx.x == 0) {
-    mbar_init(bar(KV_KVFULL), 1);
-    mbar_init(bar(KV_KVEMPTY), 1);
+    for (int s = 0; s < L::NKV; ++s) {
+      mbar_init(bar(KV_KVFULL + s), 1);
+      mbar_init(bar(KV_KVEMPTY + s), 1);
+    }
     for (int s = 0; s < NQ; ++s) {
       mbar_init(bar(KV_QFULL + s), 1);
       mbar_init(bar(KV_RSFULL + s), 32);
@@ -180,17 +183,18 @@ tc_dkdv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
       const int64_t q0 = w.q0, k0 = w.k0;
       const int Lq = w.lq;
       if (lane == 0) {
-        ok = mbar_wait(bar(KV_KVEMPTY), (kv_it & 1) ^ 1, abort, status);
+        const uint32_t ks = kv_it % L::NKV;
+        ok = mbar_wait(bar(KV_KVEMPTY + ks), ((kv_it / L::NKV) & 1) ^ 1, abort, status);
         if (ok) {
-          mbar_expect_tx(bar(KV_KVFULL), L::K_BYTES + L::V_BYTES);
+          mbar_expect_tx(bar(KV_KVFULL + ks), L::K_BYTES + L::V_BYTES);
 #pragma unroll
           for (int a = 0; a < DQK / 64; ++a)
-            tma_load_2d(sb + L::K_OFF + a * 16384, &tm_k, h * DQK + a * 64, (int32_t)(k0 + key0),
-                        bar(KV_KVFULL));
+            tma_load_2d(sb + L::K_OFF + ks * L::K_BYTES + a * 16384, &tm_k, h * DQK + a * 64,
+                        (int32_t)(k0 + key0), bar(KV_KVFULL + ks));
 #pragma unroll
           for (int a = 0; a < DV / 64; ++a)
-            tma_load_2d(sb + L::V_OFF + a * 16384, &tm_v, h * DV + a * 64, (int32_t)(k0 + key0),
-                        bar(KV_KVFULL));
+            tma_load_2d(sb + L::V_OFF + ks * L::V_BYTES + a * 16384, &tm_v, h * DV + a * 64,
+                        (int32_t)(k0 + key0), bar(KV_KVFULL + ks));
         }
       }
       ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
@@ -221,9 +225,13 @@ tc_dkdv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
             tma_load_2d(sb + L::O_OFF + st * L::O_BYTES + a * 8192, &tm_do, h * DV + a * 64,
                         (int32_t)(q0 + i0), bar(KV_QFULL + st));
         }
-        float2* rs = reinterpret_cast<float2*>(smem + L::RS_OFF + st * STEP * 8);
+        // stage layout: 64 x (-lse * log2 e), then 64 x (-D)
+        float* rs = reinterpret_cast<float*>(smem + L::RS_OFF + st * STEP * 8);
 #pragma unroll
-        for (int t = 0; t < 2; ++t) rs[lane + 32 * t] = rv[t];
+        for (int t = 0; t < 2; ++t) {
+          rs[lane + 32 * t] = -rv[t].x;
+          rs[STEP + lane + 32 * t] = -rv[t].y;
+        }
         mbar_arrive(bar(KV_RSFULL + st));
       }
     }
@@ -242,8 +250,11 @@ tc_dkdv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
         if (it + (int)gridDim.x < n_items) nxt = load_item(list, it + gridDim.x);
         const int n = w.cost;
         if (n == 0) continue;
-        if (!mbar_wait(bar(KV_KVFULL), kv_it & 1, abort, status)) break;
+        const uint32_t ks = kv_it % L::NKV;
+        if (!mbar_wait(bar(KV_KVFULL + ks), (kv_it / L::NKV) & 1, abort, status)) break;
         tc_fence_after();
+        const uint32_t k_tile = sb + L::K_OFF + ks * L::K_BYTES;
+        const uint32_t v_tile = sb + L::V_OFF + ks * L::V_BYTES;
         uint32_t prev_stage = 0;
         for (int j = 0; j <= n && ok; ++j) {
           uint32_t cur_stage = 0;
@@ -260,20 +271,20 @@ tc_dkdv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
             tc_fence_after();
 #pragma unroll
             for (int kk = 0; kk < DQK / 16; ++kk) {
-              const uint64_t ad = sw128_desc(sb + L::K_OFF + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024);
+              const uint64_t ad = sw128_desc(k_tile + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024);
               const uint64_t bd = sw128_desc(sb + L::Q_OFF + cur_stage * L::Q_BYTES + (kk >> 2) * 8192 +
                                                  (kk & 3) * 32, 16, 1024);
               mma_bf16(tmem + T_S + sbuf * STEP, ad, bd, idesc_s, kk > 0 ? 1u : 0u);
             }
 #pragma unroll
             for (int kk = 0; kk < DV / 16; ++kk) {
-              const uint64_t ad = sw128_desc(sb + L::V_OFF + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024);
+              const uint64_t ad = sw128_desc(v_tile + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024);
               const uint64_t bd = sw128_desc(sb + L::O_OFF + cur_stage * L::O_BYTES + (kk >> 2) * 8192 +
                                                  (kk & 3) * 32, 16, 1024);
               mma_bf16(tmem + T_DP + sbuf * STEP, ad, bd, idesc_s, kk > 0 ? 1u : 0u);
             }
             mma_commit(bar(KV_SFULL + sbuf));
-            if (j == n - 1) mma_commit(bar(KV_KVEMPTY));
+            if (j == n - 1) mma_commit(bar(KV_KVEMPTY + ks));
             ++s_it;
             ++q_it;
           }
@@ -315,6 +326,9 @@ tc_dkdv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
     const int r = 32 * (warp & 3) + lane;  // key of the tile = TMEM lane
     const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
     const float c_score = ACT == kActSoftmax ? p.scale * kLog2e : p.scale;
+    const float shift_raw = kMaskShift / c_score;  // masked raw scores land kMaskShift lower
+    const float2 hc = make_float2(0.5f * c_score, 0.5f * c_score);
+    const float2 one = make_float2(1.f, 1.f), half = make_float2(0.5f, 0.5f);
     uint32_t q_it = 0, s_it = 0, a_it = 0;
     bool ok = true;
     WorkItem nxt = blockIdx.x < (unsigned)n_items ? load_item(list, blockIdx.x) : WorkItem{};
@@ -327,6 +341,7 @@ tc_dkdv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
       const int Lq = w.lq, Lk = w.lk;
       const int j = key0 + r;  // key index inside the sequence
       const float inv_len = 1.0f / (float)max(Lq, 1);
+      const float2 il = make_float2(inv_len, inv_len);
       const int qs0 = CAUSAL ? key0 / STEP : 0;
       for (int step = 0; step < n; ++step, ++q_it) {
         const uint32_t sbuf = s_it & 1;
@@ -342,32 +357,40 @@ tc_dkdv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
         tmem_wait_ld();
         const uint32_t st = q_it % NQ;
         if (!mbar_wait(bar(KV_RSFULL + st), (q_it / NQ) & 1, abort, status)) { ok = false; break; }
-        const float2* rs = reinterpret_cast<const float2*>(smem + L::RS_OFF + st * STEP * 8);
+        const float* rs = reinterpret_cast<const float*>(smem + L::RS_OFF + st * STEP * 8);
         const int i0 = (qs0 + step) * STEP;
         // valid queries of this step for key j: i < Lq and (causal) i >= j
         const int lo = CAUSAL ? j - i0 : 0;
         const int hi = j < Lk ? Lq - i0 : 0;
+        if (lo > 0 || hi < STEP) {
+          // partial step: move masked raw scores down by a finite shift
+#pragma unroll
+          for (int c = 0; c < STEP; ++c) sv[c] -= (c >= lo && c < hi) ? 0.f : shift_raw;
+        }
+        const float2 cc = make_float2(c_score, c_score);
         uint32_t pk[STEP / 2], dk2[STEP / 2];
 #pragma unroll
         for (int c = 0; c < STEP; c += 2) {
-          float pv[2], ds[2];
-#pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const bool valid = c + e >= lo && c + e < hi;
-            if (ACT == kActSoftmax) {
-              const float2 ld = rs[c + e];
-              const float x = fmaf(sv[c + e], c_score, valid ? -ld.x : -ld.x - kMaskShift);
-              pv[e] = ex2(x);
-              ds[e] = pv[e] * (dp[c + e] - ld.y);
-            } else {
-              const float u = fmaf(sv[c + e], c_score, valid ? 0.f : -kMaskShift);
-              const float sg = sigmoid_fast(u);
-              pv[e] = u * sg * inv_len;
-              ds[e] = dp[c + e] * sg * fmaf(u, 1.f - sg, 1.f) * inv_len;
-            }
+          const float2 x = make_float2(sv[c], sv[c + 1]);
+          const float2 d = make_float2(dp[c], dp[c + 1]);
+          float2 pv, ds;
+          if (ACT == kActSoftmax) {
+            const float2 nl = *reinterpret_cast<const float2*>(rs + c);        // -lse log2 e
+            const float2 nd = *reinterpret_cast<const float2*>(rs + STEP + c); // -D
+            const float2 e = ffma2(x, cc, nl);
+            pv = make_float2(ex2(e.x), ex2(e.y));
+            ds = fmul2(pv, fadd2(d, nd));
+          } else {
+            // u = s c, h = u/2, t = tanh h: P = h (1+t)/L, dS = dP (1+t)/L (1 + h - h t)/2
+            const float2 hh = fmul2(x, hc);
+            const float2 t = make_float2(tanh_approx(hh.x), tanh_approx(hh.y));
+            const float2 g = ffma2(t, il, il);
+            pv = fmul2(hh, g);
+            const float2 b = ffma2(make_float2(-hh.x, -hh.y), t, fadd2(hh, one));
+            ds = fmul2(fmul2(d, g), fmul2(b, half));
           }
-          pk[c / 2] = pack_bf16(pv[0], pv[1]);
-          dk2[c / 2] = pack_bf16(ds[0], ds[1]);
+          pk[c / 2] = pack_bf16(pv.x, pv.y);
+          dk2[c / 2] = pack_bf16(ds.x, ds.y);
         }
         tmem_st32(s_tm, reinterpret_cast<const float*>(pk));
         tmem_st32(p_tm, reinterpret_cast<const float*>(dk2));
@@ -425,22 +448,25 @@ tc_dkdv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
 // reads it from there.
 template <int DQK, int DV>
 struct QLayout {
-  static constexpr int NK = 4;                             // K/V ring stages
+  // Q/dO of the next item are prefetched where shared memory allows; the K/V
+  // ring depth matters more and is kept at 4 or more.
+  static constexpr int NQO = DQK + DV > 192 ? 1 : 2;       // Q/dO tiles
+  static constexpr int NK = DQK + DV > 128 ? 4 : 6;        // K/V ring stages
   static constexpr uint32_t Q_BYTES = DQK / 64 * 16384;   // 128 rows
   static constexpr uint32_t O_BYTES = DV / 64 * 16384;
   static constexpr uint32_t K_BYTES = DQK / 64 * 8192;    // 64 keys
   static constexpr uint32_t V_BYTES = DV / 64 * 8192;
-  static constexpr uint32_t Q_OFF = 0;
-  static constexpr uint32_t O_OFF = Q_OFF + Q_BYTES;
-  static constexpr uint32_t K_OFF = O_OFF + O_BYTES;       // NK stages
+  static constexpr uint32_t Q_OFF = 0;                     // NQO stages
+  static constexpr uint32_t O_OFF = Q_OFF + NQO * Q_BYTES; // NQO stages
+  static constexpr uint32_t K_OFF = O_OFF + NQO * O_BYTES; // NK stages
   static constexpr uint32_t V_OFF = K_OFF + NK * K_BYTES;  // NK stages
   static constexpr uint32_t BAR_OFF = V_OFF + NK * V_BYTES;
-  static constexpr uint32_t SMEM = (BAR_OFF + 256 + 1024) > 122880u ? (BAR_OFF + 256 + 1024) : 122880u;
+  static constexpr uint32_t SMEM = (BAR_OFF + 512 + 1024) > 122880u ? (BAR_OFF + 512 + 1024) : 122880u;
 };
 
 enum : uint32_t {
-  Q_QFULL = 0, Q_QEMPTY = 1, Q_KFULL = 2, Q_KEMPTY = 6, Q_SFULL = 10, Q_PFULL = 12,
-  Q_ACCFULL = 14, Q_ACCEMPTY = 15, Q_COUNT = 16
+  Q_QFULL = 0, Q_QEMPTY = 2, Q_KFULL = 4, Q_KEMPTY = 10, Q_SFULL = 16, Q_PFULL = 18,
+  Q_ACCFULL = 20, Q_ACCEMPTY = 21, Q_COUNT = 22
 };
 
 template <int DQK, int DV, int ACT, bool CAUSAL>
@@ -463,8 +489,10 @@ tc_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
   const int n_items = hdr->n_q;
 
   if (threadIdx.x == 0) {
-    mbar_init(bar(Q_QFULL), 1);
-    mbar_init(bar(Q_QEMPTY), 1);
+    for (int s = 0; s < L::NQO; ++s) {
+      mbar_init(bar(Q_QFULL + s), 1);
+      mbar_init(bar(Q_QEMPTY + s), 1);
+    }
     for (int s = 0; s < NK; ++s) {
       mbar_init(bar(Q_KFULL + s), 1);
       mbar_init(bar(Q_KEMPTY + s), 1);
@@ -502,14 +530,17 @@ tc_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
         if (n == 0) continue;
         const int h = w.h, row0 = w.tile * TILE;
         const int32_t q0 = w.q0, k0 = w.k0;
-        if (!mbar_wait(bar(Q_QEMPTY), (q_it & 1) ^ 1, abort, status)) break;
-        mbar_expect_tx(bar(Q_QFULL), L::Q_BYTES + L::O_BYTES);
+        const uint32_t qs = q_it % L::NQO;
+        if (!mbar_wait(bar(Q_QEMPTY + qs), ((q_it / L::NQO) & 1) ^ 1, abort, status)) break;
+        mbar_expect_tx(bar(Q_QFULL + qs), L::Q_BYTES + L::O_BYTES);
 #pragma unroll
         for (int a = 0; a < DQK / 64; ++a)
-          tma_load_2d(sb + L::Q_OFF + a * 16384, &tm_q, h * DQK + a * 64, q0 + row0, bar(Q_QFULL));
+          tma_load_2d(sb + L::Q_OFF + qs * L::Q_BYTES + a * 16384, &tm_q, h * DQK + a * 64, q0 + row0,
+                      bar(Q_QFULL + qs));
 #pragma unroll
         for (int a = 0; a < DV / 64; ++a)
-          tma_load_2d(sb + L::O_OFF + a * 16384, &tm_do, h * DV + a * 64, q0 + row0, bar(Q_QFULL));
+          tma_load_2d(sb + L::O_OFF + qs * L::O_BYTES + a * 16384, &tm_do, h * DV + a * 64, q0 + row0,
+                      bar(Q_QFULL + qs));
         ++q_it;
         for (int j = 0; j < n; ++j, ++k_it) {
           const uint32_t st = k_it % NK, ph = (k_it / NK) & 1;
@@ -539,8 +570,11 @@ tc_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
         if (it + (int)gridDim.x < n_items) nxt = load_item(list, it + gridDim.x);
         const int n = w.cost;
         if (n == 0) continue;
-        if (!mbar_wait(bar(Q_QFULL), q_it & 1, abort, status)) break;
+        const uint32_t qs = q_it % L::NQO;
+        if (!mbar_wait(bar(Q_QFULL + qs), (q_it / L::NQO) & 1, abort, status)) break;
         tc_fence_after();
+        const uint32_t q_tile = sb + L::Q_OFF + qs * L::Q_BYTES;
+        const uint32_t o_tile = sb + L::O_OFF + qs * L::O_BYTES;
         uint32_t prev_stage = 0;
         for (int j = 0; j <= n && ok; ++j) {
           uint32_t cur_stage = 0;
@@ -554,20 +588,20 @@ tc_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
             tc_fence_after();
 #pragma unroll
             for (int kk = 0; kk < DQK / 16; ++kk) {
-              const uint64_t ad = sw128_desc(sb + L::Q_OFF + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024);
+              const uint64_t ad = sw128_desc(q_tile + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024);
               const uint64_t bd = sw128_desc(sb + L::K_OFF + cur_stage * L::K_BYTES + (kk >> 2) * 8192 +
                                                  (kk & 3) * 32, 16, 1024);
               mma_bf16(tmem + T_S + sbuf * STEP, ad, bd, idesc_s, kk > 0 ? 1u : 0u);
             }
 #pragma unroll
             for (int kk = 0; kk < DV / 16; ++kk) {
-              const uint64_t ad = sw128_desc(sb + L::O_OFF + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024);
+              const uint64_t ad = sw128_desc(o_tile + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024);
               const uint64_t bd = sw128_desc(sb + L::V_OFF + cur_stage * L::V_BYTES + (kk >> 2) * 8192 +
                                                  (kk & 3) * 32, 16, 1024);
               mma_bf16(tmem + T_DP + sbuf * STEP, ad, bd, idesc_s, kk > 0 ? 1u : 0u);
             }
             mma_commit(bar(Q_SFULL + sbuf));
-            if (j == n - 1) mma_commit(bar(Q_QEMPTY));
+            if (j == n - 1) mma_commit(bar(Q_QEMPTY + qs));
             ++s_it;
             ++k_it;
           }
@@ -601,6 +635,10 @@ tc_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
     const int r = 32 * (warp & 3) + lane;  // query row of the tile = TMEM lane
     const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
     const float c_score = ACT == kActSoftmax ? p.scale * kLog2e : p.scale;
+    const float shift_raw = kMaskShift / c_score;  // masked raw scores land kMaskShift lower
+    const float2 cc = make_float2(c_score, c_score);
+    const float2 hc = make_float2(0.5f * c_score, 0.5f * c_score);
+    const float2 one = make_float2(1.f, 1.f), half = make_float2(0.5f, 0.5f);
     uint32_t s_it = 0, a_it = 0;
     bool ok = true;
     WorkItem nxt = blockIdx.x < (unsigned)n_items ? load_item(list, blockIdx.x) : WorkItem{};
@@ -616,6 +654,8 @@ tc_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
       const float inv_len = 1.0f / (float)max(Lq, 1);
       float2 rsv = make_float2(0.f, 0.f);
       if (ACT == kActSoftmax && row_ok && n > 0) rsv = rowstat[(int64_t)h * p.total_q + q0 + i];
+      const float2 nl = make_float2(-rsv.x, -rsv.x), nd = make_float2(-rsv.y, -rsv.y);
+      const float2 il = make_float2(inv_len, inv_len);
       for (int step = 0; step < n; ++step) {
         const uint32_t sbuf = s_it & 1;
         if (!mbar_wait(bar(Q_SFULL + sbuf), (s_it >> 1) & 1, abort, status)) { ok = false; break; }
@@ -632,23 +672,28 @@ tc_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
         int nvalid = Lk - kb;
         if (CAUSAL) nvalid = min(nvalid, i - kb + 1);
         if (!row_ok) nvalid = 0;
+        if (nvalid < STEP) {
+          // partial step: move masked raw scores down by a finite shift
+#pragma unroll
+          for (int c = 0; c < STEP; ++c) sv[c] -= c < nvalid ? 0.f : shift_raw;
+        }
         uint32_t pk[STEP / 2];
 #pragma unroll
         for (int c = 0; c < STEP; c += 2) {
-          float ds[2];
-#pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const bool valid = c + e < nvalid;
-            if (ACT == kActSoftmax) {
-              const float x = fmaf(sv[c + e], c_score, valid ? -rsv.x : -rsv.x - kMaskShift);
-              ds[e] = ex2(x) * (dp[c + e] - rsv.y);
-            } else {
-              const float u = fmaf(sv[c + e], c_score, valid ? 0.f : -kMaskShift);
-              const float sg = sigmoid_fast(u);
-              ds[e] = dp[c + e] * sg * fmaf(u, 1.f - sg, 1.f) * inv_len;
-            }
+          const float2 x = make_float2(sv[c], sv[c + 1]);
+          const float2 d = make_float2(dp[c], dp[c + 1]);
+          float2 ds;
+          if (ACT == kActSoftmax) {
+            const float2 e = ffma2(x, cc, nl);
+            ds = fmul2(make_float2(ex2(e.x), ex2(e.y)), fadd2(d, nd));
+          } else {
+            const float2 hh = fmul2(x, hc);
+            const float2 t = make_float2(tanh_approx(hh.x), tanh_approx(hh.y));
+            const float2 g = ffma2(t, il, il);
+            const float2 b = ffma2(make_float2(-hh.x, -hh.y), t, fadd2(hh, one));
+            ds = fmul2(fmul2(d, g), fmul2(b, half));
           }
-          pk[c / 2] = pack_bf16(ds[0], ds[1]);
+          pk[c / 2] = pack_bf16(ds.x, ds.y);
         }
         tmem_st32(p_tm, reinterpret_cast<const float*>(pk));
         tmem_wait_st();

@@ -52,22 +52,24 @@ constexpr float kRescaleLog2 = 8.0f;
 
 template <int DQK, int DV>
 struct FwdLayout {
-  static constexpr int NS = DQK + DV <= 128 ? 4 : (DQK + DV <= 192 ? 3 : 2);  // K/V ring stages
+  // K tiles are consumed one step before V tiles, so they get the deeper ring.
+  static constexpr int NK = DQK == 64 ? 4 : 3;
+  static constexpr int NV = DV == 64 ? 4 : (DQK == 64 ? 3 : 2);
   static constexpr uint32_t Q_BYTES = DQK / 64 * 16384;  // one 128-row tile
   static constexpr uint32_t K_BYTES = DQK / 64 * 16384;
   static constexpr uint32_t V_BYTES = DV / 64 * 16384;
   static constexpr uint32_t Q_OFF = 0;                    // 2 slots
-  static constexpr uint32_t K_OFF = Q_OFF + 2 * Q_BYTES;  // NS stages
-  static constexpr uint32_t V_OFF = K_OFF + NS * K_BYTES; // NS stages
-  static constexpr uint32_t BAR_OFF = V_OFF + NS * V_BYTES;
+  static constexpr uint32_t K_OFF = Q_OFF + 2 * Q_BYTES;  // NK stages
+  static constexpr uint32_t V_OFF = K_OFF + NK * K_BYTES; // NV stages
+  static constexpr uint32_t BAR_OFF = V_OFF + NV * V_BYTES;
   // at least 120 KB so that exactly one CTA (which owns all of TMEM) fits per SM
-  static constexpr uint32_t SMEM = (BAR_OFF + 256 + 1024) > 122880u ? (BAR_OFF + 256 + 1024) : 122880u;
+  static constexpr uint32_t SMEM = (BAR_OFF + 512 + 1024) > 122880u ? (BAR_OFF + 512 + 1024) : 122880u;
 };
 
-// mbarrier slots (K_FULL, V_FULL, KV_EMPTY have up to 4 stages)
+// mbarrier slots (the K and V rings have up to 4 stages each)
 enum : uint32_t {
-  B_QFULL = 0, B_QEMPTY = 1, B_KFULL = 2, B_VFULL = 6, B_KVEMPTY = 10, B_SFULL = 14,
-  B_PFULL = 16, B_OFULL = 18, B_OEMPTY = 20, B_COUNT = 22
+  B_QFULL = 0, B_QEMPTY = 1, B_KFULL = 2, B_KEMPTY = 6, B_VFULL = 10, B_VEMPTY = 14,
+  B_SFULL = 18, B_PFULL = 20, B_OFULL = 22, B_OEMPTY = 24, B_COUNT = 26
 };
 
 template <int DQK, int DV, int ACT, bool CAUSAL>
@@ -77,7 +79,7 @@ tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
               __nv_bfloat16* __restrict__ out, float* __restrict__ lse, WsHeader* hdr,
               const WorkItem* __restrict__ list) {
   using L = FwdLayout<DQK, DV>;
-  constexpr int NS = L::NS;
+  constexpr int NK = L::NK, NV = L::NV;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   const uint32_t sb = smem_u32(smem);
@@ -92,10 +94,13 @@ tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
   if (threadIdx.x == 0) {
     mbar_init(bar(B_QFULL), 1);
     mbar_init(bar(B_QEMPTY), 1);
-    for (int s = 0; s < NS; ++s) {
+    for (int s = 0; s < NK; ++s) {
       mbar_init(bar(B_KFULL + s), 1);
+      mbar_init(bar(B_KEMPTY + s), 1);
+    }
+    for (int s = 0; s < NV; ++s) {
       mbar_init(bar(B_VFULL + s), 1);
-      mbar_init(bar(B_KVEMPTY + s), 1);
+      mbar_init(bar(B_VEMPTY + s), 1);
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(bar(B_SFULL + s), 1);
@@ -118,7 +123,7 @@ tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
       tma_prefetch_desc(&tm_q);
       tma_prefetch_desc(&tm_k);
       tma_prefetch_desc(&tm_v);
-      uint32_t kv_it = 0, q_it = 0;
+      uint32_t k_it = 0, v_it = 0, q_it = 0;
       bool ok = true;
       WorkItem nxt = blockIdx.x < (unsigned)n_items ? load_item(list, blockIdx.x) : WorkItem{};
       for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
@@ -137,19 +142,28 @@ tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                         w.q0 + row0 + s * BM, bar(B_QFULL));
         }
         ++q_it;
-        for (int j = 0; j < n; ++j, ++kv_it) {
-          const uint32_t st = kv_it % NS, ph = (kv_it / NS) & 1;
-          if (!mbar_wait(bar(B_KVEMPTY + st), ph ^ 1, abort, status)) { ok = false; break; }
-          mbar_expect_tx(bar(B_KFULL + st), L::K_BYTES);
+        // K(j) is needed one step before V(j): issue K(j), then V(j-1)
+        for (int j = 0; j <= n && ok; ++j) {
+          if (j < n) {
+            const uint32_t st = k_it % NK;
+            if (!mbar_wait(bar(B_KEMPTY + st), ((k_it / NK) & 1) ^ 1, abort, status)) { ok = false; break; }
+            mbar_expect_tx(bar(B_KFULL + st), L::K_BYTES);
 #pragma unroll
-          for (int a = 0; a < DQK / 64; ++a)
-            tma_load_2d(sb + L::K_OFF + st * L::K_BYTES + a * 16384, &tm_k, h * DQK + a * 64,
-                        w.k0 + j * BN, bar(B_KFULL + st));
-          mbar_expect_tx(bar(B_VFULL + st), L::V_BYTES);
+            for (int a = 0; a < DQK / 64; ++a)
+              tma_load_2d(sb + L::K_OFF + st * L::K_BYTES + a * 16384, &tm_k, h * DQK + a * 64,
+                          w.k0 + j * BN, bar(B_KFULL + st));
+            ++k_it;
+          }
+          if (j > 0) {
+            const uint32_t st = v_it % NV;
+            if (!mbar_wait(bar(B_VEMPTY + st), ((v_it / NV) & 1) ^ 1, abort, status)) { ok = false; break; }
+            mbar_expect_tx(bar(B_VFULL + st), L::V_BYTES);
 #pragma unroll
-          for (int a = 0; a < DV / 64; ++a)
-            tma_load_2d(sb + L::V_OFF + st * L::V_BYTES + a * 16384, &tm_v, h * DV + a * 64,
-                        w.k0 + j * BN, bar(B_VFULL + st));
+            for (int a = 0; a < DV / 64; ++a)
+              tma_load_2d(sb + L::V_OFF + st * L::V_BYTES + a * 16384, &tm_v, h * DV + a * 64,
+                          w.k0 + (j - 1) * BN, bar(B_VFULL + st));
+            ++v_it;
+          }
         }
       }
     }
@@ -159,7 +173,7 @@ tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     if (lane == 0) {
       constexpr uint32_t idesc_s = idesc_bf16(BM, BN, 0, 0);
       constexpr uint32_t idesc_o = idesc_bf16(BM, DV, 0, 1);
-      uint32_t kv_it = 0, q_it = 0;
+      uint32_t k_it = 0, v_it = 0, q_it = 0;
       uint32_t s_cnt[2] = {0, 0}, o_cnt[2] = {0, 0};
       bool ok = true;
       WorkItem nxt = blockIdx.x < (unsigned)n_items ? load_item(list, blockIdx.x) : WorkItem{};
@@ -176,16 +190,15 @@ tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         ns[1] = two ? n : 0;
         if (!mbar_wait(bar(B_QFULL), q_it & 1, abort, status)) break;
         tc_fence_after();
-        uint32_t prev_st = 0;
         for (int j = 0; j <= n && ok; ++j) {
-          const uint32_t st = kv_it % NS;
+          const uint32_t kst = k_it % NK, vst = v_it % NV;
           if (j < n) {
-            if (!mbar_wait(bar(B_KFULL + st), (kv_it / NS) & 1, abort, status)) { ok = false; break; }
+            if (!mbar_wait(bar(B_KFULL + kst), (k_it / NK) & 1, abort, status)) { ok = false; break; }
             tc_fence_after();
           }
-          if (j > 0 && !mbar_wait(bar(B_VFULL + prev_st), ((kv_it - 1) / NS) & 1, abort, status)) {
-            ok = false;
-            break;
+          if (j > 0) {
+            if (!mbar_wait(bar(B_VFULL + vst), (v_it / NV) & 1, abort, status)) { ok = false; break; }
+            tc_fence_after();
           }
 #pragma unroll
           for (int s = 0; s < 2; ++s) {
@@ -200,7 +213,7 @@ tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
               tc_fence_after();
 #pragma unroll
               for (int kk = 0; kk < BN / 16; ++kk) {
-                const uint64_t bd = sw128_desc(sb + L::V_OFF + prev_st * L::V_BYTES + kk * 2048, 16384, 1024);
+                const uint64_t bd = sw128_desc(sb + L::V_OFF + vst * L::V_BYTES + kk * 2048, 16384, 1024);
                 mma_bf16_tmem_a(s_tm + 128, s_tm + kk * 8, bd, idesc_o, (j > 1 || kk > 0) ? 1u : 0u);
               }
               if (j == ns[s]) {
@@ -214,7 +227,7 @@ tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
               for (int kk = 0; kk < DQK / 16; ++kk) {
                 const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
                 const uint64_t ad = sw128_desc(sb + L::Q_OFF + s * L::Q_BYTES + off, 16, 1024);
-                const uint64_t bd = sw128_desc(sb + L::K_OFF + st * L::K_BYTES + off, 16, 1024);
+                const uint64_t bd = sw128_desc(sb + L::K_OFF + kst * L::K_BYTES + off, 16, 1024);
                 mma_bf16(s_tm, ad, bd, idesc_s, kk > 0 ? 1u : 0u);
               }
               mma_commit(bar(B_SFULL + s));
@@ -222,11 +235,14 @@ tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             }
           }
           if (!ok) break;
-          if (j == n - 1) mma_commit(bar(B_QEMPTY));
-          if (j > 0) mma_commit(bar(B_KVEMPTY + prev_st));
           if (j < n) {
-            prev_st = st;
-            ++kv_it;
+            mma_commit(bar(B_KEMPTY + kst));  // both slots' S(j) issued
+            if (j == n - 1) mma_commit(bar(B_QEMPTY));
+            ++k_it;
+          }
+          if (j > 0) {
+            mma_commit(bar(B_VEMPTY + vst));  // both slots' PV(j-1) issued
+            ++v_it;
           }
         }
         ++q_it;
@@ -240,6 +256,7 @@ tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
     const uint32_t s_tm = tmem + slot * 256 + lane_base;
     const float c_score = ACT == kActSoftmax ? p.scale * kLog2e : p.scale;
+    const float shift_raw = kMaskShift / c_score;  // masked raw scores land kMaskShift lower
     uint32_t s_cnt = 0, o_cnt = 0;
     bool ok = true;
     WorkItem nxt = blockIdx.x < (unsigned)n_items ? load_item(list, blockIdx.x) : WorkItem{};
@@ -267,18 +284,21 @@ tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         if (CAUSAL) nvalid = min(nvalid, i - kb + 1);
         float alpha = 1.f;  // rescale factor of O for this step (softmax only)
         bool rescale = false;
+        if (nvalid < BN) {
+          // partial tile: move masked raw scores down by a finite shift (in raw units,
+          // so that after scaling the shift is kMaskShift)
+#pragma unroll
+          for (int k = 0; k < BN; ++k) sv[k] -= k < nvalid ? 0.f : shift_raw;
+        }
         if (ACT == kActSoftmax) {
-          float mt = -INFINITY;
-          if (nvalid >= BN) {
+          // row max of the raw scores (scale > 0), two independent 3-input chains
+          float m0 = fmaxf(sv[0], sv[1]), m1 = fmaxf(sv[2], sv[3]);
 #pragma unroll
-            for (int k = 0; k < BN; ++k) { sv[k] *= c_score; mt = fmaxf(mt, sv[k]); }
-          } else {
-#pragma unroll
-            for (int k = 0; k < BN; ++k) {
-              sv[k] = fmaf(sv[k], c_score, k < nvalid ? 0.f : -kMaskShift);
-              mt = fmaxf(mt, sv[k]);
-            }
+          for (int k = 4; k < BN; k += 4) {  // BN is a multiple of 4: last group is BN-4..BN-1
+            m0 = fmax3(m0, sv[k], sv[k + 1]);
+            m1 = fmax3(m1, sv[k + 2], sv[k + 3]);
           }
+          const float mt = fmaxf(m0, m1) * c_score;
           if (j == 0) {
             m = mt;
           } else {
@@ -292,31 +312,38 @@ tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
           }
           l *= alpha;
         }
-        // P = exp2(s - m) (or SiLU(u)/L), packed bf16 pairs over the first 64 S columns,
-        // written 64 values at a time so the fp32 scores die as they are consumed.
-        float rs = 0.f;
+        // P = exp2(s c - m) or SiLU(s c)/L, packed bf16 pairs over the first 64 S
+        // columns, written 64 values at a time so the fp32 scores die as they go.
+        const float2 cc = make_float2(c_score, c_score);
+        const float2 nm = make_float2(-m, -m);
+        const float2 hc = make_float2(0.5f * c_score, 0.5f * c_score);
+        const float2 il = make_float2(inv_len, inv_len);
+        float2 rs0 = make_float2(0.f, 0.f), rs1 = make_float2(0.f, 0.f);
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
           uint32_t pk[32];
 #pragma unroll
           for (int c = 0; c < 32; ++c) {
-            float x0 = sv[half * 64 + 2 * c], x1 = sv[half * 64 + 2 * c + 1];
+            const float2 x = make_float2(sv[half * 64 + 2 * c], sv[half * 64 + 2 * c + 1]);
+            float2 pv;
             if (ACT == kActSoftmax) {
-              x0 = ex2(x0 - m);
-              x1 = ex2(x1 - m);
-              rs += x0 + x1;
+              const float2 e = ffma2(x, cc, nm);
+              pv = make_float2(ex2(e.x), ex2(e.y));
+              if (c & 1) rs1 = fadd2(rs1, pv); else rs0 = fadd2(rs0, pv);
             } else {
-              const int k0i = half * 64 + 2 * c;
-              const float u0 = fmaf(x0, c_score, k0i < nvalid ? 0.f : -kMaskShift);
-              const float u1 = fmaf(x1, c_score, k0i + 1 < nvalid ? 0.f : -kMaskShift);
-              x0 = u0 * sigmoid_fast(u0) * inv_len;
-              x1 = u1 * sigmoid_fast(u1) * inv_len;
+              // SiLU(u)/L with u = s c: h = u/2, P = h (1 + tanh h) / L
+              const float2 hh = fmul2(x, hc);
+              const float2 t = make_float2(tanh_approx(hh.x), tanh_approx(hh.y));
+              pv = fmul2(hh, ffma2(t, il, il));
             }
-            pk[c] = pack_bf16(x0, x1);
+            pk[c] = pack_bf16(pv.x, pv.y);
           }
           tmem_st32(s_tm + 32 * half, reinterpret_cast<const float*>(pk));
         }
-        if (ACT == kActSoftmax) l += rs;
+        if (ACT == kActSoftmax) {
+          const float2 r = fadd2(rs0, rs1);
+          l += r.x + r.y;
+        }
         if (rescale) {
           // O_s already holds every PV issued before this S (in-order MMAs).
           float ov[32];

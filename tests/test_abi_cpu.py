@@ -77,6 +77,8 @@ def test_invalid_arguments_rejected_on_host(L):
     assert _call_fwd(L, P(dim_qk=200)) == jfa.JFA_ERR_UNSUPPORTED
     assert _call_fwd(L, P(causal=2)) == jfa.JFA_ERR_INVALID_ARG
     assert _call_fwd(L, P(scale=float("nan"))) == jfa.JFA_ERR_INVALID_ARG
+    assert _call_fwd(L, P(scale=0.0)) == jfa.JFA_ERR_INVALID_ARG
+    assert _call_fwd(L, P(scale=-0.1)) == jfa.JFA_ERR_INVALID_ARG
     assert _call_fwd(L, P(batch=0)) == jfa.JFA_ERR_INVALID_ARG  # totals must be 0 too
     assert _call_fwd(L, P(), ptr=8) == jfa.JFA_ERR_INVALID_ARG  # not 16-byte aligned
     assert _call_fwd(L, P(), ptr=0) == jfa.JFA_ERR_INVALID_ARG  # null
