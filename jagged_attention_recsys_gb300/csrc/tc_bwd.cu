@@ -33,9 +33,9 @@ namespace jfa {
 namespace {
 using namespace tc;
 
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;  // producer warp, MMA warp, two compute warpgroups
 constexpr int TILE = 128;  // keys per dK/dV item, rows per dQ item (MMA M)
-constexpr int STEP = 64;   // query rows per dK/dV step, keys per dQ step (MMA N)
+constexpr int STEP = 128;  // query rows per dK/dV step, keys per dQ step (MMA N)
 constexpr float kLog2e = 1.4426950408889634f;
 
 // ------------------------------------------------------------------ row pass
@@ -88,33 +88,43 @@ __device__ __forceinline__ void store_row_bf16(__nv_bfloat16* dst, const float* 
 // =============================================================================
 // dK / dV pass
 // =============================================================================
-// Q/dO steps are staged in an NQ-deep ring so the loads of later query steps
-// are in flight while the current ones are computed.  P^T and dS^T are written
-// back into TMEM as packed bf16 over the first 32 columns of the S^T and dP^T
-// buffers they were computed from, and the dV / dK products read them from
-// there (A operand in TMEM).
+// One item = (sequence, head, 128-key tile); the inner loop steps over 128
+// query rows (all MMAs are 128 x 128 or 128 x D).  Per step the MMA lane
+// issues S^T = K Q^T (commit S_FULL) and dP^T = V dO^T (commit DP_FULL).  The
+// two compute warpgroups (64 query columns each) turn S^T into P^T while dP^T
+// is being computed and store it as packed bf16 over their own S^T columns
+// (P_FULL); the MMA lane then issues dV += P^T dO while the warpgroups form
+// dS^T = P^T (dP^T - D) into their own dP^T columns (DS_FULL), and finally
+// dK += dS^T Q.  MMAs of one thread execute in order, so the next step's S^T
+// and dP^T are ordered after the products that read this step's P^T / dS^T.
 template <int DQK, int DV>
 struct KvLayout {
-  static constexpr int NKV = 2;                           // K/V tiles: current and next item
-  static constexpr int NQ = DQK + DV > 192 ? 3 : (DQK + DV > 128 ? 4 : 8);  // Q/dO ring stages
+  static constexpr int NKV = DQK + DV == 128 ? 2 : 1;                     // K/V tiles
+  static constexpr int NQ = DQK + DV == 256 ? 2 : (DQK + DV == 192 ? 3 : 4);  // Q/dO stages
   static constexpr uint32_t K_BYTES = DQK / 64 * 16384;   // 128 keys
   static constexpr uint32_t V_BYTES = DV / 64 * 16384;
-  static constexpr uint32_t Q_BYTES = DQK / 64 * 8192;    // 64 rows
-  static constexpr uint32_t O_BYTES = DV / 64 * 8192;
-  static constexpr uint32_t K_OFF = 0;                     // NKV stages
-  static constexpr uint32_t V_OFF = K_OFF + NKV * K_BYTES; // NKV stages
-  static constexpr uint32_t Q_OFF = V_OFF + NKV * V_BYTES; // NQ stages
-  static constexpr uint32_t O_OFF = Q_OFF + NQ * Q_BYTES;  // NQ stages (dO)
-  static constexpr uint32_t RS_OFF = O_OFF + NQ * O_BYTES; // NQ stages x 64 float2
-  static constexpr uint32_t BAR_OFF = RS_OFF + NQ * STEP * 8;
+  static constexpr uint32_t Q_BYTES = DQK / 64 * 16384;   // 128 rows
+  static constexpr uint32_t O_BYTES = DV / 64 * 16384;
+  static constexpr uint32_t RS_BYTES = 2 * STEP * 4;      // -lse log2 e and -D of 128 rows
+  static constexpr uint32_t K_OFF = 0;
+  static constexpr uint32_t V_OFF = K_OFF + NKV * K_BYTES;
+  static constexpr uint32_t Q_OFF = V_OFF + NKV * V_BYTES;
+  static constexpr uint32_t O_OFF = Q_OFF + NQ * Q_BYTES;
+  static constexpr uint32_t RS_OFF = O_OFF + NQ * O_BYTES;
+  static constexpr uint32_t BAR_OFF = RS_OFF + NQ * RS_BYTES;
   // at least 120 KB so that exactly one CTA (which owns all of TMEM) fits per SM
   static constexpr uint32_t SMEM = (BAR_OFF + 512 + 1024) > 122880u ? (BAR_OFF + 512 + 1024) : 122880u;
 };
 
 enum : uint32_t {
-  KV_KVFULL = 0, KV_KVEMPTY = 2, KV_QFULL = 4, KV_RSFULL = 12, KV_QEMPTY = 20, KV_SFULL = 28,
-  KV_PFULL = 30, KV_ACCFULL = 32, KV_ACCEMPTY = 33, KV_COUNT = 34
+  KV_KVFULL = 0, KV_KVEMPTY = 2, KV_QFULL = 4, KV_RSFULL = 8, KV_QEMPTY = 12, KV_SFULL = 16,
+  KV_DPFULL = 17, KV_PFULL = 18, KV_DSFULL = 19, KV_ACCFULL = 20, KV_ACCEMPTY = 21, KV_COUNT = 22
 };
+
+// bf16 pair (low, high) of a packed word to two floats, exactly
+__device__ __forceinline__ float2 unpack_bf16(uint32_t u) {
+  return make_float2(__uint_as_float(u << 16), __uint_as_float(u & 0xffff0000u));
+}
 
 template <int DQK, int DV, int ACT, bool CAUSAL>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -124,7 +134,7 @@ tc_dkdv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
                __nv_bfloat16* __restrict__ dk, __nv_bfloat16* __restrict__ dv, WsHeader* hdr,
                const WorkItem* __restrict__ list) {
   using L = KvLayout<DQK, DV>;
-  constexpr int NQ = L::NQ;
+  constexpr int NQ = L::NQ, NKV = L::NKV;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   const uint32_t sb = smem_u32(smem);
@@ -137,7 +147,7 @@ tc_dkdv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
   const int n_items = hdr->n_k;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < L::NKV; ++s) {
+    for (int s = 0; s < NKV; ++s) {
       mbar_init(bar(KV_KVFULL + s), 1);
       mbar_init(bar(KV_KVEMPTY + s), 1);
     }
@@ -146,12 +156,12 @@ tc_dkdv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
       mbar_init(bar(KV_RSFULL + s), 32);
       mbar_init(bar(KV_QEMPTY + s), 1);
     }
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(bar(KV_SFULL + s), 1);
-      mbar_init(bar(KV_PFULL + s), 128);
-    }
+    mbar_init(bar(KV_SFULL), 1);
+    mbar_init(bar(KV_DPFULL), 1);
+    mbar_init(bar(KV_PFULL), 256);
+    mbar_init(bar(KV_DSFULL), 256);
     mbar_init(bar(KV_ACCFULL), 1);
-    mbar_init(bar(KV_ACCEMPTY), 128);
+    mbar_init(bar(KV_ACCEMPTY), 256);
     *abort = 0;
     fence_mbar_init();
   }
@@ -160,7 +170,7 @@ tc_dkdv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  // TMEM columns: dK [0,128), dV [128,256), S^T/P^T [256 + 64 b), dP^T/dS^T [384 + 64 b)
+  // TMEM columns: dK [0,128), dV [128,256), S^T (P^T) [256,384), dP^T (dS^T) [384,512)
   constexpr uint32_t T_DK = 0, T_DV = 128, T_S = 256, T_DP = 384;
 
   if (warp == 0) {
@@ -183,8 +193,8 @@ tc_dkdv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
       const int64_t q0 = w.q0, k0 = w.k0;
       const int Lq = w.lq;
       if (lane == 0) {
-        const uint32_t ks = kv_it % L::NKV;
-        ok = mbar_wait(bar(KV_KVEMPTY + ks), ((kv_it / L::NKV) & 1) ^ 1, abort, status);
+        const uint32_t ks = kv_it % NKV;
+        ok = mbar_wait(bar(KV_KVEMPTY + ks), ((kv_it / NKV) & 1) ^ 1, abort, status);
         if (ok) {
           mbar_expect_tx(bar(KV_KVFULL + ks), L::K_BYTES + L::V_BYTES);
 #pragma unroll
@@ -205,9 +215,9 @@ tc_dkdv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
         const int i0 = (qs0 + j) * STEP;
         const uint32_t st = q_it % NQ, ph = (q_it / NQ) & 1;
         // row terms of this step: issue the global loads before waiting for the stage
-        float2 rv[2];
+        float2 rv[STEP / 32];
 #pragma unroll
-        for (int t = 0; t < 2; ++t) {
+        for (int t = 0; t < STEP / 32; ++t) {
           const int c = lane + 32 * t;
           rv[t] = make_float2(0.f, 0.f);
           if (ACT == kActSoftmax && i0 + c < Lq) rv[t] = rowstat[(int64_t)h * p.total_q + q0 + i0 + c];
@@ -218,17 +228,17 @@ tc_dkdv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
           mbar_expect_tx(bar(KV_QFULL + st), L::Q_BYTES + L::O_BYTES);
 #pragma unroll
           for (int a = 0; a < DQK / 64; ++a)
-            tma_load_2d(sb + L::Q_OFF + st * L::Q_BYTES + a * 8192, &tm_q, h * DQK + a * 64,
+            tma_load_2d(sb + L::Q_OFF + st * L::Q_BYTES + a * 16384, &tm_q, h * DQK + a * 64,
                         (int32_t)(q0 + i0), bar(KV_QFULL + st));
 #pragma unroll
           for (int a = 0; a < DV / 64; ++a)
-            tma_load_2d(sb + L::O_OFF + st * L::O_BYTES + a * 8192, &tm_do, h * DV + a * 64,
+            tma_load_2d(sb + L::O_OFF + st * L::O_BYTES + a * 16384, &tm_do, h * DV + a * 64,
                         (int32_t)(q0 + i0), bar(KV_QFULL + st));
         }
-        // stage layout: 64 x (-lse * log2 e), then 64 x (-D)
-        float* rs = reinterpret_cast<float*>(smem + L::RS_OFF + st * STEP * 8);
+        // stage layout: 128 x (-lse * log2 e), then 128 x (-D)
+        float* rs = reinterpret_cast<float*>(smem + L::RS_OFF + st * L::RS_BYTES);
 #pragma unroll
-        for (int t = 0; t < 2; ++t) {
+        for (int t = 0; t < STEP / 32; ++t) {
           rs[lane + 32 * t] = -rv[t].x;
           rs[STEP + lane + 32 * t] = -rv[t].y;
         }
@@ -250,71 +260,55 @@ tc_dkdv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
         if (it + (int)gridDim.x < n_items) nxt = load_item(list, it + gridDim.x);
         const int n = w.cost;
         if (n == 0) continue;
-        const uint32_t ks = kv_it % L::NKV;
-        if (!mbar_wait(bar(KV_KVFULL + ks), (kv_it / L::NKV) & 1, abort, status)) break;
+        const uint32_t ks = kv_it % NKV;
+        if (!mbar_wait(bar(KV_KVFULL + ks), (kv_it / NKV) & 1, abort, status)) break;
         tc_fence_after();
         const uint32_t k_tile = sb + L::K_OFF + ks * L::K_BYTES;
         const uint32_t v_tile = sb + L::V_OFF + ks * L::V_BYTES;
-        uint32_t prev_stage = 0;
-        for (int j = 0; j <= n && ok; ++j) {
-          uint32_t cur_stage = 0;
-          if (j < n) {
-            // S^T(j) = K Q(j)^T and dP^T(j) = V dO(j)^T into buffer j % 2.  The buffer
-            // held step j-2, whose P^T / dS^T were consumed by the dV / dK products
-            // issued (in order) before this point.
-            cur_stage = q_it % NQ;
-            const uint32_t sbuf = s_it & 1;
-            if (!mbar_wait(bar(KV_QFULL + cur_stage), (q_it / NQ) & 1, abort, status)) {
-              ok = false;
-              break;
-            }
-            tc_fence_after();
+        for (int j = 0; j < n; ++j, ++q_it, ++s_it) {
+          const uint32_t st = q_it % NQ;
+          const uint32_t q_tile = sb + L::Q_OFF + st * L::Q_BYTES;
+          const uint32_t o_tile = sb + L::O_OFF + st * L::O_BYTES;
+          if (!mbar_wait(bar(KV_QFULL + st), (q_it / NQ) & 1, abort, status)) { ok = false; break; }
+          tc_fence_after();
+          // S^T = K Q^T, then dP^T = V dO^T
 #pragma unroll
-            for (int kk = 0; kk < DQK / 16; ++kk) {
-              const uint64_t ad = sw128_desc(k_tile + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024);
-              const uint64_t bd = sw128_desc(sb + L::Q_OFF + cur_stage * L::Q_BYTES + (kk >> 2) * 8192 +
-                                                 (kk & 3) * 32, 16, 1024);
-              mma_bf16(tmem + T_S + sbuf * STEP, ad, bd, idesc_s, kk > 0 ? 1u : 0u);
-            }
-#pragma unroll
-            for (int kk = 0; kk < DV / 16; ++kk) {
-              const uint64_t ad = sw128_desc(v_tile + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024);
-              const uint64_t bd = sw128_desc(sb + L::O_OFF + cur_stage * L::O_BYTES + (kk >> 2) * 8192 +
-                                                 (kk & 3) * 32, 16, 1024);
-              mma_bf16(tmem + T_DP + sbuf * STEP, ad, bd, idesc_s, kk > 0 ? 1u : 0u);
-            }
-            mma_commit(bar(KV_SFULL + sbuf));
-            if (j == n - 1) mma_commit(bar(KV_KVEMPTY + ks));
-            ++s_it;
-            ++q_it;
+          for (int kk = 0; kk < DQK / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+            mma_bf16(tmem + T_S, sw128_desc(k_tile + off, 16, 1024), sw128_desc(q_tile + off, 16, 1024),
+                     idesc_s, kk > 0 ? 1u : 0u);
           }
-          if (j > 0) {
-            // dV += P^T(j-1) dO(j-1), dK += dS^T(j-1) Q(j-1); A operands from TMEM
-            const uint32_t pbuf = (s_it - (j < n ? 2 : 1)) & 1;
-            const uint32_t pidx = s_it - (j < n ? 2 : 1);
-            if (!mbar_wait(bar(KV_PFULL + pbuf), (pidx >> 1) & 1, abort, status) ||
-                (j == 1 && !mbar_wait(bar(KV_ACCEMPTY), (a_it & 1) ^ 1, abort, status))) {
-              ok = false;
-              break;
-            }
-            tc_fence_after();
-            const uint32_t acc = j > 1 ? 1u : 0u;
+          mma_commit(bar(KV_SFULL));
 #pragma unroll
-            for (int kk = 0; kk < STEP / 16; ++kk) {
-              const uint64_t bd = sw128_desc(sb + L::O_OFF + prev_stage * L::O_BYTES + kk * 2048, 8192, 1024);
-              mma_bf16_tmem_a(tmem + T_DV, tmem + T_S + pbuf * STEP + kk * 8, bd, idesc_dv,
-                              (acc | (kk > 0)) ? 1u : 0u);
-            }
-#pragma unroll
-            for (int kk = 0; kk < STEP / 16; ++kk) {
-              const uint64_t bd = sw128_desc(sb + L::Q_OFF + prev_stage * L::Q_BYTES + kk * 2048, 8192, 1024);
-              mma_bf16_tmem_a(tmem + T_DK, tmem + T_DP + pbuf * STEP + kk * 8, bd, idesc_dk,
-                              (acc | (kk > 0)) ? 1u : 0u);
-            }
-            mma_commit(bar(KV_QEMPTY + prev_stage));
-            if (j == n) mma_commit(bar(KV_ACCFULL));
+          for (int kk = 0; kk < DV / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+            mma_bf16(tmem + T_DP, sw128_desc(v_tile + off, 16, 1024), sw128_desc(o_tile + off, 16, 1024),
+                     idesc_s, kk > 0 ? 1u : 0u);
           }
-          prev_stage = cur_stage;
+          mma_commit(bar(KV_DPFULL));
+          if (j == n - 1) mma_commit(bar(KV_KVEMPTY + ks));
+          // dV += P^T dO (P^T packed in TMEM: query columns 0..63 at +0, 64..127 at +64)
+          if (!mbar_wait(bar(KV_PFULL), s_it & 1, abort, status) ||
+              (j == 0 && !mbar_wait(bar(KV_ACCEMPTY), (a_it & 1) ^ 1, abort, status))) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < STEP / 16; ++kk)
+            mma_bf16_tmem_a(tmem + T_DV, tmem + T_S + (kk >> 2) * 64 + (kk & 3) * 8,
+                            sw128_desc(o_tile + kk * 2048, 16384, 1024), idesc_dv,
+                            (j > 0 || kk > 0) ? 1u : 0u);
+          // dK += dS^T Q
+          if (!mbar_wait(bar(KV_DSFULL), s_it & 1, abort, status)) { ok = false; break; }
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < STEP / 16; ++kk)
+            mma_bf16_tmem_a(tmem + T_DK, tmem + T_DP + (kk >> 2) * 64 + (kk & 3) * 8,
+                            sw128_desc(q_tile + kk * 2048, 16384, 1024), idesc_dk,
+                            (j > 0 || kk > 0) ? 1u : 0u);
+          mma_commit(bar(KV_QEMPTY + st));
+          if (j == n - 1) mma_commit(bar(KV_ACCFULL));
         }
         ++kv_it;
         ++a_it;
@@ -322,13 +316,22 @@ tc_dkdv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
     }
     __syncwarp();
   } else {
-    // ------------------------------------------------------------ compute warpgroup
+    // ------------------------------------------------------------ compute warpgroups
+    // Warps 2..5 and 6..9 each cover all 128 keys (TMEM lanes); the first group
+    // handles query columns [0,64) of every step and the first half of the dK/dV
+    // columns in the epilogue, the second group the other halves.  Each group
+    // writes only inside its own columns.
+    const int half = (warp - 2) >> 2;
     const int r = 32 * (warp & 3) + lane;  // key of the tile = TMEM lane
     const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
     const float c_score = ACT == kActSoftmax ? p.scale * kLog2e : p.scale;
     const float shift_raw = kMaskShift / c_score;  // masked raw scores land kMaskShift lower
+    const float2 cc = make_float2(c_score, c_score);
     const float2 hc = make_float2(0.5f * c_score, 0.5f * c_score);
-    const float2 one = make_float2(1.f, 1.f), half = make_float2(0.5f, 0.5f);
+    const float2 one = make_float2(1.f, 1.f);
+    constexpr int HC = STEP / 2;  // query columns per group
+    const uint32_t s_tm = tmem + lane_base + T_S + half * HC;
+    const uint32_t p_tm = tmem + lane_base + T_DP + half * HC;
     uint32_t q_it = 0, s_it = 0, a_it = 0;
     bool ok = true;
     WorkItem nxt = blockIdx.x < (unsigned)n_items ? load_item(list, blockIdx.x) : WorkItem{};
@@ -341,63 +344,72 @@ tc_dkdv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
       const int Lq = w.lq, Lk = w.lk;
       const int j = key0 + r;  // key index inside the sequence
       const float inv_len = 1.0f / (float)max(Lq, 1);
+      const float2 hl = make_float2(0.5f * inv_len, 0.5f * inv_len);
       const float2 il = make_float2(inv_len, inv_len);
       const int qs0 = CAUSAL ? key0 / STEP : 0;
-      for (int step = 0; step < n; ++step, ++q_it) {
-        const uint32_t sbuf = s_it & 1;
-        if (!mbar_wait(bar(KV_SFULL + sbuf), (s_it >> 1) & 1, abort, status)) { ok = false; break; }
+      for (int step = 0; step < n; ++step, ++q_it, ++s_it) {
+        if (!mbar_wait(bar(KV_SFULL), s_it & 1, abort, status)) { ok = false; break; }
         tc_fence_after();
-        float sv[STEP], dp[STEP];
-        const uint32_t s_tm = tmem + lane_base + T_S + sbuf * STEP;
-        const uint32_t p_tm = tmem + lane_base + T_DP + sbuf * STEP;
+        float sv[HC];
         tmem_ld32(s_tm, sv);
         tmem_ld32(s_tm + 32, sv + 32);
-        tmem_ld32(p_tm, dp);
-        tmem_ld32(p_tm + 32, dp + 32);
         tmem_wait_ld();
         const uint32_t st = q_it % NQ;
         if (!mbar_wait(bar(KV_RSFULL + st), (q_it / NQ) & 1, abort, status)) { ok = false; break; }
-        const float* rs = reinterpret_cast<const float*>(smem + L::RS_OFF + st * STEP * 8);
-        const int i0 = (qs0 + step) * STEP;
-        // valid queries of this step for key j: i < Lq and (causal) i >= j
+        const float* rs = reinterpret_cast<const float*>(smem + L::RS_OFF + st * L::RS_BYTES) + half * HC;
+        const int i0 = (qs0 + step) * STEP + half * HC;
+        // valid queries of this group's columns for key j: i < Lq and (causal) i >= j
         const int lo = CAUSAL ? j - i0 : 0;
         const int hi = j < Lk ? Lq - i0 : 0;
-        if (lo > 0 || hi < STEP) {
-          // partial step: move masked raw scores down by a finite shift
+        if (lo > 0 || hi < HC) {
 #pragma unroll
-          for (int c = 0; c < STEP; ++c) sv[c] -= (c >= lo && c < hi) ? 0.f : shift_raw;
+          for (int c = 0; c < HC; ++c) sv[c] -= (c >= lo && c < hi) ? 0.f : shift_raw;
         }
-        const float2 cc = make_float2(c_score, c_score);
-        uint32_t pk[STEP / 2], dk2[STEP / 2];
+        // P^T (and, for SiLU/L, the factor SiLU'(u)/L used by dS^T), packed bf16
+        uint32_t pk[HC / 2], fk[ACT == kActSoftmax ? 1 : HC / 2];
 #pragma unroll
-        for (int c = 0; c < STEP; c += 2) {
+        for (int c = 0; c < HC; c += 2) {
           const float2 x = make_float2(sv[c], sv[c + 1]);
-          const float2 d = make_float2(dp[c], dp[c + 1]);
-          float2 pv, ds;
+          float2 pv;
           if (ACT == kActSoftmax) {
-            const float2 nl = *reinterpret_cast<const float2*>(rs + c);        // -lse log2 e
-            const float2 nd = *reinterpret_cast<const float2*>(rs + STEP + c); // -D
-            const float2 e = ffma2(x, cc, nl);
+            const float2 e = ffma2(x, cc, *reinterpret_cast<const float2*>(rs + c));
             pv = make_float2(ex2(e.x), ex2(e.y));
-            ds = fmul2(pv, fadd2(d, nd));
           } else {
-            // u = s c, h = u/2, t = tanh h: P = h (1+t)/L, dS = dP (1+t)/L (1 + h - h t)/2
+            // u = s c, h = u/2, t = tanh h: P = h (1+t)/L, SiLU'(u)/L = (1+t)/(2L) (1 + h - h t)
             const float2 hh = fmul2(x, hc);
             const float2 t = make_float2(tanh_approx(hh.x), tanh_approx(hh.y));
-            const float2 g = ffma2(t, il, il);
-            pv = fmul2(hh, g);
-            const float2 b = ffma2(make_float2(-hh.x, -hh.y), t, fadd2(hh, one));
-            ds = fmul2(fmul2(d, g), fmul2(b, half));
+            pv = fmul2(hh, ffma2(t, il, il));
+            const float2 f = fmul2(ffma2(t, hl, hl), ffma2(make_float2(-hh.x, -hh.y), t, fadd2(hh, one)));
+            fk[c / 2] = pack_bf16(f.x, f.y);
           }
           pk[c / 2] = pack_bf16(pv.x, pv.y);
-          dk2[c / 2] = pack_bf16(ds.x, ds.y);
         }
         tmem_st32(s_tm, reinterpret_cast<const float*>(pk));
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(bar(KV_PFULL));
+        // dS^T = P^T (dP^T - D)  or  dP^T SiLU'(u)/L
+        if (!mbar_wait(bar(KV_DPFULL), s_it & 1, abort, status)) { ok = false; break; }
+        tc_fence_after();
+        float dp[HC];
+        tmem_ld32(p_tm, dp);
+        tmem_ld32(p_tm + 32, dp + 32);
+        tmem_wait_ld();
+        uint32_t dk2[HC / 2];
+#pragma unroll
+        for (int c = 0; c < HC; c += 2) {
+          const float2 d = make_float2(dp[c], dp[c + 1]);
+          float2 ds;
+          if (ACT == kActSoftmax)
+            ds = fmul2(unpack_bf16(pk[c / 2]), fadd2(d, *reinterpret_cast<const float2*>(rs + STEP + c)));
+          else
+            ds = fmul2(d, unpack_bf16(fk[c / 2]));
+          dk2[c / 2] = pack_bf16(ds.x, ds.y);
+        }
         tmem_st32(p_tm, reinterpret_cast<const float*>(dk2));
         tmem_wait_st();
         tc_fence_before();
-        mbar_arrive(bar(KV_PFULL + sbuf));
-        ++s_it;
+        mbar_arrive(bar(KV_DSFULL));
       }
       if (!ok) break;
       // ---------------------------------------------------------- epilogue
@@ -407,27 +419,29 @@ tc_dkdv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
         if (!mbar_wait(bar(KV_ACCFULL), a_it & 1, abort, status)) { ok = false; break; }
         ++a_it;
         tc_fence_after();
-        float x[32];
+        float x[DQK / 2];
 #pragma unroll
-        for (int c = 0; c < DQK / 32; ++c) {
-          tmem_ld32(tmem + lane_base + T_DK + 32 * c, x);
-          tmem_wait_ld();
-          if (key_ok) store_row_bf16(dk + krow * DQK + 32 * c, x, p.scale);
-        }
+        for (int c = 0; c < DQK / 64; ++c) tmem_ld32(tmem + lane_base + T_DK + half * (DQK / 2) + 32 * c, x + 32 * c);
+        float y[DV / 2];
 #pragma unroll
-        for (int c = 0; c < DV / 32; ++c) {
-          tmem_ld32(tmem + lane_base + T_DV + 32 * c, x);
-          tmem_wait_ld();
-          if (key_ok) store_row_bf16(dv + krow * DV + 32 * c, x, 1.f);
-        }
+        for (int c = 0; c < DV / 64; ++c) tmem_ld32(tmem + lane_base + T_DV + half * (DV / 2) + 32 * c, y + 32 * c);
+        tmem_wait_ld();
         tc_fence_before();
         mbar_arrive(bar(KV_ACCEMPTY));
+        if (key_ok) {
+#pragma unroll
+          for (int c = 0; c < DQK / 64; ++c)
+            store_row_bf16(dk + krow * DQK + half * (DQK / 2) + 32 * c, x + 32 * c, p.scale);
+#pragma unroll
+          for (int c = 0; c < DV / 64; ++c)
+            store_row_bf16(dv + krow * DV + half * (DV / 2) + 32 * c, y + 32 * c, 1.f);
+        }
       } else if (key_ok) {
         const float z[32] = {0.f};
 #pragma unroll
-        for (int c = 0; c < DQK / 32; ++c) store_row_bf16(dk + krow * DQK + 32 * c, z, 1.f);
+        for (int c = 0; c < DQK / 64; ++c) store_row_bf16(dk + krow * DQK + half * (DQK / 2) + 32 * c, z, 1.f);
 #pragma unroll
-        for (int c = 0; c < DV / 32; ++c) store_row_bf16(dv + krow * DV + 32 * c, z, 1.f);
+        for (int c = 0; c < DV / 64; ++c) store_row_bf16(dv + krow * DV + half * (DV / 2) + 32 * c, z, 1.f);
       }
     }
   }
@@ -443,30 +457,29 @@ tc_dkdv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
 // =============================================================================
 // dQ pass
 // =============================================================================
-// K/V steps are staged in an NK-deep ring; dS is written back into TMEM as
-// packed bf16 over the first 32 columns of the dP buffer and the dQ product
-// reads it from there.
+// One item = (sequence, head, 128-row query tile); the inner loop steps over
+// 128 keys.  S is double-buffered in TMEM so that S of the next step is
+// computed while the compute warpgroups form dS of this one; dS goes back into
+// TMEM as packed bf16 over the dP columns and dQ += dS K reads it from there.
 template <int DQK, int DV>
 struct QLayout {
-  // Q/dO of the next item are prefetched where shared memory allows; the K/V
-  // ring depth matters more and is kept at 4 or more.
-  static constexpr int NQO = DQK + DV > 192 ? 1 : 2;       // Q/dO tiles
-  static constexpr int NK = DQK + DV > 128 ? 4 : 6;        // K/V ring stages
+  static constexpr int NQO = DQK + DV == 256 ? 1 : 2;      // Q/dO tiles
+  static constexpr int NK = DQK + DV == 128 ? 4 : 2;       // K/V stages of 128 keys
   static constexpr uint32_t Q_BYTES = DQK / 64 * 16384;   // 128 rows
   static constexpr uint32_t O_BYTES = DV / 64 * 16384;
-  static constexpr uint32_t K_BYTES = DQK / 64 * 8192;    // 64 keys
-  static constexpr uint32_t V_BYTES = DV / 64 * 8192;
-  static constexpr uint32_t Q_OFF = 0;                     // NQO stages
-  static constexpr uint32_t O_OFF = Q_OFF + NQO * Q_BYTES; // NQO stages
-  static constexpr uint32_t K_OFF = O_OFF + NQO * O_BYTES; // NK stages
-  static constexpr uint32_t V_OFF = K_OFF + NK * K_BYTES;  // NK stages
+  static constexpr uint32_t K_BYTES = DQK / 64 * 16384;   // 128 keys
+  static constexpr uint32_t V_BYTES = DV / 64 * 16384;
+  static constexpr uint32_t Q_OFF = 0;
+  static constexpr uint32_t O_OFF = Q_OFF + NQO * Q_BYTES;
+  static constexpr uint32_t K_OFF = O_OFF + NQO * O_BYTES;
+  static constexpr uint32_t V_OFF = K_OFF + NK * K_BYTES;
   static constexpr uint32_t BAR_OFF = V_OFF + NK * V_BYTES;
   static constexpr uint32_t SMEM = (BAR_OFF + 512 + 1024) > 122880u ? (BAR_OFF + 512 + 1024) : 122880u;
 };
 
 enum : uint32_t {
-  Q_QFULL = 0, Q_QEMPTY = 2, Q_KFULL = 4, Q_KEMPTY = 10, Q_SFULL = 16, Q_PFULL = 18,
-  Q_ACCFULL = 20, Q_ACCEMPTY = 21, Q_COUNT = 22
+  Q_QFULL = 0, Q_QEMPTY = 2, Q_KFULL = 4, Q_KEMPTY = 8, Q_SFULL = 12, Q_DPFULL = 14,
+  Q_DSFULL = 15, Q_ACCFULL = 16, Q_ACCEMPTY = 17, Q_COUNT = 18
 };
 
 template <int DQK, int DV, int ACT, bool CAUSAL>
@@ -476,7 +489,7 @@ tc_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
              const Problem p, const float2* __restrict__ rowstat, __nv_bfloat16* __restrict__ dq,
              WsHeader* hdr, const WorkItem* __restrict__ list) {
   using L = QLayout<DQK, DV>;
-  constexpr int NK = L::NK;
+  constexpr int NK = L::NK, NQO = L::NQO;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   const uint32_t sb = smem_u32(smem);
@@ -489,7 +502,7 @@ tc_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
   const int n_items = hdr->n_q;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < L::NQO; ++s) {
+    for (int s = 0; s < NQO; ++s) {
       mbar_init(bar(Q_QFULL + s), 1);
       mbar_init(bar(Q_QEMPTY + s), 1);
     }
@@ -497,12 +510,12 @@ tc_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
       mbar_init(bar(Q_KFULL + s), 1);
       mbar_init(bar(Q_KEMPTY + s), 1);
     }
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(bar(Q_SFULL + s), 1);
-      mbar_init(bar(Q_PFULL + s), 128);
-    }
+    mbar_init(bar(Q_SFULL), 1);
+    mbar_init(bar(Q_SFULL + 1), 1);
+    mbar_init(bar(Q_DPFULL), 1);
+    mbar_init(bar(Q_DSFULL), 256);
     mbar_init(bar(Q_ACCFULL), 1);
-    mbar_init(bar(Q_ACCEMPTY), 128);
+    mbar_init(bar(Q_ACCEMPTY), 256);
     *abort = 0;
     fence_mbar_init();
   }
@@ -511,8 +524,9 @@ tc_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  // TMEM columns: dQ [0,128), S [128 + 64 b), dP/dS [256 + 64 b)
-  constexpr uint32_t T_DQ = 0, T_S = 128, T_DP = 256;
+  // TMEM columns: dQ [0,128), S buffer 0 [128,256), dP (dS) [256,384), S buffer 1 [384,512)
+  constexpr uint32_t T_DQ = 0, T_DP = 256;
+  auto t_s = [](uint32_t b) { return b ? 384u : 128u; };
 
   if (warp == 0) {
     if (lane == 0) {
@@ -530,8 +544,8 @@ tc_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
         if (n == 0) continue;
         const int h = w.h, row0 = w.tile * TILE;
         const int32_t q0 = w.q0, k0 = w.k0;
-        const uint32_t qs = q_it % L::NQO;
-        if (!mbar_wait(bar(Q_QEMPTY + qs), ((q_it / L::NQO) & 1) ^ 1, abort, status)) break;
+        const uint32_t qs = q_it % NQO;
+        if (!mbar_wait(bar(Q_QEMPTY + qs), ((q_it / NQO) & 1) ^ 1, abort, status)) break;
         mbar_expect_tx(bar(Q_QFULL + qs), L::Q_BYTES + L::O_BYTES);
 #pragma unroll
         for (int a = 0; a < DQK / 64; ++a)
@@ -548,11 +562,11 @@ tc_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
           mbar_expect_tx(bar(Q_KFULL + st), L::K_BYTES + L::V_BYTES);
 #pragma unroll
           for (int a = 0; a < DQK / 64; ++a)
-            tma_load_2d(sb + L::K_OFF + st * L::K_BYTES + a * 8192, &tm_k, h * DQK + a * 64,
+            tma_load_2d(sb + L::K_OFF + st * L::K_BYTES + a * 16384, &tm_k, h * DQK + a * 64,
                         k0 + j * STEP, bar(Q_KFULL + st));
 #pragma unroll
           for (int a = 0; a < DV / 64; ++a)
-            tma_load_2d(sb + L::V_OFF + st * L::V_BYTES + a * 8192, &tm_v, h * DV + a * 64,
+            tma_load_2d(sb + L::V_OFF + st * L::V_BYTES + a * 16384, &tm_v, h * DV + a * 64,
                         k0 + j * STEP, bar(Q_KFULL + st));
         }
       }
@@ -562,7 +576,7 @@ tc_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
     if (lane == 0) {
       constexpr uint32_t idesc_s = idesc_bf16(TILE, STEP, 0, 0);
       constexpr uint32_t idesc_dq = idesc_bf16(TILE, DQK, 0, 1);
-      uint32_t q_it = 0, k_it = 0, s_it = 0, a_it = 0;
+      uint32_t q_it = 0, k_it = 0, s_it = 0, d_it = 0, a_it = 0;
       bool ok = true;
       WorkItem nxt = blockIdx.x < (unsigned)n_items ? load_item(list, blockIdx.x) : WorkItem{};
       for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
@@ -570,76 +584,87 @@ tc_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
         if (it + (int)gridDim.x < n_items) nxt = load_item(list, it + gridDim.x);
         const int n = w.cost;
         if (n == 0) continue;
-        const uint32_t qs = q_it % L::NQO;
-        if (!mbar_wait(bar(Q_QFULL + qs), (q_it / L::NQO) & 1, abort, status)) break;
+        const uint32_t qs = q_it % NQO;
+        if (!mbar_wait(bar(Q_QFULL + qs), (q_it / NQO) & 1, abort, status)) break;
         tc_fence_after();
         const uint32_t q_tile = sb + L::Q_OFF + qs * L::Q_BYTES;
         const uint32_t o_tile = sb + L::O_OFF + qs * L::O_BYTES;
-        uint32_t prev_stage = 0;
-        for (int j = 0; j <= n && ok; ++j) {
-          uint32_t cur_stage = 0;
-          if (j < n) {
-            cur_stage = k_it % NK;
-            const uint32_t sbuf = s_it & 1;
-            if (!mbar_wait(bar(Q_KFULL + cur_stage), (k_it / NK) & 1, abort, status)) {
-              ok = false;
-              break;
-            }
-            tc_fence_after();
+        auto issue_s = [&](uint32_t kst) {  // S into buffer s_it & 1
+          const uint32_t k_tile = sb + L::K_OFF + kst * L::K_BYTES;
 #pragma unroll
-            for (int kk = 0; kk < DQK / 16; ++kk) {
-              const uint64_t ad = sw128_desc(q_tile + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024);
-              const uint64_t bd = sw128_desc(sb + L::K_OFF + cur_stage * L::K_BYTES + (kk >> 2) * 8192 +
-                                                 (kk & 3) * 32, 16, 1024);
-              mma_bf16(tmem + T_S + sbuf * STEP, ad, bd, idesc_s, kk > 0 ? 1u : 0u);
-            }
-#pragma unroll
-            for (int kk = 0; kk < DV / 16; ++kk) {
-              const uint64_t ad = sw128_desc(o_tile + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024);
-              const uint64_t bd = sw128_desc(sb + L::V_OFF + cur_stage * L::V_BYTES + (kk >> 2) * 8192 +
-                                                 (kk & 3) * 32, 16, 1024);
-              mma_bf16(tmem + T_DP + sbuf * STEP, ad, bd, idesc_s, kk > 0 ? 1u : 0u);
-            }
-            mma_commit(bar(Q_SFULL + sbuf));
-            if (j == n - 1) mma_commit(bar(Q_QEMPTY + qs));
-            ++s_it;
-            ++k_it;
+          for (int kk = 0; kk < DQK / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+            mma_bf16(tmem + t_s(s_it & 1), sw128_desc(q_tile + off, 16, 1024),
+                     sw128_desc(k_tile + off, 16, 1024), idesc_s, kk > 0 ? 1u : 0u);
           }
-          if (j > 0) {
-            // dQ += dS(j-1) K(j-1), dS from TMEM
-            const uint32_t pidx = s_it - (j < n ? 2 : 1);
-            const uint32_t pbuf = pidx & 1;
-            if (!mbar_wait(bar(Q_PFULL + pbuf), (pidx >> 1) & 1, abort, status) ||
-                (j == 1 && !mbar_wait(bar(Q_ACCEMPTY), (a_it & 1) ^ 1, abort, status))) {
-              ok = false;
-              break;
-            }
-            tc_fence_after();
+          mma_commit(bar(Q_SFULL + (s_it & 1)));
+          ++s_it;
+        };
+        auto issue_dp = [&](uint32_t kst) {
+          const uint32_t v_tile = sb + L::V_OFF + kst * L::V_BYTES;
 #pragma unroll
-            for (int kk = 0; kk < STEP / 16; ++kk) {
-              const uint64_t bd = sw128_desc(sb + L::K_OFF + prev_stage * L::K_BYTES + kk * 2048, 8192, 1024);
-              mma_bf16_tmem_a(tmem + T_DQ, tmem + T_DP + pbuf * STEP + kk * 8, bd, idesc_dq,
-                              (j > 1 || kk > 0) ? 1u : 0u);
-            }
-            mma_commit(bar(Q_KEMPTY + prev_stage));
-            if (j == n) mma_commit(bar(Q_ACCFULL));
+          for (int kk = 0; kk < DV / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+            mma_bf16(tmem + T_DP, sw128_desc(o_tile + off, 16, 1024), sw128_desc(v_tile + off, 16, 1024),
+                     idesc_s, kk > 0 ? 1u : 0u);
           }
-          prev_stage = cur_stage;
+          mma_commit(bar(Q_DPFULL));
+        };
+        // prologue: S(0), dP(0)
+        const uint32_t k_base = k_it;
+        if (!mbar_wait(bar(Q_KFULL + k_base % NK), (k_base / NK) & 1, abort, status)) break;
+        tc_fence_after();
+        issue_s(k_base % NK);
+        issue_dp(k_base % NK);
+        for (int j = 0; j < n && ok; ++j) {
+          const uint32_t kst = (k_base + j) % NK;
+          if (j + 1 < n) {
+            const uint32_t k1 = k_base + j + 1;
+            if (!mbar_wait(bar(Q_KFULL + k1 % NK), (k1 / NK) & 1, abort, status)) { ok = false; break; }
+            tc_fence_after();
+            issue_s(k1 % NK);  // S(j+1) overlaps the dS(j) math
+          }
+          // dQ += dS(j) K(j); dS packed in TMEM: key columns 0..63 at +0, 64..127 at +64
+          if (!mbar_wait(bar(Q_DSFULL), d_it & 1, abort, status) ||
+              (j == 0 && !mbar_wait(bar(Q_ACCEMPTY), (a_it & 1) ^ 1, abort, status))) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t k_tile = sb + L::K_OFF + kst * L::K_BYTES;
+#pragma unroll
+          for (int kk = 0; kk < STEP / 16; ++kk)
+            mma_bf16_tmem_a(tmem + T_DQ, tmem + T_DP + (kk >> 2) * 64 + (kk & 3) * 8,
+                            sw128_desc(k_tile + kk * 2048, 16384, 1024), idesc_dq,
+                            (j > 0 || kk > 0) ? 1u : 0u);
+          mma_commit(bar(Q_KEMPTY + kst));
+          ++d_it;
+          if (j + 1 < n) issue_dp((k_base + j + 1) % NK);
         }
+        if (!ok) break;
+        mma_commit(bar(Q_QEMPTY + qs));
+        mma_commit(bar(Q_ACCFULL));
+        k_it += n;
         ++q_it;
         ++a_it;
       }
     }
     __syncwarp();
   } else {
+    // Two compute warpgroups: warps 2..5 take key columns [0,64) of every step
+    // and the first half of the dQ columns, warps 6..9 the other halves; each
+    // group writes only inside its own columns.
+    const int half = (warp - 2) >> 2;
     const int r = 32 * (warp & 3) + lane;  // query row of the tile = TMEM lane
     const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
     const float c_score = ACT == kActSoftmax ? p.scale * kLog2e : p.scale;
     const float shift_raw = kMaskShift / c_score;  // masked raw scores land kMaskShift lower
     const float2 cc = make_float2(c_score, c_score);
     const float2 hc = make_float2(0.5f * c_score, 0.5f * c_score);
-    const float2 one = make_float2(1.f, 1.f), half = make_float2(0.5f, 0.5f);
-    uint32_t s_it = 0, a_it = 0;
+    const float2 one = make_float2(1.f, 1.f);
+    constexpr int HC = STEP / 2;  // key columns per group
+    const uint32_t p_tm = tmem + lane_base + T_DP + half * HC;
+    uint32_t s_it = 0, d_it = 0, a_it = 0;
     bool ok = true;
     WorkItem nxt = blockIdx.x < (unsigned)n_items ? load_item(list, blockIdx.x) : WorkItem{};
     for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
@@ -652,54 +677,61 @@ tc_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
       const int i = row0 + r;
       const bool row_ok = i < Lq;
       const float inv_len = 1.0f / (float)max(Lq, 1);
+      const float2 hl = make_float2(0.5f * inv_len, 0.5f * inv_len);
       float2 rsv = make_float2(0.f, 0.f);
       if (ACT == kActSoftmax && row_ok && n > 0) rsv = rowstat[(int64_t)h * p.total_q + q0 + i];
       const float2 nl = make_float2(-rsv.x, -rsv.x), nd = make_float2(-rsv.y, -rsv.y);
-      const float2 il = make_float2(inv_len, inv_len);
-      for (int step = 0; step < n; ++step) {
+      for (int step = 0; step < n; ++step, ++s_it, ++d_it) {
         const uint32_t sbuf = s_it & 1;
         if (!mbar_wait(bar(Q_SFULL + sbuf), (s_it >> 1) & 1, abort, status)) { ok = false; break; }
         tc_fence_after();
-        float sv[STEP], dp[STEP];
-        const uint32_t s_tm = tmem + lane_base + T_S + sbuf * STEP;
-        const uint32_t p_tm = tmem + lane_base + T_DP + sbuf * STEP;
+        const uint32_t s_tm = tmem + lane_base + t_s(sbuf) + half * HC;
+        float sv[HC];
         tmem_ld32(s_tm, sv);
         tmem_ld32(s_tm + 32, sv + 32);
-        tmem_ld32(p_tm, dp);
-        tmem_ld32(p_tm + 32, dp + 32);
         tmem_wait_ld();
-        const int kb = step * STEP;
+        const int kb = step * STEP + half * HC;
         int nvalid = Lk - kb;
         if (CAUSAL) nvalid = min(nvalid, i - kb + 1);
         if (!row_ok) nvalid = 0;
-        if (nvalid < STEP) {
-          // partial step: move masked raw scores down by a finite shift
+        if (nvalid < HC) {
 #pragma unroll
-          for (int c = 0; c < STEP; ++c) sv[c] -= c < nvalid ? 0.f : shift_raw;
+          for (int c = 0; c < HC; ++c) sv[c] -= c < nvalid ? 0.f : shift_raw;
         }
-        uint32_t pk[STEP / 2];
+        // P (softmax) or SiLU'(u)/L, packed bf16; both multiply dP into dS
+        uint32_t fk[HC / 2];
 #pragma unroll
-        for (int c = 0; c < STEP; c += 2) {
+        for (int c = 0; c < HC; c += 2) {
           const float2 x = make_float2(sv[c], sv[c + 1]);
-          const float2 d = make_float2(dp[c], dp[c + 1]);
-          float2 ds;
+          float2 f;
           if (ACT == kActSoftmax) {
             const float2 e = ffma2(x, cc, nl);
-            ds = fmul2(make_float2(ex2(e.x), ex2(e.y)), fadd2(d, nd));
+            f = make_float2(ex2(e.x), ex2(e.y));
           } else {
             const float2 hh = fmul2(x, hc);
             const float2 t = make_float2(tanh_approx(hh.x), tanh_approx(hh.y));
-            const float2 g = ffma2(t, il, il);
-            const float2 b = ffma2(make_float2(-hh.x, -hh.y), t, fadd2(hh, one));
-            ds = fmul2(fmul2(d, g), fmul2(b, half));
+            f = fmul2(ffma2(t, hl, hl), ffma2(make_float2(-hh.x, -hh.y), t, fadd2(hh, one)));
           }
-          pk[c / 2] = pack_bf16(ds.x, ds.y);
+          fk[c / 2] = pack_bf16(f.x, f.y);
         }
-        tmem_st32(p_tm, reinterpret_cast<const float*>(pk));
+        if (!mbar_wait(bar(Q_DPFULL), d_it & 1, abort, status)) { ok = false; break; }
+        tc_fence_after();
+        float dp[HC];
+        tmem_ld32(p_tm, dp);
+        tmem_ld32(p_tm + 32, dp + 32);
+        tmem_wait_ld();
+        uint32_t dk2[HC / 2];
+#pragma unroll
+        for (int c = 0; c < HC; c += 2) {
+          const float2 d = make_float2(dp[c], dp[c + 1]);
+          const float2 ds = ACT == kActSoftmax ? fmul2(unpack_bf16(fk[c / 2]), fadd2(d, nd))
+                                               : fmul2(d, unpack_bf16(fk[c / 2]));
+          dk2[c / 2] = pack_bf16(ds.x, ds.y);
+        }
+        tmem_st32(p_tm, reinterpret_cast<const float*>(dk2));
         tmem_wait_st();
         tc_fence_before();
-        mbar_arrive(bar(Q_PFULL + sbuf));
-        ++s_it;
+        mbar_arrive(bar(Q_DSFULL));
       }
       if (!ok) break;
       const int64_t orow = (q0 + i) * p.heads + h;
@@ -707,19 +739,21 @@ tc_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
         if (!mbar_wait(bar(Q_ACCFULL), a_it & 1, abort, status)) { ok = false; break; }
         ++a_it;
         tc_fence_after();
-        float x[32];
+        float x[DQK / 2];
 #pragma unroll
-        for (int c = 0; c < DQK / 32; ++c) {
-          tmem_ld32(tmem + lane_base + T_DQ + 32 * c, x);
-          tmem_wait_ld();
-          if (row_ok) store_row_bf16(dq + orow * DQK + 32 * c, x, p.scale);
-        }
+        for (int c = 0; c < DQK / 64; ++c) tmem_ld32(tmem + lane_base + T_DQ + half * (DQK / 2) + 32 * c, x + 32 * c);
+        tmem_wait_ld();
         tc_fence_before();
         mbar_arrive(bar(Q_ACCEMPTY));
+        if (row_ok) {
+#pragma unroll
+          for (int c = 0; c < DQK / 64; ++c)
+            store_row_bf16(dq + orow * DQK + half * (DQK / 2) + 32 * c, x + 32 * c, p.scale);
+        }
       } else if (row_ok) {
         const float z[32] = {0.f};
 #pragma unroll
-        for (int c = 0; c < DQK / 32; ++c) store_row_bf16(dq + orow * DQK + 32 * c, z, 1.f);
+        for (int c = 0; c < DQK / 64; ++c) store_row_bf16(dq + orow * DQK + half * (DQK / 2) + 32 * c, z, 1.f);
       }
     }
   }
@@ -733,24 +767,20 @@ tc_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
 }
 
 // ------------------------------------------------------------------ host side
+// Every tile of both passes is 128 rows (or keys) by 64 columns.
 struct Maps {
-  CUtensorMap q64, do64, k128, v128;  // dK/dV pass: 64-row Q/dO boxes, 128-key K/V boxes
-  CUtensorMap q128, do128, k64, v64;  // dQ pass: 128-row Q/dO boxes, 64-key K/V boxes
+  CUtensorMap q, dout, k, v;
 };
 
 bool make_maps(const Problem& p, const void* q, const void* k, const void* v, const void* dout,
-               bool kv_pass, Maps* m) {
+               Maps* m) {
   const int64_t cq = (int64_t)p.heads * p.dim_qk, cv = (int64_t)p.heads * p.dim_v;
   const int64_t tk = p.total_k > 0 ? p.total_k : p.total_q;
   const void* kk = p.total_k > 0 ? k : q;
   const void* vv = p.total_k > 0 ? v : dout;
-  if (kv_pass)
-    return make_tile_map(&m->q64, q, p.total_q, cq, 64, STEP) &&
-           make_tile_map(&m->do64, dout, p.total_q, cv, 64, STEP) &&
-           make_tile_map(&m->k128, kk, tk, cq, 64, TILE) && make_tile_map(&m->v128, vv, tk, cv, 64, TILE);
-  return make_tile_map(&m->q128, q, p.total_q, cq, 64, TILE) &&
-         make_tile_map(&m->do128, dout, p.total_q, cv, 64, TILE) &&
-         make_tile_map(&m->k64, kk, tk, cq, 64, STEP) && make_tile_map(&m->v64, vv, tk, cv, 64, STEP);
+  return make_tile_map(&m->q, q, p.total_q, cq, 64, TILE) &&
+         make_tile_map(&m->dout, dout, p.total_q, cv, 64, TILE) &&
+         make_tile_map(&m->k, kk, tk, cq, 64, TILE) && make_tile_map(&m->v, vv, tk, cv, 64, TILE);
 }
 
 template <int DQK, int DV, int ACT, bool CAUSAL>
@@ -760,7 +790,7 @@ cudaError_t dkdv_t(const Maps& m, const Problem& p, const float2* rowstat, void*
   constexpr uint32_t smem = KvLayout<DQK, DV>::SMEM;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  kern<<<num_sms(), kThreads, smem, s>>>(m.k128, m.v128, m.q64, m.do64, p, rowstat,
+  kern<<<num_sms(), kThreads, smem, s>>>(m.k, m.v, m.q, m.dout, p, rowstat,
                                          (__nv_bfloat16*)dk, (__nv_bfloat16*)dv, ws.hdr, ws.list_k);
   return cudaGetLastError();
 }
@@ -772,7 +802,7 @@ cudaError_t dq_t(const Maps& m, const Problem& p, const float2* rowstat, void* d
   constexpr uint32_t smem = QLayout<DQK, DV>::SMEM;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  kern<<<num_sms(), kThreads, smem, s>>>(m.q128, m.do128, m.k64, m.v64, p, rowstat,
+  kern<<<num_sms(), kThreads, smem, s>>>(m.q, m.dout, m.k, m.v, p, rowstat,
                                          (__nv_bfloat16*)dq, ws.hdr, ws.list_q);
   return cudaGetLastError();
 }
@@ -833,7 +863,7 @@ cudaError_t launch_tc_dkdv(const Problem& p, const void* q, const void* k, const
                            const Workspace& ws, cudaStream_t s) {
   (void)lse;
   Maps m;
-  if (!make_maps(p, q, k, v, dout, true, &m)) return cudaErrorInvalidValue;
+  if (!make_maps(p, q, k, v, dout, &m)) return cudaErrorInvalidValue;
   const float2* rs = reinterpret_cast<const float2*>(ws.drow);
   JFA_TC_BWD_DISPATCH(dkdv_t, m, p, rs, dk, dv, ws, s);
 }
@@ -843,7 +873,7 @@ cudaError_t launch_tc_dq(const Problem& p, const void* q, const void* k, const v
                          cudaStream_t s) {
   (void)lse;
   Maps m;
-  if (!make_maps(p, q, k, v, dout, false, &m)) return cudaErrorInvalidValue;
+  if (!make_maps(p, q, k, v, dout, &m)) return cudaErrorInvalidValue;
   const float2* rs = reinterpret_cast<const float2*>(ws.drow);
   JFA_TC_BWD_DISPATCH(dq_t, m, p, rs, dq, ws, s);
 }

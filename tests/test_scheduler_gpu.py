@@ -89,8 +89,8 @@ def test_tensor_core_lists(causal, seed):
     jfa.jfa_bwd(batch["q"], batch["k"], batch["v"], o, lse, batch["do"], oq, causal=causal, ws=ws)
     st, got_q, got_k = read_lists(ws, len(lq), int(oq[-1]), int(oq[-1]), H)
     assert st == 0
-    assert got_q == with_rows(expected(list(lq), list(lq), H, 128, 64, causal, False), lq, lq)
-    assert got_k == with_rows(expected(list(lq), list(lq), H, 128, 64, causal, True), lq, lq)
+    assert got_q == with_rows(expected(list(lq), list(lq), H, 128, 128, causal, False), lq, lq)
+    assert got_k == with_rows(expected(list(lq), list(lq), H, 128, 128, causal, True), lq, lq)
 
 
 def test_cuda_core_lists_cross():
