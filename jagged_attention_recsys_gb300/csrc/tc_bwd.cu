@@ -76,13 +76,7 @@ rowstat_kernel(int64_t total, int heads, const __nv_bfloat16* __restrict__ o,
 
 // Shared pieces ---------------------------------------------------------------
 __device__ __forceinline__ void store_row_bf16(__nv_bfloat16* dst, const float* x, float f) {
-  uint4* d = reinterpret_cast<uint4*>(dst);
-#pragma unroll
-  for (int t = 0; t < 4; ++t) {
-    const float* y = x + 8 * t;
-    d[t] = make_uint4(pack_bf16(y[0] * f, y[1] * f), pack_bf16(y[2] * f, y[3] * f),
-                      pack_bf16(y[4] * f, y[5] * f), pack_bf16(y[6] * f, y[7] * f));
-  }
+  store32_bf16(dst, x, f);
 }
 
 // =============================================================================
@@ -265,28 +259,38 @@ tc_dkdv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
         tc_fence_after();
         const uint32_t k_tile = sb + L::K_OFF + ks * L::K_BYTES;
         const uint32_t v_tile = sb + L::V_OFF + ks * L::V_BYTES;
-        for (int j = 0; j < n; ++j, ++q_it, ++s_it) {
-          const uint32_t st = q_it % NQ;
-          const uint32_t q_tile = sb + L::Q_OFF + st * L::Q_BYTES;
-          const uint32_t o_tile = sb + L::O_OFF + st * L::O_BYTES;
-          if (!mbar_wait(bar(KV_QFULL + st), (q_it / NQ) & 1, abort, status)) { ok = false; break; }
-          tc_fence_after();
-          // S^T = K Q^T, then dP^T = V dO^T
+        auto q_tile = [&](uint32_t st) { return sb + L::Q_OFF + st * L::Q_BYTES; };
+        auto o_tile = [&](uint32_t st) { return sb + L::O_OFF + st * L::O_BYTES; };
+        auto issue_s = [&](uint32_t st) {  // S^T = K Q^T
 #pragma unroll
           for (int kk = 0; kk < DQK / 16; ++kk) {
             const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-            mma_bf16(tmem + T_S, sw128_desc(k_tile + off, 16, 1024), sw128_desc(q_tile + off, 16, 1024),
+            mma_bf16(tmem + T_S, sw128_desc(k_tile + off, 16, 1024), sw128_desc(q_tile(st) + off, 16, 1024),
                      idesc_s, kk > 0 ? 1u : 0u);
           }
           mma_commit(bar(KV_SFULL));
+        };
+        auto issue_dp = [&](uint32_t st) {  // dP^T = V dO^T
 #pragma unroll
           for (int kk = 0; kk < DV / 16; ++kk) {
             const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-            mma_bf16(tmem + T_DP, sw128_desc(v_tile + off, 16, 1024), sw128_desc(o_tile + off, 16, 1024),
+            mma_bf16(tmem + T_DP, sw128_desc(v_tile + off, 16, 1024), sw128_desc(o_tile(st) + off, 16, 1024),
                      idesc_s, kk > 0 ? 1u : 0u);
           }
           mma_commit(bar(KV_DPFULL));
-          if (j == n - 1) mma_commit(bar(KV_KVEMPTY + ks));
+        };
+        // Issue order per step j (in-order tensor pipe):
+        //   dV(j) [needs P(j)], S(j+1), dK(j) [needs dS(j)], dP(j+1)
+        // so that P(j+1) is computed while dK(j) and dP(j+1) run.
+        const uint32_t q_base = q_it;
+        if (!mbar_wait(bar(KV_QFULL + q_base % NQ), (q_base / NQ) & 1, abort, status)) break;
+        tc_fence_after();
+        issue_s(q_base % NQ);
+        issue_dp(q_base % NQ);
+        if (n == 1) mma_commit(bar(KV_KVEMPTY + ks));
+        for (int j = 0; j < n; ++j, ++s_it) {
+          const uint32_t st = (q_base + j) % NQ;
+          const uint32_t st1 = (q_base + j + 1) % NQ;
           // dV += P^T dO (P^T packed in TMEM: query columns 0..63 at +0, 64..127 at +64)
           if (!mbar_wait(bar(KV_PFULL), s_it & 1, abort, status) ||
               (j == 0 && !mbar_wait(bar(KV_ACCEMPTY), (a_it & 1) ^ 1, abort, status))) {
@@ -297,19 +301,32 @@ tc_dkdv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
 #pragma unroll
           for (int kk = 0; kk < STEP / 16; ++kk)
             mma_bf16_tmem_a(tmem + T_DV, tmem + T_S + (kk >> 2) * 64 + (kk & 3) * 8,
-                            sw128_desc(o_tile + kk * 2048, 16384, 1024), idesc_dv,
+                            sw128_desc(o_tile(st) + kk * 2048, 16384, 1024), idesc_dv,
                             (j > 0 || kk > 0) ? 1u : 0u);
+          if (j + 1 < n) {
+            const uint32_t q1 = q_base + j + 1;
+            if (!mbar_wait(bar(KV_QFULL + st1), (q1 / NQ) & 1, abort, status)) { ok = false; break; }
+            tc_fence_after();
+            issue_s(st1);
+          }
           // dK += dS^T Q
           if (!mbar_wait(bar(KV_DSFULL), s_it & 1, abort, status)) { ok = false; break; }
           tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < STEP / 16; ++kk)
             mma_bf16_tmem_a(tmem + T_DK, tmem + T_DP + (kk >> 2) * 64 + (kk & 3) * 8,
-                            sw128_desc(q_tile + kk * 2048, 16384, 1024), idesc_dk,
+                            sw128_desc(q_tile(st) + kk * 2048, 16384, 1024), idesc_dk,
                             (j > 0 || kk > 0) ? 1u : 0u);
           mma_commit(bar(KV_QEMPTY + st));
-          if (j == n - 1) mma_commit(bar(KV_ACCFULL));
+          if (j + 1 < n) {
+            issue_dp(st1);
+            if (j + 2 == n) mma_commit(bar(KV_KVEMPTY + ks));  // last S / dP of this K/V tile
+          } else {
+            mma_commit(bar(KV_ACCFULL));
+          }
         }
+        if (!ok) break;
+        q_it += n;
         ++kv_it;
         ++a_it;
       }

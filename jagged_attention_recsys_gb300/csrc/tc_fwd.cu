@@ -374,15 +374,7 @@ tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         for (int c = 0; c < DV / 32; ++c) {
           tmem_ld32(s_tm + 128 + 32 * c, ov);
           tmem_wait_ld();
-          if (row_ok) {
-            uint4* dst = reinterpret_cast<uint4*>(out + orow * DV + 32 * c);
-#pragma unroll
-            for (int t = 0; t < 4; ++t) {
-              const float* x = ov + 8 * t;
-              dst[t] = make_uint4(pack_bf16(x[0] * norm, x[1] * norm), pack_bf16(x[2] * norm, x[3] * norm),
-                                  pack_bf16(x[4] * norm, x[5] * norm), pack_bf16(x[6] * norm, x[7] * norm));
-            }
-          }
+          if (row_ok) store32_bf16(out + orow * DV + 32 * c, ov, norm);
         }
         tc_fence_before();
         mbar_arrive(bar(B_OEMPTY + slot));

@@ -5,6 +5,7 @@
 #pragma once
 
 #include <cuda.h>
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -257,6 +258,26 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   uint32_t r;
   asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
   return r;
+}
+// 32-byte global store (dst must be 32-byte aligned)
+__device__ __forceinline__ void st_global_v8(void* dst, const uint32_t* r) {
+  asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(dst), "r"(r[0]),
+               "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
+               : "memory");
+}
+// 32 floats times f as bf16 to dst: 32-byte stores when dst is 32-byte aligned
+__device__ __forceinline__ void store32_bf16(__nv_bfloat16* dst, const float* x, float f) {
+  uint32_t w[16];
+#pragma unroll
+  for (int t = 0; t < 16; ++t) w[t] = pack_bf16(x[2 * t] * f, x[2 * t + 1] * f);
+  if ((reinterpret_cast<uintptr_t>(dst) & 31) == 0) {
+    st_global_v8(dst, w);
+    st_global_v8(dst + 16, w + 8);
+  } else {
+    uint4* d = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+    for (int t = 0; t < 4; ++t) d[t] = make_uint4(w[4 * t], w[4 * t + 1], w[4 * t + 2], w[4 * t + 3]);
+  }
 }
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
                                              uint32_t d) {
