@@ -6,27 +6,25 @@
 // specialised warps; Generalized Dot-Product Attention bullet: the same
 // pipeline with a non-softmax activation (here SiLU(s)/L).
 //
-// One persistent CTA per SM walks the scheduler's heavy-first list of items;
-// an item is a PAIR of adjacent 128-row q-tiles of one (sequence, head),
-// held in two slots that share every K/V tile:
-//   warps 0..3  softmax warpgroup of slot 0, one query row per thread (TMEM lane)
-//   warps 4..7  softmax warpgroup of slot 1
-//   warp 8      TMA producer: both Q tiles once per item, K and V tiles of 128
-//               keys into an NS-stage ring, straight from the jagged [T, H*D]
-//               buffers (rows past a sequence belong to its neighbour and are
-//               masked; rows past the buffer are zero-filled by TMA)
-//   warp 9      TMEM owner and MMA issuer (one lane).  Per key step j it issues,
-//               slot by slot, O_s += P_s(j-1) V(j-1) and S_s(j) = Q_s K(j)^T, so
-//               the tensor pipe works on one slot while the other slot's
-//               warpgroup turns its S into P (ping-pong).
-// Softmax warpgroup, per step: tcgen05.ld of its S row, scale to log2 units,
-// subtract a finite shift from masked columns, online max with lazy rescaling
-// of O (only when the running max grows by more than 2^8), exp2, row sum,
-// and P as packed bf16 back into TMEM over the S columns; the PV product reads
-// P straight from TMEM.  Epilogue: O / l -> bf16, lse = (m + log2 l) ln 2.
-// TMEM per slot s: S (and P) at columns [256 s, 256 s + 128), O at
-// [256 s + 128, 256 s + 128 + Dv).  MMAs issued by one thread execute in
-// order, so S_s(j) overwriting P_s(j-1) is ordered after the PV that reads it.
+// One persistent CTA per SM walks the scheduler's heavy-first list of
+// (sequence, head, 128-row q-tile) items.  Warp roles:
+//   warps 0..3  softmax warpgroup 0: key columns [0,64) of every 128-key step
+//   warps 4..7  softmax warpgroup 1: key columns [64,128)
+//               (one query row per thread = TMEM lane; the two threads of a
+//               row exchange their partial row maximum through shared memory)
+//   warp 8      TMA producer: Q (double-buffered across items) and K / V tiles
+//               of 128 keys in separate rings, straight from the jagged
+//               [T, H*D] buffers (rows past a sequence belong to its neighbour
+//               and are masked; rows past the buffer are zero-filled by TMA)
+//   warp 9      TMEM owner and MMA issuer (one lane)
+// TMEM: S double-buffered at columns [0,128) and [128,256), O at [256, 256+Dv),
+// P (packed bf16, 128 keys) at [384, 448).  Because P has its own columns,
+// S(j+2) is issued as soon as the softmax warps have loaded S(j), and S is
+// always ready before the softmax needs it; the PV product of step j is issued
+// when P(j) is in TMEM.  Per step the softmax warpgroups scale to log2 units,
+// subtract a finite shift from masked columns, keep an online max with lazy
+// rescaling of O (only when it grows by more than 2^8), take exp2 and the row
+// sum, and write P.  Epilogue: O / l -> bf16, lse = (m + log2 l) ln 2.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
@@ -41,9 +39,9 @@ namespace jfa {
 namespace {
 using namespace tc;
 
-constexpr int BM = 128;          // rows per slot (MMA M)
-constexpr int BN = 128;          // keys per step (MMA N of S)
-constexpr int kPair = 2 * BM;    // rows per item
+constexpr int BM = 128;     // rows per item (MMA M)
+constexpr int BN = 128;     // keys per step (MMA N of S)
+constexpr int HC = BN / 2;  // key columns per softmax warpgroup
 constexpr int kThreads = 320;
 constexpr int kProducerWarp = 8, kMmaWarp = 9;
 constexpr float kLog2e = 1.4426950408889634f;
@@ -52,25 +50,34 @@ constexpr float kRescaleLog2 = 8.0f;
 
 template <int DQK, int DV>
 struct FwdLayout {
-  // K tiles are consumed one step before V tiles, so they get the deeper ring.
+  // K tiles are consumed two steps before V tiles, so they get the deeper ring.
+  // At Dqk = Dv = 128 the Q tile is single-buffered: the next item's Q still has the
+  // last three PV products of the current item to arrive in.
+  static constexpr int NQB = (DQK == 128 && DV == 128) ? 1 : 2;
   static constexpr int NK = DQK == 64 ? 4 : 3;
-  static constexpr int NV = DV == 64 ? 4 : (DQK == 64 ? 3 : 2);
+  static constexpr int NV = DV == 64 ? (DQK == 64 ? 4 : 3) : (DQK == 64 ? 3 : 2);
   static constexpr uint32_t Q_BYTES = DQK / 64 * 16384;  // one 128-row tile
   static constexpr uint32_t K_BYTES = DQK / 64 * 16384;
   static constexpr uint32_t V_BYTES = DV / 64 * 16384;
-  static constexpr uint32_t Q_OFF = 0;                    // 2 slots
-  static constexpr uint32_t K_OFF = Q_OFF + 2 * Q_BYTES;  // NK stages
+  static constexpr uint32_t Q_OFF = 0;                      // NQB buffers
+  static constexpr uint32_t K_OFF = Q_OFF + NQB * Q_BYTES;  // NK stages
   static constexpr uint32_t V_OFF = K_OFF + NK * K_BYTES; // NV stages
-  static constexpr uint32_t BAR_OFF = V_OFF + NV * V_BYTES;
-  // at least 120 KB so that exactly one CTA (which owns all of TMEM) fits per SM
-  static constexpr uint32_t SMEM = (BAR_OFF + 512 + 1024) > 122880u ? (BAR_OFF + 512 + 1024) : 122880u;
+  static constexpr uint32_t RED_OFF = V_OFF + NV * V_BYTES;  // row-max / row-sum exchange
+  static constexpr uint32_t RED_BYTES = 2 * BM * 2 * 4;
+  static constexpr uint32_t BAR_OFF = RED_OFF + RED_BYTES;
+  // 1 KB of slack to align the base for the 128-byte swizzle; at least 120 KB so
+  // that exactly one CTA (which owns all of TMEM) fits per SM.
+  static constexpr uint32_t SMEM = (BAR_OFF + 256 + 1024) > 122880u ? (BAR_OFF + 256 + 1024) : 122880u;
+  static_assert(SMEM <= 232448u, "forward tiles exceed the shared memory of one CTA");
 };
 
 // mbarrier slots (the K and V rings have up to 4 stages each)
 enum : uint32_t {
-  B_QFULL = 0, B_QEMPTY = 1, B_KFULL = 2, B_KEMPTY = 6, B_VFULL = 10, B_VEMPTY = 14,
-  B_SFULL = 18, B_PFULL = 20, B_OFULL = 22, B_OEMPTY = 24, B_COUNT = 26
+  B_QFULL = 0, B_QEMPTY = 2, B_KFULL = 4, B_KEMPTY = 8, B_VFULL = 12, B_VEMPTY = 16,
+  B_SFULL = 20, B_SEMPTY = 22, B_PFULL = 24, B_PEMPTY = 25, B_OFULL = 26, B_OEMPTY = 27,
+  B_RED = 28, B_REDL = 30, B_COUNT = 32  // B_REDL: two barriers
 };
+constexpr uint32_t T_S0 = 0, T_S1 = 128, T_O = 256, T_P = 384;
 
 template <int DQK, int DV, int ACT, bool CAUSAL>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -92,8 +99,12 @@ tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
   const int n_items = hdr->n_q;
 
   if (threadIdx.x == 0) {
-    mbar_init(bar(B_QFULL), 1);
-    mbar_init(bar(B_QEMPTY), 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(bar(B_QFULL + s), 1);
+      mbar_init(bar(B_QEMPTY + s), 1);
+      mbar_init(bar(B_SFULL + s), 1);
+      mbar_init(bar(B_SEMPTY + s), 256);
+    }
     for (int s = 0; s < NK; ++s) {
       mbar_init(bar(B_KFULL + s), 1);
       mbar_init(bar(B_KEMPTY + s), 1);
@@ -102,12 +113,15 @@ tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
       mbar_init(bar(B_VFULL + s), 1);
       mbar_init(bar(B_VEMPTY + s), 1);
     }
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(bar(B_SFULL + s), 1);
-      mbar_init(bar(B_PFULL + s), 128);
-      mbar_init(bar(B_OFULL + s), 1);
-      mbar_init(bar(B_OEMPTY + s), 128);
-    }
+    mbar_init(bar(B_PFULL), 256);
+    mbar_init(bar(B_PEMPTY), 1);
+    mbar_init(bar(B_OFULL), 1);
+    mbar_init(bar(B_OEMPTY), 256);
+    // exchanges between the two softmax warpgroups (bounded waits, never bar.sync)
+    mbar_init(bar(B_RED), 256);
+    mbar_init(bar(B_RED + 1), 256);
+    mbar_init(bar(B_REDL), 256);
+    mbar_init(bar(B_REDL + 1), 256);
     *abort = 0;
     fence_mbar_init();
   }
@@ -125,45 +139,46 @@ tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
       tma_prefetch_desc(&tm_v);
       uint32_t k_it = 0, v_it = 0, q_it = 0;
       bool ok = true;
+      auto load_k = [&](const WorkItem& w, int j) {
+        const uint32_t st = k_it % NK;
+        if (!mbar_wait(bar(B_KEMPTY + st), ((k_it / NK) & 1) ^ 1, abort, status)) return false;
+        mbar_expect_tx(bar(B_KFULL + st), L::K_BYTES);
+#pragma unroll
+        for (int a = 0; a < DQK / 64; ++a)
+          tma_load_2d(sb + L::K_OFF + st * L::K_BYTES + a * 16384, &tm_k, w.h * DQK + a * 64,
+                      w.k0 + j * BN, bar(B_KFULL + st));
+        ++k_it;
+        return true;
+      };
+      auto load_v = [&](const WorkItem& w, int j) {
+        const uint32_t st = v_it % NV;
+        if (!mbar_wait(bar(B_VEMPTY + st), ((v_it / NV) & 1) ^ 1, abort, status)) return false;
+        mbar_expect_tx(bar(B_VFULL + st), L::V_BYTES);
+#pragma unroll
+        for (int a = 0; a < DV / 64; ++a)
+          tma_load_2d(sb + L::V_OFF + st * L::V_BYTES + a * 16384, &tm_v, w.h * DV + a * 64,
+                      w.k0 + j * BN, bar(B_VFULL + st));
+        ++v_it;
+        return true;
+      };
       WorkItem nxt = blockIdx.x < (unsigned)n_items ? load_item(list, blockIdx.x) : WorkItem{};
       for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
         const WorkItem w = nxt;  // prefetched one item ahead
         if (it + (int)gridDim.x < n_items) nxt = load_item(list, it + gridDim.x);
         const int n = w.cost;
         if (n == 0) continue;
-        const int h = w.h, row0 = w.tile * kPair;
-        const bool two = row0 + BM < w.lq;
-        if (!mbar_wait(bar(B_QEMPTY), (q_it & 1) ^ 1, abort, status)) break;
-        mbar_expect_tx(bar(B_QFULL), (two ? 2u : 1u) * L::Q_BYTES);
-        for (int s = 0; s < (two ? 2 : 1); ++s) {
+        const uint32_t qs = q_it % L::NQB;
+        if (!mbar_wait(bar(B_QEMPTY + qs), ((q_it / L::NQB) & 1) ^ 1, abort, status)) break;
+        mbar_expect_tx(bar(B_QFULL + qs), L::Q_BYTES);
 #pragma unroll
-          for (int a = 0; a < DQK / 64; ++a)
-            tma_load_2d(sb + L::Q_OFF + s * L::Q_BYTES + a * 16384, &tm_q, h * DQK + a * 64,
-                        w.q0 + row0 + s * BM, bar(B_QFULL));
-        }
+        for (int a = 0; a < DQK / 64; ++a)
+          tma_load_2d(sb + L::Q_OFF + qs * L::Q_BYTES + a * 16384, &tm_q, w.h * DQK + a * 64,
+                      w.q0 + w.tile * BM, bar(B_QFULL + qs));
         ++q_it;
-        // K(j) is needed one step before V(j): issue K(j), then V(j-1)
-        for (int j = 0; j <= n && ok; ++j) {
-          if (j < n) {
-            const uint32_t st = k_it % NK;
-            if (!mbar_wait(bar(B_KEMPTY + st), ((k_it / NK) & 1) ^ 1, abort, status)) { ok = false; break; }
-            mbar_expect_tx(bar(B_KFULL + st), L::K_BYTES);
-#pragma unroll
-            for (int a = 0; a < DQK / 64; ++a)
-              tma_load_2d(sb + L::K_OFF + st * L::K_BYTES + a * 16384, &tm_k, h * DQK + a * 64,
-                          w.k0 + j * BN, bar(B_KFULL + st));
-            ++k_it;
-          }
-          if (j > 0) {
-            const uint32_t st = v_it % NV;
-            if (!mbar_wait(bar(B_VEMPTY + st), ((v_it / NV) & 1) ^ 1, abort, status)) { ok = false; break; }
-            mbar_expect_tx(bar(B_VFULL + st), L::V_BYTES);
-#pragma unroll
-            for (int a = 0; a < DV / 64; ++a)
-              tma_load_2d(sb + L::V_OFF + st * L::V_BYTES + a * 16384, &tm_v, h * DV + a * 64,
-                          w.k0 + (j - 1) * BN, bar(B_VFULL + st));
-            ++v_it;
-          }
+        // the MMA lane consumes K(j+2) before V(j): load in that order
+        for (int j = 0; j < n + 2 && ok; ++j) {
+          if (j < n) ok = load_k(w, j);
+          if (ok && j >= 2) ok = load_v(w, j - 2);
         }
       }
     }
@@ -173,8 +188,7 @@ tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     if (lane == 0) {
       constexpr uint32_t idesc_s = idesc_bf16(BM, BN, 0, 0);
       constexpr uint32_t idesc_o = idesc_bf16(BM, DV, 0, 1);
-      uint32_t k_it = 0, v_it = 0, q_it = 0;
-      uint32_t s_cnt[2] = {0, 0}, o_cnt[2] = {0, 0};
+      uint32_t k_it = 0, v_it = 0, q_it = 0, s_it = 0, p_it = 0, o_it = 0;
       bool ok = true;
       WorkItem nxt = blockIdx.x < (unsigned)n_items ? load_item(list, blockIdx.x) : WorkItem{};
       for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
@@ -182,123 +196,115 @@ tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         if (it + (int)gridDim.x < n_items) nxt = load_item(list, it + gridDim.x);
         const int n = w.cost;
         if (n == 0) continue;
-        const int row0 = w.tile * kPair;
-        const bool two = row0 + BM < w.lq;
-        // key steps of each slot: slot 1 needs n, slot 0 one fewer on the causal diagonal
-        int ns[2];
-        ns[0] = CAUSAL ? min(n, (min(w.lk, row0 + BM) + BN - 1) / BN) : n;
-        ns[1] = two ? n : 0;
-        if (!mbar_wait(bar(B_QFULL), q_it & 1, abort, status)) break;
+        const uint32_t qs = q_it % L::NQB;
+        if (!mbar_wait(bar(B_QFULL + qs), (q_it / L::NQB) & 1, abort, status)) break;
         tc_fence_after();
-        for (int j = 0; j <= n && ok; ++j) {
-          const uint32_t kst = k_it % NK, vst = v_it % NV;
-          if (j < n) {
-            if (!mbar_wait(bar(B_KFULL + kst), (k_it / NK) & 1, abort, status)) { ok = false; break; }
-            tc_fence_after();
-          }
-          if (j > 0) {
-            if (!mbar_wait(bar(B_VFULL + vst), (v_it / NV) & 1, abort, status)) { ok = false; break; }
-            tc_fence_after();
-          }
+        const uint32_t q_tile = sb + L::Q_OFF + qs * L::Q_BYTES;
+        int next_s = 0;  // step whose S is issued next
+        // S(j) = Q K(j)^T into buffer s_it % 2, once the softmax has loaded S(j-2)
+        auto issue_s = [&]() {
+          const uint32_t b = s_it & 1, kst = k_it % NK;
+          if (!mbar_wait(bar(B_SEMPTY + b), ((s_it >> 1) & 1) ^ 1, abort, status) ||
+              !mbar_wait(bar(B_KFULL + kst), (k_it / NK) & 1, abort, status))
+            return false;
+          tc_fence_after();
 #pragma unroll
-          for (int s = 0; s < 2; ++s) {
-            const uint32_t s_tm = tmem + s * 256;
-            if (j > 0 && j - 1 < ns[s]) {
-              // O_s += P_s(j-1) V(j-1), P read from TMEM
-              if (!mbar_wait(bar(B_PFULL + s), (s_cnt[s] - 1) & 1, abort, status) ||
-                  (j == 1 && !mbar_wait(bar(B_OEMPTY + s), (o_cnt[s] & 1) ^ 1, abort, status))) {
-                ok = false;
-                break;
-              }
-              tc_fence_after();
+          for (int kk = 0; kk < DQK / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+            mma_bf16(tmem + (b ? T_S1 : T_S0), sw128_desc(q_tile + off, 16, 1024),
+                     sw128_desc(sb + L::K_OFF + kst * L::K_BYTES + off, 16, 1024), idesc_s,
+                     kk > 0 ? 1u : 0u);
+          }
+          mma_commit(bar(B_SFULL + b));
+          mma_commit(bar(B_KEMPTY + kst));
+          if (next_s == n - 1) mma_commit(bar(B_QEMPTY + qs));  // last use of this Q tile
+          ++next_s;
+          ++s_it;
+          ++k_it;
+          return true;
+        };
+        ok = issue_s();
+        if (ok && n > 1) ok = issue_s();
+        for (int j = 0; j < n && ok; ++j) {
+          if (next_s < n && !(ok = issue_s())) break;  // S(j+2)
+          // O += P(j) V(j), P read from TMEM
+          const uint32_t vst = v_it % NV;
+          if (!mbar_wait(bar(B_PFULL), p_it & 1, abort, status) ||
+              !mbar_wait(bar(B_VFULL + vst), (v_it / NV) & 1, abort, status) ||
+              (j == 0 && !mbar_wait(bar(B_OEMPTY), (o_it & 1) ^ 1, abort, status))) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
 #pragma unroll
-              for (int kk = 0; kk < BN / 16; ++kk) {
-                const uint64_t bd = sw128_desc(sb + L::V_OFF + vst * L::V_BYTES + kk * 2048, 16384, 1024);
-                mma_bf16_tmem_a(s_tm + 128, s_tm + kk * 8, bd, idesc_o, (j > 1 || kk > 0) ? 1u : 0u);
-              }
-              if (j == ns[s]) {
-                mma_commit(bar(B_OFULL + s));
-                ++o_cnt[s];
-              }
-            }
-            if (j < ns[s]) {
-              // S_s(j) = Q_s K(j)^T
-#pragma unroll
-              for (int kk = 0; kk < DQK / 16; ++kk) {
-                const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-                const uint64_t ad = sw128_desc(sb + L::Q_OFF + s * L::Q_BYTES + off, 16, 1024);
-                const uint64_t bd = sw128_desc(sb + L::K_OFF + kst * L::K_BYTES + off, 16, 1024);
-                mma_bf16(s_tm, ad, bd, idesc_s, kk > 0 ? 1u : 0u);
-              }
-              mma_commit(bar(B_SFULL + s));
-              ++s_cnt[s];
-            }
+          for (int kk = 0; kk < BN / 16; ++kk) {
+            const uint64_t bd = sw128_desc(sb + L::V_OFF + vst * L::V_BYTES + kk * 2048, 16384, 1024);
+            mma_bf16_tmem_a(tmem + T_O, tmem + T_P + kk * 8, bd, idesc_o, (j > 0 || kk > 0) ? 1u : 0u);
           }
-          if (!ok) break;
-          if (j < n) {
-            mma_commit(bar(B_KEMPTY + kst));  // both slots' S(j) issued
-            if (j == n - 1) mma_commit(bar(B_QEMPTY));
-            ++k_it;
-          }
-          if (j > 0) {
-            mma_commit(bar(B_VEMPTY + vst));  // both slots' PV(j-1) issued
-            ++v_it;
-          }
+          mma_commit(bar(B_PEMPTY));
+          mma_commit(bar(B_VEMPTY + vst));
+          ++p_it;
+          ++v_it;
         }
+        if (!ok) break;
+        mma_commit(bar(B_OFULL));
+        ++o_it;
         ++q_it;
       }
     }
     __syncwarp();
   } else {
     // ------------------------------------------------------------ softmax warpgroups
-    const int slot = warp >> 2;
-    const int r = 32 * (warp & 3) + lane;  // TMEM lane = row of the slot's tile
+    const int half = warp >> 2;            // key columns [half*64, half*64+64) of each step
+    const int r = 32 * (warp & 3) + lane;  // TMEM lane = row of the tile
     const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
-    const uint32_t s_tm = tmem + slot * 256 + lane_base;
     const float c_score = ACT == kActSoftmax ? p.scale * kLog2e : p.scale;
     const float shift_raw = kMaskShift / c_score;  // masked raw scores land kMaskShift lower
-    uint32_t s_cnt = 0, o_cnt = 0;
+    float* red = reinterpret_cast<float*>(smem + L::RED_OFF);  // [2 steps][128 rows][2], then [128][2]
+    uint32_t s_it = 0, p_it = 0, o_it = 0, l_it = 0;
     bool ok = true;
     WorkItem nxt = blockIdx.x < (unsigned)n_items ? load_item(list, blockIdx.x) : WorkItem{};
     for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
       const WorkItem w = nxt;
       if (it + (int)gridDim.x < n_items) nxt = load_item(list, it + gridDim.x);
       const int n = w.cost, h = w.h;
-      const int row0 = w.tile * kPair + slot * BM;  // first row of this slot's tile
-      if (row0 >= w.lq) continue;                   // slot empty for this item
       const int Lq = w.lq, Lk = w.lk;
-      const int ns = (slot == 0 && CAUSAL) ? min(n, (min(Lk, row0 + BM) + BN - 1) / BN) : n;
-      const int i = row0 + r;
+      const int i = w.tile * BM + r;
       const float inv_len = 1.0f / (float)max(Lq, 1);
       float m = -INFINITY, l = 0.f;
-      for (int j = 0; j < ns; ++j) {
-        if (!mbar_wait(bar(B_SFULL + slot), s_cnt & 1, abort, status)) { ok = false; break; }
-        ++s_cnt;
+      for (int j = 0; j < n; ++j, ++s_it, ++p_it) {
+        const uint32_t b = s_it & 1;
+        if (!mbar_wait(bar(B_SFULL + b), (s_it >> 1) & 1, abort, status)) { ok = false; break; }
         tc_fence_after();
-        float sv[BN];
-#pragma unroll
-        for (int c = 0; c < BN / 32; ++c) tmem_ld32(s_tm + 32 * c, sv + 32 * c);
+        const uint32_t s_tm = tmem + lane_base + (b ? T_S1 : T_S0) + half * HC;
+        float sv[HC];
+        tmem_ld32(s_tm, sv);
+        tmem_ld32(s_tm + 32, sv + 32);
         tmem_wait_ld();
-        const int kb = j * BN;
+        tc_fence_before();
+        mbar_arrive(bar(B_SEMPTY + b));  // S buffer free for S(j+2)
+        const int kb = j * BN + half * HC;
         int nvalid = Lk - kb;
         if (CAUSAL) nvalid = min(nvalid, i - kb + 1);
-        float alpha = 1.f;  // rescale factor of O for this step (softmax only)
-        bool rescale = false;
-        if (nvalid < BN) {
-          // partial tile: move masked raw scores down by a finite shift (in raw units,
-          // so that after scaling the shift is kMaskShift)
+        if (nvalid < HC) {
 #pragma unroll
-          for (int k = 0; k < BN; ++k) sv[k] -= k < nvalid ? 0.f : shift_raw;
+          for (int k = 0; k < HC; ++k) sv[k] -= k < nvalid ? 0.f : shift_raw;
         }
+        float alpha = 1.f;
+        bool rescale = false;
         if (ACT == kActSoftmax) {
-          // row max of the raw scores (scale > 0), two independent 3-input chains
+          // row max of the raw scores (scale > 0): partial over this half, then exchanged
           float m0 = fmaxf(sv[0], sv[1]), m1 = fmaxf(sv[2], sv[3]);
 #pragma unroll
-          for (int k = 4; k < BN; k += 4) {  // BN is a multiple of 4: last group is BN-4..BN-1
+          for (int k = 4; k < HC; k += 4) {  // HC is a multiple of 4
             m0 = fmax3(m0, sv[k], sv[k + 1]);
             m1 = fmax3(m1, sv[k + 2], sv[k + 3]);
           }
-          const float mt = fmaxf(m0, m1) * c_score;
+          float* rb = red + (p_it & 1) * (BM * 2);
+          rb[r * 2 + half] = fmaxf(m0, m1);
+          mbar_arrive(bar(B_RED + (p_it & 1)));
+          if (!mbar_wait(bar(B_RED + (p_it & 1)), (p_it >> 1) & 1, abort, status)) { ok = false; break; }
+          const float mt = fmaxf(rb[r * 2], rb[r * 2 + 1]) * c_score;
           if (j == 0) {
             m = mt;
           } else {
@@ -312,79 +318,92 @@ tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
           }
           l *= alpha;
         }
-        // P = exp2(s c - m) or SiLU(s c)/L, packed bf16 pairs over the first 64 S
-        // columns, written 64 values at a time so the fp32 scores die as they go.
+        // P = exp2(s c - m) or SiLU(s c)/L as packed bf16 pairs
         const float2 cc = make_float2(c_score, c_score);
         const float2 nm = make_float2(-m, -m);
         const float2 hc = make_float2(0.5f * c_score, 0.5f * c_score);
         const float2 il = make_float2(inv_len, inv_len);
         float2 rs0 = make_float2(0.f, 0.f), rs1 = make_float2(0.f, 0.f);
+        uint32_t pk[HC / 2];
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          uint32_t pk[32];
-#pragma unroll
-          for (int c = 0; c < 32; ++c) {
-            const float2 x = make_float2(sv[half * 64 + 2 * c], sv[half * 64 + 2 * c + 1]);
-            float2 pv;
-            if (ACT == kActSoftmax) {
-              const float2 e = ffma2(x, cc, nm);
-              pv = make_float2(ex2(e.x), ex2(e.y));
-              if (c & 1) rs1 = fadd2(rs1, pv); else rs0 = fadd2(rs0, pv);
-            } else {
-              // SiLU(u)/L with u = s c: h = u/2, P = h (1 + tanh h) / L
-              const float2 hh = fmul2(x, hc);
-              const float2 t = make_float2(tanh_approx(hh.x), tanh_approx(hh.y));
-              pv = fmul2(hh, ffma2(t, il, il));
-            }
-            pk[c] = pack_bf16(pv.x, pv.y);
+        for (int c = 0; c < HC / 2; ++c) {
+          const float2 x = make_float2(sv[2 * c], sv[2 * c + 1]);
+          float2 pv;
+          if (ACT == kActSoftmax) {
+            const float2 e = ffma2(x, cc, nm);
+            pv = make_float2(ex2(e.x), ex2(e.y));
+            if (c & 1) rs1 = fadd2(rs1, pv); else rs0 = fadd2(rs0, pv);
+          } else {
+            // SiLU(u)/L with u = s c: h = u/2, P = h (1 + tanh h) / L
+            const float2 hh = fmul2(x, hc);
+            const float2 t = make_float2(tanh_approx(hh.x), tanh_approx(hh.y));
+            pv = fmul2(hh, ffma2(t, il, il));
           }
-          tmem_st32(s_tm + 32 * half, reinterpret_cast<const float*>(pk));
+          pk[c] = pack_bf16(pv.x, pv.y);
         }
         if (ACT == kActSoftmax) {
-          const float2 r = fadd2(rs0, rs1);
-          l += r.x + r.y;
+          const float2 rr = fadd2(rs0, rs1);
+          l += rr.x + rr.y;
         }
+        // the P columns and O are free once PV(j-1) has completed
+        if (!mbar_wait(bar(B_PEMPTY), (p_it & 1) ^ 1, abort, status)) { ok = false; break; }
+        tc_fence_after();
         if (rescale) {
-          // O_s already holds every PV issued before this S (in-order MMAs).
           float ov[32];
 #pragma unroll
-          for (int c = 0; c < DV / 32; ++c) {
-            tmem_ld32(s_tm + 128 + 32 * c, ov);
+          for (int c = 0; c < DV / 64; ++c) {
+            const uint32_t o_tm = tmem + lane_base + T_O + half * (DV / 2) + 32 * c;
+            tmem_ld32(o_tm, ov);
             tmem_wait_ld();
 #pragma unroll
             for (int t = 0; t < 32; ++t) ov[t] *= alpha;
-            tmem_st32(s_tm + 128 + 32 * c, ov);
+            tmem_st32(o_tm, ov);
           }
         }
+        tmem_st32(tmem + lane_base + T_P + half * (HC / 2), reinterpret_cast<const float*>(pk));
         tmem_wait_st();
         tc_fence_before();
-        mbar_arrive(bar(B_PFULL + slot));
+        mbar_arrive(bar(B_PFULL));
       }
       if (!ok) break;
       // ---------------------------------------------------------- epilogue
       const bool row_ok = i < Lq;
       const int64_t orow = ((int64_t)w.q0 + i) * p.heads + h;
-      if (ns > 0) {
-        if (!mbar_wait(bar(B_OFULL + slot), o_cnt & 1, abort, status)) { ok = false; break; }
-        ++o_cnt;
-        tc_fence_after();
-        const float norm = ACT == kActSoftmax ? (l > 0.f ? 1.f / l : 0.f) : 1.f;
-        float ov[32];
-#pragma unroll
-        for (int c = 0; c < DV / 32; ++c) {
-          tmem_ld32(s_tm + 128 + 32 * c, ov);
-          tmem_wait_ld();
-          if (row_ok) store32_bf16(out + orow * DV + 32 * c, ov, norm);
+      if (n > 0) {
+        float lt = l;
+        if (ACT == kActSoftmax) {
+          // Row sums are exchanged through the buffer of the item's last step: first
+          // every thread confirms it has read that step's maxima, then the sums go in.
+          float* rl = red + ((p_it - 1) & 1) * (BM * 2);
+          mbar_arrive(bar(B_REDL));
+          if (!mbar_wait(bar(B_REDL), l_it & 1, abort, status)) { ok = false; break; }
+          rl[r * 2 + half] = l;
+          mbar_arrive(bar(B_REDL + 1));
+          if (!mbar_wait(bar(B_REDL + 1), l_it & 1, abort, status)) { ok = false; break; }
+          ++l_it;
+          lt = rl[r * 2] + rl[r * 2 + 1];
         }
-        tc_fence_before();
-        mbar_arrive(bar(B_OEMPTY + slot));
-        if (ACT == kActSoftmax && row_ok && lse != nullptr)
-          lse[orow] = l > 0.f ? (m + log2f(l)) * kLn2 : -INFINITY;
-      } else if (row_ok) {
-        uint4* dst = reinterpret_cast<uint4*>(out + orow * DV);
+        if (!mbar_wait(bar(B_OFULL), o_it & 1, abort, status)) { ok = false; break; }
+        ++o_it;
+        tc_fence_after();
+        float ov[DV / 2];
 #pragma unroll
-        for (int t = 0; t < DV / 8; ++t) dst[t] = make_uint4(0, 0, 0, 0);
-        if (ACT == kActSoftmax && lse != nullptr) lse[orow] = -INFINITY;
+        for (int c = 0; c < DV / 64; ++c) tmem_ld32(tmem + lane_base + T_O + half * (DV / 2) + 32 * c, ov + 32 * c);
+        tmem_wait_ld();
+        tc_fence_before();
+        mbar_arrive(bar(B_OEMPTY));
+        const float norm = ACT == kActSoftmax ? (lt > 0.f ? 1.f / lt : 0.f) : 1.f;
+        if (row_ok) {
+#pragma unroll
+          for (int c = 0; c < DV / 64; ++c) store32_bf16(out + orow * DV + half * (DV / 2) + 32 * c, ov + 32 * c, norm);
+          if (ACT == kActSoftmax && half == 0 && lse != nullptr)
+            lse[orow] = lt > 0.f ? (m + log2f(lt)) * kLn2 : -INFINITY;
+        }
+      } else if (row_ok) {
+        const float z[32] = {0.f};
+#pragma unroll
+        for (int c = 0; c < DV / 64; ++c) store32_bf16(out + orow * DV + half * (DV / 2) + 32 * c, z, 1.f);
+        if (ACT == kActSoftmax && half == 0 && lse != nullptr) lse[orow] = -INFINITY;
       }
     }
   }
@@ -426,8 +445,8 @@ bool tc_supports(int dim_qk, int dim_v) {
   return (dim_qk == 64 || dim_qk == 128) && (dim_v == 64 || dim_v == 128);
 }
 
-// Items are pairs of 128-row q-tiles; the cost is the number of 128-key steps.
-SchedConfig tc_fwd_sched(const Problem&) { return SchedConfig{kPair, BN, BN, BM, 1, 0, 0}; }
+// Items are 128-row q-tiles; the cost is the number of 128-key steps.
+SchedConfig tc_fwd_sched(const Problem&) { return SchedConfig{BM, BN, BN, BM, 1, 0, 0}; }
 
 cudaError_t launch_tc_fwd(const Problem& p, const void* q, const void* k, const void* v, void* o,
                           float* lse, const Workspace& ws, cudaStream_t s) {

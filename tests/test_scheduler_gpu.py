@@ -85,7 +85,7 @@ def test_tensor_core_lists(causal, seed):
     o, lse = jfa.jfa_fwd(batch["q"], batch["k"], batch["v"], oq, causal=causal, ws=ws)
     st, got_q, _ = read_lists(ws, len(lq), int(oq[-1]), int(oq[-1]), H)
     assert st == 0
-    assert got_q == with_rows(expected(list(lq), list(lq), H, 256, 128, causal, False), lq, lq)
+    assert got_q == with_rows(expected(list(lq), list(lq), H, 128, 128, causal, False), lq, lq)
     jfa.jfa_bwd(batch["q"], batch["k"], batch["v"], o, lse, batch["do"], oq, causal=causal, ws=ws)
     st, got_q, got_k = read_lists(ws, len(lq), int(oq[-1]), int(oq[-1]), H)
     assert st == 0
@@ -131,4 +131,4 @@ def test_large_batch_many_rounds(nseq):
     jfa.jfa_fwd(batch["q"], batch["k"], batch["v"], oq, causal=True, ws=ws)
     st, got_q, _ = read_lists(ws, len(lq), int(oq[-1]), int(oq[-1]), H)
     assert st == 0
-    assert got_q == with_rows(expected(list(lq), list(lq), H, 256, 128, True, False), lq, lq)
+    assert got_q == with_rows(expected(list(lq), list(lq), H, 128, 128, True, False), lq, lq)
