@@ -12,16 +12,18 @@
 //   warps 4..7  softmax warpgroup 1: key columns [64,128)
 //               (one query row per thread = TMEM lane; the two threads of a
 //               row exchange their partial row maximum through shared memory)
-//   warp 8      TMA producer: Q (double-buffered across items) and K / V tiles
+//   warp 8      TMA producer: Q (double-buffered across items unless
+//               Dqk = Dv = 128) and K / V tiles
 //               of 128 keys in separate rings, straight from the jagged
 //               [T, H*D] buffers (rows past a sequence belong to its neighbour
 //               and are masked; rows past the buffer are zero-filled by TMA)
 //   warp 9      TMEM owner and MMA issuer (one lane)
 // TMEM: S double-buffered at columns [0,128) and [128,256), O at [256, 256+Dv),
-// P (packed bf16, 128 keys) at [384, 448).  Because P has its own columns,
-// S(j+2) is issued as soon as the softmax warps have loaded S(j), and S is
-// always ready before the softmax needs it; the PV product of step j is issued
-// when P(j) is in TMEM.  Per step the softmax warpgroups scale to log2 units,
+// P (packed bf16, 128 keys) at [384, 448).  MMA issue order per step j: PV(j)
+// as soon as P(j) is in TMEM, then S(j+2) into the buffer that held S(j).  An
+// MMA issue blocks while the tensor pipe is busy, so PV(j) goes first: it
+// releases P to the softmax warps, while S(j+2) is needed only a step later.
+// Per step the softmax warpgroups scale to log2 units,
 // subtract a finite shift from masked columns, keep an online max with lazy
 // rescaling of O (only when it grows by more than 2^8), take exp2 and the row
 // sum, and write P.  Epilogue: O / l -> bf16, lse = (m + log2 l) ln 2.
@@ -42,42 +44,43 @@ using namespace tc;
 constexpr int BM = 128;     // rows per item (MMA M)
 constexpr int BN = 128;     // keys per step (MMA N of S)
 constexpr int HC = BN / 2;  // key columns per softmax warpgroup
-constexpr int kThreads = 320;
-constexpr int kProducerWarp = 8, kMmaWarp = 9;
+constexpr int kThreads = 352;
+constexpr int kProducerWarp = 8, kSWarp = 9, kPvWarp = 10;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleLog2 = 8.0f;
 
 template <int DQK, int DV>
 struct FwdLayout {
-  // K tiles are consumed two steps before V tiles, so they get the deeper ring.
-  // At Dqk = Dv = 128 the Q tile is single-buffered: the next item's Q still has the
-  // last three PV products of the current item to arrive in.
-  static constexpr int NQB = (DQK == 128 && DV == 128) ? 1 : 2;
-  static constexpr int NK = DQK == 64 ? 4 : 3;
-  static constexpr int NV = DV == 64 ? (DQK == 64 ? 4 : 3) : (DQK == 64 ? 3 : 2);
   static constexpr uint32_t Q_BYTES = DQK / 64 * 16384;  // one 128-row tile
-  static constexpr uint32_t K_BYTES = DQK / 64 * 16384;
+  static constexpr uint32_t K_BYTES = DQK / 64 * 16384;  // one 128-key tile
   static constexpr uint32_t V_BYTES = DV / 64 * 16384;
-  static constexpr uint32_t Q_OFF = 0;                      // NQB buffers
-  static constexpr uint32_t K_OFF = Q_OFF + NQB * Q_BYTES;  // NK stages
-  static constexpr uint32_t V_OFF = K_OFF + NK * K_BYTES; // NV stages
-  static constexpr uint32_t RED_OFF = V_OFF + NV * V_BYTES;  // row-max / row-sum exchange
+  // In front of the tiles: mbarriers, TMEM slot and abort flag (384 bytes), then the
+  // row statistics exchanged by the two softmax warpgroups ([2 steps][128 rows][2]).
+  static constexpr uint32_t RED_OFF = 384;
   static constexpr uint32_t RED_BYTES = 2 * BM * 2 * 4;
-  static constexpr uint32_t BAR_OFF = RED_OFF + RED_BYTES;
-  // 1 KB of slack to align the base for the 128-byte swizzle; at least 120 KB so
-  // that exactly one CTA (which owns all of TMEM) fits per SM.
-  static constexpr uint32_t SMEM = (BAR_OFF + 256 + 1024) > 122880u ? (BAR_OFF + 256 + 1024) : 122880u;
-  static_assert(SMEM <= 232448u, "forward tiles exceed the shared memory of one CTA");
+  static constexpr uint32_t SMALL = RED_OFF + RED_BYTES;
+  static constexpr uint32_t TILE0 = (SMALL + 1023) / 1024 * 1024;  // for a 1 KB-aligned base
+  static constexpr uint32_t kMaxSmem = 232448;
+  // Q is single-buffered at Dqk = Dv = 128; the K and V rings take the rest.
+  static constexpr int NQB = (DQK == 128 && DV == 128) ? 1 : 2;
+  static constexpr int NK = DQK == 64 ? (DV == 64 ? 6 : 4) : 3;
+  static constexpr int NV = DV == 64 ? (DQK == 64 ? 6 : 4) : (DQK == 64 ? 4 : 3);
+  static constexpr uint32_t Q_OFF = 0;  // offsets from the 1 KB-aligned tile base
+  static constexpr uint32_t K_OFF = Q_OFF + NQB * Q_BYTES;
+  static constexpr uint32_t V_OFF = K_OFF + NK * K_BYTES;
+  static constexpr uint32_t TILES = V_OFF + NV * V_BYTES;
+  static constexpr uint32_t SMEM = TILE0 + TILES;
+  static_assert(SMEM <= kMaxSmem, "forward tiles exceed the shared memory of one CTA");
+  static_assert(SMEM >= 122880u, "one CTA per SM: it owns all of TMEM");
 };
 
-// mbarrier slots (the K and V rings have up to 4 stages each)
 enum : uint32_t {
-  B_QFULL = 0, B_QEMPTY = 2, B_KFULL = 4, B_KEMPTY = 8, B_VFULL = 12, B_VEMPTY = 16,
-  B_SFULL = 20, B_SEMPTY = 22, B_PFULL = 24, B_PEMPTY = 25, B_OFULL = 26, B_OEMPTY = 27,
-  B_RED = 28, B_REDL = 30, B_COUNT = 32  // B_REDL: two barriers
+  B_QFULL = 0, B_QEMPTY = 2, B_KFULL = 4, B_KEMPTY = 10, B_VFULL = 16, B_VEMPTY = 22,
+  B_SFULL = 28, B_PFULL = 30, B_PEMPTY = 32, B_OFULL = 34, B_OEMPTY = 35, B_RED = 36, B_REDL = 38,
+  B_COUNT = 40
 };
-constexpr uint32_t T_S0 = 0, T_S1 = 128, T_O = 256, T_P = 384;
+constexpr uint32_t T_S = 0, T_O = 256, T_P = 384;  // S: 2 x 128 columns; P: 2 x 64 columns
 
 template <int DQK, int DV, int ACT, bool CAUSAL>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -88,13 +91,18 @@ tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
   using L = FwdLayout<DQK, DV>;
   constexpr int NK = L::NK, NV = L::NV;
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-  const uint32_t sb = smem_u32(smem);
-  const uint32_t bar0 = sb + L::BAR_OFF;
-  auto bar = [&](uint32_t i) { return bar0 + 8u * i; };
-  uint32_t* tmem_slot = (uint32_t*)(smem + L::BAR_OFF + 8 * B_COUNT);
-  volatile int* abort = (volatile int*)(smem + L::BAR_OFF + 8 * B_COUNT + 4);
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t sb = (raw + L::SMALL + 1023u) & ~1023u;  // 128-byte swizzled tiles: 1 KB aligned
   int* status = &hdr->status;
+  uint32_t dyn_bytes;
+  asm("mov.u32 %0, %%dynamic_smem_size;" : "=r"(dyn_bytes));
+  if (sb - raw + L::TILES > dyn_bytes) {  // same for every thread: nothing has started yet
+    if (threadIdx.x == 0) atomicExch(status, (int)JFA_ERR_CUDA);
+    return;
+  }
+  auto bar = [&](uint32_t i) { return raw + 8u * i; };
+  uint32_t* tmem_slot = (uint32_t*)(smem_raw + 8 * B_COUNT);
+  volatile int* abort = (volatile int*)(smem_raw + 8 * B_COUNT + 4);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n_items = hdr->n_q;
 
@@ -103,7 +111,11 @@ tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
       mbar_init(bar(B_QFULL + s), 1);
       mbar_init(bar(B_QEMPTY + s), 1);
       mbar_init(bar(B_SFULL + s), 1);
-      mbar_init(bar(B_SEMPTY + s), 256);
+      mbar_init(bar(B_PFULL + s), 256);
+      mbar_init(bar(B_PEMPTY + s), 1);
+      // exchanges between the two softmax warpgroups (bounded waits, never bar.sync)
+      mbar_init(bar(B_RED + s), 256);
+      mbar_init(bar(B_REDL + s), 256);
     }
     for (int s = 0; s < NK; ++s) {
       mbar_init(bar(B_KFULL + s), 1);
@@ -113,19 +125,12 @@ tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
       mbar_init(bar(B_VFULL + s), 1);
       mbar_init(bar(B_VEMPTY + s), 1);
     }
-    mbar_init(bar(B_PFULL), 256);
-    mbar_init(bar(B_PEMPTY), 1);
     mbar_init(bar(B_OFULL), 1);
     mbar_init(bar(B_OEMPTY), 256);
-    // exchanges between the two softmax warpgroups (bounded waits, never bar.sync)
-    mbar_init(bar(B_RED), 256);
-    mbar_init(bar(B_RED + 1), 256);
-    mbar_init(bar(B_REDL), 256);
-    mbar_init(bar(B_REDL + 1), 256);
     *abort = 0;
     fence_mbar_init();
   }
-  if (warp == kMmaWarp) tmem_alloc(smem_u32(tmem_slot), 512);
+  if (warp == kSWarp) tmem_alloc(smem_u32(tmem_slot), 512);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -175,20 +180,24 @@ tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
           tma_load_2d(sb + L::Q_OFF + qs * L::Q_BYTES + a * 16384, &tm_q, w.h * DQK + a * 64,
                       w.q0 + w.tile * BM, bar(B_QFULL + qs));
         ++q_it;
-        // the MMA lane consumes K(j+2) before V(j): load in that order
-        for (int j = 0; j < n + 2 && ok; ++j) {
-          if (j < n) ok = load_k(w, j);
-          if (ok && j >= 2) ok = load_v(w, j - 2);
+        // consumption order: S(0), S(1), then PV(j) and S(j+2) together
+        ok = load_k(w, 0);
+        if (ok && n > 1) ok = load_k(w, 1);
+        for (int j = 0; j < n && ok; ++j) {
+          ok = load_v(w, j);
+          if (ok && j + 2 < n) ok = load_k(w, j + 2);
         }
       }
     }
     __syncwarp();
-  } else if (warp == kMmaWarp) {
-    // ------------------------------------------------------------ MMA issuer
+  } else if (warp == kSWarp) {
+    // ------------------------------------------------------------ S = Q K^T issuer
+    // An MMA issue occupies the issuing thread for most of the MMA's own duration
+    // and the tensor pipe queues only a few, so the S and PV products come from two
+    // threads: the waits and commits of one overlap the other's MMAs.
     if (lane == 0) {
       constexpr uint32_t idesc_s = idesc_bf16(BM, BN, 0, 0);
-      constexpr uint32_t idesc_o = idesc_bf16(BM, DV, 0, 1);
-      uint32_t k_it = 0, v_it = 0, q_it = 0, s_it = 0, p_it = 0, o_it = 0;
+      uint32_t k_it = 0, q_it = 0, gs = 0;
       bool ok = true;
       WorkItem nxt = blockIdx.x < (unsigned)n_items ? load_item(list, blockIdx.x) : WorkItem{};
       for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
@@ -198,38 +207,46 @@ tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         if (n == 0) continue;
         const uint32_t qs = q_it % L::NQB;
         if (!mbar_wait(bar(B_QFULL + qs), (q_it / L::NQB) & 1, abort, status)) break;
-        tc_fence_after();
         const uint32_t q_tile = sb + L::Q_OFF + qs * L::Q_BYTES;
-        int next_s = 0;  // step whose S is issued next
-        // S(j) = Q K(j)^T into buffer s_it % 2, once the softmax has loaded S(j-2)
-        auto issue_s = [&]() {
-          const uint32_t b = s_it & 1, kst = k_it % NK;
-          if (!mbar_wait(bar(B_SEMPTY + b), ((s_it >> 1) & 1) ^ 1, abort, status) ||
-              !mbar_wait(bar(B_KFULL + kst), (k_it / NK) & 1, abort, status))
-            return false;
+        for (int i = 0; i < n; ++i, ++gs, ++k_it) {
+          // S(gs) goes into the buffer of S(gs - 2): free once the softmax has written P(gs - 2)
+          const uint32_t b = gs & 1, kst = k_it % NK;
+          if (!mbar_wait(bar(B_PFULL + b), ((gs >> 1) & 1) ^ 1, abort, status) ||
+              !mbar_wait(bar(B_KFULL + kst), (k_it / NK) & 1, abort, status)) {
+            ok = false;
+            break;
+          }
           tc_fence_after();
+          const uint32_t k_tile = sb + L::K_OFF + kst * L::K_BYTES;
 #pragma unroll
           for (int kk = 0; kk < DQK / 16; ++kk) {
             const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-            mma_bf16(tmem + (b ? T_S1 : T_S0), sw128_desc(q_tile + off, 16, 1024),
-                     sw128_desc(sb + L::K_OFF + kst * L::K_BYTES + off, 16, 1024), idesc_s,
-                     kk > 0 ? 1u : 0u);
+            mma_bf16(tmem + T_S + b * 128, sw128_desc(q_tile + off, 16, 1024),
+                     sw128_desc(k_tile + off, 16, 1024), idesc_s, kk > 0 ? 1u : 0u);
           }
           mma_commit(bar(B_SFULL + b));
           mma_commit(bar(B_KEMPTY + kst));
-          if (next_s == n - 1) mma_commit(bar(B_QEMPTY + qs));  // last use of this Q tile
-          ++next_s;
-          ++s_it;
-          ++k_it;
-          return true;
-        };
-        ok = issue_s();
-        if (ok && n > 1) ok = issue_s();
-        for (int j = 0; j < n && ok; ++j) {
-          if (next_s < n && !(ok = issue_s())) break;  // S(j+2)
-          // O += P(j) V(j), P read from TMEM
-          const uint32_t vst = v_it % NV;
-          if (!mbar_wait(bar(B_PFULL), p_it & 1, abort, status) ||
+          if (i == n - 1) mma_commit(bar(B_QEMPTY + qs));  // last use of this Q tile
+        }
+        ++q_it;
+      }
+    }
+    __syncwarp();
+  } else if (warp == kPvWarp) {
+    // ------------------------------------------------------------ O += P V issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc_o = idesc_bf16(BM, DV, 0, 1);
+      uint32_t v_it = 0, o_it = 0, gs = 0;
+      bool ok = true;
+      WorkItem nxt = blockIdx.x < (unsigned)n_items ? load_item(list, blockIdx.x) : WorkItem{};
+      for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
+        const WorkItem w = nxt;
+        if (it + (int)gridDim.x < n_items) nxt = load_item(list, it + gridDim.x);
+        const int n = w.cost;
+        if (n == 0) continue;
+        for (int j = 0; j < n; ++j, ++gs, ++v_it) {
+          const uint32_t b = gs & 1, vst = v_it % NV;
+          if (!mbar_wait(bar(B_PFULL + b), (gs >> 1) & 1, abort, status) ||
               !mbar_wait(bar(B_VFULL + vst), (v_it / NV) & 1, abort, status) ||
               (j == 0 && !mbar_wait(bar(B_OEMPTY), (o_it & 1) ^ 1, abort, status))) {
             ok = false;
@@ -239,17 +256,15 @@ tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
 #pragma unroll
           for (int kk = 0; kk < BN / 16; ++kk) {
             const uint64_t bd = sw128_desc(sb + L::V_OFF + vst * L::V_BYTES + kk * 2048, 16384, 1024);
-            mma_bf16_tmem_a(tmem + T_O, tmem + T_P + kk * 8, bd, idesc_o, (j > 0 || kk > 0) ? 1u : 0u);
+            mma_bf16_tmem_a(tmem + T_O, tmem + T_P + b * 64 + kk * 8, bd, idesc_o,
+                            (j > 0 || kk > 0) ? 1u : 0u);
           }
-          mma_commit(bar(B_PEMPTY));
+          mma_commit(bar(B_PEMPTY + b));
           mma_commit(bar(B_VEMPTY + vst));
-          ++p_it;
-          ++v_it;
+          if (j == n - 1) mma_commit(bar(B_OFULL));
         }
         if (!ok) break;
-        mma_commit(bar(B_OFULL));
         ++o_it;
-        ++q_it;
       }
     }
     __syncwarp();
@@ -260,8 +275,8 @@ tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
     const float c_score = ACT == kActSoftmax ? p.scale * kLog2e : p.scale;
     const float shift_raw = kMaskShift / c_score;  // masked raw scores land kMaskShift lower
-    float* red = reinterpret_cast<float*>(smem + L::RED_OFF);  // [2 steps][128 rows][2], then [128][2]
-    uint32_t s_it = 0, p_it = 0, o_it = 0, l_it = 0;
+    float* red = reinterpret_cast<float*>(smem_raw + L::RED_OFF);  // [2 steps][128 rows][2]
+    uint32_t p_it = 0, o_it = 0, l_it = 0;  // p_it: global step (S / P buffer p_it & 1)
     bool ok = true;
     WorkItem nxt = blockIdx.x < (unsigned)n_items ? load_item(list, blockIdx.x) : WorkItem{};
     for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
@@ -272,17 +287,15 @@ tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
       const int i = w.tile * BM + r;
       const float inv_len = 1.0f / (float)max(Lq, 1);
       float m = -INFINITY, l = 0.f;
-      for (int j = 0; j < n; ++j, ++s_it, ++p_it) {
-        const uint32_t b = s_it & 1;
-        if (!mbar_wait(bar(B_SFULL + b), (s_it >> 1) & 1, abort, status)) { ok = false; break; }
+      for (int j = 0; j < n; ++j, ++p_it) {
+        const uint32_t b = p_it & 1;
+        if (!mbar_wait(bar(B_SFULL + b), (p_it >> 1) & 1, abort, status)) { ok = false; break; }
         tc_fence_after();
-        const uint32_t s_tm = tmem + lane_base + (b ? T_S1 : T_S0) + half * HC;
+        const uint32_t s_tm = tmem + lane_base + T_S + b * 128 + half * HC;
         float sv[HC];
         tmem_ld32(s_tm, sv);
         tmem_ld32(s_tm + 32, sv + 32);
         tmem_wait_ld();
-        tc_fence_before();
-        mbar_arrive(bar(B_SEMPTY + b));  // S buffer free for S(j+2)
         const int kb = j * BN + half * HC;
         int nvalid = Lk - kb;
         if (CAUSAL) nvalid = min(nvalid, i - kb + 1);
@@ -345,8 +358,13 @@ tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
           const float2 rr = fadd2(rs0, rs1);
           l += rr.x + rr.y;
         }
-        // the P columns and O are free once PV(j-1) has completed
-        if (!mbar_wait(bar(B_PEMPTY), (p_it & 1) ^ 1, abort, status)) { ok = false; break; }
+        // P buffer b is free once PV(p_it - 2) has completed; rescaling O also needs
+        // PV(p_it - 1) complete.
+        if (!mbar_wait(bar(B_PEMPTY + b), ((p_it >> 1) & 1) ^ 1, abort, status) ||
+            (rescale && !mbar_wait(bar(B_PEMPTY + (b ^ 1)), ((p_it - 1) >> 1) & 1, abort, status))) {
+          ok = false;
+          break;
+        }
         tc_fence_after();
         if (rescale) {
           float ov[32];
@@ -360,10 +378,10 @@ tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             tmem_st32(o_tm, ov);
           }
         }
-        tmem_st32(tmem + lane_base + T_P + half * (HC / 2), reinterpret_cast<const float*>(pk));
+        tmem_st32(tmem + lane_base + T_P + b * 64 + half * (HC / 2), reinterpret_cast<const float*>(pk));
         tmem_wait_st();
         tc_fence_before();
-        mbar_arrive(bar(B_PFULL));
+        mbar_arrive(bar(B_PFULL + b));
       }
       if (!ok) break;
       // ---------------------------------------------------------- epilogue
@@ -410,7 +428,7 @@ tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
 
   tc_fence_before();
   __syncthreads();
-  if (warp == kMmaWarp) {
+  if (warp == kSWarp) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
