@@ -33,7 +33,9 @@ namespace jfa {
 namespace {
 using namespace tc;
 
-constexpr int kThreads = 320;  // producer warp, MMA warp, two compute warpgroups
+// producer warp 0, MMA issuer warps 1 and 10, compute warpgroups 2..5 and 6..9
+constexpr int kThreads = 352;
+constexpr int kIssuerB = 10;
 constexpr int TILE = 128;  // keys per dK/dV item, rows per dQ item (MMA M)
 constexpr int STEP = 128;  // query rows per dK/dV step, keys per dQ step (MMA N)
 constexpr float kLog2e = 1.4426950408889634f;
@@ -93,26 +95,34 @@ __device__ __forceinline__ void store_row_bf16(__nv_bfloat16* dst, const float* 
 // and dP^T are ordered after the products that read this step's P^T / dS^T.
 template <int DQK, int DV>
 struct KvLayout {
-  static constexpr int NKV = DQK + DV == 128 ? 2 : 1;                     // K/V tiles
-  static constexpr int NQ = DQK + DV == 256 ? 2 : (DQK + DV == 192 ? 3 : 4);  // Q/dO stages
+  // Q(g+1) is wanted as soon as P(g) is written, dO(g+1) only after dK(g): the Q ring
+  // is one stage deeper than the dO ring (a TMA load takes about a step).  The row
+  // terms (-lse log2 e, -D) of a step travel with its dO stage.
+  static constexpr int NKV = DQK + DV == 256 ? 1 : 2;  // K/V tiles
+  static constexpr int NQ = DQK == 128 ? 3 : 4;        // Q stages
+  static constexpr int NO = DQK == 64 && DV == 64 ? 4 : 2;  // dO stages
   static constexpr uint32_t K_BYTES = DQK / 64 * 16384;   // 128 keys
   static constexpr uint32_t V_BYTES = DV / 64 * 16384;
   static constexpr uint32_t Q_BYTES = DQK / 64 * 16384;   // 128 rows
   static constexpr uint32_t O_BYTES = DV / 64 * 16384;
-  static constexpr uint32_t RS_BYTES = 2 * STEP * 4;      // -lse log2 e and -D of 128 rows
-  static constexpr uint32_t K_OFF = 0;
+  static constexpr uint32_t RS_BYTES = 2 * STEP * 4;
+  // in front of the tiles: mbarriers, TMEM slot, abort flag (512 bytes), row terms
+  static constexpr uint32_t RS_OFF = 512;
+  static constexpr uint32_t SMALL = RS_OFF + NO * RS_BYTES;
+  static constexpr uint32_t TILE0 = (SMALL + 1023) / 1024 * 1024;  // for a 1 KB-aligned base
+  static constexpr uint32_t K_OFF = 0;  // offsets from the 1 KB-aligned tile base
   static constexpr uint32_t V_OFF = K_OFF + NKV * K_BYTES;
   static constexpr uint32_t Q_OFF = V_OFF + NKV * V_BYTES;
   static constexpr uint32_t O_OFF = Q_OFF + NQ * Q_BYTES;
-  static constexpr uint32_t RS_OFF = O_OFF + NQ * O_BYTES;
-  static constexpr uint32_t BAR_OFF = RS_OFF + NQ * RS_BYTES;
-  // at least 120 KB so that exactly one CTA (which owns all of TMEM) fits per SM
-  static constexpr uint32_t SMEM = (BAR_OFF + 512 + 1024) > 122880u ? (BAR_OFF + 512 + 1024) : 122880u;
+  static constexpr uint32_t TILES = O_OFF + NO * O_BYTES;
+  static constexpr uint32_t SMEM = TILE0 + TILES;
+  static_assert(SMEM <= 232448u && SMEM >= 122880u, "one CTA per SM within its shared memory");
 };
 
 enum : uint32_t {
-  KV_KVFULL = 0, KV_KVEMPTY = 2, KV_QFULL = 4, KV_RSFULL = 8, KV_QEMPTY = 12, KV_SFULL = 16,
-  KV_DPFULL = 17, KV_PFULL = 18, KV_DSFULL = 19, KV_ACCFULL = 20, KV_ACCEMPTY = 21, KV_COUNT = 22
+  KV_KVFULL = 0, KV_KVEMPTY = 2, KV_QFULL = 4, KV_QEMPTY = 8, KV_OFULL = 12, KV_OEMPTY = 16,
+  KV_RSFULL = 20, KV_SFULL = 24, KV_DPFULL = 25, KV_PFULL = 26, KV_DSFULL = 27, KV_ACCFULL = 28,
+  KV_ACCEMPTY = 29, KV_DPEMPTY = 30, KV_VDONE = 31, KV_KDONE = 33, KV_SISSUED = 35, KV_COUNT = 37
 };
 
 // bf16 pair (low, high) of a packed word to two floats, exactly
@@ -128,33 +138,49 @@ tc_dkdv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
                __nv_bfloat16* __restrict__ dk, __nv_bfloat16* __restrict__ dv, WsHeader* hdr,
                const WorkItem* __restrict__ list) {
   using L = KvLayout<DQK, DV>;
-  constexpr int NQ = L::NQ, NKV = L::NKV;
+  constexpr int NQ = L::NQ, NO = L::NO, NKV = L::NKV;
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-  const uint32_t sb = smem_u32(smem);
-  const uint32_t bar0 = sb + L::BAR_OFF;
-  auto bar = [&](uint32_t i) { return bar0 + 8u * i; };
-  uint32_t* tmem_slot = (uint32_t*)(smem + L::BAR_OFF + 8 * KV_COUNT);
-  volatile int* abort = (volatile int*)(smem + L::BAR_OFF + 8 * KV_COUNT + 4);
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t sb = (raw + L::SMALL + 1023u) & ~1023u;  // 128-byte swizzled tiles: 1 KB aligned
   int* status = &hdr->status;
+  uint32_t dyn_bytes;
+  asm("mov.u32 %0, %%dynamic_smem_size;" : "=r"(dyn_bytes));
+  if (sb - raw + L::TILES > dyn_bytes) {  // same for every thread: nothing has started yet
+    if (threadIdx.x == 0) atomicExch(status, (int)JFA_ERR_CUDA);
+    return;
+  }
+  auto bar = [&](uint32_t i) { return raw + 8u * i; };
+  uint32_t* tmem_slot = (uint32_t*)(smem_raw + 8 * KV_COUNT);
+  volatile int* abort = (volatile int*)(smem_raw + 8 * KV_COUNT + 4);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n_items = hdr->n_k;
 
   if (threadIdx.x == 0) {
+    // K/V tiles, Q/dO stages and the dK/dV accumulators are released by both issuers
     for (int s = 0; s < NKV; ++s) {
       mbar_init(bar(KV_KVFULL + s), 1);
-      mbar_init(bar(KV_KVEMPTY + s), 1);
+      mbar_init(bar(KV_KVEMPTY + s), 2);
     }
     for (int s = 0; s < NQ; ++s) {
       mbar_init(bar(KV_QFULL + s), 1);
+      mbar_init(bar(KV_QEMPTY + s), 2);
+    }
+    for (int s = 0; s < NO; ++s) {
+      mbar_init(bar(KV_OFULL + s), 1);
+      mbar_init(bar(KV_OEMPTY + s), 2);
       mbar_init(bar(KV_RSFULL + s), 32);
-      mbar_init(bar(KV_QEMPTY + s), 1);
     }
     mbar_init(bar(KV_SFULL), 1);
     mbar_init(bar(KV_DPFULL), 1);
     mbar_init(bar(KV_PFULL), 256);
     mbar_init(bar(KV_DSFULL), 256);
-    mbar_init(bar(KV_ACCFULL), 1);
+    mbar_init(bar(KV_ACCFULL), 2);
+    mbar_init(bar(KV_DPEMPTY), 256);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(bar(KV_VDONE + s), 1);
+      mbar_init(bar(KV_KDONE + s), 1);
+      mbar_init(bar(KV_SISSUED + s), 1);
+    }
     mbar_init(bar(KV_ACCEMPTY), 256);
     *abort = 0;
     fence_mbar_init();
@@ -164,8 +190,12 @@ tc_dkdv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  // TMEM columns: dK [0,128), dV [128,256), S^T (P^T) [256,384), dP^T (dS^T) [384,512)
-  constexpr uint32_t T_DK = 0, T_DV = 128, T_S = 256, T_DP = 384;
+  // TMEM columns: dK [0,128), dV [128,256), score buffers X0 [256,384) and X1 [384,512).
+  // Step g (counted over the CTA's whole list) computes S^T into X[g & 1] and dP^T into
+  // X[~g & 1]; P^T and dS^T are written packed over the S^T columns (each warpgroup
+  // into its own 64: P^T in the first 32, dS^T in the next 32), so dP^T(g) is free as
+  // soon as it is loaded and S^T(g+1) can take its place without waiting for dV(g).
+  constexpr uint32_t T_DK = 0, T_DV = 128, T_X = 256;
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer warp
@@ -205,9 +235,24 @@ tc_dkdv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
       if (!ok) break;
       ++kv_it;
       const int qs0 = CAUSAL ? key0 / STEP : 0;
-      for (int j = 0; j < n; ++j, ++q_it) {
+      // Q(j) into the Q ring (issued one step ahead of dO(j) and the row terms)
+      auto load_q = [&](uint32_t qq, int j) {
+        const uint32_t st = qq % NQ;
+        bool w_ok = mbar_wait(bar(KV_QEMPTY + st), ((qq / NQ) & 1) ^ 1, abort, status);
+        if (!__all_sync(0xffffffffu, w_ok)) return false;
+        if (lane == 0) {
+          mbar_expect_tx(bar(KV_QFULL + st), L::Q_BYTES);
+#pragma unroll
+          for (int a = 0; a < DQK / 64; ++a)
+            tma_load_2d(sb + L::Q_OFF + st * L::Q_BYTES + a * 16384, &tm_q, h * DQK + a * 64,
+                        (int32_t)(q0 + (qs0 + j) * STEP), bar(KV_QFULL + st));
+        }
+        return true;
+      };
+      ok = load_q(q_it, 0);
+      for (int j = 0; j < n && ok; ++j, ++q_it) {
         const int i0 = (qs0 + j) * STEP;
-        const uint32_t st = q_it % NQ, ph = (q_it / NQ) & 1;
+        const uint32_t st = q_it % NO;
         // row terms of this step: issue the global loads before waiting for the stage
         float2 rv[STEP / 32];
 #pragma unroll
@@ -216,37 +261,41 @@ tc_dkdv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
           rv[t] = make_float2(0.f, 0.f);
           if (ACT == kActSoftmax && i0 + c < Lq) rv[t] = rowstat[(int64_t)h * p.total_q + q0 + i0 + c];
         }
-        ok = mbar_wait(bar(KV_QEMPTY + st), ph ^ 1, abort, status);
+        ok = mbar_wait(bar(KV_OEMPTY + st), ((q_it / NO) & 1) ^ 1, abort, status);
         if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
         if (lane == 0) {
-          mbar_expect_tx(bar(KV_QFULL + st), L::Q_BYTES + L::O_BYTES);
-#pragma unroll
-          for (int a = 0; a < DQK / 64; ++a)
-            tma_load_2d(sb + L::Q_OFF + st * L::Q_BYTES + a * 16384, &tm_q, h * DQK + a * 64,
-                        (int32_t)(q0 + i0), bar(KV_QFULL + st));
+          mbar_expect_tx(bar(KV_OFULL + st), L::O_BYTES);
 #pragma unroll
           for (int a = 0; a < DV / 64; ++a)
             tma_load_2d(sb + L::O_OFF + st * L::O_BYTES + a * 16384, &tm_do, h * DV + a * 64,
-                        (int32_t)(q0 + i0), bar(KV_QFULL + st));
+                        (int32_t)(q0 + i0), bar(KV_OFULL + st));
         }
-        // stage layout: 128 x (-lse * log2 e), then 128 x (-D)
-        float* rs = reinterpret_cast<float*>(smem + L::RS_OFF + st * L::RS_BYTES);
+        // row-term stage: 128 x (-lse * log2 e), then 128 x (-D)
+        float* rs = reinterpret_cast<float*>(smem_raw + L::RS_OFF + st * L::RS_BYTES);
 #pragma unroll
         for (int t = 0; t < STEP / 32; ++t) {
           rs[lane + 32 * t] = -rv[t].x;
           rs[STEP + lane + 32 * t] = -rv[t].y;
         }
         mbar_arrive(bar(KV_RSFULL + st));
+        if (j + 1 < n) ok = load_q(q_it + 1, j + 1);
       }
     }
     __syncwarp();
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
+  } else if (warp == 1 || warp == kIssuerB) {
+    // ------------------------------------------------------------ MMA issuers
+    // An MMA issue occupies the issuing thread for most of the MMA's duration and
+    // the tensor pipe queues only a few, so the products come from two threads:
+    //   warp 1 (chain P):  S^T(g+1) = K Q^T, then dV += P^T(g) dO
+    //   warp 10 (chain dS): dK += dS^T(g) Q, then dP^T(g+1) = V dO^T
+    // Each commit covers only its own thread's MMAs; resources used by both chains
+    // (Q/dO stages, K/V tiles, the accumulators) take one commit from each.
     if (lane == 0) {
+      const bool chain_p = warp == 1;
       constexpr uint32_t idesc_s = idesc_bf16(TILE, STEP, 0, 0);
       constexpr uint32_t idesc_dv = idesc_bf16(TILE, DV, 0, 1);
       constexpr uint32_t idesc_dk = idesc_bf16(TILE, DQK, 0, 1);
-      uint32_t kv_it = 0, q_it = 0, s_it = 0, a_it = 0;
+      uint32_t kv_it = 0, q_it = 0, g = 0, a_it = 0;
       bool ok = true;
       WorkItem nxt = blockIdx.x < (unsigned)n_items ? load_item(list, blockIdx.x) : WorkItem{};
       for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
@@ -256,73 +305,90 @@ tc_dkdv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
         if (n == 0) continue;
         const uint32_t ks = kv_it % NKV;
         if (!mbar_wait(bar(KV_KVFULL + ks), (kv_it / NKV) & 1, abort, status)) break;
-        tc_fence_after();
         const uint32_t k_tile = sb + L::K_OFF + ks * L::K_BYTES;
         const uint32_t v_tile = sb + L::V_OFF + ks * L::V_BYTES;
-        auto q_tile = [&](uint32_t st) { return sb + L::Q_OFF + st * L::Q_BYTES; };
-        auto o_tile = [&](uint32_t st) { return sb + L::O_OFF + st * L::O_BYTES; };
-        auto issue_s = [&](uint32_t st) {  // S^T = K Q^T
+        auto q_tile = [&](uint32_t qq) { return sb + L::Q_OFF + (qq % NQ) * L::Q_BYTES; };
+        auto o_tile = [&](uint32_t qq) { return sb + L::O_OFF + (qq % NO) * L::O_BYTES; };
+        const uint32_t q_base = q_it;
+        // S^T(gg) into X[gg & 1]: that buffer held dP^T(gg-1), loaded by the compute
+        // warps, and before it P^T / dS^T(gg-2), read by dV(gg-2) (this thread) and
+        // dK(gg-2) (the other issuer).
+        auto issue_s = [&](uint32_t gg, uint32_t qq) {
+          if (!mbar_wait(bar(KV_QFULL + qq % NQ), (qq / NQ) & 1, abort, status) ||
+              !mbar_wait(bar(KV_DPEMPTY), (gg & 1) ^ 1, abort, status) ||
+              !mbar_wait(bar(KV_KDONE + (gg & 1)), ((gg >> 1) & 1) ^ 1, abort, status))
+            return false;
+          tc_fence_after();
+          const uint64_t da = sw128_desc(k_tile, 16, 1024), db = sw128_desc(q_tile(qq), 16, 1024);
 #pragma unroll
           for (int kk = 0; kk < DQK / 16; ++kk) {
-            const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-            mma_bf16(tmem + T_S, sw128_desc(k_tile + off, 16, 1024), sw128_desc(q_tile(st) + off, 16, 1024),
-                     idesc_s, kk > 0 ? 1u : 0u);
+            const uint32_t off = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;  // descriptor units
+            mma_bf16(tmem + T_X + (gg & 1) * 128, da + off, db + off, idesc_s, kk > 0 ? 1u : 0u);
           }
           mma_commit(bar(KV_SFULL));
+          return true;
         };
-        auto issue_dp = [&](uint32_t st) {  // dP^T = V dO^T
+        // dP^T(gg) into X[~gg & 1]: that buffer held S^T(gg-1) and P^T / dS^T(gg-1),
+        // read by dK(gg-1) (this thread) and dV(gg-1) (the other issuer).
+        auto issue_dp = [&](uint32_t gg, uint32_t qq) {
+          if (!mbar_wait(bar(KV_OFULL + qq % NO), (qq / NO) & 1, abort, status) ||
+              (gg > 0 && !mbar_wait(bar(KV_VDONE + ((gg - 1) & 1)), ((gg - 1) >> 1) & 1, abort, status)))
+            return false;
+          tc_fence_after();
+          const uint64_t da = sw128_desc(v_tile, 16, 1024), db = sw128_desc(o_tile(qq), 16, 1024);
 #pragma unroll
           for (int kk = 0; kk < DV / 16; ++kk) {
-            const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-            mma_bf16(tmem + T_DP, sw128_desc(v_tile + off, 16, 1024), sw128_desc(o_tile(st) + off, 16, 1024),
-                     idesc_s, kk > 0 ? 1u : 0u);
+            const uint32_t off = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
+            mma_bf16(tmem + T_X + ((gg & 1) ^ 1) * 128, da + off, db + off, idesc_s, kk > 0 ? 1u : 0u);
           }
           mma_commit(bar(KV_DPFULL));
+          return true;
         };
-        // Issue order per step j (in-order tensor pipe):
-        //   dV(j) [needs P(j)], S(j+1), dK(j) [needs dS(j)], dP(j+1)
-        // so that P(j+1) is computed while dK(j) and dP(j+1) run.
-        const uint32_t q_base = q_it;
-        if (!mbar_wait(bar(KV_QFULL + q_base % NQ), (q_base / NQ) & 1, abort, status)) break;
-        tc_fence_after();
-        issue_s(q_base % NQ);
-        issue_dp(q_base % NQ);
-        if (n == 1) mma_commit(bar(KV_KVEMPTY + ks));
-        for (int j = 0; j < n; ++j, ++s_it) {
-          const uint32_t st = (q_base + j) % NQ;
-          const uint32_t st1 = (q_base + j + 1) % NQ;
-          // dV += P^T dO (P^T packed in TMEM: query columns 0..63 at +0, 64..127 at +64)
-          if (!mbar_wait(bar(KV_PFULL), s_it & 1, abort, status) ||
+        ok = chain_p ? issue_s(g, q_base) : issue_dp(g, q_base);
+        if (ok && n == 1) mma_commit(bar(KV_KVEMPTY + ks));
+        for (int j = 0; j < n && ok; ++j, ++g) {
+          const uint32_t qq = q_base + j;            // this step's Q and dO stages
+          const uint32_t xb = T_X + (g & 1) * 128;  // P^T / dS^T of this step
+          if (!mbar_wait(bar(chain_p ? KV_PFULL : KV_DSFULL), g & 1, abort, status) ||
               (j == 0 && !mbar_wait(bar(KV_ACCEMPTY), (a_it & 1) ^ 1, abort, status))) {
             ok = false;
             break;
           }
-          tc_fence_after();
-#pragma unroll
-          for (int kk = 0; kk < STEP / 16; ++kk)
-            mma_bf16_tmem_a(tmem + T_DV, tmem + T_S + (kk >> 2) * 64 + (kk & 3) * 8,
-                            sw128_desc(o_tile(st) + kk * 2048, 16384, 1024), idesc_dv,
-                            (j > 0 || kk > 0) ? 1u : 0u);
-          if (j + 1 < n) {
-            const uint32_t q1 = q_base + j + 1;
-            if (!mbar_wait(bar(KV_QFULL + st1), (q1 / NQ) & 1, abort, status)) { ok = false; break; }
+          if (chain_p) {
+            // the compute warps need S^T(g+1) next: issue it ahead of dV(g), and let
+            // the other issuer know, so that dK(g) queues behind it
+            if (j + 1 < n) {
+              if (!(ok = issue_s(g + 1, q_base + j + 1))) break;
+              if (j + 2 == n) mma_commit(bar(KV_KVEMPTY + ks));  // last S^T of this K tile
+            }
+            mbar_arrive(bar(KV_SISSUED + (g & 1)));
             tc_fence_after();
-            issue_s(st1);
-          }
-          // dK += dS^T Q
-          if (!mbar_wait(bar(KV_DSFULL), s_it & 1, abort, status)) { ok = false; break; }
-          tc_fence_after();
+            const uint64_t db = sw128_desc(o_tile(qq), 16384, 1024);
 #pragma unroll
-          for (int kk = 0; kk < STEP / 16; ++kk)
-            mma_bf16_tmem_a(tmem + T_DK, tmem + T_DP + (kk >> 2) * 64 + (kk & 3) * 8,
-                            sw128_desc(q_tile(st) + kk * 2048, 16384, 1024), idesc_dk,
-                            (j > 0 || kk > 0) ? 1u : 0u);
-          mma_commit(bar(KV_QEMPTY + st));
-          if (j + 1 < n) {
-            issue_dp(st1);
-            if (j + 2 == n) mma_commit(bar(KV_KVEMPTY + ks));  // last S / dP of this K/V tile
+            for (int kk = 0; kk < STEP / 16; ++kk)
+              mma_bf16_tmem_a(tmem + T_DV, xb + (kk >> 2) * 64 + (kk & 3) * 8, db + ((kk * 2048) >> 4),
+                              idesc_dv, (j > 0 || kk > 0) ? 1u : 0u);
+            mma_commit(bar(KV_VDONE + (g & 1)));
+            mma_commit(bar(KV_QEMPTY + qq % NQ));
+            mma_commit(bar(KV_OEMPTY + qq % NO));
+            if (j + 1 == n) mma_commit(bar(KV_ACCFULL));
           } else {
-            mma_commit(bar(KV_ACCFULL));
+            if (!mbar_wait(bar(KV_SISSUED + (g & 1)), (g >> 1) & 1, abort, status)) { ok = false; break; }
+            tc_fence_after();
+            const uint64_t db = sw128_desc(q_tile(qq), 16384, 1024);
+#pragma unroll
+            for (int kk = 0; kk < STEP / 16; ++kk)
+              mma_bf16_tmem_a(tmem + T_DK, xb + (kk >> 2) * 64 + 32 + (kk & 3) * 8, db + ((kk * 2048) >> 4),
+                              idesc_dk, (j > 0 || kk > 0) ? 1u : 0u);
+            mma_commit(bar(KV_KDONE + (g & 1)));
+            mma_commit(bar(KV_QEMPTY + qq % NQ));
+            mma_commit(bar(KV_OEMPTY + qq % NO));
+            if (j + 1 == n) {
+              mma_commit(bar(KV_ACCFULL));
+            } else {
+              if (!(ok = issue_dp(g + 1, q_base + j + 1))) break;
+              if (j + 2 == n) mma_commit(bar(KV_KVEMPTY + ks));  // last dP^T of this V tile
+            }
           }
         }
         if (!ok) break;
@@ -347,8 +413,6 @@ tc_dkdv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
     const float2 hc = make_float2(0.5f * c_score, 0.5f * c_score);
     const float2 one = make_float2(1.f, 1.f);
     constexpr int HC = STEP / 2;  // query columns per group
-    const uint32_t s_tm = tmem + lane_base + T_S + half * HC;
-    const uint32_t p_tm = tmem + lane_base + T_DP + half * HC;
     uint32_t q_it = 0, s_it = 0, a_it = 0;
     bool ok = true;
     WorkItem nxt = blockIdx.x < (unsigned)n_items ? load_item(list, blockIdx.x) : WorkItem{};
@@ -365,15 +429,18 @@ tc_dkdv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
       const float2 il = make_float2(inv_len, inv_len);
       const int qs0 = CAUSAL ? key0 / STEP : 0;
       for (int step = 0; step < n; ++step, ++q_it, ++s_it) {
+        // S^T, then P^T and dS^T, in X[s_it & 1]; dP^T in the other buffer
+        const uint32_t s_tm = tmem + lane_base + T_X + (s_it & 1) * 128 + half * HC;
+        const uint32_t p_tm = tmem + lane_base + T_X + ((s_it & 1) ^ 1) * 128 + half * HC;
         if (!mbar_wait(bar(KV_SFULL), s_it & 1, abort, status)) { ok = false; break; }
         tc_fence_after();
         float sv[HC];
         tmem_ld32(s_tm, sv);
         tmem_ld32(s_tm + 32, sv + 32);
         tmem_wait_ld();
-        const uint32_t st = q_it % NQ;
-        if (!mbar_wait(bar(KV_RSFULL + st), (q_it / NQ) & 1, abort, status)) { ok = false; break; }
-        const float* rs = reinterpret_cast<const float*>(smem + L::RS_OFF + st * L::RS_BYTES) + half * HC;
+        const uint32_t st = q_it % NO;
+        if (!mbar_wait(bar(KV_RSFULL + st), (q_it / NO) & 1, abort, status)) { ok = false; break; }
+        const float* rs = reinterpret_cast<const float*>(smem_raw + L::RS_OFF + st * L::RS_BYTES) + half * HC;
         const int i0 = (qs0 + step) * STEP + half * HC;
         // valid queries of this group's columns for key j: i < Lq and (causal) i >= j
         const int lo = CAUSAL ? j - i0 : 0;
@@ -412,6 +479,8 @@ tc_dkdv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
         tmem_ld32(p_tm, dp);
         tmem_ld32(p_tm + 32, dp + 32);
         tmem_wait_ld();
+        tc_fence_before();
+        mbar_arrive(bar(KV_DPEMPTY));  // S^T(s_it+1) may overwrite the dP^T columns
         uint32_t dk2[HC / 2];
 #pragma unroll
         for (int c = 0; c < HC; c += 2) {
@@ -423,7 +492,7 @@ tc_dkdv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
             ds = fmul2(d, unpack_bf16(fk[c / 2]));
           dk2[c / 2] = pack_bf16(ds.x, ds.y);
         }
-        tmem_st32(p_tm, reinterpret_cast<const float*>(dk2));
+        tmem_st32(s_tm + 32, reinterpret_cast<const float*>(dk2));  // dS^T after P^T
         tmem_wait_st();
         tc_fence_before();
         mbar_arrive(bar(KV_DSFULL));
@@ -480,23 +549,31 @@ tc_dkdv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
 // TMEM as packed bf16 over the dP columns and dQ += dS K reads it from there.
 template <int DQK, int DV>
 struct QLayout {
-  static constexpr int NQO = DQK + DV == 256 ? 1 : 2;      // Q/dO tiles
-  static constexpr int NK = DQK + DV == 128 ? 4 : 2;       // K/V stages of 128 keys
+  // K(j+2) is wanted right after dQ(j) and V(j+1) right after dP(j) is loaded, so
+  // the K ring is one stage deeper than the V ring: a TMA load takes about a step.
+  static constexpr int NQO = DQK + DV == 256 ? 1 : 2;  // Q / dO tiles
+  static constexpr int NK = DQK == 128 ? 3 : (DV == 128 ? 4 : 6);
+  static constexpr int NV = DQK == 64 && DV == 64 ? 4 : 2;
   static constexpr uint32_t Q_BYTES = DQK / 64 * 16384;   // 128 rows
   static constexpr uint32_t O_BYTES = DV / 64 * 16384;
   static constexpr uint32_t K_BYTES = DQK / 64 * 16384;   // 128 keys
   static constexpr uint32_t V_BYTES = DV / 64 * 16384;
-  static constexpr uint32_t Q_OFF = 0;
+  static constexpr uint32_t TILE0 = 1024;  // mbarriers, TMEM slot, abort flag in front
+  static constexpr uint32_t Q_OFF = 0;     // offsets from the 1 KB-aligned tile base
   static constexpr uint32_t O_OFF = Q_OFF + NQO * Q_BYTES;
   static constexpr uint32_t K_OFF = O_OFF + NQO * O_BYTES;
   static constexpr uint32_t V_OFF = K_OFF + NK * K_BYTES;
-  static constexpr uint32_t BAR_OFF = V_OFF + NK * V_BYTES;
-  static constexpr uint32_t SMEM = (BAR_OFF + 512 + 1024) > 122880u ? (BAR_OFF + 512 + 1024) : 122880u;
+  static constexpr uint32_t TILES = V_OFF + NV * V_BYTES;
+  static constexpr uint32_t SMEM = TILE0 + TILES;
+  static_assert(SMEM <= 232448u && SMEM >= 122880u, "one CTA per SM within its shared memory");
 };
 
+// Each ring has one consumer thread: Q and K feed issuer A (S and dQ), dO and V
+// feed issuer B (dP).
 enum : uint32_t {
-  Q_QFULL = 0, Q_QEMPTY = 2, Q_KFULL = 4, Q_KEMPTY = 8, Q_SFULL = 12, Q_DPFULL = 14,
-  Q_DSFULL = 15, Q_ACCFULL = 16, Q_ACCEMPTY = 17, Q_COUNT = 18
+  Q_QFULL = 0, Q_QEMPTY = 2, Q_OFULL = 4, Q_OEMPTY = 6, Q_KFULL = 8, Q_KEMPTY = 14, Q_VFULL = 20,
+  Q_VEMPTY = 24, Q_SFULL = 28, Q_DPFULL = 30, Q_DPEMPTY = 31, Q_DSFULL = 32, Q_ACCFULL = 33,
+  Q_ACCEMPTY = 34, Q_COUNT = 35
 };
 
 template <int DQK, int DV, int ACT, bool CAUSAL>
@@ -506,15 +583,20 @@ tc_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
              const Problem p, const float2* __restrict__ rowstat, __nv_bfloat16* __restrict__ dq,
              WsHeader* hdr, const WorkItem* __restrict__ list) {
   using L = QLayout<DQK, DV>;
-  constexpr int NK = L::NK, NQO = L::NQO;
+  constexpr int NK = L::NK, NV = L::NV, NQO = L::NQO;
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-  const uint32_t sb = smem_u32(smem);
-  const uint32_t bar0 = sb + L::BAR_OFF;
-  auto bar = [&](uint32_t i) { return bar0 + 8u * i; };
-  uint32_t* tmem_slot = (uint32_t*)(smem + L::BAR_OFF + 8 * Q_COUNT);
-  volatile int* abort = (volatile int*)(smem + L::BAR_OFF + 8 * Q_COUNT + 4);
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t sb = (raw + 512u + 1023u) & ~1023u;  // 128-byte swizzled tiles: 1 KB aligned
   int* status = &hdr->status;
+  uint32_t dyn_bytes;
+  asm("mov.u32 %0, %%dynamic_smem_size;" : "=r"(dyn_bytes));
+  if (sb - raw + L::TILES > dyn_bytes) {  // same for every thread: nothing has started yet
+    if (threadIdx.x == 0) atomicExch(status, (int)JFA_ERR_CUDA);
+    return;
+  }
+  auto bar = [&](uint32_t i) { return raw + 8u * i; };
+  uint32_t* tmem_slot = (uint32_t*)(smem_raw + 8 * Q_COUNT);
+  volatile int* abort = (volatile int*)(smem_raw + 8 * Q_COUNT + 4);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n_items = hdr->n_q;
 
@@ -522,14 +604,21 @@ tc_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
     for (int s = 0; s < NQO; ++s) {
       mbar_init(bar(Q_QFULL + s), 1);
       mbar_init(bar(Q_QEMPTY + s), 1);
+      mbar_init(bar(Q_OFULL + s), 1);
+      mbar_init(bar(Q_OEMPTY + s), 1);
     }
     for (int s = 0; s < NK; ++s) {
       mbar_init(bar(Q_KFULL + s), 1);
       mbar_init(bar(Q_KEMPTY + s), 1);
     }
+    for (int s = 0; s < NV; ++s) {
+      mbar_init(bar(Q_VFULL + s), 1);
+      mbar_init(bar(Q_VEMPTY + s), 1);
+    }
     mbar_init(bar(Q_SFULL), 1);
     mbar_init(bar(Q_SFULL + 1), 1);
     mbar_init(bar(Q_DPFULL), 1);
+    mbar_init(bar(Q_DPEMPTY), 256);
     mbar_init(bar(Q_DSFULL), 256);
     mbar_init(bar(Q_ACCFULL), 1);
     mbar_init(bar(Q_ACCEMPTY), 256);
@@ -551,7 +640,7 @@ tc_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
       tma_prefetch_desc(&tm_do);
       tma_prefetch_desc(&tm_k);
       tma_prefetch_desc(&tm_v);
-      uint32_t q_it = 0, k_it = 0;
+      uint32_t q_it = 0, k_it = 0, v_it = 0;
       bool ok = true;
       WorkItem nxt = blockIdx.x < (unsigned)n_items ? load_item(list, blockIdx.x) : WorkItem{};
       for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
@@ -561,35 +650,57 @@ tc_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
         if (n == 0) continue;
         const int h = w.h, row0 = w.tile * TILE;
         const int32_t q0 = w.q0, k0 = w.k0;
-        const uint32_t qs = q_it % NQO;
-        if (!mbar_wait(bar(Q_QEMPTY + qs), ((q_it / NQO) & 1) ^ 1, abort, status)) break;
-        mbar_expect_tx(bar(Q_QFULL + qs), L::Q_BYTES + L::O_BYTES);
-#pragma unroll
-        for (int a = 0; a < DQK / 64; ++a)
-          tma_load_2d(sb + L::Q_OFF + qs * L::Q_BYTES + a * 16384, &tm_q, h * DQK + a * 64, q0 + row0,
-                      bar(Q_QFULL + qs));
-#pragma unroll
-        for (int a = 0; a < DV / 64; ++a)
-          tma_load_2d(sb + L::O_OFF + qs * L::O_BYTES + a * 16384, &tm_do, h * DV + a * 64, q0 + row0,
-                      bar(Q_QFULL + qs));
-        ++q_it;
-        for (int j = 0; j < n; ++j, ++k_it) {
-          const uint32_t st = k_it % NK, ph = (k_it / NK) & 1;
-          if (!mbar_wait(bar(Q_KEMPTY + st), ph ^ 1, abort, status)) { ok = false; break; }
-          mbar_expect_tx(bar(Q_KFULL + st), L::K_BYTES + L::V_BYTES);
+        auto load_k = [&](int j) {
+          const uint32_t st = k_it % NK;
+          if (!mbar_wait(bar(Q_KEMPTY + st), ((k_it / NK) & 1) ^ 1, abort, status)) return false;
+          mbar_expect_tx(bar(Q_KFULL + st), L::K_BYTES);
 #pragma unroll
           for (int a = 0; a < DQK / 64; ++a)
             tma_load_2d(sb + L::K_OFF + st * L::K_BYTES + a * 16384, &tm_k, h * DQK + a * 64,
                         k0 + j * STEP, bar(Q_KFULL + st));
+          ++k_it;
+          return true;
+        };
+        auto load_v = [&](int j) {
+          const uint32_t st = v_it % NV;
+          if (!mbar_wait(bar(Q_VEMPTY + st), ((v_it / NV) & 1) ^ 1, abort, status)) return false;
+          mbar_expect_tx(bar(Q_VFULL + st), L::V_BYTES);
 #pragma unroll
           for (int a = 0; a < DV / 64; ++a)
             tma_load_2d(sb + L::V_OFF + st * L::V_BYTES + a * 16384, &tm_v, h * DV + a * 64,
-                        k0 + j * STEP, bar(Q_KFULL + st));
+                        k0 + j * STEP, bar(Q_VFULL + st));
+          ++v_it;
+          return true;
+        };
+        const uint32_t qs = q_it % NQO, qph = ((q_it / NQO) & 1) ^ 1;
+        if (!mbar_wait(bar(Q_QEMPTY + qs), qph, abort, status)) break;
+        mbar_expect_tx(bar(Q_QFULL + qs), L::Q_BYTES);
+#pragma unroll
+        for (int a = 0; a < DQK / 64; ++a)
+          tma_load_2d(sb + L::Q_OFF + qs * L::Q_BYTES + a * 16384, &tm_q, h * DQK + a * 64, q0 + row0,
+                      bar(Q_QFULL + qs));
+        if (!mbar_wait(bar(Q_OEMPTY + qs), qph, abort, status)) break;
+        mbar_expect_tx(bar(Q_OFULL + qs), L::O_BYTES);
+#pragma unroll
+        for (int a = 0; a < DV / 64; ++a)
+          tma_load_2d(sb + L::O_OFF + qs * L::O_BYTES + a * 16384, &tm_do, h * DV + a * 64, q0 + row0,
+                      bar(Q_OFULL + qs));
+        ++q_it;
+        // consumption order: S(0), S(1), then dP(j) and S(j+2)
+        ok = load_k(0);
+        if (ok && n > 1) ok = load_k(1);
+        for (int j = 0; j < n && ok; ++j) {
+          ok = load_v(j);
+          if (ok && j + 2 < n) ok = load_k(j + 2);
         }
       }
     }
     __syncwarp();
   } else if (warp == 1) {
+    // ------------------------------------------------------------ issuer A: S and dQ
+    // dS(j) is written by the compute warpgroups over their own (already read) S(j)
+    // columns, so the dP columns are free as soon as dP(j) is loaded and dP(j+1)
+    // need not wait for dQ(j); S(j+2) reuses the buffer after dQ(j) has read dS(j).
     if (lane == 0) {
       constexpr uint32_t idesc_s = idesc_bf16(TILE, STEP, 0, 0);
       constexpr uint32_t idesc_dq = idesc_bf16(TILE, DQK, 0, 1);
@@ -603,45 +714,28 @@ tc_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
         if (n == 0) continue;
         const uint32_t qs = q_it % NQO;
         if (!mbar_wait(bar(Q_QFULL + qs), (q_it / NQO) & 1, abort, status)) break;
-        tc_fence_after();
         const uint32_t q_tile = sb + L::Q_OFF + qs * L::Q_BYTES;
-        const uint32_t o_tile = sb + L::O_OFF + qs * L::O_BYTES;
-        auto issue_s = [&](uint32_t kst) {  // S into buffer s_it & 1
+        const uint32_t k_base = k_it, s_base = s_it;
+        auto issue_s = [&](int i) {  // S(i) = Q K(i)^T into buffer (s_base + i) & 1
+          const uint32_t kk_it = k_base + i, kst = kk_it % NK;
+          if (!mbar_wait(bar(Q_KFULL + kst), (kk_it / NK) & 1, abort, status)) return false;
+          tc_fence_after();
           const uint32_t k_tile = sb + L::K_OFF + kst * L::K_BYTES;
 #pragma unroll
           for (int kk = 0; kk < DQK / 16; ++kk) {
             const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-            mma_bf16(tmem + t_s(s_it & 1), sw128_desc(q_tile + off, 16, 1024),
+            mma_bf16(tmem + t_s((s_base + i) & 1), sw128_desc(q_tile + off, 16, 1024),
                      sw128_desc(k_tile + off, 16, 1024), idesc_s, kk > 0 ? 1u : 0u);
           }
-          mma_commit(bar(Q_SFULL + (s_it & 1)));
-          ++s_it;
+          mma_commit(bar(Q_SFULL + ((s_base + i) & 1)));
+          if (i == n - 1) mma_commit(bar(Q_QEMPTY + qs));  // last use of this Q tile
+          return true;
         };
-        auto issue_dp = [&](uint32_t kst) {
-          const uint32_t v_tile = sb + L::V_OFF + kst * L::V_BYTES;
-#pragma unroll
-          for (int kk = 0; kk < DV / 16; ++kk) {
-            const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-            mma_bf16(tmem + T_DP, sw128_desc(o_tile + off, 16, 1024), sw128_desc(v_tile + off, 16, 1024),
-                     idesc_s, kk > 0 ? 1u : 0u);
-          }
-          mma_commit(bar(Q_DPFULL));
-        };
-        // prologue: S(0), dP(0)
-        const uint32_t k_base = k_it;
-        if (!mbar_wait(bar(Q_KFULL + k_base % NK), (k_base / NK) & 1, abort, status)) break;
-        tc_fence_after();
-        issue_s(k_base % NK);
-        issue_dp(k_base % NK);
+        ok = issue_s(0);
+        if (ok && n > 1) ok = issue_s(1);
         for (int j = 0; j < n && ok; ++j) {
           const uint32_t kst = (k_base + j) % NK;
-          if (j + 1 < n) {
-            const uint32_t k1 = k_base + j + 1;
-            if (!mbar_wait(bar(Q_KFULL + k1 % NK), (k1 / NK) & 1, abort, status)) { ok = false; break; }
-            tc_fence_after();
-            issue_s(k1 % NK);  // S(j+1) overlaps the dS(j) math
-          }
-          // dQ += dS(j) K(j); dS packed in TMEM: key columns 0..63 at +0, 64..127 at +64
+          // dQ += dS(j) K(j); dS packed in TMEM over the S(j) columns of each group
           if (!mbar_wait(bar(Q_DSFULL), d_it & 1, abort, status) ||
               (j == 0 && !mbar_wait(bar(Q_ACCEMPTY), (a_it & 1) ^ 1, abort, status))) {
             ok = false;
@@ -649,21 +743,62 @@ tc_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
           }
           tc_fence_after();
           const uint32_t k_tile = sb + L::K_OFF + kst * L::K_BYTES;
+          const uint32_t ds_tm = tmem + t_s((s_base + j) & 1);
 #pragma unroll
           for (int kk = 0; kk < STEP / 16; ++kk)
-            mma_bf16_tmem_a(tmem + T_DQ, tmem + T_DP + (kk >> 2) * 64 + (kk & 3) * 8,
+            mma_bf16_tmem_a(tmem + T_DQ, ds_tm + (kk >> 2) * 64 + (kk & 3) * 8,
                             sw128_desc(k_tile + kk * 2048, 16384, 1024), idesc_dq,
                             (j > 0 || kk > 0) ? 1u : 0u);
           mma_commit(bar(Q_KEMPTY + kst));
           ++d_it;
-          if (j + 1 < n) issue_dp((k_base + j + 1) % NK);
+          if (j + 2 < n) ok = issue_s(j + 2);
         }
         if (!ok) break;
-        mma_commit(bar(Q_QEMPTY + qs));
         mma_commit(bar(Q_ACCFULL));
         k_it += n;
+        s_it += n;
         ++q_it;
         ++a_it;
+      }
+    }
+    __syncwarp();
+  } else if (warp == kIssuerB) {
+    // ------------------------------------------------------------ issuer B: dP = dO V^T
+    if (lane == 0) {
+      constexpr uint32_t idesc_s = idesc_bf16(TILE, STEP, 0, 0);
+      uint32_t q_it = 0, v_it = 0, dp_it = 0;  // V ring: v_it % NV
+      bool ok = true;
+      WorkItem nxt = blockIdx.x < (unsigned)n_items ? load_item(list, blockIdx.x) : WorkItem{};
+      for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
+        const WorkItem w = nxt;
+        if (it + (int)gridDim.x < n_items) nxt = load_item(list, it + gridDim.x);
+        const int n = w.cost;
+        if (n == 0) continue;
+        const uint32_t qs = q_it % NQO;
+        if (!mbar_wait(bar(Q_OFULL + qs), (q_it / NQO) & 1, abort, status)) break;
+        const uint32_t o_tile = sb + L::O_OFF + qs * L::O_BYTES;
+        for (int j = 0; j < n; ++j, ++v_it, ++dp_it) {
+          const uint32_t vst = v_it % NV;
+          // the dP columns are free once the compute warpgroups have loaded dP(j-1)
+          if (!mbar_wait(bar(Q_VFULL + vst), (v_it / NV) & 1, abort, status) ||
+              !mbar_wait(bar(Q_DPEMPTY), (dp_it & 1) ^ 1, abort, status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t v_tile = sb + L::V_OFF + vst * L::V_BYTES;
+#pragma unroll
+          for (int kk = 0; kk < DV / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+            mma_bf16(tmem + T_DP, sw128_desc(o_tile + off, 16, 1024), sw128_desc(v_tile + off, 16, 1024),
+                     idesc_s, kk > 0 ? 1u : 0u);
+          }
+          mma_commit(bar(Q_DPFULL));
+          mma_commit(bar(Q_VEMPTY + vst));
+          if (j == n - 1) mma_commit(bar(Q_OEMPTY + qs));  // last use of this dO tile
+        }
+        if (!ok) break;
+        ++q_it;
       }
     }
     __syncwarp();
@@ -737,6 +872,8 @@ tc_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
         tmem_ld32(p_tm, dp);
         tmem_ld32(p_tm + 32, dp + 32);
         tmem_wait_ld();
+        tc_fence_before();
+        mbar_arrive(bar(Q_DPEMPTY));  // dP(step + 1) may overwrite the dP columns
         uint32_t dk2[HC / 2];
 #pragma unroll
         for (int c = 0; c < HC; c += 2) {
@@ -745,7 +882,8 @@ tc_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
                                                : fmul2(d, unpack_bf16(fk[c / 2]));
           dk2[c / 2] = pack_bf16(ds.x, ds.y);
         }
-        tmem_st32(p_tm, reinterpret_cast<const float*>(dk2));
+        // dS over this group's own S columns (already loaded above)
+        tmem_st32(s_tm, reinterpret_cast<const float*>(dk2));
         tmem_wait_st();
         tc_fence_before();
         mbar_arrive(bar(Q_DSFULL));
