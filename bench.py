@@ -49,6 +49,25 @@ def dist_env():
     return ws, rank, local
 
 
+def max_over_ranks(x, world, device):
+    """The largest x over all ranks: a job is as slow as its slowest replica."""
+    if world <= 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tflops(step_flops, world, seconds_per_step):
+    """Whole-job throughput: every rank processes one batch of step_flops per step."""
+    return world * step_flops / seconds_per_step / 1e12
+
+
+def replica_seed(rank):
+    """Each replica draws its own input values (same lengths, same shapes)."""
+    return rank
+
+
 def peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -234,7 +253,7 @@ def run_ours(args):
     if args.max_seqs:
         # profiling aid: the first N sequences of the workload (not a benchmark line)
         lq, lk = lq[:args.max_seqs], lk[:args.max_seqs]
-    batch = workloads.make_batch(w, lq, lk, seed=0, device=dev)
+    batch = workloads.make_batch(w, lq, lk, seed=replica_seed(rank), device=dev)
     d = dict(q=batch["q"], k=batch["k"], v=batch["v"], do=batch["do"],
              oq=torch.as_tensor(batch["offs_q"], device=dev),
              ok=torch.as_tensor(batch["offs_k"], device=dev))
@@ -274,16 +293,13 @@ def run_ours(args):
             ends[i].record(stream)
         torch.cuda.synchronize()
     jfa.jfa_profile_enable(False)
-    ms_total = sum(s.elapsed_time(e) for s, e in zip(starts, ends))
+    ms_total = max_over_ranks(sum(s.elapsed_time(e) for s, e in zip(starts, ends)), world, dev)
     if world > 1:
-        t = torch.tensor([ms_total], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms_total = float(t.item())
         torch.distributed.barrier()
     prof = {k: jfa.jfa_profile_read(k) for k in jfa.KERNEL_KINDS}
     launches = sum(n for n, _ in prof.values())
     ms_per_step = ms_total / args.steps
-    value = world * step_flops / (ms_per_step * 1e-3) / 1e12
+    value = job_tflops(step_flops, world, ms_per_step * 1e-3)
 
     # roofline of the dominant kernel
     pk, peak_src = peaks()
@@ -369,12 +385,8 @@ def e2e_measure(jfa, w, batch, d, ws, p, args, dev, step_flops, world):
     t0 = time.perf_counter()
     for _ in range(args.steps):
         one()
-    dt = time.perf_counter() - t0
-    if world > 1:
-        t = torch.tensor([dt], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        dt = float(t.item())
-    return {"value": round(world * step_flops * args.steps / dt / 1e12, 3), "unit": "TFLOP/s",
+    dt = max_over_ranks(time.perf_counter() - t0, world, dev)
+    return {"value": round(job_tflops(step_flops, world, dt / args.steps), 3), "unit": "TFLOP/s",
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
             "ms_per_step": round(dt / args.steps * 1e3, 4)}
 
