@@ -113,6 +113,38 @@ struct Timed {
 
 inline jfa_status cu(cudaError_t e) { return e == cudaSuccess ? JFA_OK : JFA_ERR_CUDA; }
 
+// A second stream per device and host thread, with a fork and a join event, for
+// independent work that may overlap the caller's stream (the backward row terms
+// run beside the scheduler).  Created on first use and kept for the thread's life;
+// nullptr when it cannot be created (the work then runs on the caller's stream).
+struct SideStream {
+  cudaStream_t s = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr;
+};
+
+SideStream* side_stream() {
+  constexpr int kMaxDevices = 64;
+  thread_local SideStream sides[kMaxDevices];
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  SideStream& sd = sides[dev];
+  if (!sd.s) {
+    cudaStream_t st = nullptr;
+    cudaEvent_t a = nullptr, b = nullptr;
+    if (cudaStreamCreateWithFlags(&st, cudaStreamNonBlocking) != cudaSuccess) return nullptr;
+    if (cudaEventCreateWithFlags(&a, cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&b, cudaEventDisableTiming) != cudaSuccess) {
+      if (a) cudaEventDestroy(a);
+      cudaStreamDestroy(st);
+      return nullptr;
+    }
+    sd.s = st;
+    sd.fork = a;
+    sd.join = b;
+  }
+  return &sd;
+}
+
 bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
 
 enum class Kind { Self, Cross, Gdpa };
@@ -217,14 +249,27 @@ jfa_status run_bwd(const jfa_params* p, Kind kind, int act, const void* q, const
   sc.build_q = 1;
   sc.build_k = 1;
   sc.self_attention = (kind == Kind::Self) || p->causal;
+  // The row terms (softmax only) depend on o, dout and lse alone: they run on a side
+  // stream while the scheduler builds the lists, and the caller's stream waits for
+  // them before the dK/dV pass.
+  SideStream* sd = act == kActSoftmax ? side_stream() : nullptr;
+  if (sd && (cudaEventRecord(sd->fork, s) != cudaSuccess ||
+             cudaStreamWaitEvent(sd->s, sd->fork, 0) != cudaSuccess))
+    return JFA_ERR_CUDA;
   {
     Timed t(JFA_KERNEL_SCHEDULE, s);
     if ((st = cu(launch_schedule(pr, w, sc, s))) != JFA_OK) return st;
   }
   if (act == kActSoftmax) {
-    Timed t(JFA_KERNEL_BWD_D, s);
-    st = path == 1 ? cu(launch_tc_rowstat(pr, o, dout, lse, w, s))
-                   : cu(launch_bwd_rowterm(pr, p->dtype, o, dout, w, s));
+    cudaStream_t rs = sd ? sd->s : s;
+    {
+      Timed t(JFA_KERNEL_BWD_D, rs);
+      st = path == 1 ? cu(launch_tc_rowstat(pr, o, dout, lse, w, rs))
+                     : cu(launch_bwd_rowterm(pr, p->dtype, o, dout, w, rs));
+    }
+    if (sd && (cudaEventRecord(sd->join, rs) != cudaSuccess ||
+               cudaStreamWaitEvent(s, sd->join, 0) != cudaSuccess))
+      return JFA_ERR_CUDA;
     if (st != JFA_OK) return st;
   }
   {

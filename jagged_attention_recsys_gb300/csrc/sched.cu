@@ -198,24 +198,28 @@ __device__ void build_list(const Problem& p, const ListSpec& L, const Arrays& A,
     __syncthreads();
   }
 
-  // 6. write the items: one thread per sequence, its tiles heaviest first
-  for (int r = tid; r < B; r += kThreads) {
-    const int b = A.order[r];
-    const int4 s = A.seq[b];
-    const int n = A.ntile[b];
-    for (int k = 0; k < n; ++k) {
-      const int t = tile_at(L, p.causal, n, k);
-      WorkItem w;
-      w.b = b; w.tile = t; w.cost = cost_of(L, p.causal, s.z, s.w, t);
-      w.q0 = s.x; w.k0 = s.y; w.lq = s.z; w.lk = s.w;
-      const int64_t pos = (int64_t)(A.first[r] + k) * p.heads;
-      for (int h = 0; h < p.heads; ++h) {
-        w.h = h;
-        list[pos + h] = w;
-      }
+  // 6. write the items, one per thread in list order (coalesced 32-byte stores).
+  //    Item i is head i % H of unit u = i / H; the unit belongs to the last list
+  //    position r with first[r] <= u (positions without tiles share their first[]
+  //    with the next one, so the search never lands on them), and is that
+  //    sequence's k-th tile in list order, k = u - first[r].
+  const int64_t n_items = (int64_t)carry * p.heads;
+  for (int64_t i = tid; i < n_items; i += kThreads) {
+    const int u = (int)(i / p.heads), h = (int)(i - (int64_t)u * p.heads);
+    int lo = 0, hi = B - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (A.first[mid] <= u) lo = mid; else hi = mid - 1;
     }
+    const int b = A.order[lo];
+    const int4 s = A.seq[b];
+    const int t = tile_at(L, p.causal, A.ntile[b], u - A.first[lo]);
+    WorkItem w;
+    w.b = b; w.h = h; w.tile = t; w.cost = cost_of(L, p.causal, s.z, s.w, t);
+    w.q0 = s.x; w.k0 = s.y; w.lq = s.z; w.lk = s.w;
+    list[i] = w;
   }
-  if (tid == 0) *n_out = carry * p.heads;
+  if (tid == 0) *n_out = (int)n_items;
   __syncthreads();
 }
 

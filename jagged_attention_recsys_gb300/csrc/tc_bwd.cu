@@ -84,35 +84,39 @@ __device__ __forceinline__ void store_row_bf16(__nv_bfloat16* dst, const float* 
 // =============================================================================
 // dK / dV pass
 // =============================================================================
-// One item = (sequence, head, 128-key tile); the inner loop steps over 128
-// query rows (all MMAs are 128 x 128 or 128 x D).  Per step the MMA lane
-// issues S^T = K Q^T (commit S_FULL) and dP^T = V dO^T (commit DP_FULL).  The
-// two compute warpgroups (64 query columns each) turn S^T into P^T while dP^T
-// is being computed and store it as packed bf16 over their own S^T columns
-// (P_FULL); the MMA lane then issues dV += P^T dO while the warpgroups form
-// dS^T = P^T (dP^T - D) into their own dP^T columns (DS_FULL), and finally
-// dK += dS^T Q.  MMAs of one thread execute in order, so the next step's S^T
-// and dP^T are ordered after the products that read this step's P^T / dS^T.
+// One item = (sequence, head, 128-key tile); the inner loop steps over 128 query
+// rows.  TMEM holds the dK and dV accumulators and two 128-column buffers; step g
+// (counted over the CTA's whole list) uses buffer X[g & 1] three times over:
+//   S^T = K Q^T  ->  loaded by the compute warps  ->  dP^T = V dO^T over it  ->
+//   loaded  ->  P^T and dS^T packed over it (each warpgroup in its own 64
+//   columns: P^T in the first 32, dS^T in the next 32)  ->  read by dV and dK.
+// Step g+1 uses the other buffer, so nothing of step g waits for it:
+//   warp 1  (issuer A): S^T(g+1) once dK(g-1) has read X[(g+1) & 1], then
+//                       dV += P^T(g) dO(g)
+//   warp 10 (issuer B): dP^T(g+1) once S^T(g+1) has been loaded, then
+//                       dK += dS^T(g) Q(g)
+// The compute warps compute P^T(g) while dP^T(g) runs and find S^T(g+1) ready
+// when they finish step g.  Only the step's valid query rows (rounded up to 16)
+// enter the MMAs.  K and V have separate slots, so the next item's K loads as
+// soon as its last S^T has been issued and its V after the last dP^T.
+constexpr int KSTEP = 128;  // query rows per dK/dV step
+
 template <int DQK, int DV>
 struct KvLayout {
-  // Q(g+1) is wanted as soon as P(g) is written, dO(g+1) only after dK(g): the Q ring
-  // is one stage deeper than the dO ring (a TMA load takes about a step).  The row
-  // terms (-lse log2 e, -D) of a step travel with its dO stage.
-  static constexpr int NKV = DQK + DV == 256 ? 1 : 2;  // K/V tiles
-  static constexpr int NQ = DQK == 128 ? 3 : 4;        // Q stages
-  static constexpr int NO = DQK == 64 && DV == 64 ? 4 : 2;  // dO stages
-  static constexpr uint32_t K_BYTES = DQK / 64 * 16384;   // 128 keys
+  static constexpr int NQ = DQK == 128 ? 3 : 4;             // Q stages
+  static constexpr int NO = DQK == 64 && DV == 64 ? 4 : 2;  // dO stages, with the row terms
+  static constexpr uint32_t K_BYTES = DQK / 64 * 16384;  // 128 keys
   static constexpr uint32_t V_BYTES = DV / 64 * 16384;
-  static constexpr uint32_t Q_BYTES = DQK / 64 * 16384;   // 128 rows
+  static constexpr uint32_t Q_BYTES = DQK / 64 * 16384;  // 128 rows
   static constexpr uint32_t O_BYTES = DV / 64 * 16384;
-  static constexpr uint32_t RS_BYTES = 2 * STEP * 4;
+  static constexpr uint32_t RS_BYTES = 2 * KSTEP * 4;    // -lse log2 e and -D of 128 rows
   // in front of the tiles: mbarriers, TMEM slot, abort flag (512 bytes), row terms
   static constexpr uint32_t RS_OFF = 512;
   static constexpr uint32_t SMALL = RS_OFF + NO * RS_BYTES;
   static constexpr uint32_t TILE0 = (SMALL + 1023) / 1024 * 1024;  // for a 1 KB-aligned base
   static constexpr uint32_t K_OFF = 0;  // offsets from the 1 KB-aligned tile base
-  static constexpr uint32_t V_OFF = K_OFF + NKV * K_BYTES;
-  static constexpr uint32_t Q_OFF = V_OFF + NKV * V_BYTES;
+  static constexpr uint32_t V_OFF = K_OFF + K_BYTES;
+  static constexpr uint32_t Q_OFF = V_OFF + V_BYTES;
   static constexpr uint32_t O_OFF = Q_OFF + NQ * Q_BYTES;
   static constexpr uint32_t TILES = O_OFF + NO * O_BYTES;
   static constexpr uint32_t SMEM = TILE0 + TILES;
@@ -120,15 +124,63 @@ struct KvLayout {
 };
 
 enum : uint32_t {
-  KV_KVFULL = 0, KV_KVEMPTY = 2, KV_QFULL = 4, KV_QEMPTY = 8, KV_OFULL = 12, KV_OEMPTY = 16,
-  KV_RSFULL = 20, KV_SFULL = 24, KV_DPFULL = 25, KV_PFULL = 26, KV_DSFULL = 27, KV_ACCFULL = 28,
-  KV_ACCEMPTY = 29, KV_DPEMPTY = 30, KV_VDONE = 31, KV_KDONE = 33, KV_SISSUED = 35, KV_COUNT = 37
+  KV_KFULL = 0, KV_KEMPTY = 1, KV_VFULL = 2, KV_VEMPTY = 3, KV_QFULL = 4, KV_QEMPTY = 8,
+  KV_OFULL = 12, KV_OEMPTY = 16, KV_RSFULL = 20, KV_SFULL = 24, KV_SEMPTY = 26, KV_DPFULL = 28,
+  KV_PDSFULL = 30, KV_KDONE = 32, KV_ACCFULL = 34, KV_ACCEMPTY = 35, KV_COUNT = 36
 };
 
 // bf16 pair (low, high) of a packed word to two floats, exactly
 __device__ __forceinline__ float2 unpack_bf16(uint32_t u) {
   return make_float2(__uint_as_float(u << 16), __uint_as_float(u & 0xffff0000u));
 }
+
+// Walks the steps of a CTA's items in order (items without steps are skipped):
+// item w, local step j, global step g, Q/dO stage counter q, item counter kv.
+// The item after w is always loaded one ahead, so a step never waits for memory.
+struct StepCursor {
+  const WorkItem* list;
+  int n_items, it;
+  WorkItem w, nxt;
+  int j;
+  uint32_t g, q, kv;
+  bool valid;
+  __device__ void next_item() {  // w <- the item after it, nxt <- the one after that
+    it += gridDim.x;
+    w = nxt;
+    if (it + (int)gridDim.x < n_items) nxt = load_item(list, it + gridDim.x);
+  }
+  __device__ void skip_empty() {
+    while (it < n_items && w.cost == 0) next_item();
+    valid = it < n_items;
+  }
+  __device__ void init(const WorkItem* l, int n) {
+    list = l;
+    n_items = n;
+    it = blockIdx.x;
+    j = 0;
+    g = q = kv = 0;
+    if (it < n_items) w = load_item(list, it);
+    if (it + (int)gridDim.x < n_items) nxt = load_item(list, it + gridDim.x);
+    skip_empty();
+  }
+  __device__ void advance() {
+    ++g;
+    ++q;
+    if (++j < w.cost) return;
+    j = 0;
+    ++kv;
+    next_item();
+    skip_empty();
+  }
+  __device__ bool last() const { return j == w.cost - 1; }
+  // valid query rows of this step, rounded up to 16 (MMA N of S^T / dP^T)
+  template <bool CAUSAL>
+  __device__ int n16() const {
+    const int qs0 = CAUSAL ? (w.tile * TILE) / KSTEP : 0;
+    const int v = min(KSTEP, w.lq - (qs0 + j) * KSTEP);
+    return (max(v, 1) + 15) & ~15;
+  }
+};
 
 template <int DQK, int DV, int ACT, bool CAUSAL>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -138,7 +190,7 @@ tc_dkdv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
                __nv_bfloat16* __restrict__ dk, __nv_bfloat16* __restrict__ dv, WsHeader* hdr,
                const WorkItem* __restrict__ list) {
   using L = KvLayout<DQK, DV>;
-  constexpr int NQ = L::NQ, NO = L::NO, NKV = L::NKV;
+  constexpr int NQ = L::NQ, NO = L::NO;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t sb = (raw + L::SMALL + 1023u) & ~1023u;  // 128-byte swizzled tiles: 1 KB aligned
@@ -156,11 +208,11 @@ tc_dkdv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
   const int n_items = hdr->n_k;
 
   if (threadIdx.x == 0) {
-    // K/V tiles, Q/dO stages and the dK/dV accumulators are released by both issuers
-    for (int s = 0; s < NKV; ++s) {
-      mbar_init(bar(KV_KVFULL + s), 1);
-      mbar_init(bar(KV_KVEMPTY + s), 2);
-    }
+    mbar_init(bar(KV_KFULL), 1);
+    mbar_init(bar(KV_KEMPTY), 1);
+    mbar_init(bar(KV_VFULL), 1);
+    mbar_init(bar(KV_VEMPTY), 1);
+    // Q / dO stages and the accumulators are released by both issuers
     for (int s = 0; s < NQ; ++s) {
       mbar_init(bar(KV_QFULL + s), 1);
       mbar_init(bar(KV_QEMPTY + s), 2);
@@ -170,17 +222,14 @@ tc_dkdv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
       mbar_init(bar(KV_OEMPTY + s), 2);
       mbar_init(bar(KV_RSFULL + s), 32);
     }
-    mbar_init(bar(KV_SFULL), 1);
-    mbar_init(bar(KV_DPFULL), 1);
-    mbar_init(bar(KV_PFULL), 256);
-    mbar_init(bar(KV_DSFULL), 256);
-    mbar_init(bar(KV_ACCFULL), 2);
-    mbar_init(bar(KV_DPEMPTY), 256);
     for (int s = 0; s < 2; ++s) {
-      mbar_init(bar(KV_VDONE + s), 1);
+      mbar_init(bar(KV_SFULL + s), 1);
+      mbar_init(bar(KV_SEMPTY + s), 256);
+      mbar_init(bar(KV_DPFULL + s), 1);
+      mbar_init(bar(KV_PDSFULL + s), 256);
       mbar_init(bar(KV_KDONE + s), 1);
-      mbar_init(bar(KV_SISSUED + s), 1);
     }
+    mbar_init(bar(KV_ACCFULL), 2);
     mbar_init(bar(KV_ACCEMPTY), 256);
     *abort = 0;
     fence_mbar_init();
@@ -190,11 +239,7 @@ tc_dkdv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  // TMEM columns: dK [0,128), dV [128,256), score buffers X0 [256,384) and X1 [384,512).
-  // Step g (counted over the CTA's whole list) computes S^T into X[g & 1] and dP^T into
-  // X[~g & 1]; P^T and dS^T are written packed over the S^T columns (each warpgroup
-  // into its own 64: P^T in the first 32, dS^T in the next 32), so dP^T(g) is free as
-  // soon as it is loaded and S^T(g+1) can take its place without waiting for dV(g).
+  // TMEM columns: dK [0,128), dV [128,256), step buffers X0 [256,384), X1 [384,512)
   constexpr uint32_t T_DK = 0, T_DV = 128, T_X = 256;
 
   if (warp == 0) {
@@ -216,185 +261,170 @@ tc_dkdv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
       const int h = w.h, key0 = w.tile * TILE;
       const int64_t q0 = w.q0, k0 = w.k0;
       const int Lq = w.lq;
-      if (lane == 0) {
-        const uint32_t ks = kv_it % NKV;
-        ok = mbar_wait(bar(KV_KVEMPTY + ks), ((kv_it / NKV) & 1) ^ 1, abort, status);
-        if (ok) {
-          mbar_expect_tx(bar(KV_KVFULL + ks), L::K_BYTES + L::V_BYTES);
-#pragma unroll
-          for (int a = 0; a < DQK / 64; ++a)
-            tma_load_2d(sb + L::K_OFF + ks * L::K_BYTES + a * 16384, &tm_k, h * DQK + a * 64,
-                        (int32_t)(k0 + key0), bar(KV_KVFULL + ks));
-#pragma unroll
-          for (int a = 0; a < DV / 64; ++a)
-            tma_load_2d(sb + L::V_OFF + ks * L::V_BYTES + a * 16384, &tm_v, h * DV + a * 64,
-                        (int32_t)(k0 + key0), bar(KV_KVFULL + ks));
-        }
-      }
-      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-      if (!ok) break;
+      const uint32_t kph = (kv_it & 1) ^ 1;
       ++kv_it;
-      const int qs0 = CAUSAL ? key0 / STEP : 0;
-      // Q(j) into the Q ring (issued one step ahead of dO(j) and the row terms)
-      auto load_q = [&](uint32_t qq, int j) {
-        const uint32_t st = qq % NQ;
-        bool w_ok = mbar_wait(bar(KV_QEMPTY + st), ((qq / NQ) & 1) ^ 1, abort, status);
-        if (!__all_sync(0xffffffffu, w_ok)) return false;
+      const int qs0 = CAUSAL ? key0 / KSTEP : 0;
+      // K is wanted one step before V (S^T runs a step ahead of dP^T): K, Q(0), V first
+      bool v_done = false;
+      auto load_kv = [&](bool is_k) {
+        if (lane == 0) {
+          ok = mbar_wait(bar(is_k ? KV_KEMPTY : KV_VEMPTY), kph, abort, status);
+          if (ok) {
+            mbar_expect_tx(bar(is_k ? KV_KFULL : KV_VFULL), is_k ? L::K_BYTES : L::V_BYTES);
+            if (is_k) {
+#pragma unroll
+              for (int a = 0; a < DQK / 64; ++a)
+                tma_load_2d(sb + L::K_OFF + a * 16384, &tm_k, h * DQK + a * 64, (int32_t)(k0 + key0),
+                            bar(KV_KFULL));
+            } else {
+#pragma unroll
+              for (int a = 0; a < DV / 64; ++a)
+                tma_load_2d(sb + L::V_OFF + a * 16384, &tm_v, h * DV + a * 64, (int32_t)(k0 + key0),
+                            bar(KV_VFULL));
+            }
+          }
+        }
+        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+      };
+      load_kv(true);
+      for (int j = 0; j < n && ok; ++j, ++q_it) {
+        const int i0 = (qs0 + j) * KSTEP;
+        // row terms of this step: issue the global loads before waiting for the stage
+        float2 rv[KSTEP / 32];
+#pragma unroll
+        for (int t = 0; t < KSTEP / 32; ++t) {
+          const int c = lane + 32 * t;
+          rv[t] = make_float2(0.f, 0.f);
+          if (ACT == kActSoftmax && i0 + c < Lq) rv[t] = rowstat[(int64_t)h * p.total_q + q0 + i0 + c];
+        }
+        const uint32_t st = q_it % NQ;
+        ok = mbar_wait(bar(KV_QEMPTY + st), ((q_it / NQ) & 1) ^ 1, abort, status);
+        if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
         if (lane == 0) {
           mbar_expect_tx(bar(KV_QFULL + st), L::Q_BYTES);
 #pragma unroll
           for (int a = 0; a < DQK / 64; ++a)
             tma_load_2d(sb + L::Q_OFF + st * L::Q_BYTES + a * 16384, &tm_q, h * DQK + a * 64,
-                        (int32_t)(q0 + (qs0 + j) * STEP), bar(KV_QFULL + st));
+                        (int32_t)(q0 + i0), bar(KV_QFULL + st));
         }
-        return true;
-      };
-      ok = load_q(q_it, 0);
-      for (int j = 0; j < n && ok; ++j, ++q_it) {
-        const int i0 = (qs0 + j) * STEP;
-        const uint32_t st = q_it % NO;
-        // row terms of this step: issue the global loads before waiting for the stage
-        float2 rv[STEP / 32];
-#pragma unroll
-        for (int t = 0; t < STEP / 32; ++t) {
-          const int c = lane + 32 * t;
-          rv[t] = make_float2(0.f, 0.f);
-          if (ACT == kActSoftmax && i0 + c < Lq) rv[t] = rowstat[(int64_t)h * p.total_q + q0 + i0 + c];
+        if (!v_done) {
+          load_kv(false);
+          v_done = true;
+          if (!ok) break;
         }
-        ok = mbar_wait(bar(KV_OEMPTY + st), ((q_it / NO) & 1) ^ 1, abort, status);
+        const uint32_t so = q_it % NO;
+        ok = mbar_wait(bar(KV_OEMPTY + so), ((q_it / NO) & 1) ^ 1, abort, status);
         if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
         if (lane == 0) {
-          mbar_expect_tx(bar(KV_OFULL + st), L::O_BYTES);
+          mbar_expect_tx(bar(KV_OFULL + so), L::O_BYTES);
 #pragma unroll
           for (int a = 0; a < DV / 64; ++a)
-            tma_load_2d(sb + L::O_OFF + st * L::O_BYTES + a * 16384, &tm_do, h * DV + a * 64,
-                        (int32_t)(q0 + i0), bar(KV_OFULL + st));
+            tma_load_2d(sb + L::O_OFF + so * L::O_BYTES + a * 16384, &tm_do, h * DV + a * 64,
+                        (int32_t)(q0 + i0), bar(KV_OFULL + so));
         }
-        // row-term stage: 128 x (-lse * log2 e), then 128 x (-D)
-        float* rs = reinterpret_cast<float*>(smem_raw + L::RS_OFF + st * L::RS_BYTES);
+        // the row terms share the dO stage: it is released by dV(g), which waits for
+        // the compute warps to finish dS^T(g)
+        float* rs = reinterpret_cast<float*>(smem_raw + L::RS_OFF + so * L::RS_BYTES);
 #pragma unroll
-        for (int t = 0; t < STEP / 32; ++t) {
+        for (int t = 0; t < KSTEP / 32; ++t) {
           rs[lane + 32 * t] = -rv[t].x;
-          rs[STEP + lane + 32 * t] = -rv[t].y;
+          rs[KSTEP + lane + 32 * t] = -rv[t].y;
         }
-        mbar_arrive(bar(KV_RSFULL + st));
-        if (j + 1 < n) ok = load_q(q_it + 1, j + 1);
+        mbar_arrive(bar(KV_RSFULL + so));
       }
     }
     __syncwarp();
   } else if (warp == 1 || warp == kIssuerB) {
     // ------------------------------------------------------------ MMA issuers
     // An MMA issue occupies the issuing thread for most of the MMA's duration and
-    // the tensor pipe queues only a few, so the products come from two threads:
-    //   warp 1 (chain P):  S^T(g+1) = K Q^T, then dV += P^T(g) dO
-    //   warp 10 (chain dS): dK += dS^T(g) Q, then dP^T(g+1) = V dO^T
+    // the tensor pipe queues only a few, so the products come from two threads.
     // Each commit covers only its own thread's MMAs; resources used by both chains
-    // (Q/dO stages, K/V tiles, the accumulators) take one commit from each.
+    // (Q / dO stages, the accumulators) take one commit from each.
     if (lane == 0) {
       const bool chain_p = warp == 1;
-      constexpr uint32_t idesc_s = idesc_bf16(TILE, STEP, 0, 0);
       constexpr uint32_t idesc_dv = idesc_bf16(TILE, DV, 0, 1);
       constexpr uint32_t idesc_dk = idesc_bf16(TILE, DQK, 0, 1);
-      uint32_t kv_it = 0, q_it = 0, g = 0, a_it = 0;
+      uint32_t a_it = 0;
       bool ok = true;
-      WorkItem nxt = blockIdx.x < (unsigned)n_items ? load_item(list, blockIdx.x) : WorkItem{};
-      for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
-        const WorkItem w = nxt;
-        if (it + (int)gridDim.x < n_items) nxt = load_item(list, it + gridDim.x);
-        const int n = w.cost;
-        if (n == 0) continue;
-        const uint32_t ks = kv_it % NKV;
-        if (!mbar_wait(bar(KV_KVFULL + ks), (kv_it / NKV) & 1, abort, status)) break;
-        const uint32_t k_tile = sb + L::K_OFF + ks * L::K_BYTES;
-        const uint32_t v_tile = sb + L::V_OFF + ks * L::V_BYTES;
-        auto q_tile = [&](uint32_t qq) { return sb + L::Q_OFF + (qq % NQ) * L::Q_BYTES; };
-        auto o_tile = [&](uint32_t qq) { return sb + L::O_OFF + (qq % NO) * L::O_BYTES; };
-        const uint32_t q_base = q_it;
-        // S^T(gg) into X[gg & 1]: that buffer held dP^T(gg-1), loaded by the compute
-        // warps, and before it P^T / dS^T(gg-2), read by dV(gg-2) (this thread) and
-        // dK(gg-2) (the other issuer).
-        auto issue_s = [&](uint32_t gg, uint32_t qq) {
-          if (!mbar_wait(bar(KV_QFULL + qq % NQ), (qq / NQ) & 1, abort, status) ||
-              !mbar_wait(bar(KV_DPEMPTY), (gg & 1) ^ 1, abort, status) ||
-              !mbar_wait(bar(KV_KDONE + (gg & 1)), ((gg >> 1) & 1) ^ 1, abort, status))
-            return false;
-          tc_fence_after();
-          const uint64_t da = sw128_desc(k_tile, 16, 1024), db = sw128_desc(q_tile(qq), 16, 1024);
+      // Score product of step c into X[g & 1]: S^T (chain P) once dK(g-2) has read
+      // the buffer (dV(g-2) was issued earlier by this thread); dP^T (chain dS)
+      // once the compute warps have loaded S^T(g) from it.
+      auto issue_score = [&](const StepCursor& c) {
+        const uint32_t b = c.g & 1;
+        const uint32_t st = chain_p ? c.q % NQ : c.q % NO;
+        const uint32_t ph = chain_p ? (c.q / NQ) & 1 : (c.q / NO) & 1;
+        if ((c.j == 0 && !mbar_wait(bar(chain_p ? KV_KFULL : KV_VFULL), c.kv & 1, abort, status)) ||
+            !mbar_wait(bar((chain_p ? KV_QFULL : KV_OFULL) + st), ph, abort, status) ||
+            (chain_p && !mbar_wait(bar(KV_KDONE + b), ((c.g >> 1) & 1) ^ 1, abort, status)) ||
+            (!chain_p && !mbar_wait(bar(KV_SEMPTY + b), (c.g >> 1) & 1, abort, status)))
+          return false;
+        tc_fence_after();
+        const uint32_t a_tile = sb + (chain_p ? L::K_OFF : L::V_OFF);
+        const uint32_t b_tile = chain_p ? sb + L::Q_OFF + st * L::Q_BYTES : sb + L::O_OFF + st * L::O_BYTES;
+        const uint64_t da = sw128_desc(a_tile, 16, 1024), db = sw128_desc(b_tile, 16, 1024);
+        const uint32_t idesc = idesc_bf16(TILE, c.template n16<CAUSAL>(), 0, 0);
+        const uint32_t d_tm = tmem + T_X + b * 128;
 #pragma unroll
-          for (int kk = 0; kk < DQK / 16; ++kk) {
-            const uint32_t off = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;  // descriptor units
-            mma_bf16(tmem + T_X + (gg & 1) * 128, da + off, db + off, idesc_s, kk > 0 ? 1u : 0u);
-          }
-          mma_commit(bar(KV_SFULL));
-          return true;
-        };
-        // dP^T(gg) into X[~gg & 1]: that buffer held S^T(gg-1) and P^T / dS^T(gg-1),
-        // read by dK(gg-1) (this thread) and dV(gg-1) (the other issuer).
-        auto issue_dp = [&](uint32_t gg, uint32_t qq) {
-          if (!mbar_wait(bar(KV_OFULL + qq % NO), (qq / NO) & 1, abort, status) ||
-              (gg > 0 && !mbar_wait(bar(KV_VDONE + ((gg - 1) & 1)), ((gg - 1) >> 1) & 1, abort, status)))
-            return false;
-          tc_fence_after();
-          const uint64_t da = sw128_desc(v_tile, 16, 1024), db = sw128_desc(o_tile(qq), 16, 1024);
-#pragma unroll
-          for (int kk = 0; kk < DV / 16; ++kk) {
-            const uint32_t off = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
-            mma_bf16(tmem + T_X + ((gg & 1) ^ 1) * 128, da + off, db + off, idesc_s, kk > 0 ? 1u : 0u);
-          }
-          mma_commit(bar(KV_DPFULL));
-          return true;
-        };
-        ok = chain_p ? issue_s(g, q_base) : issue_dp(g, q_base);
-        if (ok && n == 1) mma_commit(bar(KV_KVEMPTY + ks));
-        for (int j = 0; j < n && ok; ++j, ++g) {
-          const uint32_t qq = q_base + j;            // this step's Q and dO stages
-          const uint32_t xb = T_X + (g & 1) * 128;  // P^T / dS^T of this step
-          if (!mbar_wait(bar(chain_p ? KV_PFULL : KV_DSFULL), g & 1, abort, status) ||
-              (j == 0 && !mbar_wait(bar(KV_ACCEMPTY), (a_it & 1) ^ 1, abort, status))) {
-            ok = false;
-            break;
-          }
-          if (chain_p) {
-            // the compute warps need S^T(g+1) next: issue it ahead of dV(g), and let
-            // the other issuer know, so that dK(g) queues behind it
-            if (j + 1 < n) {
-              if (!(ok = issue_s(g + 1, q_base + j + 1))) break;
-              if (j + 2 == n) mma_commit(bar(KV_KVEMPTY + ks));  // last S^T of this K tile
-            }
-            mbar_arrive(bar(KV_SISSUED + (g & 1)));
-            tc_fence_after();
-            const uint64_t db = sw128_desc(o_tile(qq), 16384, 1024);
-#pragma unroll
-            for (int kk = 0; kk < STEP / 16; ++kk)
-              mma_bf16_tmem_a(tmem + T_DV, xb + (kk >> 2) * 64 + (kk & 3) * 8, db + ((kk * 2048) >> 4),
-                              idesc_dv, (j > 0 || kk > 0) ? 1u : 0u);
-            mma_commit(bar(KV_VDONE + (g & 1)));
-            mma_commit(bar(KV_QEMPTY + qq % NQ));
-            mma_commit(bar(KV_OEMPTY + qq % NO));
-            if (j + 1 == n) mma_commit(bar(KV_ACCFULL));
-          } else {
-            if (!mbar_wait(bar(KV_SISSUED + (g & 1)), (g >> 1) & 1, abort, status)) { ok = false; break; }
-            tc_fence_after();
-            const uint64_t db = sw128_desc(q_tile(qq), 16384, 1024);
-#pragma unroll
-            for (int kk = 0; kk < STEP / 16; ++kk)
-              mma_bf16_tmem_a(tmem + T_DK, xb + (kk >> 2) * 64 + 32 + (kk & 3) * 8, db + ((kk * 2048) >> 4),
-                              idesc_dk, (j > 0 || kk > 0) ? 1u : 0u);
-            mma_commit(bar(KV_KDONE + (g & 1)));
-            mma_commit(bar(KV_QEMPTY + qq % NQ));
-            mma_commit(bar(KV_OEMPTY + qq % NO));
-            if (j + 1 == n) {
-              mma_commit(bar(KV_ACCFULL));
-            } else {
-              if (!(ok = issue_dp(g + 1, q_base + j + 1))) break;
-              if (j + 2 == n) mma_commit(bar(KV_KVEMPTY + ks));  // last dP^T of this V tile
-            }
-          }
+        for (int kk = 0; kk < (chain_p ? DQK : DV) / 16; ++kk) {
+          const uint32_t off = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;  // descriptor units
+          mma_bf16(d_tm, da + off, db + off, idesc, kk > 0 ? 1u : 0u);
         }
-        if (!ok) break;
-        q_it += n;
-        ++kv_it;
-        ++a_it;
+        mma_commit(bar((chain_p ? KV_SFULL : KV_DPFULL) + b));
+        mma_commit(bar((chain_p ? KV_QEMPTY : KV_OEMPTY) + st));
+        if (c.last()) mma_commit(bar(chain_p ? KV_KEMPTY : KV_VEMPTY));  // last use of this tile
+        return true;
+      };
+      StepCursor cs, cg;  // cs: next score product (one step ahead); cg: gradient product
+      cs.init(list, n_items);
+      cg = cs;
+      if (cs.valid) {
+        ok = issue_score(cs);
+        cs.advance();
+      }
+      while (ok && cg.valid) {
+        // Issuer A issues S^T(g+1) before dV(g): the compute warps want it next.
+        // Issuer B issues dK(g) before dP^T(g+1): dP^T(g+1) waits for S^T(g+1) to be
+        // loaded, S^T(g+1) waits for dK(g-1), and the epilogue of an item waits for
+        // its last dK, so dK must never queue behind a dP^T.
+        const bool score_first = chain_p;
+        if (score_first && cs.valid) {
+          if (!(ok = issue_score(cs))) break;
+          cs.advance();
+        }
+        // chain P: dV += P^T(g) dO(g); chain dS: dK += dS^T(g) Q(g)
+        const uint32_t b = cg.g & 1;
+        const uint32_t sq = cg.q % NQ, so = cg.q % NO;
+        if (!mbar_wait(bar(KV_PDSFULL + b), (cg.g >> 1) & 1, abort, status) ||
+            (cg.j == 0 && !mbar_wait(bar(KV_ACCEMPTY), (a_it & 1) ^ 1, abort, status))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const int ksteps = cg.template n16<CAUSAL>() >> 4;
+        const uint32_t xb = tmem + T_X + b * 128 + (chain_p ? 0 : 32);  // P^T or dS^T
+        const uint64_t db = sw128_desc(chain_p ? sb + L::O_OFF + so * L::O_BYTES : sb + L::Q_OFF + sq * L::Q_BYTES,
+                                       16384, 1024);
+#pragma unroll
+        for (int kk = 0; kk < KSTEP / 16; ++kk)
+          if (kk < ksteps)
+            mma_bf16_tmem_a(tmem + (chain_p ? T_DV : T_DK), xb + (kk >> 2) * 64 + (kk & 3) * 8,
+                            db + ((kk * 2048) >> 4), chain_p ? idesc_dv : idesc_dk,
+                            (cg.j > 0 || kk > 0) ? 1u : 0u);
+        if (chain_p) {
+          mma_commit(bar(KV_OEMPTY + so));
+        } else {
+          mma_commit(bar(KV_KDONE + b));
+          mma_commit(bar(KV_QEMPTY + sq));
+        }
+        if (cg.last()) {
+          mma_commit(bar(KV_ACCFULL));
+          ++a_it;
+        }
+        if (!score_first && cs.valid) {
+          if (!(ok = issue_score(cs))) break;
+          cs.advance();
+        }
+        cg.advance();
       }
     }
     __syncwarp();
@@ -403,7 +433,7 @@ tc_dkdv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
     // Warps 2..5 and 6..9 each cover all 128 keys (TMEM lanes); the first group
     // handles query columns [0,64) of every step and the first half of the dK/dV
     // columns in the epilogue, the second group the other halves.  Each group
-    // writes only inside its own columns.
+    // reads and writes only inside its own columns.
     const int half = (warp - 2) >> 2;
     const int r = 32 * (warp & 3) + lane;  // key of the tile = TMEM lane
     const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
@@ -412,7 +442,7 @@ tc_dkdv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
     const float2 cc = make_float2(c_score, c_score);
     const float2 hc = make_float2(0.5f * c_score, 0.5f * c_score);
     const float2 one = make_float2(1.f, 1.f);
-    constexpr int HC = STEP / 2;  // query columns per group
+    constexpr int HC = KSTEP / 2;  // query columns per group
     uint32_t q_it = 0, s_it = 0, a_it = 0;
     bool ok = true;
     WorkItem nxt = blockIdx.x < (unsigned)n_items ? load_item(list, blockIdx.x) : WorkItem{};
@@ -427,21 +457,30 @@ tc_dkdv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
       const float inv_len = 1.0f / (float)max(Lq, 1);
       const float2 hl = make_float2(0.5f * inv_len, 0.5f * inv_len);
       const float2 il = make_float2(inv_len, inv_len);
-      const int qs0 = CAUSAL ? key0 / STEP : 0;
+      const int qs0 = CAUSAL ? key0 / KSTEP : 0;
       for (int step = 0; step < n; ++step, ++q_it, ++s_it) {
-        // S^T, then P^T and dS^T, in X[s_it & 1]; dP^T in the other buffer
-        const uint32_t s_tm = tmem + lane_base + T_X + (s_it & 1) * 128 + half * HC;
-        const uint32_t p_tm = tmem + lane_base + T_X + ((s_it & 1) ^ 1) * 128 + half * HC;
-        if (!mbar_wait(bar(KV_SFULL), s_it & 1, abort, status)) { ok = false; break; }
+        const uint32_t b = s_it & 1;
+        const uint32_t x_tm = tmem + lane_base + T_X + b * 128 + half * HC;  // this group's columns
+        const int i0 = (qs0 + step) * KSTEP + half * HC;
+        if (!mbar_wait(bar(KV_SFULL + b), (s_it >> 1) & 1, abort, status)) { ok = false; break; }
         tc_fence_after();
+        if (Lq - i0 <= 0) {
+          // No valid query among this group's columns: the step's MMAs stop before
+          // them (N and K are trimmed to the valid rows), so only the arrivals remain.
+          mbar_arrive(bar(KV_SEMPTY + b));
+          if (!mbar_wait(bar(KV_DPFULL + b), (s_it >> 1) & 1, abort, status)) { ok = false; break; }
+          mbar_arrive(bar(KV_PDSFULL + b));
+          continue;
+        }
         float sv[HC];
-        tmem_ld32(s_tm, sv);
-        tmem_ld32(s_tm + 32, sv + 32);
+        tmem_ld32(x_tm, sv);
+        tmem_ld32(x_tm + 32, sv + 32);
         tmem_wait_ld();
+        tc_fence_before();
+        mbar_arrive(bar(KV_SEMPTY + b));  // dP^T(s_it) may overwrite the buffer
         const uint32_t st = q_it % NO;
         if (!mbar_wait(bar(KV_RSFULL + st), (q_it / NO) & 1, abort, status)) { ok = false; break; }
         const float* rs = reinterpret_cast<const float*>(smem_raw + L::RS_OFF + st * L::RS_BYTES) + half * HC;
-        const int i0 = (qs0 + step) * STEP + half * HC;
         // valid queries of this group's columns for key j: i < Lq and (causal) i >= j
         const int lo = CAUSAL ? j - i0 : 0;
         const int hi = j < Lk ? Lq - i0 : 0;
@@ -468,34 +507,30 @@ tc_dkdv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
           }
           pk[c / 2] = pack_bf16(pv.x, pv.y);
         }
-        tmem_st32(s_tm, reinterpret_cast<const float*>(pk));
-        tmem_wait_st();
-        tc_fence_before();
-        mbar_arrive(bar(KV_PFULL));
         // dS^T = P^T (dP^T - D)  or  dP^T SiLU'(u)/L
-        if (!mbar_wait(bar(KV_DPFULL), s_it & 1, abort, status)) { ok = false; break; }
+        if (!mbar_wait(bar(KV_DPFULL + b), (s_it >> 1) & 1, abort, status)) { ok = false; break; }
         tc_fence_after();
         float dp[HC];
-        tmem_ld32(p_tm, dp);
-        tmem_ld32(p_tm + 32, dp + 32);
+        tmem_ld32(x_tm, dp);
+        tmem_ld32(x_tm + 32, dp + 32);
         tmem_wait_ld();
-        tc_fence_before();
-        mbar_arrive(bar(KV_DPEMPTY));  // S^T(s_it+1) may overwrite the dP^T columns
         uint32_t dk2[HC / 2];
 #pragma unroll
         for (int c = 0; c < HC; c += 2) {
           const float2 d = make_float2(dp[c], dp[c + 1]);
           float2 ds;
           if (ACT == kActSoftmax)
-            ds = fmul2(unpack_bf16(pk[c / 2]), fadd2(d, *reinterpret_cast<const float2*>(rs + STEP + c)));
+            ds = fmul2(unpack_bf16(pk[c / 2]), fadd2(d, *reinterpret_cast<const float2*>(rs + KSTEP + c)));
           else
             ds = fmul2(d, unpack_bf16(fk[c / 2]));
           dk2[c / 2] = pack_bf16(ds.x, ds.y);
         }
-        tmem_st32(s_tm + 32, reinterpret_cast<const float*>(dk2));  // dS^T after P^T
+        // P^T then dS^T over this group's own, already loaded columns
+        tmem_st32(x_tm, reinterpret_cast<const float*>(pk));
+        tmem_st32(x_tm + 32, reinterpret_cast<const float*>(dk2));
         tmem_wait_st();
         tc_fence_before();
-        mbar_arrive(bar(KV_DSFULL));
+        mbar_arrive(bar(KV_PDSFULL + b));
       }
       if (!ok) break;
       // ---------------------------------------------------------- epilogue
@@ -994,7 +1029,8 @@ cudaError_t dq_t(const Maps& m, const Problem& p, const float2* rowstat, void* d
 
 }  // namespace
 
-SchedConfig tc_bwd_sched(const Problem&) { return SchedConfig{TILE, STEP, TILE, STEP, 1, 1, 0}; }
+// q-list: 128-row tiles over 128-key steps (dQ); k-list: 128-key tiles over 128-row steps (dK/dV)
+SchedConfig tc_bwd_sched(const Problem&) { return SchedConfig{TILE, STEP, TILE, KSTEP, 1, 1, 0}; }
 
 cudaError_t launch_tc_rowstat(const Problem& p, const void* o, const void* dout, const float* lse,
                               const Workspace& ws, cudaStream_t s) {
