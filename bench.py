@@ -128,57 +128,93 @@ def measured_traffic(kind, workload):
 
 
 class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled every 50 ms in the background.
+
+    Each line is stamped with the host time it arrived; the summary covers the lines
+    that arrived inside the marked window (``mark_start`` / ``mark_end``), or, when
+    the window is shorter than the sampling period, the nearest line on each side.
+    """
     FIELDS = ("clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,"
               "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
               "clocks_event_reasons.sw_power_cap")
+    NAMES = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
 
     def __init__(self, device_index):
         self.proc = None
         self.dev = device_index
+        self.stamped = []
+        self.t0 = self.t1 = None
+
+    def _reader(self):
+        for line in self.proc.stdout:
+            if line.strip():
+                self.stamped.append((time.time(), line))
 
     def __enter__(self):
+        import threading
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.dev), "--query-gpu=" + self.FIELDS,
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "50"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._reader, daemon=True)
+            self.thread.start()
+            deadline = time.time() + 3.0  # let the sampler come up before the timed region
+            while not self.stamped and time.time() < deadline:
+                time.sleep(0.01)
         except Exception:
             self.proc = None
         return self
 
+    def mark_start(self):
+        self.t0 = time.time()
+
+    def mark_end(self):
+        self.t1 = time.time()
+        if self.proc is not None:  # one more sample after the window
+            n = len(self.stamped)
+            deadline = time.time() + 0.5
+            while len(self.stamped) == n and time.time() < deadline:
+                time.sleep(0.01)
+
     def __exit__(self, *exc):
-        self.lines = []
         if self.proc is not None:
             self.proc.terminate()
             try:
-                out, _ = self.proc.communicate(timeout=5)
+                self.proc.wait(timeout=5)
             except Exception:
                 self.proc.kill()
-                out, _ = self.proc.communicate()
-            self.lines = [l for l in out.splitlines() if l.strip()]
+            self.thread.join(timeout=2)
 
     def summary(self):
-        if not getattr(self, "lines", None):
-            return None
-        sm, mx = [], []
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = set()
-        for l in self.lines:
+        rows = []
+        for t, l in self.stamped:
             parts = [x.strip() for x in l.split(",")]
             if len(parts) < 6:
                 continue
             try:
-                sm.append(float(parts[0]))
-                mx.append(float(parts[1]))
+                rows.append((t, float(parts[0]), float(parts[1]), parts[2:6]))
             except ValueError:
                 continue
-            for n, val in zip(names, parts[2:6]):
+        if not rows:
+            return None
+        t0 = self.t0 if self.t0 is not None else rows[0][0]
+        t1 = self.t1 if self.t1 is not None else rows[-1][0]
+        inside = [r for r in rows if t0 <= r[0] <= t1]
+        where = "during the timed region"
+        if not inside:  # region shorter than the sampling period: nearest on each side
+            before = [r for r in rows if r[0] < t0][-1:]
+            after = [r for r in rows if r[0] > t1][:1]
+            inside = before + after
+            where = "nearest samples around a %.0f ms timed region" % ((t1 - t0) * 1e3)
+        reasons = set()
+        for r in inside:
+            for n, val in zip(self.NAMES, r[3]):
                 if val.lower().startswith("active"):
                     reasons.add(n)
-        if not sm:
-            return None
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
-                "reasons": sorted(reasons)}
+        return {"sm_mhz": statistics.median(r[1] for r in inside),
+                "sm_max_mhz": max(r[2] for r in inside), "samples": len(inside),
+                "window": where, "reasons": sorted(reasons)}
 
 
 # ----------------------------------------------------------------------------- our arm
@@ -286,12 +322,14 @@ def run_ours(args):
     jfa.jfa_profile_reset()
     jfa.jfa_profile_enable(True)
     with ClockSampler(local) as clk:
+        clk.mark_start()
         for i in range(args.steps):
             flush.fill_(float(i))  # evicts the inputs from L2 between timed steps
             starts[i].record(stream)
             step()
             ends[i].record(stream)
         torch.cuda.synchronize()
+        clk.mark_end()
     jfa.jfa_profile_enable(False)
     ms_total = max_over_ranks(sum(s.elapsed_time(e) for s, e in zip(starts, ends)), world, dev)
     if world > 1:
