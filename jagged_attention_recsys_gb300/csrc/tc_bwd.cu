@@ -383,10 +383,11 @@ tc_dkdv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
       }
       while (ok && cg.valid) {
         // Issuer A issues S^T(g+1) before dV(g): the compute warps want it next.
-        // Issuer B issues dK(g) before dP^T(g+1): dP^T(g+1) waits for S^T(g+1) to be
-        // loaded, S^T(g+1) waits for dK(g-1), and the epilogue of an item waits for
-        // its last dK, so dK must never queue behind a dP^T.
-        const bool score_first = chain_p;
+        // Issuer B issues dK(g) before dP^T(g+1) (dP^T(g+1) waits for S^T(g+1) to be
+        // loaded, and S^T(g+1) waits for dK(g-1)), except at an item's first step:
+        // there dK(g) waits for the previous item's epilogue, which the compute warps
+        // run after this step, so dP^T(g+1) goes first.
+        const bool score_first = chain_p || cg.j == 0;
         if (score_first && cs.valid) {
           if (!(ok = issue_score(cs))) break;
           cs.advance();
@@ -445,6 +446,35 @@ tc_dkdv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
     constexpr int HC = KSTEP / 2;  // query columns per group
     uint32_t q_it = 0, s_it = 0, a_it = 0;
     bool ok = true;
+    // The epilogue of an item (dK, dV from TMEM to HBM) runs after the next item's
+    // first step, when its last dV / dK products have long completed; the next
+    // item's first dV / dK wait for it (ACCEMPTY).
+    bool pend = false, pend_key_ok = false;
+    int64_t pend_krow = 0;
+    auto epilogue = [&]() -> bool {
+      if (!mbar_wait(bar(KV_ACCFULL), a_it & 1, abort, status)) return false;
+      ++a_it;
+      tc_fence_after();
+      float x[DQK / 2];
+#pragma unroll
+      for (int c = 0; c < DQK / 64; ++c) tmem_ld32(tmem + lane_base + T_DK + half * (DQK / 2) + 32 * c, x + 32 * c);
+      float y[DV / 2];
+#pragma unroll
+      for (int c = 0; c < DV / 64; ++c) tmem_ld32(tmem + lane_base + T_DV + half * (DV / 2) + 32 * c, y + 32 * c);
+      tmem_wait_ld();
+      tc_fence_before();
+      mbar_arrive(bar(KV_ACCEMPTY));
+      if (pend_key_ok) {
+#pragma unroll
+        for (int c = 0; c < DQK / 64; ++c)
+          store_row_bf16(dk + pend_krow * DQK + half * (DQK / 2) + 32 * c, x + 32 * c, p.scale);
+#pragma unroll
+        for (int c = 0; c < DV / 64; ++c)
+          store_row_bf16(dv + pend_krow * DV + half * (DV / 2) + 32 * c, y + 32 * c, 1.f);
+      }
+      pend = false;
+      return true;
+    };
     WorkItem nxt = blockIdx.x < (unsigned)n_items ? load_item(list, blockIdx.x) : WorkItem{};
     for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
       const WorkItem w = nxt;
@@ -470,6 +500,7 @@ tc_dkdv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
           mbar_arrive(bar(KV_SEMPTY + b));
           if (!mbar_wait(bar(KV_DPFULL + b), (s_it >> 1) & 1, abort, status)) { ok = false; break; }
           mbar_arrive(bar(KV_PDSFULL + b));
+          if (pend && !epilogue()) { ok = false; break; }
           continue;
         }
         float sv[HC];
@@ -531,32 +562,17 @@ tc_dkdv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
         tmem_wait_st();
         tc_fence_before();
         mbar_arrive(bar(KV_PDSFULL + b));
+        if (pend && !epilogue()) { ok = false; break; }
       }
       if (!ok) break;
-      // ---------------------------------------------------------- epilogue
+      // ---------------------------------------------------------- epilogue (deferred)
       const bool key_ok = j < Lk;
       const int64_t krow = (k0 + j) * p.heads + h;
       if (n > 0) {
-        if (!mbar_wait(bar(KV_ACCFULL), a_it & 1, abort, status)) { ok = false; break; }
-        ++a_it;
-        tc_fence_after();
-        float x[DQK / 2];
-#pragma unroll
-        for (int c = 0; c < DQK / 64; ++c) tmem_ld32(tmem + lane_base + T_DK + half * (DQK / 2) + 32 * c, x + 32 * c);
-        float y[DV / 2];
-#pragma unroll
-        for (int c = 0; c < DV / 64; ++c) tmem_ld32(tmem + lane_base + T_DV + half * (DV / 2) + 32 * c, y + 32 * c);
-        tmem_wait_ld();
-        tc_fence_before();
-        mbar_arrive(bar(KV_ACCEMPTY));
-        if (key_ok) {
-#pragma unroll
-          for (int c = 0; c < DQK / 64; ++c)
-            store_row_bf16(dk + krow * DQK + half * (DQK / 2) + 32 * c, x + 32 * c, p.scale);
-#pragma unroll
-          for (int c = 0; c < DV / 64; ++c)
-            store_row_bf16(dv + krow * DV + half * (DV / 2) + 32 * c, y + 32 * c, 1.f);
-        }
+        if (pend && !epilogue()) { ok = false; break; }  // defensive: flushed after step 0
+        pend = true;
+        pend_key_ok = key_ok;
+        pend_krow = krow;
       } else if (key_ok) {
         const float z[32] = {0.f};
 #pragma unroll
@@ -565,6 +581,7 @@ tc_dkdv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
         for (int c = 0; c < DV / 64; ++c) store_row_bf16(dv + krow * DV + half * (DV / 2) + 32 * c, z, 1.f);
       }
     }
+    if (ok && pend) ok = epilogue();
   }
 
   tc_fence_before();
