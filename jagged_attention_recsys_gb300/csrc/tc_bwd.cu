@@ -870,6 +870,29 @@ tc_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
     const uint32_t p_tm = tmem + lane_base + T_DP + half * HC;
     uint32_t s_it = 0, d_it = 0, a_it = 0;
     bool ok = true;
+    // The epilogue of an item (dQ from TMEM to HBM) runs after the next item's first
+    // step, when its last dQ product has long completed; the next item's first dQ
+    // product waits for it (ACCEMPTY).
+    bool pend = false, pend_row_ok = false;
+    int64_t pend_orow = 0;
+    auto epilogue = [&]() -> bool {
+      if (!mbar_wait(bar(Q_ACCFULL), a_it & 1, abort, status)) return false;
+      ++a_it;
+      tc_fence_after();
+      float x[DQK / 2];
+#pragma unroll
+      for (int c = 0; c < DQK / 64; ++c) tmem_ld32(tmem + lane_base + T_DQ + half * (DQK / 2) + 32 * c, x + 32 * c);
+      tmem_wait_ld();
+      tc_fence_before();
+      mbar_arrive(bar(Q_ACCEMPTY));
+      if (pend_row_ok) {
+#pragma unroll
+        for (int c = 0; c < DQK / 64; ++c)
+          store_row_bf16(dq + pend_orow * DQK + half * (DQK / 2) + 32 * c, x + 32 * c, p.scale);
+      }
+      pend = false;
+      return true;
+    };
     WorkItem nxt = blockIdx.x < (unsigned)n_items ? load_item(list, blockIdx.x) : WorkItem{};
     for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
       const WorkItem w = nxt;
@@ -939,30 +962,22 @@ tc_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
         tmem_wait_st();
         tc_fence_before();
         mbar_arrive(bar(Q_DSFULL));
+        if (pend && !epilogue()) { ok = false; break; }
       }
       if (!ok) break;
       const int64_t orow = (q0 + i) * p.heads + h;
-      if (n > 0) {
-        if (!mbar_wait(bar(Q_ACCFULL), a_it & 1, abort, status)) { ok = false; break; }
-        ++a_it;
-        tc_fence_after();
-        float x[DQK / 2];
-#pragma unroll
-        for (int c = 0; c < DQK / 64; ++c) tmem_ld32(tmem + lane_base + T_DQ + half * (DQK / 2) + 32 * c, x + 32 * c);
-        tmem_wait_ld();
-        tc_fence_before();
-        mbar_arrive(bar(Q_ACCEMPTY));
-        if (row_ok) {
-#pragma unroll
-          for (int c = 0; c < DQK / 64; ++c)
-            store_row_bf16(dq + orow * DQK + half * (DQK / 2) + 32 * c, x + 32 * c, p.scale);
-        }
+      if (n > 0) {  // epilogue deferred to the next item's first step
+        if (pend && !epilogue()) { ok = false; break; }
+        pend = true;
+        pend_row_ok = row_ok;
+        pend_orow = orow;
       } else if (row_ok) {
         const float z[32] = {0.f};
 #pragma unroll
         for (int c = 0; c < DQK / 64; ++c) store_row_bf16(dq + orow * DQK + half * (DQK / 2) + 32 * c, z, 1.f);
       }
     }
+    if (ok && pend) ok = epilogue();
   }
 
   tc_fence_before();

@@ -278,6 +278,31 @@ tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     float* red = reinterpret_cast<float*>(smem_raw + L::RED_OFF);  // [2 steps][128 rows][2]
     uint32_t p_it = 0, o_it = 0, l_it = 0;  // p_it: global step (S / P buffer p_it & 1)
     bool ok = true;
+    // The output of an item (O from TMEM to HBM) is written after the next item's
+    // first P, when its last PV product has long completed; the next item's first
+    // PV waits for it (OEMPTY).  The row statistics are settled before that.
+    bool pend = false, pend_row_ok = false;
+    int64_t pend_orow = 0;
+    float pend_norm = 0.f, pend_lse = 0.f;
+    auto epilogue = [&]() -> bool {
+      if (!mbar_wait(bar(B_OFULL), o_it & 1, abort, status)) return false;
+      ++o_it;
+      tc_fence_after();
+      float ov[DV / 2];
+#pragma unroll
+      for (int c = 0; c < DV / 64; ++c) tmem_ld32(tmem + lane_base + T_O + half * (DV / 2) + 32 * c, ov + 32 * c);
+      tmem_wait_ld();
+      tc_fence_before();
+      mbar_arrive(bar(B_OEMPTY));
+      if (pend_row_ok) {
+#pragma unroll
+        for (int c = 0; c < DV / 64; ++c)
+          store32_bf16(out + pend_orow * DV + half * (DV / 2) + 32 * c, ov + 32 * c, pend_norm);
+        if (ACT == kActSoftmax && half == 0 && lse != nullptr) lse[pend_orow] = pend_lse;
+      }
+      pend = false;
+      return true;
+    };
     WorkItem nxt = blockIdx.x < (unsigned)n_items ? load_item(list, blockIdx.x) : WorkItem{};
     for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
       const WorkItem w = nxt;
@@ -382,9 +407,10 @@ tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         tmem_wait_st();
         tc_fence_before();
         mbar_arrive(bar(B_PFULL + b));
+        if (pend && !epilogue()) { ok = false; break; }
       }
       if (!ok) break;
-      // ---------------------------------------------------------- epilogue
+      // ---------------------------------------------------------- epilogue (deferred)
       const bool row_ok = i < Lq;
       const int64_t orow = ((int64_t)w.q0 + i) * p.heads + h;
       if (n > 0) {
@@ -401,22 +427,12 @@ tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
           ++l_it;
           lt = rl[r * 2] + rl[r * 2 + 1];
         }
-        if (!mbar_wait(bar(B_OFULL), o_it & 1, abort, status)) { ok = false; break; }
-        ++o_it;
-        tc_fence_after();
-        float ov[DV / 2];
-#pragma unroll
-        for (int c = 0; c < DV / 64; ++c) tmem_ld32(tmem + lane_base + T_O + half * (DV / 2) + 32 * c, ov + 32 * c);
-        tmem_wait_ld();
-        tc_fence_before();
-        mbar_arrive(bar(B_OEMPTY));
-        const float norm = ACT == kActSoftmax ? (lt > 0.f ? 1.f / lt : 0.f) : 1.f;
-        if (row_ok) {
-#pragma unroll
-          for (int c = 0; c < DV / 64; ++c) store32_bf16(out + orow * DV + half * (DV / 2) + 32 * c, ov + 32 * c, norm);
-          if (ACT == kActSoftmax && half == 0 && lse != nullptr)
-            lse[orow] = lt > 0.f ? (m + log2f(lt)) * kLn2 : -INFINITY;
-        }
+        if (pend && !epilogue()) { ok = false; break; }  // defensive: flushed after step 0
+        pend = true;
+        pend_row_ok = row_ok;
+        pend_orow = orow;
+        pend_norm = ACT == kActSoftmax ? (lt > 0.f ? 1.f / lt : 0.f) : 1.f;
+        pend_lse = lt > 0.f ? (m + log2f(lt)) * kLn2 : -INFINITY;
       } else if (row_ok) {
         const float z[32] = {0.f};
 #pragma unroll
@@ -424,6 +440,7 @@ tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         if (ACT == kActSoftmax && half == 0 && lse != nullptr) lse[orow] = -INFINITY;
       }
     }
+    if (ok && pend) ok = epilogue();
   }
 
   tc_fence_before();
