@@ -60,7 +60,7 @@ __device__ int block_inclusive_scan(int x, int* warp_tot) {
   if (lane == 31) warp_tot[warp] = x;
   __syncthreads();
   if (warp == 0) {
-    int t = warp_tot[lane];
+    int t = lane < kWarps ? warp_tot[lane] : 0;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       int y = __shfl_up_sync(0xffffffffu, t, o);
@@ -198,26 +198,24 @@ __device__ void build_list(const Problem& p, const ListSpec& L, const Arrays& A,
     __syncthreads();
   }
 
-  // 6. write the items, one per thread in list order (coalesced 32-byte stores).
-  //    Item i is head i % H of unit u = i / H; the unit belongs to the last list
-  //    position r with first[r] <= u (positions without tiles share their first[]
-  //    with the next one, so the search never lands on them), and is that
-  //    sequence's k-th tile in list order, k = u - first[r].
+  // 6. write the items: warp w takes list positions r = w, w + kWarps, ...; its lanes
+  //    write that sequence's items (tiles heaviest first, heads adjacent) as
+  //    consecutive 32-byte stores.
   const int64_t n_items = (int64_t)carry * p.heads;
-  for (int64_t i = tid; i < n_items; i += kThreads) {
-    const int u = (int)(i / p.heads), h = (int)(i - (int64_t)u * p.heads);
-    int lo = 0, hi = B - 1;
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if (A.first[mid] <= u) lo = mid; else hi = mid - 1;
-    }
-    const int b = A.order[lo];
+  for (int r = warp; r < B; r += kWarps) {
+    const int b = A.order[r];
     const int4 s = A.seq[b];
-    const int t = tile_at(L, p.causal, A.ntile[b], u - A.first[lo]);
-    WorkItem w;
-    w.b = b; w.h = h; w.tile = t; w.cost = cost_of(L, p.causal, s.z, s.w, t);
-    w.q0 = s.x; w.k0 = s.y; w.lq = s.z; w.lk = s.w;
-    list[i] = w;
+    const int n = A.ntile[b];
+    const int cnt = n * p.heads;
+    WorkItem* out = list + (int64_t)A.first[r] * p.heads;
+    for (int e = lane; e < cnt; e += 32) {
+      const int k = e / p.heads, h = e - k * p.heads;
+      const int t = tile_at(L, p.causal, n, k);
+      WorkItem w;
+      w.b = b; w.h = h; w.tile = t; w.cost = cost_of(L, p.causal, s.z, s.w, t);
+      w.q0 = s.x; w.k0 = s.y; w.lq = s.z; w.lk = s.w;
+      out[e] = w;
+    }
   }
   if (tid == 0) *n_out = (int)n_items;
   __syncthreads();
