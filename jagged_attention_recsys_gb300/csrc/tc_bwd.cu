@@ -7,15 +7,17 @@
 //   * row pass      rowstat[h][t] = (lse * log2 e, D = <dO, O>), head-major so
 //                   a 64-row block of one head is contiguous;
 //   * dK/dV pass    one item = (sequence, head, 128-key tile).  TMEM holds
-//                   dK, dV and two buffers of S^T = K Q^T and dP^T = V dO^T
-//                   for 64-row query steps; per step the compute warpgroup
-//                   (one key per thread) forms P^T and dS^T = P^T (dP^T - D)
-//                   into swizzled smem and the MMA lane issues dV += P^T dO and
-//                   dK += dS^T Q (Q and dO read MN-major from the same tiles);
+//                   dK, dV and two 128-column step buffers that take, in turn,
+//                   S^T = K Q^T, dP^T = V dO^T and the packed bf16 P^T and
+//                   dS^T = P^T (dP^T - D) for 128-row query steps; the compute
+//                   warpgroups (one key per thread) form P^T and dS^T and two
+//                   issuer warps add dV += P^T dO and dK += dS^T Q with the
+//                   left operand in TMEM (Q and dO read MN-major from the
+//                   tiles S^T and dP^T were read K-major from);
 //   * dQ pass       one item = (sequence, head, 128-row query tile).  TMEM holds
-//                   dQ and two buffers of S = Q K^T, dP = dO V^T over 64-key
-//                   steps; the compute warpgroup (one row per thread) forms dS
-//                   and the MMA lane issues dQ += dS K.
+//                   dQ, two buffers of S = Q K^T and one of dP = dO V^T over
+//                   128-key steps; the compute warpgroups (one row per thread)
+//                   form dS into TMEM and dQ += dS K reads it from there.
 // The SiLU/L variant has no lse and no D: P = SiLU(u)/L and
 // dS = dP SiLU'(u)/L with u = scale s.  Masking is by subtraction as in the
 // forward; masked (query, key) pairs contribute exact zeros.
@@ -25,6 +27,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <type_traits>
+
 #include "tc.h"
 #include "tc_host.h"
 #include "tc_ptx.cuh"
@@ -33,9 +37,16 @@ namespace jfa {
 namespace {
 using namespace tc;
 
-// producer warp 0, MMA issuer warps 1 and 10, compute warpgroups 2..5 and 6..9
-constexpr int kThreads = 352;
-constexpr int kIssuerB = 10;
+// Both passes: producer warp 0, MMA issuer warp 1, G compute warpgroups (warps
+// 2 .. 4G+1), MMA issuer warp 4G+2 and, with P2 = 1, a second producer warp 4G+3.
+template <int G_, int P2 = 0>
+struct Groups {
+  static constexpr int G = G_;
+  static constexpr int kThreads = 32 * (3 + 4 * G + P2);
+  static constexpr int kIssuerB = 2 + 4 * G;
+  static constexpr int kProducer2 = P2 ? 3 + 4 * G : 0;
+  static constexpr int HC = 128 / G;  // query columns of a step per compute warpgroup
+};
 constexpr int TILE = 128;  // keys per dK/dV item, rows per dQ item (MMA M)
 constexpr int STEP = 128;  // query rows per dK/dV step, keys per dQ step (MMA N)
 constexpr float kLog2e = 1.4426950408889634f;
@@ -88,13 +99,14 @@ __device__ __forceinline__ void store_row_bf16(__nv_bfloat16* dst, const float* 
 // rows.  TMEM holds the dK and dV accumulators and two 128-column buffers; step g
 // (counted over the CTA's whole list) uses buffer X[g & 1] three times over:
 //   S^T = K Q^T  ->  loaded by the compute warps  ->  dP^T = V dO^T over it  ->
-//   loaded  ->  P^T and dS^T packed over it (each warpgroup in its own 64
-//   columns: P^T in the first 32, dS^T in the next 32)  ->  read by dV and dK.
+//   loaded  ->  P^T and dS^T packed over it (each compute warpgroup in its own
+//   HC columns: P^T in the first HC/2, dS^T in the next HC/2)  ->  read by dV
+//   and dK.
 // Step g+1 uses the other buffer, so nothing of step g waits for it:
-//   warp 1  (issuer A): S^T(g+1) once dK(g-1) has read X[(g+1) & 1], then
-//                       dV += P^T(g) dO(g)
-//   warp 10 (issuer B): dP^T(g+1) once S^T(g+1) has been loaded, then
-//                       dK += dS^T(g) Q(g)
+//   issuer A (warp 1):        S^T(g+1) once dK(g-1) has read X[(g+1) & 1], then
+//                             dV += P^T(g) dO(g)
+//   issuer B (the last warp): dP^T(g+1) once S^T(g+1) has been loaded, then
+//                             dK += dS^T(g) Q(g)
 // The compute warps compute P^T(g) while dP^T(g) runs and find S^T(g+1) ready
 // when they finish step g.  Only the step's valid query rows (rounded up to 16)
 // enter the MMAs.  K and V have separate slots, so the next item's K loads as
@@ -182,15 +194,32 @@ struct StepCursor {
   }
 };
 
+// dK/dV: the SiLU/L variant has about three times the per-element work of the softmax
+// one (two MUFU operations and twice the FMAs per key and query), and its compute
+// warps, not the tensor pipe, set the pace; four groups of 32 query columns hide that
+// work's latencies with twice the warps.  Softmax keeps two groups of 64 columns,
+// which leave its issuers' warp schedulers less busy.
+template <int ACT>
+using KvGroups = Groups<ACT == kActSoftmax ? 2 : 4, 1>;
+// dQ: two groups of 64 key columns for both activations (four were no faster), and
+// two producers: Q and K in warp 0, dO and V in the last warp, so that a V load
+// never queues behind a K load that waits for its slot (K(j+2) takes the slot of
+// K(j-1), which dQ(j-1) frees late in the step, while dP(j+1) wants V(j+1) early).
+using QGroups = Groups<2, 1>;
+
 template <int DQK, int DV, int ACT, bool CAUSAL>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(KvGroups<ACT>::kThreads, 1)
 tc_dkdv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
                const Problem p, const float2* __restrict__ rowstat,
                __nv_bfloat16* __restrict__ dk, __nv_bfloat16* __restrict__ dv, WsHeader* hdr,
                const WorkItem* __restrict__ list) {
   using L = KvLayout<DQK, DV>;
+  using Gr = KvGroups<ACT>;
   constexpr int NQ = L::NQ, NO = L::NO;
+  constexpr int HC = Gr::HC;  // query columns per compute warpgroup
+  static_assert(HC * Gr::G == KSTEP && HC % 32 == 0, "the compute warpgroups split a step's query rows");
+  constexpr uint32_t kCompute = 32 * 4 * Gr::G;  // compute threads
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t sb = (raw + L::SMALL + 1023u) & ~1023u;  // 128-byte swizzled tiles: 1 KB aligned
@@ -224,13 +253,13 @@ tc_dkdv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(bar(KV_SFULL + s), 1);
-      mbar_init(bar(KV_SEMPTY + s), 256);
+      mbar_init(bar(KV_SEMPTY + s), kCompute);
       mbar_init(bar(KV_DPFULL + s), 1);
-      mbar_init(bar(KV_PDSFULL + s), 256);
+      mbar_init(bar(KV_PDSFULL + s), kCompute);
       mbar_init(bar(KV_KDONE + s), 1);
     }
     mbar_init(bar(KV_ACCFULL), 2);
-    mbar_init(bar(KV_ACCEMPTY), 256);
+    mbar_init(bar(KV_ACCEMPTY), kCompute);
     *abort = 0;
     fence_mbar_init();
   }
@@ -243,11 +272,49 @@ tc_dkdv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
   constexpr uint32_t T_DK = 0, T_DV = 128, T_X = 256;
 
   if (warp == 0) {
-    // ------------------------------------------------------------ producer warp
+    // ------------------------------------------------------------ producer: K and Q
+    // Two producers, so that neither ring waits behind a load of the other: warp 0
+    // loads each item's K and every step's Q, the last warp its V and every step's
+    // dO with the step's row terms.
     if (lane == 0) {
       tma_prefetch_desc(&tm_k);
-      tma_prefetch_desc(&tm_v);
       tma_prefetch_desc(&tm_q);
+      uint32_t kv_it = 0, q_it = 0;
+      bool ok = true;
+      WorkItem nxt = blockIdx.x < (unsigned)n_items ? load_item(list, blockIdx.x) : WorkItem{};
+      for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
+        const WorkItem w = nxt;  // prefetched one item ahead
+        if (it + (int)gridDim.x < n_items) nxt = load_item(list, it + gridDim.x);
+        const int n = w.cost;
+        if (n == 0) continue;
+        const int h = w.h, key0 = w.tile * TILE;
+        const int64_t q0 = w.q0, k0 = w.k0;
+        const int qs0 = CAUSAL ? key0 / KSTEP : 0;
+        if (!mbar_wait(bar(KV_KEMPTY), (kv_it & 1) ^ 1, abort, status)) break;
+        ++kv_it;
+        mbar_expect_tx(bar(KV_KFULL), L::K_BYTES);
+#pragma unroll
+        for (int a = 0; a < DQK / 64; ++a)
+          tma_load_2d(sb + L::K_OFF + a * 16384, &tm_k, h * DQK + a * 64, (int32_t)(k0 + key0), bar(KV_KFULL));
+        for (int j = 0; j < n; ++j, ++q_it) {
+          const uint32_t st = q_it % NQ;
+          if (!mbar_wait(bar(KV_QEMPTY + st), ((q_it / NQ) & 1) ^ 1, abort, status)) {
+            ok = false;
+            break;
+          }
+          mbar_expect_tx(bar(KV_QFULL + st), L::Q_BYTES);
+#pragma unroll
+          for (int a = 0; a < DQK / 64; ++a)
+            tma_load_2d(sb + L::Q_OFF + st * L::Q_BYTES + a * 16384, &tm_q, h * DQK + a * 64,
+                        (int32_t)(q0 + (qs0 + j) * KSTEP), bar(KV_QFULL + st));
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == Gr::kProducer2) {
+    // ------------------------------------------------------------ producer: V, dO, row terms
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_v);
       tma_prefetch_desc(&tm_do);
     }
     uint32_t kv_it = 0, q_it = 0;
@@ -261,32 +328,18 @@ tc_dkdv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
       const int h = w.h, key0 = w.tile * TILE;
       const int64_t q0 = w.q0, k0 = w.k0;
       const int Lq = w.lq;
-      const uint32_t kph = (kv_it & 1) ^ 1;
-      ++kv_it;
       const int qs0 = CAUSAL ? key0 / KSTEP : 0;
-      // K is wanted one step before V (S^T runs a step ahead of dP^T): K, Q(0), V first
-      bool v_done = false;
-      auto load_kv = [&](bool is_k) {
-        if (lane == 0) {
-          ok = mbar_wait(bar(is_k ? KV_KEMPTY : KV_VEMPTY), kph, abort, status);
-          if (ok) {
-            mbar_expect_tx(bar(is_k ? KV_KFULL : KV_VFULL), is_k ? L::K_BYTES : L::V_BYTES);
-            if (is_k) {
+      if (lane == 0) {
+        ok = mbar_wait(bar(KV_VEMPTY), (kv_it & 1) ^ 1, abort, status);
+        if (ok) {
+          mbar_expect_tx(bar(KV_VFULL), L::V_BYTES);
 #pragma unroll
-              for (int a = 0; a < DQK / 64; ++a)
-                tma_load_2d(sb + L::K_OFF + a * 16384, &tm_k, h * DQK + a * 64, (int32_t)(k0 + key0),
-                            bar(KV_KFULL));
-            } else {
-#pragma unroll
-              for (int a = 0; a < DV / 64; ++a)
-                tma_load_2d(sb + L::V_OFF + a * 16384, &tm_v, h * DV + a * 64, (int32_t)(k0 + key0),
-                            bar(KV_VFULL));
-            }
-          }
+          for (int a = 0; a < DV / 64; ++a)
+            tma_load_2d(sb + L::V_OFF + a * 16384, &tm_v, h * DV + a * 64, (int32_t)(k0 + key0), bar(KV_VFULL));
         }
-        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-      };
-      load_kv(true);
+      }
+      ++kv_it;
+      if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) { ok = false; break; }
       for (int j = 0; j < n && ok; ++j, ++q_it) {
         const int i0 = (qs0 + j) * KSTEP;
         // row terms of this step: issue the global loads before waiting for the stage
@@ -296,21 +349,6 @@ tc_dkdv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
           const int c = lane + 32 * t;
           rv[t] = make_float2(0.f, 0.f);
           if (ACT == kActSoftmax && i0 + c < Lq) rv[t] = rowstat[(int64_t)h * p.total_q + q0 + i0 + c];
-        }
-        const uint32_t st = q_it % NQ;
-        ok = mbar_wait(bar(KV_QEMPTY + st), ((q_it / NQ) & 1) ^ 1, abort, status);
-        if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-        if (lane == 0) {
-          mbar_expect_tx(bar(KV_QFULL + st), L::Q_BYTES);
-#pragma unroll
-          for (int a = 0; a < DQK / 64; ++a)
-            tma_load_2d(sb + L::Q_OFF + st * L::Q_BYTES + a * 16384, &tm_q, h * DQK + a * 64,
-                        (int32_t)(q0 + i0), bar(KV_QFULL + st));
-        }
-        if (!v_done) {
-          load_kv(false);
-          v_done = true;
-          if (!ok) break;
         }
         const uint32_t so = q_it % NO;
         ok = mbar_wait(bar(KV_OEMPTY + so), ((q_it / NO) & 1) ^ 1, abort, status);
@@ -334,7 +372,7 @@ tc_dkdv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
       }
     }
     __syncwarp();
-  } else if (warp == 1 || warp == kIssuerB) {
+  } else if (warp == 1 || warp == Gr::kIssuerB) {
     // ------------------------------------------------------------ MMA issuers
     // An MMA issue occupies the issuing thread for most of the MMA's duration and
     // the tensor pipe queues only a few, so the products come from two threads.
@@ -402,13 +440,15 @@ tc_dkdv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
         }
         tc_fence_after();
         const int ksteps = cg.template n16<CAUSAL>() >> 4;
-        const uint32_t xb = tmem + T_X + b * 128 + (chain_p ? 0 : 32);  // P^T or dS^T
+        // P^T or dS^T: each group's HC columns hold P^T of its HC queries in the first
+        // HC/2 (16-query K-steps of 8 columns) and dS^T in the next HC/2
+        const uint32_t xb = tmem + T_X + b * 128 + (chain_p ? 0 : HC / 2);
         const uint64_t db = sw128_desc(chain_p ? sb + L::O_OFF + so * L::O_BYTES : sb + L::Q_OFF + sq * L::Q_BYTES,
                                        16384, 1024);
 #pragma unroll
         for (int kk = 0; kk < KSTEP / 16; ++kk)
           if (kk < ksteps)
-            mma_bf16_tmem_a(tmem + (chain_p ? T_DV : T_DK), xb + (kk >> 2) * 64 + (kk & 3) * 8,
+            mma_bf16_tmem_a(tmem + (chain_p ? T_DV : T_DK), xb + (kk / (HC / 16)) * HC + (kk % (HC / 16)) * 8,
                             db + ((kk * 2048) >> 4), chain_p ? idesc_dv : idesc_dk,
                             (cg.j > 0 || kk > 0) ? 1u : 0u);
         if (chain_p) {
@@ -431,11 +471,12 @@ tc_dkdv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
     __syncwarp();
   } else {
     // ------------------------------------------------------------ compute warpgroups
-    // Warps 2..5 and 6..9 each cover all 128 keys (TMEM lanes); the first group
-    // handles query columns [0,64) of every step and the first half of the dK/dV
-    // columns in the epilogue, the second group the other halves.  Each group
-    // reads and writes only inside its own columns.
-    const int half = (warp - 2) >> 2;
+    // Each group of four consecutive warps covers all 128 keys (TMEM lanes) and
+    // handles query columns [HC grp, HC grp + HC) of every step.  In the epilogue
+    // two groups store the two halves of dK and of dV each; four groups store one
+    // half of dK (groups 0, 1) or of dV (groups 2, 3) each.  Each group reads and
+    // writes only inside its own columns.
+    const int grp = (warp - 2) >> 2;
     const int r = 32 * (warp & 3) + lane;  // key of the tile = TMEM lane
     const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
     const float c_score = ACT == kActSoftmax ? p.scale * kLog2e : p.scale;
@@ -443,7 +484,6 @@ tc_dkdv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
     const float2 cc = make_float2(c_score, c_score);
     const float2 hc = make_float2(0.5f * c_score, 0.5f * c_score);
     const float2 one = make_float2(1.f, 1.f);
-    constexpr int HC = KSTEP / 2;  // query columns per group
     uint32_t q_it = 0, s_it = 0, a_it = 0;
     bool ok = true;
     // The epilogue of an item (dK, dV from TMEM to HBM) runs after the next item's
@@ -455,22 +495,45 @@ tc_dkdv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
       if (!mbar_wait(bar(KV_ACCFULL), a_it & 1, abort, status)) return false;
       ++a_it;
       tc_fence_after();
-      float x[DQK / 2];
+      if constexpr (Gr::G == 4) {
+        // one half of dK or of dV, through an array of exactly its columns
+        auto drain = [&](auto cols, uint32_t t_acc, __nv_bfloat16* dst, float f) {
+          constexpr int NC = decltype(cols)::value;
+          float x[NC];
 #pragma unroll
-      for (int c = 0; c < DQK / 64; ++c) tmem_ld32(tmem + lane_base + T_DK + half * (DQK / 2) + 32 * c, x + 32 * c);
-      float y[DV / 2];
+          for (int c = 0; c < NC / 32; ++c) tmem_ld32(t_acc + 32 * c, x + 32 * c);
+          tmem_wait_ld();
+          tc_fence_before();
+          mbar_arrive(bar(KV_ACCEMPTY));
+          if (pend_key_ok) {
 #pragma unroll
-      for (int c = 0; c < DV / 64; ++c) tmem_ld32(tmem + lane_base + T_DV + half * (DV / 2) + 32 * c, y + 32 * c);
-      tmem_wait_ld();
-      tc_fence_before();
-      mbar_arrive(bar(KV_ACCEMPTY));
-      if (pend_key_ok) {
+            for (int c = 0; c < NC / 32; ++c) store_row_bf16(dst + 32 * c, x + 32 * c, f);
+          }
+        };
+        if (grp >= 2)
+          drain(std::integral_constant<int, DV / 2>{}, tmem + lane_base + T_DV + (grp & 1) * (DV / 2),
+                dv + pend_krow * DV + (grp & 1) * (DV / 2), 1.f);
+        else
+          drain(std::integral_constant<int, DQK / 2>{}, tmem + lane_base + T_DK + (grp & 1) * (DQK / 2),
+                dk + pend_krow * DQK + (grp & 1) * (DQK / 2), p.scale);
+      } else {
+        // half grp of dK and half grp of dV
+        float x[DQK / 2], y[DV / 2];
 #pragma unroll
-        for (int c = 0; c < DQK / 64; ++c)
-          store_row_bf16(dk + pend_krow * DQK + half * (DQK / 2) + 32 * c, x + 32 * c, p.scale);
+        for (int c = 0; c < DQK / 64; ++c) tmem_ld32(tmem + lane_base + T_DK + grp * (DQK / 2) + 32 * c, x + 32 * c);
 #pragma unroll
-        for (int c = 0; c < DV / 64; ++c)
-          store_row_bf16(dv + pend_krow * DV + half * (DV / 2) + 32 * c, y + 32 * c, 1.f);
+        for (int c = 0; c < DV / 64; ++c) tmem_ld32(tmem + lane_base + T_DV + grp * (DV / 2) + 32 * c, y + 32 * c);
+        tmem_wait_ld();
+        tc_fence_before();
+        mbar_arrive(bar(KV_ACCEMPTY));
+        if (pend_key_ok) {
+#pragma unroll
+          for (int c = 0; c < DQK / 64; ++c)
+            store_row_bf16(dk + pend_krow * DQK + grp * (DQK / 2) + 32 * c, x + 32 * c, p.scale);
+#pragma unroll
+          for (int c = 0; c < DV / 64; ++c)
+            store_row_bf16(dv + pend_krow * DV + grp * (DV / 2) + 32 * c, y + 32 * c, 1.f);
+        }
       }
       pend = false;
       return true;
@@ -490,8 +553,8 @@ tc_dkdv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
       const int qs0 = CAUSAL ? key0 / KSTEP : 0;
       for (int step = 0; step < n; ++step, ++q_it, ++s_it) {
         const uint32_t b = s_it & 1;
-        const uint32_t x_tm = tmem + lane_base + T_X + b * 128 + half * HC;  // this group's columns
-        const int i0 = (qs0 + step) * KSTEP + half * HC;
+        const uint32_t x_tm = tmem + lane_base + T_X + b * 128 + grp * HC;  // this group's columns
+        const int i0 = (qs0 + step) * KSTEP + grp * HC;
         if (!mbar_wait(bar(KV_SFULL + b), (s_it >> 1) & 1, abort, status)) { ok = false; break; }
         tc_fence_after();
         if (Lq - i0 <= 0) {
@@ -504,14 +567,14 @@ tc_dkdv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
           continue;
         }
         float sv[HC];
-        tmem_ld32(x_tm, sv);
-        tmem_ld32(x_tm + 32, sv + 32);
+#pragma unroll
+        for (int c = 0; c < HC / 32; ++c) tmem_ld32(x_tm + 32 * c, sv + 32 * c);
         tmem_wait_ld();
         tc_fence_before();
         mbar_arrive(bar(KV_SEMPTY + b));  // dP^T(s_it) may overwrite the buffer
         const uint32_t st = q_it % NO;
         if (!mbar_wait(bar(KV_RSFULL + st), (q_it / NO) & 1, abort, status)) { ok = false; break; }
-        const float* rs = reinterpret_cast<const float*>(smem_raw + L::RS_OFF + st * L::RS_BYTES) + half * HC;
+        const float* rs = reinterpret_cast<const float*>(smem_raw + L::RS_OFF + st * L::RS_BYTES) + grp * HC;
         // valid queries of this group's columns for key j: i < Lq and (causal) i >= j
         const int lo = CAUSAL ? j - i0 : 0;
         const int hi = j < Lk ? Lq - i0 : 0;
@@ -542,8 +605,8 @@ tc_dkdv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
         if (!mbar_wait(bar(KV_DPFULL + b), (s_it >> 1) & 1, abort, status)) { ok = false; break; }
         tc_fence_after();
         float dp[HC];
-        tmem_ld32(x_tm, dp);
-        tmem_ld32(x_tm + 32, dp + 32);
+#pragma unroll
+        for (int c = 0; c < HC / 32; ++c) tmem_ld32(x_tm + 32 * c, dp + 32 * c);
         tmem_wait_ld();
         uint32_t dk2[HC / 2];
 #pragma unroll
@@ -557,8 +620,13 @@ tc_dkdv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
           dk2[c / 2] = pack_bf16(ds.x, ds.y);
         }
         // P^T then dS^T over this group's own, already loaded columns
-        tmem_st32(x_tm, reinterpret_cast<const float*>(pk));
-        tmem_st32(x_tm + 32, reinterpret_cast<const float*>(dk2));
+        if constexpr (HC == 64) {
+          tmem_st32(x_tm, reinterpret_cast<const float*>(pk));
+          tmem_st32(x_tm + 32, reinterpret_cast<const float*>(dk2));
+        } else {
+          tmem_st16(x_tm, pk);
+          tmem_st16(x_tm + 16, dk2);
+        }
         tmem_wait_st();
         tc_fence_before();
         mbar_arrive(bar(KV_PDSFULL + b));
@@ -575,10 +643,16 @@ tc_dkdv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
         pend_krow = krow;
       } else if (key_ok) {
         const float z[32] = {0.f};
+        const bool do_k = Gr::G == 2 || grp < 2, do_v = Gr::G == 2 || grp >= 2;
+        const int hk = Gr::G == 2 ? grp : (grp & 1);  // which half
+        if (do_k) {
 #pragma unroll
-        for (int c = 0; c < DQK / 64; ++c) store_row_bf16(dk + krow * DQK + half * (DQK / 2) + 32 * c, z, 1.f);
+          for (int c = 0; c < DQK / 64; ++c) store_row_bf16(dk + krow * DQK + hk * (DQK / 2) + 32 * c, z, 1.f);
+        }
+        if (do_v) {
 #pragma unroll
-        for (int c = 0; c < DV / 64; ++c) store_row_bf16(dv + krow * DV + half * (DV / 2) + 32 * c, z, 1.f);
+          for (int c = 0; c < DV / 64; ++c) store_row_bf16(dv + krow * DV + hk * (DV / 2) + 32 * c, z, 1.f);
+        }
       }
     }
     if (ok && pend) ok = epilogue();
@@ -598,7 +672,9 @@ tc_dkdv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
 // One item = (sequence, head, 128-row query tile); the inner loop steps over
 // 128 keys.  S is double-buffered in TMEM so that S of the next step is
 // computed while the compute warpgroups form dS of this one; dS goes back into
-// TMEM as packed bf16 over the dP columns and dQ += dS K reads it from there.
+// TMEM as packed bf16 over the S columns it was formed from (each warpgroup its
+// own, already loaded), so dP of the next step may start as soon as dP of this
+// one is loaded, and dQ += dS K reads dS from there.
 template <int DQK, int DV>
 struct QLayout {
   // K(j+2) is wanted right after dQ(j) and V(j+1) right after dP(j) is loaded, so
@@ -629,13 +705,17 @@ enum : uint32_t {
 };
 
 template <int DQK, int DV, int ACT, bool CAUSAL>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(QGroups::kThreads, 1)
 tc_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
              const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
              const Problem p, const float2* __restrict__ rowstat, __nv_bfloat16* __restrict__ dq,
              WsHeader* hdr, const WorkItem* __restrict__ list) {
   using L = QLayout<DQK, DV>;
+  using Gr = QGroups;
   constexpr int NK = L::NK, NV = L::NV, NQO = L::NQO;
+  constexpr int HC = Gr::HC;  // key columns per compute warpgroup
+  static_assert(HC * Gr::G == STEP && HC % 32 == 0, "the compute warpgroups split a step's keys");
+  constexpr uint32_t kCompute = 32 * 4 * Gr::G;  // compute threads
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t sb = (raw + 512u + 1023u) & ~1023u;  // 128-byte swizzled tiles: 1 KB aligned
@@ -670,10 +750,10 @@ tc_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
     mbar_init(bar(Q_SFULL), 1);
     mbar_init(bar(Q_SFULL + 1), 1);
     mbar_init(bar(Q_DPFULL), 1);
-    mbar_init(bar(Q_DPEMPTY), 256);
-    mbar_init(bar(Q_DSFULL), 256);
+    mbar_init(bar(Q_DPEMPTY), kCompute);
+    mbar_init(bar(Q_DSFULL), kCompute);
     mbar_init(bar(Q_ACCFULL), 1);
-    mbar_init(bar(Q_ACCEMPTY), 256);
+    mbar_init(bar(Q_ACCEMPTY), kCompute);
     *abort = 0;
     fence_mbar_init();
   }
@@ -686,13 +766,23 @@ tc_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
   constexpr uint32_t T_DQ = 0, T_DP = 256;
   auto t_s = [](uint32_t b) { return b ? 384u : 128u; };
 
-  if (warp == 0) {
+  if (warp == 0 || warp == Gr::kProducer2) {
+    // ------------------------------------------------------------ producers
+    // warp 0: the item's Q tile, then K(0), K(1), ...; the second producer: its dO
+    // tile, then V(0), V(1), ...  Each ring is filled in consumption order.
     if (lane == 0) {
-      tma_prefetch_desc(&tm_q);
-      tma_prefetch_desc(&tm_do);
-      tma_prefetch_desc(&tm_k);
-      tma_prefetch_desc(&tm_v);
-      uint32_t q_it = 0, k_it = 0, v_it = 0;
+      const bool qk = warp == 0;
+      const CUtensorMap* tm_row = qk ? &tm_q : &tm_do;
+      const CUtensorMap* tm_key = qk ? &tm_k : &tm_v;
+      tma_prefetch_desc(tm_row);
+      tma_prefetch_desc(tm_key);
+      const int D = qk ? DQK : DV;
+      const uint32_t row_off = qk ? L::Q_OFF : L::O_OFF, row_bytes = qk ? L::Q_BYTES : L::O_BYTES;
+      const uint32_t key_off = qk ? L::K_OFF : L::V_OFF, key_bytes = qk ? L::K_BYTES : L::V_BYTES;
+      const uint32_t nring = qk ? NK : NV;
+      const uint32_t b_rfull = qk ? Q_QFULL : Q_OFULL, b_rempty = qk ? Q_QEMPTY : Q_OEMPTY;
+      const uint32_t b_kfull = qk ? Q_KFULL : Q_VFULL, b_kempty = qk ? Q_KEMPTY : Q_VEMPTY;
+      uint32_t q_it = 0, t_it = 0;
       bool ok = true;
       WorkItem nxt = blockIdx.x < (unsigned)n_items ? load_item(list, blockIdx.x) : WorkItem{};
       for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
@@ -702,48 +792,23 @@ tc_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
         if (n == 0) continue;
         const int h = w.h, row0 = w.tile * TILE;
         const int32_t q0 = w.q0, k0 = w.k0;
-        auto load_k = [&](int j) {
-          const uint32_t st = k_it % NK;
-          if (!mbar_wait(bar(Q_KEMPTY + st), ((k_it / NK) & 1) ^ 1, abort, status)) return false;
-          mbar_expect_tx(bar(Q_KFULL + st), L::K_BYTES);
-#pragma unroll
-          for (int a = 0; a < DQK / 64; ++a)
-            tma_load_2d(sb + L::K_OFF + st * L::K_BYTES + a * 16384, &tm_k, h * DQK + a * 64,
-                        k0 + j * STEP, bar(Q_KFULL + st));
-          ++k_it;
-          return true;
-        };
-        auto load_v = [&](int j) {
-          const uint32_t st = v_it % NV;
-          if (!mbar_wait(bar(Q_VEMPTY + st), ((v_it / NV) & 1) ^ 1, abort, status)) return false;
-          mbar_expect_tx(bar(Q_VFULL + st), L::V_BYTES);
-#pragma unroll
-          for (int a = 0; a < DV / 64; ++a)
-            tma_load_2d(sb + L::V_OFF + st * L::V_BYTES + a * 16384, &tm_v, h * DV + a * 64,
-                        k0 + j * STEP, bar(Q_VFULL + st));
-          ++v_it;
-          return true;
-        };
         const uint32_t qs = q_it % NQO, qph = ((q_it / NQO) & 1) ^ 1;
-        if (!mbar_wait(bar(Q_QEMPTY + qs), qph, abort, status)) break;
-        mbar_expect_tx(bar(Q_QFULL + qs), L::Q_BYTES);
-#pragma unroll
-        for (int a = 0; a < DQK / 64; ++a)
-          tma_load_2d(sb + L::Q_OFF + qs * L::Q_BYTES + a * 16384, &tm_q, h * DQK + a * 64, q0 + row0,
-                      bar(Q_QFULL + qs));
-        if (!mbar_wait(bar(Q_OEMPTY + qs), qph, abort, status)) break;
-        mbar_expect_tx(bar(Q_OFULL + qs), L::O_BYTES);
-#pragma unroll
-        for (int a = 0; a < DV / 64; ++a)
-          tma_load_2d(sb + L::O_OFF + qs * L::O_BYTES + a * 16384, &tm_do, h * DV + a * 64, q0 + row0,
-                      bar(Q_OFULL + qs));
+        if (!mbar_wait(bar(b_rempty + qs), qph, abort, status)) break;
+        mbar_expect_tx(bar(b_rfull + qs), row_bytes);
+        for (int a = 0; a < D / 64; ++a)
+          tma_load_2d(sb + row_off + qs * row_bytes + a * 16384, tm_row, h * D + a * 64, q0 + row0,
+                      bar(b_rfull + qs));
         ++q_it;
-        // consumption order: S(0), S(1), then dP(j) and S(j+2)
-        ok = load_k(0);
-        if (ok && n > 1) ok = load_k(1);
-        for (int j = 0; j < n && ok; ++j) {
-          ok = load_v(j);
-          if (ok && j + 2 < n) ok = load_k(j + 2);
+        for (int j = 0; j < n; ++j, ++t_it) {
+          const uint32_t st = t_it % nring;
+          if (!mbar_wait(bar(b_kempty + st), ((t_it / nring) & 1) ^ 1, abort, status)) {
+            ok = false;
+            break;
+          }
+          mbar_expect_tx(bar(b_kfull + st), key_bytes);
+          for (int a = 0; a < D / 64; ++a)
+            tma_load_2d(sb + key_off + st * key_bytes + a * 16384, tm_key, h * D + a * 64, k0 + j * STEP,
+                        bar(b_kfull + st));
         }
       }
     }
@@ -798,7 +863,7 @@ tc_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
           const uint32_t ds_tm = tmem + t_s((s_base + j) & 1);
 #pragma unroll
           for (int kk = 0; kk < STEP / 16; ++kk)
-            mma_bf16_tmem_a(tmem + T_DQ, ds_tm + (kk >> 2) * 64 + (kk & 3) * 8,
+            mma_bf16_tmem_a(tmem + T_DQ, ds_tm + (kk / (HC / 16)) * HC + (kk % (HC / 16)) * 8,
                             sw128_desc(k_tile + kk * 2048, 16384, 1024), idesc_dq,
                             (j > 0 || kk > 0) ? 1u : 0u);
           mma_commit(bar(Q_KEMPTY + kst));
@@ -814,7 +879,7 @@ tc_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
       }
     }
     __syncwarp();
-  } else if (warp == kIssuerB) {
+  } else if (warp == Gr::kIssuerB) {
     // ------------------------------------------------------------ issuer B: dP = dO V^T
     if (lane == 0) {
       constexpr uint32_t idesc_s = idesc_bf16(TILE, STEP, 0, 0);
@@ -855,10 +920,10 @@ tc_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
     }
     __syncwarp();
   } else {
-    // Two compute warpgroups: warps 2..5 take key columns [0,64) of every step
-    // and the first half of the dQ columns, warps 6..9 the other halves; each
-    // group writes only inside its own columns.
-    const int half = (warp - 2) >> 2;
+    // Compute warpgroups: group grp (four consecutive warps, all 128 rows) takes key
+    // columns [HC grp, HC grp + HC) of every step and dQ columns [CQ grp, CQ grp + CQ)
+    // in the epilogue; each group writes only inside its own columns.
+    const int grp = (warp - 2) >> 2;
     const int r = 32 * (warp & 3) + lane;  // query row of the tile = TMEM lane
     const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
     const float c_score = ACT == kActSoftmax ? p.scale * kLog2e : p.scale;
@@ -866,8 +931,11 @@ tc_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
     const float2 cc = make_float2(c_score, c_score);
     const float2 hc = make_float2(0.5f * c_score, 0.5f * c_score);
     const float2 one = make_float2(1.f, 1.f);
-    constexpr int HC = STEP / 2;  // key columns per group
-    const uint32_t p_tm = tmem + lane_base + T_DP + half * HC;
+    const uint32_t p_tm = tmem + lane_base + T_DP + grp * HC;
+    // dQ columns drained per group, in whole 32-column loads: with four groups and
+    // Dqk = 64 the last two groups drain nothing
+    constexpr int CQ = DQK / Gr::G >= 32 ? DQK / Gr::G : 32;
+    const bool drains = CQ * Gr::G == DQK || grp * CQ < DQK;
     uint32_t s_it = 0, d_it = 0, a_it = 0;
     bool ok = true;
     // The epilogue of an item (dQ from TMEM to HBM) runs after the next item's first
@@ -879,16 +947,20 @@ tc_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
       if (!mbar_wait(bar(Q_ACCFULL), a_it & 1, abort, status)) return false;
       ++a_it;
       tc_fence_after();
-      float x[DQK / 2];
+      if (drains) {
+        float x[CQ];
 #pragma unroll
-      for (int c = 0; c < DQK / 64; ++c) tmem_ld32(tmem + lane_base + T_DQ + half * (DQK / 2) + 32 * c, x + 32 * c);
-      tmem_wait_ld();
-      tc_fence_before();
-      mbar_arrive(bar(Q_ACCEMPTY));
-      if (pend_row_ok) {
+        for (int c = 0; c < CQ / 32; ++c) tmem_ld32(tmem + lane_base + T_DQ + grp * CQ + 32 * c, x + 32 * c);
+        tmem_wait_ld();
+        tc_fence_before();
+        mbar_arrive(bar(Q_ACCEMPTY));
+        if (pend_row_ok) {
 #pragma unroll
-        for (int c = 0; c < DQK / 64; ++c)
-          store_row_bf16(dq + pend_orow * DQK + half * (DQK / 2) + 32 * c, x + 32 * c, p.scale);
+          for (int c = 0; c < CQ / 32; ++c) store_row_bf16(dq + pend_orow * DQK + grp * CQ + 32 * c, x + 32 * c, p.scale);
+        }
+      } else {
+        tc_fence_before();
+        mbar_arrive(bar(Q_ACCEMPTY));
       }
       pend = false;
       return true;
@@ -912,12 +984,12 @@ tc_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
         const uint32_t sbuf = s_it & 1;
         if (!mbar_wait(bar(Q_SFULL + sbuf), (s_it >> 1) & 1, abort, status)) { ok = false; break; }
         tc_fence_after();
-        const uint32_t s_tm = tmem + lane_base + t_s(sbuf) + half * HC;
+        const uint32_t s_tm = tmem + lane_base + t_s(sbuf) + grp * HC;
         float sv[HC];
-        tmem_ld32(s_tm, sv);
-        tmem_ld32(s_tm + 32, sv + 32);
+#pragma unroll
+        for (int c = 0; c < HC / 32; ++c) tmem_ld32(s_tm + 32 * c, sv + 32 * c);
         tmem_wait_ld();
-        const int kb = step * STEP + half * HC;
+        const int kb = step * STEP + grp * HC;
         int nvalid = Lk - kb;
         if (CAUSAL) nvalid = min(nvalid, i - kb + 1);
         if (!row_ok) nvalid = 0;
@@ -944,8 +1016,8 @@ tc_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
         if (!mbar_wait(bar(Q_DPFULL), d_it & 1, abort, status)) { ok = false; break; }
         tc_fence_after();
         float dp[HC];
-        tmem_ld32(p_tm, dp);
-        tmem_ld32(p_tm + 32, dp + 32);
+#pragma unroll
+        for (int c = 0; c < HC / 32; ++c) tmem_ld32(p_tm + 32 * c, dp + 32 * c);
         tmem_wait_ld();
         tc_fence_before();
         mbar_arrive(bar(Q_DPEMPTY));  // dP(step + 1) may overwrite the dP columns
@@ -958,7 +1030,10 @@ tc_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
           dk2[c / 2] = pack_bf16(ds.x, ds.y);
         }
         // dS over this group's own S columns (already loaded above)
-        tmem_st32(s_tm, reinterpret_cast<const float*>(dk2));
+        if constexpr (HC == 64)
+          tmem_st32(s_tm, reinterpret_cast<const float*>(dk2));
+        else
+          tmem_st16(s_tm, dk2);
         tmem_wait_st();
         tc_fence_before();
         mbar_arrive(bar(Q_DSFULL));
@@ -973,8 +1048,10 @@ tc_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
         pend_orow = orow;
       } else if (row_ok) {
         const float z[32] = {0.f};
+        if (drains) {
 #pragma unroll
-        for (int c = 0; c < DQK / 64; ++c) store_row_bf16(dq + orow * DQK + half * (DQK / 2) + 32 * c, z, 1.f);
+          for (int c = 0; c < CQ / 32; ++c) store_row_bf16(dq + orow * DQK + grp * CQ + 32 * c, z, 1.f);
+        }
       }
     }
     if (ok && pend) ok = epilogue();
@@ -1012,7 +1089,7 @@ cudaError_t dkdv_t(const Maps& m, const Problem& p, const float2* rowstat, void*
   constexpr uint32_t smem = KvLayout<DQK, DV>::SMEM;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  kern<<<num_sms(), kThreads, smem, s>>>(m.k, m.v, m.q, m.dout, p, rowstat,
+  kern<<<num_sms(), KvGroups<ACT>::kThreads, smem, s>>>(m.k, m.v, m.q, m.dout, p, rowstat,
                                          (__nv_bfloat16*)dk, (__nv_bfloat16*)dv, ws.hdr, ws.list_k);
   return cudaGetLastError();
 }
@@ -1024,7 +1101,7 @@ cudaError_t dq_t(const Maps& m, const Problem& p, const float2* rowstat, void* d
   constexpr uint32_t smem = QLayout<DQK, DV>::SMEM;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  kern<<<num_sms(), kThreads, smem, s>>>(m.q, m.dout, m.k, m.v, p, rowstat,
+  kern<<<num_sms(), QGroups::kThreads, smem, s>>>(m.q, m.dout, m.k, m.v, p, rowstat,
                                          (__nv_bfloat16*)dq, ws.hdr, ws.list_q);
   return cudaGetLastError();
 }

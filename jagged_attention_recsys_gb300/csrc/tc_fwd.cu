@@ -17,12 +17,12 @@
 //               of 128 keys in separate rings, straight from the jagged
 //               [T, H*D] buffers (rows past a sequence belong to its neighbour
 //               and are masked; rows past the buffer are zero-filled by TMA)
-//   warp 9      TMEM owner and MMA issuer (one lane)
+//   warp 9      TMEM owner and S = Q K^T issuer (one lane)
+//   warp 10     O += P V issuer (one lane)
 // TMEM: S double-buffered at columns [0,128) and [128,256), O at [256, 256+Dv),
-// P (packed bf16, 128 keys) at [384, 448).  MMA issue order per step j: PV(j)
-// as soon as P(j) is in TMEM, then S(j+2) into the buffer that held S(j).  An
-// MMA issue blocks while the tensor pipe is busy, so PV(j) goes first: it
-// releases P to the softmax warps, while S(j+2) is needed only a step later.
+// P (packed bf16, 128 keys) double-buffered at [384, 448) and [448, 512).  S of
+// step j+2 goes into the buffer of S(j) once P(j) has been written; PV(j) reads
+// P buffer j & 1, which P(j+2) reuses once PV(j) has completed.
 // Per step the softmax warpgroups scale to log2 units,
 // subtract a finite shift from masked columns, keep an online max with lazy
 // rescaling of O (only when it grows by more than 2^8), take exp2 and the row

@@ -54,7 +54,7 @@ def test_bf16_self_softmax(dims, causal):
     full_check(W(*dims, causal=causal), TILE_EDGES, seed=1)
 
 
-@pytest.mark.parametrize("dims", [(64, 64), (128, 128)])
+@pytest.mark.parametrize("dims", [(64, 64), (128, 128), (128, 64), (64, 128)])
 @pytest.mark.parametrize("causal", [False, True])
 def test_bf16_gdpa(dims, causal):
     full_check(W(*dims, causal=causal, act=GD), TILE_EDGES, seed=2)
