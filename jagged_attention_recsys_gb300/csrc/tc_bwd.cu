@@ -679,7 +679,12 @@ template <int DQK, int DV>
 struct QLayout {
   // K(j+2) is wanted right after dQ(j) and V(j+1) right after dP(j) is loaded, so
   // the K ring is one stage deeper than the V ring: a TMA load takes about a step.
-  static constexpr int NQO = DQK + DV == 256 ? 1 : 2;  // Q / dO tiles
+  // Q and dO tiles are double-buffered across items except at Dqk = Dv = 128, where
+  // the K ring keeps its third stage instead (a two-deep K ring there was measured
+  // 15-30% slower than single Q and dO tiles).
+  static constexpr bool kWide = DQK + DV == 256;
+  static constexpr int NQ = kWide ? 1 : 2;  // Q tiles
+  static constexpr int NO = kWide ? 1 : 2;  // dO tiles
   static constexpr int NK = DQK == 128 ? 3 : (DV == 128 ? 4 : 6);
   static constexpr int NV = DQK == 64 && DV == 64 ? 4 : 2;
   static constexpr uint32_t Q_BYTES = DQK / 64 * 16384;   // 128 rows
@@ -688,8 +693,8 @@ struct QLayout {
   static constexpr uint32_t V_BYTES = DV / 64 * 16384;
   static constexpr uint32_t TILE0 = 1024;  // mbarriers, TMEM slot, abort flag in front
   static constexpr uint32_t Q_OFF = 0;     // offsets from the 1 KB-aligned tile base
-  static constexpr uint32_t O_OFF = Q_OFF + NQO * Q_BYTES;
-  static constexpr uint32_t K_OFF = O_OFF + NQO * O_BYTES;
+  static constexpr uint32_t O_OFF = Q_OFF + NQ * Q_BYTES;
+  static constexpr uint32_t K_OFF = O_OFF + NO * O_BYTES;
   static constexpr uint32_t V_OFF = K_OFF + NK * K_BYTES;
   static constexpr uint32_t TILES = V_OFF + NV * V_BYTES;
   static constexpr uint32_t SMEM = TILE0 + TILES;
@@ -712,7 +717,7 @@ tc_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
              WsHeader* hdr, const WorkItem* __restrict__ list) {
   using L = QLayout<DQK, DV>;
   using Gr = QGroups;
-  constexpr int NK = L::NK, NV = L::NV, NQO = L::NQO;
+  constexpr int NK = L::NK, NV = L::NV, NQ = L::NQ, NO = L::NO;
   constexpr int HC = Gr::HC;  // key columns per compute warpgroup
   static_assert(HC * Gr::G == STEP && HC % 32 == 0, "the compute warpgroups split a step's keys");
   constexpr uint32_t kCompute = 32 * 4 * Gr::G;  // compute threads
@@ -733,9 +738,11 @@ tc_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
   const int n_items = hdr->n_q;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < NQO; ++s) {
+    for (int s = 0; s < NQ; ++s) {
       mbar_init(bar(Q_QFULL + s), 1);
       mbar_init(bar(Q_QEMPTY + s), 1);
+    }
+    for (int s = 0; s < NO; ++s) {
       mbar_init(bar(Q_OFULL + s), 1);
       mbar_init(bar(Q_OEMPTY + s), 1);
     }
@@ -792,7 +799,8 @@ tc_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
         if (n == 0) continue;
         const int h = w.h, row0 = w.tile * TILE;
         const int32_t q0 = w.q0, k0 = w.k0;
-        const uint32_t qs = q_it % NQO, qph = ((q_it / NQO) & 1) ^ 1;
+        const uint32_t nrow = qk ? NQ : NO;
+        const uint32_t qs = q_it % nrow, qph = ((q_it / nrow) & 1) ^ 1;
         if (!mbar_wait(bar(b_rempty + qs), qph, abort, status)) break;
         mbar_expect_tx(bar(b_rfull + qs), row_bytes);
         for (int a = 0; a < D / 64; ++a)
@@ -829,8 +837,8 @@ tc_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
         if (it + (int)gridDim.x < n_items) nxt = load_item(list, it + gridDim.x);
         const int n = w.cost;
         if (n == 0) continue;
-        const uint32_t qs = q_it % NQO;
-        if (!mbar_wait(bar(Q_QFULL + qs), (q_it / NQO) & 1, abort, status)) break;
+        const uint32_t qs = q_it % NQ;
+        if (!mbar_wait(bar(Q_QFULL + qs), (q_it / NQ) & 1, abort, status)) break;
         const uint32_t q_tile = sb + L::Q_OFF + qs * L::Q_BYTES;
         const uint32_t k_base = k_it, s_base = s_it;
         auto issue_s = [&](int i) {  // S(i) = Q K(i)^T into buffer (s_base + i) & 1
@@ -891,8 +899,8 @@ tc_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
         if (it + (int)gridDim.x < n_items) nxt = load_item(list, it + gridDim.x);
         const int n = w.cost;
         if (n == 0) continue;
-        const uint32_t qs = q_it % NQO;
-        if (!mbar_wait(bar(Q_OFULL + qs), (q_it / NQO) & 1, abort, status)) break;
+        const uint32_t qs = q_it % NO;
+        if (!mbar_wait(bar(Q_OFULL + qs), (q_it / NO) & 1, abort, status)) break;
         const uint32_t o_tile = sb + L::O_OFF + qs * L::O_BYTES;
         for (int j = 0; j < n; ++j, ++v_it, ++dp_it) {
           const uint32_t vst = v_it % NV;

@@ -12,11 +12,11 @@
 //   warps 4..7  softmax warpgroup 1: key columns [64,128)
 //               (one query row per thread = TMEM lane; the two threads of a
 //               row exchange their partial row maximum through shared memory)
-//   warp 8      TMA producer: Q (double-buffered across items unless
-//               Dqk = Dv = 128) and K / V tiles
-//               of 128 keys in separate rings, straight from the jagged
-//               [T, H*D] buffers (rows past a sequence belong to its neighbour
-//               and are masked; rows past the buffer are zero-filled by TMA)
+//   warp 8      TMA producer of Q (double-buffered across items) and of the K
+//               ring; warp 11 that of the V ring.  128-key tiles come straight
+//               from the jagged [T, H*D] buffers (rows past a sequence belong
+//               to its neighbour and are masked; rows past the buffer are
+//               zero-filled by TMA)
 //   warp 9      TMEM owner and S = Q K^T issuer (one lane)
 //   warp 10     O += P V issuer (one lane)
 // TMEM: S double-buffered at columns [0,128) and [128,256), O at [256, 256+Dv),
@@ -44,8 +44,8 @@ using namespace tc;
 constexpr int BM = 128;     // rows per item (MMA M)
 constexpr int BN = 128;     // keys per step (MMA N of S)
 constexpr int HC = BN / 2;  // key columns per softmax warpgroup
-constexpr int kThreads = 352;
-constexpr int kProducerWarp = 8, kSWarp = 9, kPvWarp = 10;
+constexpr int kThreads = 384;
+constexpr int kProducerWarp = 8, kSWarp = 9, kPvWarp = 10, kVWarp = 11;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleLog2 = 8.0f;
@@ -62,10 +62,12 @@ struct FwdLayout {
   static constexpr uint32_t SMALL = RED_OFF + RED_BYTES;
   static constexpr uint32_t TILE0 = (SMALL + 1023) / 1024 * 1024;  // for a 1 KB-aligned base
   static constexpr uint32_t kMaxSmem = 232448;
-  // Q is single-buffered at Dqk = Dv = 128; the K and V rings take the rest.
-  static constexpr int NQB = (DQK == 128 && DV == 128) ? 1 : 2;
+  // Q is double-buffered, so the next item's Q tile loads during this item; the K
+  // and V rings take the rest (at Dqk = Dv = 128 the V ring is the shorter one: V(j)
+  // is wanted a step after K(j)).
+  static constexpr int NQB = 2;
   static constexpr int NK = DQK == 64 ? (DV == 64 ? 6 : 4) : 3;
-  static constexpr int NV = DV == 64 ? (DQK == 64 ? 6 : 4) : (DQK == 64 ? 4 : 3);
+  static constexpr int NV = DV == 64 ? (DQK == 64 ? 6 : 4) : (DQK == 64 ? 4 : 2);
   static constexpr uint32_t Q_OFF = 0;  // offsets from the 1 KB-aligned tile base
   static constexpr uint32_t K_OFF = Q_OFF + NQB * Q_BYTES;
   static constexpr uint32_t V_OFF = K_OFF + NK * K_BYTES;
@@ -136,56 +138,54 @@ tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == kProducerWarp) {
-    // ------------------------------------------------------------ TMA producer
+  if (warp == kProducerWarp || warp == kVWarp) {
+    // ------------------------------------------------------------ TMA producers
+    // warp 8: each item's Q tile, then K(0), K(1), ...; warp 11: V(0), V(1), ...
+    // Two threads, so that neither ring waits behind a load of the other.
     if (lane == 0) {
-      tma_prefetch_desc(&tm_q);
-      tma_prefetch_desc(&tm_k);
-      tma_prefetch_desc(&tm_v);
-      uint32_t k_it = 0, v_it = 0, q_it = 0;
+      const bool qk = warp == kProducerWarp;
+      if (qk) {
+        tma_prefetch_desc(&tm_q);
+        tma_prefetch_desc(&tm_k);
+      } else {
+        tma_prefetch_desc(&tm_v);
+      }
+      uint32_t t_it = 0, q_it = 0;
       bool ok = true;
-      auto load_k = [&](const WorkItem& w, int j) {
-        const uint32_t st = k_it % NK;
-        if (!mbar_wait(bar(B_KEMPTY + st), ((k_it / NK) & 1) ^ 1, abort, status)) return false;
-        mbar_expect_tx(bar(B_KFULL + st), L::K_BYTES);
-#pragma unroll
-        for (int a = 0; a < DQK / 64; ++a)
-          tma_load_2d(sb + L::K_OFF + st * L::K_BYTES + a * 16384, &tm_k, w.h * DQK + a * 64,
-                      w.k0 + j * BN, bar(B_KFULL + st));
-        ++k_it;
-        return true;
-      };
-      auto load_v = [&](const WorkItem& w, int j) {
-        const uint32_t st = v_it % NV;
-        if (!mbar_wait(bar(B_VEMPTY + st), ((v_it / NV) & 1) ^ 1, abort, status)) return false;
-        mbar_expect_tx(bar(B_VFULL + st), L::V_BYTES);
-#pragma unroll
-        for (int a = 0; a < DV / 64; ++a)
-          tma_load_2d(sb + L::V_OFF + st * L::V_BYTES + a * 16384, &tm_v, w.h * DV + a * 64,
-                      w.k0 + j * BN, bar(B_VFULL + st));
-        ++v_it;
-        return true;
-      };
       WorkItem nxt = blockIdx.x < (unsigned)n_items ? load_item(list, blockIdx.x) : WorkItem{};
       for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
         const WorkItem w = nxt;  // prefetched one item ahead
         if (it + (int)gridDim.x < n_items) nxt = load_item(list, it + gridDim.x);
         const int n = w.cost;
         if (n == 0) continue;
-        const uint32_t qs = q_it % L::NQB;
-        if (!mbar_wait(bar(B_QEMPTY + qs), ((q_it / L::NQB) & 1) ^ 1, abort, status)) break;
-        mbar_expect_tx(bar(B_QFULL + qs), L::Q_BYTES);
+        if (qk) {
+          const uint32_t qs = q_it % L::NQB;
+          if (!mbar_wait(bar(B_QEMPTY + qs), ((q_it / L::NQB) & 1) ^ 1, abort, status)) break;
+          mbar_expect_tx(bar(B_QFULL + qs), L::Q_BYTES);
 #pragma unroll
-        for (int a = 0; a < DQK / 64; ++a)
-          tma_load_2d(sb + L::Q_OFF + qs * L::Q_BYTES + a * 16384, &tm_q, w.h * DQK + a * 64,
-                      w.q0 + w.tile * BM, bar(B_QFULL + qs));
-        ++q_it;
-        // consumption order: S(0), S(1), then PV(j) and S(j+2) together
-        ok = load_k(w, 0);
-        if (ok && n > 1) ok = load_k(w, 1);
-        for (int j = 0; j < n && ok; ++j) {
-          ok = load_v(w, j);
-          if (ok && j + 2 < n) ok = load_k(w, j + 2);
+          for (int a = 0; a < DQK / 64; ++a)
+            tma_load_2d(sb + L::Q_OFF + qs * L::Q_BYTES + a * 16384, &tm_q, w.h * DQK + a * 64,
+                        w.q0 + w.tile * BM, bar(B_QFULL + qs));
+          ++q_it;
+        }
+        for (int j = 0; j < n; ++j, ++t_it) {
+          if (qk) {
+            const uint32_t st = t_it % NK;
+            if (!mbar_wait(bar(B_KEMPTY + st), ((t_it / NK) & 1) ^ 1, abort, status)) { ok = false; break; }
+            mbar_expect_tx(bar(B_KFULL + st), L::K_BYTES);
+#pragma unroll
+            for (int a = 0; a < DQK / 64; ++a)
+              tma_load_2d(sb + L::K_OFF + st * L::K_BYTES + a * 16384, &tm_k, w.h * DQK + a * 64,
+                          w.k0 + j * BN, bar(B_KFULL + st));
+          } else {
+            const uint32_t st = t_it % NV;
+            if (!mbar_wait(bar(B_VEMPTY + st), ((t_it / NV) & 1) ^ 1, abort, status)) { ok = false; break; }
+            mbar_expect_tx(bar(B_VFULL + st), L::V_BYTES);
+#pragma unroll
+            for (int a = 0; a < DV / 64; ++a)
+              tma_load_2d(sb + L::V_OFF + st * L::V_BYTES + a * 16384, &tm_v, w.h * DV + a * 64,
+                          w.k0 + j * BN, bar(B_VFULL + st));
+          }
         }
       }
     }
