@@ -702,11 +702,13 @@ struct QLayout {
 };
 
 // Each ring has one consumer thread: Q and K feed issuer A (S and dQ), dO and V
-// feed issuer B (dP).
+// feed issuer B (dP).  dS(g) is signalled on DSFULL[g & 1]: S(g+1) is issued before
+// issuer A waits for dS(g), so the compute warps may finish steps g and g+1 before
+// it looks, and a single barrier would then have moved on by two phases.
 enum : uint32_t {
   Q_QFULL = 0, Q_QEMPTY = 2, Q_OFULL = 4, Q_OEMPTY = 6, Q_KFULL = 8, Q_KEMPTY = 14, Q_VFULL = 20,
-  Q_VEMPTY = 24, Q_SFULL = 28, Q_DPFULL = 30, Q_DPEMPTY = 31, Q_DSFULL = 32, Q_ACCFULL = 33,
-  Q_ACCEMPTY = 34, Q_COUNT = 35
+  Q_VEMPTY = 24, Q_SFULL = 28, Q_DPFULL = 30, Q_DPEMPTY = 31, Q_DSFULL = 32, Q_ACCFULL = 34,
+  Q_ACCEMPTY = 35, Q_COUNT = 36
 };
 
 template <int DQK, int DV, int ACT, bool CAUSAL>
@@ -759,6 +761,7 @@ tc_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
     mbar_init(bar(Q_DPFULL), 1);
     mbar_init(bar(Q_DPEMPTY), kCompute);
     mbar_init(bar(Q_DSFULL), kCompute);
+    mbar_init(bar(Q_DSFULL + 1), kCompute);
     mbar_init(bar(Q_ACCFULL), 1);
     mbar_init(bar(Q_ACCEMPTY), kCompute);
     *abort = 0;
@@ -823,67 +826,131 @@ tc_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
     __syncwarp();
   } else if (warp == 1) {
     // ------------------------------------------------------------ issuer A: S and dQ
-    // dS(j) is written by the compute warpgroups over their own (already read) S(j)
-    // columns, so the dP columns are free as soon as dP(j) is loaded and dP(j+1)
-    // need not wait for dQ(j); S(j+2) reuses the buffer after dQ(j) has read dS(j).
+    // dS(g) is written by the compute warpgroups over their own (already read) S(g)
+    // columns, so the dP columns are free as soon as dP(g) is loaded and dP(g+1)
+    // need not wait for dQ(g); S(g+2) reuses the buffer after dQ(g) has read dS(g).
+    // With two Q tiles the steps are walked over the CTA's whole list, so S of the
+    // next item's first two steps is issued before the last two dQ products of this
+    // one.  With a single Q tile the items are walked one by one: the next Q tile
+    // loads only once this item's last S has completed, and the cross-item walk was
+    // measured 2-12% slower there.
     if (lane == 0) {
       constexpr uint32_t idesc_s = idesc_bf16(TILE, STEP, 0, 0);
       constexpr uint32_t idesc_dq = idesc_bf16(TILE, DQK, 0, 1);
-      uint32_t q_it = 0, k_it = 0, s_it = 0, d_it = 0, a_it = 0;
-      bool ok = true;
-      WorkItem nxt = blockIdx.x < (unsigned)n_items ? load_item(list, blockIdx.x) : WorkItem{};
-      for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
-        const WorkItem w = nxt;
-        if (it + (int)gridDim.x < n_items) nxt = load_item(list, it + gridDim.x);
-        const int n = w.cost;
-        if (n == 0) continue;
-        const uint32_t qs = q_it % NQ;
-        if (!mbar_wait(bar(Q_QFULL + qs), (q_it / NQ) & 1, abort, status)) break;
-        const uint32_t q_tile = sb + L::Q_OFF + qs * L::Q_BYTES;
-        const uint32_t k_base = k_it, s_base = s_it;
-        auto issue_s = [&](int i) {  // S(i) = Q K(i)^T into buffer (s_base + i) & 1
-          const uint32_t kk_it = k_base + i, kst = kk_it % NK;
-          if (!mbar_wait(bar(Q_KFULL + kst), (kk_it / NK) & 1, abort, status)) return false;
+      if constexpr (NQ == 1) {
+        uint32_t q_it = 0, k_it = 0, s_it = 0, d_it = 0, a_it = 0;
+        bool ok = true;
+        WorkItem nxt = blockIdx.x < (unsigned)n_items ? load_item(list, blockIdx.x) : WorkItem{};
+        for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
+          const WorkItem w = nxt;
+          if (it + (int)gridDim.x < n_items) nxt = load_item(list, it + gridDim.x);
+          const int n = w.cost;
+          if (n == 0) continue;
+          const uint32_t qs = q_it % NQ;
+          if (!mbar_wait(bar(Q_QFULL + qs), (q_it / NQ) & 1, abort, status)) break;
+          const uint32_t q_tile = sb + L::Q_OFF + qs * L::Q_BYTES;
+          const uint32_t k_base = k_it, s_base = s_it;
+          auto issue_s = [&](int i) {  // S(i) = Q K(i)^T into buffer (s_base + i) & 1
+            const uint32_t kk_it = k_base + i, kst = kk_it % NK;
+            if (!mbar_wait(bar(Q_KFULL + kst), (kk_it / NK) & 1, abort, status)) return false;
+            tc_fence_after();
+            const uint32_t k_tile = sb + L::K_OFF + kst * L::K_BYTES;
+#pragma unroll
+            for (int kk = 0; kk < DQK / 16; ++kk) {
+              const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+              mma_bf16(tmem + t_s((s_base + i) & 1), sw128_desc(q_tile + off, 16, 1024),
+                       sw128_desc(k_tile + off, 16, 1024), idesc_s, kk > 0 ? 1u : 0u);
+            }
+            mma_commit(bar(Q_SFULL + ((s_base + i) & 1)));
+            if (i == n - 1) mma_commit(bar(Q_QEMPTY + qs));  // last use of this Q tile
+            return true;
+          };
+          ok = issue_s(0);
+          if (ok && n > 1) ok = issue_s(1);
+          for (int j = 0; j < n && ok; ++j) {
+            const uint32_t kst = (k_base + j) % NK;
+            // dQ += dS(j) K(j); dS packed in TMEM over the S(j) columns of each group
+            if (!mbar_wait(bar(Q_DSFULL + (d_it & 1)), (d_it >> 1) & 1, abort, status) ||
+                (j == 0 && !mbar_wait(bar(Q_ACCEMPTY), (a_it & 1) ^ 1, abort, status))) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t k_tile = sb + L::K_OFF + kst * L::K_BYTES;
+            const uint32_t ds_tm = tmem + t_s((s_base + j) & 1);
+#pragma unroll
+            for (int kk = 0; kk < STEP / 16; ++kk)
+              mma_bf16_tmem_a(tmem + T_DQ, ds_tm + (kk / (HC / 16)) * HC + (kk % (HC / 16)) * 8,
+                              sw128_desc(k_tile + kk * 2048, 16384, 1024), idesc_dq,
+                              (j > 0 || kk > 0) ? 1u : 0u);
+            mma_commit(bar(Q_KEMPTY + kst));
+            ++d_it;
+            if (j + 2 < n) ok = issue_s(j + 2);
+          }
+          if (!ok) break;
+          mma_commit(bar(Q_ACCFULL));
+          k_it += n;
+          s_it += n;
+          ++q_it;
+          ++a_it;
+        }
+      } else {
+        uint32_t a_it = 0;
+        bool ok = true;
+        // S(c.g) = Q K(c.g)^T into buffer c.g & 1; the item's Q tile is stage c.kv % NQ
+        auto issue_s = [&](const StepCursor& c) -> bool {
+          const uint32_t qs = c.kv % NQ, kst = c.g % NK;
+          if ((c.j == 0 && !mbar_wait(bar(Q_QFULL + qs), (c.kv / NQ) & 1, abort, status)) ||
+              !mbar_wait(bar(Q_KFULL + kst), (c.g / NK) & 1, abort, status))
+            return false;
           tc_fence_after();
+          const uint32_t q_tile = sb + L::Q_OFF + qs * L::Q_BYTES;
           const uint32_t k_tile = sb + L::K_OFF + kst * L::K_BYTES;
 #pragma unroll
           for (int kk = 0; kk < DQK / 16; ++kk) {
             const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-            mma_bf16(tmem + t_s((s_base + i) & 1), sw128_desc(q_tile + off, 16, 1024),
+            mma_bf16(tmem + t_s(c.g & 1), sw128_desc(q_tile + off, 16, 1024),
                      sw128_desc(k_tile + off, 16, 1024), idesc_s, kk > 0 ? 1u : 0u);
           }
-          mma_commit(bar(Q_SFULL + ((s_base + i) & 1)));
-          if (i == n - 1) mma_commit(bar(Q_QEMPTY + qs));  // last use of this Q tile
+          mma_commit(bar(Q_SFULL + (c.g & 1)));
+          if (c.last()) mma_commit(bar(Q_QEMPTY + qs));  // last use of this Q tile
           return true;
         };
-        ok = issue_s(0);
-        if (ok && n > 1) ok = issue_s(1);
-        for (int j = 0; j < n && ok; ++j) {
-          const uint32_t kst = (k_base + j) % NK;
-          // dQ += dS(j) K(j); dS packed in TMEM over the S(j) columns of each group
-          if (!mbar_wait(bar(Q_DSFULL), d_it & 1, abort, status) ||
-              (j == 0 && !mbar_wait(bar(Q_ACCEMPTY), (a_it & 1) ^ 1, abort, status))) {
+        StepCursor cs, cg;  // cs: next S (up to two steps ahead); cg: next dQ
+        cs.init(list, n_items);
+        cg = cs;
+        auto run_ahead = [&]() -> bool {  // S up to step cg.g + 1
+          while (cs.valid && cg.valid && cs.g < cg.g + 2) {
+            if (!issue_s(cs)) return false;
+            cs.advance();
+          }
+          return true;
+        };
+        ok = run_ahead();
+        while (ok && cg.valid) {
+          // dQ += dS(g) K(g); dS packed in TMEM over the S(g) columns of each group
+          const uint32_t kst = cg.g % NK;
+          if (!mbar_wait(bar(Q_DSFULL + (cg.g & 1)), (cg.g >> 1) & 1, abort, status) ||
+              (cg.j == 0 && !mbar_wait(bar(Q_ACCEMPTY), (a_it & 1) ^ 1, abort, status))) {
             ok = false;
             break;
           }
           tc_fence_after();
           const uint32_t k_tile = sb + L::K_OFF + kst * L::K_BYTES;
-          const uint32_t ds_tm = tmem + t_s((s_base + j) & 1);
+          const uint32_t ds_tm = tmem + t_s(cg.g & 1);
 #pragma unroll
           for (int kk = 0; kk < STEP / 16; ++kk)
             mma_bf16_tmem_a(tmem + T_DQ, ds_tm + (kk / (HC / 16)) * HC + (kk % (HC / 16)) * 8,
                             sw128_desc(k_tile + kk * 2048, 16384, 1024), idesc_dq,
-                            (j > 0 || kk > 0) ? 1u : 0u);
+                            (cg.j > 0 || kk > 0) ? 1u : 0u);
           mma_commit(bar(Q_KEMPTY + kst));
-          ++d_it;
-          if (j + 2 < n) ok = issue_s(j + 2);
+          if (cg.last()) {
+            mma_commit(bar(Q_ACCFULL));
+            ++a_it;
+          }
+          cg.advance();
+          ok = run_ahead();
         }
-        if (!ok) break;
-        mma_commit(bar(Q_ACCFULL));
-        k_it += n;
-        s_it += n;
-        ++q_it;
-        ++a_it;
       }
     }
     __syncwarp();
@@ -1044,7 +1111,7 @@ tc_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
           tmem_st16(s_tm, dk2);
         tmem_wait_st();
         tc_fence_before();
-        mbar_arrive(bar(Q_DSFULL));
+        mbar_arrive(bar(Q_DSFULL + sbuf));
         if (pend && !epilogue()) { ok = false; break; }
       }
       if (!ok) break;
