@@ -138,8 +138,9 @@ struct KvLayout {
 enum : uint32_t {
   KV_KFULL = 0, KV_KEMPTY = 1, KV_VFULL = 2, KV_VEMPTY = 3, KV_QFULL = 4, KV_QEMPTY = 8,
   KV_OFULL = 12, KV_OEMPTY = 16, KV_RSFULL = 20, KV_SFULL = 24, KV_SEMPTY = 26, KV_DPFULL = 28,
-  KV_PDSFULL = 30, KV_KDONE = 32, KV_ACCFULL = 34, KV_ACCEMPTY = 35, KV_COUNT = 36
+  KV_PDSFULL = 30, KV_KDONE = 32, KV_ACCFULL = 34, KV_ACCEMPTY = 35, KV_DRAIN = 36, KV_COUNT = 38
 };
+static_assert(8 * KV_COUNT + 8 <= 512, "mbarriers, TMEM slot and abort flag in front of the row terms");
 
 // bf16 pair (low, high) of a packed word to two floats, exactly
 __device__ __forceinline__ float2 unpack_bf16(uint32_t u) {
@@ -260,6 +261,8 @@ tc_dkdv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
     }
     mbar_init(bar(KV_ACCFULL), 2);
     mbar_init(bar(KV_ACCEMPTY), kCompute);
+    mbar_init(bar(KV_DRAIN), 1);      // issuer A's exit drain
+    mbar_init(bar(KV_DRAIN + 1), 1);  // issuer B's exit drain
     *abort = 0;
     fence_mbar_init();
   }
@@ -309,6 +312,9 @@ tc_dkdv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
                         (int32_t)(q0 + (qs0 + j) * KSTEP), bar(KV_QFULL + st));
         }
       }
+      // every load issued has landed before the CTA leaves (also after giving up)
+      drain_ring(bar(KV_KFULL), 1, kv_it, status);
+      drain_ring(bar(KV_QFULL), NQ, q_it, status);
     }
     __syncwarp();
   } else if (warp == Gr::kProducer2) {
@@ -338,8 +344,8 @@ tc_dkdv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
             tma_load_2d(sb + L::V_OFF + a * 16384, &tm_v, h * DV + a * 64, (int32_t)(k0 + key0), bar(KV_VFULL));
         }
       }
-      ++kv_it;
       if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) { ok = false; break; }
+      ++kv_it;
       for (int j = 0; j < n && ok; ++j, ++q_it) {
         const int i0 = (qs0 + j) * KSTEP;
         // row terms of this step: issue the global loads before waiting for the stage
@@ -370,6 +376,10 @@ tc_dkdv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
         }
         mbar_arrive(bar(KV_RSFULL + so));
       }
+    }
+    if (lane == 0) {  // every load issued has landed before the CTA leaves
+      drain_ring(bar(KV_VFULL), 1, kv_it, status);
+      drain_ring(bar(KV_OFULL), NO, q_it, status);
     }
     __syncwarp();
   } else if (warp == 1 || warp == Gr::kIssuerB) {
@@ -467,6 +477,7 @@ tc_dkdv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
         }
         cg.advance();
       }
+      mma_drain(bar(KV_DRAIN + (chain_p ? 0 : 1)), status);  // every MMA issued has completed
     }
     __syncwarp();
   } else {
@@ -708,8 +719,9 @@ struct QLayout {
 enum : uint32_t {
   Q_QFULL = 0, Q_QEMPTY = 2, Q_OFULL = 4, Q_OEMPTY = 6, Q_KFULL = 8, Q_KEMPTY = 14, Q_VFULL = 20,
   Q_VEMPTY = 24, Q_SFULL = 28, Q_DPFULL = 30, Q_DPEMPTY = 31, Q_DSFULL = 32, Q_ACCFULL = 34,
-  Q_ACCEMPTY = 35, Q_COUNT = 36
+  Q_ACCEMPTY = 35, Q_DRAIN = 36, Q_COUNT = 38
 };
+static_assert(8 * Q_COUNT + 8 <= 512, "mbarriers, TMEM slot and abort flag in front of the tiles");
 
 template <int DQK, int DV, int ACT, bool CAUSAL>
 __global__ void __launch_bounds__(QGroups::kThreads, 1)
@@ -764,6 +776,8 @@ tc_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
     mbar_init(bar(Q_DSFULL + 1), kCompute);
     mbar_init(bar(Q_ACCFULL), 1);
     mbar_init(bar(Q_ACCEMPTY), kCompute);
+    mbar_init(bar(Q_DRAIN), 1);      // issuer A's exit drain
+    mbar_init(bar(Q_DRAIN + 1), 1);  // issuer B's exit drain
     *abort = 0;
     fence_mbar_init();
   }
@@ -789,7 +803,7 @@ tc_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
       const int D = qk ? DQK : DV;
       const uint32_t row_off = qk ? L::Q_OFF : L::O_OFF, row_bytes = qk ? L::Q_BYTES : L::O_BYTES;
       const uint32_t key_off = qk ? L::K_OFF : L::V_OFF, key_bytes = qk ? L::K_BYTES : L::V_BYTES;
-      const uint32_t nring = qk ? NK : NV;
+      const uint32_t nring = qk ? NK : NV, nrow = qk ? NQ : NO;
       const uint32_t b_rfull = qk ? Q_QFULL : Q_OFULL, b_rempty = qk ? Q_QEMPTY : Q_OEMPTY;
       const uint32_t b_kfull = qk ? Q_KFULL : Q_VFULL, b_kempty = qk ? Q_KEMPTY : Q_VEMPTY;
       uint32_t q_it = 0, t_it = 0;
@@ -802,7 +816,6 @@ tc_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
         if (n == 0) continue;
         const int h = w.h, row0 = w.tile * TILE;
         const int32_t q0 = w.q0, k0 = w.k0;
-        const uint32_t nrow = qk ? NQ : NO;
         const uint32_t qs = q_it % nrow, qph = ((q_it / nrow) & 1) ^ 1;
         if (!mbar_wait(bar(b_rempty + qs), qph, abort, status)) break;
         mbar_expect_tx(bar(b_rfull + qs), row_bytes);
@@ -822,6 +835,9 @@ tc_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
                         bar(b_kfull + st));
         }
       }
+      // every load issued has landed before the CTA leaves (also after giving up)
+      drain_ring(bar(b_rfull), nrow, q_it, status);
+      drain_ring(bar(b_kfull), nring, t_it, status);
     }
     __syncwarp();
   } else if (warp == 1) {
@@ -952,6 +968,7 @@ tc_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
           ok = run_ahead();
         }
       }
+      mma_drain(bar(Q_DRAIN), status);  // every MMA issued has completed
     }
     __syncwarp();
   } else if (warp == Gr::kIssuerB) {
@@ -992,6 +1009,7 @@ tc_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
         if (!ok) break;
         ++q_it;
       }
+      mma_drain(bar(Q_DRAIN + 1), status);  // every MMA issued has completed
     }
     __syncwarp();
   } else {

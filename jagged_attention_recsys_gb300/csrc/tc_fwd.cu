@@ -80,8 +80,9 @@ struct FwdLayout {
 enum : uint32_t {
   B_QFULL = 0, B_QEMPTY = 2, B_KFULL = 4, B_KEMPTY = 10, B_VFULL = 16, B_VEMPTY = 22,
   B_SFULL = 28, B_PFULL = 30, B_PEMPTY = 32, B_OFULL = 34, B_OEMPTY = 35, B_RED = 36, B_REDL = 38,
-  B_COUNT = 40
+  B_DRAIN = 40, B_COUNT = 42
 };
+static_assert(8 * B_COUNT + 8 <= FwdLayout<128, 128>::RED_OFF, "mbarriers, TMEM slot and abort flag in front");
 constexpr uint32_t T_S = 0, T_O = 256, T_P = 384;  // S: 2 x 128 columns; P: 2 x 64 columns
 
 template <int DQK, int DV, int ACT, bool CAUSAL>
@@ -129,6 +130,8 @@ tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     }
     mbar_init(bar(B_OFULL), 1);
     mbar_init(bar(B_OEMPTY), 256);
+    mbar_init(bar(B_DRAIN), 1);      // S issuer's exit drain
+    mbar_init(bar(B_DRAIN + 1), 1);  // PV issuer's exit drain
     *abort = 0;
     fence_mbar_init();
   }
@@ -188,6 +191,13 @@ tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
           }
         }
       }
+      // every load issued has landed before the CTA leaves (also after giving up)
+      if (qk) {
+        drain_ring(bar(B_QFULL), L::NQB, q_it, status);
+        drain_ring(bar(B_KFULL), NK, t_it, status);
+      } else {
+        drain_ring(bar(B_VFULL), NV, t_it, status);
+      }
     }
     __syncwarp();
   } else if (warp == kSWarp) {
@@ -230,6 +240,7 @@ tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         }
         ++q_it;
       }
+      mma_drain(bar(B_DRAIN), status);  // every MMA issued has completed
     }
     __syncwarp();
   } else if (warp == kPvWarp) {
@@ -266,6 +277,7 @@ tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         if (!ok) break;
         ++o_it;
       }
+      mma_drain(bar(B_DRAIN + 1), status);  // every MMA issued has completed
     }
     __syncwarp();
   } else {

@@ -64,6 +64,33 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
   }
 }
 
+// Bounded wait used when a role leaves its loop, normally or after giving up: it
+// ignores the abort flag, so that a role that gave up still waits for its own
+// asynchronous operations (MMAs, TMA loads) to land before the CTA frees TMEM and
+// exits.  They always complete, so the limit is only a guard.
+__device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity, int* status) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  const long long limit = 4000000000LL;  // ~2 s at 2 GHz
+  for (uint32_t i = 1;; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 255u) == 0 && clock64() - t0 > limit) {
+      atomicExch(status, (int)JFA_ERR_TIMEOUT);
+      return false;
+    }
+  }
+}
+
+// A producer's loads into a ring of `stages` stages with `loads` loads issued in
+// stage order: waits until the last load into every stage has landed.
+__device__ __forceinline__ void drain_ring(uint32_t full_bar0, uint32_t stages, uint32_t loads,
+                                           int* status) {
+  for (uint32_t s = 0; s < stages && s < loads; ++s) {
+    const uint32_t count = (loads - s + stages - 1) / stages;  // loads into stage s
+    mbar_wait_drain(full_bar0 + 8u * s, (count - 1) & 1u, status);
+  }
+}
+
 // ---------------------------------------------------------------- fences
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -123,6 +150,12 @@ __device__ __forceinline__ void mma_commit(uint32_t bar) {
   asm volatile(
       "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
       : "memory");
+}
+// An MMA issuer's drain when it leaves its loop: a commit of everything it issued
+// to a barrier of its own (count 1, used once), and a wait for it.
+__device__ __forceinline__ void mma_drain(uint32_t drain_bar, int* status) {
+  mma_commit(drain_bar);
+  mbar_wait_drain(drain_bar, 0, status);
 }
 
 // 32 consecutive fp32 columns of this thread's TMEM lane (warp-collective).
