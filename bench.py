@@ -35,7 +35,7 @@ METRIC = "useful (unpadded) attention TFLOP/s fwd+bwd on 1 GB300; % of dense BF1
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 L2_FLUSH_BYTES = 256 << 20
 KERNEL_SOURCES = {"fwd": "tc_fwd.cu", "bwd_dkdv": "tc_bwd.cu", "bwd_dq": "tc_bwd.cu",
-                  "bwd_d": "simt.cu", "schedule": "sched.cu"}
+                  "bwd_d": "tc_bwd.cu", "schedule": "sched.cu"}
 
 
 def log(*a):
