@@ -203,6 +203,39 @@ jfa_status jfa_profile_read(int kind, int64_t* launches, double* total_ms);
  */
 int jfa_path_for(const jfa_params* p);
 
+/*
+ * Base Batch Shuffling: a plan that spreads a global batch over `ranks`
+ * data-parallel ranks with balanced attention work and no data exchanged
+ * between ranks (Meta GEM MFU write-up, piletech.kr/articles/112134, details
+ * section, Base Batch Shuffling bullet: sub-batches of 128 samples sorted by
+ * sequence length, the heaviest merged with the lightest in turn).  Host
+ * function; touches no GPU.  Every rank calls it with the same per-sample
+ * costs and gets the same plan, then loads only the sub-batches assigned to
+ * it.
+ *
+ * Plan (readings where the pages are silent):
+ *   - sub-batch s holds samples s*sub .. min((s+1)*sub, n_samples)-1, and costs
+ *     the sum of their `cost` (the caller's measure, e.g. useful attention
+ *     FLOPs: Lq*Lk, or L(L+1)/2 when causal);
+ *   - sub-batches are sorted by cost, heaviest first, ties by index;
+ *   - pair i merges the i-th heaviest with the i-th lightest (the middle one of
+ *     an odd count stays single);
+ *   - pairs go to ranks in serpentine order 0, 1, .., R-1, R-1, .., 0, 0, ..,
+ *     so ranks receive equally many pairs, within one.
+ *
+ * cost       host int64 [n_samples], every value >= 0
+ * sub        samples per sub-batch (the pages use 128), >= 1
+ * ranks      number of ranks, >= 1
+ * sub_rank   host int32 [ceil(n_samples/sub)], out: rank of each sub-batch
+ * sub_slot   host int32 [ceil(n_samples/sub)], out: its position in that
+ *            rank's list (heavy member of a pair first)
+ * rank_cost  host int64 [ranks] or NULL, out: each rank's total cost
+ * Returns JFA_ERR_INVALID_ARG (and writes nothing) for n_samples < 0, sub < 1,
+ * ranks < 1, a negative cost, or a NULL array with n_samples > 0.
+ */
+jfa_status jfa_bbs_plan(const int64_t* cost, int64_t n_samples, int32_t sub, int32_t ranks,
+                        int32_t* sub_rank, int32_t* sub_slot, int64_t* rank_cost);
+
 #ifdef __cplusplus
 }
 #endif

@@ -14,6 +14,7 @@ import ctypes
 import math
 import os
 
+import numpy as np
 import torch
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -36,7 +37,7 @@ KERNEL_KINDS = {"schedule": 0, "fwd": 1, "bwd_d": 2, "bwd_dkdv": 3, "bwd_dq": 4}
 EXPORTS = ("jfa_workspace_size", "jfa_fwd", "jfa_bwd", "jfa_cross_fwd", "jfa_cross_bwd",
            "jfa_gdpa_fwd", "jfa_gdpa_bwd", "jfa_status_check", "jfa_status_string",
            "jfa_profile_enable", "jfa_profile_reset", "jfa_profile_read", "jfa_path_for",
-           "jfa_fwd_noalloc")
+           "jfa_fwd_noalloc", "jfa_bbs_plan")
 
 
 class JfaError(RuntimeError):
@@ -93,6 +94,8 @@ def lib():
         L.jfa_profile_read.argtypes = [ctypes.c_int, ctypes.POINTER(ctypes.c_int64),
                                        ctypes.POINTER(ctypes.c_double)]
         L.jfa_profile_read.restype = ctypes.c_int
+        L.jfa_bbs_plan.argtypes = [vp, ctypes.c_int64, ctypes.c_int32, ctypes.c_int32, vp, vp, vp]
+        L.jfa_bbs_plan.restype = ctypes.c_int
         _lib = L
     return _lib
 
@@ -132,6 +135,20 @@ def jfa_workspace_size(p: jfa_params) -> int:
 
 def jfa_path_for(p: jfa_params) -> int:
     return int(lib().jfa_path_for(ctypes.byref(p)))
+
+
+def jfa_bbs_plan(cost, sub=128, ranks=1):
+    """Base Batch Shuffling plan (host only): returns (sub_rank, sub_slot, rank_cost) numpy
+    arrays for per-sample costs `cost`, `sub` samples per sub-batch and `ranks` ranks."""
+    c = np.ascontiguousarray(np.asarray(cost, dtype=np.int64))
+    n_sub = -(-c.size // int(sub)) if int(sub) > 0 else 0
+    sub_rank = np.zeros(max(n_sub, 1), np.int32)
+    sub_slot = np.zeros(max(n_sub, 1), np.int32)
+    rank_cost = np.zeros(max(int(ranks), 1), np.int64)
+    _check(lib().jfa_bbs_plan(c.ctypes.data if c.size else None, c.size, int(sub), int(ranks),
+                              sub_rank.ctypes.data, sub_slot.ctypes.data, rank_cost.ctypes.data),
+           "jfa_bbs_plan")
+    return sub_rank[:n_sub], sub_slot[:n_sub], rank_cost[:int(ranks)]
 
 
 def workspace(p: jfa_params, device="cuda") -> torch.Tensor:
