@@ -14,6 +14,10 @@ on variable-length tensors; self / cross / asymmetric-QKV patterns) and the
 Generalized Dot-Product Attention bullet (non-softmax activation).  The
 library fixes that activation to SiLU(u)/L with L the sequence length.
 
+Pooled multi-head attention (``pooled_fwd`` / ``pooled_bwd``) is the cross-attention
+above with every sequence's query block equal to the same shared rows, and the
+shared rows' gradient summed over sequences.
+
 Every oracle function here has independent pins in ``tests/test_oracle_pins.py``
 (50-digit brute force, finite differences, padded dense attention through
 torch autograd, closed forms and invariants).
@@ -140,3 +144,29 @@ def bwd(q, k, v, dout, offs_q, offs_k=None, scale=None, causal=False, act=ACT_SO
         raise ValueError("oracle_bwd: " + _ERRORS.get(rc, str(rc)))
     return dq, dk, dv
 
+
+
+def pooled_fwd(q, k, v, offs_k, scale=None):
+    """Pooled multi-head attention forward: the m rows of q [m,H,Dqk] are the query block of
+    every sequence (Meta GEM MFU write-up, details section, jagged-input bullet: pooled
+    multi-head attention is one of the attention patterns).  Softmax, non-causal.
+    Returns (o [B*m,H,Dv], lse [B*m,H]); sequence b's outputs are rows b*m .. b*m+m-1."""
+    q = _f64(q)
+    offs_k = _i64(offs_k)
+    B, m = offs_k.shape[0] - 1, q.shape[0]
+    q_rep = np.tile(q, (max(B, 0), 1, 1))
+    offs_q = np.arange(B + 1, dtype=np.int64) * m
+    return fwd(q_rep, k, v, offs_q, offs_k, scale=scale)
+
+
+def pooled_bwd(q, k, v, dout, offs_k, scale=None):
+    """Pooled multi-head attention backward: (dq [m,H,Dqk], dk, dv).  The shared queries'
+    gradient is the sum over sequences of each sequence's query-block gradient."""
+    q = _f64(q)
+    offs_k = _i64(offs_k)
+    B, m = offs_k.shape[0] - 1, q.shape[0]
+    q_rep = np.tile(q, (max(B, 0), 1, 1))
+    offs_q = np.arange(B + 1, dtype=np.int64) * m
+    dq_rep, dk, dv = bwd(q_rep, k, v, dout, offs_q, offs_k, scale=scale)
+    dq = dq_rep.reshape(max(B, 0), m, *q.shape[1:]).sum(axis=0) if B > 0 else np.zeros_like(q)
+    return dq, dk, dv

@@ -424,3 +424,41 @@ def test_bad_offsets_rejected():
         oracle.fwd(q, q, q, np.array([0, 3, 2, 4]))
     with pytest.raises(ValueError):
         oracle.fwd(q, q, q, np.array([0, 1, 4]), np.array([0, 2, 4]), causal=True)
+
+
+# --------------------------------------------------------------------------------------
+# Pooled multi-head attention: shared queries, through torch autograd per sequence
+# --------------------------------------------------------------------------------------
+def test_pooled_matches_shared_query_autograd():
+    """m shared query rows attend each sequence; torch autograd sums the shared rows'
+    gradient over sequences by itself.  A sequence without keys contributes o = 0."""
+    m, H, Dqk, Dv = 5, 2, 16, 8
+    lk = [7, 1, 0, 40, 13]
+    rng = np.random.default_rng(33)
+    q = rng.standard_normal((m, H, Dqk))
+    k = rng.standard_normal((sum(lk), H, Dqk))
+    v = rng.standard_normal((sum(lk), H, Dv))
+    do = rng.standard_normal((len(lk) * m, H, Dv))
+    ok = _offs(lk)
+    scale = 1.0 / math.sqrt(Dqk)
+    o, lse = oracle.pooled_fwd(q, k, v, ok, scale=scale)
+    dq, dk, dv = oracle.pooled_bwd(q, k, v, do, ok, scale=scale)
+
+    tq = torch.tensor(q, requires_grad=True)
+    tk = torch.tensor(k, requires_grad=True)
+    tv = torch.tensor(v, requires_grad=True)
+    outs = []
+    for b, n in enumerate(lk):
+        if n == 0:
+            outs.append(torch.zeros(m, H, Dv, dtype=torch.float64))
+            continue
+        kb, vb = tk[ok[b]:ok[b + 1]], tv[ok[b]:ok[b + 1]]
+        s = torch.einsum("ihd,jhd->hij", tq, kb) * scale
+        outs.append(torch.einsum("hij,jhd->ihd", torch.softmax(s, dim=-1), vb))
+    out = torch.cat(outs)
+    (out * torch.tensor(do)).sum().backward()
+    np.testing.assert_allclose(o, out.detach().numpy(), rtol=0, atol=1e-12)
+    np.testing.assert_allclose(dq, tq.grad.numpy(), rtol=0, atol=1e-12)
+    np.testing.assert_allclose(dk, tk.grad.numpy(), rtol=0, atol=1e-12)
+    np.testing.assert_allclose(dv, tv.grad.numpy(), rtol=0, atol=1e-12)
+    assert np.all(np.isneginf(lse[2 * m:3 * m]))  # the sequence without keys
