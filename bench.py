@@ -104,6 +104,9 @@ def kernel_flops_bytes(w, lq, lk, tq, tk):
                    e * H * (tq * dq + tk * dq + tk * dv + tq * dv + tq * dq) + rowb),
         "bwd_d": (2 * H * tq * dv, e * H * 2 * tq * dv + 4 * H * tq),
         "schedule": (0, 8 * (len(lq) + 1) * 2),
+        # pooled attention: shared query rows broadcast (tq rows written), per-sequence query
+        # gradients summed (tq rows read)
+        "pool": (0, e * H * dq * 2 * tq),
     }
 
 
@@ -222,7 +225,11 @@ def gpu_step_fn(jfa, w, d, ws):
     q, k, v, do, oq, ok = d["q"], d["k"], d["v"], d["do"], d["oq"], d["ok"]
     o, lse, dq, dk, dv = d["o"], d["lse"], d["dq"], d["dk"], d["dv"]
     sc = w.scale
-    if w.act == workloads.ACT_SILU_OVER_LEN:
+    if w.pooled:
+        def step():
+            jfa.jfa_pooled_fwd(q, k, v, ok, scale=sc, o=o, lse=lse, ws=ws)
+            jfa.jfa_pooled_bwd(q, k, v, o, lse, do, ok, scale=sc, dq=dq, dk=dk, dv=dv, ws=ws)
+    elif w.act == workloads.ACT_SILU_OVER_LEN:
         def step():
             jfa.jfa_gdpa_fwd(q, k, v, oq, ok, scale=sc, causal=w.causal, o=o, ws=ws)
             jfa.jfa_gdpa_bwd(q, k, v, do, oq, ok, scale=sc, causal=w.causal, dq=dq, dk=dk, dv=dv,
@@ -264,8 +271,12 @@ def cpu_baseline(w, lq, lk, budget_s=12.0, seed=0):
     q, k, v, do = f64(q), f64(k), f64(v), f64(do)
     oracle.build()
     t0 = time.perf_counter()
-    oracle.fwd(q, k, v, oq, ok, scale=w.scale, causal=w.causal, act=w.act)
-    oracle.bwd(q, k, v, do, oq, ok, scale=w.scale, causal=w.causal, act=w.act)
+    if w.pooled:
+        oracle.pooled_fwd(q[:w.pooled], k, v, ok, scale=w.scale)
+        oracle.pooled_bwd(q[:w.pooled], k, v, do, ok, scale=w.scale)
+    else:
+        oracle.fwd(q, k, v, oq, ok, scale=w.scale, causal=w.causal, act=w.act)
+        oracle.bwd(q, k, v, do, oq, ok, scale=w.scale, causal=w.causal, act=w.act)
     dt = time.perf_counter() - t0
     f, g = workloads.useful_flops(w, slq, slk)
     return {"value": (f + g) / dt / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
@@ -293,14 +304,18 @@ def run_ours(args):
     d = dict(q=batch["q"], k=batch["k"], v=batch["v"], do=batch["do"],
              oq=torch.as_tensor(batch["offs_q"], device=dev),
              ok=torch.as_tensor(batch["offs_k"], device=dev))
-    tq, tk = d["q"].shape[0], d["k"].shape[0]
+    tq, tk = int(batch["offs_q"][-1]), d["k"].shape[0]
     d["o"] = torch.empty(tq, w.heads, w.dim_v, dtype=w.dtype, device=dev)
     d["lse"] = torch.empty(tq, w.heads, dtype=torch.float32, device=dev)
     d["dq"] = torch.empty_like(d["q"])
     d["dk"] = torch.empty_like(d["k"])
     d["dv"] = torch.empty_like(d["v"])
-    p = jfa.params_for(d["q"], d["k"], d["v"], d["oq"], w.scale, w.causal)
-    ws = jfa.workspace(p, dev)
+    if w.pooled:
+        p, m = jfa.pooled_params(d["q"], d["k"], d["v"], d["ok"], w.scale)
+        ws = jfa.pooled_workspace(p, m, dev)
+    else:
+        p = jfa.params_for(d["q"], d["k"], d["v"], d["oq"], w.scale, w.causal)
+        ws = jfa.workspace(p, dev)
     step = gpu_step_fn(jfa, w, d, ws)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     fwd_f, bwd_f = workloads.useful_flops(w, lq, lk)
@@ -377,7 +392,7 @@ def run_ours(args):
         "config": {"workload": w.name, "batch": w.batch, "heads": w.heads, "dim_qk": w.dim_qk,
                    "dim_v": w.dim_v, "causal": w.causal,
                    "activation": "softmax" if w.act == 0 else "silu_over_len",
-                   "cross": w.cross, "total_q": tq, "total_k": tk,
+                   "cross": w.cross, "pooled_queries": w.pooled or None, "total_q": tq, "total_k": tk,
                    "useful_gflop_fwd": round(fwd_f / 1e9, 3),
                    "useful_gflop_bwd": round(bwd_f / 1e9, 3),
                    "l2": "flushed between timed steps (256 MiB write)",

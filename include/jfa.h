@@ -169,6 +169,35 @@ jfa_status jfa_fwd_noalloc(const jfa_params* p, const void* q, const void* k, co
                            const int64_t* offs, void* o, float* lse, jfa_stream_t stream);
 
 /*
+ * Pooled multi-head attention (Meta GEM MFU write-up,
+ * piletech.kr/articles/112134, details section, jagged-input bullet: pooled
+ * multi-head attention is one of the attention patterns over jagged
+ * sequences).  m learned query rows per head, q [m, H, Dqk], are shared by
+ * every sequence: sequence b's m outputs are the softmax attention of those
+ * rows over its own keys and values, k/v rows offs_k[b] .. offs_k[b+1]-1
+ * (non-causal, scale = p->scale).
+ *   o   [B*m, H, Dv], lse [B*m, H]: sequence b's rows are b*m .. b*m+m-1;
+ *       a sequence without keys gets o = 0, lse = -inf.
+ *   dq  [m, H, Dqk]: the sum over sequences of each sequence's gradient of the
+ *       shared rows (fixed order, bitwise reproducible); dk, dv as in
+ *       jfa_cross_bwd.
+ * p->batch = B, p->total_q = B*m (the rows of o), p->total_k = offs_k[B],
+ * p->causal = 0.  The workspace (size from jfa_pooled_workspace_size, 256-byte
+ * aligned) also holds the query rows broadcast to every sequence and their
+ * per-sequence gradients; it is used as by jfa_cross_fwd / jfa_cross_bwd
+ * otherwise, and errors are reported the same way.  Runs on the
+ * cross-attention kernels.
+ */
+size_t jfa_pooled_workspace_size(const jfa_params* p, int32_t m);
+jfa_status jfa_pooled_fwd(const jfa_params* p, int32_t m, const void* q, const void* k,
+                          const void* v, const int64_t* offs_k, void* o, float* lse, void* ws,
+                          size_t ws_bytes, jfa_stream_t stream);
+jfa_status jfa_pooled_bwd(const jfa_params* p, int32_t m, const void* q, const void* k,
+                          const void* v, const void* o, const float* lse, const void* dout,
+                          const int64_t* offs_k, void* dq, void* dk, void* dv, void* ws,
+                          size_t ws_bytes, jfa_stream_t stream);
+
+/*
  * Synchronises `stream`, then returns the device status word of the last
  * call that used `ws` (JFA_OK, JFA_ERR_BAD_OFFSETS or JFA_ERR_TIMEOUT), or
  * JFA_ERR_CUDA if the synchronisation itself failed.
@@ -191,7 +220,8 @@ enum {
   JFA_KERNEL_BWD_D = 2,    /* backward row term D = rowsum(dO * O) */
   JFA_KERNEL_BWD_DKDV = 3, /* key-tile-major dK/dV pass */
   JFA_KERNEL_BWD_DQ = 4,   /* query-tile-major dQ pass */
-  JFA_KERNEL_KINDS = 5
+  JFA_KERNEL_POOL = 5,     /* pooled attention: query broadcast and query-gradient sum */
+  JFA_KERNEL_KINDS = 6
 };
 jfa_status jfa_profile_enable(int on);
 jfa_status jfa_profile_reset(void);

@@ -31,13 +31,14 @@ JFA_ERR_CUDA = 6
 JFA_F32 = 0
 JFA_BF16 = 1
 
-KERNEL_KINDS = {"schedule": 0, "fwd": 1, "bwd_d": 2, "bwd_dkdv": 3, "bwd_dq": 4}
+KERNEL_KINDS = {"schedule": 0, "fwd": 1, "bwd_d": 2, "bwd_dkdv": 3, "bwd_dq": 4, "pool": 5}
 
 # Every symbol include/jfa.h declares.
 EXPORTS = ("jfa_workspace_size", "jfa_fwd", "jfa_bwd", "jfa_cross_fwd", "jfa_cross_bwd",
            "jfa_gdpa_fwd", "jfa_gdpa_bwd", "jfa_status_check", "jfa_status_string",
            "jfa_profile_enable", "jfa_profile_reset", "jfa_profile_read", "jfa_path_for",
-           "jfa_fwd_noalloc", "jfa_bbs_plan")
+           "jfa_fwd_noalloc", "jfa_bbs_plan", "jfa_pooled_workspace_size", "jfa_pooled_fwd",
+           "jfa_pooled_bwd")
 
 
 class JfaError(RuntimeError):
@@ -96,6 +97,13 @@ def lib():
         L.jfa_profile_read.restype = ctypes.c_int
         L.jfa_bbs_plan.argtypes = [vp, ctypes.c_int64, ctypes.c_int32, ctypes.c_int32, vp, vp, vp]
         L.jfa_bbs_plan.restype = ctypes.c_int
+        i32 = ctypes.c_int32
+        L.jfa_pooled_workspace_size.argtypes = [P, i32]
+        L.jfa_pooled_workspace_size.restype = sz
+        L.jfa_pooled_fwd.argtypes = [P, i32, vp, vp, vp, i64p, vp, fp, vp, sz, vp]
+        L.jfa_pooled_fwd.restype = ctypes.c_int
+        L.jfa_pooled_bwd.argtypes = [P, i32, vp, vp, vp, vp, fp, vp, i64p, vp, vp, vp, vp, sz, vp]
+        L.jfa_pooled_bwd.restype = ctypes.c_int
         _lib = L
     return _lib
 
@@ -294,3 +302,55 @@ def jfa_profile_read(kind: str):
     _check(lib().jfa_profile_read(KERNEL_KINDS[kind], ctypes.byref(n), ctypes.byref(ms)),
            "jfa_profile_read")
     return int(n.value), float(ms.value)
+
+
+# ----------------------------------------------------------------------------- pooled attention
+def pooled_params(q, k, v, offs_k, scale=None):
+    """Params of a pooled call: q [m,H,Dqk] shared rows; B = len(offs_k)-1; o has B*m rows."""
+    B, m = offs_k.numel() - 1, q.shape[0]
+    return make_params(B, B * m, k.shape[0], q.shape[1], q.shape[2], v.shape[2], q.dtype, scale,
+                       False), m
+
+
+def pooled_workspace(p: jfa_params, m: int, device="cuda") -> torch.Tensor:
+    n = int(lib().jfa_pooled_workspace_size(ctypes.byref(p), int(m)))
+    return torch.empty(max(n, 256), dtype=torch.uint8, device=device)
+
+
+def _pooled_prep(q, k, v, offs_k, ws, scale):
+    for t in (q, k, v):
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError("q, k, v must be contiguous CUDA tensors")
+    if offs_k.dtype != torch.int64 or not offs_k.is_cuda:
+        raise ValueError("offsets must be int64 CUDA tensors")
+    p, m = pooled_params(q, k, v, offs_k, scale)
+    if ws is None:
+        ws = pooled_workspace(p, m, q.device)
+    return p, m, ws
+
+
+def jfa_pooled_fwd(q, k, v, offs_k, *, scale=None, o=None, lse=None, ws=None, stream=None):
+    """Pooled multi-head attention forward: the m rows of q attend every sequence;
+    returns (o [B*m,H,Dv], lse [B*m,H])."""
+    p, m, ws = _pooled_prep(q, k, v, offs_k, ws, scale)
+    if o is None:
+        o = torch.empty(p.total_q, q.shape[1], v.shape[2], dtype=q.dtype, device=q.device)
+    if lse is None:
+        lse = torch.empty(p.total_q, q.shape[1], dtype=torch.float32, device=q.device)
+    _check(lib().jfa_pooled_fwd(ctypes.byref(p), m, _ptr(q), _ptr(k), _ptr(v), _ptr(offs_k),
+                                _ptr(o), _ptr(lse), _ptr(ws), ws.numel(), _stream(stream)),
+           "jfa_pooled_fwd")
+    return o, lse
+
+
+def jfa_pooled_bwd(q, k, v, o, lse, dout, offs_k, *, scale=None, dq=None, dk=None, dv=None,
+                   ws=None, stream=None):
+    """Backward of jfa_pooled_fwd; returns (dq [m,H,Dqk] summed over sequences, dk, dv)."""
+    p, m, ws = _pooled_prep(q, k, v, offs_k, ws, scale)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    _check(lib().jfa_pooled_bwd(ctypes.byref(p), m, _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse),
+                                _ptr(dout), _ptr(offs_k), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(ws),
+                                ws.numel(), _stream(stream)), "jfa_pooled_bwd")
+    return dq, dk, dv

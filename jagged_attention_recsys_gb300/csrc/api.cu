@@ -285,6 +285,37 @@ jfa_status run_bwd(const jfa_params* p, Kind kind, int act, const void* q, const
   return cu(launch_simt_dq(pr, p->dtype, q, k, v, lse, dout, dq, w, s));
 }
 
+// Pooled multi-head attention: the cross-attention workspace, then the query-row offsets
+// b*m, the broadcast query rows and their per-sequence gradients.
+struct PooledWs {
+  size_t base, offs, q_rep, dq_rep, total;
+};
+PooledWs pooled_layout(const jfa_params* p, int32_t m) {
+  PooledWs r;
+  const size_t e = p->dtype == JFA_BF16 ? 2 : 4;
+  const size_t rows = (size_t)p->batch * (size_t)m * (size_t)p->heads * (size_t)p->dim_qk * e;
+  r.base = workspace_layout(p->batch, p->total_q, p->total_k, p->heads, nullptr, nullptr);
+  r.offs = align_up(r.base, 256);
+  r.q_rep = align_up(r.offs + 8 * (size_t)(p->batch + 1), 256);
+  r.dq_rep = align_up(r.q_rep + rows, 256);
+  r.total = align_up(r.dq_rep + rows, 256);
+  return r;
+}
+
+jfa_status check_pooled(const jfa_params* p, int32_t m, void* ws, size_t ws_bytes, PooledWs* lay) {
+  if (!p || m < 1) return JFA_ERR_INVALID_ARG;
+  if (p->total_q != p->batch * (int64_t)m) return JFA_ERR_INVALID_ARG;
+  if (p->causal) return JFA_ERR_UNSUPPORTED;
+  const size_t e = p->dtype == JFA_BF16 ? 2 : 4;
+  if (((size_t)p->heads * (size_t)p->dim_qk * e) % 4 != 0) return JFA_ERR_UNSUPPORTED;
+  jfa_status st = check_params(p, Kind::Cross);
+  if (st != JFA_OK) return st;
+  if (!ws || ((uintptr_t)ws & 255u) != 0) return JFA_ERR_WORKSPACE;
+  *lay = pooled_layout(p, m);
+  if (ws_bytes < lay->total) return JFA_ERR_WORKSPACE;
+  return JFA_OK;
+}
+
 }  // namespace
 }  // namespace jfa
 
@@ -348,6 +379,66 @@ jfa_status jfa_gdpa_bwd(const jfa_params* p, const void* q, const void* k, const
                         jfa_stream_t stream) {
   return run_bwd(p, Kind::Gdpa, kActSiluOverLen, q, k, v, nullptr, nullptr, dout, offs_q, offs_k,
                  dq, dk, dv, ws, ws_bytes, (cudaStream_t)stream);
+}
+
+size_t jfa_pooled_workspace_size(const jfa_params* p, int32_t m) {
+  if (!p || m < 1 || p->batch < 0 || p->total_k < 0 || p->heads < 1 || p->dim_qk < 1) return 0;
+  if (p->total_q != p->batch * (int64_t)m) return 0;
+  return pooled_layout(p, m).total;
+}
+
+jfa_status jfa_pooled_fwd(const jfa_params* p, int32_t m, const void* q, const void* k,
+                          const void* v, const int64_t* offs_k, void* o, float* lse, void* ws,
+                          size_t ws_bytes, jfa_stream_t stream) {
+  PooledWs lay;
+  jfa_status st = check_pooled(p, m, ws, ws_bytes, &lay);
+  if (st != JFA_OK) return st;
+  // every argument is checked before the broadcast kernel is launched
+  if ((st = check_ptrs({offs_k})) != JFA_OK) return st;
+  if (p->batch > 0 && (st = check_ptrs({q, o, lse})) != JFA_OK) return st;
+  if (p->total_k > 0 && (st = check_ptrs({k, v})) != JFA_OK) return st;
+  cudaStream_t s = (cudaStream_t)stream;
+  char* base = (char*)ws;
+  int64_t* offs_q = (int64_t*)(base + lay.offs);
+  void* q_rep = base + lay.q_rep;
+  if (p->batch > 0) {
+    const size_t e = p->dtype == JFA_BF16 ? 2 : 4;
+    Timed t(JFA_KERNEL_POOL, s);
+    if ((st = cu(launch_pooled_broadcast(p->batch, m, (int64_t)p->heads * p->dim_qk * (int64_t)e, q,
+                                         q_rep, offs_q, s))) != JFA_OK)
+      return st;
+  }
+  return run_fwd(p, Kind::Cross, kActSoftmax, q_rep, k, v, offs_q, offs_k, o, lse, ws, ws_bytes, s);
+}
+
+jfa_status jfa_pooled_bwd(const jfa_params* p, int32_t m, const void* q, const void* k,
+                          const void* v, const void* o, const float* lse, const void* dout,
+                          const int64_t* offs_k, void* dq, void* dk, void* dv, void* ws,
+                          size_t ws_bytes, jfa_stream_t stream) {
+  PooledWs lay;
+  jfa_status st = check_pooled(p, m, ws, ws_bytes, &lay);
+  if (st != JFA_OK) return st;
+  // every argument is checked before the broadcast kernel is launched
+  if ((st = check_ptrs({offs_k})) != JFA_OK) return st;
+  if (p->batch > 0 && (st = check_ptrs({q, dq, o, lse, dout})) != JFA_OK) return st;
+  if (p->total_k > 0 && (st = check_ptrs({k, v, dk, dv})) != JFA_OK) return st;
+  cudaStream_t s = (cudaStream_t)stream;
+  char* base = (char*)ws;
+  int64_t* offs_q = (int64_t*)(base + lay.offs);
+  void* q_rep = base + lay.q_rep;
+  void* dq_rep = base + lay.dq_rep;
+  const size_t e = p->dtype == JFA_BF16 ? 2 : 4;
+  if (p->batch > 0) {
+    Timed t(JFA_KERNEL_POOL, s);
+    if ((st = cu(launch_pooled_broadcast(p->batch, m, (int64_t)p->heads * p->dim_qk * (int64_t)e, q,
+                                         q_rep, offs_q, s))) != JFA_OK)
+      return st;
+  }
+  st = run_bwd(p, Kind::Cross, kActSoftmax, q_rep, k, v, o, lse, dout, offs_q, offs_k, dq_rep, dk,
+               dv, ws, ws_bytes, s);
+  if (st != JFA_OK || p->batch == 0) return st;
+  Timed t(JFA_KERNEL_POOL, s);
+  return cu(launch_pooled_reduce(p->dtype, p->batch, (int64_t)m * p->heads * p->dim_qk, dq_rep, dq, s));
 }
 
 jfa_status jfa_status_check(const void* ws, jfa_stream_t stream) {

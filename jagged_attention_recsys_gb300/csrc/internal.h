@@ -103,6 +103,13 @@ cudaError_t launch_simt_dq(const Problem& p, int dtype, const void* q, const voi
                            const void* v, const float* lse, const void* dout, void* dq,
                            const Workspace& ws, cudaStream_t s);
 
+// Pooled multi-head attention: broadcast of the m shared query rows into B blocks of
+// m rows with offsets b*m, and the fixed-order sum of the B per-block query gradients.
+cudaError_t launch_pooled_broadcast(int64_t batch, int32_t m, int64_t row_bytes, const void* q,
+                                    void* q_rep, int64_t* offs_q, cudaStream_t s);
+cudaError_t launch_pooled_reduce(int dtype, int64_t batch, int64_t per_seq_elems, const void* dq_rep,
+                                 void* dq, cudaStream_t s);
+
 int num_sms();
 
 }  // namespace jfa

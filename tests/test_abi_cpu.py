@@ -95,6 +95,24 @@ def test_cross_rejects_causal(L):
     assert rc == jfa.JFA_ERR_UNSUPPORTED
 
 
+def test_pooled_checks_on_host(L):
+    vp = ctypes.c_void_p
+    # 3 sequences, m = 4 shared query rows: o has 12 rows
+    p = P(batch=3, total_q=12, total_k=30)
+    assert L.jfa_pooled_workspace_size(ctypes.byref(p), 4) > L.jfa_workspace_size(ctypes.byref(p))
+    assert L.jfa_pooled_workspace_size(ctypes.byref(p), 5) == 0  # total_q != B*m
+
+    def fwd(p, m=4, ptr=16, ws_bytes=1 << 24):
+        return L.jfa_pooled_fwd(ctypes.byref(p), m, vp(ptr), vp(ptr), vp(ptr), vp(ptr), vp(ptr),
+                                vp(ptr), vp(256), ws_bytes, None)
+
+    assert fwd(p, m=0) == jfa.JFA_ERR_INVALID_ARG
+    assert fwd(p, m=5) == jfa.JFA_ERR_INVALID_ARG
+    assert fwd(P(batch=3, total_q=12, total_k=30, causal=1)) == jfa.JFA_ERR_UNSUPPORTED
+    assert fwd(p, ptr=8) == jfa.JFA_ERR_INVALID_ARG  # misaligned: nothing is launched
+    assert fwd(p, ws_bytes=1024) == jfa.JFA_ERR_WORKSPACE
+
+
 def test_profile_read_rejects_bad_kind(L):
     n = ctypes.c_int64()
     ms = ctypes.c_double()

@@ -11,7 +11,7 @@ import torch
 import workloads
 from workloads import ACT_SILU_OVER_LEN as GD, ACT_SOFTMAX as SM, Workload
 
-from parity_util import full_check, run_gpu, sample_indices, sampled_check, to64
+from parity_util import compare, full_check, run_gpu, sample_indices, sampled_check, to64
 
 pytestmark = pytest.mark.gpu
 
@@ -165,3 +165,67 @@ def test_full_size_workload_sampled(name):
             assert torch.isfinite(t).all()
     idx = sample_indices(batch["lq"], count=5)
     sampled_check(w, batch, got, idx)
+
+
+# ----------------------------------------------------------------------------- pooled
+def _pooled_run(m, lk, H, Dqk, Dv, dtype, seed):
+    import jagged_attention_recsys_gb300 as jfa
+
+    B = len(lk)
+    ok = workloads.offsets(lk)
+    q, k, v, do = workloads.values(B * m, int(ok[-1]), H, Dqk, Dv, dtype, seed, "cuda")
+    q = q[:m].contiguous()  # the shared query rows
+    okd = torch.as_tensor(ok, device="cuda")
+    o, lse = jfa.jfa_pooled_fwd(q, k, v, okd)
+    dq, dk, dv = jfa.jfa_pooled_bwd(q, k, v, o, lse, do, okd)
+    torch.cuda.synchronize()
+    got = dict(o=to64(o), lse=to64(lse), dq=to64(dq), dk=to64(dk), dv=to64(dv))
+    import oracle
+
+    qq, kk, vv, dd = (to64(t) for t in (q, k, v, do))
+    ro, rlse = oracle.pooled_fwd(qq, kk, vv, ok)
+    rdq, rdk, rdv = oracle.pooled_bwd(qq, kk, vv, dd, ok)
+    ref = dict(o=ro, lse=rlse, dq=rdq, dk=rdk, dv=rdv)
+    return got, ref
+
+
+@pytest.mark.parametrize("dims,m", [((128, 64), 32), ((64, 64), 1), ((128, 128), 130)])
+def test_bf16_pooled(dims, m):
+    """m shared query rows over ragged key sequences (one empty, one longer than a tile)."""
+    got, ref = _pooled_run(m, [1, 0, 300, 4096, 129, 64, 17], 2, *dims, BF16, seed=4)
+    compare(W(*dims, cross=True), got, ref, fp32=False)
+
+
+def test_fp32_pooled():
+    got, ref = _pooled_run(5, [3, 0, 40, 129], 2, 32, 16, F32, seed=5)
+    compare(W(32, 16, dtype=F32, cross=True), got, ref, fp32=True)
+
+
+def test_full_size_pooled_workload():
+    """The pooled workload at full size (512 sequences, 32 shared rows, keys up to 4096):
+    o, lse, dk, dv equal, bit for bit, the cross-attention path given the shared rows
+    broadcast to every sequence; dq equals the fp64 sum of that path's per-sequence query
+    gradients; a sample of whole sequences matches the oracle."""
+    import jagged_attention_recsys_gb300 as jfa
+
+    w = workloads.WORKLOADS["pooled"]
+    batch = workloads.make_batch(w, device="cuda")
+    q, k, v, do = batch["q"], batch["k"], batch["v"], batch["do"]
+    B, m = len(batch["lk"]), w.pooled
+    okd = torch.as_tensor(batch["offs_k"], device="cuda")
+    oqd = torch.as_tensor(batch["offs_q"], device="cuda")
+    o, lse = jfa.jfa_pooled_fwd(q, k, v, okd)
+    dq, dk, dv = jfa.jfa_pooled_bwd(q, k, v, o, lse, do, okd)
+    q_rep = q.repeat(B, 1, 1)
+    o2, lse2 = jfa.jfa_cross_fwd(q_rep, k, v, oqd, okd)
+    dq2, dk2, dv2 = jfa.jfa_cross_bwd(q_rep, k, v, o2, lse2, do, oqd, okd)
+    torch.cuda.synchronize()
+    for a, b, n in ((o, o2, "o"), (lse, lse2, "lse"), (dk, dk2, "dk"), (dv, dv2, "dv")):
+        assert torch.equal(a, b), n
+    assert torch.isfinite(dq.float()).all()
+    ref_dq = dq2.double().view(B, m, *q.shape[1:]).sum(0)
+    err = float(torch.linalg.vector_norm(dq.double() - ref_dq) / torch.linalg.vector_norm(ref_dq))
+    assert err <= 4e-3, err  # bf16 rounding of the sum
+    rep = dict(batch, q=q_rep)
+    idx = sample_indices(batch["lk"], count=5)
+    sampled_check(w, rep, dict(o=o, lse=lse, dq=dq2, dk=dk, dv=dv), idx)

@@ -20,6 +20,9 @@ Workloads (named by what they are):
             key lengths uniform in [1, 4096], H=4, Dqk=128, Dv=64, bf16, softmax.
 ``gdpa``    B=256 causal non-softmax attention P = SiLU(QK^T/sqrt(D))/L, lengths uniform
             in [256, 4096], H=8, D=128, bf16.
+``pooled``  B=512 pooled multi-head attention: 32 shared learned query rows per head attend
+            every sequence, key lengths uniform in [1, 4096], H=4, Dqk=128, Dv=64, bf16,
+            softmax.  Q holds the 32 shared rows; O and dO have 32 rows per sequence.
 """
 from __future__ import annotations
 
@@ -44,6 +47,7 @@ class Workload:
     act: int
     dtype: torch.dtype
     cross: bool
+    pooled: int = 0  # shared query rows per sequence (pooled attention); 0 = not pooled
 
     @property
     def scale(self) -> float:
@@ -56,6 +60,7 @@ WORKLOADS = {
     "causal": Workload("causal", 1024, 8, 128, 128, True, ACT_SOFTMAX, torch.bfloat16, False),
     "cross": Workload("cross", 512, 4, 128, 64, False, ACT_SOFTMAX, torch.bfloat16, True),
     "gdpa": Workload("gdpa", 256, 8, 128, 128, True, ACT_SILU_OVER_LEN, torch.bfloat16, False),
+    "pooled": Workload("pooled", 512, 4, 128, 64, False, ACT_SOFTMAX, torch.bfloat16, True, 32),
 }
 
 
@@ -78,6 +83,9 @@ def lengths(name: str, seed: int = 0):
     if name == "gdpa":
         lq = rng.integers(256, 4096, 256, endpoint=True).astype(np.int64)
         return lq, lq.copy()
+    if name == "pooled":
+        lk = rng.integers(1, 4096, 512, endpoint=True).astype(np.int64)
+        return np.full(512, 32, dtype=np.int64), lk
     raise KeyError(name)
 
 
@@ -109,6 +117,8 @@ def make_batch(w: Workload, lq=None, lk=None, seed: int = 0, device="cpu"):
     lk = lq.copy() if lk is None else np.asarray(lk, dtype=np.int64)
     oq, ok = offsets(lq), offsets(lk)
     q, k, v, do = values(int(oq[-1]), int(ok[-1]), w.heads, w.dim_qk, w.dim_v, w.dtype, seed, device)
+    if w.pooled:
+        q = q[:w.pooled].contiguous()  # the shared query rows; every lq equals w.pooled
     return dict(lq=lq, lk=lk, offs_q=oq, offs_k=ok, q=q, k=k, v=v, do=do)
 
 
