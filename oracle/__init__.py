@@ -18,6 +18,10 @@ Pooled multi-head attention (``pooled_fwd`` / ``pooled_bwd``) is the cross-atten
 above with every sequence's query block equal to the same shared rows, and the
 shared rows' gradient summed over sequences.
 
+BlockAttention (``block_fwd`` / ``block_bwd``) is softmax self-attention in which a row
+sees only the keys of its own fixed 64-row block of the sequence: the definition above
+applied to every block as a sequence of its own.
+
 Every oracle function here has independent pins in ``tests/test_oracle_pins.py``
 (50-digit brute force, finite differences, padded dense attention through
 torch autograd, closed forms and invariants).
@@ -170,3 +174,33 @@ def pooled_bwd(q, k, v, dout, offs_k, scale=None):
     dq_rep, dk, dv = bwd(q_rep, k, v, dout, offs_q, offs_k, scale=scale)
     dq = dq_rep.reshape(max(B, 0), m, *q.shape[1:]).sum(axis=0) if B > 0 else np.zeros_like(q)
     return dq, dk, dv
+
+
+BLOCK = 64  # BlockAttention block length (tokens)
+
+
+def block_offsets(offs, block=BLOCK):
+    """Offsets of the fixed blocks: every sequence cut into pieces of `block` rows from its
+    first row on (the last piece of a sequence may be shorter)."""
+    offs = _i64(offs)
+    out = [0]
+    for b in range(offs.shape[0] - 1):
+        start, end = int(offs[b]), int(offs[b + 1])
+        for s in range(start, end, block):
+            out.append(min(s + block, end))
+    return np.asarray(out, dtype=np.int64)
+
+
+def block_fwd(q, k, v, offs, scale=None, causal=False):
+    """BlockAttention forward (Meta GEM MFU write-up, details section, BlockAttention bullet:
+    attention within fixed 64-token blocks, linear in the sequence length): softmax
+    self-attention of every row over the keys of its own block (and, if causal, not after
+    it).  Returns (o, lse) like ``fwd``."""
+    bo = block_offsets(offs)
+    return fwd(q, k, v, bo, bo, scale=scale, causal=causal)
+
+
+def block_bwd(q, k, v, dout, offs, scale=None, causal=False):
+    """BlockAttention backward: (dq, dk, dv)."""
+    bo = block_offsets(offs)
+    return bwd(q, k, v, dout, bo, bo, scale=scale, causal=causal)

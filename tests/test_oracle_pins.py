@@ -462,3 +462,46 @@ def test_pooled_matches_shared_query_autograd():
     np.testing.assert_allclose(dk, tk.grad.numpy(), rtol=0, atol=1e-12)
     np.testing.assert_allclose(dv, tv.grad.numpy(), rtol=0, atol=1e-12)
     assert np.all(np.isneginf(lse[2 * m:3 * m]))  # the sequence without keys
+
+
+# --------------------------------------------------------------------------------------
+# BlockAttention: dense attention over the whole sequence with a block-diagonal mask
+# --------------------------------------------------------------------------------------
+def test_block_offsets_cut_each_sequence():
+    assert oracle.block_offsets([0, 3, 3, 200, 264]).tolist() == [0, 3, 67, 131, 195, 200, 264]
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_block_matches_block_diagonal_mask(causal):
+    """Each row attends the keys of its own 64-row block (0-63, 64-127, ... from the start
+    of its sequence), through torch autograd on the whole sequence with an explicit mask."""
+    lens = [1, 64, 65, 200, 0, 130]
+    H, D = 2, 8
+    rng = np.random.default_rng(41)
+    T = sum(lens)
+    q, k, v, do = (rng.standard_normal((T, H, D)) for _ in range(4))
+    offs = _offs(lens)
+    scale = 1.0 / math.sqrt(D)
+    o, lse = oracle.block_fwd(q, k, v, offs, scale=scale, causal=causal)
+    dq, dk, dv = oracle.block_bwd(q, k, v, do, offs, scale=scale, causal=causal)
+    tq, tk, tv = (torch.tensor(x, requires_grad=True) for x in (q, k, v))
+    outs, lses = [], []
+    for b, L in enumerate(lens):
+        if L == 0:
+            continue
+        sl = slice(offs[b], offs[b + 1])
+        i = torch.arange(L)
+        mask = (i[:, None] // 64) == (i[None, :] // 64)
+        if causal:
+            mask &= i[None, :] <= i[:, None]
+        s = torch.einsum("ihd,jhd->hij", tq[sl], tk[sl]) * scale
+        s = s.masked_fill(~mask, float("-inf"))
+        outs.append(torch.einsum("hij,jhd->ihd", torch.softmax(s, dim=-1), tv[sl]))
+        lses.append(torch.logsumexp(s, dim=-1).T)
+    out = torch.cat(outs)
+    (out * torch.tensor(do)).sum().backward()
+    np.testing.assert_allclose(o, out.detach().numpy(), rtol=0, atol=1e-12)
+    np.testing.assert_allclose(lse, torch.cat(lses).detach().numpy(), rtol=0, atol=1e-12)
+    np.testing.assert_allclose(dq, tq.grad.numpy(), rtol=0, atol=1e-12)
+    np.testing.assert_allclose(dk, tk.grad.numpy(), rtol=0, atol=1e-12)
+    np.testing.assert_allclose(dv, tv.grad.numpy(), rtol=0, atol=1e-12)
