@@ -91,7 +91,7 @@ def kernel_flops_bytes(w, lq, lk, tq, tk):
     dkdv: S^T and dP^T recompute, dV and dK products; reads Q, K, V, dO, lse, D, writes dK, dV.
     dq:   S and dP recompute, dQ product; reads Q, K, V, dO, lse, D, writes dQ.
     """
-    P = workloads.valid_pairs(lq, lk, w.causal)
+    P = workloads.valid_pairs(lq, lk, w.causal, w.block)
     H, dq, dv = w.heads, w.dim_qk, w.dim_v
     e = 2 if w.dtype == torch.bfloat16 else 4
     sm = w.act == workloads.ACT_SOFTMAX
@@ -106,7 +106,7 @@ def kernel_flops_bytes(w, lq, lk, tq, tk):
         "schedule": (0, 8 * (len(lq) + 1) * 2),
         # pooled attention: shared query rows broadcast (tq rows written), per-sequence query
         # gradients summed (tq rows read)
-        "pool": (0, e * H * dq * 2 * tq),
+        "aux": (0, e * H * dq * 2 * tq),
     }
 
 
@@ -225,7 +225,12 @@ def gpu_step_fn(jfa, w, d, ws):
     q, k, v, do, oq, ok = d["q"], d["k"], d["v"], d["do"], d["oq"], d["ok"]
     o, lse, dq, dk, dv = d["o"], d["lse"], d["dq"], d["dk"], d["dv"]
     sc = w.scale
-    if w.pooled:
+    if w.block:
+        def step():
+            jfa.jfa_block_fwd(q, k, v, oq, scale=sc, causal=w.causal, o=o, lse=lse, ws=ws)
+            jfa.jfa_block_bwd(q, k, v, o, lse, do, oq, scale=sc, causal=w.causal, dq=dq, dk=dk,
+                              dv=dv, ws=ws)
+    elif w.pooled:
         def step():
             jfa.jfa_pooled_fwd(q, k, v, ok, scale=sc, o=o, lse=lse, ws=ws)
             jfa.jfa_pooled_bwd(q, k, v, o, lse, do, ok, scale=sc, dq=dq, dk=dk, dv=dv, ws=ws)
@@ -274,6 +279,9 @@ def cpu_baseline(w, lq, lk, budget_s=12.0, seed=0):
     if w.pooled:
         oracle.pooled_fwd(q[:w.pooled], k, v, ok, scale=w.scale)
         oracle.pooled_bwd(q[:w.pooled], k, v, do, ok, scale=w.scale)
+    elif w.block:
+        oracle.block_fwd(q, k, v, oq, scale=w.scale, causal=w.causal)
+        oracle.block_bwd(q, k, v, do, oq, scale=w.scale, causal=w.causal)
     else:
         oracle.fwd(q, k, v, oq, ok, scale=w.scale, causal=w.causal, act=w.act)
         oracle.bwd(q, k, v, do, oq, ok, scale=w.scale, causal=w.causal, act=w.act)
@@ -313,6 +321,9 @@ def run_ours(args):
     if w.pooled:
         p, m = jfa.pooled_params(d["q"], d["k"], d["v"], d["ok"], w.scale)
         ws = jfa.pooled_workspace(p, m, dev)
+    elif w.block:
+        p = jfa.params_for(d["q"], d["k"], d["v"], d["oq"], w.scale, w.causal)
+        ws = jfa.block_workspace(p, dev)
     else:
         p = jfa.params_for(d["q"], d["k"], d["v"], d["oq"], w.scale, w.causal)
         ws = jfa.workspace(p, dev)
@@ -392,7 +403,8 @@ def run_ours(args):
         "config": {"workload": w.name, "batch": w.batch, "heads": w.heads, "dim_qk": w.dim_qk,
                    "dim_v": w.dim_v, "causal": w.causal,
                    "activation": "softmax" if w.act == 0 else "silu_over_len",
-                   "cross": w.cross, "pooled_queries": w.pooled or None, "total_q": tq, "total_k": tk,
+                   "cross": w.cross, "pooled_queries": w.pooled or None,
+                   "block": w.block or None, "total_q": tq, "total_k": tk,
                    "useful_gflop_fwd": round(fwd_f / 1e9, 3),
                    "useful_gflop_bwd": round(bwd_f / 1e9, 3),
                    "l2": "flushed between timed steps (256 MiB write)",

@@ -198,6 +198,28 @@ jfa_status jfa_pooled_bwd(const jfa_params* p, int32_t m, const void* q, const v
                           size_t ws_bytes, jfa_stream_t stream);
 
 /*
+ * BlockAttention (Meta GEM MFU write-up, piletech.kr/articles/112134, details
+ * section, BlockAttention bullet: fixed 64-token blocks make attention linear
+ * in the sequence length).  Softmax self-attention in which row i of a
+ * sequence sees only the keys of its own block, rows 64*floor(i/64) ..
+ * 64*floor(i/64)+63 of the same sequence (the last block may be shorter), and
+ * with p->causal = 1 only those not after it.  Arguments and outputs as for
+ * jfa_fwd / jfa_bwd.  The offsets are cut into blocks on the device and the
+ * self-attention kernels run on the blocks as sequences of their own; the
+ * workspace (jfa_block_workspace_size) holds the block offsets and room for up
+ * to B + ceil(T/64) block sequences.  The pages combine the blocks with a fused
+ * rotary position embedding; that embedding is not part of this call.
+ */
+size_t jfa_block_workspace_size(const jfa_params* p);
+jfa_status jfa_block_fwd(const jfa_params* p, const void* q, const void* k, const void* v,
+                         const int64_t* offs, void* o, float* lse, void* ws, size_t ws_bytes,
+                         jfa_stream_t stream);
+jfa_status jfa_block_bwd(const jfa_params* p, const void* q, const void* k, const void* v,
+                         const void* o, const float* lse, const void* dout, const int64_t* offs,
+                         void* dq, void* dk, void* dv, void* ws, size_t ws_bytes,
+                         jfa_stream_t stream);
+
+/*
  * Synchronises `stream`, then returns the device status word of the last
  * call that used `ws` (JFA_OK, JFA_ERR_BAD_OFFSETS or JFA_ERR_TIMEOUT), or
  * JFA_ERR_CUDA if the synchronisation itself failed.
@@ -220,7 +242,7 @@ enum {
   JFA_KERNEL_BWD_D = 2,    /* backward row term D = rowsum(dO * O) */
   JFA_KERNEL_BWD_DKDV = 3, /* key-tile-major dK/dV pass */
   JFA_KERNEL_BWD_DQ = 4,   /* query-tile-major dQ pass */
-  JFA_KERNEL_POOL = 5,     /* pooled attention: query broadcast and query-gradient sum */
+  JFA_KERNEL_AUX = 5,      /* pooled query broadcast and gradient sum; block offsets */
   JFA_KERNEL_KINDS = 6
 };
 jfa_status jfa_profile_enable(int on);

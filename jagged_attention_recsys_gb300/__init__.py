@@ -31,14 +31,14 @@ JFA_ERR_CUDA = 6
 JFA_F32 = 0
 JFA_BF16 = 1
 
-KERNEL_KINDS = {"schedule": 0, "fwd": 1, "bwd_d": 2, "bwd_dkdv": 3, "bwd_dq": 4, "pool": 5}
+KERNEL_KINDS = {"schedule": 0, "fwd": 1, "bwd_d": 2, "bwd_dkdv": 3, "bwd_dq": 4, "aux": 5}
 
 # Every symbol include/jfa.h declares.
 EXPORTS = ("jfa_workspace_size", "jfa_fwd", "jfa_bwd", "jfa_cross_fwd", "jfa_cross_bwd",
            "jfa_gdpa_fwd", "jfa_gdpa_bwd", "jfa_status_check", "jfa_status_string",
            "jfa_profile_enable", "jfa_profile_reset", "jfa_profile_read", "jfa_path_for",
            "jfa_fwd_noalloc", "jfa_bbs_plan", "jfa_pooled_workspace_size", "jfa_pooled_fwd",
-           "jfa_pooled_bwd")
+           "jfa_pooled_bwd", "jfa_block_workspace_size", "jfa_block_fwd", "jfa_block_bwd")
 
 
 class JfaError(RuntimeError):
@@ -104,6 +104,12 @@ def lib():
         L.jfa_pooled_fwd.restype = ctypes.c_int
         L.jfa_pooled_bwd.argtypes = [P, i32, vp, vp, vp, vp, fp, vp, i64p, vp, vp, vp, vp, sz, vp]
         L.jfa_pooled_bwd.restype = ctypes.c_int
+        L.jfa_block_workspace_size.argtypes = [P]
+        L.jfa_block_workspace_size.restype = sz
+        L.jfa_block_fwd.argtypes = [P, vp, vp, vp, i64p, vp, fp, vp, sz, vp]
+        L.jfa_block_fwd.restype = ctypes.c_int
+        L.jfa_block_bwd.argtypes = [P, vp, vp, vp, vp, fp, vp, i64p, vp, vp, vp, vp, sz, vp]
+        L.jfa_block_bwd.restype = ctypes.c_int
         _lib = L
     return _lib
 
@@ -173,14 +179,17 @@ def _stream(stream):
     return ctypes.c_void_p(s.cuda_stream)
 
 
-def _prep(q, k, v, offs_q, offs_k, ws, scale, causal):
+def _check_tensors(q, k, v, offs_q, offs_k=None):
     for t in (q, k, v):
         if not t.is_cuda or not t.is_contiguous():
             raise ValueError("q, k, v must be contiguous CUDA tensors")
-    if offs_q.dtype != torch.int64 or not offs_q.is_cuda:
-        raise ValueError("offsets must be int64 CUDA tensors")
-    if offs_k is not None and (offs_k.dtype != torch.int64 or not offs_k.is_cuda):
-        raise ValueError("offsets must be int64 CUDA tensors")
+    for o in (offs_q, offs_k):
+        if o is not None and (o.dtype != torch.int64 or not o.is_cuda):
+            raise ValueError("offsets must be int64 CUDA tensors")
+
+
+def _prep(q, k, v, offs_q, offs_k, ws, scale, causal):
+    _check_tensors(q, k, v, offs_q, offs_k)
     p = params_for(q, k, v, offs_q, scale, causal)
     if ws is None:
         ws = workspace(p, q.device)
@@ -318,11 +327,7 @@ def pooled_workspace(p: jfa_params, m: int, device="cuda") -> torch.Tensor:
 
 
 def _pooled_prep(q, k, v, offs_k, ws, scale):
-    for t in (q, k, v):
-        if not t.is_cuda or not t.is_contiguous():
-            raise ValueError("q, k, v must be contiguous CUDA tensors")
-    if offs_k.dtype != torch.int64 or not offs_k.is_cuda:
-        raise ValueError("offsets must be int64 CUDA tensors")
+    _check_tensors(q, k, v, offs_k)
     p, m = pooled_params(q, k, v, offs_k, scale)
     if ws is None:
         ws = pooled_workspace(p, m, q.device)
@@ -353,4 +358,40 @@ def jfa_pooled_bwd(q, k, v, o, lse, dout, offs_k, *, scale=None, dq=None, dk=Non
     _check(lib().jfa_pooled_bwd(ctypes.byref(p), m, _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse),
                                 _ptr(dout), _ptr(offs_k), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(ws),
                                 ws.numel(), _stream(stream)), "jfa_pooled_bwd")
+    return dq, dk, dv
+
+
+# ----------------------------------------------------------------------------- BlockAttention
+def block_workspace(p: jfa_params, device="cuda") -> torch.Tensor:
+    n = int(lib().jfa_block_workspace_size(ctypes.byref(p)))
+    return torch.empty(max(n, 256), dtype=torch.uint8, device=device)
+
+
+def jfa_block_fwd(q, k, v, offs, *, scale=None, causal=False, o=None, lse=None, ws=None,
+                  stream=None):
+    """BlockAttention forward (softmax within fixed 64-row blocks); returns (o, lse)."""
+    _check_tensors(q, k, v, offs)
+    p = params_for(q, k, v, offs, scale, causal)
+    ws = block_workspace(p, q.device) if ws is None else ws
+    if o is None:
+        o = torch.empty(q.shape[0], q.shape[1], v.shape[2], dtype=q.dtype, device=q.device)
+    if lse is None:
+        lse = torch.empty(q.shape[0], q.shape[1], dtype=torch.float32, device=q.device)
+    _check(lib().jfa_block_fwd(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(offs), _ptr(o),
+                               _ptr(lse), _ptr(ws), ws.numel(), _stream(stream)), "jfa_block_fwd")
+    return o, lse
+
+
+def jfa_block_bwd(q, k, v, o, lse, dout, offs, *, scale=None, causal=False, dq=None, dk=None,
+                  dv=None, ws=None, stream=None):
+    """Backward of jfa_block_fwd; returns (dq, dk, dv)."""
+    _check_tensors(q, k, v, offs)
+    p = params_for(q, k, v, offs, scale, causal)
+    ws = block_workspace(p, q.device) if ws is None else ws
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    _check(lib().jfa_block_bwd(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse),
+                               _ptr(dout), _ptr(offs), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(ws),
+                               ws.numel(), _stream(stream)), "jfa_block_bwd")
     return dq, dk, dv

@@ -316,6 +316,33 @@ jfa_status check_pooled(const jfa_params* p, int32_t m, void* ws, size_t ws_byte
   return JFA_OK;
 }
 
+// BlockAttention: the self-attention workspace for B + ceil(T/64) block sequences, then the
+// block offsets.
+constexpr int kBlock = 64;
+int64_t block_count(const jfa_params* p) { return p->batch + (p->total_q + kBlock - 1) / kBlock; }
+struct BlockWs {
+  size_t offs, total;
+};
+BlockWs block_layout(const jfa_params* p) {
+  BlockWs r;
+  const int64_t nb = block_count(p);
+  r.offs = align_up(workspace_layout(nb, p->total_q, p->total_k, p->heads, nullptr, nullptr), 256);
+  r.total = align_up(r.offs + 8 * (size_t)(nb + 1), 256);
+  return r;
+}
+
+// params of the block sequences, after the checks a block call makes before any launch
+jfa_status check_block(const jfa_params* p, void* ws, size_t ws_bytes, jfa_params* pb, BlockWs* lay) {
+  jfa_status st = check_params(p, Kind::Self);
+  if (st != JFA_OK) return st;
+  if (!ws || ((uintptr_t)ws & 255u) != 0) return JFA_ERR_WORKSPACE;
+  *lay = block_layout(p);
+  if (ws_bytes < lay->total) return JFA_ERR_WORKSPACE;
+  *pb = *p;
+  pb->batch = block_count(p);
+  return JFA_OK;
+}
+
 }  // namespace
 }  // namespace jfa
 
@@ -403,7 +430,7 @@ jfa_status jfa_pooled_fwd(const jfa_params* p, int32_t m, const void* q, const v
   void* q_rep = base + lay.q_rep;
   if (p->batch > 0) {
     const size_t e = p->dtype == JFA_BF16 ? 2 : 4;
-    Timed t(JFA_KERNEL_POOL, s);
+    Timed t(JFA_KERNEL_AUX, s);
     if ((st = cu(launch_pooled_broadcast(p->batch, m, (int64_t)p->heads * p->dim_qk * (int64_t)e, q,
                                          q_rep, offs_q, s))) != JFA_OK)
       return st;
@@ -429,7 +456,7 @@ jfa_status jfa_pooled_bwd(const jfa_params* p, int32_t m, const void* q, const v
   void* dq_rep = base + lay.dq_rep;
   const size_t e = p->dtype == JFA_BF16 ? 2 : 4;
   if (p->batch > 0) {
-    Timed t(JFA_KERNEL_POOL, s);
+    Timed t(JFA_KERNEL_AUX, s);
     if ((st = cu(launch_pooled_broadcast(p->batch, m, (int64_t)p->heads * p->dim_qk * (int64_t)e, q,
                                          q_rep, offs_q, s))) != JFA_OK)
       return st;
@@ -437,8 +464,53 @@ jfa_status jfa_pooled_bwd(const jfa_params* p, int32_t m, const void* q, const v
   st = run_bwd(p, Kind::Cross, kActSoftmax, q_rep, k, v, o, lse, dout, offs_q, offs_k, dq_rep, dk,
                dv, ws, ws_bytes, s);
   if (st != JFA_OK || p->batch == 0) return st;
-  Timed t(JFA_KERNEL_POOL, s);
+  Timed t(JFA_KERNEL_AUX, s);
   return cu(launch_pooled_reduce(p->dtype, p->batch, (int64_t)m * p->heads * p->dim_qk, dq_rep, dq, s));
+}
+
+size_t jfa_block_workspace_size(const jfa_params* p) {
+  if (!p || p->batch < 0 || p->total_q < 0 || p->total_k < 0 || p->heads < 1) return 0;
+  return block_layout(p).total;
+}
+
+jfa_status jfa_block_fwd(const jfa_params* p, const void* q, const void* k, const void* v,
+                         const int64_t* offs, void* o, float* lse, void* ws, size_t ws_bytes,
+                         jfa_stream_t stream) {
+  jfa_params pb;
+  BlockWs lay;
+  jfa_status st = check_block(p, ws, ws_bytes, &pb, &lay);
+  if (st != JFA_OK) return st;
+  if ((st = check_ptrs({offs})) != JFA_OK) return st;
+  if (p->total_q > 0 && (st = check_ptrs({q, k, v, o, lse})) != JFA_OK) return st;
+  cudaStream_t s = (cudaStream_t)stream;
+  int64_t* boffs = (int64_t*)((char*)ws + lay.offs);
+  if (p->batch > 0) {
+    Timed t(JFA_KERNEL_AUX, s);
+    if ((st = cu(launch_block_offsets(offs, p->batch, p->total_q, kBlock, boffs, pb.batch, s))) != JFA_OK)
+      return st;
+  }
+  return run_fwd(&pb, Kind::Self, kActSoftmax, q, k, v, boffs, boffs, o, lse, ws, ws_bytes, s);
+}
+
+jfa_status jfa_block_bwd(const jfa_params* p, const void* q, const void* k, const void* v,
+                         const void* o, const float* lse, const void* dout, const int64_t* offs,
+                         void* dq, void* dk, void* dv, void* ws, size_t ws_bytes,
+                         jfa_stream_t stream) {
+  jfa_params pb;
+  BlockWs lay;
+  jfa_status st = check_block(p, ws, ws_bytes, &pb, &lay);
+  if (st != JFA_OK) return st;
+  if ((st = check_ptrs({offs})) != JFA_OK) return st;
+  if (p->total_q > 0 && (st = check_ptrs({q, k, v, o, lse, dout, dq, dk, dv})) != JFA_OK) return st;
+  cudaStream_t s = (cudaStream_t)stream;
+  int64_t* boffs = (int64_t*)((char*)ws + lay.offs);
+  if (p->batch > 0) {
+    Timed t(JFA_KERNEL_AUX, s);
+    if ((st = cu(launch_block_offsets(offs, p->batch, p->total_q, kBlock, boffs, pb.batch, s))) != JFA_OK)
+      return st;
+  }
+  return run_bwd(&pb, Kind::Self, kActSoftmax, q, k, v, o, lse, dout, boffs, boffs, dq, dk, dv, ws,
+                 ws_bytes, s);
 }
 
 jfa_status jfa_status_check(const void* ws, jfa_stream_t stream) {

@@ -110,6 +110,11 @@ cudaError_t launch_pooled_broadcast(int64_t batch, int32_t m, int64_t row_bytes,
 cudaError_t launch_pooled_reduce(int dtype, int64_t batch, int64_t per_seq_elems, const void* dq_rep,
                                  void* dq, cudaStream_t s);
 
+// BlockAttention: the offsets of the fixed `block`-row blocks of every sequence, then empty
+// sequences up to n_out (n_out + 1 entries); out[0] = -1 for offsets that are not valid.
+cudaError_t launch_block_offsets(const int64_t* offs, int64_t batch, int64_t total, int block,
+                                 int64_t* out, int64_t n_out, cudaStream_t s);
+
 int num_sms();
 
 }  // namespace jfa

@@ -33,7 +33,7 @@ namespace {
 constexpr int kThreads = 1024;
 constexpr int kWarps = kThreads / 32;
 constexpr int kBuckets = 128;
-constexpr int kCacheB = 4096;  // sequences whose arrays fit in shared memory
+constexpr int kCacheB = 6144;  // sequences whose arrays fit in shared memory (32 B each)
 
 struct SchedShared {
   int warp_tot[32];
@@ -46,6 +46,8 @@ struct SchedShared {
   int order[kCacheB];     // sequences in list order
   int first[kCacheB + 1]; // first unit of the r-th sequence in list order
 };
+
+static_assert(sizeof(SchedShared) <= 232448, "scheduler arrays within one CTA's shared memory");
 
 __device__ __forceinline__ int cdiv(int a, int b) { return (a + b - 1) / b; }
 

@@ -229,3 +229,75 @@ def test_full_size_pooled_workload():
     rep = dict(batch, q=q_rep)
     idx = sample_indices(batch["lk"], count=5)
     sampled_check(w, rep, dict(o=o, lse=lse, dq=dq2, dk=dk, dv=dv), idx)
+
+
+# ----------------------------------------------------------------------------- BlockAttention
+def _block_run(lens, H, Dqk, Dv, dtype, causal, seed):
+    import jagged_attention_recsys_gb300 as jfa
+    import oracle
+
+    offs = workloads.offsets(lens)
+    q, k, v, do = workloads.values(int(offs[-1]), int(offs[-1]), H, Dqk, Dv, dtype, seed, "cuda")
+    od = torch.as_tensor(offs, device="cuda")
+    o, lse = jfa.jfa_block_fwd(q, k, v, od, causal=causal)
+    dq, dk, dv = jfa.jfa_block_bwd(q, k, v, o, lse, do, od, causal=causal)
+    torch.cuda.synchronize()
+    got = dict(o=to64(o), lse=to64(lse), dq=to64(dq), dk=to64(dk), dv=to64(dv))
+    qq, kk, vv, dd = (to64(t) for t in (q, k, v, do))
+    ro, rlse = oracle.block_fwd(qq, kk, vv, offs, causal=causal)
+    rdq, rdk, rdv = oracle.block_bwd(qq, kk, vv, dd, offs, causal=causal)
+    return got, dict(o=ro, lse=rlse, dq=rdq, dk=rdk, dv=rdv)
+
+
+@pytest.mark.parametrize("dims", [(64, 64), (128, 128)])
+@pytest.mark.parametrize("causal", [False, True])
+def test_bf16_block(dims, causal):
+    """Blocks of 64 rows from the start of every sequence; lengths around block and tile edges."""
+    got, ref = _block_run(TILE_EDGES + [0, 1000], 2, *dims, BF16, causal, seed=6)
+    compare(W(*dims, causal=causal), got, ref, fp32=False)
+
+
+def test_fp32_block():
+    got, ref = _block_run([1, 63, 64, 65, 130, 0, 200], 2, 32, 32, F32, True, seed=7)
+    compare(W(32, 32, causal=True, dtype=F32), got, ref, fp32=True)
+
+
+def test_block_bad_offsets_reported():
+    import jagged_attention_recsys_gb300 as jfa
+
+    q, k, v, do = workloads.values(100, 100, 2, 64, 64, BF16, 0, "cuda")
+    bad = torch.as_tensor([0, 60, 40, 100], device="cuda")  # not monotone
+    p = jfa.params_for(q, k, v, bad)
+    ws = jfa.block_workspace(p)
+    o = torch.full((100, 2, 64), 7.0, dtype=BF16, device="cuda")
+    lse = torch.zeros(100, 2, dtype=torch.float32, device="cuda")
+    jfa.jfa_block_fwd(q, k, v, bad, o=o, lse=lse, ws=ws)
+    assert jfa.jfa_status_check(ws) == jfa.JFA_ERR_BAD_OFFSETS
+    assert torch.all(o == 7.0)  # untouched
+
+
+def test_full_size_block_workload():
+    """BlockAttention over the causal workload's 1024 sequences (H=8, D=128) on the GPU; a
+    sample of whole sequences against the oracle."""
+    import jagged_attention_recsys_gb300 as jfa
+    import oracle
+
+    w = workloads.WORKLOADS["block"]
+    batch = workloads.make_batch(w, device="cuda")
+    od = torch.as_tensor(batch["offs_q"], device="cuda")
+    q, k, v, do = batch["q"], batch["k"], batch["v"], batch["do"]
+    o, lse = jfa.jfa_block_fwd(q, k, v, od, causal=True)
+    dq, dk, dv = jfa.jfa_block_bwd(q, k, v, o, lse, do, od, causal=True)
+    torch.cuda.synchronize()
+    for t in (o, lse, dq, dk, dv):
+        assert torch.isfinite(t.float()).all()
+    offs = batch["offs_q"]
+    for b in sample_indices(batch["lq"], count=5):
+        rows = torch.arange(int(offs[b]), int(offs[b + 1]), device="cuda")
+        sub = workloads.offsets([int(offs[b + 1] - offs[b])])
+        qq, kk, vv, dd = (to64(t[rows]) for t in (q, k, v, do))
+        ro, rlse = oracle.block_fwd(qq, kk, vv, sub, causal=True)
+        rdq, rdk, rdv = oracle.block_bwd(qq, kk, vv, dd, sub, causal=True)
+        got = dict(o=to64(o[rows]), lse=to64(lse[rows]), dq=to64(dq[rows]), dk=to64(dk[rows]),
+                   dv=to64(dv[rows]))
+        compare(w, got, dict(o=ro, lse=rlse, dq=rdq, dk=rdk, dv=rdv), fp32=False, strict_o=True)

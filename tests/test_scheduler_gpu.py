@@ -114,7 +114,7 @@ def test_cuda_core_lists_cross():
     assert got_k == with_rows(expected(list(lq), list(lk), H, 64, 32, False, True), lq, lk)
 
 
-@pytest.mark.parametrize("nseq", [2500, 5000])
+@pytest.mark.parametrize("nseq", [2500, 7000])
 def test_large_batch_many_rounds(nseq):
     """More sequences than scheduler threads (several scan rounds), and more than the
     shared-memory cache holds (per-sequence data in the workspace)."""

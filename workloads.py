@@ -23,6 +23,9 @@ Workloads (named by what they are):
 ``pooled``  B=512 pooled multi-head attention: 32 shared learned query rows per head attend
             every sequence, key lengths uniform in [1, 4096], H=4, Dqk=128, Dv=64, bf16,
             softmax.  Q holds the 32 shared rows; O and dO have 32 rows per sequence.
+``block``   BlockAttention over the causal workload's sequences (B=1024, lognormal lengths
+            clipped to [1, 2048], H=8, D=128, bf16): every row attends only the keys of its
+            own 64-row block, causally.
 """
 from __future__ import annotations
 
@@ -48,6 +51,7 @@ class Workload:
     dtype: torch.dtype
     cross: bool
     pooled: int = 0  # shared query rows per sequence (pooled attention); 0 = not pooled
+    block: int = 0   # BlockAttention block length; 0 = whole sequences
 
     @property
     def scale(self) -> float:
@@ -61,6 +65,7 @@ WORKLOADS = {
     "cross": Workload("cross", 512, 4, 128, 64, False, ACT_SOFTMAX, torch.bfloat16, True),
     "gdpa": Workload("gdpa", 256, 8, 128, 128, True, ACT_SILU_OVER_LEN, torch.bfloat16, False),
     "pooled": Workload("pooled", 512, 4, 128, 64, False, ACT_SOFTMAX, torch.bfloat16, True, 32),
+    "block": Workload("block", 1024, 8, 128, 128, True, ACT_SOFTMAX, torch.bfloat16, False, 0, 64),
 }
 
 
@@ -73,7 +78,7 @@ def lengths(name: str, seed: int = 0):
     if name == "d64":
         lq = rng.integers(1, 512, 256, endpoint=True).astype(np.int64)
         return lq, lq.copy()
-    if name == "causal":
+    if name in ("causal", "block"):
         lq = np.clip(np.rint(rng.lognormal(5.5, 0.8, 1024)), 1, 2048).astype(np.int64)
         return lq, lq.copy()
     if name == "cross":
@@ -122,10 +127,15 @@ def make_batch(w: Workload, lq=None, lk=None, seed: int = 0, device="cpu"):
     return dict(lq=lq, lk=lk, offs_q=oq, offs_k=ok, q=q, k=k, v=v, do=do)
 
 
-def valid_pairs(lq, lk, causal: bool) -> float:
-    """Number of (query, key) pairs that take part in attention, per head."""
+def valid_pairs(lq, lk, causal: bool, block: int = 0) -> float:
+    """Number of (query, key) pairs that take part in attention, per head.  With ``block``,
+    attention stays inside each sequence's consecutive blocks of that many rows."""
     lq = np.asarray(lq, dtype=np.float64)
     lk = np.asarray(lk, dtype=np.float64)
+    if block:
+        full, rest = np.floor(lq / block), lq % block
+        per = (lambda n: n * (n + 1) / 2) if causal else (lambda n: n * n)
+        return float(np.sum(full * per(block) + per(rest)))
     if causal:
         return float(np.sum(lq * (lq + 1) / 2))
     return float(np.sum(lq * lk))
@@ -137,7 +147,7 @@ def useful_flops(w: Workload, lq, lk):
     Forward: QK^T and PV, 2*P*H*(Dqk+Dv).  Backward: S recompute, dV, dP, dQ and
     dK, 2*P*H*(3*Dqk+2*Dv).  P = valid pairs per head.
     """
-    p = valid_pairs(lq, lk, w.causal)
+    p = valid_pairs(lq, lk, w.causal, w.block)
     return 2.0 * p * w.heads * (w.dim_qk + w.dim_v), 2.0 * p * w.heads * (3 * w.dim_qk + 2 * w.dim_v)
 
 
