@@ -200,24 +200,25 @@ __device__ void build_list(const Problem& p, const ListSpec& L, const Arrays& A,
     __syncthreads();
   }
 
-  // 6. write the items: warp w takes list positions r = w, w + kWarps, ...; its lanes
-  //    write that sequence's items (tiles heaviest first, heads adjacent) as
-  //    consecutive 32-byte stores.
+  // 6. write the items: one thread per item (unit u = item / H, head h = item % H), so
+  //    that a warp's 32-byte stores are consecutive; the unit's sequence comes from a
+  //    binary search of the units' prefix first[].  Every thread has work even when a
+  //    few sequences hold most of the units.
   const int64_t n_items = (int64_t)carry * p.heads;
-  for (int r = warp; r < B; r += kWarps) {
-    const int b = A.order[r];
-    const int4 s = A.seq[b];
-    const int n = A.ntile[b];
-    const int cnt = n * p.heads;
-    WorkItem* out = list + (int64_t)A.first[r] * p.heads;
-    for (int e = lane; e < cnt; e += 32) {
-      const int k = e / p.heads, h = e - k * p.heads;
-      const int t = tile_at(L, p.causal, n, k);
-      WorkItem w;
-      w.b = b; w.h = h; w.tile = t; w.cost = cost_of(L, p.causal, s.z, s.w, t);
-      w.q0 = s.x; w.k0 = s.y; w.lq = s.z; w.lk = s.w;
-      out[e] = w;
+  for (int64_t e = tid; e < n_items; e += kThreads) {
+    const int u = (int)(e / p.heads), h = (int)(e - (int64_t)u * p.heads);
+    int lo = 0, hi = B - 1;  // the last r with first[r] <= u (sequences without units skipped)
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (A.first[mid] <= u) lo = mid; else hi = mid - 1;
     }
+    const int b = A.order[lo];
+    const int4 s = A.seq[b];
+    const int t = tile_at(L, p.causal, A.ntile[b], u - A.first[lo]);
+    WorkItem w;
+    w.b = b; w.h = h; w.tile = t; w.cost = cost_of(L, p.causal, s.z, s.w, t);
+    w.q0 = s.x; w.k0 = s.y; w.lq = s.z; w.lk = s.w;
+    list[e] = w;
   }
   if (tid == 0) *n_out = (int)n_items;
   __syncthreads();
