@@ -17,8 +17,9 @@
 // Each item also carries its sequence's first rows and lengths, so a kernel
 // needs one 32-byte load per item and no dependent offset lookups.
 //
-// The list is built by one CTA from the offsets in device memory, so a call
-// never synchronises with the host and can be captured in a CUDA graph.  The
+// The lists are built from the offsets in device memory by one CTA (two when both
+// lists are wanted and fit in shared memory, one list each), so a call never
+// synchronises with the host and can be captured in a CUDA graph.  The
 // same kernel validates the offsets and writes the status word.  Per-sequence
 // arrays live in shared memory for up to kCacheB sequences and in the
 // workspace beyond that.
@@ -264,14 +265,21 @@ schedule_kernel(Problem p, Workspace ws, ListSpec lq_spec, ListSpec lk_spec, int
     }
     return;
   }
-  if (build_q)
-    build_list(p, lq_spec, A, ws.list_q, &ws.hdr->n_q, sh);
-  else if (tid == 0)
-    ws.hdr->n_q = 0;
-  if (build_k)
-    build_list(p, lk_spec, A, ws.list_k, &ws.hdr->n_k, sh);
-  else if (tid == 0)
-    ws.hdr->n_k = 0;
+  // With two CTAs (both lists wanted, per-sequence arrays in each CTA's shared memory),
+  // CTA 0 builds the q-list and CTA 1 the k-list; both validated the same offsets.
+  const bool split = gridDim.x == 2;
+  if (!split || blockIdx.x == 0) {
+    if (build_q)
+      build_list(p, lq_spec, A, ws.list_q, &ws.hdr->n_q, sh);
+    else if (tid == 0)
+      ws.hdr->n_q = 0;
+  }
+  if (!split || blockIdx.x == 1) {
+    if (build_k)
+      build_list(p, lk_spec, A, ws.list_k, &ws.hdr->n_k, sh);
+    else if (tid == 0)
+      ws.hdr->n_k = 0;
+  }
   if (tid == 0) ws.hdr->status = JFA_OK;
 }
 
@@ -284,7 +292,9 @@ cudaError_t launch_schedule(const Problem& p, const Workspace& ws, const SchedCo
   const int smem = (int)sizeof(SchedShared);
   cudaError_t e = cudaFuncSetAttribute(schedule_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  schedule_kernel<<<1, kThreads, smem, s>>>(p, ws, lq, lk, c.build_q, c.build_k, c.self_attention);
+  // both lists from two CTAs at once when each CTA can keep its own per-sequence arrays
+  const int grid = (c.build_q && c.build_k && p.batch <= kCacheB) ? 2 : 1;
+  schedule_kernel<<<grid, kThreads, smem, s>>>(p, ws, lq, lk, c.build_q, c.build_k, c.self_attention);
   return cudaGetLastError();
 }
 
