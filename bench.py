@@ -338,6 +338,7 @@ def run_ours(args):
     st = jfa.jfa_status_check(ws)
     if st != 0:
         raise RuntimeError("device status after warm-up: %s" % jfa.status_string(st))
+    run, launch = capture_graph(jfa, step, ws) if not args.no_graph else (step, "eager")
 
     stream = torch.cuda.current_stream()
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
@@ -345,21 +346,27 @@ def run_ours(args):
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
-    jfa.jfa_profile_reset()
-    jfa.jfa_profile_enable(True)
     with ClockSampler(local) as clk:
         clk.mark_start()
         for i in range(args.steps):
             flush.fill_(float(i))  # evicts the inputs from L2 between timed steps
             starts[i].record(stream)
-            step()
+            run()
             ends[i].record(stream)
         torch.cuda.synchronize()
         clk.mark_end()
-    jfa.jfa_profile_enable(False)
     ms_total = max_over_ranks(sum(s.elapsed_time(e) for s, e in zip(starts, ends)), world, dev)
     if world > 1:
         torch.distributed.barrier()
+    # per-kernel times: the same steps launched one call at a time with event timing (the
+    # graph replays exactly these kernels)
+    jfa.jfa_profile_reset()
+    jfa.jfa_profile_enable(True)
+    for i in range(args.steps):
+        flush.fill_(float(i))
+        step()
+    torch.cuda.synchronize()
+    jfa.jfa_profile_enable(False)
     prof = {k: jfa.jfa_profile_read(k) for k in jfa.KERNEL_KINDS}
     launches = sum(n for n, _ in prof.values())
     ms_per_step = ms_total / args.steps
@@ -409,6 +416,7 @@ def run_ours(args):
                    "useful_gflop_bwd": round(bwd_f / 1e9, 3),
                    "l2": "flushed between timed steps (256 MiB write)",
                    "parallelism": "replicas" if world > 1 else "single",
+                   "launch": launch,
                    "max_seqs": args.max_seqs or None},
         "roofline": roof, "kernels": kernels, "gpu_launches": launches,
         "e2e": e2e, "cpu_baseline": cpu, "clocks": clk.summary(),
@@ -417,6 +425,30 @@ def run_ours(args):
         print(json.dumps(line), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()
+
+
+def capture_graph(jfa, step, ws):
+    """One step (the library's forward and backward calls, as a training loop issues them)
+    captured in a CUDA graph; returns (replay function, launch description).  Steps whose
+    capture fails run as separate calls."""
+    try:
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):  # warm the library's own streams and events off-capture
+            step()
+        torch.cuda.current_stream().wait_stream(side)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            step()
+        g.replay()
+        torch.cuda.synchronize()
+        st = jfa.jfa_status_check(ws)
+        if st != 0:
+            raise RuntimeError(jfa.status_string(st))
+        return g.replay, "one CUDA graph per step (the library's calls captured)"
+    except Exception as e:  # noqa: BLE001 - report and time the calls instead
+        return step, "separate calls (graph capture failed: %s)" % str(e).splitlines()[0][:100]
 
 
 def e2e_measure(jfa, w, batch, d, ws, p, args, dev, step_flops, world):
@@ -515,6 +547,8 @@ def main():
     ap.add_argument("--workload", default="d64", choices=sorted(workloads.WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-graph", action="store_true",
+                    help="time the step as separate API calls instead of one CUDA graph")
     ap.add_argument("--max-seqs", type=int, default=0,
                     help="profiling aid: only the first N sequences of the workload")
     args = ap.parse_args()

@@ -26,6 +26,29 @@ int num_sms() {
 
 static size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
+cudaError_t kernel_setup(const void* func, int threads, size_t smem, int* per_sm) {
+  struct Entry { int dev; const void* func; int threads; size_t smem; int per_sm; };
+  static std::mutex mu;
+  static std::vector<Entry> cache;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lock(mu);
+  for (const Entry& x : cache)
+    if (x.dev == dev && x.func == func && x.threads == threads && x.smem == smem) {
+      if (per_sm) *per_sm = x.per_sm;
+      return cudaSuccess;
+    }
+  e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  int n = 0;
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, func, threads, smem);
+  if (e != cudaSuccess) return e;
+  cache.push_back({dev, func, threads, smem, n});
+  if (per_sm) *per_sm = n;
+  return cudaSuccess;
+}
+
 size_t workspace_layout(int64_t batch, int64_t total_q, int64_t total_k, int heads, void* base,
                         Workspace* out) {
   char* b = (char*)base;

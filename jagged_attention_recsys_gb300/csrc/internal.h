@@ -117,4 +117,9 @@ cudaError_t launch_block_offsets(const int64_t* offs, int64_t batch, int64_t tot
 
 int num_sms();
 
+// Sets a kernel's dynamic shared-memory limit, and returns its resident CTAs per SM at
+// (threads, smem), once per kernel and device; later calls answer from a cache.  These
+// are not stream operations, so launches that follow stay capturable in a CUDA graph.
+cudaError_t kernel_setup(const void* func, int threads, size_t smem, int* per_sm = nullptr);
+
 }  // namespace jfa

@@ -290,7 +290,7 @@ cudaError_t launch_schedule(const Problem& p, const Workspace& ws, const SchedCo
   ListSpec lq{false, c.q_rows, c.q_keys_step};
   ListSpec lk{true, c.k_keys, c.k_rows_step};
   const int smem = (int)sizeof(SchedShared);
-  cudaError_t e = cudaFuncSetAttribute(schedule_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  cudaError_t e = kernel_setup((const void*)schedule_kernel, kThreads, smem);
   if (e != cudaSuccess) return e;
   // both lists from two CTAs at once when each CTA can keep its own per-sequence arrays
   const int grid = (c.build_q && c.build_k && p.batch <= kCacheB) ? 2 : 1;

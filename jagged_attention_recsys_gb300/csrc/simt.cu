@@ -395,10 +395,8 @@ int padded(int d) { return d <= 32 ? 32 : (d <= 64 ? 64 : 128); }
 
 template <typename Kern>
 cudaError_t launch_persistent(Kern kern, size_t smem, cudaStream_t s, void** args) {
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (e != cudaSuccess) return e;
   int per_sm = 0;
-  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, smem);
+  cudaError_t e = kernel_setup((const void*)kern, kThreads, smem, &per_sm);
   if (e != cudaSuccess) return e;
   if (per_sm < 1) per_sm = 1;
   dim3 grid(num_sms() * per_sm);

@@ -1180,7 +1180,7 @@ cudaError_t dkdv_t(const Maps& m, const Problem& p, const float2* rowstat, void*
                    const Workspace& ws, cudaStream_t s) {
   auto kern = tc_dkdv_kernel<DQK, DV, ACT, CAUSAL>;
   constexpr uint32_t smem = KvLayout<DQK, DV>::SMEM;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  cudaError_t e = kernel_setup((const void*)kern, KvGroups<ACT>::kThreads, smem);
   if (e != cudaSuccess) return e;
   kern<<<num_sms(), KvGroups<ACT>::kThreads, smem, s>>>(m.k, m.v, m.q, m.dout, p, rowstat,
                                          (__nv_bfloat16*)dk, (__nv_bfloat16*)dv, ws.hdr, ws.list_k);
@@ -1192,7 +1192,7 @@ cudaError_t dq_t(const Maps& m, const Problem& p, const float2* rowstat, void* d
                  const Workspace& ws, cudaStream_t s) {
   auto kern = tc_dq_kernel<DQK, DV, ACT, CAUSAL>;
   constexpr uint32_t smem = QLayout<DQK, DV>::SMEM;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  cudaError_t e = kernel_setup((const void*)kern, QGroups::kThreads, smem);
   if (e != cudaSuccess) return e;
   kern<<<num_sms(), QGroups::kThreads, smem, s>>>(m.q, m.dout, m.k, m.v, p, rowstat,
                                          (__nv_bfloat16*)dq, ws.hdr, ws.list_q);

@@ -469,7 +469,7 @@ cudaError_t launch_fwd_t(const Problem& p, const CUtensorMap& mq, const CUtensor
                          cudaStream_t s) {
   auto kern = tc_fwd_kernel<DQK, DV, ACT, CAUSAL>;
   constexpr uint32_t smem = FwdLayout<DQK, DV>::SMEM;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  cudaError_t e = kernel_setup((const void*)kern, kThreads, smem);
   if (e != cudaSuccess) return e;
   kern<<<num_sms(), kThreads, smem, s>>>(mq, mk, mv, p, (__nv_bfloat16*)o, lse, ws.hdr, ws.list_q);
   return cudaGetLastError();
