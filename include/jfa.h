@@ -74,9 +74,10 @@ typedef enum { JFA_F32 = 0, JFA_BF16 = 1 } jfa_dtype;
 
 typedef struct {
   int64_t batch;   /* B >= 0 */
-  int64_t total_q; /* T_q = offs_q[B] */
-  int64_t total_k; /* T_k = offs_k[B]; equal to total_q for self-attention */
-  int32_t heads;   /* H >= 1 */
+  int64_t total_q; /* T_q = offs_q[B] <= 2^31 - 1 */
+  int64_t total_k; /* T_k = offs_k[B] <= 2^31 - 1; equal to total_q for self-attention */
+  int32_t heads;   /* H >= 1; H * (max(T_q, T_k) / 32 + B + 1) <= 2^31 - 1 (work-list
+                      items), else JFA_ERR_UNSUPPORTED */
   int32_t dim_qk;  /* Dqk: bf16 supports 64 and 128; fp32 supports 1..128 */
   int32_t dim_v;   /* Dv:  bf16 supports 64 and 128; fp32 supports 1..128 */
   float scale;     /* score scale > 0, normally 1/sqrt(Dqk) */

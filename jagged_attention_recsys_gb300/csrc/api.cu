@@ -181,6 +181,9 @@ jfa_status check_params(const jfa_params* p, Kind kind) {
   if (p->causal != 0 && p->causal != 1) return JFA_ERR_INVALID_ARG;
   if (p->batch == 0 && (p->total_q != 0 || p->total_k != 0)) return JFA_ERR_INVALID_ARG;
   if (p->total_q > INT32_MAX || p->total_k > INT32_MAX) return JFA_ERR_UNSUPPORTED;
+  // the work lists' item counts (and item indices) are 32-bit
+  const int64_t rows = p->total_q > p->total_k ? p->total_q : p->total_k;
+  if ((int64_t)p->heads * (rows / kMinTile + p->batch + 1) > INT32_MAX) return JFA_ERR_UNSUPPORTED;
   if (kind == Kind::Self && p->total_k != p->total_q) return JFA_ERR_INVALID_ARG;
   if (kind == Kind::Cross && p->causal) return JFA_ERR_UNSUPPORTED;
   if (kind == Kind::Gdpa && p->causal && p->total_k != p->total_q) return JFA_ERR_INVALID_ARG;

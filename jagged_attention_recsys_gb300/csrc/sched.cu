@@ -35,11 +35,12 @@ constexpr int kThreads = 1024;
 constexpr int kWarps = kThreads / 32;
 constexpr int kBuckets = 128;
 constexpr int kCacheB = 6144;  // sequences whose arrays fit in shared memory (32 B each)
+static_assert(kWarps == 32, "the per-bucket prefix over warps takes one lane per warp");
 
 struct SchedShared {
   int warp_tot[32];
   int hist[kBuckets], start[kBuckets], run[kBuckets];
-  int wcount[kWarps][kBuckets];
+  int wcount[kWarps][kBuckets + 1];  // padded: a bucket's column spans all 32 banks
   int red;
   int4 seq[kCacheB];      // (q0, k0, lq, lk)
   int ntile[kCacheB];     // tiles of the list being built
@@ -134,7 +135,7 @@ __device__ void build_list(const Problem& p, const ListSpec& L, const Arrays& A,
   __syncthreads();
   if (lane == 0) atomicMax(&sh.red, (int)min(cmax, (long long)0x7fffffff));
   for (int c = tid; c < kBuckets; c += kThreads) { sh.hist[c] = 0; sh.run[c] = 0; }
-  for (int i = tid; i < kWarps * kBuckets; i += kThreads) (&sh.wcount[0][0])[i] = 0;
+  for (int i = tid; i < kWarps * (kBuckets + 1); i += kThreads) (&sh.wcount[0][0])[i] = 0;
   __syncthreads();
   const long long top = sh.red;
 
@@ -172,19 +173,25 @@ __device__ void build_list(const Problem& p, const ListSpec& L, const Arrays& A,
     const int rank = __popc(peers & ((1u << lane) - 1u));
     if (valid && rank == 0) sh.wcount[warp][c] = __popc(peers);
     __syncthreads();
-    for (int cc = tid; cc < kBuckets; cc += kThreads) {
-      int acc = sh.run[cc];
-      for (int w = 0; w < kWarps; ++w) {
-        const int x = sh.wcount[w][cc];
-        sh.wcount[w][cc] = acc;
-        acc += x;
+    // per bucket, exclusive prefix of the warps' counts: one warp per bucket, lane w
+    // holding warp w's count
+    for (int cc = warp; cc < kBuckets; cc += kWarps) {
+      const int x = sh.wcount[lane][cc];
+      const int before = sh.run[cc];
+      int inc = x;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, inc, o);
+        if (lane >= o) inc += y;
       }
-      sh.run[cc] = acc;
+      sh.wcount[lane][cc] = before + inc - x;
+      __syncwarp();
+      if (lane == 31) sh.run[cc] = before + inc;
     }
     __syncthreads();
     if (valid) A.order[sh.start[c] + sh.wcount[warp][c] + rank] = b;
     __syncthreads();
-    for (int i = tid; i < kWarps * kBuckets; i += kThreads) (&sh.wcount[0][0])[i] = 0;
+    for (int i = tid; i < kWarps * (kBuckets + 1); i += kThreads) (&sh.wcount[0][0])[i] = 0;
     __syncthreads();
   }
 
@@ -205,9 +212,10 @@ __device__ void build_list(const Problem& p, const ListSpec& L, const Arrays& A,
   //    that a warp's 32-byte stores are consecutive; the unit's sequence comes from a
   //    binary search of the units' prefix first[].  Every thread has work even when a
   //    few sequences hold most of the units.
-  const int64_t n_items = (int64_t)carry * p.heads;
-  for (int64_t e = tid; e < n_items; e += kThreads) {
-    const int u = (int)(e / p.heads), h = (int)(e - (int64_t)u * p.heads);
+  //    Item counts stay below 2^31 (checked on the host), so the indices are 32-bit.
+  const int n_items = carry * p.heads;
+  for (int64_t e64 = tid; e64 < n_items; e64 += kThreads) {
+    const int e = (int)e64, u = e / p.heads, h = e - u * p.heads;
     int lo = 0, hi = B - 1;  // the last r with first[r] <= u (sequences without units skipped)
     while (lo < hi) {
       const int mid = (lo + hi + 1) >> 1;
@@ -221,7 +229,7 @@ __device__ void build_list(const Problem& p, const ListSpec& L, const Arrays& A,
     w.q0 = s.x; w.k0 = s.y; w.lq = s.z; w.lk = s.w;
     list[e] = w;
   }
-  if (tid == 0) *n_out = (int)n_items;
+  if (tid == 0) *n_out = n_items;
   __syncthreads();
 }
 

@@ -75,6 +75,9 @@ def test_invalid_arguments_rejected_on_host(L):
     assert _call_fwd(L, P(batch=-1)) == jfa.JFA_ERR_INVALID_ARG
     assert _call_fwd(L, P(total_k=11)) == jfa.JFA_ERR_INVALID_ARG  # self-attention
     assert _call_fwd(L, P(dim_qk=200)) == jfa.JFA_ERR_UNSUPPORTED
+    # work-list items H * (10 // 32 + 2 + 1) = 3H must stay within the 32-bit item index
+    assert _call_fwd(L, P(heads=715827883)) == jfa.JFA_ERR_UNSUPPORTED  # 3H = 2^31 + 1
+    assert _call_fwd(L, P(heads=715827882)) == jfa.JFA_ERR_WORKSPACE  # 3H = 2^31 - 2
     assert _call_fwd(L, P(causal=2)) == jfa.JFA_ERR_INVALID_ARG
     assert _call_fwd(L, P(scale=float("nan"))) == jfa.JFA_ERR_INVALID_ARG
     assert _call_fwd(L, P(scale=0.0)) == jfa.JFA_ERR_INVALID_ARG
