@@ -17,28 +17,52 @@
 namespace jfa {
 namespace {
 
-// offs_q[b] = b*m for b <= B; rows b*m + i of q_rep = row i of q (32-bit words).
-__global__ void pooled_broadcast_kernel(const uint32_t* __restrict__ q, uint32_t* __restrict__ q_rep,
+// offs_q[b] = b*m for b <= B; rows b*m + i of q_rep = row i of q.  W is the copied word
+// (16 bytes when a sequence's block of rows is a multiple of 16 bytes, else 4).  Threads
+// along x own words of the shared block; CTAs along y take the sequences.
+template <typename W>
+__global__ void pooled_broadcast_kernel(const W* __restrict__ q, W* __restrict__ q_rep,
                                         int64_t* __restrict__ offs_q, int64_t batch, int32_t m,
-                                        int64_t row_words) {
-  const int64_t tid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-  for (int64_t b = tid; b <= batch; b += stride) offs_q[b] = b * m;
-  const int64_t per_seq = (int64_t)m * row_words;
-  const int64_t total = batch * per_seq;
-  for (int64_t e = tid; e < total; e += stride) q_rep[e] = q[e % per_seq];
+                                        int64_t per_seq_words) {
+  const int64_t x = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const int64_t nx = (int64_t)gridDim.x * blockDim.x;
+  if (blockIdx.y == 0)
+    for (int64_t b = x; b <= batch; b += nx) offs_q[b] = b * m;
+  for (int64_t w = x; w < per_seq_words; w += nx) {
+    const W v = q[w];
+    for (int64_t b = blockIdx.y; b < batch; b += gridDim.y) q_rep[b * per_seq_words + w] = v;
+  }
 }
 
-// dq[e] = sum over b of dq_rep[b*m*row + e], accumulated in fp32 in sequence order.
+// dq[e] = sum over b of dq_rep[b*per_seq + e], in fp32, in a fixed order: warp w of a CTA
+// sums the sequences b = w, w + kSumWarps, ... in increasing b for 32 consecutive elements,
+// then the warps' partial sums are added in warp order.  The order depends only on the
+// sizes, so the result is bitwise reproducible (no atomics).
+constexpr int kSumWarps = 16;
+
 template <typename T>
-__global__ void pooled_reduce_kernel(const T* __restrict__ dq_rep, T* __restrict__ dq, int64_t batch,
-                                     int64_t per_seq) {
-  const int64_t tid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-  for (int64_t e = tid; e < per_seq; e += stride) {
+__global__ void __launch_bounds__(kSumWarps * 32)
+pooled_reduce_kernel(const T* __restrict__ dq_rep, T* __restrict__ dq, int64_t batch,
+                     int64_t per_seq) {
+  __shared__ float part[kSumWarps][32];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  for (int64_t e0 = (int64_t)blockIdx.x * 32; e0 < per_seq; e0 += (int64_t)gridDim.x * 32) {
+    const int64_t e = e0 + lane;
     float acc = 0.f;
-    for (int64_t b = 0; b < batch; ++b) acc += static_cast<float>(dq_rep[b * per_seq + e]);
-    dq[e] = static_cast<T>(acc);
+    if (e < per_seq) {
+#pragma unroll 4
+      for (int64_t b = warp; b < batch; b += kSumWarps)
+        acc += static_cast<float>(dq_rep[b * per_seq + e]);
+    }
+    part[warp][lane] = acc;
+    __syncthreads();
+    if (warp == 0 && e < per_seq) {
+      float sum = 0.f;
+#pragma unroll
+      for (int w = 0; w < kSumWarps; ++w) sum += part[w][lane];
+      dq[e] = static_cast<T>(sum);
+    }
+    __syncthreads();
   }
 }
 
@@ -53,21 +77,39 @@ unsigned grid_for(int64_t n, int threads) {
 
 cudaError_t launch_pooled_broadcast(int64_t batch, int32_t m, int64_t row_bytes, const void* q,
                                     void* q_rep, int64_t* offs_q, cudaStream_t s) {
-  const int64_t row_words = row_bytes / 4;  // row_bytes is a multiple of 4 (checked by the caller)
-  const int64_t n = batch * m * row_words > batch + 1 ? batch * m * row_words : batch + 1;
-  pooled_broadcast_kernel<<<grid_for(n, 256), 256, 0, s>>>((const uint32_t*)q, (uint32_t*)q_rep, offs_q,
-                                                           batch, m, row_words);
+  // row_bytes is a multiple of 4 and q, q_rep are 16-byte aligned (checked by the caller)
+  const int64_t per_seq_bytes = (int64_t)m * row_bytes;
+  const bool wide = per_seq_bytes % 16 == 0;
+  const int64_t words = per_seq_bytes / (wide ? 16 : 4);
+  const int64_t xs = (words > batch + 1 ? words : batch + 1);
+  const unsigned gx = grid_for(xs, 256);
+  // enough CTAs along the sequences to fill the GPU about 8 CTAs deep
+  int64_t gy = ((int64_t)num_sms() * 8 + gx - 1) / gx;
+  if (gy > batch) gy = batch;
+  if (gy > 65535) gy = 65535;
+  if (gy < 1) gy = 1;
+  const dim3 grid(gx, (unsigned)gy);
+  if (wide)
+    pooled_broadcast_kernel<uint4><<<grid, 256, 0, s>>>((const uint4*)q, (uint4*)q_rep, offs_q, batch, m,
+                                                         words);
+  else
+    pooled_broadcast_kernel<uint32_t><<<grid, 256, 0, s>>>((const uint32_t*)q, (uint32_t*)q_rep, offs_q,
+                                                           batch, m, words);
   return cudaGetLastError();
 }
 
 cudaError_t launch_pooled_reduce(int dtype, int64_t batch, int64_t per_seq_elems, const void* dq_rep,
                                  void* dq, cudaStream_t s) {
-  const unsigned g = grid_for(per_seq_elems, 256);
+  int64_t blocks = (per_seq_elems + 31) / 32;
+  const int64_t cap = (int64_t)num_sms() * 4;  // 4 CTAs of 512 threads per SM
+  if (blocks > cap) blocks = cap;
+  if (blocks < 1) blocks = 1;
   if (dtype == JFA_BF16)
-    pooled_reduce_kernel<__nv_bfloat16><<<g, 256, 0, s>>>((const __nv_bfloat16*)dq_rep,
-                                                          (__nv_bfloat16*)dq, batch, per_seq_elems);
+    pooled_reduce_kernel<__nv_bfloat16><<<(unsigned)blocks, kSumWarps * 32, 0, s>>>(
+        (const __nv_bfloat16*)dq_rep, (__nv_bfloat16*)dq, batch, per_seq_elems);
   else
-    pooled_reduce_kernel<float><<<g, 256, 0, s>>>((const float*)dq_rep, (float*)dq, batch, per_seq_elems);
+    pooled_reduce_kernel<float><<<(unsigned)blocks, kSumWarps * 32, 0, s>>>(
+        (const float*)dq_rep, (float*)dq, batch, per_seq_elems);
   return cudaGetLastError();
 }
 

@@ -139,12 +139,18 @@ __device__ void build_list(const Problem& p, const ListSpec& L, const Arrays& A,
   __syncthreads();
   const long long top = sh.red;
 
-  // 2. cost buckets (relative to the heaviest sequence) and their histogram
-  for (int b = tid; b < B; b += kThreads) {
-    const long long c = A.bucket[b];
-    const int k = top > 0 ? (int)(c * (kBuckets - 1) / top) : 0;
-    A.bucket[b] = k;
-    atomicAdd(&sh.hist[k], 1);
+  // 2. cost buckets (relative to the heaviest sequence) and their histogram; one atomic
+  //    per bucket and warp (equal costs are common: fixed-size blocks all share one)
+  for (int base = 0; base < B; base += kThreads) {
+    const int b = base + tid;
+    int k = -1;
+    if (b < B) {
+      const long long c = A.bucket[b];
+      k = top > 0 ? (int)(c * (kBuckets - 1) / top) : 0;
+      A.bucket[b] = k;
+    }
+    const unsigned peers = __match_any_sync(0xffffffffu, k);
+    if (k >= 0 && lane == __ffs(peers) - 1) atomicAdd(&sh.hist[k], __popc(peers));
   }
   __syncthreads();
   // 3. bucket starts, heaviest bucket first (descending exclusive scan, 4 buckets per lane)

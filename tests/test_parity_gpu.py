@@ -201,6 +201,13 @@ def test_fp32_pooled():
     compare(W(32, 16, dtype=F32, cross=True), got, ref, fp32=True)
 
 
+def test_fp32_pooled_rows_not_a_multiple_of_16_bytes():
+    # 3 shared rows of one head, Dqk = 5: the broadcast copies 60 bytes per sequence in
+    # 4-byte words
+    got, ref = _pooled_run(3, [3, 0, 7, 70], 1, 5, 3, F32, seed=6)
+    compare(W(5, 3, dtype=F32, cross=True, heads=1), got, ref, fp32=True)
+
+
 def test_full_size_pooled_workload():
     """The pooled workload at full size (512 sequences, 32 shared rows, keys up to 4096):
     o, lse, dk, dv equal, bit for bit, the cross-attention path given the shared rows
@@ -223,6 +230,10 @@ def test_full_size_pooled_workload():
     for a, b, n in ((o, o2, "o"), (lse, lse2, "lse"), (dk, dk2, "dk"), (dv, dv2, "dv")):
         assert torch.equal(a, b), n
     assert torch.isfinite(dq.float()).all()
+    # the sum over sequences has a fixed order: a second call gives the same bits
+    dq_again, _, _ = jfa.jfa_pooled_bwd(q, k, v, o, lse, do, okd)
+    torch.cuda.synchronize()
+    assert torch.equal(dq, dq_again)
     ref_dq = dq2.double().view(B, m, *q.shape[1:]).sum(0)
     err = float(torch.linalg.vector_norm(dq.double() - ref_dq) / torch.linalg.vector_norm(ref_dq))
     assert err <= 4e-3, err  # bf16 rounding of the sum
