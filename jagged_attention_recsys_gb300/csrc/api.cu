@@ -125,7 +125,13 @@ struct Timed {
     if (prof().pending.size() > 65536) drain();
     a = take_event();
     b = take_event();
-    if (a) cudaEventRecord(a, s);
+    if (!a || !b) {  // no timing for this launch; keep whichever event was made
+      if (a) prof().pool.push_back(a);
+      if (b) prof().pool.push_back(b);
+      a = b = nullptr;
+      return;
+    }
+    cudaEventRecord(a, s);
   }
   ~Timed() {
     if (!a || !b) return;
