@@ -63,7 +63,7 @@ typedef struct CUstream_st* jfa_stream_t;
 typedef enum {
   JFA_OK = 0,
   JFA_ERR_INVALID_ARG = 1, /* null pointer, bad size, misaligned pointer */
-  JFA_ERR_UNSUPPORTED = 2, /* valid request this build does not implement */
+  JFA_ERR_UNSUPPORTED = 2, /* valid request the library does not implement */
   JFA_ERR_WORKSPACE = 3,   /* workspace missing, misaligned or too small */
   JFA_ERR_BAD_OFFSETS = 4, /* (device) offsets are not a jagged layout of the given totals */
   JFA_ERR_TIMEOUT = 5,     /* (device) a bounded wait inside a kernel gave up */
