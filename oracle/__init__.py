@@ -22,6 +22,13 @@ BlockAttention (``block_fwd`` / ``block_bwd``) is softmax self-attention in whic
 sees only the keys of its own fixed 64-row block of the sequence: the definition above
 applied to every block as a sequence of its own.
 
+Rotary position embedding (``rope``) and BlockAttention with it (``block_rope_fwd`` /
+``block_rope_bwd``): the BlockAttention bullet pairs the blocks with a fused rotary
+position embedding but gives none of its parameters, so the oracle takes the embedding's
+published definition (RoFormer, Su et al. 2021, section 3.4): coordinate pairs
+(x[2i], x[2i+1]) of a row at position p rotated by the angle p * base^(-2i/D), base
+10000, applied to q and k; position p counts rows from the start of the row's sequence.
+
 Every oracle function here has independent pins in ``tests/test_oracle_pins.py``
 (50-digit brute force, finite differences, padded dense attention through
 torch autograd, closed forms and invariants).
@@ -204,3 +211,49 @@ def block_bwd(q, k, v, dout, offs, scale=None, causal=False):
     """BlockAttention backward: (dq, dk, dv)."""
     bo = block_offsets(offs)
     return bwd(q, k, v, dout, bo, bo, scale=scale, causal=causal)
+
+
+ROPE_BASE = 10000.0  # RoFormer's base for the rotation frequencies
+
+
+def rope(x, offs, base=ROPE_BASE, inverse=False):
+    """Rotary position embedding of x [T, H, D] (D even), rows grouped into sequences by offs:
+    row t of sequence b sits at position p = t - offs[b], and its pair i, the coordinates
+    (2i, 2i+1), is rotated by the angle p * theta_i with theta_i = base^(-2i/D) (RoFormer,
+    Su et al. 2021, section 3.4).  inverse=True rotates by the opposite angle, which is the
+    transpose: it maps a gradient with respect to the rotated rows back to the rows."""
+    x = _f64(x)
+    offs = _i64(offs)
+    T, H, D = x.shape
+    if D % 2:
+        raise ValueError("rope needs an even head dimension, got %d" % D)
+    pos = np.zeros(T)
+    for b in range(offs.shape[0] - 1):
+        start, end = int(offs[b]), int(offs[b + 1])
+        pos[start:end] = np.arange(end - start)
+    theta = base ** (-2.0 * np.arange(D // 2) / D)
+    angle = pos[:, None] * theta[None, :]
+    c = np.cos(angle)[:, None, :]
+    s = np.sin(angle)[:, None, :]
+    if inverse:
+        s = -s
+    x0, x1 = x[..., 0::2], x[..., 1::2]
+    out = np.empty_like(x)
+    out[..., 0::2] = x0 * c - x1 * s
+    out[..., 1::2] = x0 * s + x1 * c
+    return out
+
+
+def block_rope_fwd(q, k, v, offs, scale=None, causal=False, base=ROPE_BASE):
+    """BlockAttention with the rotary position embedding applied to q and k first (Meta GEM
+    MFU write-up, details section, BlockAttention bullet: fixed blocks combined with a fused
+    rotary position embedding).  Returns (o, lse) like ``block_fwd``."""
+    return block_fwd(rope(q, offs, base), rope(k, offs, base), v, offs, scale=scale, causal=causal)
+
+
+def block_rope_bwd(q, k, v, dout, offs, scale=None, causal=False, base=ROPE_BASE):
+    """Backward of ``block_rope_fwd``: (dq, dk, dv).  The gradients with respect to the rotated
+    q and k are rotated back (the rotation's transpose)."""
+    dqr, dkr, dv = block_bwd(rope(q, offs, base), rope(k, offs, base), v, dout, offs, scale=scale,
+                             causal=causal)
+    return rope(dqr, offs, base, inverse=True), rope(dkr, offs, base, inverse=True), dv

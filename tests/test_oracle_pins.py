@@ -505,3 +505,145 @@ def test_block_matches_block_diagonal_mask(causal):
     np.testing.assert_allclose(dq, tq.grad.numpy(), rtol=0, atol=1e-12)
     np.testing.assert_allclose(dk, tk.grad.numpy(), rtol=0, atol=1e-12)
     np.testing.assert_allclose(dv, tv.grad.numpy(), rtol=0, atol=1e-12)
+
+
+# --------------------------------------------------------------------------------------
+# Rotary position embedding (RoFormer's definition) and BlockAttention with it
+# --------------------------------------------------------------------------------------
+def _rope_complex_d8(x, offs):
+    """The rotation in RoFormer's complex form for D = 8 and base 10000: pair i is the complex
+    number x[2i] + i x[2i+1], multiplied by e^(i p theta_i); with D = 8 the frequencies are
+    10000^(-2i/8) = 10^-i exactly."""
+    T, H, D = x.shape
+    assert D == 8
+    pos = np.concatenate([np.arange(offs[b + 1] - offs[b]) for b in range(len(offs) - 1)])
+    theta = np.array([1.0, 0.1, 0.01, 0.001])
+    z = x[..., 0::2] + 1j * x[..., 1::2]
+    z = z * np.exp(1j * pos[:, None, None] * theta[None, None, :])
+    out = np.empty_like(x)
+    out[..., 0::2], out[..., 1::2] = z.real, z.imag
+    return out
+
+
+def test_rope_complex_form():
+    rng = np.random.default_rng(50)
+    offs = _offs([5, 0, 130, 1])
+    x = rng.standard_normal((int(offs[-1]), 3, 8))
+    np.testing.assert_allclose(oracle.rope(x, offs), _rope_complex_d8(x, offs), rtol=0, atol=1e-13)
+
+
+def test_rope_pairs_adjacent_coordinates_counterclockwise():
+    # a unit vector on the second coordinate of pair 0, at position 3 of its sequence:
+    # rotated by 3 radians to (-sin 3, cos 3); no other coordinate moves
+    x = np.zeros((4, 1, 6))
+    x[3, 0, 1] = 1.0
+    y = oracle.rope(x, [0, 4])
+    expect = np.zeros(6)
+    expect[0], expect[1] = -math.sin(3.0), math.cos(3.0)
+    np.testing.assert_allclose(y[3, 0], expect, rtol=0, atol=1e-15)
+    assert not y[:3].any()
+
+
+def test_rope_positions_restart_per_sequence_and_preserve_norms():
+    rng = np.random.default_rng(51)
+    offs = _offs([3, 7, 2])
+    x = rng.standard_normal((12, 2, 16))
+    y = oracle.rope(x, offs)
+    for start in offs[:-1]:  # position 0 of every sequence: the identity
+        np.testing.assert_array_equal(y[start], x[start])
+    pair_norm = lambda a: np.hypot(a[..., 0::2], a[..., 1::2])
+    np.testing.assert_allclose(pair_norm(y), pair_norm(x), rtol=1e-14)
+
+
+def test_rope_inverse_is_the_transpose():
+    rng = np.random.default_rng(52)
+    offs = _offs([9, 40])
+    x, y = rng.standard_normal((2, 49, 2, 32))
+    lhs = np.sum(oracle.rope(x, offs) * y)
+    rhs = np.sum(x * oracle.rope(y, offs, inverse=True))
+    assert abs(lhs - rhs) <= 1e-12 * (abs(lhs) + 1)
+    np.testing.assert_allclose(oracle.rope(oracle.rope(x, offs), offs, inverse=True), x,
+                               rtol=0, atol=1e-13)
+
+
+def test_rope_scores_depend_on_relative_position_only():
+    # the same q and k vectors placed at (m, n) and at (m + s, n + s) give the same score
+    rng = np.random.default_rng(53)
+    D = 64
+    q, k = rng.standard_normal((2, D))
+    L = 300
+    for m, n, s in ((10, 4, 200), (0, 37, 150), (99, 99, 1)):
+        xq, xk = np.zeros((L, 1, D)), np.zeros((L, 1, D))
+        xq[m, 0], xk[n, 0] = q, k
+        xq2, xk2 = np.zeros((L, 1, D)), np.zeros((L, 1, D))
+        xq2[m + s, 0], xk2[n + s, 0] = q, k
+        a = oracle.rope(xq, [0, L])[m, 0] @ oracle.rope(xk, [0, L])[n, 0]
+        b = oracle.rope(xq2, [0, L])[m + s, 0] @ oracle.rope(xk2, [0, L])[n + s, 0]
+        assert abs(a - b) <= 1e-11 * (abs(a) + 1), (m, n, s, a, b)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_block_rope_matches_autograd(causal):
+    """BlockAttention with q and k rotated (complex form, in torch) through torch autograd on
+    the whole sequence with a block-diagonal mask: o, lse and the gradients of the
+    unrotated q, k, v."""
+    lens = [1, 64, 65, 200, 0, 130]
+    H, D = 2, 8
+    rng = np.random.default_rng(54)
+    T = sum(lens)
+    q, k, v, do = (rng.standard_normal((T, H, D)) for _ in range(4))
+    offs = _offs(lens)
+    scale = 1.0 / math.sqrt(D)
+    o, lse = oracle.block_rope_fwd(q, k, v, offs, scale=scale, causal=causal)
+    dq, dk, dv = oracle.block_rope_bwd(q, k, v, do, offs, scale=scale, causal=causal)
+
+    tq, tk, tv = (torch.tensor(x, requires_grad=True) for x in (q, k, v))
+    theta = torch.tensor([1.0, 0.1, 0.01, 0.001], dtype=torch.float64)
+
+    def rot(t, L):
+        z = torch.view_as_complex(t.reshape(L, H, D // 2, 2).contiguous())
+        ang = torch.arange(L, dtype=torch.float64)[:, None, None] * theta
+        return torch.view_as_real(z * torch.polar(torch.ones_like(ang), ang)).reshape(L, H, D)
+
+    outs, lses = [], []
+    for b, L in enumerate(lens):
+        if L == 0:
+            continue
+        sl = slice(offs[b], offs[b + 1])
+        i = torch.arange(L)
+        mask = (i[:, None] // 64) == (i[None, :] // 64)
+        if causal:
+            mask &= i[None, :] <= i[:, None]
+        s = torch.einsum("ihd,jhd->hij", rot(tq[sl], L), rot(tk[sl], L)) * scale
+        s = s.masked_fill(~mask, float("-inf"))
+        outs.append(torch.einsum("hij,jhd->ihd", torch.softmax(s, dim=-1), tv[sl]))
+        lses.append(torch.logsumexp(s, dim=-1).T)
+    out = torch.cat(outs)
+    (out * torch.tensor(do)).sum().backward()
+    np.testing.assert_allclose(o, out.detach().numpy(), rtol=0, atol=1e-12)
+    np.testing.assert_allclose(lse, torch.cat(lses).detach().numpy(), rtol=0, atol=1e-12)
+    np.testing.assert_allclose(dq, tq.grad.numpy(), rtol=0, atol=1e-12)
+    np.testing.assert_allclose(dk, tk.grad.numpy(), rtol=0, atol=1e-12)
+    np.testing.assert_allclose(dv, tv.grad.numpy(), rtol=0, atol=1e-12)
+
+
+def test_block_rope_same_with_positions_counted_per_block():
+    """Scores under the rotation depend only on the offset between query and key, and both
+    lie in one block: counting positions from the block's first row gives the same
+    outputs and gradients as counting from the sequence's first row."""
+    lens = [70, 3, 129]
+    H, D = 2, 16
+    rng = np.random.default_rng(55)
+    T = sum(lens)
+    q, k, v, do = (rng.standard_normal((T, H, D)) for _ in range(4))
+    offs = _offs(lens)
+    bo = oracle.block_offsets(offs)
+    o, lse = oracle.block_rope_fwd(q, k, v, offs, causal=True)
+    o2, lse2 = oracle.block_fwd(oracle.rope(q, bo), oracle.rope(k, bo), v, offs, causal=True)
+    np.testing.assert_allclose(o, o2, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(lse, lse2, rtol=0, atol=1e-12)
+    grads = oracle.block_rope_bwd(q, k, v, do, offs, causal=True)
+    dqr, dkr, dv2 = oracle.block_bwd(oracle.rope(q, bo), oracle.rope(k, bo), v, do, offs, causal=True)
+    grads2 = (oracle.rope(dqr, bo, inverse=True), oracle.rope(dkr, bo, inverse=True), dv2)
+    for a, b in zip(grads, grads2):
+        np.testing.assert_allclose(a, b, rtol=0, atol=1e-12)
