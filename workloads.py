@@ -142,10 +142,12 @@ def valid_pairs(lq, lk, causal: bool, block: int = 0) -> float:
 
 
 def useful_flops(w: Workload, lq, lk):
-    """(forward, backward) useful FLOPs: no padding, no masked area, no recompute.
+    """(forward, backward) useful FLOPs: no padding and no masked area.
 
-    Forward: QK^T and PV, 2*P*H*(Dqk+Dv).  Backward: S recompute, dV, dP, dQ and
-    dK, 2*P*H*(3*Dqk+2*Dv).  P = valid pairs per head.
+    Forward: QK^T and PV, 2*P*H*(Dqk+Dv).  Backward: one recompute of S, then dV, dP,
+    dQ and dK, 2*P*H*(3*Dqk+2*Dv) (2.5 times the forward when Dqk = Dv, the usual
+    count for flash attention).  The atomic-free backward computes S and dP once in
+    each of its two passes; the second time is not counted.  P = valid pairs per head.
     """
     p = valid_pairs(lq, lk, w.causal, w.block)
     return 2.0 * p * w.heads * (w.dim_qk + w.dim_v), 2.0 * p * w.heads * (3 * w.dim_qk + 2 * w.dim_v)
