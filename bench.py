@@ -90,23 +90,31 @@ def kernel_flops_bytes(w, lq, lk, tq, tk):
     fwd:  QK^T and PV over the valid pairs; reads Q, K, V, writes O and lse.
     dkdv: S^T and dP^T recompute, dV and dK products; reads Q, K, V, dO, lse, D, writes dK, dV.
     dq:   S and dP recompute, dQ product; reads Q, K, V, dO, lse, D, writes dQ.
+    d:    the row pass; reads O, dO and lse, writes the (lse, D) pairs.
+    aux:  pooled attention's broadcast (writes the T_q query rows) or sum (reads the T_q
+          per-sequence query-gradient rows); BlockAttention's block offsets.
     """
     P = workloads.valid_pairs(lq, lk, w.causal, w.block)
     H, dq, dv = w.heads, w.dim_qk, w.dim_v
     e = 2 if w.dtype == torch.bfloat16 else 4
     sm = w.act == workloads.ACT_SOFTMAX
     rowb = 8 * H * tq if sm else 0
+    if w.pooled:
+        aux = e * H * dq * tq
+    elif w.block:
+        n_blocks = int(sum(-(-int(n) // w.block) for n in lq))
+        aux = 8 * (len(lq) + 1) + 8 * (n_blocks + 1)
+    else:
+        aux = 0
     return {
         "fwd": (2 * P * H * (dq + dv), e * H * (tq * dq + tk * dq + tk * dv + tq * dv) + (4 * H * tq if sm else 0)),
         "bwd_dkdv": (2 * P * H * (2 * dq + 2 * dv),
                      e * H * (tq * dq + tk * dq + tk * dv + tq * dv + tk * dq + tk * dv) + rowb),
         "bwd_dq": (2 * P * H * (2 * dq + dv),
                    e * H * (tq * dq + tk * dq + tk * dv + tq * dv + tq * dq) + rowb),
-        "bwd_d": (2 * H * tq * dv, e * H * 2 * tq * dv + 4 * H * tq),
+        "bwd_d": (2 * H * tq * dv, e * H * 2 * tq * dv + 12 * H * tq),
         "schedule": (0, 8 * (len(lq) + 1) * 2),
-        # pooled attention: shared query rows broadcast (tq rows written), per-sequence query
-        # gradients summed (tq rows read)
-        "aux": (0, e * H * dq * 2 * tq),
+        "aux": (0, aux),
     }
 
 

@@ -62,3 +62,53 @@ def test_reference_arm_under_torchrun_two_ranks():
     lines = _json_lines(r.stdout)
     assert len(lines) == 1  # rank 0 alone
     _check_line(lines[0], 2)
+
+
+def test_roofline_counts_hand_worked():
+    """Per-launch algorithmic FLOPs and bytes behind the roofline object, on one causal
+    sequence of 3 rows (6 valid pairs), H=2, Dqk=4, Dv=2, bf16."""
+    import torch
+
+    import bench
+    import workloads
+
+    w = workloads.Workload("t", 1, 2, 4, 2, True, workloads.ACT_SOFTMAX, torch.bfloat16, False)
+    r = bench.kernel_flops_bytes(w, [3], [3], 3, 3)
+    P, H, dq, dv, T = 6, 2, 4, 2, 3
+    assert r["fwd"] == (2 * P * H * (dq + dv), 2 * H * T * (2 * dq + 2 * dv) + 4 * H * T)
+    # dK/dV: reads Q, K, V, dO and the (lse, D) pairs; writes dK, dV
+    assert r["bwd_dkdv"] == (2 * P * H * (2 * dq + 2 * dv),
+                             2 * H * T * (dq + dq + dv + dv + dq + dv) + 8 * H * T)
+    # dQ: reads Q, K, V, dO and the pairs; writes dQ
+    assert r["bwd_dq"] == (2 * P * H * (2 * dq + dv),
+                           2 * H * T * (dq + dq + dv + dv + dq) + 8 * H * T)
+    # row pass: reads O, dO, lse; writes the pairs
+    assert r["bwd_d"] == (2 * H * T * dv, 2 * H * T * 2 * dv + 12 * H * T)
+    assert r["aux"] == (0, 0)
+
+
+def test_roofline_counts_d64_workload():
+    """The default line's dominant kernel, dK/dV on the d64 workload."""
+    import bench
+    import workloads
+
+    w = workloads.WORKLOADS["d64"]
+    lq, lk = workloads.lengths("d64")
+    r = bench.kernel_flops_bytes(w, lq, lk, int(lq.sum()), int(lk.sum()))
+    assert r["bwd_dkdv"] == (49681547264.0, 212475008)
+
+
+def test_roofline_counts_auxiliary_kernels():
+    import torch
+
+    import bench
+    import workloads
+
+    w = workloads.WORKLOADS["pooled"]
+    lq, lk = workloads.lengths("pooled")
+    tq = int(lq.sum())
+    assert bench.kernel_flops_bytes(w, lq, lk, tq, int(lk.sum()))["aux"] == (0, 2 * 4 * 128 * tq)
+    w = workloads.Workload("b", 2, 1, 64, 64, True, workloads.ACT_SOFTMAX, torch.bfloat16, False,
+                           block=64)
+    # lengths 65 and 64: 2 + 1 blocks; reads 3 offsets, writes 4
+    assert bench.kernel_flops_bytes(w, [65, 64], [65, 64], 129, 129)["aux"] == (0, 8 * 3 + 8 * 4)
