@@ -33,7 +33,7 @@ void* scratch_on_current_device() {
   if (g_scratch_ptr[dev] == nullptr) {
     void* ptr = nullptr;
     if (cudaGetSymbolAddress(&ptr, g_scratch) != cudaSuccess || ptr == nullptr) {
-      cudaGetLastError();  // clear the sticky-free error so later calls are unaffected
+      cudaGetLastError();  // clear this (non-sticky) error so later calls do not see it
       return nullptr;
     }
     g_scratch_ptr[dev] = ptr;

@@ -6,16 +6,18 @@
 
 namespace jfa {
 namespace {
+// The driver's tensor-map encoder, looked up once (a function-local static is initialised
+// exactly once even when several host threads launch at the same time).
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  if (fn == nullptr) {
+  static const PFN_cuTensorMapEncodeTiled_v12000 fn = []() -> PFN_cuTensorMapEncodeTiled_v12000 {
     void* ptr = nullptr;
     cudaDriverEntryPointQueryResult q;
     if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
                                          &q) == cudaSuccess &&
         q == cudaDriverEntryPointSuccess)
-      fn = (PFN_cuTensorMapEncodeTiled_v12000)ptr;
-  }
+      return (PFN_cuTensorMapEncodeTiled_v12000)ptr;
+    return nullptr;
+  }();
   return fn;
 }
 }  // namespace
