@@ -76,3 +76,28 @@ def test_useful_flops_hand_worked():
     w = workloads.Workload("t", 1, 1, 8, 8, False, workloads.ACT_SOFTMAX, torch.float32, False)
     fwd, bwd = workloads.useful_flops(w, [5], [5])
     assert bwd == 2.5 * fwd
+
+
+def test_executed_pairs_hand_worked():
+    ep = workloads.executed_pairs
+    assert ep([100], [100], False) == 128 * 128
+    assert ep([129], [300], False) == 2 * 3 * 128 * 128
+    # causal, 300 rows: q-tiles 0, 1, 2 cover 1, 2, 3 key tiles
+    assert ep([300], [300], True) == 6 * 128 * 128
+    assert ep([0, 5], [0, 5], True) == 128 * 128
+    # blocks of 64 over 130 rows: blocks of 64, 64, 2, one tile each
+    assert ep([130], [130], True, block=64) == 3 * 128 * 128
+
+
+def test_tile_occupancy_of_the_workloads():
+    """The share of executed 128 x 128 MMA area that holds valid pairs, seed-0 draws."""
+    occ = {}
+    for name in ("d64", "causal", "cross", "gdpa", "pooled", "block"):
+        w = workloads.WORKLOADS[name]
+        lq, lk = workloads.lengths(name)
+        occ[name] = workloads.valid_pairs(lq, lk, w.causal, w.block) / workloads.executed_pairs(
+            lq, lk, w.causal, w.block)
+    expect = {"d64": 0.723, "causal": 0.656, "cross": 0.265, "gdpa": 0.918, "pooled": 0.243,
+              "block": 0.112}
+    for name, v in expect.items():
+        assert abs(occ[name] - v) < 5e-4, (name, occ[name])
