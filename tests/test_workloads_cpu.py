@@ -101,3 +101,12 @@ def test_tile_occupancy_of_the_workloads():
               "block": 0.112}
     for name, v in expect.items():
         assert abs(occ[name] - v) < 5e-4, (name, occ[name])
+
+
+def test_executed_pairs_trimmed_queries_hand_worked():
+    ep = workloads.executed_pairs
+    # dK/dV: a step's products cover its valid queries rounded up to 16
+    assert ep([100], [100], False, trim_queries=True) == 128 * 112
+    assert ep([130], [300], False, trim_queries=True) == 3 * 128 * (128 + 16)
+    # causal, 300 queries: query tiles of 128, 128, 44 -> 48 rows; 1 + 2 + 3 key tiles
+    assert ep([300], [300], True, trim_queries=True) == 128 * (1 * 128 + 2 * 128 + 3 * 48)

@@ -141,25 +141,31 @@ def valid_pairs(lq, lk, causal: bool, block: int = 0) -> float:
     return float(np.sum(lq * lk))
 
 
-def executed_pairs(lq, lk, causal: bool, block: int = 0, tile: int = 128) -> float:
-    """(query, key) pairs the tensor-core kernels cover with whole tile x tile MMA tiles, per
-    head: every tile of a sequence's query x key grid that holds at least one valid pair
-    (for causal attention, the tiles on and below the diagonal).  With ``block``, each
-    block is a sequence of its own.  valid_pairs / executed_pairs is the share of the
-    executed MMA area that does useful work."""
+def executed_pairs(lq, lk, causal: bool, block: int = 0, tile: int = 128,
+                   trim_queries: bool = False) -> float:
+    """(query, key) pairs the tensor-core kernels cover with their MMA tiles, per head:
+    every tile x tile tile of a sequence's query x key grid that holds at least one valid
+    pair (for causal attention, the tiles on and below the diagonal).  With
+    ``trim_queries`` (the dK/dV pass, whose products run over a step's valid queries
+    only), a tile's query side counts the valid queries rounded up to 16.  With
+    ``block``, each block is a sequence of its own.  valid_pairs / executed_pairs is the
+    share of the executed MMA area that does useful work."""
     lq = [int(x) for x in np.asarray(lq).ravel()]
     lk = [int(x) for x in np.asarray(lk).ravel()]
     if block:
         cut = lambda n: [block] * (n // block) + ([n % block] if n % block else [])
         lq = [x for n in lq for x in cut(n)]
         lk = list(lq)
+
+    def rows(a, t):  # query rows a tile at query-tile index t covers
+        return ((min(tile, a - t * tile) + 15) // 16 * 16) if trim_queries else tile
+
     total = 0
     for a, b in zip(lq, lk):
         nq, nk = -(-a // tile), -(-b // tile)
-        if causal:
-            total += sum(min(nk, t + 1) for t in range(nq)) * tile * tile
-        else:
-            total += nq * nk * tile * tile
+        for t in range(nq):
+            keys = min(nk, t + 1) if causal else nk
+            total += keys * tile * rows(a, t)
     return float(total)
 
 
