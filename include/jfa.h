@@ -37,13 +37,16 @@
  * allocates device memory on these paths and keeps no per-call state; its
  * only scratch is the caller's workspace (size from jfa_workspace_size).
  * One workspace must not be used by two calls that may run concurrently.
+ * The one exception is jfa_fwd_noalloc below, whose scratch is a fixed array
+ * inside the library shared by all of its calls.
  *
  * Asynchrony and errors.  Every compute call only enqueues work on `stream`
  * (NULL = the legacy default stream) and returns.  Argument errors are
  * detected on the host before anything is launched, and returned.  Errors
- * found on the device (offsets that are not a valid jagged layout) are
- * written to a status word inside the workspace; the affected call then
- * computes nothing and leaves its outputs untouched.  jfa_status_check()
+ * found on the device are written to a status word inside the workspace:
+ * offsets that are not a valid jagged layout (the call then computes nothing
+ * and leaves its outputs untouched), or a bounded wait inside a kernel that
+ * gave up (the outputs are then incomplete).  jfa_status_check()
  * synchronises the stream and returns that word.  The library never aborts,
  * traps or prints.
  */
@@ -159,12 +162,18 @@ jfa_status jfa_gdpa_bwd(const jfa_params* p, const void* q, const void* k, const
  * The call itself never allocates: no cudaMalloc, no cudaFree, no allocating
  * library routine.  The first call on a device looks up the array's device
  * address (cudaGetSymbolAddress, with that device current) and caches it;
- * make that first call before any stream capture.  All calls share the one
+ * make that first call before any stream capture.  The cache is keyed on the
+ * CUDA context, not the device number: after cudaDeviceReset, or under another
+ * context on the same device, the first call looks the address up again (and
+ * that call, too, should come before any capture).  All calls share the one
  * array, which keeps the last call's contents, so calls that may overlap on
  * the GPU (different streams, or different host threads) race and must be
- * serialised by the caller.  Offsets found invalid on the device make the
- * call compute nothing, as in jfa_fwd; this variant has no status word the
- * caller can read.
+ * serialised by the caller.  Errors found on the device are silent here:
+ * offsets that are not a valid jagged layout make the call compute nothing,
+ * as in jfa_fwd, and a bounded wait inside a kernel that gives up leaves the
+ * outputs incomplete; the status word that jfa_fwd's caller reads with
+ * jfa_status_check lives in the shared array, which this variant's caller
+ * cannot name.
  */
 jfa_status jfa_fwd_noalloc(const jfa_params* p, const void* q, const void* k, const void* v,
                            const int64_t* offs, void* o, float* lse, jfa_stream_t stream);
@@ -249,6 +258,21 @@ enum {
 jfa_status jfa_profile_enable(int on);
 jfa_status jfa_profile_reset(void);
 jfa_status jfa_profile_read(int kind, int64_t* launches, double* total_ms);
+
+/*
+ * Test hook for the bounded waits inside the tensor-core kernels.  Every wait on
+ * an mbarrier in those kernels gives up after about two seconds, records
+ * JFA_ERR_TIMEOUT in the workspace's status word, lets the CTA's other roles
+ * leave, waits for the CTA's own copies and MMAs in flight and frees its
+ * tensor memory, so the context stays usable.  While `on` is nonzero, every
+ * bf16 forward launch in the calling thread's current context (jfa_fwd,
+ * jfa_cross_fwd, jfa_gdpa_fwd and the calls built on them) starts with its MMA
+ * issuer waiting on a barrier that nothing arrives on, before any MMA is
+ * issued; the call then reports JFA_ERR_TIMEOUT through jfa_status_check and
+ * leaves its outputs incomplete.  Off by default; turn it off again before
+ * normal use.  Synchronises the device.
+ */
+jfa_status jfa_test_hold(int on);
 
 /*
  * Which kernel family serves a request with these params: 1 = tcgen05/TMA

@@ -38,7 +38,8 @@ EXPORTS = ("jfa_workspace_size", "jfa_fwd", "jfa_bwd", "jfa_cross_fwd", "jfa_cro
            "jfa_gdpa_fwd", "jfa_gdpa_bwd", "jfa_status_check", "jfa_status_string",
            "jfa_profile_enable", "jfa_profile_reset", "jfa_profile_read", "jfa_path_for",
            "jfa_fwd_noalloc", "jfa_bbs_plan", "jfa_pooled_workspace_size", "jfa_pooled_fwd",
-           "jfa_pooled_bwd", "jfa_block_workspace_size", "jfa_block_fwd", "jfa_block_bwd")
+           "jfa_pooled_bwd", "jfa_block_workspace_size", "jfa_block_fwd", "jfa_block_bwd",
+           "jfa_test_hold")
 
 
 class JfaError(RuntimeError):
@@ -88,6 +89,8 @@ def lib():
         L.jfa_status_check.restype = ctypes.c_int
         L.jfa_status_string.argtypes = [ctypes.c_int]
         L.jfa_status_string.restype = ctypes.c_char_p
+        L.jfa_test_hold.argtypes = [ctypes.c_int]
+        L.jfa_test_hold.restype = ctypes.c_int
         L.jfa_profile_enable.argtypes = [ctypes.c_int]
         L.jfa_profile_enable.restype = ctypes.c_int
         L.jfa_profile_reset.argtypes = []
@@ -294,6 +297,11 @@ def jfa_gdpa_bwd(q, k, v, dout, offs_q, offs_k=None, *, scale=None, causal=False
 def jfa_status_check(ws, stream=None) -> int:
     """Synchronises the stream and returns the device status word of the last call on ``ws``."""
     return int(lib().jfa_status_check(_ptr(ws), _stream(stream)))
+
+
+def jfa_test_hold(on: bool):
+    """Test hook of the kernels' bounded waits (see jfa_test_hold in include/jfa.h)."""
+    _check(lib().jfa_test_hold(int(bool(on))), "jfa_test_hold")
 
 
 def jfa_profile_enable(on: bool = True):

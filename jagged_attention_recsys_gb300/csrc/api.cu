@@ -1,5 +1,6 @@
 // C ABI of libjfa: argument validation, workspace carve-up, kernel dispatch,
 // status reporting and optional per-kernel event timing.  See include/jfa.h.
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -27,25 +28,54 @@ int num_sms() {
 
 static size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
+// The driver's context queries, looked up once.
+namespace {
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long*);
+template <class F>
+F driver_fn(const char* name) {
+  void* ptr = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion(name, &ptr, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+      q == cudaDriverEntryPointSuccess)
+    return (F)ptr;
+  return nullptr;
+}
+}  // namespace
+
+unsigned long long current_context_id() {
+  static const CtxGetCurrentFn get_current = driver_fn<CtxGetCurrentFn>("cuCtxGetCurrent");
+  static const CtxGetIdFn get_id = driver_fn<CtxGetIdFn>("cuCtxGetId");
+  if (!get_current || !get_id) return 0;
+  CUcontext ctx = nullptr;
+  if (get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr) return 0;
+  unsigned long long id = 0;
+  if (get_id(ctx, &id) != CUDA_SUCCESS) return 0;
+  return id + 1;  // never 0 for a real context
+}
+
 cudaError_t kernel_setup(const void* func, int threads, size_t smem, int* per_sm) {
-  struct Entry { int dev; const void* func; int threads; size_t smem; int per_sm; };
+  // Kernel attributes belong to the context's copy of the module: the cache is keyed on
+  // the context, so a reset device (a new primary context) or another context on the
+  // same device sets them up again.
+  struct Entry { unsigned long long ctx; const void* func; int threads; size_t smem; int per_sm; };
   static std::mutex mu;
   static std::vector<Entry> cache;
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
+  const unsigned long long ctx = current_context_id();
   std::lock_guard<std::mutex> lock(mu);
-  for (const Entry& x : cache)
-    if (x.dev == dev && x.func == func && x.threads == threads && x.smem == smem) {
-      if (per_sm) *per_sm = x.per_sm;
-      return cudaSuccess;
-    }
-  e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (ctx != 0)
+    for (const Entry& x : cache)
+      if (x.ctx == ctx && x.func == func && x.threads == threads && x.smem == smem) {
+        if (per_sm) *per_sm = x.per_sm;
+        return cudaSuccess;
+      }
+  cudaError_t e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   int n = 0;
   e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, func, threads, smem);
   if (e != cudaSuccess) return e;
-  cache.push_back({dev, func, threads, smem, n});
+  const unsigned long long now = current_context_id();  // set once the runtime made one current
+  if (now != 0) cache.push_back({now, func, threads, smem, n});
   if (per_sm) *per_sm = n;
   return cudaSuccess;
 }
@@ -148,6 +178,7 @@ inline jfa_status cu(cudaError_t e) { return e == cudaSuccess ? JFA_OK : JFA_ERR
 // run beside the scheduler).  Created on first use and kept for the thread's life;
 // nullptr when it cannot be created (the work then runs on the caller's stream).
 struct SideStream {
+  unsigned long long ctx = 0;  // the context the stream and events belong to
   cudaStream_t s = nullptr;
   cudaEvent_t fork = nullptr, join = nullptr;
 };
@@ -157,8 +188,10 @@ SideStream* side_stream() {
   thread_local SideStream sides[kMaxDevices];
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  const unsigned long long ctx = current_context_id();
+  if (ctx == 0) return nullptr;
   SideStream& sd = sides[dev];
-  if (!sd.s) {
+  if (!sd.s || sd.ctx != ctx) {  // first use, or a new context (the old handles died with it)
     cudaStream_t st = nullptr;
     cudaEvent_t a = nullptr, b = nullptr;
     if (cudaStreamCreateWithFlags(&st, cudaStreamNonBlocking) != cudaSuccess) return nullptr;
@@ -168,6 +201,7 @@ SideStream* side_stream() {
       cudaStreamDestroy(st);
       return nullptr;
     }
+    sd.ctx = ctx;
     sd.s = st;
     sd.fork = a;
     sd.join = b;
@@ -567,6 +601,8 @@ const char* jfa_status_string(jfa_status s) {
   }
   return "unknown status";
 }
+
+jfa_status jfa_test_hold(int on) { return cu(tc_set_test_hold(on)); }
 
 jfa_status jfa_profile_enable(int on) {
   prof().on = on != 0;

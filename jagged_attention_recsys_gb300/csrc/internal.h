@@ -117,8 +117,16 @@ cudaError_t launch_block_offsets(const int64_t* offs, int64_t batch, int64_t tot
 
 int num_sms();
 
+// Identity of the CUDA context current on the calling host thread, or 0 when none is
+// current (or the driver cannot say).  Per-context state the library caches (kernel
+// attributes, the no-allocation scratch address, the side stream) is keyed on it, so
+// that state set up under one context is never used under another: after
+// cudaDeviceReset the primary context is a new one, and a driver-API context on the
+// same device loads its own copy of the module.
+unsigned long long current_context_id();
+
 // Sets a kernel's dynamic shared-memory limit, and returns its resident CTAs per SM at
-// (threads, smem), once per kernel and device; later calls answer from a cache.  These
+// (threads, smem), once per kernel and context; later calls answer from a cache.  These
 // are not stream operations, so launches that follow stay capturable in a CUDA graph.
 cudaError_t kernel_setup(const void* func, int threads, size_t smem, int* per_sm = nullptr);
 

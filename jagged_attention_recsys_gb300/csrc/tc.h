@@ -6,6 +6,8 @@
 namespace jfa {
 
 bool tc_supports(int dim_qk, int dim_v);
+// Test hook of the forward kernel's bounded waits (jfa_test_hold); synchronous.
+cudaError_t tc_set_test_hold(int on);
 SchedConfig tc_fwd_sched(const Problem& p);
 SchedConfig tc_bwd_sched(const Problem& p);
 cudaError_t launch_tc_fwd(const Problem& p, const void* q, const void* k, const void* v, void* o,

@@ -80,10 +80,15 @@ struct FwdLayout {
 enum : uint32_t {
   B_QFULL = 0, B_QEMPTY = 2, B_KFULL = 4, B_KEMPTY = 10, B_VFULL = 16, B_VEMPTY = 22,
   B_SFULL = 28, B_PFULL = 30, B_PEMPTY = 32, B_OFULL = 34, B_OEMPTY = 35, B_RED = 36, B_REDL = 38,
-  B_DRAIN = 40, B_COUNT = 42
+  B_DRAIN = 40, B_HOLD = 42, B_COUNT = 43
 };
 static_assert(8 * B_COUNT + 8 <= FwdLayout<128, 128>::RED_OFF, "mbarriers, TMEM slot and abort flag in front");
 constexpr uint32_t T_S = 0, T_O = 256, T_P = 384;  // S: 2 x 128 columns; P: 2 x 64 columns
+
+// Test hook (jfa_test_hold): while nonzero, the S issuer of every CTA first waits on
+// B_HOLD, on which no role ever arrives, so that its bounded wait gives up before any
+// MMA is issued and the CTA leaves through its abort path.  Zero unless a test sets it.
+__device__ int g_test_hold = 0;
 
 template <int DQK, int DV, int ACT, bool CAUSAL>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -132,6 +137,7 @@ tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     mbar_init(bar(B_OEMPTY), 256);
     mbar_init(bar(B_DRAIN), 1);      // S issuer's exit drain
     mbar_init(bar(B_DRAIN + 1), 1);  // PV issuer's exit drain
+    mbar_init(bar(B_HOLD), 1);       // test hook: nothing arrives on it
     *abort = 0;
     fence_mbar_init();
   }
@@ -209,6 +215,7 @@ tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
       constexpr uint32_t idesc_s = idesc_bf16(BM, BN, 0, 0);
       uint32_t k_it = 0, q_it = 0, gs = 0;
       bool ok = true;
+      if (*(volatile int*)&g_test_hold) ok = mbar_wait(bar(B_HOLD), 0, abort, status);
       WorkItem nxt = blockIdx.x < (unsigned)n_items ? load_item(list, blockIdx.x) : WorkItem{};
       for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
         const WorkItem w = nxt;
@@ -487,6 +494,11 @@ cudaError_t launch_fwd_d(const Problem& p, const CUtensorMap& mq, const CUtensor
 }
 
 }  // namespace
+
+cudaError_t tc_set_test_hold(int on) {
+  const int v = on != 0;
+  return cudaMemcpyToSymbol(g_test_hold, &v, sizeof(int));
+}
 
 bool tc_supports(int dim_qk, int dim_v) {
   return (dim_qk == 64 || dim_qk == 128) && (dim_v == 64 || dim_v == 128);

@@ -112,3 +112,28 @@ def test_roofline_counts_auxiliary_kernels():
                            block=64)
     # lengths 65 and 64: 2 + 1 blocks; reads 3 offsets, writes 4
     assert bench.kernel_flops_bytes(w, [65, 64], [65, 64], 129, 129)["aux"] == (0, 8 * 3 + 8 * 4)
+
+
+def test_reference_arm_config_is_the_gpu_arms():
+    """Both arms describe the workload with the same config dict (config_of)."""
+    sys.path.insert(0, ROOT)
+    import bench
+    import workloads
+
+    r = subprocess.run([sys.executable] + ARGS, cwd=ROOT, capture_output=True, text=True,
+                       timeout=300)
+    assert r.returncode == 0, r.stderr[-2000:]
+    line = _json_lines(r.stdout)[0]
+    lq, lk = workloads.lengths("tiny")
+    assert line["config"] == json.loads(json.dumps(bench.config_of(
+        workloads.WORKLOADS["tiny"], lq, lk, 1)))
+    assert line["config"]["activation"] == "softmax" and line["config"]["total_q"] == 105
+
+
+def test_default_workload_is_gdpa():
+    sys.path.insert(0, ROOT)
+    import argparse
+    import bench
+
+    src = open(os.path.join(ROOT, "bench.py")).read()
+    assert 'ap.add_argument("--workload", default="gdpa"' in src

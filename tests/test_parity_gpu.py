@@ -1,8 +1,12 @@
 """GPU parity: libjfa (through its C ABI) against the fp64 CPU oracle, element by element.
 
-Small cases span several tiles and ragged tails and run the whole batch through
-the oracle; the full-size workloads run the whole batch on the GPU in the
-launch configuration the benchmark times and check sampled whole sequences.
+Small cases span several tiles and ragged tails and run the whole batch through the
+oracle.  Mid-size batches give every persistent CTA several work items, so that the
+kernels' hand-offs between items (deferred epilogues, tiles loaded for the next item,
+products issued across item boundaries) are compared with the oracle too.  The
+full-size workloads run on the GPU in the launch configuration the benchmark times and
+are compared with the oracle over every sequence (the SiLU/L workload, whose oracle
+cost is about 12 fp64 TFLOP, over a labelled stratified subset of 32 sequences).
 """
 import numpy as np
 import pytest
@@ -11,7 +15,8 @@ import torch
 import workloads
 from workloads import ACT_SILU_OVER_LEN as GD, ACT_SOFTMAX as SM, Workload
 
-from parity_util import compare, full_check, run_gpu, sample_indices, sampled_check, to64
+from parity_util import (compare, full_check, run_gpu, sample_indices, sampled_check,
+                         stratified_subset, to64, whole_batch_check)
 
 pytestmark = pytest.mark.gpu
 
@@ -154,17 +159,62 @@ def test_deterministic_bitwise():
         assert torch.equal(a[n], b[n]), n
 
 
+# ----------------------------------------------------------------------------- mid size
+# 600 sequences of lengths U[1, 300] at H = 2 give about 2,000 q-tile and k-tile items,
+# 13 per CTA of the 152 persistent CTAs; cross-attention with query lengths U[1, 64] and
+# key lengths U[1, 600] gives 1,200 q-tile items (8 per CTA) and about 3,400 k-tile items.
+def _mid_lengths(seed, n=600, hi=300):
+    rng = np.random.default_rng(seed)
+    return rng.integers(1, hi, n, endpoint=True).astype(np.int64)
+
+
+@pytest.mark.parametrize("dims", [(64, 64), (128, 128)])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("act", [SM, GD])
+def test_mid_size_many_items_per_cta(dims, causal, act):
+    w = W(*dims, causal=causal, act=act)
+    lq = _mid_lengths(10 + dims[0] + 2 * causal + act)
+    batch = workloads.make_batch(w, lq, seed=11, device="cuda")
+    got = run_gpu(w, batch, check_status=True)
+    whole_batch_check(w, batch, got, strict_o=False)
+
+
+@pytest.mark.parametrize("act", [SM, GD])
+def test_mid_size_cross_many_items_per_cta(act):
+    w = W(128, 64, act=act, cross=True)
+    rng = np.random.default_rng(20 + act)
+    lq = rng.integers(1, 64, 600, endpoint=True).astype(np.int64)
+    lk = rng.integers(1, 600, 600, endpoint=True).astype(np.int64)
+    batch = workloads.make_batch(w, lq, lk, seed=12, device="cuda")
+    got = run_gpu(w, batch, check_status=True)
+    whole_batch_check(w, batch, got, strict_o=False)
+
+
 # ----------------------------------------------------------------------------- full size
-@pytest.mark.parametrize("name", ["d64", "causal", "cross", "gdpa"])
-def test_full_size_workload_sampled(name):
+@pytest.mark.parametrize("name", ["d64", "causal", "cross"])
+def test_full_size_workload_whole_batch(name):
+    """Every sequence of the named workload, as the benchmark runs it, against the oracle;
+    the error metrics are taken over the whole batch."""
     w = workloads.WORKLOADS[name]
     batch = workloads.make_batch(w, device="cuda")
-    got = run_gpu(w, batch)
+    got = run_gpu(w, batch, check_status=True)
+    fig = whole_batch_check(w, batch, got)
+    print("\n%s whole batch: %s" % (name, fig))
+
+
+def test_full_size_gdpa_stratified_subset():
+    """The SiLU/L workload at full size on the GPU; against the oracle on its labelled
+    stratified subset: the 8 longest and 8 shortest sequences and 16 drawn with seed 0."""
+    w = workloads.WORKLOADS["gdpa"]
+    batch = workloads.make_batch(w, device="cuda")
+    got = run_gpu(w, batch, check_status=True)
     for t in got.values():
         if t is not None:
             assert torch.isfinite(t).all()
-    idx = sample_indices(batch["lq"], count=5)
-    sampled_check(w, batch, got, idx)
+    idx = stratified_subset(batch["lq"])
+    assert len(idx) == 32
+    fig = whole_batch_check(w, batch, got, seqs=idx)
+    print("\ngdpa stratified subset (32 of 256 sequences): %s" % fig)
 
 
 # ----------------------------------------------------------------------------- pooled
@@ -238,8 +288,8 @@ def test_full_size_pooled_workload():
     err = float(torch.linalg.vector_norm(dq.double() - ref_dq) / torch.linalg.vector_norm(ref_dq))
     assert err <= 4e-3, err  # bf16 rounding of the sum
     rep = dict(batch, q=q_rep)
-    idx = sample_indices(batch["lk"], count=5)
-    sampled_check(w, rep, dict(o=o, lse=lse, dq=dq2, dk=dk, dv=dv), idx)
+    fig = whole_batch_check(w, rep, dict(o=o, lse=lse, dq=dq2, dk=dk, dv=dv))
+    print("\npooled whole batch: %s" % fig)
 
 
 # ----------------------------------------------------------------------------- BlockAttention
@@ -288,8 +338,9 @@ def test_block_bad_offsets_reported():
 
 
 def test_full_size_block_workload():
-    """BlockAttention over the causal workload's 1024 sequences (H=8, D=128) on the GPU; a
-    sample of whole sequences against the oracle."""
+    """BlockAttention over the causal workload's 1024 sequences (H=8, D=128) on the GPU;
+    every block of every sequence against the oracle's definition (causal softmax
+    attention within each 64-row block), error metrics over the whole batch."""
     import jagged_attention_recsys_gb300 as jfa
     import oracle
 
@@ -297,21 +348,16 @@ def test_full_size_block_workload():
     batch = workloads.make_batch(w, device="cuda")
     od = torch.as_tensor(batch["offs_q"], device="cuda")
     q, k, v, do = batch["q"], batch["k"], batch["v"], batch["do"]
-    o, lse = jfa.jfa_block_fwd(q, k, v, od, causal=True)
-    dq, dk, dv = jfa.jfa_block_bwd(q, k, v, o, lse, do, od, causal=True)
-    torch.cuda.synchronize()
-    for t in (o, lse, dq, dk, dv):
-        assert torch.isfinite(t.float()).all()
-    offs = batch["offs_q"]
-    for b in sample_indices(batch["lq"], count=5):
-        rows = torch.arange(int(offs[b]), int(offs[b + 1]), device="cuda")
-        sub = workloads.offsets([int(offs[b + 1] - offs[b])])
-        qq, kk, vv, dd = (to64(t[rows]) for t in (q, k, v, do))
-        ro, rlse = oracle.block_fwd(qq, kk, vv, sub, causal=True)
-        rdq, rdk, rdv = oracle.block_bwd(qq, kk, vv, dd, sub, causal=True)
-        got = dict(o=to64(o[rows]), lse=to64(lse[rows]), dq=to64(dq[rows]), dk=to64(dk[rows]),
-                   dv=to64(dv[rows]))
-        compare(w, got, dict(o=ro, lse=rlse, dq=rdq, dk=rdk, dv=rdv), fp32=False, strict_o=True)
+    p = jfa.params_for(q, k, v, od, causal=True)
+    ws = jfa.block_workspace(p)
+    o, lse = jfa.jfa_block_fwd(q, k, v, od, causal=True, ws=ws)
+    dq, dk, dv = jfa.jfa_block_bwd(q, k, v, o, lse, do, od, causal=True, ws=ws)
+    assert jfa.jfa_status_check(ws) == jfa.JFA_OK
+    bo = oracle.block_offsets(batch["offs_q"])
+    blocks = dict(batch, offs_q=bo, offs_k=bo)
+    wb = W(128, 128, causal=True, heads=w.heads)
+    fig = whole_batch_check(wb, blocks, dict(o=o, lse=lse, dq=dq, dk=dk, dv=dv))
+    print("\nblock whole batch (%d blocks): %s" % (len(bo) - 1, fig))
 
 
 # ----------------------------------------------------------------------------- CUDA graphs

@@ -66,3 +66,49 @@ def test_noalloc_rejects_requests_beyond_its_scratch():
     rc = jfa.lib().jfa_fwd_noalloc(ctypes.byref(p), vp(256), vp(256), vp(256), vp(256),
                                    vp(256), vp(256), None)
     assert rc == jfa.JFA_ERR_WORKSPACE
+
+
+def test_noalloc_many_sequences_matches_workspace_forward():
+    """More sequences than the scheduler keeps in shared memory (6,144), so its
+    per-sequence arrays go to the scratch: here the fixed array.  Bitwise equal to
+    jfa_fwd with a workspace, twice in a row."""
+    import jagged_attention_recsys_gb300 as jfa
+
+    w = workloads.Workload("noalloc", 0, 2, 64, 64, False, workloads.ACT_SOFTMAX,
+                           torch.bfloat16, False)
+    rng = np.random.default_rng(3)
+    for seed in (0, 1):
+        lens = rng.integers(0, 9, 7000).astype(np.int64)
+        batch = workloads.make_batch(w, lens, seed=seed, device="cuda")
+        offs = torch.as_tensor(batch["offs_q"], device="cuda")
+        q, k, v = batch["q"], batch["k"], batch["v"]
+        ref_o, ref_lse = jfa.jfa_fwd(q, k, v, offs)
+        p = jfa.params_for(q, k, v, offs)
+        o = torch.full_like(ref_o, float("nan"))
+        lse = torch.full_like(ref_lse, float("nan"))
+        rc = _call_noalloc(jfa, p, q, k, v, offs, o, lse)
+        assert rc == jfa.JFA_OK, jfa.status_string(rc)
+        torch.cuda.synchronize()
+        assert torch.equal(o, ref_o) and torch.equal(lse, ref_lse)
+
+
+def test_noalloc_bad_offsets_leave_outputs_untouched():
+    """Offsets that are not a jagged layout: the call computes nothing (the status word is
+    in the fixed array, out of the caller's reach), so NaN-filled outputs stay NaN; a
+    following valid call through the same array computes normally."""
+    import jagged_attention_recsys_gb300 as jfa
+
+    T, H, D = 40, 2, 64
+    q = torch.randn(T, H, D, device="cuda").to(torch.bfloat16)
+    bad = torch.tensor([0, 30, 20, 40], dtype=torch.int64, device="cuda")  # not monotone
+    p = jfa.params_for(q, q, q, bad)
+    o = torch.full((T, H, D), float("nan"), dtype=torch.bfloat16, device="cuda")
+    lse = torch.full((T, H), float("nan"), device="cuda")
+    assert _call_noalloc(jfa, p, q, q, q, bad, o, lse) == jfa.JFA_OK
+    torch.cuda.synchronize()
+    assert torch.isnan(o.float()).all() and torch.isnan(lse).all()
+    good = torch.tensor([0, 20, 30, 40], dtype=torch.int64, device="cuda")
+    assert _call_noalloc(jfa, p, q, q, q, good, o, lse) == jfa.JFA_OK
+    ref_o, ref_lse = jfa.jfa_fwd(q, q, q, good)
+    torch.cuda.synchronize()
+    assert torch.equal(o, ref_o) and torch.equal(lse, ref_lse)
