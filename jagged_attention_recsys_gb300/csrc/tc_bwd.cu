@@ -218,6 +218,7 @@ using KvGroups = Groups<ACT == kActSoftmax ? 2 : 4, 1>;
 // two producers: Q and K in warp 0, dO and V in the last warp, so that a V load
 // never queues behind a K load that waits for its slot (K(j+2) takes the slot of
 // K(j-1), which dQ(j-1) frees late in the step, while dP(j+1) wants V(j+1) early).
+template <int ACT>
 using QGroups = Groups<2, 1>;
 
 template <int DQK, int DV, int ACT, bool CAUSAL>
@@ -400,7 +401,7 @@ tc_dkdv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
     // the tensor pipe queues only a few, so the products come from two threads.
     // Each commit covers only its own thread's MMAs; resources used by both chains
     // (Q / dO stages, the accumulators) take one commit from each.
-    if (lane == 0) {
+    {  // the whole warp runs the issuer loop; one elected lane issues
       const bool chain_p = warp == 1;
       constexpr uint32_t idesc_dv = idesc_bf16(TILE, DV, 0, 1);
       constexpr uint32_t idesc_dk = idesc_bf16(TILE, DQK, 0, 1);
@@ -418,6 +419,7 @@ tc_dkdv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
             (chain_p && !mbar_wait(bar(KV_KDONE + b), ((c.g >> 1) & 1) ^ 1, abort, status)) ||
             (!chain_p && !mbar_wait(bar(KV_SEMPTY + b), (c.g >> 1) & 1, abort, status)))
           return false;
+        __syncwarp();  // converged for elect.sync
         tc_fence_after();
         const uint32_t a_tile = sb + (chain_p ? L::K_OFF : L::V_OFF);
         const uint32_t b_tile = chain_p ? sb + L::Q_OFF + st * L::Q_BYTES : sb + L::O_OFF + st * L::O_BYTES;
@@ -460,6 +462,7 @@ tc_dkdv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
           ok = false;
           break;
         }
+        __syncwarp();  // converged for elect.sync
         tc_fence_after();
         const int ksteps = cg.template n16<CAUSAL>() >> 4;
         // P^T or dS^T: each group's HC columns hold P^T of its HC queries in the first
@@ -489,6 +492,7 @@ tc_dkdv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
         }
         cg.advance();
       }
+      __syncwarp();
       mma_drain(bar(KV_DRAIN + (chain_p ? 0 : 1)), status);  // every MMA issued has completed
     }
     __syncwarp();
@@ -736,13 +740,13 @@ enum : uint32_t {
 static_assert(8 * Q_COUNT + 8 <= 512, "mbarriers, TMEM slot and abort flag in front of the tiles");
 
 template <int DQK, int DV, int ACT, bool CAUSAL>
-__global__ void __launch_bounds__(QGroups::kThreads, 1)
+__global__ void __launch_bounds__(QGroups<ACT>::kThreads, 1)
 tc_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
              const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
              const Problem p, const float2* __restrict__ rowstat, __nv_bfloat16* __restrict__ dq,
              WsHeader* hdr, const WorkItem* __restrict__ list) {
   using L = QLayout<DQK, DV>;
-  using Gr = QGroups;
+  using Gr = QGroups<ACT>;
   constexpr int NK = L::NK, NV = L::NV, NQ = L::NQ, NO = L::NO;
   constexpr int HC = Gr::HC;  // key columns per compute warpgroup
   static_assert(HC * Gr::G == STEP && HC % 32 == 0, "the compute warpgroups split a step's keys");
@@ -862,7 +866,7 @@ tc_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
     // one.  With a single Q tile the items are walked one by one: the next Q tile
     // loads only once this item's last S has completed, and the cross-item walk was
     // measured 2-12% slower there.
-    if (lane == 0) {
+    {  // the whole warp runs the issuer loop; one elected lane issues
       constexpr uint32_t idesc_s = idesc_bf16(TILE, STEP, 0, 0);
       constexpr uint32_t idesc_dq = idesc_bf16(TILE, DQK, 0, 1);
       if constexpr (NQ == 1) {
@@ -881,6 +885,7 @@ tc_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
           auto issue_s = [&](int i) {  // S(i) = Q K(i)^T into buffer (s_base + i) & 1
             const uint32_t kk_it = k_base + i, kst = kk_it % NK;
             if (!mbar_wait(bar(Q_KFULL + kst), (kk_it / NK) & 1, abort, status)) return false;
+            __syncwarp();  // converged for elect.sync
             tc_fence_after();
             const uint32_t k_tile = sb + L::K_OFF + kst * L::K_BYTES;
 #pragma unroll
@@ -903,6 +908,7 @@ tc_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
               ok = false;
               break;
             }
+            __syncwarp();  // converged for elect.sync
             tc_fence_after();
             const uint32_t k_tile = sb + L::K_OFF + kst * L::K_BYTES;
             const uint32_t ds_tm = tmem + t_s((s_base + j) & 1);
@@ -931,6 +937,7 @@ tc_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
           if ((c.j == 0 && !mbar_wait(bar(Q_QFULL + qs), (c.kv / NQ) & 1, abort, status)) ||
               !mbar_wait(bar(Q_KFULL + kst), (c.g / NK) & 1, abort, status))
             return false;
+          __syncwarp();  // converged for elect.sync
           tc_fence_after();
           const uint32_t q_tile = sb + L::Q_OFF + qs * L::Q_BYTES;
           const uint32_t k_tile = sb + L::K_OFF + kst * L::K_BYTES;
@@ -963,6 +970,7 @@ tc_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
             ok = false;
             break;
           }
+          __syncwarp();  // converged for elect.sync
           tc_fence_after();
           const uint32_t k_tile = sb + L::K_OFF + kst * L::K_BYTES;
           const uint32_t ds_tm = tmem + t_s(cg.g & 1);
@@ -980,12 +988,13 @@ tc_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
           ok = run_ahead();
         }
       }
+      __syncwarp();
       mma_drain(bar(Q_DRAIN), status);  // every MMA issued has completed
     }
     __syncwarp();
   } else if (warp == Gr::kIssuerB) {
     // ------------------------------------------------------------ issuer B: dP = dO V^T
-    if (lane == 0) {
+    {  // the whole warp runs the issuer loop; one elected lane issues
       constexpr uint32_t idesc_s = idesc_bf16(TILE, STEP, 0, 0);
       uint32_t q_it = 0, v_it = 0, dp_it = 0;  // V ring: v_it % NV
       bool ok = true;
@@ -1006,6 +1015,7 @@ tc_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
             ok = false;
             break;
           }
+          __syncwarp();  // converged for elect.sync
           tc_fence_after();
           const uint32_t v_tile = sb + L::V_OFF + vst * L::V_BYTES;
 #pragma unroll
@@ -1021,6 +1031,7 @@ tc_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
         if (!ok) break;
         ++q_it;
       }
+      __syncwarp();
       mma_drain(bar(Q_DRAIN + 1), status);  // every MMA issued has completed
     }
     __syncwarp();
@@ -1204,9 +1215,9 @@ cudaError_t dq_t(const Maps& m, const Problem& p, const float2* rowstat, void* d
                  const Workspace& ws, cudaStream_t s) {
   auto kern = tc_dq_kernel<DQK, DV, ACT, CAUSAL>;
   constexpr uint32_t smem = QLayout<DQK, DV>::SMEM;
-  cudaError_t e = kernel_setup((const void*)kern, QGroups::kThreads, smem);
+  cudaError_t e = kernel_setup((const void*)kern, QGroups<ACT>::kThreads, smem);
   if (e != cudaSuccess) return e;
-  kern<<<num_sms(), QGroups::kThreads, smem, s>>>(m.q, m.dout, m.k, m.v, p, rowstat,
+  kern<<<num_sms(), QGroups<ACT>::kThreads, smem, s>>>(m.q, m.dout, m.k, m.v, p, rowstat,
                                          (__nv_bfloat16*)dq, ws.hdr, ws.list_q);
   return cudaGetLastError();
 }

@@ -7,18 +7,22 @@
 // pipeline with a non-softmax activation (here SiLU(s)/L).
 //
 // One persistent CTA per SM walks the scheduler's heavy-first list of
-// (sequence, head, 128-row q-tile) items.  Warp roles:
-//   warps 0..3  softmax warpgroup 0: key columns [0,64) of every 128-key step
-//   warps 4..7  softmax warpgroup 1: key columns [64,128)
-//               (one query row per thread = TMEM lane; the two threads of a
-//               row exchange their partial row maximum through shared memory)
-//   warp 8      TMA producer of Q (double-buffered across items) and of the K
-//               ring; warp 11 that of the V ring.  128-key tiles come straight
-//               from the jagged [T, H*D] buffers (rows past a sequence belong
-//               to its neighbour and are masked; rows past the buffer are
-//               zero-filled by TMA)
-//   warp 9      TMEM owner and S = Q K^T issuer (one lane)
-//   warp 10     O += P V issuer (one lane)
+// (sequence, head, 128-row q-tile) items.  Warp roles (G compute warpgroups: 2 for
+// softmax, 4 for SiLU/L):
+//   warps 0..4G-1  compute warpgroups: group g takes key columns
+//                  [g*128/G, (g+1)*128/G) of every 128-key step (one query row
+//                  per thread = TMEM lane).  Softmax: the two threads of a row
+//                  exchange their partial row maximum through shared memory.
+//                  SiLU/L has no row statistics, so its elementwise work is
+//                  split four ways: twice the warps hide the latencies of the
+//                  TMEM loads and of tanh.
+//   warp 4G        TMA producer of Q (double-buffered across items) and of the K
+//                  ring; warp 4G+3 that of the V ring.  128-key tiles come
+//                  straight from the jagged [T, H*D] buffers (rows past a
+//                  sequence belong to its neighbour and are masked; rows past
+//                  the buffer are zero-filled by TMA)
+//   warp 4G+1      TMEM owner and S = Q K^T issuer (one lane)
+//   warp 4G+2      O += P V issuer (one lane)
 // TMEM: S double-buffered at columns [0,128) and [128,256), O at [256, 256+Dv),
 // P (packed bf16, 128 keys) double-buffered at [384, 448) and [448, 512).  S of
 // step j+2 goes into the buffer of S(j) once P(j) has been written; PV(j) reads
@@ -43,9 +47,17 @@ using namespace tc;
 
 constexpr int BM = 128;     // rows per item (MMA M)
 constexpr int BN = 128;     // keys per step (MMA N of S)
-constexpr int HC = BN / 2;  // key columns per softmax warpgroup
-constexpr int kThreads = 384;
-constexpr int kProducerWarp = 8, kSWarp = 9, kPvWarp = 10, kVWarp = 11;
+
+// Warp roles of the forward for activation ACT (see the file comment).
+template <int ACT>
+struct FwdRoles {
+  static constexpr int G = ACT == kActSoftmax ? 2 : 4;  // compute warpgroups
+  static constexpr int HC = BN / G;                      // key columns per group
+  static constexpr int kCompute = 128 * G;               // compute threads
+  static constexpr int kProducerWarp = 4 * G, kSWarp = 4 * G + 1, kPvWarp = 4 * G + 2,
+                       kVWarp = 4 * G + 3;
+  static constexpr int kThreads = 32 * (4 * G + 4);
+};
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleLog2 = 8.0f;
@@ -91,13 +103,19 @@ constexpr uint32_t T_S = 0, T_O = 256, T_P = 384;  // S: 2 x 128 columns; P: 2 x
 __device__ int g_test_hold = 0;
 
 template <int DQK, int DV, int ACT, bool CAUSAL>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(FwdRoles<ACT>::kThreads, 1)
 tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
               const __grid_constant__ CUtensorMap tm_v, const Problem p,
               __nv_bfloat16* __restrict__ out, float* __restrict__ lse, WsHeader* hdr,
               const WorkItem* __restrict__ list) {
   using L = FwdLayout<DQK, DV>;
+  using R = FwdRoles<ACT>;
   constexpr int NK = L::NK, NV = L::NV;
+  constexpr int HC = R::HC;
+  constexpr int OC = DV / R::G;  // O columns drained per compute warpgroup
+  constexpr int kProducerWarp = R::kProducerWarp, kSWarp = R::kSWarp, kPvWarp = R::kPvWarp,
+                kVWarp = R::kVWarp;
+  static_assert(R::G == 2 || ACT != kActSoftmax, "softmax row statistics are exchanged in pairs");
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t sb = (raw + L::SMALL + 1023u) & ~1023u;  // 128-byte swizzled tiles: 1 KB aligned
@@ -119,7 +137,7 @@ tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
       mbar_init(bar(B_QFULL + s), 1);
       mbar_init(bar(B_QEMPTY + s), 1);
       mbar_init(bar(B_SFULL + s), 1);
-      mbar_init(bar(B_PFULL + s), 256);
+      mbar_init(bar(B_PFULL + s), R::kCompute);
       mbar_init(bar(B_PEMPTY + s), 1);
       // exchanges between the two softmax warpgroups (bounded waits, never bar.sync)
       mbar_init(bar(B_RED + s), 256);
@@ -134,7 +152,7 @@ tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
       mbar_init(bar(B_VEMPTY + s), 1);
     }
     mbar_init(bar(B_OFULL), 1);
-    mbar_init(bar(B_OEMPTY), 256);
+    mbar_init(bar(B_OEMPTY), R::kCompute);
     mbar_init(bar(B_DRAIN), 1);      // S issuer's exit drain
     mbar_init(bar(B_DRAIN + 1), 1);  // PV issuer's exit drain
     mbar_init(bar(B_HOLD), 1);       // test hook: nothing arrives on it
@@ -211,7 +229,7 @@ tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     // An MMA issue occupies the issuing thread for most of the MMA's own duration
     // and the tensor pipe queues only a few, so the S and PV products come from two
     // threads: the waits and commits of one overlap the other's MMAs.
-    if (lane == 0) {
+    {  // the whole warp runs the issuer loop; one elected lane issues
       constexpr uint32_t idesc_s = idesc_bf16(BM, BN, 0, 0);
       uint32_t k_it = 0, q_it = 0, gs = 0;
       bool ok = true;
@@ -233,6 +251,7 @@ tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             ok = false;
             break;
           }
+          __syncwarp();  // converged for elect.sync
           tc_fence_after();
           const uint32_t k_tile = sb + L::K_OFF + kst * L::K_BYTES;
 #pragma unroll
@@ -247,12 +266,13 @@ tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         }
         ++q_it;
       }
+      __syncwarp();
       mma_drain(bar(B_DRAIN), status);  // every MMA issued has completed
     }
     __syncwarp();
   } else if (warp == kPvWarp) {
     // ------------------------------------------------------------ O += P V issuer
-    if (lane == 0) {
+    {  // the whole warp runs the issuer loop; one elected lane issues
       constexpr uint32_t idesc_o = idesc_bf16(BM, DV, 0, 1);
       uint32_t v_it = 0, o_it = 0, gs = 0;
       bool ok = true;
@@ -270,6 +290,7 @@ tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             ok = false;
             break;
           }
+          __syncwarp();  // converged for elect.sync
           tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < BN / 16; ++kk) {
@@ -284,12 +305,13 @@ tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         if (!ok) break;
         ++o_it;
       }
+      __syncwarp();
       mma_drain(bar(B_DRAIN + 1), status);  // every MMA issued has completed
     }
     __syncwarp();
   } else {
     // ------------------------------------------------------------ softmax warpgroups
-    const int half = warp >> 2;            // key columns [half*64, half*64+64) of each step
+    const int grp = warp >> 2;             // key columns [grp*HC, grp*HC+HC) of each step
     const int r = 32 * (warp & 3) + lane;  // TMEM lane = row of the tile
     const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
     const float c_score = ACT == kActSoftmax ? p.scale * kLog2e : p.scale;
@@ -307,17 +329,14 @@ tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
       if (!mbar_wait(bar(B_OFULL), o_it & 1, abort, status)) return false;
       ++o_it;
       tc_fence_after();
-      float ov[DV / 2];
-#pragma unroll
-      for (int c = 0; c < DV / 64; ++c) tmem_ld32(tmem + lane_base + T_O + half * (DV / 2) + 32 * c, ov + 32 * c);
+      float ov[OC];
+      tmem_ld<OC>(tmem + lane_base + T_O + grp * OC, ov);
       tmem_wait_ld();
       tc_fence_before();
       mbar_arrive(bar(B_OEMPTY));
       if (pend_row_ok) {
-#pragma unroll
-        for (int c = 0; c < DV / 64; ++c)
-          store32_bf16(out + pend_orow * DV + half * (DV / 2) + 32 * c, ov + 32 * c, pend_norm);
-        if (ACT == kActSoftmax && half == 0 && lse != nullptr) lse[pend_orow] = pend_lse;
+        store_bf16<OC>(out + pend_orow * DV + grp * OC, ov, pend_norm);
+        if (ACT == kActSoftmax && grp == 0 && lse != nullptr) lse[pend_orow] = pend_lse;
       }
       pend = false;
       return true;
@@ -335,12 +354,11 @@ tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         const uint32_t b = p_it & 1;
         if (!mbar_wait(bar(B_SFULL + b), (p_it >> 1) & 1, abort, status)) { ok = false; break; }
         tc_fence_after();
-        const uint32_t s_tm = tmem + lane_base + T_S + b * 128 + half * HC;
+        const uint32_t s_tm = tmem + lane_base + T_S + b * 128 + grp * HC;
         float sv[HC];
-        tmem_ld32(s_tm, sv);
-        tmem_ld32(s_tm + 32, sv + 32);
+        tmem_ld<HC>(s_tm, sv);
         tmem_wait_ld();
-        const int kb = j * BN + half * HC;
+        const int kb = j * BN + grp * HC;
         int nvalid = Lk - kb;
         if (CAUSAL) nvalid = min(nvalid, i - kb + 1);
         if (nvalid < HC) {
@@ -358,7 +376,7 @@ tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             m1 = fmax3(m1, sv[k + 2], sv[k + 3]);
           }
           float* rb = red + (p_it & 1) * (BM * 2);
-          rb[r * 2 + half] = fmaxf(m0, m1);
+          rb[r * 2 + grp] = fmaxf(m0, m1);
           mbar_arrive(bar(B_RED + (p_it & 1)));
           if (!mbar_wait(bar(B_RED + (p_it & 1)), (p_it >> 1) & 1, abort, status)) { ok = false; break; }
           const float mt = fmaxf(rb[r * 2], rb[r * 2 + 1]) * c_score;
@@ -410,19 +428,26 @@ tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
           break;
         }
         tc_fence_after();
-        if (rescale) {
-          float ov[32];
+        if constexpr (ACT == kActSoftmax) {
+          if (rescale) {
+            float ov[32];
 #pragma unroll
-          for (int c = 0; c < DV / 64; ++c) {
-            const uint32_t o_tm = tmem + lane_base + T_O + half * (DV / 2) + 32 * c;
-            tmem_ld32(o_tm, ov);
-            tmem_wait_ld();
+            for (int c = 0; c < OC / 32; ++c) {
+              const uint32_t o_tm = tmem + lane_base + T_O + grp * OC + 32 * c;
+              tmem_ld32(o_tm, ov);
+              tmem_wait_ld();
 #pragma unroll
-            for (int t = 0; t < 32; ++t) ov[t] *= alpha;
-            tmem_st32(o_tm, ov);
+              for (int t = 0; t < 32; ++t) ov[t] *= alpha;
+              tmem_st32(o_tm, ov);
+            }
           }
         }
-        tmem_st32(tmem + lane_base + T_P + b * 64 + half * (HC / 2), reinterpret_cast<const float*>(pk));
+        // P of this group's keys, packed: HC/2 columns at the group's offset, so that the
+        // P buffer holds the step's 128 keys in order
+        if constexpr (HC == 64)
+          tmem_st32(tmem + lane_base + T_P + b * 64 + grp * (HC / 2), reinterpret_cast<const float*>(pk));
+        else
+          tmem_st16(tmem + lane_base + T_P + b * 64 + grp * (HC / 2), pk);
         tmem_wait_st();
         tc_fence_before();
         mbar_arrive(bar(B_PFULL + b));
@@ -440,7 +465,7 @@ tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
           float* rl = red + ((p_it - 1) & 1) * (BM * 2);
           mbar_arrive(bar(B_REDL));
           if (!mbar_wait(bar(B_REDL), l_it & 1, abort, status)) { ok = false; break; }
-          rl[r * 2 + half] = l;
+          rl[r * 2 + grp] = l;
           mbar_arrive(bar(B_REDL + 1));
           if (!mbar_wait(bar(B_REDL + 1), l_it & 1, abort, status)) { ok = false; break; }
           ++l_it;
@@ -453,10 +478,9 @@ tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         pend_norm = ACT == kActSoftmax ? (lt > 0.f ? 1.f / lt : 0.f) : 1.f;
         pend_lse = lt > 0.f ? (m + log2f(lt)) * kLn2 : -INFINITY;
       } else if (row_ok) {
-        const float z[32] = {0.f};
-#pragma unroll
-        for (int c = 0; c < DV / 64; ++c) store32_bf16(out + orow * DV + half * (DV / 2) + 32 * c, z, 1.f);
-        if (ACT == kActSoftmax && half == 0 && lse != nullptr) lse[orow] = -INFINITY;
+        const float z[OC] = {0.f};
+        store_bf16<OC>(out + orow * DV + grp * OC, z, 1.f);
+        if (ACT == kActSoftmax && grp == 0 && lse != nullptr) lse[orow] = -INFINITY;
       }
     }
     if (ok && pend) ok = epilogue();
@@ -476,9 +500,10 @@ cudaError_t launch_fwd_t(const Problem& p, const CUtensorMap& mq, const CUtensor
                          cudaStream_t s) {
   auto kern = tc_fwd_kernel<DQK, DV, ACT, CAUSAL>;
   constexpr uint32_t smem = FwdLayout<DQK, DV>::SMEM;
-  cudaError_t e = kernel_setup((const void*)kern, kThreads, smem);
+  constexpr int threads = FwdRoles<ACT>::kThreads;
+  cudaError_t e = kernel_setup((const void*)kern, threads, smem);
   if (e != cudaSuccess) return e;
-  kern<<<num_sms(), kThreads, smem, s>>>(mq, mk, mv, p, (__nv_bfloat16*)o, lse, ws.hdr, ws.list_q);
+  kern<<<num_sms(), threads, smem, s>>>(mq, mk, mv, p, (__nv_bfloat16*)o, lse, ws.hdr, ws.list_q);
   return cudaGetLastError();
 }
 

@@ -126,12 +126,19 @@ __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
                : "memory");
 }
 
+// MMA issue.  The issuing warp runs converged: all 32 lanes compute the same
+// descriptors (so they stay warp-uniform) and execute these helpers together; one
+// lane, chosen by elect.sync, issues the instruction.  Issuing from inside an
+// `if (lane == 0)` branch instead costs the issuing thread markedly more per MMA.
+// elect.sync picks the lowest active lane, the same lane every time, so a commit
+// covers the MMAs issued before it.
+
 // D[tmem] (+)= A[smem] * B[smem]^T, kind::f16 (bf16 in, fp32 accumulate), one CTA.
 __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
                                          uint32_t idesc, uint32_t accumulate) {
   asm volatile(
-      "{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\n"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(d_tmem),
+      "{\n.reg .pred p, e;\nsetp.ne.b32 p, %4, 0;\nelect.sync _|e, 0xffffffff;\n"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(d_tmem),
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
@@ -140,19 +147,21 @@ __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint6
 __device__ __forceinline__ void mma_bf16_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
                                                 uint32_t idesc, uint32_t accumulate) {
   asm volatile(
-      "{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\n"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}" ::"r"(d_tmem),
+      "{\n.reg .pred p, e;\nsetp.ne.b32 p, %4, 0;\nelect.sync _|e, 0xffffffff;\n"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}" ::"r"(d_tmem),
       "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
-// Arrive on `bar` once every tcgen05 operation issued so far by this thread has completed.
+// Arrive on `bar` once every tcgen05 operation issued so far by the issuing lane has
+// completed (warp-collective, like the MMA helpers).
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
   asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+      "{\n.reg .pred e;\nelect.sync _|e, 0xffffffff;\n"
+      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n}" ::"r"(bar)
       : "memory");
 }
 // An MMA issuer's drain when it leaves its loop: a commit of everything it issued
-// to a barrier of its own (count 1, used once), and a wait for it.
+// to a barrier of its own (count 1, used once), and a wait for it (warp-collective).
 __device__ __forceinline__ void mma_drain(uint32_t drain_bar, int* status) {
   mma_commit(drain_bar);
   mbar_wait_drain(drain_bar, 0, status);
@@ -170,6 +179,17 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v) {
         "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
         "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
         "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+}
+// 16 consecutive fp32 columns of this thread's TMEM lane (warp-collective).
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float* v) {
+  uint32_t* r = reinterpret_cast<uint32_t*>(v);
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, "
+      "%12, %13, %14, %15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15])
       : "r"(taddr));
 }
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float* v) {
@@ -310,6 +330,41 @@ __device__ __forceinline__ void store32_bf16(__nv_bfloat16* dst, const float* x,
     uint4* d = reinterpret_cast<uint4*>(dst);
 #pragma unroll
     for (int t = 0; t < 4; ++t) d[t] = make_uint4(w[4 * t], w[4 * t + 1], w[4 * t + 2], w[4 * t + 3]);
+  }
+}
+// 16 floats times f as bf16 to dst (32 bytes): one 32-byte store when dst is 32-byte aligned
+__device__ __forceinline__ void store16_bf16(__nv_bfloat16* dst, const float* x, float f) {
+  uint32_t w[8];
+#pragma unroll
+  for (int t = 0; t < 8; ++t) w[t] = pack_bf16(x[2 * t] * f, x[2 * t + 1] * f);
+  if ((reinterpret_cast<uintptr_t>(dst) & 31) == 0) {
+    st_global_v8(dst, w);
+  } else {
+    uint4* d = reinterpret_cast<uint4*>(dst);
+    d[0] = make_uint4(w[0], w[1], w[2], w[3]);
+    d[1] = make_uint4(w[4], w[5], w[6], w[7]);
+  }
+}
+// n (16 or a multiple of 32) floats times f as bf16 to dst
+template <int N>
+__device__ __forceinline__ void store_bf16(__nv_bfloat16* dst, const float* x, float f) {
+  static_assert(N == 16 || N % 32 == 0, "16 or whole 32-column chunks");
+  if constexpr (N == 16) {
+    store16_bf16(dst, x, f);
+  } else {
+#pragma unroll
+    for (int c = 0; c < N / 32; ++c) store32_bf16(dst + 32 * c, x + 32 * c, f);
+  }
+}
+// n (16 or a multiple of 32) consecutive fp32 columns of this thread's TMEM lane
+template <int N>
+__device__ __forceinline__ void tmem_ld(uint32_t taddr, float* v) {
+  static_assert(N == 16 || N % 32 == 0, "16 or whole 32-column chunks");
+  if constexpr (N == 16) {
+    tmem_ld16(taddr, v);
+  } else {
+#pragma unroll
+    for (int c = 0; c < N / 32; ++c) tmem_ld32(taddr + 32 * c, v + 32 * c);
   }
 }
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
