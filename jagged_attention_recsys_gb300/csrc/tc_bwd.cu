@@ -214,12 +214,13 @@ struct StepCursor {
 // which leave its issuers' warp schedulers less busy.
 template <int ACT>
 using KvGroups = Groups<ACT == kActSoftmax ? 2 : 4, 1>;
-// dQ: two groups of 64 key columns for both activations (four were no faster), and
-// two producers: Q and K in warp 0, dO and V in the last warp, so that a V load
-// never queues behind a K load that waits for its slot (K(j+2) takes the slot of
-// K(j-1), which dQ(j-1) frees late in the step, while dP(j+1) wants V(j+1) early).
+// dQ: two groups of 64 key columns for softmax, four of 32 for SiLU/L (its compute
+// warps set the pace once the issuers run converged: 3.95 -> 3.80 ms on the GDPA
+// workload), and two producers: Q and K in warp 0, dO and V in the last warp, so that
+// a V load never queues behind a K load that waits for its slot (K(j+2) takes the slot
+// of K(j-1), which dQ(j-1) frees late in the step, while dP(j+1) wants V(j+1) early).
 template <int ACT>
-using QGroups = Groups<2, 1>;
+using QGroups = Groups<ACT == kActSoftmax ? 2 : 4, 1>;
 
 template <int DQK, int DV, int ACT, bool CAUSAL>
 __global__ void __launch_bounds__(KvGroups<ACT>::kThreads, 1)
