@@ -245,6 +245,7 @@ def config_of(w, lq, lk, world):
             "dim_v": w.dim_v, "causal": w.causal,
             "activation": "softmax" if w.act == workloads.ACT_SOFTMAX else "silu_over_len",
             "cross": w.cross, "pooled_queries": w.pooled or None, "block": w.block or None,
+            "rope": w.rope or None,
             "total_q": tq, "total_k": tk,
             "useful_gflop_fwd": round(fwd_f / 1e9, 3), "useful_gflop_bwd": round(bwd_f / 1e9, 3),
             "l2": "inputs %.2f GB (L2 is 0.13 GB); the GPU arm also writes 256 MiB between "
@@ -258,9 +259,10 @@ def gpu_step_fn(jfa, w, d, ws):
     sc = w.scale
     if w.block:
         def step():
-            jfa.jfa_block_fwd(q, k, v, oq, scale=sc, causal=w.causal, o=o, lse=lse, ws=ws)
+            jfa.jfa_block_fwd(q, k, v, oq, scale=sc, causal=w.causal, o=o, lse=lse, ws=ws,
+                              rope=w.rope)
             jfa.jfa_block_bwd(q, k, v, o, lse, do, oq, scale=sc, causal=w.causal, dq=dq, dk=dk,
-                              dv=dv, ws=ws)
+                              dv=dv, ws=ws, rope=w.rope)
     elif w.pooled:
         def step():
             jfa.jfa_pooled_fwd(q, k, v, ok, scale=sc, o=o, lse=lse, ws=ws)
@@ -310,6 +312,9 @@ def cpu_baseline(w, lq, lk, budget_s=12.0, seed=0):
     if w.pooled:
         oracle.pooled_fwd(q[:w.pooled], k, v, ok, scale=w.scale)
         oracle.pooled_bwd(q[:w.pooled], k, v, do, ok, scale=w.scale)
+    elif w.block and w.rope:
+        oracle.block_rope_fwd(q, k, v, oq, scale=w.scale, causal=w.causal)
+        oracle.block_rope_bwd(q, k, v, do, oq, scale=w.scale, causal=w.causal)
     elif w.block:
         oracle.block_fwd(q, k, v, oq, scale=w.scale, causal=w.causal)
         oracle.block_bwd(q, k, v, do, oq, scale=w.scale, causal=w.causal)

@@ -218,7 +218,7 @@ jfa_status jfa_pooled_bwd(const jfa_params* p, int32_t m, const void* q, const v
  * self-attention kernels run on the blocks as sequences of their own; the
  * workspace (jfa_block_workspace_size) holds the block offsets and room for up
  * to B + ceil(T/64) block sequences.  The pages combine the blocks with a fused
- * rotary position embedding; that embedding is not part of this call.
+ * rotary position embedding: see jfa_block_rope_fwd / jfa_block_rope_bwd below.
  */
 size_t jfa_block_workspace_size(const jfa_params* p);
 jfa_status jfa_block_fwd(const jfa_params* p, const void* q, const void* k, const void* v,
@@ -228,6 +228,28 @@ jfa_status jfa_block_bwd(const jfa_params* p, const void* q, const void* k, cons
                          const void* o, const float* lse, const void* dout, const int64_t* offs,
                          void* dq, void* dk, void* dv, void* ws, size_t ws_bytes,
                          jfa_stream_t stream);
+
+/*
+ * BlockAttention with the fused rotary position embedding (same bullet: the 64-token
+ * blocks are combined with a fused rotary position embedding).  The page gives none of
+ * the embedding's parameters; this library follows RoFormer's definition: columns
+ * (2i, 2i+1) of every q and k row, at position p, turn by the angle p * 10000^(-2i/D)
+ * (D = dim_qk), with p the row's index inside its sequence.  Inside one block the scores
+ * depend only on the difference of positions, so this equals counting positions from
+ * each block's first row, which is how the kernels do it.  q and k are the unrotated
+ * inputs; dq and dk are the gradients with respect to them.  The rotation is applied to
+ * the Q and K tiles in shared memory between their load and the MMAs (no extra pass over
+ * HBM), and its transpose to dQ and dK before they are stored.  Arguments, outputs,
+ * workspace (jfa_block_workspace_size) and errors as for jfa_block_fwd / jfa_block_bwd;
+ * bf16 with dim_qk == dim_v (64 or 128) only, else JFA_ERR_UNSUPPORTED.
+ */
+jfa_status jfa_block_rope_fwd(const jfa_params* p, const void* q, const void* k, const void* v,
+                              const int64_t* offs, void* o, float* lse, void* ws, size_t ws_bytes,
+                              jfa_stream_t stream);
+jfa_status jfa_block_rope_bwd(const jfa_params* p, const void* q, const void* k, const void* v,
+                              const void* o, const float* lse, const void* dout, const int64_t* offs,
+                              void* dq, void* dk, void* dv, void* ws, size_t ws_bytes,
+                              jfa_stream_t stream);
 
 /*
  * Synchronises `stream`, then returns the device status word of the last

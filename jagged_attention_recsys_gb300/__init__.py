@@ -39,7 +39,7 @@ EXPORTS = ("jfa_workspace_size", "jfa_fwd", "jfa_bwd", "jfa_cross_fwd", "jfa_cro
            "jfa_profile_enable", "jfa_profile_reset", "jfa_profile_read", "jfa_path_for",
            "jfa_fwd_noalloc", "jfa_bbs_plan", "jfa_pooled_workspace_size", "jfa_pooled_fwd",
            "jfa_pooled_bwd", "jfa_block_workspace_size", "jfa_block_fwd", "jfa_block_bwd",
-           "jfa_test_hold")
+           "jfa_test_hold", "jfa_block_rope_fwd", "jfa_block_rope_bwd")
 
 
 class JfaError(RuntimeError):
@@ -113,6 +113,10 @@ def lib():
         L.jfa_block_fwd.restype = ctypes.c_int
         L.jfa_block_bwd.argtypes = [P, vp, vp, vp, vp, fp, vp, i64p, vp, vp, vp, vp, sz, vp]
         L.jfa_block_bwd.restype = ctypes.c_int
+        L.jfa_block_rope_fwd.argtypes = [P, vp, vp, vp, i64p, vp, fp, vp, sz, vp]
+        L.jfa_block_rope_fwd.restype = ctypes.c_int
+        L.jfa_block_rope_bwd.argtypes = [P, vp, vp, vp, vp, fp, vp, i64p, vp, vp, vp, vp, sz, vp]
+        L.jfa_block_rope_bwd.restype = ctypes.c_int
         _lib = L
     return _lib
 
@@ -376,8 +380,9 @@ def block_workspace(p: jfa_params, device="cuda") -> torch.Tensor:
 
 
 def jfa_block_fwd(q, k, v, offs, *, scale=None, causal=False, o=None, lse=None, ws=None,
-                  stream=None):
-    """BlockAttention forward (softmax within fixed 64-row blocks); returns (o, lse)."""
+                  stream=None, rope=False):
+    """BlockAttention forward (softmax within fixed 64-row blocks); returns (o, lse).
+    With ``rope``, the fused rotary position embedding (jfa_block_rope_fwd)."""
     _check_tensors(q, k, v, offs)
     p = params_for(q, k, v, offs, scale, causal)
     ws = block_workspace(p, q.device) if ws is None else ws
@@ -385,21 +390,24 @@ def jfa_block_fwd(q, k, v, offs, *, scale=None, causal=False, o=None, lse=None, 
         o = torch.empty(q.shape[0], q.shape[1], v.shape[2], dtype=q.dtype, device=q.device)
     if lse is None:
         lse = torch.empty(q.shape[0], q.shape[1], dtype=torch.float32, device=q.device)
-    _check(lib().jfa_block_fwd(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(offs), _ptr(o),
-                               _ptr(lse), _ptr(ws), ws.numel(), _stream(stream)), "jfa_block_fwd")
+    name = "jfa_block_rope_fwd" if rope else "jfa_block_fwd"
+    _check(getattr(lib(), name)(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(offs), _ptr(o),
+                                _ptr(lse), _ptr(ws), ws.numel(), _stream(stream)), name)
     return o, lse
 
 
 def jfa_block_bwd(q, k, v, o, lse, dout, offs, *, scale=None, causal=False, dq=None, dk=None,
-                  dv=None, ws=None, stream=None):
-    """Backward of jfa_block_fwd; returns (dq, dk, dv)."""
+                  dv=None, ws=None, stream=None, rope=False):
+    """Backward of jfa_block_fwd; returns (dq, dk, dv).  With ``rope``, the backward of the
+    fused rotary position embedding as well (jfa_block_rope_bwd)."""
     _check_tensors(q, k, v, offs)
     p = params_for(q, k, v, offs, scale, causal)
     ws = block_workspace(p, q.device) if ws is None else ws
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv
-    _check(lib().jfa_block_bwd(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse),
-                               _ptr(dout), _ptr(offs), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(ws),
-                               ws.numel(), _stream(stream)), "jfa_block_bwd")
+    name = "jfa_block_rope_bwd" if rope else "jfa_block_bwd"
+    _check(getattr(lib(), name)(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse),
+                                _ptr(dout), _ptr(offs), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(ws),
+                                ws.numel(), _stream(stream)), name)
     return dq, dk, dv

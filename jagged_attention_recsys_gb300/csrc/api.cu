@@ -258,6 +258,8 @@ Problem make_problem(const jfa_params* p, const int64_t* oq, const int64_t* ok, 
   r.scale = p->scale;
   r.causal = p->causal;
   r.act = act;
+  r.rope = nullptr;
+  r.rope_npos = 0;
   return r;
 }
 
@@ -268,7 +270,8 @@ jfa_status empty_call(const Workspace& w, cudaStream_t s) {
 
 jfa_status run_fwd(const jfa_params* p, Kind kind, int act, const void* q, const void* k,
                    const void* v, const int64_t* oq, const int64_t* ok, void* o, float* lse,
-                   void* ws, size_t ws_bytes, cudaStream_t s) {
+                   void* ws, size_t ws_bytes, cudaStream_t s, const float2* rope = nullptr,
+                   int rope_npos = 0) {
   jfa_status st = check_params(p, kind);
   if (st != JFA_OK) return st;
   if ((st = check_ptrs({oq, ok})) != JFA_OK) return st;
@@ -281,6 +284,8 @@ jfa_status run_fwd(const jfa_params* p, Kind kind, int act, const void* q, const
   if ((st = prepare(p, ws, ws_bytes, &w)) != JFA_OK) return st;
   if (p->batch == 0) return empty_call(w, s);
   Problem pr = make_problem(p, oq, ok, act);
+  pr.rope = rope;
+  pr.rope_npos = rope_npos;
   const int path = jfa_path_for(p);
   SchedConfig sc = path == 1 ? tc_fwd_sched(pr) : kSimtSched;
   sc.build_q = 1;
@@ -298,7 +303,8 @@ jfa_status run_fwd(const jfa_params* p, Kind kind, int act, const void* q, const
 jfa_status run_bwd(const jfa_params* p, Kind kind, int act, const void* q, const void* k,
                    const void* v, const void* o, const float* lse, const void* dout,
                    const int64_t* oq, const int64_t* ok, void* dq, void* dk, void* dv, void* ws,
-                   size_t ws_bytes, cudaStream_t s) {
+                   size_t ws_bytes, cudaStream_t s, const float2* rope = nullptr,
+                   int rope_npos = 0) {
   jfa_status st = check_params(p, kind);
   if (st != JFA_OK) return st;
   if ((st = check_ptrs({oq, ok})) != JFA_OK) return st;
@@ -311,6 +317,8 @@ jfa_status run_bwd(const jfa_params* p, Kind kind, int act, const void* q, const
   if ((st = prepare(p, ws, ws_bytes, &w)) != JFA_OK) return st;
   if (p->batch == 0) return empty_call(w, s);
   Problem pr = make_problem(p, oq, ok, act);
+  pr.rope = rope;
+  pr.rope_npos = rope_npos;
   const int path = jfa_path_for(p);
   SchedConfig sc = path == 1 ? tc_bwd_sched(pr) : kSimtSched;
   sc.build_q = 1;
@@ -387,14 +395,17 @@ jfa_status check_pooled(const jfa_params* p, int32_t m, void* ws, size_t ws_byte
 // block offsets.
 constexpr int kBlock = 64;
 int64_t block_count(const jfa_params* p) { return p->batch + (p->total_q + kBlock - 1) / kBlock; }
+constexpr double kRopeBase = 10000.0;  // the rotary embedding's frequency base
 struct BlockWs {
-  size_t offs, total;
+  size_t offs, rope, total;
 };
 BlockWs block_layout(const jfa_params* p) {
   BlockWs r;
   const int64_t nb = block_count(p);
   r.offs = align_up(workspace_layout(nb, p->total_q, p->total_k, p->heads, nullptr, nullptr), 256);
-  r.total = align_up(r.offs + 8 * (size_t)(nb + 1), 256);
+  // then the rotary embedding's (cos, sin) table: kBlock positions by dim_qk/2 pairs
+  r.rope = align_up(r.offs + 8 * (size_t)(nb + 1), 256);
+  r.total = align_up(r.rope + sizeof(float2) * kBlock * (size_t)(p->dim_qk > 0 ? p->dim_qk / 2 : 0), 256);
   return r;
 }
 
@@ -410,6 +421,62 @@ jfa_status check_block(const jfa_params* p, void* ws, size_t ws_bytes, jfa_param
   return JFA_OK;
 }
 
+}  // namespace
+}  // namespace jfa
+
+namespace jfa {
+namespace {
+// The rotary embedding needs the tensor-core path with Dqk = Dv (its kernels rotate the
+// Q and K tiles in shared memory).
+jfa_status check_rope(const jfa_params* p) {
+  if (jfa_path_for(p) != 1 || p->dim_qk != p->dim_v) return JFA_ERR_UNSUPPORTED;
+  return JFA_OK;
+}
+
+jfa_status block_fwd(const jfa_params* p, const void* q, const void* k, const void* v,
+                     const int64_t* offs, void* o, float* lse, void* ws, size_t ws_bytes,
+                     cudaStream_t s, bool rope) {
+  jfa_params pb;
+  BlockWs lay;
+  jfa_status st = check_block(p, ws, ws_bytes, &pb, &lay);
+  if (st != JFA_OK) return st;
+  if (rope && (st = check_rope(p)) != JFA_OK) return st;
+  if ((st = check_ptrs({offs})) != JFA_OK) return st;
+  if (p->total_q > 0 && (st = check_ptrs({q, k, v, o, lse})) != JFA_OK) return st;
+  int64_t* boffs = (int64_t*)((char*)ws + lay.offs);
+  float2* table = (float2*)((char*)ws + lay.rope);
+  if (p->batch > 0) {
+    Timed t(JFA_KERNEL_AUX, s);
+    if ((st = cu(launch_block_offsets(offs, p->batch, p->total_q, kBlock, boffs, pb.batch, s))) != JFA_OK)
+      return st;
+    if (rope && (st = cu(launch_rope_table(table, kBlock, p->dim_qk, kRopeBase, s))) != JFA_OK) return st;
+  }
+  return run_fwd(&pb, Kind::Self, kActSoftmax, q, k, v, boffs, boffs, o, lse, ws, ws_bytes, s,
+                 rope ? table : nullptr, rope ? kBlock : 0);
+}
+
+jfa_status block_bwd(const jfa_params* p, const void* q, const void* k, const void* v,
+                     const void* o, const float* lse, const void* dout, const int64_t* offs,
+                     void* dq, void* dk, void* dv, void* ws, size_t ws_bytes, cudaStream_t s,
+                     bool rope) {
+  jfa_params pb;
+  BlockWs lay;
+  jfa_status st = check_block(p, ws, ws_bytes, &pb, &lay);
+  if (st != JFA_OK) return st;
+  if (rope && (st = check_rope(p)) != JFA_OK) return st;
+  if ((st = check_ptrs({offs})) != JFA_OK) return st;
+  if (p->total_q > 0 && (st = check_ptrs({q, k, v, o, lse, dout, dq, dk, dv})) != JFA_OK) return st;
+  int64_t* boffs = (int64_t*)((char*)ws + lay.offs);
+  float2* table = (float2*)((char*)ws + lay.rope);
+  if (p->batch > 0) {
+    Timed t(JFA_KERNEL_AUX, s);
+    if ((st = cu(launch_block_offsets(offs, p->batch, p->total_q, kBlock, boffs, pb.batch, s))) != JFA_OK)
+      return st;
+    if (rope && (st = cu(launch_rope_table(table, kBlock, p->dim_qk, kRopeBase, s))) != JFA_OK) return st;
+  }
+  return run_bwd(&pb, Kind::Self, kActSoftmax, q, k, v, o, lse, dout, boffs, boffs, dq, dk, dv, ws,
+                 ws_bytes, s, rope ? table : nullptr, rope ? kBlock : 0);
+}
 }  // namespace
 }  // namespace jfa
 
@@ -543,41 +610,27 @@ size_t jfa_block_workspace_size(const jfa_params* p) {
 jfa_status jfa_block_fwd(const jfa_params* p, const void* q, const void* k, const void* v,
                          const int64_t* offs, void* o, float* lse, void* ws, size_t ws_bytes,
                          jfa_stream_t stream) {
-  jfa_params pb;
-  BlockWs lay;
-  jfa_status st = check_block(p, ws, ws_bytes, &pb, &lay);
-  if (st != JFA_OK) return st;
-  if ((st = check_ptrs({offs})) != JFA_OK) return st;
-  if (p->total_q > 0 && (st = check_ptrs({q, k, v, o, lse})) != JFA_OK) return st;
-  cudaStream_t s = (cudaStream_t)stream;
-  int64_t* boffs = (int64_t*)((char*)ws + lay.offs);
-  if (p->batch > 0) {
-    Timed t(JFA_KERNEL_AUX, s);
-    if ((st = cu(launch_block_offsets(offs, p->batch, p->total_q, kBlock, boffs, pb.batch, s))) != JFA_OK)
-      return st;
-  }
-  return run_fwd(&pb, Kind::Self, kActSoftmax, q, k, v, boffs, boffs, o, lse, ws, ws_bytes, s);
+  return block_fwd(p, q, k, v, offs, o, lse, ws, ws_bytes, (cudaStream_t)stream, false);
+}
+
+jfa_status jfa_block_rope_fwd(const jfa_params* p, const void* q, const void* k, const void* v,
+                              const int64_t* offs, void* o, float* lse, void* ws, size_t ws_bytes,
+                              jfa_stream_t stream) {
+  return block_fwd(p, q, k, v, offs, o, lse, ws, ws_bytes, (cudaStream_t)stream, true);
 }
 
 jfa_status jfa_block_bwd(const jfa_params* p, const void* q, const void* k, const void* v,
                          const void* o, const float* lse, const void* dout, const int64_t* offs,
                          void* dq, void* dk, void* dv, void* ws, size_t ws_bytes,
                          jfa_stream_t stream) {
-  jfa_params pb;
-  BlockWs lay;
-  jfa_status st = check_block(p, ws, ws_bytes, &pb, &lay);
-  if (st != JFA_OK) return st;
-  if ((st = check_ptrs({offs})) != JFA_OK) return st;
-  if (p->total_q > 0 && (st = check_ptrs({q, k, v, o, lse, dout, dq, dk, dv})) != JFA_OK) return st;
-  cudaStream_t s = (cudaStream_t)stream;
-  int64_t* boffs = (int64_t*)((char*)ws + lay.offs);
-  if (p->batch > 0) {
-    Timed t(JFA_KERNEL_AUX, s);
-    if ((st = cu(launch_block_offsets(offs, p->batch, p->total_q, kBlock, boffs, pb.batch, s))) != JFA_OK)
-      return st;
-  }
-  return run_bwd(&pb, Kind::Self, kActSoftmax, q, k, v, o, lse, dout, boffs, boffs, dq, dk, dv, ws,
-                 ws_bytes, s);
+  return block_bwd(p, q, k, v, o, lse, dout, offs, dq, dk, dv, ws, ws_bytes, (cudaStream_t)stream, false);
+}
+
+jfa_status jfa_block_rope_bwd(const jfa_params* p, const void* q, const void* k, const void* v,
+                              const void* o, const float* lse, const void* dout, const int64_t* offs,
+                              void* dq, void* dk, void* dv, void* ws, size_t ws_bytes,
+                              jfa_stream_t stream) {
+  return block_bwd(p, q, k, v, o, lse, dout, offs, dq, dk, dv, ws, ws_bytes, (cudaStream_t)stream, true);
 }
 
 jfa_status jfa_status_check(const void* ws, jfa_stream_t stream) {

@@ -75,7 +75,22 @@ block_offsets_kernel(const int64_t* __restrict__ offs, int64_t batch, int64_t to
   for (int64_t i = carry_sh + tid; i <= n_out; i += kThreads) out[i] = total;
 }
 
+// (cos, sin) of the rotary angle p * base^(-2i/dim) for p < npos and i < dim/2
+__global__ void rope_table_kernel(float2* __restrict__ table, int npos, int half, double base) {
+  const int idx = blockIdx.x * blockDim.x + threadIdx.x;
+  if (idx >= npos * half) return;
+  const int p = idx / half, i = idx % half;
+  const double theta = (double)p * pow(base, -2.0 * (double)i / (double)(2 * half));
+  table[idx] = make_float2((float)cos(theta), (float)sin(theta));
+}
+
 }  // namespace
+
+cudaError_t launch_rope_table(float2* table, int npos, int dim, double base, cudaStream_t s) {
+  const int n = npos * (dim / 2);
+  rope_table_kernel<<<(n + 255) / 256, 256, 0, s>>>(table, npos, dim / 2, base);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_block_offsets(const int64_t* offs, int64_t batch, int64_t total, int block,
                                  int64_t* out, int64_t n_out, cudaStream_t s) {

@@ -57,6 +57,11 @@ struct Problem {
   float scale;
   int causal;
   int act;
+  // Rotary position embedding of q and k (BlockAttention), or nullptr: (cos, sin) of the
+  // angle of position p and pair i at rope[p * (dim_qk/2) + i], for p < rope_npos.  Rows
+  // are at the position of their index inside their sequence.
+  const float2* rope;
+  int rope_npos;
 };
 
 // Carve-up of the caller's workspace.
@@ -109,6 +114,10 @@ cudaError_t launch_pooled_broadcast(int64_t batch, int32_t m, int64_t row_bytes,
                                     void* q_rep, int64_t* offs_q, cudaStream_t s);
 cudaError_t launch_pooled_reduce(int dtype, int64_t batch, int64_t per_seq_elems, const void* dq_rep,
                                  void* dq, cudaStream_t s);
+
+// The rotary embedding's (cos, sin) table: npos positions by dim/2 pairs, angle
+// p * base^(-2i/dim), computed in double precision.
+cudaError_t launch_rope_table(float2* table, int npos, int dim, double base, cudaStream_t s);
 
 // BlockAttention: the offsets of the fixed `block`-row blocks of every sequence, then empty
 // sequences up to n_out (n_out + 1 entries); out[0] = -1 for offsets that are not valid.

@@ -150,7 +150,8 @@ struct KvLayout {
 enum : uint32_t {
   KV_KFULL = 0, KV_KEMPTY = 1, KV_VFULL = 2, KV_VEMPTY = 3, KV_QFULL = 4, KV_QEMPTY = 8,
   KV_OFULL = 12, KV_OEMPTY = 16, KV_RSFULL = 20, KV_SFULL = 24, KV_SEMPTY = 26, KV_DPFULL = 28,
-  KV_PDSFULL = 30, KV_KDONE = 32, KV_ACCFULL = 34, KV_ACCEMPTY = 35, KV_DRAIN = 36, KV_COUNT = 38
+  KV_PDSFULL = 30, KV_KDONE = 32, KV_ACCFULL = 34, KV_ACCEMPTY = 35, KV_DRAIN = 36, KV_KREADY = 38,
+  KV_QREADY = 39, KV_COUNT = 43
 };
 static_assert(8 * KV_COUNT + 8 <= 512, "mbarriers, TMEM slot and abort flag in front of the row terms");
 
@@ -222,7 +223,39 @@ using KvGroups = Groups<ACT == kActSoftmax ? 2 : 4, 1>;
 template <int ACT>
 using QGroups = Groups<ACT == kActSoftmax ? 2 : 4, 1>;
 
-template <int DQK, int DV, int ACT, bool CAUSAL>
+// Rotary embedding (BlockAttention), done by the compute warps: the next non-empty item
+// of the CTA's list (index rot_next, advanced) has its tiles rotated once they have
+// landed, and signalled ready (one arrival per compute warp).  rot_cnt counts the items
+// rotated, which fixes their ring stages (every item of the rotary kernels has one step).
+// Warp wi of the nw compute warps takes its share of the rows.  False if a wait gave up.
+template <int DQK, int NQ, bool CAUSAL, class L>
+__device__ __forceinline__ bool kv_rotate_next(int& rot_next, uint32_t& rot_cnt, const WorkItem* list,
+                                               int n_items, uint32_t raw, uint32_t sb, const Problem& p,
+                                               int wi, int nw, int lane, volatile int* abort,
+                                               int* status) {
+  auto bar = [&](uint32_t i) { return raw + 8u * i; };
+  while (rot_next < n_items && load_item(list, rot_next).cost == 0) rot_next += gridDim.x;
+  if (rot_next >= n_items) return true;
+  const WorkItem x = load_item(list, rot_next);
+  rot_next += gridDim.x;
+  const int key0 = x.tile * TILE, row0 = (CAUSAL ? key0 / KSTEP : 0) * KSTEP;
+  const uint32_t qs = rot_cnt % NQ;
+  if (!mbar_wait(bar(KV_KFULL), rot_cnt & 1, abort, status) ||
+      !mbar_wait(bar(KV_QFULL + qs), (rot_cnt / NQ) & 1, abort, status))
+    return false;
+  rope_rotate_share<DQK>(sb + L::K_OFF, rope_rows(key0, x.lk, p.rope_npos), key0, p.rope, wi, nw, lane);
+  rope_rotate_share<DQK>(sb + L::Q_OFF + qs * L::Q_BYTES, rope_rows(row0, x.lq, p.rope_npos), row0, p.rope,
+                         wi, nw, lane);
+  __syncwarp();
+  if (lane == 0) {
+    mbar_arrive(bar(KV_KREADY));
+    mbar_arrive(bar(KV_QREADY + qs));
+  }
+  ++rot_cnt;
+  return true;
+}
+
+template <int DQK, int DV, int ACT, bool CAUSAL, bool ROPE>
 __global__ void __launch_bounds__(KvGroups<ACT>::kThreads, 1)
 tc_dkdv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
@@ -277,6 +310,9 @@ tc_dkdv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
     mbar_init(bar(KV_ACCEMPTY), kCompute);
     mbar_init(bar(KV_DRAIN), 1);      // issuer A's exit drain
     mbar_init(bar(KV_DRAIN + 1), 1);  // issuer B's exit drain
+    // rotated K and Q tiles (rotary embedding): one arrival per compute warp
+    mbar_init(bar(KV_KREADY), kCompute / 32);
+    for (int s = 0; s < NQ; ++s) mbar_init(bar(KV_QREADY + s), kCompute / 32);
     *abort = 0;
     fence_mbar_init();
   }
@@ -288,6 +324,12 @@ tc_dkdv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
   // TMEM columns: dK [0,128), dV [128,256), step buffers X0 [256,384), X1 [384,512)
   constexpr uint32_t T_DK = 0, T_DV = 128, T_X = 256;
 
+  // Rotary embedding of Q and K (BlockAttention): the compute warps rotate each item's K
+  // and Q tiles in shared memory once they have landed and signal them ready; issuer A
+  // waits for that instead of the loads.  Its items are blocks of at most 64 rows, so
+  // each has exactly one step; the compute warps rotate the next item's tiles right after
+  // the current item's step, while its gradient products run.
+  constexpr bool rope = ROPE;
   if (warp == 0) {
     // ------------------------------------------------------------ producer: K and Q
     // Two producers, so that neither ring waits behind a load of the other: warp 0
@@ -415,8 +457,10 @@ tc_dkdv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
         const uint32_t b = c.g & 1;
         const uint32_t st = chain_p ? c.q % NQ : c.q % NO;
         const uint32_t ph = chain_p ? (c.q / NQ) & 1 : (c.q / NO) & 1;
-        if ((c.j == 0 && !mbar_wait(bar(chain_p ? KV_KFULL : KV_VFULL), c.kv & 1, abort, status)) ||
-            !mbar_wait(bar((chain_p ? KV_QFULL : KV_OFULL) + st), ph, abort, status) ||
+        const uint32_t kbar = chain_p ? (rope ? KV_KREADY : KV_KFULL) : KV_VFULL;
+        const uint32_t qbar = chain_p ? (rope ? KV_QREADY : KV_QFULL) : KV_OFULL;
+        if ((c.j == 0 && !mbar_wait(bar(kbar), c.kv & 1, abort, status)) ||
+            !mbar_wait(bar(qbar + st), ph, abort, status) ||
             (chain_p && !mbar_wait(bar(KV_KDONE + b), ((c.g >> 1) & 1) ^ 1, abort, status)) ||
             (!chain_p && !mbar_wait(bar(KV_SEMPTY + b), (c.g >> 1) & 1, abort, status)))
           return false;
@@ -519,12 +563,14 @@ tc_dkdv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
     // item's first dV / dK wait for it (ACCEMPTY).
     bool pend = false, pend_key_ok = false;
     int64_t pend_krow = 0;
+    int pend_kpos = 0;  // key index inside its sequence: the rotary embedding's position
     auto epilogue = [&]() -> bool {
       if (!mbar_wait(bar(KV_ACCFULL), a_it & 1, abort, status)) return false;
       ++a_it;
       tc_fence_after();
       if constexpr (Gr::G == 4) {
         // one half of dK or of dV, through an array of exactly its columns
+        // (four groups serve SiLU/L only, which has no rotary variant)
         auto drain = [&](auto cols, uint32_t t_acc, __nv_bfloat16* dst, float f) {
           constexpr int NC = decltype(cols)::value;
           float x[NC];
@@ -554,6 +600,9 @@ tc_dkdv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
         tmem_wait_ld();
         tc_fence_before();
         mbar_arrive(bar(KV_ACCEMPTY));
+        // dK with the rotary embedding: the gradient of the rotated keys turned back
+        if (rope && pend_key_ok && pend_kpos < p.rope_npos)
+          rope_unrotate_row<DQK / 2>(x, grp * (DQK / 2), pend_kpos, DQK, p.rope);
         if (pend_key_ok) {
 #pragma unroll
           for (int c = 0; c < DQK / 64; ++c)
@@ -566,6 +615,15 @@ tc_dkdv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
       pend = false;
       return true;
     };
+    // rotary embedding: the next non-empty item to rotate (list index) and the count of
+    // items rotated so far (which fixes its K and Q stages)
+    int rot_next = blockIdx.x;
+    uint32_t rot_cnt = 0;
+    if constexpr (ROPE) {
+      if (!kv_rotate_next<DQK, NQ, CAUSAL, L>(rot_next, rot_cnt, list, n_items, raw, sb, p, warp - 2,
+                                               kCompute / 32, lane, abort, status))
+        ok = false;
+    }
     WorkItem nxt = blockIdx.x < (unsigned)n_items ? load_item(list, blockIdx.x) : WorkItem{};
     for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
       const WorkItem w = nxt;
@@ -575,6 +633,12 @@ tc_dkdv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
       const int64_t k0 = w.k0;
       const int Lq = w.lq, Lk = w.lk;
       const int j = key0 + r;  // key index inside the sequence
+      if (rope && n > 1) {  // the rotary kernels take items of one step only
+        if (lane == 0) atomicExch(status, (int)JFA_ERR_UNSUPPORTED);
+        *abort = 1;
+        ok = false;
+        break;
+      }
       const float inv_len = 1.0f / (float)max(Lq, 1);
       const float2 hl = make_float2(0.5f * inv_len, 0.5f * inv_len);
       const float2 il = make_float2(inv_len, inv_len);
@@ -592,6 +656,13 @@ tc_dkdv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
           if (!mbar_wait(bar(KV_DPFULL + b), (s_it >> 1) & 1, abort, status)) { ok = false; break; }
           mbar_arrive(bar(KV_PDSFULL + b));
           if (pend && !epilogue()) { ok = false; break; }
+          if constexpr (ROPE) {  // the next item's K and Q tiles
+            if (!kv_rotate_next<DQK, NQ, CAUSAL, L>(rot_next, rot_cnt, list, n_items, raw, sb, p, warp - 2,
+                                                     kCompute / 32, lane, abort, status)) {
+              ok = false;
+              break;
+            }
+          }
           continue;
         }
         float sv[HC];
@@ -659,6 +730,13 @@ tc_dkdv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
         tc_fence_before();
         mbar_arrive(bar(KV_PDSFULL + b));
         if (pend && !epilogue()) { ok = false; break; }
+        if constexpr (ROPE) {  // the next item's K and Q tiles
+            if (!kv_rotate_next<DQK, NQ, CAUSAL, L>(rot_next, rot_cnt, list, n_items, raw, sb, p, warp - 2,
+                                                     kCompute / 32, lane, abort, status)) {
+              ok = false;
+              break;
+            }
+          }
       }
       if (!ok) break;
       // ---------------------------------------------------------- epilogue (deferred)
@@ -669,6 +747,7 @@ tc_dkdv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
         pend = true;
         pend_key_ok = key_ok;
         pend_krow = krow;
+        if constexpr (ROPE) pend_kpos = j;
       } else if (key_ok) {
         const float z[32] = {0.f};
         const bool do_k = Gr::G == 2 || grp < 2, do_v = Gr::G == 2 || grp >= 2;
@@ -736,11 +815,40 @@ struct QLayout {
 enum : uint32_t {
   Q_QFULL = 0, Q_QEMPTY = 2, Q_OFULL = 4, Q_OEMPTY = 6, Q_KFULL = 8, Q_KEMPTY = 14, Q_VFULL = 20,
   Q_VEMPTY = 24, Q_SFULL = 28, Q_DPFULL = 30, Q_DPEMPTY = 31, Q_DSFULL = 32, Q_ACCFULL = 34,
-  Q_ACCEMPTY = 35, Q_DRAIN = 36, Q_COUNT = 38
+  Q_ACCEMPTY = 35, Q_DRAIN = 36, Q_QREADY = 38, Q_KREADY = 40, Q_COUNT = 46
 };
 static_assert(8 * Q_COUNT + 8 <= 512, "mbarriers, TMEM slot and abort flag in front of the tiles");
 
-template <int DQK, int DV, int ACT, bool CAUSAL>
+// The dQ pass's counterpart of kv_rotate_next: the item's Q tile and its one K tile.
+template <int DQK, int NQ, int NK, class L>
+__device__ __forceinline__ bool q_rotate_next(int& rot_next, uint32_t& rot_cnt, const WorkItem* list,
+                                              int n_items, uint32_t raw, uint32_t sb, const Problem& p,
+                                              int wi, int nw, int lane, volatile int* abort,
+                                              int* status) {
+  auto bar = [&](uint32_t i) { return raw + 8u * i; };
+  while (rot_next < n_items && load_item(list, rot_next).cost == 0) rot_next += gridDim.x;
+  if (rot_next >= n_items) return true;
+  const WorkItem x = load_item(list, rot_next);
+  rot_next += gridDim.x;
+  const int row0 = x.tile * TILE;
+  const uint32_t qs = rot_cnt % NQ, ks = rot_cnt % NK;
+  if (!mbar_wait(bar(Q_QFULL + qs), (rot_cnt / NQ) & 1, abort, status) ||
+      !mbar_wait(bar(Q_KFULL + ks), (rot_cnt / NK) & 1, abort, status))
+    return false;
+  rope_rotate_share<DQK>(sb + L::Q_OFF + qs * L::Q_BYTES, rope_rows(row0, x.lq, p.rope_npos), row0, p.rope,
+                         wi, nw, lane);
+  rope_rotate_share<DQK>(sb + L::K_OFF + ks * L::K_BYTES, rope_rows(0, x.lk, p.rope_npos), 0, p.rope, wi, nw,
+                         lane);
+  __syncwarp();
+  if (lane == 0) {
+    mbar_arrive(bar(Q_QREADY + qs));
+    mbar_arrive(bar(Q_KREADY + ks));
+  }
+  ++rot_cnt;
+  return true;
+}
+
+template <int DQK, int DV, int ACT, bool CAUSAL, bool ROPE>
 __global__ void __launch_bounds__(QGroups<ACT>::kThreads, 1)
 tc_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
              const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
@@ -795,6 +903,9 @@ tc_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
     mbar_init(bar(Q_ACCEMPTY), kCompute);
     mbar_init(bar(Q_DRAIN), 1);      // issuer A's exit drain
     mbar_init(bar(Q_DRAIN + 1), 1);  // issuer B's exit drain
+    // rotated Q and K tiles (rotary embedding): one arrival per compute warp
+    for (int s = 0; s < NQ; ++s) mbar_init(bar(Q_QREADY + s), kCompute / 32);
+    for (int s = 0; s < NK; ++s) mbar_init(bar(Q_KREADY + s), kCompute / 32);
     *abort = 0;
     fence_mbar_init();
   }
@@ -807,6 +918,12 @@ tc_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
   constexpr uint32_t T_DQ = 0, T_DP = 256;
   auto t_s = [](uint32_t b) { return b ? 384u : 128u; };
 
+  // Rotary embedding of Q and K (BlockAttention): the compute warps rotate each item's K
+  // and Q tiles in shared memory once they have landed and signal them ready; issuer A
+  // waits for that instead of the loads.  Its items are blocks of at most 64 rows, so
+  // each has exactly one step; the compute warps rotate the next item's tiles right after
+  // the current item's step, while its gradient products run.
+  constexpr bool rope = ROPE;
   if (warp == 0 || warp == Gr::kProducer2) {
     // ------------------------------------------------------------ producers
     // warp 0: the item's Q tile, then K(0), K(1), ...; the second producer: its dO
@@ -880,12 +997,12 @@ tc_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
           const int n = w.cost;
           if (n == 0) continue;
           const uint32_t qs = q_it % NQ;
-          if (!mbar_wait(bar(Q_QFULL + qs), (q_it / NQ) & 1, abort, status)) break;
+          if (!mbar_wait(bar((rope ? Q_QREADY : Q_QFULL) + qs), (q_it / NQ) & 1, abort, status)) break;
           const uint32_t q_tile = sb + L::Q_OFF + qs * L::Q_BYTES;
           const uint32_t k_base = k_it, s_base = s_it;
           auto issue_s = [&](int i) {  // S(i) = Q K(i)^T into buffer (s_base + i) & 1
             const uint32_t kk_it = k_base + i, kst = kk_it % NK;
-            if (!mbar_wait(bar(Q_KFULL + kst), (kk_it / NK) & 1, abort, status)) return false;
+            if (!mbar_wait(bar((rope ? Q_KREADY : Q_KFULL) + kst), (kk_it / NK) & 1, abort, status)) return false;
             __syncwarp();  // converged for elect.sync
             tc_fence_after();
             const uint32_t k_tile = sb + L::K_OFF + kst * L::K_BYTES;
@@ -935,8 +1052,8 @@ tc_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
         // S(c.g) = Q K(c.g)^T into buffer c.g & 1; the item's Q tile is stage c.kv % NQ
         auto issue_s = [&](const StepCursor& c) -> bool {
           const uint32_t qs = c.kv % NQ, kst = c.g % NK;
-          if ((c.j == 0 && !mbar_wait(bar(Q_QFULL + qs), (c.kv / NQ) & 1, abort, status)) ||
-              !mbar_wait(bar(Q_KFULL + kst), (c.g / NK) & 1, abort, status))
+          if ((c.j == 0 && !mbar_wait(bar((rope ? Q_QREADY : Q_QFULL) + qs), (c.kv / NQ) & 1, abort, status)) ||
+              !mbar_wait(bar((rope ? Q_KREADY : Q_KFULL) + kst), (c.g / NK) & 1, abort, status))
             return false;
           __syncwarp();  // converged for elect.sync
           tc_fence_after();
@@ -1060,6 +1177,7 @@ tc_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
     // product waits for it (ACCEMPTY).
     bool pend = false, pend_row_ok = false;
     int64_t pend_orow = 0;
+    int pend_pos = 0;  // row index inside its sequence: the rotary embedding's position
     auto epilogue = [&]() -> bool {
       if (!mbar_wait(bar(Q_ACCFULL), a_it & 1, abort, status)) return false;
       ++a_it;
@@ -1071,6 +1189,9 @@ tc_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
         tmem_wait_ld();
         tc_fence_before();
         mbar_arrive(bar(Q_ACCEMPTY));
+        // dQ with the rotary embedding: the gradient of the rotated queries turned back
+        if (rope && pend_row_ok && pend_pos < p.rope_npos)
+          rope_unrotate_row<CQ>(x, grp * CQ, pend_pos, DQK, p.rope);
         if (pend_row_ok) {
 #pragma unroll
           for (int c = 0; c < CQ / 32; ++c) store_row_bf16(dq + pend_orow * DQK + grp * CQ + 32 * c, x + 32 * c, p.scale);
@@ -1082,6 +1203,15 @@ tc_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
       pend = false;
       return true;
     };
+    // rotary embedding: the next non-empty item to rotate (list index) and the count of
+    // items rotated so far (which fixes its Q and K stages)
+    int rot_next = blockIdx.x;
+    uint32_t rot_cnt = 0;
+    if constexpr (ROPE) {
+      if (!q_rotate_next<DQK, NQ, NK, L>(rot_next, rot_cnt, list, n_items, raw, sb, p, warp - 2,
+                                          kCompute / 32, lane, abort, status))
+        ok = false;
+    }
     WorkItem nxt = blockIdx.x < (unsigned)n_items ? load_item(list, blockIdx.x) : WorkItem{};
     for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
       const WorkItem w = nxt;
@@ -1092,6 +1222,12 @@ tc_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
       const int Lq = w.lq, Lk = w.lk;
       const int i = row0 + r;
       const bool row_ok = i < Lq;
+      if (rope && n > 1) {  // the rotary kernels take items of one step only
+        if (lane == 0) atomicExch(status, (int)JFA_ERR_UNSUPPORTED);
+        *abort = 1;
+        ok = false;
+        break;
+      }
       const float inv_len = 1.0f / (float)max(Lq, 1);
       const float2 hl = make_float2(0.5f * inv_len, 0.5f * inv_len);
       float2 rsv = make_float2(0.f, 0.f);
@@ -1155,6 +1291,13 @@ tc_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
         tc_fence_before();
         mbar_arrive(bar(Q_DSFULL + sbuf));
         if (pend && !epilogue()) { ok = false; break; }
+        if constexpr (ROPE) {  // the next item's Q and K tiles
+          if (!q_rotate_next<DQK, NQ, NK, L>(rot_next, rot_cnt, list, n_items, raw, sb, p, warp - 2,
+                                              kCompute / 32, lane, abort, status)) {
+            ok = false;
+            break;
+          }
+        }
       }
       if (!ok) break;
       const int64_t orow = (q0 + i) * p.heads + h;
@@ -1163,6 +1306,7 @@ tc_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
         pend = true;
         pend_row_ok = row_ok;
         pend_orow = orow;
+        if constexpr (ROPE) pend_pos = i;
       } else if (row_ok) {
         const float z[32] = {0.f};
         if (drains) {
@@ -1199,10 +1343,10 @@ bool make_maps(const Problem& p, const void* q, const void* k, const void* v, co
          make_tile_map(&m->k, kk, tk, cq, 64, TILE) && make_tile_map(&m->v, vv, tk, cv, 64, TILE);
 }
 
-template <int DQK, int DV, int ACT, bool CAUSAL>
+template <int DQK, int DV, int ACT, bool CAUSAL, bool ROPE = false>
 cudaError_t dkdv_t(const Maps& m, const Problem& p, const float2* rowstat, void* dk, void* dv,
                    const Workspace& ws, cudaStream_t s) {
-  auto kern = tc_dkdv_kernel<DQK, DV, ACT, CAUSAL>;
+  auto kern = tc_dkdv_kernel<DQK, DV, ACT, CAUSAL, ROPE>;
   constexpr uint32_t smem = KvLayout<DQK, DV>::SMEM;
   cudaError_t e = kernel_setup((const void*)kern, KvGroups<ACT>::kThreads, smem);
   if (e != cudaSuccess) return e;
@@ -1211,10 +1355,10 @@ cudaError_t dkdv_t(const Maps& m, const Problem& p, const float2* rowstat, void*
   return cudaGetLastError();
 }
 
-template <int DQK, int DV, int ACT, bool CAUSAL>
+template <int DQK, int DV, int ACT, bool CAUSAL, bool ROPE = false>
 cudaError_t dq_t(const Maps& m, const Problem& p, const float2* rowstat, void* dq,
                  const Workspace& ws, cudaStream_t s) {
-  auto kern = tc_dq_kernel<DQK, DV, ACT, CAUSAL>;
+  auto kern = tc_dq_kernel<DQK, DV, ACT, CAUSAL, ROPE>;
   constexpr uint32_t smem = QLayout<DQK, DV>::SMEM;
   cudaError_t e = kernel_setup((const void*)kern, QGroups<ACT>::kThreads, smem);
   if (e != cudaSuccess) return e;
@@ -1226,6 +1370,14 @@ cudaError_t dq_t(const Maps& m, const Problem& p, const float2* rowstat, void* d
 #define JFA_TC_BWD_DISPATCH(FN, ...)                                                          \
   do {                                                                                        \
     const bool sm_ = p.act == kActSoftmax, c_ = p.causal != 0;                               \
+    if (p.rope != nullptr) { /* rotary embedding: softmax, Dqk = Dv */                       \
+      if (!sm_ || p.dim_qk != p.dim_v) return cudaErrorInvalidValue;                         \
+      if (p.dim_qk == 128) return c_ ? FN<128, 128, kActSoftmax, true, true>(__VA_ARGS__)     \
+                                     : FN<128, 128, kActSoftmax, false, true>(__VA_ARGS__);   \
+      if (p.dim_qk == 64) return c_ ? FN<64, 64, kActSoftmax, true, true>(__VA_ARGS__)        \
+                                    : FN<64, 64, kActSoftmax, false, true>(__VA_ARGS__);      \
+      return cudaErrorInvalidValue;                                                           \
+    }                                                                                         \
     if (p.dim_qk == 128 && p.dim_v == 128) {                                                  \
       if (sm_) return c_ ? FN<128, 128, kActSoftmax, true>(__VA_ARGS__)                       \
                          : FN<128, 128, kActSoftmax, false>(__VA_ARGS__);                     \

@@ -67,9 +67,9 @@ struct FwdLayout {
   static constexpr uint32_t Q_BYTES = DQK / 64 * 16384;  // one 128-row tile
   static constexpr uint32_t K_BYTES = DQK / 64 * 16384;  // one 128-key tile
   static constexpr uint32_t V_BYTES = DV / 64 * 16384;
-  // In front of the tiles: mbarriers, TMEM slot and abort flag (384 bytes), then the
+  // In front of the tiles: mbarriers, TMEM slot and abort flag (512 bytes), then the
   // row statistics exchanged by the two softmax warpgroups ([2 steps][128 rows][2]).
-  static constexpr uint32_t RED_OFF = 384;
+  static constexpr uint32_t RED_OFF = 512;
   static constexpr uint32_t RED_BYTES = 2 * BM * 2 * 4;
   static constexpr uint32_t SMALL = RED_OFF + RED_BYTES;
   static constexpr uint32_t TILE0 = (SMALL + 1023) / 1024 * 1024;  // for a 1 KB-aligned base
@@ -92,17 +92,50 @@ struct FwdLayout {
 enum : uint32_t {
   B_QFULL = 0, B_QEMPTY = 2, B_KFULL = 4, B_KEMPTY = 10, B_VFULL = 16, B_VEMPTY = 22,
   B_SFULL = 28, B_PFULL = 30, B_PEMPTY = 32, B_OFULL = 34, B_OEMPTY = 35, B_RED = 36, B_REDL = 38,
-  B_DRAIN = 40, B_HOLD = 42, B_COUNT = 43
+  B_DRAIN = 40, B_HOLD = 42, B_QREADY = 43, B_KREADY = 45, B_COUNT = 51
 };
 static_assert(8 * B_COUNT + 8 <= FwdLayout<128, 128>::RED_OFF, "mbarriers, TMEM slot and abort flag in front");
 constexpr uint32_t T_S = 0, T_O = 256, T_P = 384;  // S: 2 x 128 columns; P: 2 x 64 columns
+
+// Rotary embedding (BlockAttention), done by the compute warps: the next non-empty item
+// of the CTA's list (index rot_next, advanced) has its Q and K tiles rotated once they
+// have landed, and signalled ready (one arrival per compute warp).  rot_cnt counts the
+// items rotated, which fixes their ring stages (every item of the rotary kernels has one
+// step).  Warp wi of the nw compute warps takes its share of the rows.  False if a wait
+// gave up.
+template <int DQK, int NK, class L>
+__device__ __forceinline__ bool fwd_rotate_next(int& rot_next, uint32_t& rot_cnt, const WorkItem* list,
+                                                int n_items, uint32_t raw, uint32_t sb, const Problem& p,
+                                                int wi, int nw, int lane, volatile int* abort,
+                                                int* status) {
+  auto bar = [&](uint32_t i) { return raw + 8u * i; };
+  while (rot_next < n_items && load_item(list, rot_next).cost == 0) rot_next += gridDim.x;
+  if (rot_next >= n_items) return true;
+  const WorkItem x = load_item(list, rot_next);
+  rot_next += gridDim.x;
+  const uint32_t qs = rot_cnt % L::NQB, ks = rot_cnt % NK;
+  if (!mbar_wait(bar(B_QFULL + qs), (rot_cnt / L::NQB) & 1, abort, status) ||
+      !mbar_wait(bar(B_KFULL + ks), (rot_cnt / NK) & 1, abort, status))
+    return false;
+  rope_rotate_share<DQK>(sb + L::Q_OFF + qs * L::Q_BYTES, rope_rows(x.tile * BM, x.lq, p.rope_npos),
+                         x.tile * BM, p.rope, wi, nw, lane);
+  rope_rotate_share<DQK>(sb + L::K_OFF + ks * L::K_BYTES, rope_rows(0, x.lk, p.rope_npos), 0, p.rope, wi, nw,
+                         lane);
+  __syncwarp();
+  if (lane == 0) {
+    mbar_arrive(bar(B_QREADY + qs));
+    mbar_arrive(bar(B_KREADY + ks));
+  }
+  ++rot_cnt;
+  return true;
+}
 
 // Test hook (jfa_test_hold): while nonzero, the S issuer of every CTA first waits on
 // B_HOLD, on which no role ever arrives, so that its bounded wait gives up before any
 // MMA is issued and the CTA leaves through its abort path.  Zero unless a test sets it.
 __device__ int g_test_hold = 0;
 
-template <int DQK, int DV, int ACT, bool CAUSAL>
+template <int DQK, int DV, int ACT, bool CAUSAL, bool ROPE>
 __global__ void __launch_bounds__(FwdRoles<ACT>::kThreads, 1)
 tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
               const __grid_constant__ CUtensorMap tm_v, const Problem p,
@@ -156,6 +189,9 @@ tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     mbar_init(bar(B_DRAIN), 1);      // S issuer's exit drain
     mbar_init(bar(B_DRAIN + 1), 1);  // PV issuer's exit drain
     mbar_init(bar(B_HOLD), 1);       // test hook: nothing arrives on it
+    // rotated Q and K tiles (rotary embedding): one arrival per compute warp
+    for (int s = 0; s < 2; ++s) mbar_init(bar(B_QREADY + s), R::kCompute / 32);
+    for (int s = 0; s < NK; ++s) mbar_init(bar(B_KREADY + s), R::kCompute / 32);
     *abort = 0;
     fence_mbar_init();
   }
@@ -165,6 +201,12 @@ tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
+  // Rotary embedding of Q and K (BlockAttention): the compute warps rotate each item's Q
+  // and K tiles in shared memory once they have landed and signal them ready; the S
+  // issuer waits for that instead of the loads.  Its items are blocks of at most 64
+  // rows, so each has exactly one step; the compute warps rotate the next item's tiles
+  // before they turn to the current item's scores, while its S product runs.
+  constexpr bool rope = ROPE;
   if (warp == kProducerWarp || warp == kVWarp) {
     // ------------------------------------------------------------ TMA producers
     // warp 8: each item's Q tile, then K(0), K(1), ...; warp 11: V(0), V(1), ...
@@ -241,13 +283,13 @@ tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         const int n = w.cost;
         if (n == 0) continue;
         const uint32_t qs = q_it % L::NQB;
-        if (!mbar_wait(bar(B_QFULL + qs), (q_it / L::NQB) & 1, abort, status)) break;
+        if (!mbar_wait(bar((rope ? B_QREADY : B_QFULL) + qs), (q_it / L::NQB) & 1, abort, status)) break;
         const uint32_t q_tile = sb + L::Q_OFF + qs * L::Q_BYTES;
         for (int i = 0; i < n; ++i, ++gs, ++k_it) {
           // S(gs) goes into the buffer of S(gs - 2): free once the softmax has written P(gs - 2)
           const uint32_t b = gs & 1, kst = k_it % NK;
           if (!mbar_wait(bar(B_PFULL + b), ((gs >> 1) & 1) ^ 1, abort, status) ||
-              !mbar_wait(bar(B_KFULL + kst), (k_it / NK) & 1, abort, status)) {
+              !mbar_wait(bar((rope ? B_KREADY : B_KFULL) + kst), (k_it / NK) & 1, abort, status)) {
             ok = false;
             break;
           }
@@ -341,12 +383,36 @@ tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
       pend = false;
       return true;
     };
+    // rotary embedding: the next non-empty item to rotate (list index) and the count of
+    // items rotated so far (which fixes its Q and K stages)
+    int rot_next = blockIdx.x;
+    uint32_t rot_cnt = 0;
+    if constexpr (ROPE) {
+      if (!fwd_rotate_next<DQK, NK, L>(rot_next, rot_cnt, list, n_items, raw, sb, p, warp, R::kCompute / 32,
+                                        lane, abort, status))
+        ok = false;
+    }
     WorkItem nxt = blockIdx.x < (unsigned)n_items ? load_item(list, blockIdx.x) : WorkItem{};
     for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
       const WorkItem w = nxt;
       if (it + (int)gridDim.x < n_items) nxt = load_item(list, it + gridDim.x);
       const int n = w.cost, h = w.h;
       const int Lq = w.lq, Lk = w.lk;
+      if (rope && n > 1) {  // the rotary kernels take items of one step only
+        if (lane == 0) atomicExch(status, (int)JFA_ERR_UNSUPPORTED);
+        *abort = 1;
+        ok = false;
+        break;
+      }
+      // the next item's Q and K tiles, while S of this item runs (its rings are deep
+      // enough that they have landed)
+      if constexpr (ROPE) {
+        if (n > 0 && !fwd_rotate_next<DQK, NK, L>(rot_next, rot_cnt, list, n_items, raw, sb, p, warp,
+                                                  R::kCompute / 32, lane, abort, status)) {
+          ok = false;
+          break;
+        }
+      }
       const int i = w.tile * BM + r;
       const float inv_len = 1.0f / (float)max(Lq, 1);
       float m = -INFINITY, l = 0.f;
@@ -494,11 +560,11 @@ tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
   }
 }
 
-template <int DQK, int DV, int ACT, bool CAUSAL>
+template <int DQK, int DV, int ACT, bool CAUSAL, bool ROPE = false>
 cudaError_t launch_fwd_t(const Problem& p, const CUtensorMap& mq, const CUtensorMap& mk,
                          const CUtensorMap& mv, void* o, float* lse, const Workspace& ws,
                          cudaStream_t s) {
-  auto kern = tc_fwd_kernel<DQK, DV, ACT, CAUSAL>;
+  auto kern = tc_fwd_kernel<DQK, DV, ACT, CAUSAL, ROPE>;
   constexpr uint32_t smem = FwdLayout<DQK, DV>::SMEM;
   constexpr int threads = FwdRoles<ACT>::kThreads;
   cudaError_t e = kernel_setup((const void*)kern, threads, smem);
@@ -511,6 +577,14 @@ template <int DQK, int DV>
 cudaError_t launch_fwd_d(const Problem& p, const CUtensorMap& mq, const CUtensorMap& mk,
                          const CUtensorMap& mv, void* o, float* lse, const Workspace& ws,
                          cudaStream_t s) {
+  if (p.rope != nullptr) {  // rotary embedding: softmax self-attention with Dqk = Dv only
+    if constexpr (DQK == DV) {
+      if (p.act == kActSoftmax)
+        return p.causal ? launch_fwd_t<DQK, DV, kActSoftmax, true, true>(p, mq, mk, mv, o, lse, ws, s)
+                        : launch_fwd_t<DQK, DV, kActSoftmax, false, true>(p, mq, mk, mv, o, lse, ws, s);
+    }
+    return cudaErrorInvalidValue;
+  }
   if (p.act == kActSoftmax)
     return p.causal ? launch_fwd_t<DQK, DV, kActSoftmax, true>(p, mq, mk, mv, o, lse, ws, s)
                     : launch_fwd_t<DQK, DV, kActSoftmax, false>(p, mq, mk, mv, o, lse, ws, s);

@@ -374,6 +374,81 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
                : "memory");
 }
 
+__device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(addr)
+               : "memory");
+  return v;
+}
+
+// ---------------------------------------------------------------- rotary embedding
+// The pair (x0, x1) of a bf16x2 word turned by the angle with cosine c and sine s:
+// (x0 c - x1 s, x0 s + x1 c), rounded to bf16.
+__device__ __forceinline__ uint32_t rope_rotate_word(uint32_t w, float c, float s) {
+  const float x0 = __uint_as_float(w << 16), x1 = __uint_as_float(w & 0xffff0000u);
+  return pack_bf16(fmaf(x0, c, -x1 * s), fmaf(x0, s, x1 * c));
+}
+
+// Rotates rows [r0, r1) of a tile in shared memory in place by the rotary position
+// embedding: row r sits at position pos0 + r, and its columns (2i, 2i+1) turn by the
+// angle whose (cos, sin) is table[(pos0 + r) * (D/2) + i].  The tile is D/64 boxes of
+// 64 bf16 columns, 16 KB apart, each a stack of 128-byte-swizzled 8-row atoms (as a TMA
+// load with 128-byte swizzle writes them).  The lanes of the calling warp share the
+// rows' 16-byte chunks; each lane fences its writes to the async proxy, so that once the
+// warp has signalled a barrier, an MMA issued after waiting on it reads the rotated values.
+template <int D>
+__device__ __forceinline__ void rope_rotate_rows(uint32_t tile, int r0, int r1, int pos0,
+                                                 const float2* __restrict__ table, int lane) {
+  constexpr int kChunks = D / 8;  // 16-byte chunks per row
+  for (int idx = r0 * kChunks + lane; idx < r1 * kChunks; idx += 32) {
+    const int r = idx / kChunks, cc = idx % kChunks, a = cc >> 3, c = cc & 7;
+    const uint32_t addr = tile + a * 16384u + (r >> 3) * 1024 + (r & 7) * 128 + ((c ^ (r & 7)) << 4);
+    uint4 v = ld_shared_v4(addr);
+    const float4* tb = reinterpret_cast<const float4*>(table + (size_t)(pos0 + r) * (D / 2) + a * 32 + c * 4);
+    const float4 t01 = __ldg(tb), t23 = __ldg(tb + 1);
+    v.x = rope_rotate_word(v.x, t01.x, t01.y);
+    v.y = rope_rotate_word(v.y, t01.z, t01.w);
+    v.z = rope_rotate_word(v.z, t23.x, t23.y);
+    v.w = rope_rotate_word(v.w, t23.z, t23.w);
+    st_shared_v4(addr, v.x, v.y, v.z, v.w);
+  }
+  fence_proxy_async_smem();
+}
+
+// Warp wi of nw rotating warps takes its share of a tile's `rows` rows.
+template <int D>
+__device__ __forceinline__ void rope_rotate_share(uint32_t tile, int rows, int pos0,
+                                                  const float2* __restrict__ table, int wi, int nw,
+                                                  int lane) {
+  const int per = (rows + nw - 1) / nw;
+  const int r0 = min(rows, wi * per), r1 = min(rows, r0 + per);
+  rope_rotate_rows<D>(tile, r0, r1, pos0, table, lane);
+}
+
+// Rows of a 128-row tile starting at position pos0 that the rotation covers: the rows of
+// the sequence (len rows) that the table has positions for (npos).
+__device__ __forceinline__ int rope_rows(int pos0, int len, int npos) {
+  return max(0, min(128, min(len, npos) - pos0));
+}
+
+// The transpose of the rotation on n consecutive fp32 columns of one row (a gradient with
+// respect to rotated values back to the unrotated ones): columns col0 + 2t, col0 + 2t + 1
+// form the pair i = col0/2 + t, turned by the angle of position pos backwards.
+template <int N>
+__device__ __forceinline__ void rope_unrotate_row(float* x, int col0, int pos, int D,
+                                                  const float2* __restrict__ table) {
+  const float2* tb = table + (size_t)pos * (D / 2) + col0 / 2;
+#pragma unroll
+  for (int t = 0; t < N / 2; ++t) {
+    const float2 cs = __ldg(tb + t);
+    const float y0 = x[2 * t], y1 = x[2 * t + 1];
+    x[2 * t] = fmaf(y0, cs.x, y1 * cs.y);
+    x[2 * t + 1] = fmaf(y1, cs.x, -y0 * cs.y);
+  }
+}
+
 // Byte offset of 16-byte chunk `chunk` (0..7) of row `row` inside a stack of
 // 128-byte-swizzled atoms (8 rows x 128 bytes per atom).
 __device__ __forceinline__ uint32_t sw128_offset(uint32_t row, uint32_t chunk) {

@@ -140,7 +140,7 @@ def sampled_check(w: workloads.Workload, batch, got, idx, strict_o=True):
 
 
 def whole_batch_check(w: workloads.Workload, batch, got, seqs=None, max_rows=60000,
-                      strict_o=True):
+                      strict_o=True, oracle_fn=None):
     """Every sequence of a (full-size) batch against the oracle, at the tolerances above,
     with the error metrics taken over the whole batch (or over the sequences ``seqs``).
 
@@ -151,7 +151,8 @@ def whole_batch_check(w: workloads.Workload, batch, got, seqs=None, max_rows=600
     worst sequence for each tensor (largest max-abs error for O, largest relative L2 error
     among sequences with a nonzero reference for the gradients).  ``strict_o`` applies the
     plain O max-abs bound (the named workloads); otherwise it is scaled by
-    max(1, max |o|) as in ``compare``.
+    max(1, max |o|) as in ``compare``.  ``oracle_fn(w, q, k, v, do, offs_q, offs_k)``
+    replaces the plain oracle (for example BlockAttention with the rotary embedding).
     """
     oq, ok = np.asarray(batch["offs_q"]), np.asarray(batch["offs_k"])
     dev = batch["q"].device
@@ -174,7 +175,7 @@ def whole_batch_check(w: workloads.Workload, batch, got, seqs=None, max_rows=600
         q, do = to64(batch["q"][tq]), to64(batch["do"][tq])
         k, v = to64(batch["k"][tk]), to64(batch["v"][tk])
         sub_q, sub_k = workloads.offsets(lq), workloads.offsets(lk)
-        ref = run_oracle(w, q, k, v, do, sub_q, sub_k)
+        ref = (oracle_fn or run_oracle)(w, q, k, v, do, sub_q, sub_k)
         g = dict(o=to64(got["o"][tq]), dq=to64(got["dq"][tq]), dk=to64(got["dk"][tk]),
                  dv=to64(got["dv"][tk]))
         if ref["o"].size:

@@ -360,6 +360,78 @@ def test_full_size_block_workload():
     print("\nblock whole batch (%d blocks): %s" % (len(bo) - 1, fig))
 
 
+# ----------------------------------------------------------------------------- BlockAttention + RoPE
+def _block_rope_oracle(w, q, k, v, do, offs_q, offs_k):
+    import oracle
+
+    o, lse = oracle.block_rope_fwd(q, k, v, offs_q, scale=w.scale, causal=w.causal)
+    dq, dk, dv = oracle.block_rope_bwd(q, k, v, do, offs_q, scale=w.scale, causal=w.causal)
+    return dict(o=o, lse=lse, dq=dq, dk=dk, dv=dv)
+
+
+def _block_rope_gpu(batch, causal, ws=None):
+    import jagged_attention_recsys_gb300 as jfa
+
+    od = torch.as_tensor(batch["offs_q"], device="cuda")
+    q, k, v, do = batch["q"], batch["k"], batch["v"], batch["do"]
+    p = jfa.params_for(q, k, v, od, causal=causal)
+    ws = jfa.block_workspace(p) if ws is None else ws
+    o, lse = jfa.jfa_block_fwd(q, k, v, od, causal=causal, ws=ws, rope=True)
+    dq, dk, dv = jfa.jfa_block_bwd(q, k, v, o, lse, do, od, causal=causal, ws=ws, rope=True)
+    assert jfa.jfa_status_check(ws) == jfa.JFA_OK
+    return dict(o=o, lse=lse, dq=dq, dk=dk, dv=dv)
+
+
+@pytest.mark.parametrize("dim", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+def test_bf16_block_rope(dim, causal):
+    """BlockAttention with the fused rotary embedding against the oracle (RoFormer's rotation
+    of q and k, positions counted from each sequence's first row), lengths around block and
+    tile edges, and a sequence of many blocks."""
+    w = W(dim, dim, causal=causal)
+    batch = workloads.make_batch(w, TILE_EDGES + [0, 1000], seed=13, device="cuda")
+    got = _block_rope_gpu(batch, causal)
+    got = {n: to64(t) for n, t in got.items()}
+    ref = _block_rope_oracle(w, *(to64(batch[n]) for n in ("q", "k", "v", "do")), batch["offs_q"],
+                             batch["offs_k"])
+    compare(w, got, ref, fp32=False)
+
+
+def test_block_rope_differs_from_plain_block():
+    """The rotation changes the result (a kernel that skipped it would match plain
+    BlockAttention instead)."""
+    w = W(64, 64, causal=True)
+    batch = workloads.make_batch(w, [64, 40], seed=14, device="cuda")
+    got = _block_rope_gpu(batch, True)
+    import jagged_attention_recsys_gb300 as jfa
+
+    od = torch.as_tensor(batch["offs_q"], device="cuda")
+    o_plain, _ = jfa.jfa_block_fwd(batch["q"], batch["k"], batch["v"], od, causal=True)
+    torch.cuda.synchronize()
+    assert float((got["o"].float() - o_plain.float()).abs().max()) > 0.05
+
+
+def test_block_rope_rejects_fp32():
+    import jagged_attention_recsys_gb300 as jfa
+
+    q, k, v, do = workloads.values(70, 70, 2, 32, 32, F32, 0, "cuda")
+    od = torch.as_tensor(workloads.offsets([70]), device="cuda")
+    with pytest.raises(jfa.JfaError) as e:
+        jfa.jfa_block_fwd(q, k, v, od, rope=True)
+    assert e.value.code == jfa.JFA_ERR_UNSUPPORTED
+
+
+def test_full_size_block_rope_workload():
+    """BlockAttention with the rotary embedding over the causal workload's 1024 sequences
+    (H=8, D=128): every sequence against the oracle, error metrics over the whole batch."""
+    w = workloads.WORKLOADS["block_rope"]
+    batch = workloads.make_batch(w, device="cuda")
+    got = _block_rope_gpu(batch, True)
+    wb = W(128, 128, causal=True, heads=w.heads)
+    fig = whole_batch_check(wb, batch, got, oracle_fn=_block_rope_oracle)
+    print("\nblock_rope whole batch: %s" % fig)
+
+
 # ----------------------------------------------------------------------------- CUDA graphs
 @pytest.mark.parametrize("name", ["d64", "gdpa"])
 def test_cuda_graph_replay_matches_separate_calls(name):

@@ -26,6 +26,7 @@ Workloads (named by what they are):
 ``block``   BlockAttention over the causal workload's sequences (B=1024, lognormal lengths
             clipped to [1, 2048], H=8, D=128, bf16): every row attends only the keys of its
             own 64-row block, causally.
+``block_rope``  the same, with the rotary position embedding of q and k.
 """
 from __future__ import annotations
 
@@ -52,6 +53,7 @@ class Workload:
     cross: bool
     pooled: int = 0  # shared query rows per sequence (pooled attention); 0 = not pooled
     block: int = 0   # BlockAttention block length; 0 = whole sequences
+    rope: bool = False  # rotary position embedding of q and k (BlockAttention)
 
     @property
     def scale(self) -> float:
@@ -66,6 +68,8 @@ WORKLOADS = {
     "gdpa": Workload("gdpa", 256, 8, 128, 128, True, ACT_SILU_OVER_LEN, torch.bfloat16, False),
     "pooled": Workload("pooled", 512, 4, 128, 64, False, ACT_SOFTMAX, torch.bfloat16, True, 32),
     "block": Workload("block", 1024, 8, 128, 128, True, ACT_SOFTMAX, torch.bfloat16, False, 0, 64),
+    "block_rope": Workload("block_rope", 1024, 8, 128, 128, True, ACT_SOFTMAX, torch.bfloat16,
+                           False, 0, 64, True),
 }
 
 
@@ -78,7 +82,7 @@ def lengths(name: str, seed: int = 0):
     if name == "d64":
         lq = rng.integers(1, 512, 256, endpoint=True).astype(np.int64)
         return lq, lq.copy()
-    if name in ("causal", "block"):
+    if name in ("causal", "block", "block_rope"):
         lq = np.clip(np.rint(rng.lognormal(5.5, 0.8, 1024)), 1, 2048).astype(np.int64)
         return lq, lq.copy()
     if name == "cross":
