@@ -42,11 +42,14 @@ __device__ __forceinline__ WorkItem load_item(const WorkItem* list, int i) {
 
 // Device workspace header; lives at offset 0 of the caller's workspace.
 struct WsHeader {
-  int status;  // jfa_status of the last call (device-detected errors only)
-  int n_q;     // items in the query-major list
-  int n_k;     // items in the key-major list
-  int pad[61];
+  int status;    // jfa_status of the last call (device-detected errors only)
+  int n_q;       // items in the query-major list
+  int n_k;       // items in the key-major list
+  int claim[3];  // next list item to take: forward, dK/dV, dQ (zeroed by the scheduler)
+  int pad[58];
 };
+static_assert(sizeof(WsHeader) == 256, "workspace header");
+enum : int { kClaimFwd = 0, kClaimDkdv = 1, kClaimDq = 2 };
 
 // Everything a kernel needs to know about one request.
 struct Problem {

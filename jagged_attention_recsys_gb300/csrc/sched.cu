@@ -42,6 +42,7 @@ struct SchedShared {
   int hist[kBuckets], start[kBuckets], run[kBuckets];
   int wcount[kWarps][kBuckets + 1];  // padded: a bucket's column spans all 32 banks
   int red;
+  unsigned long long ctot;  // total cost of the list's units
   int4 seq[kCacheB];      // (q0, k0, lq, lk)
   int ntile[kCacheB];     // tiles of the list being built
   int bucket[kCacheB];    // cost bucket of the sequence
@@ -113,13 +114,18 @@ struct Arrays {
   int* first;
 };
 
+// Lists whose items average at least this many steps are taken by the tensor-core
+// kernels' CTAs from a counter as they become free; shorter items keep the fixed
+// round-robin assignment, whose per-item cost is lower.
+constexpr int kClaimMinMeanCost = 6;
+
 __device__ void build_list(const Problem& p, const ListSpec& L, const Arrays& A, WorkItem* list,
-                           int* n_out, SchedShared& sh) {
+                           int* n_out, int* claim0, int* claim1, SchedShared& sh) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int B = (int)p.batch;
 
   // 1. tiles and total cost per sequence; the heaviest total
-  long long cmax = 0;
+  long long cmax = 0, csum = 0;
   for (int b = tid; b < B; b += kThreads) {
     const int4 s = A.seq[b];
     const int n = tiles_of(L, s.z, s.w);
@@ -128,12 +134,16 @@ __device__ void build_list(const Problem& p, const ListSpec& L, const Arrays& A,
     A.ntile[b] = n;
     A.bucket[b] = (int)min(c, (long long)0x7fffffff);  // total cost for now
     cmax = max(cmax, c);
+    csum += c;
   }
+  if (tid == 0) sh.ctot = 0;
   // block max
   for (int o = 16; o > 0; o >>= 1) cmax = max(cmax, __shfl_xor_sync(0xffffffffu, cmax, o));
   if (tid == 0) sh.red = 0;
   __syncthreads();
   if (lane == 0) atomicMax(&sh.red, (int)min(cmax, (long long)0x7fffffff));
+  for (int o = 16; o > 0; o >>= 1) csum += __shfl_xor_sync(0xffffffffu, csum, o);
+  if (lane == 0) atomicAdd(&sh.ctot, (unsigned long long)csum);
   for (int c = tid; c < kBuckets; c += kThreads) { sh.hist[c] = 0; sh.run[c] = 0; }
   for (int i = tid; i < kWarps * (kBuckets + 1); i += kThreads) (&sh.wcount[0][0])[i] = 0;
   __syncthreads();
@@ -235,7 +245,14 @@ __device__ void build_list(const Problem& p, const ListSpec& L, const Arrays& A,
     w.q0 = s.x; w.k0 = s.y; w.lq = s.z; w.lk = s.w;
     list[e] = w;
   }
-  if (tid == 0) *n_out = n_items;
+  if (tid == 0) {
+    *n_out = n_items;
+    // claim counters of the kernels that walk this list: 0 (taken from), or -1 (fixed
+    // assignment)
+    const int init = sh.ctot >= (unsigned long long)kClaimMinMeanCost * (unsigned long long)carry ? 0 : -1;
+    *claim0 = init;
+    if (claim1) *claim1 = init;
+  }
   __syncthreads();
 }
 
@@ -276,6 +293,7 @@ schedule_kernel(Problem p, Workspace ws, ListSpec lq_spec, ListSpec lk_spec, int
       ws.hdr->status = JFA_ERR_BAD_OFFSETS;
       ws.hdr->n_q = 0;
       ws.hdr->n_k = 0;
+      for (int c = 0; c < 3; ++c) ws.hdr->claim[c] = 0;
     }
     return;
   }
@@ -284,13 +302,13 @@ schedule_kernel(Problem p, Workspace ws, ListSpec lq_spec, ListSpec lk_spec, int
   const bool split = gridDim.x == 2;
   if (!split || blockIdx.x == 0) {
     if (build_q)
-      build_list(p, lq_spec, A, ws.list_q, &ws.hdr->n_q, sh);
+      build_list(p, lq_spec, A, ws.list_q, &ws.hdr->n_q, &ws.hdr->claim[kClaimFwd], &ws.hdr->claim[kClaimDq], sh);
     else if (tid == 0)
       ws.hdr->n_q = 0;
   }
   if (!split || blockIdx.x == 1) {
     if (build_k)
-      build_list(p, lk_spec, A, ws.list_k, &ws.hdr->n_k, sh);
+      build_list(p, lk_spec, A, ws.list_k, &ws.hdr->n_k, &ws.hdr->claim[kClaimDkdv], nullptr, sh);
     else if (tid == 0)
       ws.hdr->n_k = 0;
   }

@@ -32,6 +32,7 @@
 #include "tc.h"
 #include "tc_host.h"
 #include "tc_ptx.cuh"
+#include "feed.cuh"
 
 namespace jfa {
 namespace {
@@ -134,8 +135,10 @@ struct KvLayout {
   static constexpr uint32_t Q_BYTES = DQK / 64 * 16384;  // 128 rows
   static constexpr uint32_t O_BYTES = DV / 64 * 16384;
   static constexpr uint32_t RS_BYTES = 2 * KSTEP * 4;    // -lse log2 e and -D of 128 rows
-  // in front of the tiles: mbarriers, TMEM slot, abort flag (512 bytes), row terms
-  static constexpr uint32_t RS_OFF = 512;
+  // in front of the tiles: mbarriers, TMEM slot, abort flag (640 bytes), the work item
+  // ring, row terms
+  static constexpr uint32_t FEED_OFF = 640;
+  static constexpr uint32_t RS_OFF = FEED_OFF + kFeedSlots * sizeof(WorkItem);
   static constexpr uint32_t SMALL = RS_OFF + NO * RS_BYTES;
   static constexpr uint32_t TILE0 = (SMALL + 1023) / 1024 * 1024;  // for a 1 KB-aligned base
   static constexpr uint32_t K_OFF = 0;  // offsets from the 1 KB-aligned tile base
@@ -151,9 +154,9 @@ enum : uint32_t {
   KV_KFULL = 0, KV_KEMPTY = 1, KV_VFULL = 2, KV_VEMPTY = 3, KV_QFULL = 4, KV_QEMPTY = 8,
   KV_OFULL = 12, KV_OEMPTY = 16, KV_RSFULL = 20, KV_SFULL = 24, KV_SEMPTY = 26, KV_DPFULL = 28,
   KV_PDSFULL = 30, KV_KDONE = 32, KV_ACCFULL = 34, KV_ACCEMPTY = 35, KV_DRAIN = 36, KV_KREADY = 38,
-  KV_QREADY = 39, KV_COUNT = 43
+  KV_QREADY = 39, KV_FEEDFULL = 43, KV_FEEDEMPTY = 51, KV_COUNT = 59
 };
-static_assert(8 * KV_COUNT + 8 <= 512, "mbarriers, TMEM slot and abort flag in front of the row terms");
+static_assert(8 * KV_COUNT + 8 <= 640, "mbarriers, TMEM slot and abort flag in front of the item ring");
 
 // bf16 pair (low, high) of a packed word to two floats, exactly
 __device__ __forceinline__ float2 unpack_bf16(uint32_t u) {
@@ -161,32 +164,32 @@ __device__ __forceinline__ float2 unpack_bf16(uint32_t u) {
 }
 
 // Walks the steps of a CTA's items in order (items without steps are skipped):
-// item w, local step j, global step g, Q/dO stage counter q, item counter kv.
-// The item after w is always loaded one ahead, so a step never waits for memory.
+// item w, local step j, global step g, Q/dO stage counter q, item counter kv.  The
+// items come from the CTA's feed; `arrive` marks the cursor that releases each feed
+// slot (an issuer's lagging cursor).  Becomes invalid at the end of the list or when a
+// bounded wait gave up.
+template <bool DYN>
 struct StepCursor {
-  const WorkItem* list;
-  int n_items, it;
-  WorkItem w, nxt;
+  Feed<DYN> feed;
+  volatile int* abort;
+  int* status;
+  WorkItem w;
   int j;
   uint32_t g, q, kv;
-  bool valid;
-  __device__ void next_item() {  // w <- the item after it, nxt <- the one after that
-    it += gridDim.x;
-    w = nxt;
-    if (it + (int)gridDim.x < n_items) nxt = load_item(list, it + gridDim.x);
-  }
+  bool valid, arrive;
+  __device__ void next_item() { valid = feed.take(w, true, arrive, abort, status); }
   __device__ void skip_empty() {
-    while (it < n_items && w.cost == 0) next_item();
-    valid = it < n_items;
+    while (valid && w.cost == 0) next_item();
   }
-  __device__ void init(const WorkItem* l, int n) {
-    list = l;
-    n_items = n;
-    it = blockIdx.x;
+  __device__ void init(const FeedRing& r, const WorkItem* l, const int* ctr, int n, bool arr,
+                       volatile int* ab, int* st) {
+    feed.init(r, l, ctr, n);
+    abort = ab;
+    status = st;
+    arrive = arr;
     j = 0;
     g = q = kv = 0;
-    if (it < n_items) w = load_item(list, it);
-    if (it + (int)gridDim.x < n_items) nxt = load_item(list, it + gridDim.x);
+    next_item();
     skip_empty();
   }
   __device__ void advance() {
@@ -313,6 +316,12 @@ tc_dkdv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
     // rotated K and Q tiles (rotary embedding): one arrival per compute warp
     mbar_init(bar(KV_KREADY), kCompute / 32);
     for (int s = 0; s < NQ; ++s) mbar_init(bar(KV_QREADY + s), kCompute / 32);
+    // work item ring: warp 0 claims; the second producer, both issuers and every
+    // compute warp read
+    for (int s = 0; s < kFeedSlots; ++s) {
+      mbar_init(bar(KV_FEEDFULL + s), 1);
+      mbar_init(bar(KV_FEEDEMPTY + s), 3 + kCompute / 32);
+    }
     *abort = 0;
     fence_mbar_init();
   }
@@ -323,6 +332,14 @@ tc_dkdv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
   const uint32_t tmem = *tmem_slot;
   // TMEM columns: dK [0,128), dV [128,256), step buffers X0 [256,384), X1 [384,512)
   constexpr uint32_t T_DK = 0, T_DV = 128, T_X = 256;
+  // SiLU/L items may be claimed from the launch's counter as CTAs become free (the
+  // scheduler decides per list).  The softmax kernels keep the fixed assignment: their
+  // workloads' items are short, and the feed's registers would cost them spills; so do
+  // the rotary kernels, whose compute warps look ahead in the list.
+  constexpr bool kDyn = !ROPE && ACT != kActSoftmax;
+  static_assert(KV_FEEDEMPTY == KV_FEEDFULL + kFeedSlots, "feed ring barriers");
+  const FeedRing ring{bar(KV_FEEDFULL), raw + L::FEED_OFF};
+  int* const claim_ctr = &hdr->claim[kClaimDkdv];
 
   // Rotary embedding of Q and K (BlockAttention): the compute warps rotate each item's K
   // and Q tiles in shared memory once they have landed and signal them ready; issuer A
@@ -340,10 +357,10 @@ tc_dkdv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
       tma_prefetch_desc(&tm_q);
       uint32_t kv_it = 0, q_it = 0;
       bool ok = true;
-      WorkItem nxt = blockIdx.x < (unsigned)n_items ? load_item(list, blockIdx.x) : WorkItem{};
-      for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
-        const WorkItem w = nxt;  // prefetched one item ahead
-        if (it + (int)gridDim.x < n_items) nxt = load_item(list, it + gridDim.x);
+      FeedClaimer<kDyn> claimer;
+      claimer.init(ring, list, claim_ctr, n_items);
+      WorkItem w;
+      while (ok && claimer.claim(w, abort, status)) {
         const int n = w.cost;
         if (n == 0) continue;
         const int h = w.h, key0 = w.tile * TILE;
@@ -381,10 +398,10 @@ tc_dkdv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
     }
     uint32_t kv_it = 0, q_it = 0;
     bool ok = true;
-    WorkItem nxt = blockIdx.x < (unsigned)n_items ? load_item(list, blockIdx.x) : WorkItem{};
-    for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
-      const WorkItem w = nxt;  // prefetched one item ahead
-      if (it + (int)gridDim.x < n_items) nxt = load_item(list, it + gridDim.x);
+    Feed<kDyn> feed;
+    feed.init(ring, list, claim_ctr, n_items);
+    WorkItem w;
+    while (ok && feed.take(w, true, true, abort, status)) {
       const int n = w.cost;
       if (n == 0) continue;
       const int h = w.h, key0 = w.tile * TILE;
@@ -453,7 +470,7 @@ tc_dkdv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
       // Score product of step c into X[g & 1]: S^T (chain P) once dK(g-2) has read
       // the buffer (dV(g-2) was issued earlier by this thread); dP^T (chain dS)
       // once the compute warps have loaded S^T(g) from it.
-      auto issue_score = [&](const StepCursor& c) {
+      auto issue_score = [&](const StepCursor<kDyn>& c) {
         const uint32_t b = c.g & 1;
         const uint32_t st = chain_p ? c.q % NQ : c.q % NO;
         const uint32_t ph = chain_p ? (c.q / NQ) & 1 : (c.q / NO) & 1;
@@ -481,9 +498,9 @@ tc_dkdv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
         if (c.last()) mma_commit(bar(chain_p ? KV_KEMPTY : KV_VEMPTY));  // last use of this tile
         return true;
       };
-      StepCursor cs, cg;  // cs: next score product (one step ahead); cg: gradient product
-      cs.init(list, n_items);
-      cg = cs;
+      StepCursor<kDyn> cs, cg;  // cs: next score product (one step ahead); cg: gradient product
+      cs.init(ring, list, claim_ctr, n_items, false, abort, status);
+      cg.init(ring, list, claim_ctr, n_items, true, abort, status);
       if (cs.valid) {
         ok = issue_score(cs);
         cs.advance();
@@ -624,10 +641,10 @@ tc_dkdv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
                                                kCompute / 32, lane, abort, status))
         ok = false;
     }
-    WorkItem nxt = blockIdx.x < (unsigned)n_items ? load_item(list, blockIdx.x) : WorkItem{};
-    for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
-      const WorkItem w = nxt;
-      if (it + (int)gridDim.x < n_items) nxt = load_item(list, it + gridDim.x);
+    Feed<kDyn> feed;
+    feed.init(ring, list, claim_ctr, n_items);
+    WorkItem w;
+    while (ok && feed.take(w, true, true, abort, status)) {
       const int n = w.cost;
       const int h = w.h, key0 = w.tile * TILE;
       const int64_t k0 = w.k0;
@@ -798,7 +815,11 @@ struct QLayout {
   static constexpr uint32_t O_BYTES = DV / 64 * 16384;
   static constexpr uint32_t K_BYTES = DQK / 64 * 16384;   // 128 keys
   static constexpr uint32_t V_BYTES = DV / 64 * 16384;
-  static constexpr uint32_t TILE0 = 1024;  // mbarriers, TMEM slot, abort flag in front
+  // in front: mbarriers, TMEM slot, abort flag (640 bytes), the work item ring
+  static constexpr uint32_t FEED_OFF = 640;
+  static constexpr uint32_t SMALL = FEED_OFF + kFeedSlots * sizeof(WorkItem);
+  static constexpr uint32_t TILE0 = 1024;
+  static_assert(SMALL <= TILE0, "the front area fits below the tiles");
   static constexpr uint32_t Q_OFF = 0;     // offsets from the 1 KB-aligned tile base
   static constexpr uint32_t O_OFF = Q_OFF + NQ * Q_BYTES;
   static constexpr uint32_t K_OFF = O_OFF + NO * O_BYTES;
@@ -815,9 +836,10 @@ struct QLayout {
 enum : uint32_t {
   Q_QFULL = 0, Q_QEMPTY = 2, Q_OFULL = 4, Q_OEMPTY = 6, Q_KFULL = 8, Q_KEMPTY = 14, Q_VFULL = 20,
   Q_VEMPTY = 24, Q_SFULL = 28, Q_DPFULL = 30, Q_DPEMPTY = 31, Q_DSFULL = 32, Q_ACCFULL = 34,
-  Q_ACCEMPTY = 35, Q_DRAIN = 36, Q_QREADY = 38, Q_KREADY = 40, Q_COUNT = 46
+  Q_ACCEMPTY = 35, Q_DRAIN = 36, Q_QREADY = 38, Q_KREADY = 40, Q_FEEDFULL = 46, Q_FEEDEMPTY = 54,
+  Q_COUNT = 62
 };
-static_assert(8 * Q_COUNT + 8 <= 512, "mbarriers, TMEM slot and abort flag in front of the tiles");
+static_assert(8 * Q_COUNT + 8 <= 640, "mbarriers, TMEM slot and abort flag in front of the item ring");
 
 // The dQ pass's counterpart of kv_rotate_next: the item's Q tile and its one K tile.
 template <int DQK, int NQ, int NK, class L>
@@ -862,7 +884,7 @@ tc_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
   constexpr uint32_t kCompute = 32 * 4 * Gr::G;  // compute threads
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
-  const uint32_t sb = (raw + 512u + 1023u) & ~1023u;  // 128-byte swizzled tiles: 1 KB aligned
+  const uint32_t sb = (raw + L::SMALL + 1023u) & ~1023u;  // 128-byte swizzled tiles: 1 KB aligned
   int* status = &hdr->status;
   uint32_t dyn_bytes;
   asm("mov.u32 %0, %%dynamic_smem_size;" : "=r"(dyn_bytes));
@@ -906,6 +928,12 @@ tc_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
     // rotated Q and K tiles (rotary embedding): one arrival per compute warp
     for (int s = 0; s < NQ; ++s) mbar_init(bar(Q_QREADY + s), kCompute / 32);
     for (int s = 0; s < NK; ++s) mbar_init(bar(Q_KREADY + s), kCompute / 32);
+    // work item ring: warp 0 claims; the second producer, both issuers and every
+    // compute warp read
+    for (int s = 0; s < kFeedSlots; ++s) {
+      mbar_init(bar(Q_FEEDFULL + s), 1);
+      mbar_init(bar(Q_FEEDEMPTY + s), 3 + kCompute / 32);
+    }
     *abort = 0;
     fence_mbar_init();
   }
@@ -917,6 +945,14 @@ tc_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
   // TMEM columns: dQ [0,128), S buffer 0 [128,256), dP (dS) [256,384), S buffer 1 [384,512)
   constexpr uint32_t T_DQ = 0, T_DP = 256;
   auto t_s = [](uint32_t b) { return b ? 384u : 128u; };
+  // SiLU/L items may be claimed from the launch's counter as CTAs become free (the
+  // scheduler decides per list).  The softmax kernels keep the fixed assignment: their
+  // workloads' items are short, and the feed's registers would cost them spills; so do
+  // the rotary kernels, whose compute warps look ahead in the list.
+  constexpr bool kDyn = !ROPE && ACT != kActSoftmax;
+  static_assert(Q_FEEDEMPTY == Q_FEEDFULL + kFeedSlots, "feed ring barriers");
+  const FeedRing ring{bar(Q_FEEDFULL), raw + L::FEED_OFF};
+  int* const claim_ctr = &hdr->claim[kClaimDq];
 
   // Rotary embedding of Q and K (BlockAttention): the compute warps rotate each item's K
   // and Q tiles in shared memory once they have landed and signal them ready; issuer A
@@ -942,10 +978,14 @@ tc_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
       const uint32_t b_kfull = qk ? Q_KFULL : Q_VFULL, b_kempty = qk ? Q_KEMPTY : Q_VEMPTY;
       uint32_t q_it = 0, t_it = 0;
       bool ok = true;
-      WorkItem nxt = blockIdx.x < (unsigned)n_items ? load_item(list, blockIdx.x) : WorkItem{};
-      for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
-        const WorkItem w = nxt;  // prefetched one item ahead
-        if (it + (int)gridDim.x < n_items) nxt = load_item(list, it + gridDim.x);
+      FeedClaimer<kDyn> claimer;  // warp 0 claims, the second producer reads
+      Feed<kDyn> feed;
+      if (qk)
+        claimer.init(ring, list, claim_ctr, n_items);
+      else
+        feed.init(ring, list, claim_ctr, n_items);
+      WorkItem w;
+      while (ok && (qk ? claimer.claim(w, abort, status) : feed.take(w, false, true, abort, status))) {
         const int n = w.cost;
         if (n == 0) continue;
         const int h = w.h, row0 = w.tile * TILE;
@@ -990,10 +1030,10 @@ tc_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
       if constexpr (NQ == 1) {
         uint32_t q_it = 0, k_it = 0, s_it = 0, d_it = 0, a_it = 0;
         bool ok = true;
-        WorkItem nxt = blockIdx.x < (unsigned)n_items ? load_item(list, blockIdx.x) : WorkItem{};
-        for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
-          const WorkItem w = nxt;
-          if (it + (int)gridDim.x < n_items) nxt = load_item(list, it + gridDim.x);
+        Feed<kDyn> feed;
+        feed.init(ring, list, claim_ctr, n_items);
+        WorkItem w;
+        while (ok && feed.take(w, true, true, abort, status)) {
           const int n = w.cost;
           if (n == 0) continue;
           const uint32_t qs = q_it % NQ;
@@ -1050,7 +1090,7 @@ tc_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
         uint32_t a_it = 0;
         bool ok = true;
         // S(c.g) = Q K(c.g)^T into buffer c.g & 1; the item's Q tile is stage c.kv % NQ
-        auto issue_s = [&](const StepCursor& c) -> bool {
+        auto issue_s = [&](const StepCursor<kDyn>& c) -> bool {
           const uint32_t qs = c.kv % NQ, kst = c.g % NK;
           if ((c.j == 0 && !mbar_wait(bar((rope ? Q_QREADY : Q_QFULL) + qs), (c.kv / NQ) & 1, abort, status)) ||
               !mbar_wait(bar((rope ? Q_KREADY : Q_KFULL) + kst), (c.g / NK) & 1, abort, status))
@@ -1069,9 +1109,9 @@ tc_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
           if (c.last()) mma_commit(bar(Q_QEMPTY + qs));  // last use of this Q tile
           return true;
         };
-        StepCursor cs, cg;  // cs: next S (up to two steps ahead); cg: next dQ
-        cs.init(list, n_items);
-        cg = cs;
+        StepCursor<kDyn> cs, cg;  // cs: next S (up to two steps ahead); cg: next dQ
+        cs.init(ring, list, claim_ctr, n_items, false, abort, status);
+        cg.init(ring, list, claim_ctr, n_items, true, abort, status);
         auto run_ahead = [&]() -> bool {  // S up to step cg.g + 1
           while (cs.valid && cg.valid && cs.g < cg.g + 2) {
             if (!issue_s(cs)) return false;
@@ -1116,10 +1156,10 @@ tc_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
       constexpr uint32_t idesc_s = idesc_bf16(TILE, STEP, 0, 0);
       uint32_t q_it = 0, v_it = 0, dp_it = 0;  // V ring: v_it % NV
       bool ok = true;
-      WorkItem nxt = blockIdx.x < (unsigned)n_items ? load_item(list, blockIdx.x) : WorkItem{};
-      for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
-        const WorkItem w = nxt;
-        if (it + (int)gridDim.x < n_items) nxt = load_item(list, it + gridDim.x);
+      Feed<kDyn> feed;
+      feed.init(ring, list, claim_ctr, n_items);
+      WorkItem w;
+      while (ok && feed.take(w, true, true, abort, status)) {
         const int n = w.cost;
         if (n == 0) continue;
         const uint32_t qs = q_it % NO;
@@ -1212,10 +1252,10 @@ tc_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
                                           kCompute / 32, lane, abort, status))
         ok = false;
     }
-    WorkItem nxt = blockIdx.x < (unsigned)n_items ? load_item(list, blockIdx.x) : WorkItem{};
-    for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
-      const WorkItem w = nxt;
-      if (it + (int)gridDim.x < n_items) nxt = load_item(list, it + gridDim.x);
+    Feed<kDyn> feed;
+    feed.init(ring, list, claim_ctr, n_items);
+    WorkItem w;
+    while (ok && feed.take(w, true, true, abort, status)) {
       const int n = w.cost;
       const int h = w.h, row0 = w.tile * TILE;
       const int64_t q0 = w.q0;

@@ -40,6 +40,7 @@
 #include "tc.h"
 #include "tc_host.h"
 #include "tc_ptx.cuh"
+#include "feed.cuh"
 
 namespace jfa {
 namespace {
@@ -67,9 +68,11 @@ struct FwdLayout {
   static constexpr uint32_t Q_BYTES = DQK / 64 * 16384;  // one 128-row tile
   static constexpr uint32_t K_BYTES = DQK / 64 * 16384;  // one 128-key tile
   static constexpr uint32_t V_BYTES = DV / 64 * 16384;
-  // In front of the tiles: mbarriers, TMEM slot and abort flag (512 bytes), then the
-  // row statistics exchanged by the two softmax warpgroups ([2 steps][128 rows][2]).
-  static constexpr uint32_t RED_OFF = 512;
+  // In front of the tiles: mbarriers, TMEM slot and abort flag (640 bytes), the work
+  // item ring, then the row statistics exchanged by the two softmax warpgroups
+  // ([2 steps][128 rows][2]).
+  static constexpr uint32_t FEED_OFF = 640;
+  static constexpr uint32_t RED_OFF = FEED_OFF + kFeedSlots * sizeof(WorkItem);
   static constexpr uint32_t RED_BYTES = 2 * BM * 2 * 4;
   static constexpr uint32_t SMALL = RED_OFF + RED_BYTES;
   static constexpr uint32_t TILE0 = (SMALL + 1023) / 1024 * 1024;  // for a 1 KB-aligned base
@@ -92,9 +95,10 @@ struct FwdLayout {
 enum : uint32_t {
   B_QFULL = 0, B_QEMPTY = 2, B_KFULL = 4, B_KEMPTY = 10, B_VFULL = 16, B_VEMPTY = 22,
   B_SFULL = 28, B_PFULL = 30, B_PEMPTY = 32, B_OFULL = 34, B_OEMPTY = 35, B_RED = 36, B_REDL = 38,
-  B_DRAIN = 40, B_HOLD = 42, B_QREADY = 43, B_KREADY = 45, B_COUNT = 51
+  B_DRAIN = 40, B_HOLD = 42, B_QREADY = 43, B_KREADY = 45, B_FEEDFULL = 51, B_FEEDEMPTY = 59,
+  B_COUNT = 67
 };
-static_assert(8 * B_COUNT + 8 <= FwdLayout<128, 128>::RED_OFF, "mbarriers, TMEM slot and abort flag in front");
+static_assert(8 * B_COUNT + 8 <= FwdLayout<128, 128>::FEED_OFF, "mbarriers, TMEM slot and abort flag in front");
 constexpr uint32_t T_S = 0, T_O = 256, T_P = 384;  // S: 2 x 128 columns; P: 2 x 64 columns
 
 // Rotary embedding (BlockAttention), done by the compute warps: the next non-empty item
@@ -192,6 +196,12 @@ tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     // rotated Q and K tiles (rotary embedding): one arrival per compute warp
     for (int s = 0; s < 2; ++s) mbar_init(bar(B_QREADY + s), R::kCompute / 32);
     for (int s = 0; s < NK; ++s) mbar_init(bar(B_KREADY + s), R::kCompute / 32);
+    // work item ring: the Q/K producer claims; the V producer, both issuers and every
+    // compute warp read
+    for (int s = 0; s < kFeedSlots; ++s) {
+      mbar_init(bar(B_FEEDFULL + s), 1);
+      mbar_init(bar(B_FEEDEMPTY + s), 3 + R::kCompute / 32);
+    }
     *abort = 0;
     fence_mbar_init();
   }
@@ -200,6 +210,15 @@ tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // SiLU/L items may be claimed from the launch's counter as CTAs become free (the
+  // scheduler decides per list).  The softmax kernels keep the fixed assignment: their
+  // workloads' items are short, and the feed's registers would cost them spills; so do
+  // the rotary kernels, whose compute warps look ahead in the list.
+  constexpr bool kDyn = !ROPE && ACT != kActSoftmax;
+  static_assert(B_FEEDEMPTY == B_FEEDFULL + kFeedSlots, "feed ring barriers");
+  const FeedRing ring{bar(B_FEEDFULL), raw + L::FEED_OFF};
+  Feed<kDyn> feed;
+  feed.init(ring, list, &hdr->claim[kClaimFwd], n_items);
 
   // Rotary embedding of Q and K (BlockAttention): the compute warps rotate each item's Q
   // and K tiles in shared memory once they have landed and signal them ready; the S
@@ -221,10 +240,10 @@ tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
       }
       uint32_t t_it = 0, q_it = 0;
       bool ok = true;
-      WorkItem nxt = blockIdx.x < (unsigned)n_items ? load_item(list, blockIdx.x) : WorkItem{};
-      for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
-        const WorkItem w = nxt;  // prefetched one item ahead
-        if (it + (int)gridDim.x < n_items) nxt = load_item(list, it + gridDim.x);
+      FeedClaimer<kDyn> claimer;  // the Q/K thread claims, the V thread reads
+      claimer.init(ring, list, &hdr->claim[kClaimFwd], n_items);
+      WorkItem w;
+      while (ok && (qk ? claimer.claim(w, abort, status) : feed.take(w, false, true, abort, status))) {
         const int n = w.cost;
         if (n == 0) continue;
         if (qk) {
@@ -276,10 +295,8 @@ tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
       uint32_t k_it = 0, q_it = 0, gs = 0;
       bool ok = true;
       if (*(volatile int*)&g_test_hold) ok = mbar_wait(bar(B_HOLD), 0, abort, status);
-      WorkItem nxt = blockIdx.x < (unsigned)n_items ? load_item(list, blockIdx.x) : WorkItem{};
-      for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
-        const WorkItem w = nxt;
-        if (it + (int)gridDim.x < n_items) nxt = load_item(list, it + gridDim.x);
+      WorkItem w;
+      while (ok && feed.take(w, true, true, abort, status)) {
         const int n = w.cost;
         if (n == 0) continue;
         const uint32_t qs = q_it % L::NQB;
@@ -318,10 +335,8 @@ tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
       constexpr uint32_t idesc_o = idesc_bf16(BM, DV, 0, 1);
       uint32_t v_it = 0, o_it = 0, gs = 0;
       bool ok = true;
-      WorkItem nxt = blockIdx.x < (unsigned)n_items ? load_item(list, blockIdx.x) : WorkItem{};
-      for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
-        const WorkItem w = nxt;
-        if (it + (int)gridDim.x < n_items) nxt = load_item(list, it + gridDim.x);
+      WorkItem w;
+      while (ok && feed.take(w, true, true, abort, status)) {
         const int n = w.cost;
         if (n == 0) continue;
         for (int j = 0; j < n; ++j, ++gs, ++v_it) {
@@ -392,10 +407,8 @@ tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                                         lane, abort, status))
         ok = false;
     }
-    WorkItem nxt = blockIdx.x < (unsigned)n_items ? load_item(list, blockIdx.x) : WorkItem{};
-    for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
-      const WorkItem w = nxt;
-      if (it + (int)gridDim.x < n_items) nxt = load_item(list, it + gridDim.x);
+    WorkItem w;
+    while (ok && feed.take(w, true, true, abort, status)) {
       const int n = w.cost, h = w.h;
       const int Lq = w.lq, Lk = w.lk;
       if (rope && n > 1) {  // the rotary kernels take items of one step only
