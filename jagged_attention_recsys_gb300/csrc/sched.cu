@@ -11,8 +11,10 @@
 // sequence granularity; costs are bucketed into 128 levels relative to the
 // heaviest sequence, ties by sequence index).  The tiles of one sequence are
 // contiguous, heaviest tile first, and the heads of one tile are adjacent.
-// Persistent CTAs take items i, i + grid, i + 2*grid, ...: the items that run
-// at the same time therefore belong to few sequences and share their K/V
+// Persistent CTAs take items i, i + grid, i + 2*grid, ..., or, for lists whose
+// items average at least kClaimMinMeanCost steps, claim the next item from a
+// counter as they become free (the SiLU/L kernels; see feed.cuh).  Either way the
+// items that run at the same time belong to few sequences and share their K/V
 // tiles through L2, while the heavy sequences start first.
 // Each item also carries its sequence's first rows and lengths, so a kernel
 // needs one 32-byte load per item and no dependent offset lookups.

@@ -82,8 +82,57 @@ def bars_of(spec):
     return {name: Bar(count) for name, count in spec}
 
 
+# The work-item ring of the claimed mode (`csrc/feed.cuh`): the claimer publishes list
+# entry e + 1 when it claims entry e (entry 0 first; the entry after the last item is
+# the end marker), and every other role takes the entries in order, skipping items of no
+# steps, with one arrival on the slot's EMPTY barrier per role (an issuer's leading
+# cursor "cs" only waits).  Roles mark where they move on: ("claim", kv) before the
+# claimer's kv-th item of steps, ("take", kv, cursor) where a cursor moves to it (kv
+# equal to the number of such items: the end of the list).
+FEED_SLOTS = 8
+
+
+def feed_bars(costs, readers):
+    spec = [(("FEEDFULL", s), 1) for s in range(FEED_SLOTS)]
+    spec += [(("FEEDEMPTY", s), readers) for s in range(FEED_SLOTS)]
+    return bars_of(spec)
+
+
+def with_feed(gen, costs, role_kind, feed):
+    """Turns a role's markers into feed waits and arrivals (or drops them)."""
+    li = [i for i, n in enumerate(costs) if n > 0] + [len(costs)]  # list index; last: end
+    pos = {}
+
+    def upto(cursor, last):
+        e = pos.get(cursor, 0)
+        while e <= last:
+            s = e % FEED_SLOTS
+            if role_kind == "claimer":
+                yield W(("FEEDEMPTY", s), ((e // FEED_SLOTS) & 1) ^ 1)
+                yield A(("FEEDFULL", s))
+            else:
+                yield W(("FEEDFULL", s), (e // FEED_SLOTS) & 1)
+                if cursor != "cs":
+                    yield A(("FEEDEMPTY", s))
+            e += 1
+        pos[cursor] = e
+
+    for ev in gen:
+        if ev[0] == "claim":
+            if feed:
+                yield from upto("main", min(li[ev[1]] + 1, len(costs)))
+        elif ev[0] == "take":
+            if feed:
+                yield from upto(ev[2], li[ev[1]])
+        else:
+            yield ev
+    if feed:  # the end marker: published by the claimer, taken by every cursor
+        for cursor in pos or ["main"]:
+            yield from upto(cursor, len(costs))
+
+
 # ----------------------------------------------------------------------------- forward
-def fwd_roles(costs, NQB, NK, NV, softmax, seed):
+def fwd_roles(costs, NQB, NK, NV, softmax, seed, feed=False):
     G = 2 if softmax else 4  # softmax warpgroups
     spec = [(("QFULL", s), 1) for s in range(NQB)] + [(("QEMPTY", s), 1) for s in range(NQB)]
     spec += [(("KFULL", s), 1) for s in range(NK)] + [(("KEMPTY", s), 1) for s in range(NK)]
@@ -99,6 +148,7 @@ def fwd_roles(costs, NQB, NK, NV, softmax, seed):
     def producer_qk():
         t = 0
         for kv, n in enumerate(items):
+            yield ("claim", kv)
             qs = kv % NQB
             yield W(("QEMPTY", qs), ((kv // NQB) & 1) ^ 1)
             yield A(("QFULL", qs))
@@ -110,7 +160,8 @@ def fwd_roles(costs, NQB, NK, NV, softmax, seed):
 
     def producer_v():
         t = 0
-        for n in items:
+        for kv, n in enumerate(items):
+            yield ("take", kv, "main")
             for _ in range(n):
                 st = t % NV
                 yield W(("VEMPTY", st), ((t // NV) & 1) ^ 1)
@@ -120,6 +171,7 @@ def fwd_roles(costs, NQB, NK, NV, softmax, seed):
     def s_issuer():
         gs = 0
         for kv, n in enumerate(items):
+            yield ("take", kv, "main")
             qs = kv % NQB
             yield W(("QFULL", qs), (kv // NQB) & 1)
             for i in range(n):
@@ -134,7 +186,8 @@ def fwd_roles(costs, NQB, NK, NV, softmax, seed):
 
     def pv_issuer():
         gs, o_it = 0, 0
-        for n in items:
+        for kv, n in enumerate(items):
+            yield ("take", kv, "main")
             for j in range(n):
                 b, vst = gs & 1, gs % NV
                 yield W(("PFULL", b), (gs >> 1) & 1)
@@ -158,7 +211,8 @@ def fwd_roles(costs, NQB, NK, NV, softmax, seed):
             yield A("OEMPTY")
             pend = False
 
-        for n in items:
+        for kv, n in enumerate(items):
+            yield ("take", kv, "main")
             for j in range(n):
                 b = p_it & 1
                 yield W(("SFULL", b), (p_it >> 1) & 1)
@@ -189,11 +243,14 @@ def fwd_roles(costs, NQB, NK, NV, softmax, seed):
     roles = dict(producer_qk=producer_qk(), producer_v=producer_v(), s_issuer=s_issuer(),
                  pv_issuer=pv_issuer())
     roles.update({f"softmax{g}": softmax_group() for g in range(G)})
+    bars.update(feed_bars(costs, len(roles) - 1))
+    roles = {k: with_feed(g, costs, "claimer" if k == "producer_qk" else "reader", feed)
+             for k, g in roles.items()}
     return roles, bars
 
 
 # ----------------------------------------------------------------------------- dK/dV
-def dkdv_roles(costs, NQ, NO, softmax, seed):
+def dkdv_roles(costs, NQ, NO, softmax, seed, feed=False):
     G = 2 if softmax else 4  # compute warpgroups
     spec = [("KFULL", 1), ("KEMPTY", 1), ("VFULL", 1), ("VEMPTY", 1)]
     spec += [(("QFULL", s), 1) for s in range(NQ)] + [(("QEMPTY", s), 2) for s in range(NQ)]
@@ -211,6 +268,7 @@ def dkdv_roles(costs, NQ, NO, softmax, seed):
     def producer_kq():
         q = 0
         for kv, n in enumerate(items):
+            yield ("claim", kv)
             yield W("KEMPTY", (kv & 1) ^ 1)
             yield A("KFULL")
             for _ in range(n):
@@ -222,6 +280,7 @@ def dkdv_roles(costs, NQ, NO, softmax, seed):
     def producer_vo():  # V, dO and the row terms (on the dO stage)
         q = 0
         for kv, n in enumerate(items):
+            yield ("take", kv, "main")
             yield W("VEMPTY", (kv & 1) ^ 1)
             yield A("VFULL")
             for _ in range(n):
@@ -249,7 +308,10 @@ def dkdv_roles(costs, NQ, NO, softmax, seed):
             yield A(("QEMPTY" if chain_p else "OEMPTY", st))
             if c["last"]:
                 yield A("KEMPTY" if chain_p else "VEMPTY")
+                yield ("take", c["kv"] + 1, "cs")  # the leading cursor moves on
 
+        yield ("take", 0, "cs")
+        yield ("take", 0, "main")
         cs = 0
         if ST:
             yield from score(ST[0])
@@ -271,6 +333,7 @@ def dkdv_roles(costs, NQ, NO, softmax, seed):
             if cg["last"]:
                 yield A("ACCFULL")
                 a_it += 1
+                yield ("take", cg["kv"] + 1, "main")
             if not score_first and cs < len(ST):
                 yield from score(ST[cs])
                 cs += 1
@@ -286,6 +349,8 @@ def dkdv_roles(costs, NQ, NO, softmax, seed):
             pend = False
 
         for c in ST:
+            if c["j"] == 0:
+                yield ("take", c["kv"], "main")
             b = c["g"] & 1
             yield W(("SFULL", b), (c["g"] >> 1) & 1)
             skip = rng.random() < 0.2  # no valid query among this group's columns
@@ -306,11 +371,14 @@ def dkdv_roles(costs, NQ, NO, softmax, seed):
     roles = dict(producer_kq=producer_kq(), producer_vo=producer_vo(), issuer_a=issuer(True),
                  issuer_b=issuer(False))
     roles.update({f"compute{g}": compute_group() for g in range(G)})
+    bars.update(feed_bars(costs, len(roles) - 1))
+    roles = {k: with_feed(g, costs, "claimer" if k == "producer_kq" else "reader", feed)
+             for k, g in roles.items()}
     return roles, bars
 
 
 # ----------------------------------------------------------------------------- dQ
-def dq_roles(costs, NQ, NO, NK, NV, single_ds_barrier=False):
+def dq_roles(costs, NQ, NO, NK, NV, single_ds_barrier=False, feed=False):
     G = 2  # compute warpgroups
     spec = [(("QFULL", s), 1) for s in range(NQ)] + [(("QEMPTY", s), 1) for s in range(NQ)]
     spec += [(("OFULL", s), 1) for s in range(NO)] + [(("OEMPTY", s), 1) for s in range(NO)]
@@ -329,7 +397,8 @@ def dq_roles(costs, NQ, NO, NK, NV, single_ds_barrier=False):
         q_it, t = 0, 0
         n_row, n_ring = (NQ, NK) if qk else (NO, NV)
         rf, re, kf, ke = ("QFULL", "QEMPTY", "KFULL", "KEMPTY") if qk else ("OFULL", "OEMPTY", "VFULL", "VEMPTY")
-        for n in items:
+        for kv, n in enumerate(items):
+            yield ("claim", kv) if qk else ("take", kv, "main")
             qs = q_it % n_row
             yield W((re, qs), ((q_it // n_row) & 1) ^ 1)
             yield A((rf, qs))
@@ -351,6 +420,8 @@ def dq_roles(costs, NQ, NO, NK, NV, single_ds_barrier=False):
             yield A(("SFULL", c["g"] & 1))
             if c["last"]:
                 yield A(("QEMPTY", qs))
+                if NQ > 1:
+                    yield ("take", c["kv"] + 1, "cs")
 
         def dq_step(c):
             nonlocal a_it
@@ -361,10 +432,13 @@ def dq_roles(costs, NQ, NO, NK, NV, single_ds_barrier=False):
             if c["last"]:
                 yield A("ACCFULL")
                 a_it += 1
+                if NQ > 1:
+                    yield ("take", c["kv"] + 1, "main")
 
         if NQ == 1:  # items one by one: S(0), S(1), then dQ(j) and S(j+2)
             i = 0
             while i < len(ST):
+                yield ("take", ST[i]["kv"], "main")
                 n = ST[i]["n"]
                 it = ST[i:i + n]
                 yield from issue_s(it[0])
@@ -384,6 +458,8 @@ def dq_roles(costs, NQ, NO, NK, NV, single_ds_barrier=False):
                     yield from issue_s(ST[cs])
                     cs += 1
 
+            yield ("take", 0, "cs")
+            yield ("take", 0, "main")
             yield from ahead(0)
             for i, c in enumerate(ST):
                 yield from dq_step(c)
@@ -392,6 +468,7 @@ def dq_roles(costs, NQ, NO, NK, NV, single_ds_barrier=False):
     def issuer_b():  # dP
         v_it = 0
         for kv, n in enumerate(items):
+            yield ("take", kv, "main")
             qs = kv % NO
             yield W(("OFULL", qs), (kv // NO) & 1)
             for j in range(n):
@@ -415,6 +492,8 @@ def dq_roles(costs, NQ, NO, NK, NV, single_ds_barrier=False):
             pend = False
 
         for c in ST:
+            if c["j"] == 0:
+                yield ("take", c["kv"], "main")
             yield W(("SFULL", c["g"] & 1), (c["g"] >> 1) & 1)
             yield W("DPFULL", c["g"] & 1)
             yield A("DPEMPTY")
@@ -431,6 +510,9 @@ def dq_roles(costs, NQ, NO, NK, NV, single_ds_barrier=False):
     roles = dict(producer_qk=producer(True), producer_dov=producer(False), issuer_a=issuer_a(),
                  issuer_b=issuer_b())
     roles.update({f"compute{g}": compute_group() for g in range(G)})
+    bars.update(feed_bars(costs, len(roles) - 1))
+    roles = {k: with_feed(g, costs, "claimer" if k == "producer_qk" else "reader", feed)
+             for k, g in roles.items()}
     return roles, bars
 
 
@@ -465,6 +547,39 @@ def test_dq_protocol(rings):
     for seed in SEEDS:
         roles, bars = dq_roles(item_costs(seed), *rings)
         assert run(roles, bars, seed) is None, f"seed {seed}"
+
+
+# The claimed mode runs only in the SiLU/L kernels (softmax=False) of the dK/dV and
+# forward passes; the dQ model has the SiLU/L kernel's two-Q-tile walk for D = 64 and the
+# single-tile one for D = 128.
+@pytest.mark.parametrize("rings", [(2, 3, 2), (2, 6, 6)])
+def test_forward_protocol_with_item_ring(rings):
+    for seed in SEEDS:
+        roles, bars = fwd_roles(item_costs(seed), *rings, False, seed, feed=True)
+        assert run(roles, bars, seed) is None, f"seed {seed}"
+
+
+@pytest.mark.parametrize("rings", [(3, 2), (4, 4)])
+def test_dkdv_protocol_with_item_ring(rings):
+    for seed in SEEDS:
+        roles, bars = dkdv_roles(item_costs(seed), *rings, False, seed, feed=True)
+        assert run(roles, bars, seed) is None, f"seed {seed}"
+
+
+@pytest.mark.parametrize("rings", [(1, 1, 3, 2), (2, 2, 6, 4)])
+def test_dq_protocol_with_item_ring(rings):
+    for seed in SEEDS:
+        roles, bars = dq_roles(item_costs(seed), *rings, feed=True)
+        assert run(roles, bars, seed) is None, f"seed {seed}"
+
+
+def test_item_ring_model_finds_a_missing_arrival():
+    """A reader role that never releases its slots must stall the claimer once the ring
+    is full; the model must report it."""
+    costs = [1] * 40
+    roles, bars = fwd_roles(costs, 2, 3, 2, False, 0, feed=True)
+    bars[("FEEDEMPTY", 0)].count = bars[("FEEDEMPTY", 0)].pending = 99  # never completes
+    assert run(roles, bars, 0) is not None
 
 
 def test_model_finds_a_planted_race():
