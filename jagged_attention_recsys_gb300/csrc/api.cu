@@ -260,6 +260,7 @@ Problem make_problem(const jfa_params* p, const int64_t* oq, const int64_t* ok, 
   r.act = act;
   r.rope = nullptr;
   r.rope_npos = 0;
+  r.block_mask = 0;
   return r;
 }
 
@@ -271,7 +272,7 @@ jfa_status empty_call(const Workspace& w, cudaStream_t s) {
 jfa_status run_fwd(const jfa_params* p, Kind kind, int act, const void* q, const void* k,
                    const void* v, const int64_t* oq, const int64_t* ok, void* o, float* lse,
                    void* ws, size_t ws_bytes, cudaStream_t s, const float2* rope = nullptr,
-                   int rope_npos = 0) {
+                   int rope_npos = 0, int block_mask = 0) {
   jfa_status st = check_params(p, kind);
   if (st != JFA_OK) return st;
   if ((st = check_ptrs({oq, ok})) != JFA_OK) return st;
@@ -286,6 +287,7 @@ jfa_status run_fwd(const jfa_params* p, Kind kind, int act, const void* q, const
   Problem pr = make_problem(p, oq, ok, act);
   pr.rope = rope;
   pr.rope_npos = rope_npos;
+  pr.block_mask = block_mask;
   const int path = jfa_path_for(p);
   SchedConfig sc = path == 1 ? tc_fwd_sched(pr) : kSimtSched;
   sc.build_q = 1;
@@ -304,7 +306,7 @@ jfa_status run_bwd(const jfa_params* p, Kind kind, int act, const void* q, const
                    const void* v, const void* o, const float* lse, const void* dout,
                    const int64_t* oq, const int64_t* ok, void* dq, void* dk, void* dv, void* ws,
                    size_t ws_bytes, cudaStream_t s, const float2* rope = nullptr,
-                   int rope_npos = 0) {
+                   int rope_npos = 0, int block_mask = 0) {
   jfa_status st = check_params(p, kind);
   if (st != JFA_OK) return st;
   if ((st = check_ptrs({oq, ok})) != JFA_OK) return st;
@@ -319,6 +321,7 @@ jfa_status run_bwd(const jfa_params* p, Kind kind, int act, const void* q, const
   Problem pr = make_problem(p, oq, ok, act);
   pr.rope = rope;
   pr.rope_npos = rope_npos;
+  pr.block_mask = block_mask;
   const int path = jfa_path_for(p);
   SchedConfig sc = path == 1 ? tc_bwd_sched(pr) : kSimtSched;
   sc.build_q = 1;
@@ -394,7 +397,15 @@ jfa_status check_pooled(const jfa_params* p, int32_t m, void* ws, size_t ws_byte
 // BlockAttention: the self-attention workspace for B + ceil(T/64) block sequences, then the
 // block offsets.
 constexpr int kBlock = 64;
-int64_t block_count(const jfa_params* p) { return p->batch + (p->total_q + kBlock - 1) / kBlock; }
+// The tensor-core path runs two blocks per 128-row tile: the offsets are cut into pieces
+// of two blocks, and the kernels mask each row to its own block's keys (Problem's
+// block_mask), which halves the tiles and items against one block per tile.  The fp32
+// path keeps one block per sequence.
+constexpr int kPiece = 2 * kBlock;
+int piece_rows(const jfa_params* p) { return jfa_path_for(p) == 1 ? kPiece : kBlock; }
+int64_t piece_count(const jfa_params* p, int rows) { return p->batch + (p->total_q + rows - 1) / rows; }
+// the workspace is laid out for the larger count, so that its size does not depend on the path
+int64_t block_count(const jfa_params* p) { return piece_count(p, kBlock); }
 constexpr double kRopeBase = 10000.0;  // the rotary embedding's frequency base
 struct BlockWs {
   size_t offs, rope, total;
@@ -403,9 +414,9 @@ BlockWs block_layout(const jfa_params* p) {
   BlockWs r;
   const int64_t nb = block_count(p);
   r.offs = align_up(workspace_layout(nb, p->total_q, p->total_k, p->heads, nullptr, nullptr), 256);
-  // then the rotary embedding's (cos, sin) table: kBlock positions by dim_qk/2 pairs
+  // then the rotary embedding's (cos, sin) table: the positions of a piece by dim_qk/2 pairs
   r.rope = align_up(r.offs + 8 * (size_t)(nb + 1), 256);
-  r.total = align_up(r.rope + sizeof(float2) * kBlock * (size_t)(p->dim_qk > 0 ? p->dim_qk / 2 : 0), 256);
+  r.total = align_up(r.rope + sizeof(float2) * kPiece * (size_t)(p->dim_qk > 0 ? p->dim_qk / 2 : 0), 256);
   return r;
 }
 
@@ -417,7 +428,7 @@ jfa_status check_block(const jfa_params* p, void* ws, size_t ws_bytes, jfa_param
   *lay = block_layout(p);
   if (ws_bytes < lay->total) return JFA_ERR_WORKSPACE;
   *pb = *p;
-  pb->batch = block_count(p);
+  pb->batch = piece_count(p, piece_rows(p));
   return JFA_OK;
 }
 
@@ -445,14 +456,15 @@ jfa_status block_fwd(const jfa_params* p, const void* q, const void* k, const vo
   if (p->total_q > 0 && (st = check_ptrs({q, k, v, o, lse})) != JFA_OK) return st;
   int64_t* boffs = (int64_t*)((char*)ws + lay.offs);
   float2* table = (float2*)((char*)ws + lay.rope);
+  const int rows = piece_rows(p);
   if (p->batch > 0) {
     Timed t(JFA_KERNEL_AUX, s);
-    if ((st = cu(launch_block_offsets(offs, p->batch, p->total_q, kBlock, boffs, pb.batch, s))) != JFA_OK)
+    if ((st = cu(launch_block_offsets(offs, p->batch, p->total_q, rows, boffs, pb.batch, s))) != JFA_OK)
       return st;
-    if (rope && (st = cu(launch_rope_table(table, kBlock, p->dim_qk, kRopeBase, s))) != JFA_OK) return st;
+    if (rope && (st = cu(launch_rope_table(table, rows, p->dim_qk, kRopeBase, s))) != JFA_OK) return st;
   }
   return run_fwd(&pb, Kind::Self, kActSoftmax, q, k, v, boffs, boffs, o, lse, ws, ws_bytes, s,
-                 rope ? table : nullptr, rope ? kBlock : 0);
+                 rope ? table : nullptr, rope ? rows : 0, rows == kPiece ? kBlock : 0);
 }
 
 jfa_status block_bwd(const jfa_params* p, const void* q, const void* k, const void* v,
@@ -468,14 +480,15 @@ jfa_status block_bwd(const jfa_params* p, const void* q, const void* k, const vo
   if (p->total_q > 0 && (st = check_ptrs({q, k, v, o, lse, dout, dq, dk, dv})) != JFA_OK) return st;
   int64_t* boffs = (int64_t*)((char*)ws + lay.offs);
   float2* table = (float2*)((char*)ws + lay.rope);
+  const int rows = piece_rows(p);
   if (p->batch > 0) {
     Timed t(JFA_KERNEL_AUX, s);
-    if ((st = cu(launch_block_offsets(offs, p->batch, p->total_q, kBlock, boffs, pb.batch, s))) != JFA_OK)
+    if ((st = cu(launch_block_offsets(offs, p->batch, p->total_q, rows, boffs, pb.batch, s))) != JFA_OK)
       return st;
-    if (rope && (st = cu(launch_rope_table(table, kBlock, p->dim_qk, kRopeBase, s))) != JFA_OK) return st;
+    if (rope && (st = cu(launch_rope_table(table, rows, p->dim_qk, kRopeBase, s))) != JFA_OK) return st;
   }
   return run_bwd(&pb, Kind::Self, kActSoftmax, q, k, v, o, lse, dout, boffs, boffs, dq, dk, dv, ws,
-                 ws_bytes, s, rope ? table : nullptr, rope ? kBlock : 0);
+                 ws_bytes, s, rope ? table : nullptr, rope ? rows : 0, rows == kPiece ? kBlock : 0);
 }
 }  // namespace
 }  // namespace jfa

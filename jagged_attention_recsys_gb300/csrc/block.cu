@@ -3,12 +3,14 @@
 // Meta GEM MFU write-up (piletech.kr/articles/112134), details section, BlockAttention
 // bullet: fixed 64-token blocks turn attention from quadratic into linear in the sequence
 // length.  A block is the rows 64c .. 64c+63 of a sequence, counted from its first row (the
-// last block may be shorter).  Attention restricted to blocks is jagged attention over the
-// blocks as sequences of their own, so this kernel only rewrites the offsets: sequence b of
-// length L becomes ceil(L/64) blocks.  The scheduler and the attention kernels then run on
-// the block offsets unchanged.  The block count depends on the lengths, which only the
-// device holds, so the host reserves B + ceil(T/64) block sequences (an upper bound) and
-// the unused ones at the end are empty.
+// last block may be shorter).  Attention restricted to blocks is jagged attention over
+// pieces of the sequences, so this kernel only rewrites the offsets: sequence b of length
+// L becomes ceil(L/P) pieces of P rows.  On the fp32 path a piece is one block (P = 64)
+// and the kernels run on the piece offsets unchanged; on the tensor-core path a piece is
+// two blocks (P = 128, one MMA tile), and the kernels mask each row to its own block's
+// keys, which halves the tiles and the work items.  The piece count depends on the
+// lengths, which only the device holds, so the host reserves B + ceil(T/P) piece
+// sequences (an upper bound) and the unused ones at the end are empty.
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -44,8 +46,8 @@ __device__ int64_t cta_inclusive_scan(int64_t x, int64_t* warp_tot) {
   return r;
 }
 
-// out[0 .. n_out] (n_out + 1 entries): the block offsets, then empty block sequences up to
-// n_out.  Offsets that are not a valid jagged layout give out[0] = -1, which the scheduler
+// out[0 .. n_out] (n_out + 1 entries): the piece offsets (pieces of `block` rows), then
+// empty piece sequences up to n_out.  Offsets that are not a valid jagged layout give out[0] = -1, which the scheduler
 // reports as JFA_ERR_BAD_OFFSETS (nothing is then computed).
 __global__ void __launch_bounds__(kThreads, 1)
 block_offsets_kernel(const int64_t* __restrict__ offs, int64_t batch, int64_t total, int block,

@@ -65,6 +65,10 @@ struct Problem {
   // are at the position of their index inside their sequence.
   const float2* rope;
   int rope_npos;
+  // BlockAttention with two blocks per tile: a row attends only keys of its own
+  // block_mask-row block, counted from its sequence's first row (a power of two that the
+  // compute warpgroups' column spans divide; 0: whole sequences).
+  int block_mask;
 };
 
 // Carve-up of the caller's workspace.

@@ -693,7 +693,8 @@ tc_dkdv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
         const float* rs = reinterpret_cast<const float*>(smem_raw + L::RS_OFF + st * L::RS_BYTES) + grp * HC;
         // valid queries of this group's columns for key j: i < Lq and (causal) i >= j
         const int lo = CAUSAL ? j - i0 : 0;
-        const int hi = j < Lk ? Lq - i0 : 0;
+        int hi = j < Lk ? Lq - i0 : 0;
+        if (p.block_mask > 0 && (j ^ i0) >= p.block_mask) hi = 0;  // another block's queries
         if (lo > 0 || hi < HC) {
 #pragma unroll
           for (int c = 0; c < HC; ++c) sv[c] -= (c >= lo && c < hi) ? 0.f : shift_raw;
@@ -1285,6 +1286,7 @@ tc_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
         const int kb = step * STEP + grp * HC;
         int nvalid = Lk - kb;
         if (CAUSAL) nvalid = min(nvalid, i - kb + 1);
+        if (p.block_mask > 0 && (kb ^ i) >= p.block_mask) nvalid = 0;  // another block's keys
         if (!row_ok) nvalid = 0;
         if (nvalid < HC) {
 #pragma unroll

@@ -440,6 +440,7 @@ tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         const int kb = j * BN + grp * HC;
         int nvalid = Lk - kb;
         if (CAUSAL) nvalid = min(nvalid, i - kb + 1);
+        if (p.block_mask > 0 && (kb ^ i) >= p.block_mask) nvalid = 0;  // another block's keys
         if (nvalid < HC) {
 #pragma unroll
           for (int k = 0; k < HC; ++k) sv[k] -= k < nvalid ? 0.f : shift_raw;

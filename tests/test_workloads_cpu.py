@@ -85,8 +85,9 @@ def test_executed_pairs_hand_worked():
     # causal, 300 rows: q-tiles 0, 1, 2 cover 1, 2, 3 key tiles
     assert ep([300], [300], True) == 6 * 128 * 128
     assert ep([0, 5], [0, 5], True) == 128 * 128
-    # blocks of 64 over 130 rows: blocks of 64, 64, 2, one tile each
-    assert ep([130], [130], True, block=64) == 3 * 128 * 128
+    # blocks of 64 over 130 rows, two blocks per 128-row tile: pieces of 128 and 2 rows
+    assert ep([130], [130], True, block=64) == 2 * 128 * 128
+    assert ep([300, 64], [300, 64], False, block=64) == 4 * 128 * 128
 
 
 def test_tile_occupancy_of_the_workloads():
@@ -98,7 +99,7 @@ def test_tile_occupancy_of_the_workloads():
         occ[name] = workloads.valid_pairs(lq, lk, w.causal, w.block) / workloads.executed_pairs(
             lq, lk, w.causal, w.block)
     expect = {"d64": 0.723, "causal": 0.656, "cross": 0.265, "gdpa": 0.918, "pooled": 0.243,
-              "block": 0.112}
+              "block": 0.205}
     for name, v in expect.items():
         assert abs(occ[name] - v) < 5e-4, (name, occ[name])
 

@@ -152,12 +152,14 @@ def executed_pairs(lq, lk, causal: bool, block: int = 0, tile: int = 128,
     pair (for causal attention, the tiles on and below the diagonal).  With
     ``trim_queries`` (the dK/dV pass, whose products run over a step's valid queries
     only), a tile's query side counts the valid queries rounded up to 16.  With
-    ``block``, each block is a sequence of its own.  valid_pairs / executed_pairs is the
-    share of the executed MMA area that does useful work."""
+    ``block``, the sequences are cut into pieces of ``tile`` rows (tile / block blocks,
+    masked to their own block inside the tile), each a sequence of its own.
+    valid_pairs / executed_pairs is the share of the executed MMA area that does useful
+    work."""
     lq = [int(x) for x in np.asarray(lq).ravel()]
     lk = [int(x) for x in np.asarray(lk).ravel()]
     if block:
-        cut = lambda n: [block] * (n // block) + ([n % block] if n % block else [])
+        cut = lambda n: [tile] * (n // tile) + ([n % tile] if n % tile else [])
         lq = [x for n in lq for x in cut(n)]
         lk = list(lq)
 
