@@ -246,9 +246,15 @@ __device__ __forceinline__ bool kv_rotate_next(int& rot_next, uint32_t& rot_cnt,
   if (!mbar_wait(bar(KV_KFULL), rot_cnt & 1, abort, status) ||
       !mbar_wait(bar(KV_QFULL + qs), (rot_cnt / NQ) & 1, abort, status))
     return false;
-  rope_rotate_share<DQK>(sb + L::K_OFF, rope_rows(key0, x.lk, p.rope_npos), key0, p.rope, wi, nw, lane);
-  rope_rotate_share<DQK>(sb + L::Q_OFF + qs * L::Q_BYTES, rope_rows(row0, x.lq, p.rope_npos), row0, p.rope,
-                         wi, nw, lane);
+  if (key0 == row0) {  // one step: the K and Q tiles start at the same position
+    rope_rotate_pair_share<DQK>(sb + L::K_OFF, rope_rows(key0, x.lk, p.rope_npos), sb + L::Q_OFF + qs * L::Q_BYTES,
+                                rope_rows(row0, x.lq, p.rope_npos), key0, p.rope, wi, nw, lane);
+  } else {
+    rope_rotate_pair_share<DQK>(sb + L::K_OFF, rope_rows(key0, x.lk, p.rope_npos), 0, 0, key0, p.rope, wi, nw,
+                                lane);
+    rope_rotate_pair_share<DQK>(sb + L::Q_OFF + qs * L::Q_BYTES, rope_rows(row0, x.lq, p.rope_npos), 0, 0, row0,
+                                p.rope, wi, nw, lane);
+  }
   __syncwarp();
   if (lane == 0) {
     mbar_arrive(bar(KV_KREADY));
@@ -858,10 +864,16 @@ __device__ __forceinline__ bool q_rotate_next(int& rot_next, uint32_t& rot_cnt, 
   if (!mbar_wait(bar(Q_QFULL + qs), (rot_cnt / NQ) & 1, abort, status) ||
       !mbar_wait(bar(Q_KFULL + ks), (rot_cnt / NK) & 1, abort, status))
     return false;
-  rope_rotate_share<DQK>(sb + L::Q_OFF + qs * L::Q_BYTES, rope_rows(row0, x.lq, p.rope_npos), row0, p.rope,
-                         wi, nw, lane);
-  rope_rotate_share<DQK>(sb + L::K_OFF + ks * L::K_BYTES, rope_rows(0, x.lk, p.rope_npos), 0, p.rope, wi, nw,
-                         lane);
+  if (row0 == 0) {  // the Q tile and the item's one K tile start at position 0
+    rope_rotate_pair_share<DQK>(sb + L::Q_OFF + qs * L::Q_BYTES, rope_rows(0, x.lq, p.rope_npos),
+                                        sb + L::K_OFF + ks * L::K_BYTES, rope_rows(0, x.lk, p.rope_npos), 0,
+                                        p.rope, wi, nw, lane);
+  } else {
+    rope_rotate_pair_share<DQK>(sb + L::Q_OFF + qs * L::Q_BYTES, rope_rows(row0, x.lq, p.rope_npos), 0, 0, row0,
+                                p.rope, wi, nw, lane);
+    rope_rotate_pair_share<DQK>(sb + L::K_OFF + ks * L::K_BYTES, rope_rows(0, x.lk, p.rope_npos), 0, 0, 0, p.rope,
+                                wi, nw, lane);
+  }
   __syncwarp();
   if (lane == 0) {
     mbar_arrive(bar(Q_QREADY + qs));

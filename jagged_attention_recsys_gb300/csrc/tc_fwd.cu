@@ -121,10 +121,16 @@ __device__ __forceinline__ bool fwd_rotate_next(int& rot_next, uint32_t& rot_cnt
   if (!mbar_wait(bar(B_QFULL + qs), (rot_cnt / L::NQB) & 1, abort, status) ||
       !mbar_wait(bar(B_KFULL + ks), (rot_cnt / NK) & 1, abort, status))
     return false;
-  rope_rotate_share<DQK>(sb + L::Q_OFF + qs * L::Q_BYTES, rope_rows(x.tile * BM, x.lq, p.rope_npos),
-                         x.tile * BM, p.rope, wi, nw, lane);
-  rope_rotate_share<DQK>(sb + L::K_OFF + ks * L::K_BYTES, rope_rows(0, x.lk, p.rope_npos), 0, p.rope, wi, nw,
-                         lane);
+  if (x.tile == 0) {  // the Q tile and the item's one K tile start at position 0
+    rope_rotate_pair_share<DQK>(sb + L::Q_OFF + qs * L::Q_BYTES, rope_rows(0, x.lq, p.rope_npos),
+                                   sb + L::K_OFF + ks * L::K_BYTES, rope_rows(0, x.lk, p.rope_npos), 0, p.rope,
+                                   wi, nw, lane);
+  } else {
+    rope_rotate_pair_share<DQK>(sb + L::Q_OFF + qs * L::Q_BYTES, rope_rows(x.tile * BM, x.lq, p.rope_npos), 0,
+                                0, x.tile * BM, p.rope, wi, nw, lane);
+    rope_rotate_pair_share<DQK>(sb + L::K_OFF + ks * L::K_BYTES, rope_rows(0, x.lk, p.rope_npos), 0, 0, 0,
+                                p.rope, wi, nw, lane);
+  }
   __syncwarp();
   if (lane == 0) {
     mbar_arrive(bar(B_QREADY + qs));
