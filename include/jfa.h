@@ -194,9 +194,9 @@ jfa_status jfa_fwd_noalloc(const jfa_params* p, const void* q, const void* k, co
  * p->batch = B, p->total_q = B*m (the rows of o), p->total_k = offs_k[B],
  * p->causal = 0.  The workspace (size from jfa_pooled_workspace_size, 256-byte
  * aligned) also holds the query rows broadcast to every sequence and their
- * per-sequence gradients; it is used as by jfa_cross_fwd / jfa_cross_bwd
- * otherwise, and errors are reported the same way.  Runs on the
- * cross-attention kernels.
+ * per-sequence gradients, kept in fp32 until they are summed; it is used as by
+ * jfa_cross_fwd / jfa_cross_bwd otherwise, and errors are reported the same
+ * way.  Runs on the cross-attention kernels.
  */
 size_t jfa_pooled_workspace_size(const jfa_params* p, int32_t m);
 jfa_status jfa_pooled_fwd(const jfa_params* p, int32_t m, const void* q, const void* k,

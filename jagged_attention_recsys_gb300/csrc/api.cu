@@ -261,6 +261,7 @@ Problem make_problem(const jfa_params* p, const int64_t* oq, const int64_t* ok, 
   r.rope = nullptr;
   r.rope_npos = 0;
   r.block_mask = 0;
+  r.dq_f32 = nullptr;
   return r;
 }
 
@@ -306,7 +307,7 @@ jfa_status run_bwd(const jfa_params* p, Kind kind, int act, const void* q, const
                    const void* v, const void* o, const float* lse, const void* dout,
                    const int64_t* oq, const int64_t* ok, void* dq, void* dk, void* dv, void* ws,
                    size_t ws_bytes, cudaStream_t s, const float2* rope = nullptr,
-                   int rope_npos = 0, int block_mask = 0) {
+                   int rope_npos = 0, int block_mask = 0, float* dq_f32 = nullptr) {
   jfa_status st = check_params(p, kind);
   if (st != JFA_OK) return st;
   if ((st = check_ptrs({oq, ok})) != JFA_OK) return st;
@@ -322,6 +323,7 @@ jfa_status run_bwd(const jfa_params* p, Kind kind, int act, const void* q, const
   pr.rope = rope;
   pr.rope_npos = rope_npos;
   pr.block_mask = block_mask;
+  pr.dq_f32 = jfa_path_for(p) == 1 ? dq_f32 : nullptr;
   const int path = jfa_path_for(p);
   SchedConfig sc = path == 1 ? tc_bwd_sched(pr) : kSimtSched;
   sc.build_q = 1;
@@ -371,12 +373,13 @@ struct PooledWs {
 PooledWs pooled_layout(const jfa_params* p, int32_t m) {
   PooledWs r;
   const size_t e = p->dtype == JFA_BF16 ? 2 : 4;
-  const size_t rows = (size_t)p->batch * (size_t)m * (size_t)p->heads * (size_t)p->dim_qk * e;
+  const size_t elems = (size_t)p->batch * (size_t)m * (size_t)p->heads * (size_t)p->dim_qk;
   r.base = workspace_layout(p->batch, p->total_q, p->total_k, p->heads, nullptr, nullptr);
   r.offs = align_up(r.base, 256);
   r.q_rep = align_up(r.offs + 8 * (size_t)(p->batch + 1), 256);
-  r.dq_rep = align_up(r.q_rep + rows, 256);
-  r.total = align_up(r.dq_rep + rows, 256);
+  // the per-sequence query gradients stay in fp32 until they are summed
+  r.dq_rep = align_up(r.q_rep + elems * e, 256);
+  r.total = align_up(r.dq_rep + elems * 4, 256);
   return r;
 }
 
@@ -608,11 +611,15 @@ jfa_status jfa_pooled_bwd(const jfa_params* p, int32_t m, const void* q, const v
                                          q_rep, offs_q, s))) != JFA_OK)
       return st;
   }
+  // the tensor-core dQ pass leaves the per-sequence gradients in fp32 (no bf16 rounding
+  // before the sum); the fp32 path computes in fp32 anyway
+  const bool rep_f32 = p->dtype == JFA_BF16 && jfa_path_for(p) == 1;
   st = run_bwd(p, Kind::Cross, kActSoftmax, q_rep, k, v, o, lse, dout, offs_q, offs_k, dq_rep, dk,
-               dv, ws, ws_bytes, s);
+               dv, ws, ws_bytes, s, nullptr, 0, 0, rep_f32 ? (float*)dq_rep : nullptr);
   if (st != JFA_OK || p->batch == 0) return st;
   Timed t(JFA_KERNEL_AUX, s);
-  return cu(launch_pooled_reduce(p->dtype, p->batch, (int64_t)m * p->heads * p->dim_qk, dq_rep, dq, s));
+  return cu(launch_pooled_reduce(p->dtype, rep_f32, p->batch, (int64_t)m * p->heads * p->dim_qk, dq_rep, dq,
+                                 s));
 }
 
 size_t jfa_block_workspace_size(const jfa_params* p) {

@@ -69,6 +69,9 @@ struct Problem {
   // block_mask-row block, counted from its sequence's first row (a power of two that the
   // compute warpgroups' column spans divide; 0: whole sequences).
   int block_mask;
+  // When set, the tensor-core dQ pass writes its rows in fp32 here instead of bf16 into
+  // its dq argument (pooled attention's per-sequence query gradients, summed afterwards).
+  float* dq_f32;
 };
 
 // Carve-up of the caller's workspace.
@@ -119,8 +122,8 @@ cudaError_t launch_simt_dq(const Problem& p, int dtype, const void* q, const voi
 // m rows with offsets b*m, and the fixed-order sum of the B per-block query gradients.
 cudaError_t launch_pooled_broadcast(int64_t batch, int32_t m, int64_t row_bytes, const void* q,
                                     void* q_rep, int64_t* offs_q, cudaStream_t s);
-cudaError_t launch_pooled_reduce(int dtype, int64_t batch, int64_t per_seq_elems, const void* dq_rep,
-                                 void* dq, cudaStream_t s);
+cudaError_t launch_pooled_reduce(int dtype, bool rep_f32, int64_t batch, int64_t per_seq_elems,
+                                 const void* dq_rep, void* dq, cudaStream_t s);
 
 // The rotary embedding's (cos, sin) table: npos positions by dim/2 pairs, angle
 // p * base^(-2i/dim), computed in double precision.

@@ -40,9 +40,9 @@ __global__ void pooled_broadcast_kernel(const W* __restrict__ q, W* __restrict__
 // sizes, so the result is bitwise reproducible (no atomics).
 constexpr int kSumWarps = 16;
 
-template <typename T>
+template <typename TI, typename T>
 __global__ void __launch_bounds__(kSumWarps * 32)
-pooled_reduce_kernel(const T* __restrict__ dq_rep, T* __restrict__ dq, int64_t batch,
+pooled_reduce_kernel(const TI* __restrict__ dq_rep, T* __restrict__ dq, int64_t batch,
                      int64_t per_seq) {
   __shared__ float part[kSumWarps][32];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -98,17 +98,20 @@ cudaError_t launch_pooled_broadcast(int64_t batch, int32_t m, int64_t row_bytes,
   return cudaGetLastError();
 }
 
-cudaError_t launch_pooled_reduce(int dtype, int64_t batch, int64_t per_seq_elems, const void* dq_rep,
-                                 void* dq, cudaStream_t s) {
+cudaError_t launch_pooled_reduce(int dtype, bool rep_f32, int64_t batch, int64_t per_seq_elems,
+                                 const void* dq_rep, void* dq, cudaStream_t s) {
   int64_t blocks = (per_seq_elems + 31) / 32;
   const int64_t cap = (int64_t)num_sms() * 4;  // 4 CTAs of 512 threads per SM
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
-  if (dtype == JFA_BF16)
-    pooled_reduce_kernel<__nv_bfloat16><<<(unsigned)blocks, kSumWarps * 32, 0, s>>>(
+  if (dtype == JFA_BF16 && rep_f32)
+    pooled_reduce_kernel<float, __nv_bfloat16><<<(unsigned)blocks, kSumWarps * 32, 0, s>>>(
+        (const float*)dq_rep, (__nv_bfloat16*)dq, batch, per_seq_elems);
+  else if (dtype == JFA_BF16)
+    pooled_reduce_kernel<__nv_bfloat16, __nv_bfloat16><<<(unsigned)blocks, kSumWarps * 32, 0, s>>>(
         (const __nv_bfloat16*)dq_rep, (__nv_bfloat16*)dq, batch, per_seq_elems);
   else
-    pooled_reduce_kernel<float><<<(unsigned)blocks, kSumWarps * 32, 0, s>>>(
+    pooled_reduce_kernel<float, float><<<(unsigned)blocks, kSumWarps * 32, 0, s>>>(
         (const float*)dq_rep, (float*)dq, batch, per_seq_elems);
   return cudaGetLastError();
 }

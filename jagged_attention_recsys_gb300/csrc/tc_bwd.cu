@@ -104,6 +104,12 @@ rowstat_kernel(int64_t total, int heads, const __nv_bfloat16* __restrict__ o,
 __device__ __forceinline__ void store_row_bf16(__nv_bfloat16* dst, const float* x, float f) {
   store32_bf16(dst, x, f);
 }
+// 32 fp32 values times f (dst 16-byte aligned)
+__device__ __forceinline__ void store_row_f32(float* dst, const float* x, float f) {
+#pragma unroll
+  for (int t = 0; t < 32; t += 4)
+    *reinterpret_cast<float4*>(dst + t) = make_float4(x[t] * f, x[t + 1] * f, x[t + 2] * f, x[t + 3] * f);
+}
 
 // =============================================================================
 // dK / dV pass
@@ -1247,7 +1253,12 @@ tc_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
           rope_unrotate_row<CQ>(x, grp * CQ, pend_pos, DQK, p.rope);
         if (pend_row_ok) {
 #pragma unroll
-          for (int c = 0; c < CQ / 32; ++c) store_row_bf16(dq + pend_orow * DQK + grp * CQ + 32 * c, x + 32 * c, p.scale);
+          for (int c = 0; c < CQ / 32; ++c) {
+            if (p.dq_f32)
+              store_row_f32(p.dq_f32 + pend_orow * DQK + grp * CQ + 32 * c, x + 32 * c, p.scale);
+            else
+              store_row_bf16(dq + pend_orow * DQK + grp * CQ + 32 * c, x + 32 * c, p.scale);
+          }
         }
       } else {
         tc_fence_before();
@@ -1365,7 +1376,12 @@ tc_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
         const float z[32] = {0.f};
         if (drains) {
 #pragma unroll
-          for (int c = 0; c < CQ / 32; ++c) store_row_bf16(dq + orow * DQK + grp * CQ + 32 * c, z, 1.f);
+          for (int c = 0; c < CQ / 32; ++c) {
+            if (p.dq_f32)
+              store_row_f32(p.dq_f32 + orow * DQK + grp * CQ + 32 * c, z, 1.f);
+            else
+              store_row_bf16(dq + orow * DQK + grp * CQ + 32 * c, z, 1.f);
+          }
         }
       }
     }

@@ -286,7 +286,8 @@ def test_full_size_pooled_workload():
     assert torch.equal(dq, dq_again)
     ref_dq = dq2.double().view(B, m, *q.shape[1:]).sum(0)
     err = float(torch.linalg.vector_norm(dq.double() - ref_dq) / torch.linalg.vector_norm(ref_dq))
-    assert err <= 4e-3, err  # bf16 rounding of the sum
+    print("\npooled dq against the fp64 sum of the per-sequence cross gradients: rel-L2 %.3g" % err)
+    assert err <= 4e-3, err  # bf16 rounding of those per-sequence terms and of the sum
     rep = dict(batch, q=q_rep)
     fig = whole_batch_check(w, rep, dict(o=o, lse=lse, dq=dq2, dk=dk, dv=dv))
     print("\npooled whole batch: %s" % fig)
