@@ -132,7 +132,9 @@ def with_feed(gen, costs, role_kind, feed):
 
 
 # ----------------------------------------------------------------------------- forward
-def fwd_roles(costs, NQB, NK, NV, softmax, seed, feed=False):
+def fwd_roles(costs, NQB, NK, NV, softmax, seed, feed=False, late_epilogue=False):
+    """late_epilogue: drain the previous item's output after the next item's second step
+    instead of its first (a variant the kernel does not use; with softmax it hangs)."""
     G = 2 if softmax else 4  # softmax warpgroups
     spec = [(("QFULL", s), 1) for s in range(NQB)] + [(("QEMPTY", s), 1) for s in range(NQB)]
     spec += [(("KFULL", s), 1) for s in range(NK)] + [(("KEMPTY", s), 1) for s in range(NK)]
@@ -225,7 +227,7 @@ def fwd_roles(costs, NQB, NK, NV, softmax, seed, feed=False):
                 if rescale:
                     yield W(("PEMPTY", b ^ 1), ((p_it - 1) >> 1) & 1)
                 yield A(("PFULL", b))
-                if pend:
+                if pend and (not late_epilogue or j >= 1 or j == n - 1):  # late: after step 2
                     yield from epilogue()
                 p_it += 1
             if softmax:  # row sums through the REDL pair
@@ -580,6 +582,17 @@ def test_item_ring_model_finds_a_missing_arrival():
     roles, bars = fwd_roles(costs, 2, 3, 2, False, 0, feed=True)
     bars[("FEEDEMPTY", 0)].count = bars[("FEEDEMPTY", 0)].pending = 99  # never completes
     assert run(roles, bars, 0) is not None
+
+
+def test_model_finds_the_softmax_late_epilogue_deadlock():
+    """Softmax may wait, at an item's second step, for the item's first PV product before
+    rescaling O; that product waits for the previous item's output to be drained.  So the
+    forward drains at the first step; drained at the second, the model must hang."""
+    found = 0
+    for seed in SEEDS:
+        roles, bars = fwd_roles(item_costs(seed), 2, 3, 2, True, seed, late_epilogue=True)
+        found += run(roles, bars, seed) is not None
+    assert found > 0
 
 
 def test_model_finds_a_planted_race():
