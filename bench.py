@@ -254,33 +254,42 @@ def config_of(w, lq, lk, world):
 
 
 def gpu_step_fn(jfa, w, d, ws):
+    """One step as a training loop issues it: the batch's work lists built once (the plan),
+    then the forward and backward calls on them.  The pooled calls schedule for themselves
+    (they take no plan)."""
     q, k, v, do, oq, ok = d["q"], d["k"], d["v"], d["do"], d["oq"], d["ok"]
     o, lse, dq, dk, dv = d["o"], d["lse"], d["dq"], d["dk"], d["dv"]
     sc = w.scale
     if w.block:
         def step():
+            jfa.jfa_block_plan(q, k, v, oq, scale=sc, causal=w.causal, ws=ws)
             jfa.jfa_block_fwd(q, k, v, oq, scale=sc, causal=w.causal, o=o, lse=lse, ws=ws,
-                              rope=w.rope)
+                              rope=w.rope, planned=True)
             jfa.jfa_block_bwd(q, k, v, o, lse, do, oq, scale=sc, causal=w.causal, dq=dq, dk=dk,
-                              dv=dv, ws=ws, rope=w.rope)
+                              dv=dv, ws=ws, rope=w.rope, planned=True)
     elif w.pooled:
         def step():
             jfa.jfa_pooled_fwd(q, k, v, ok, scale=sc, o=o, lse=lse, ws=ws)
             jfa.jfa_pooled_bwd(q, k, v, o, lse, do, ok, scale=sc, dq=dq, dk=dk, dv=dv, ws=ws)
     elif w.act == workloads.ACT_SILU_OVER_LEN:
         def step():
-            jfa.jfa_gdpa_fwd(q, k, v, oq, ok, scale=sc, causal=w.causal, o=o, ws=ws)
+            jfa.jfa_plan(q, k, v, oq, ok, scale=sc, causal=w.causal, ws=ws)
+            jfa.jfa_gdpa_fwd(q, k, v, oq, ok, scale=sc, causal=w.causal, o=o, ws=ws, planned=True)
             jfa.jfa_gdpa_bwd(q, k, v, do, oq, ok, scale=sc, causal=w.causal, dq=dq, dk=dk, dv=dv,
-                             ws=ws)
+                             ws=ws, planned=True)
     elif w.cross:
         def step():
-            jfa.jfa_cross_fwd(q, k, v, oq, ok, scale=sc, o=o, lse=lse, ws=ws)
-            jfa.jfa_cross_bwd(q, k, v, o, lse, do, oq, ok, scale=sc, dq=dq, dk=dk, dv=dv, ws=ws)
+            jfa.jfa_plan(q, k, v, oq, ok, scale=sc, ws=ws)
+            jfa.jfa_cross_fwd(q, k, v, oq, ok, scale=sc, o=o, lse=lse, ws=ws, planned=True)
+            jfa.jfa_cross_bwd(q, k, v, o, lse, do, oq, ok, scale=sc, dq=dq, dk=dk, dv=dv, ws=ws,
+                              planned=True)
     else:
         def step():
-            jfa.jfa_fwd(q, k, v, oq, scale=sc, causal=w.causal, o=o, lse=lse, ws=ws)
+            jfa.jfa_plan(q, k, v, oq, scale=sc, causal=w.causal, ws=ws)
+            jfa.jfa_fwd(q, k, v, oq, scale=sc, causal=w.causal, o=o, lse=lse, ws=ws,
+                        planned=True)
             jfa.jfa_bwd(q, k, v, o, lse, do, oq, scale=sc, causal=w.causal, dq=dq, dk=dk, dv=dv,
-                        ws=ws)
+                        ws=ws, planned=True)
     return step
 
 
@@ -446,6 +455,8 @@ def run_ours(args):
         "frac_of_bf16_peak": round(value / world / pk["bf16_tflops"], 4),
         "config": config_of(w, lq, lk, world),
         "timing": {"l2_flush": "256 MiB written between timed steps", "launch": launch,
+                   "schedule": "pooled: each call builds its lists" if w.pooled else
+                               "one plan per step, used by the forward and backward calls",
                    "max_seqs": args.max_seqs or None},
         "roofline": roof, "kernels": kernels, "gpu_launches": launches,
         "e2e": e2e, "cpu_baseline": cpu, "clocks": clk.summary(),

@@ -86,7 +86,10 @@ typedef struct {
   float scale;     /* score scale > 0, normally 1/sqrt(Dqk) */
   int32_t causal;  /* 1: key j visible to query i only if j <= i (self-attention only) */
   int32_t dtype;   /* jfa_dtype of Q, K, V, O, dO, dQ, dK, dV */
+  int32_t flags;   /* 0, or JFA_PLANNED (see jfa_plan); other bits: JFA_ERR_INVALID_ARG */
 } jfa_params;
+
+#define JFA_PLANNED 1
 
 /*
  * Bytes of device workspace the calls below need for these params (work lists
@@ -95,6 +98,43 @@ typedef struct {
  * total_k and heads only.  Returns 0 for a null pointer.
  */
 size_t jfa_workspace_size(const jfa_params* p);
+
+/*
+ * Work lists built once for several calls (the jagged tile scheduler of the
+ * Generalized Dot-Product Attention bullet, run once per batch instead of once
+ * per call).  Every compute call starts by validating its offsets and building
+ * its heavy-first work lists in the workspace.  jfa_plan does that once, for
+ * the forward and the backward calls of these params: the same offsets serve
+ * every call of a training step, and the plan serves every layer whose params
+ * differ from the plan's only in scale, dim_qk, dim_v or dtype, as long as
+ * jfa_path_for gives the same kernel family (and, for jfa_block_rope_*, dim_qk
+ * is the plan's: the rotary table depends on it).
+ *
+ * A later call then passes params with flags = JFA_PLANNED, the same offsets
+ * (the same pointers, their contents unchanged) and the same workspace; it
+ * launches no scheduler and reads the planned lists.  Calls ordered after the
+ * plan on the GPU (the same stream, or an event) may use it any number of
+ * times, one at a time; it stays valid until the workspace is used by a call
+ * without JFA_PLANNED or by another plan.  A planned call does not reset the
+ * status word: it keeps the plan's status (JFA_ERR_BAD_OFFSETS makes every
+ * planned call compute nothing), and after JFA_ERR_TIMEOUT the lists must be
+ * planned again.  Nothing checks that a planned call's offsets are the plan's:
+ * other offsets with the same totals produce wrong results, within the
+ * buffers' bounds.
+ *
+ * jfa_plan serves jfa_fwd, jfa_bwd, jfa_cross_fwd, jfa_cross_bwd, jfa_gdpa_fwd
+ * and jfa_gdpa_bwd (pass offs_q == offs_k for self-attention; causal needs
+ * Lq_b == Lk_b, checked on the device); jfa_block_plan serves the four
+ * BlockAttention calls (it also writes their block offsets and, where
+ * jfa_block_rope_* is supported, the rotary table).  The pooled calls and
+ * jfa_fwd_noalloc return JFA_ERR_UNSUPPORTED for JFA_PLANNED.  Argument errors
+ * are those of the calls served; p->flags may be 0 or JFA_PLANNED and does not
+ * change what is built.
+ */
+jfa_status jfa_plan(const jfa_params* p, const int64_t* offs_q, const int64_t* offs_k, void* ws,
+                    size_t ws_bytes, jfa_stream_t stream);
+jfa_status jfa_block_plan(const jfa_params* p, const int64_t* offs, void* ws, size_t ws_bytes,
+                          jfa_stream_t stream);
 
 /*
  * Softmax self-attention forward (Jagged Flash Attention bullet).  One offsets

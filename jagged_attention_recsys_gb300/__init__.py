@@ -31,6 +31,8 @@ JFA_ERR_CUDA = 6
 JFA_F32 = 0
 JFA_BF16 = 1
 
+JFA_PLANNED = 1
+
 KERNEL_KINDS = {"schedule": 0, "fwd": 1, "bwd_d": 2, "bwd_dkdv": 3, "bwd_dq": 4, "aux": 5}
 
 # Every symbol include/jfa.h declares.
@@ -39,7 +41,8 @@ EXPORTS = ("jfa_workspace_size", "jfa_fwd", "jfa_bwd", "jfa_cross_fwd", "jfa_cro
            "jfa_profile_enable", "jfa_profile_reset", "jfa_profile_read", "jfa_path_for",
            "jfa_fwd_noalloc", "jfa_bbs_plan", "jfa_pooled_workspace_size", "jfa_pooled_fwd",
            "jfa_pooled_bwd", "jfa_block_workspace_size", "jfa_block_fwd", "jfa_block_bwd",
-           "jfa_test_hold", "jfa_block_rope_fwd", "jfa_block_rope_bwd")
+           "jfa_test_hold", "jfa_block_rope_fwd", "jfa_block_rope_bwd", "jfa_plan",
+           "jfa_block_plan")
 
 
 class JfaError(RuntimeError):
@@ -53,7 +56,7 @@ class jfa_params(ctypes.Structure):
                 ("total_k", ctypes.c_int64), ("heads", ctypes.c_int32),
                 ("dim_qk", ctypes.c_int32), ("dim_v", ctypes.c_int32),
                 ("scale", ctypes.c_float), ("causal", ctypes.c_int32),
-                ("dtype", ctypes.c_int32)]
+                ("dtype", ctypes.c_int32), ("flags", ctypes.c_int32)]
 
 
 _lib = None
@@ -117,6 +120,10 @@ def lib():
         L.jfa_block_rope_fwd.restype = ctypes.c_int
         L.jfa_block_rope_bwd.argtypes = [P, vp, vp, vp, vp, fp, vp, i64p, vp, vp, vp, vp, sz, vp]
         L.jfa_block_rope_bwd.restype = ctypes.c_int
+        L.jfa_plan.argtypes = [P, i64p, i64p, vp, sz, vp]
+        L.jfa_plan.restype = ctypes.c_int
+        L.jfa_block_plan.argtypes = [P, i64p, vp, sz, vp]
+        L.jfa_block_plan.restype = ctypes.c_int
         _lib = L
     return _lib
 
@@ -195,17 +202,34 @@ def _check_tensors(q, k, v, offs_q, offs_k=None):
             raise ValueError("offsets must be int64 CUDA tensors")
 
 
-def _prep(q, k, v, offs_q, offs_k, ws, scale, causal):
+def _prep(q, k, v, offs_q, offs_k, ws, scale, causal, planned=False):
     _check_tensors(q, k, v, offs_q, offs_k)
     p = params_for(q, k, v, offs_q, scale, causal)
+    if planned:
+        if ws is None:
+            raise ValueError("a planned call needs the workspace its plan was built in")
+        p.flags = JFA_PLANNED
     if ws is None:
         ws = workspace(p, q.device)
     return p, ws
 
 
-def jfa_fwd(q, k, v, offs, *, scale=None, causal=False, o=None, lse=None, ws=None, stream=None):
+def jfa_plan(q, k, v, offs_q, offs_k=None, *, scale=None, causal=False, ws=None, stream=None):
+    """Builds the work lists of the forward and backward calls on these inputs' shapes and
+    offsets into ``ws`` (allocated if None) and returns ``ws``; later calls given
+    ``planned=True``, the same offsets and this workspace skip their own scheduling.
+    offs_k=None means self-attention."""
+    offs_k = offs_q if offs_k is None else offs_k
+    p, ws = _prep(q, k, v, offs_q, offs_k, ws, scale, causal)
+    _check(lib().jfa_plan(ctypes.byref(p), _ptr(offs_q), _ptr(offs_k), _ptr(ws), ws.numel(),
+                          _stream(stream)), "jfa_plan")
+    return ws
+
+
+def jfa_fwd(q, k, v, offs, *, scale=None, causal=False, o=None, lse=None, ws=None, stream=None,
+            planned=False):
     """Softmax self-attention forward; returns (o, lse)."""
-    p, ws = _prep(q, k, v, offs, None, ws, scale, causal)
+    p, ws = _prep(q, k, v, offs, None, ws, scale, causal, planned)
     if o is None:
         o = torch.empty(q.shape[0], q.shape[1], v.shape[2], dtype=q.dtype, device=q.device)
     if lse is None:
@@ -232,9 +256,9 @@ def jfa_fwd_noalloc(q, k, v, offs, *, scale=None, causal=False, o=None, lse=None
 
 
 def jfa_bwd(q, k, v, o, lse, dout, offs, *, scale=None, causal=False, dq=None, dk=None,
-            dv=None, ws=None, stream=None):
+            dv=None, ws=None, stream=None, planned=False):
     """Softmax self-attention backward; returns (dq, dk, dv)."""
-    p, ws = _prep(q, k, v, offs, None, ws, scale, causal)
+    p, ws = _prep(q, k, v, offs, None, ws, scale, causal, planned)
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv
@@ -245,9 +269,9 @@ def jfa_bwd(q, k, v, o, lse, dout, offs, *, scale=None, causal=False, dq=None, d
 
 
 def jfa_cross_fwd(q, k, v, offs_q, offs_k, *, scale=None, o=None, lse=None, ws=None,
-                  stream=None):
+                  stream=None, planned=False):
     """Softmax cross-attention forward (independent key offsets); returns (o, lse)."""
-    p, ws = _prep(q, k, v, offs_q, offs_k, ws, scale, False)
+    p, ws = _prep(q, k, v, offs_q, offs_k, ws, scale, False, planned)
     if o is None:
         o = torch.empty(q.shape[0], q.shape[1], v.shape[2], dtype=q.dtype, device=q.device)
     if lse is None:
@@ -259,9 +283,9 @@ def jfa_cross_fwd(q, k, v, offs_q, offs_k, *, scale=None, o=None, lse=None, ws=N
 
 
 def jfa_cross_bwd(q, k, v, o, lse, dout, offs_q, offs_k, *, scale=None, dq=None, dk=None,
-                  dv=None, ws=None, stream=None):
+                  dv=None, ws=None, stream=None, planned=False):
     """Backward of jfa_cross_fwd; returns (dq, dk, dv)."""
-    p, ws = _prep(q, k, v, offs_q, offs_k, ws, scale, False)
+    p, ws = _prep(q, k, v, offs_q, offs_k, ws, scale, False, planned)
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv
@@ -272,10 +296,10 @@ def jfa_cross_bwd(q, k, v, o, lse, dout, offs_q, offs_k, *, scale=None, dq=None,
 
 
 def jfa_gdpa_fwd(q, k, v, offs_q, offs_k=None, *, scale=None, causal=False, o=None, ws=None,
-                 stream=None):
+                 stream=None, planned=False):
     """SiLU(s)/L attention forward; returns o.  offs_k=None means self-attention."""
     offs_k = offs_q if offs_k is None else offs_k
-    p, ws = _prep(q, k, v, offs_q, offs_k, ws, scale, causal)
+    p, ws = _prep(q, k, v, offs_q, offs_k, ws, scale, causal, planned)
     if o is None:
         o = torch.empty(q.shape[0], q.shape[1], v.shape[2], dtype=q.dtype, device=q.device)
     _check(lib().jfa_gdpa_fwd(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(offs_q),
@@ -285,10 +309,10 @@ def jfa_gdpa_fwd(q, k, v, offs_q, offs_k=None, *, scale=None, causal=False, o=No
 
 
 def jfa_gdpa_bwd(q, k, v, dout, offs_q, offs_k=None, *, scale=None, causal=False, dq=None,
-                 dk=None, dv=None, ws=None, stream=None):
+                 dk=None, dv=None, ws=None, stream=None, planned=False):
     """Backward of jfa_gdpa_fwd; returns (dq, dk, dv)."""
     offs_k = offs_q if offs_k is None else offs_k
-    p, ws = _prep(q, k, v, offs_q, offs_k, ws, scale, causal)
+    p, ws = _prep(q, k, v, offs_q, offs_k, ws, scale, causal, planned)
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv
@@ -379,13 +403,30 @@ def block_workspace(p: jfa_params, device="cuda") -> torch.Tensor:
     return torch.empty(max(n, 256), dtype=torch.uint8, device=device)
 
 
-def jfa_block_fwd(q, k, v, offs, *, scale=None, causal=False, o=None, lse=None, ws=None,
-                  stream=None, rope=False):
-    """BlockAttention forward (softmax within fixed 64-row blocks); returns (o, lse).
-    With ``rope``, the fused rotary position embedding (jfa_block_rope_fwd)."""
+def _block_prep(q, k, v, offs, ws, scale, causal, planned=False):
     _check_tensors(q, k, v, offs)
     p = params_for(q, k, v, offs, scale, causal)
-    ws = block_workspace(p, q.device) if ws is None else ws
+    if planned:
+        if ws is None:
+            raise ValueError("a planned call needs the workspace its plan was built in")
+        p.flags = JFA_PLANNED
+    return p, block_workspace(p, q.device) if ws is None else ws
+
+
+def jfa_block_plan(q, k, v, offs, *, scale=None, causal=False, ws=None, stream=None):
+    """The block offsets, rotary table and work lists of the BlockAttention calls on these
+    inputs, built into ``ws`` (allocated if None); returns ``ws``."""
+    p, ws = _block_prep(q, k, v, offs, ws, scale, causal)
+    _check(lib().jfa_block_plan(ctypes.byref(p), _ptr(offs), _ptr(ws), ws.numel(),
+                                _stream(stream)), "jfa_block_plan")
+    return ws
+
+
+def jfa_block_fwd(q, k, v, offs, *, scale=None, causal=False, o=None, lse=None, ws=None,
+                  stream=None, rope=False, planned=False):
+    """BlockAttention forward (softmax within fixed 64-row blocks); returns (o, lse).
+    With ``rope``, the fused rotary position embedding (jfa_block_rope_fwd)."""
+    p, ws = _block_prep(q, k, v, offs, ws, scale, causal, planned)
     if o is None:
         o = torch.empty(q.shape[0], q.shape[1], v.shape[2], dtype=q.dtype, device=q.device)
     if lse is None:
@@ -397,12 +438,10 @@ def jfa_block_fwd(q, k, v, offs, *, scale=None, causal=False, o=None, lse=None, 
 
 
 def jfa_block_bwd(q, k, v, o, lse, dout, offs, *, scale=None, causal=False, dq=None, dk=None,
-                  dv=None, ws=None, stream=None, rope=False):
+                  dv=None, ws=None, stream=None, rope=False, planned=False):
     """Backward of jfa_block_fwd; returns (dq, dk, dv).  With ``rope``, the backward of the
     fused rotary position embedding as well (jfa_block_rope_bwd)."""
-    _check_tensors(q, k, v, offs)
-    p = params_for(q, k, v, offs, scale, causal)
-    ws = block_workspace(p, q.device) if ws is None else ws
+    p, ws = _block_prep(q, k, v, offs, ws, scale, causal, planned)
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv

@@ -220,6 +220,7 @@ jfa_status check_params(const jfa_params* p, Kind kind) {
   if (p->dtype != JFA_F32 && p->dtype != JFA_BF16) return JFA_ERR_INVALID_ARG;
   if (!(p->scale > 0.f) || p->scale == INFINITY) return JFA_ERR_INVALID_ARG;
   if (p->causal != 0 && p->causal != 1) return JFA_ERR_INVALID_ARG;
+  if ((p->flags & ~JFA_PLANNED) != 0) return JFA_ERR_INVALID_ARG;
   if (p->batch == 0 && (p->total_q != 0 || p->total_k != 0)) return JFA_ERR_INVALID_ARG;
   if (p->total_q > INT32_MAX || p->total_k > INT32_MAX) return JFA_ERR_UNSUPPORTED;
   // the work lists' item counts (and item indices) are 32-bit
@@ -290,11 +291,11 @@ jfa_status run_fwd(const jfa_params* p, Kind kind, int act, const void* q, const
   pr.rope_npos = rope_npos;
   pr.block_mask = block_mask;
   const int path = jfa_path_for(p);
-  SchedConfig sc = path == 1 ? tc_fwd_sched(pr) : kSimtSched;
-  sc.build_q = 1;
-  sc.build_k = 0;
-  sc.self_attention = (kind == Kind::Self) || p->causal;
-  {
+  if (!(p->flags & JFA_PLANNED)) {
+    SchedConfig sc = path == 1 ? tc_fwd_sched(pr) : kSimtSched;
+    sc.build_q = 1;
+    sc.build_k = 0;
+    sc.self_attention = (kind == Kind::Self) || p->causal;
     Timed t(JFA_KERNEL_SCHEDULE, s);
     if ((st = cu(launch_schedule(pr, w, sc, s))) != JFA_OK) return st;
   }
@@ -325,18 +326,19 @@ jfa_status run_bwd(const jfa_params* p, Kind kind, int act, const void* q, const
   pr.block_mask = block_mask;
   pr.dq_f32 = jfa_path_for(p) == 1 ? dq_f32 : nullptr;
   const int path = jfa_path_for(p);
-  SchedConfig sc = path == 1 ? tc_bwd_sched(pr) : kSimtSched;
-  sc.build_q = 1;
-  sc.build_k = 1;
-  sc.self_attention = (kind == Kind::Self) || p->causal;
+  const bool planned = (p->flags & JFA_PLANNED) != 0;
   // The row terms (softmax only) depend on o, dout and lse alone: they run on a side
   // stream while the scheduler builds the lists, and the caller's stream waits for
-  // them before the dK/dV pass.
-  SideStream* sd = act == kActSoftmax ? side_stream() : nullptr;
+  // them before the dK/dV pass.  A planned call builds no lists and runs them in line.
+  SideStream* sd = act == kActSoftmax && !planned ? side_stream() : nullptr;
   if (sd && (cudaEventRecord(sd->fork, s) != cudaSuccess ||
              cudaStreamWaitEvent(sd->s, sd->fork, 0) != cudaSuccess))
     return JFA_ERR_CUDA;
-  {
+  if (!planned) {
+    SchedConfig sc = path == 1 ? tc_bwd_sched(pr) : kSimtSched;
+    sc.build_q = 1;
+    sc.build_k = 1;
+    sc.self_attention = (kind == Kind::Self) || p->causal;
     Timed t(JFA_KERNEL_SCHEDULE, s);
     if ((st = cu(launch_schedule(pr, w, sc, s))) != JFA_OK) return st;
   }
@@ -363,6 +365,29 @@ jfa_status run_bwd(const jfa_params* p, Kind kind, int act, const void* q, const
   Timed t(JFA_KERNEL_BWD_DQ, s);
   if (path == 1) return cu(launch_tc_dq(pr, q, k, v, lse, dout, dq, w, s));
   return cu(launch_simt_dq(pr, p->dtype, q, k, v, lse, dout, dq, w, s));
+}
+
+// Both lists, for the forward and backward calls of these params: the backward's q-list
+// is the forward's (same tiles and steps on each path), so one build serves the three
+// passes.  self_attention: Lq_b must equal Lk_b.
+jfa_status run_plan(const jfa_params* p, const int64_t* oq, const int64_t* ok, bool self_attention,
+                    void* ws, size_t ws_bytes, cudaStream_t s) {
+  Workspace w;
+  jfa_status st = prepare(p, ws, ws_bytes, &w);
+  if (st != JFA_OK) return st;
+  if (p->batch == 0) return empty_call(w, s);
+  Problem pr = make_problem(p, oq, ok, kActSoftmax);
+  const int path = jfa_path_for(p);
+  SchedConfig sc = path == 1 ? tc_bwd_sched(pr) : kSimtSched;
+  if (path == 1) {
+    const SchedConfig f = tc_fwd_sched(pr);
+    if (f.q_rows != sc.q_rows || f.q_keys_step != sc.q_keys_step) return JFA_ERR_UNSUPPORTED;
+  }
+  sc.build_q = 1;
+  sc.build_k = 1;
+  sc.self_attention = self_attention || p->causal;
+  Timed t(JFA_KERNEL_SCHEDULE, s);
+  return cu(launch_schedule(pr, w, sc, s));
 }
 
 // Pooled multi-head attention: the cross-attention workspace, then the query-row offsets
@@ -460,7 +485,8 @@ jfa_status block_fwd(const jfa_params* p, const void* q, const void* k, const vo
   int64_t* boffs = (int64_t*)((char*)ws + lay.offs);
   float2* table = (float2*)((char*)ws + lay.rope);
   const int rows = piece_rows(p);
-  if (p->batch > 0) {
+  // a planned call finds the block offsets and the rotary table in the workspace
+  if (p->batch > 0 && !(p->flags & JFA_PLANNED)) {
     Timed t(JFA_KERNEL_AUX, s);
     if ((st = cu(launch_block_offsets(offs, p->batch, p->total_q, rows, boffs, pb.batch, s))) != JFA_OK)
       return st;
@@ -484,7 +510,8 @@ jfa_status block_bwd(const jfa_params* p, const void* q, const void* k, const vo
   int64_t* boffs = (int64_t*)((char*)ws + lay.offs);
   float2* table = (float2*)((char*)ws + lay.rope);
   const int rows = piece_rows(p);
-  if (p->batch > 0) {
+  // a planned call finds the block offsets and the rotary table in the workspace
+  if (p->batch > 0 && !(p->flags & JFA_PLANNED)) {
     Timed t(JFA_KERNEL_AUX, s);
     if ((st = cu(launch_block_offsets(offs, p->batch, p->total_q, rows, boffs, pb.batch, s))) != JFA_OK)
       return st;
@@ -492,6 +519,27 @@ jfa_status block_bwd(const jfa_params* p, const void* q, const void* k, const vo
   }
   return run_bwd(&pb, Kind::Self, kActSoftmax, q, k, v, o, lse, dout, boffs, boffs, dq, dk, dv, ws,
                  ws_bytes, s, rope ? table : nullptr, rope ? rows : 0, rows == kPiece ? kBlock : 0);
+}
+
+// The block offsets, the rotary table (where the rotary calls are supported) and the
+// lists of the block sequences.
+jfa_status block_plan(const jfa_params* p, const int64_t* offs, void* ws, size_t ws_bytes, cudaStream_t s) {
+  jfa_params pb;
+  BlockWs lay;
+  jfa_status st = check_block(p, ws, ws_bytes, &pb, &lay);
+  if (st != JFA_OK) return st;
+  if ((st = check_ptrs({offs})) != JFA_OK) return st;
+  int64_t* boffs = (int64_t*)((char*)ws + lay.offs);
+  float2* table = (float2*)((char*)ws + lay.rope);
+  const int rows = piece_rows(p);
+  if (p->batch > 0) {
+    Timed t(JFA_KERNEL_AUX, s);
+    if ((st = cu(launch_block_offsets(offs, p->batch, p->total_q, rows, boffs, pb.batch, s))) != JFA_OK)
+      return st;
+    if (check_rope(p) == JFA_OK && (st = cu(launch_rope_table(table, rows, p->dim_qk, kRopeBase, s))) != JFA_OK)
+      return st;
+  }
+  return run_plan(&pb, boffs, boffs, true, ws, ws_bytes, s);
 }
 }  // namespace
 }  // namespace jfa
@@ -511,6 +559,19 @@ int jfa_path_for(const jfa_params* p) {
   if (p->dtype == JFA_BF16 && tc_supports(p->dim_qk, p->dim_v)) return 1;
   if (p->dtype == JFA_F32 || p->dtype == JFA_BF16) return 0;
   return -1;
+}
+
+jfa_status jfa_plan(const jfa_params* p, const int64_t* offs_q, const int64_t* offs_k, void* ws,
+                    size_t ws_bytes, jfa_stream_t stream) {
+  jfa_status st = check_params(p, Kind::Gdpa);
+  if (st != JFA_OK) return st;
+  if ((st = check_ptrs({offs_q, offs_k})) != JFA_OK) return st;
+  return run_plan(p, offs_q, offs_k, offs_q == offs_k, ws, ws_bytes, (cudaStream_t)stream);
+}
+
+jfa_status jfa_block_plan(const jfa_params* p, const int64_t* offs, void* ws, size_t ws_bytes,
+                          jfa_stream_t stream) {
+  return block_plan(p, offs, ws, ws_bytes, (cudaStream_t)stream);
 }
 
 jfa_status jfa_fwd(const jfa_params* p, const void* q, const void* k, const void* v,
@@ -570,6 +631,7 @@ jfa_status jfa_pooled_fwd(const jfa_params* p, int32_t m, const void* q, const v
   PooledWs lay;
   jfa_status st = check_pooled(p, m, ws, ws_bytes, &lay);
   if (st != JFA_OK) return st;
+  if (p->flags & JFA_PLANNED) return JFA_ERR_UNSUPPORTED;
   // every argument is checked before the broadcast kernel is launched
   if ((st = check_ptrs({offs_k})) != JFA_OK) return st;
   if (p->batch > 0 && (st = check_ptrs({q, o, lse})) != JFA_OK) return st;
@@ -595,6 +657,7 @@ jfa_status jfa_pooled_bwd(const jfa_params* p, int32_t m, const void* q, const v
   PooledWs lay;
   jfa_status st = check_pooled(p, m, ws, ws_bytes, &lay);
   if (st != JFA_OK) return st;
+  if (p->flags & JFA_PLANNED) return JFA_ERR_UNSUPPORTED;
   // every argument is checked before the broadcast kernel is launched
   if ((st = check_ptrs({offs_k})) != JFA_OK) return st;
   if (p->batch > 0 && (st = check_ptrs({q, dq, o, lse, dout})) != JFA_OK) return st;

@@ -81,7 +81,8 @@ struct Feed {
     n_items = n;
     k = 0;
     it = blockIdx.x;
-    // read before any claim of this launch can have raised it; -1 stays -1
+    // -1 (fixed assignment) stays -1; in claimed mode the counter is >= 0 throughout
+    // the launch, including after the rewind at its end
     dyn = DYN && *reinterpret_cast<const volatile int*>(ctr) >= 0;
     if (!dyn && it < n_items) nxt = load_item(list, it);
   }
@@ -122,6 +123,14 @@ struct Feed {
 // still loads the current item's, and indices are taken two ahead, so that neither the
 // counter's round trip nor the list load is waited for where it is issued: the index
 // taken at one call is loaded at the next and published at the one after.
+//
+// Every claimer stops at the first index past the end, so each CTA takes exactly one
+// such index, as its last: they are n_items, n_items + 1, ..., n_items + grid - 1.  The
+// CTA that takes the last of them is the last to touch the counter in the launch and
+// sets it back to 0, so that the next launch over the same list (a list reused by
+// several calls) starts from the beginning.  A CTA that gives up in a bounded wait
+// stops claiming early; the counter then stays where it is, and the lists must be
+// built again (the status word reports the timeout).
 template <bool DYN>
 struct FeedClaimer {
   Feed<DYN> f;   // fixed assignment, ring and published count
@@ -134,6 +143,11 @@ struct FeedClaimer {
   __device__ void init(const FeedRing& r, const WorkItem* l, int* ctr, int n) {
     f.init(r, l, ctr, n);
     counter = ctr;
+  }
+  __device__ int take_index() {
+    const int i = atomicAdd(counter, 1);
+    if ((long long)i == (long long)f.n_items + gridDim.x - 1) atomicExch(counter, 0);
+    return i;
   }
   __device__ bool publish(const WorkItem& x, volatile int* abort, int* status) {
     const uint32_t s = f.k % kFeedSlots;
@@ -163,15 +177,15 @@ struct FeedClaimer {
     if (f.k == 0) {  // prime: item 0 published, item 1 loading, item 2's index taken
       WorkItem x0{};
       x0.cost = -1;
-      const int i0 = f.n_items > 0 ? atomicAdd(counter, 1) : f.n_items;
+      const int i0 = f.n_items > 0 ? take_index() : f.n_items;
       if ((unsigned)i0 < (unsigned)f.n_items) x0 = load_item(f.list, i0);
       cur = x0;
       if (!publish(cur, abort, status)) return false;
       if (cur.cost < 0) {
         nxt_end = true;
       } else {
-        fetch(atomicAdd(counter, 1));
-        if (!nxt_end) idx = atomicAdd(counter, 1);
+        fetch(take_index());
+        if (!nxt_end) idx = take_index();
       }
     }
     const WorkItem x = cur;  // published at the previous call
@@ -182,7 +196,7 @@ struct FeedClaimer {
     cur = y;
     if (!nxt_end) {
       fetch(idx);  // taken at the previous call
-      if (!nxt_end) idx = atomicAdd(counter, 1);
+      if (!nxt_end) idx = take_index();
     }
     w = x;
     return true;

@@ -45,7 +45,8 @@ struct WsHeader {
   int status;    // jfa_status of the last call (device-detected errors only)
   int n_q;       // items in the query-major list
   int n_k;       // items in the key-major list
-  int claim[3];  // next list item to take: forward, dK/dV, dQ (zeroed by the scheduler)
+  int claim[3];  // next list item to take: forward, dK/dV, dQ (0 or -1, set by the
+                 // scheduler; a kernel that takes items rewinds its counter to 0)
   int pad[58];
 };
 static_assert(sizeof(WsHeader) == 256, "workspace header");

@@ -59,6 +59,8 @@ extern "C" jfa_status jfa_fwd_noalloc(const jfa_params* p, const void* q, const 
                                       const void* v, const int64_t* offs, void* o, float* lse,
                                       jfa_stream_t stream) {
   if (p == nullptr) return JFA_ERR_INVALID_ARG;
+  // its scratch is shared by every call, so it cannot hold a plan for later calls
+  if (p->flags != 0) return (p->flags & ~JFA_PLANNED) ? JFA_ERR_INVALID_ARG : JFA_ERR_UNSUPPORTED;
   const size_t need = jfa_workspace_size(p);
   if (need == 0) return JFA_ERR_INVALID_ARG;
   if (need > kNoallocScratchBytes) return JFA_ERR_WORKSPACE;

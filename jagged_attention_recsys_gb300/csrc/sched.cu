@@ -226,27 +226,46 @@ __device__ void build_list(const Problem& p, const ListSpec& L, const Arrays& A,
     __syncthreads();
   }
 
-  // 6. write the items: one thread per item (unit u = item / H, head h = item % H), so
-  //    that a warp's 32-byte stores are consecutive; the unit's sequence comes from a
-  //    binary search of the units' prefix first[].  Every thread has work even when a
-  //    few sequences hold most of the units.
+  // 6. write the items (unit u = sequence tile, item u * H + h).  A warp takes 32
+  //    consecutive units, one per lane: the lane finds its unit's sequence by a binary
+  //    search of the units' prefix first[] (sequences without units are skipped) and forms
+  //    the unit's fields.  The warp then writes the 32 units' items in order, lane l of a
+  //    round writing the round's item l with its unit's fields fetched by shuffles, so the
+  //    warp's 32-byte stores are consecutive and each unit costs one search, not H.
   //    Item counts stay below 2^31 (checked on the host), so the indices are 32-bit.
-  const int n_items = carry * p.heads;
-  for (int64_t e64 = tid; e64 < n_items; e64 += kThreads) {
-    const int e = (int)e64, u = e / p.heads, h = e - u * p.heads;
-    int lo = 0, hi = B - 1;  // the last r with first[r] <= u (sequences without units skipped)
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if (A.first[mid] <= u) lo = mid; else hi = mid - 1;
+  const int n_units = carry, H = p.heads;
+  for (int u0 = warp * 32; u0 < n_units; u0 += kThreads) {
+    const int u = u0 + lane;
+    int fb = 0, ft = 0, fc = 0;
+    int4 fs = make_int4(0, 0, 0, 0);
+    if (u < n_units) {
+      int lo = 0, hi = B - 1;  // the last r with first[r] <= u
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (A.first[mid] <= u) lo = mid; else hi = mid - 1;
+      }
+      fb = A.order[lo];
+      fs = A.seq[fb];
+      ft = tile_at(L, p.causal, A.ntile[fb], u - A.first[lo]);
+      fc = cost_of(L, p.causal, fs.z, fs.w, ft);
     }
-    const int b = A.order[lo];
-    const int4 s = A.seq[b];
-    const int t = tile_at(L, p.causal, A.ntile[b], u - A.first[lo]);
-    WorkItem w;
-    w.b = b; w.h = h; w.tile = t; w.cost = cost_of(L, p.causal, s.z, s.w, t);
-    w.q0 = s.x; w.k0 = s.y; w.lq = s.z; w.lk = s.w;
-    list[e] = w;
+    const int n = min(32, n_units - u0) * H;  // items of this warp's units
+    WorkItem* dst = list + (int64_t)u0 * H;
+    for (int e0 = 0; e0 < n; e0 += 32) {  // uniform over the warp: every lane shuffles
+      const int e = e0 + lane, src = min(e, n - 1) / H;
+      WorkItem w;
+      w.b = __shfl_sync(0xffffffffu, fb, src);
+      w.h = e - src * H;
+      w.tile = __shfl_sync(0xffffffffu, ft, src);
+      w.cost = __shfl_sync(0xffffffffu, fc, src);
+      w.q0 = __shfl_sync(0xffffffffu, fs.x, src);
+      w.k0 = __shfl_sync(0xffffffffu, fs.y, src);
+      w.lq = __shfl_sync(0xffffffffu, fs.z, src);
+      w.lk = __shfl_sync(0xffffffffu, fs.w, src);
+      if (e < n) dst[e] = w;
+    }
   }
+  const int n_items = n_units * H;
   if (tid == 0) {
     *n_out = n_items;
     // claim counters of the kernels that walk this list: 0 (taken from), or -1 (fixed

@@ -120,3 +120,41 @@ def test_profile_read_rejects_bad_kind(L):
     n = ctypes.c_int64()
     ms = ctypes.c_double()
     assert L.jfa_profile_read(99, ctypes.byref(n), ctypes.byref(ms)) == jfa.JFA_ERR_INVALID_ARG
+
+
+def _flagged(flags, **kw):
+    p = P(**kw)
+    p.flags = flags
+    return p
+
+
+def test_plan_and_flags_checked_on_host(L):
+    vp = ctypes.c_void_p
+    # unknown flag bits are argument errors in every call
+    assert _call_fwd(L, _flagged(2)) == jfa.JFA_ERR_INVALID_ARG
+    assert _call_fwd(L, _flagged(3)) == jfa.JFA_ERR_INVALID_ARG
+    assert _call_fwd(L, _flagged(jfa.JFA_PLANNED), ptr=8) == jfa.JFA_ERR_INVALID_ARG
+
+    def plan(p, oq=16, ok=16, ws_ptr=256, ws_bytes=1 << 20):
+        return L.jfa_plan(ctypes.byref(p) if p is not None else None, vp(oq), vp(ok), vp(ws_ptr),
+                          ws_bytes, None)
+
+    assert plan(None) == jfa.JFA_ERR_INVALID_ARG
+    assert plan(P(), oq=0) == jfa.JFA_ERR_INVALID_ARG
+    assert plan(P(), ok=8) == jfa.JFA_ERR_INVALID_ARG
+    assert plan(P(causal=1, total_k=30)) == jfa.JFA_ERR_INVALID_ARG  # causal: equal totals
+    assert plan(_flagged(4)) == jfa.JFA_ERR_INVALID_ARG
+    assert plan(P(), ws_ptr=128) == jfa.JFA_ERR_WORKSPACE
+    assert plan(P(), ws_bytes=16) == jfa.JFA_ERR_WORKSPACE
+    assert L.jfa_block_plan(ctypes.byref(P()), vp(0), vp(256), 1 << 24, None) == jfa.JFA_ERR_INVALID_ARG
+    assert L.jfa_block_plan(ctypes.byref(P()), vp(16), vp(256), 64, None) == jfa.JFA_ERR_WORKSPACE
+    # calls that cannot use a plan say so before anything is launched
+    rc = L.jfa_fwd_noalloc(ctypes.byref(_flagged(jfa.JFA_PLANNED)), vp(16), vp(16), vp(16),
+                           vp(16), vp(16), vp(16), None)
+    assert rc == jfa.JFA_ERR_UNSUPPORTED
+    rc = L.jfa_fwd_noalloc(ctypes.byref(_flagged(2)), vp(16), vp(16), vp(16), vp(16), vp(16),
+                           vp(16), None)
+    assert rc == jfa.JFA_ERR_INVALID_ARG
+    rc = L.jfa_pooled_fwd(ctypes.byref(_flagged(jfa.JFA_PLANNED, batch=3, total_q=12, total_k=30)),
+                          4, vp(16), vp(16), vp(16), vp(16), vp(16), vp(16), vp(256), 1 << 24, None)
+    assert rc == jfa.JFA_ERR_UNSUPPORTED
