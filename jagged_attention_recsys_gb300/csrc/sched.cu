@@ -19,13 +19,19 @@
 // Each item also carries its sequence's first rows and lengths, so a kernel
 // needs one 32-byte load per item and no dependent offset lookups.
 //
-// The lists are built from the offsets in device memory by one CTA (two when both
-// lists are wanted and fit in shared memory, one list each), so a call never
-// synchronises with the host and can be captured in a CUDA graph.  The
-// same kernel validates the offsets and writes the status word.  Per-sequence
-// arrays live in shared memory for up to kCacheB sequences and in the
-// workspace beyond that.
+// The lists are built from the offsets in device memory, so a call never
+// synchronises with the host and can be captured in a CUDA graph.  The same kernel
+// validates the offsets and writes the status word.  Per-sequence arrays live in
+// shared memory for up to kCacheB sequences (sized to the batch, so that a small batch
+// asks for little) and in the workspace beyond that.  Each CTA computes a list's whole
+// order and prefix, which takes a few thousand cycles and no communication; one SM then
+// stores only about 16 bytes a cycle, so a large list is written by several CTAs, each
+// taking a share of the units ("slices"), and both lists, when both are wanted and the
+// arrays fit in shared memory, by separate CTAs.  Past kCacheB sequences one CTA builds
+// everything, in the workspace.
 #include <cuda_runtime.h>
+
+#include <algorithm>
 #include <stdint.h>
 
 #include "internal.h"
@@ -43,16 +49,20 @@ struct SchedShared {
   int warp_tot[32];
   int hist[kBuckets], start[kBuckets], run[kBuckets];
   int wcount[kWarps][kBuckets + 1];  // padded: a bucket's column spans all 32 banks
-  int red;
-  unsigned long long ctot;  // total cost of the list's units
-  int4 seq[kCacheB];      // (q0, k0, lq, lk)
-  int ntile[kCacheB];     // tiles of the list being built
-  int bucket[kCacheB];    // cost bucket of the sequence
-  int order[kCacheB];     // sequences in list order
-  int first[kCacheB + 1]; // first unit of the r-th sequence in list order
+  int wmax[kWarps];                  // per warp: the heaviest sequence's cost
+  unsigned long long wsum[kWarps];   // per warp: the summed cost of its sequences
 };
 
-static_assert(sizeof(SchedShared) <= 232448, "scheduler arrays within one CTA's shared memory");
+// Per-sequence arrays in shared memory, after SchedShared, for up to `cap` sequences:
+// seq (q0, k0, lq, lk) int4 [cap], then int ntile [cap] (tiles of the list being built),
+// bucket [cap] (cost bucket), order [cap] (sequences in list order) and first [cap + 1]
+// (first unit of the r-th sequence in list order).  A launch reserves them for its own
+// batch only, so that a small batch asks for little shared memory.
+constexpr size_t kSeqArraysOff = (sizeof(SchedShared) + 15) / 16 * 16;
+__host__ __device__ constexpr size_t sched_smem_bytes(int cap) {
+  return kSeqArraysOff + 16 * (size_t)cap + 4 * (4 * (size_t)cap + 1);
+}
+static_assert(sched_smem_bytes(kCacheB) <= 232448, "scheduler arrays within one CTA's shared memory");
 
 __device__ __forceinline__ int cdiv(int a, int b) { return (a + b - 1) / b; }
 
@@ -81,25 +91,38 @@ __device__ int block_inclusive_scan(int x, int* warp_tot) {
   return res;
 }
 
+// Tiles and steps are powers of two (checked on the host), so the scheduler divides by
+// shifting.
 struct ListSpec {
   bool key_major;  // false: q-tiles, true: k-tiles
   int tile;        // rows (q-list) or keys (k-list) per item
   int step;        // keys (q-list) or rows (k-list) per inner step
+  int tile_shift, step_shift;  // log2 of tile and step
 };
 
+__device__ __forceinline__ int cdiv_shift(int a, int sh) { return (a + (1 << sh) - 1) >> sh; }
+
 __device__ __forceinline__ int tiles_of(const ListSpec& L, int lq, int lk) {
-  return cdiv(L.key_major ? lk : lq, L.tile);
+  return cdiv_shift(L.key_major ? lk : lq, L.tile_shift);
 }
 
 // Inner steps the kernel runs for tile t of a sequence with lengths (lq, lk).
 __device__ __forceinline__ int cost_of(const ListSpec& L, int causal, int lq, int lk, int t) {
   if (!L.key_major) {
     const int keys = causal ? min(lk, (t + 1) * L.tile) : lk;
-    return cdiv(keys, L.step);
+    return cdiv_shift(keys, L.step_shift);
   }
-  if (!causal) return cdiv(lq, L.step);
+  if (!causal) return cdiv_shift(lq, L.step_shift);
   // rows >= the first key of this tile, counted in whole inner steps
-  return max(0, cdiv(lq, L.step) - (t * L.tile) / L.step);
+  return max(0, cdiv_shift(lq, L.step_shift) - ((t * L.tile) >> L.step_shift));
+}
+
+// Total cost of a sequence's n tiles: closed form where every tile costs the same.
+__device__ __forceinline__ long long total_cost(const ListSpec& L, int causal, int lq, int lk, int n) {
+  if (!causal) return (long long)n * cost_of(L, 0, lq, lk, 0);
+  long long c = 0;
+  for (int t = 0; t < n; ++t) c += cost_of(L, causal, lq, lk, t);
+  return c;
 }
 
 // k-th tile of a sequence in list order (heaviest first): causal q-tiles grow
@@ -121,35 +144,41 @@ struct Arrays {
 // round-robin assignment, whose per-item cost is lower.
 constexpr int kClaimMinMeanCost = 6;
 
+// Builds one list.  Slice `slice` of `slices` CTAs building the same list: every CTA
+// computes the whole order and prefix (steps 1-5, a few thousand cycles) and writes the
+// items of its own share of the units only, so large lists are written by many SMs
+// without any CTA waiting for another.  Slice 0 writes the list's count and counters.
 __device__ void build_list(const Problem& p, const ListSpec& L, const Arrays& A, WorkItem* list,
-                           int* n_out, int* claim0, int* claim1, SchedShared& sh) {
+                           int* n_out, int* claim0, int* claim1, SchedShared& sh, int slice,
+                           int slices) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int B = (int)p.batch;
 
-  // 1. tiles and total cost per sequence; the heaviest total
-  long long cmax = 0, csum = 0;
+  // 1. tiles and total cost per sequence; the heaviest total (per-warp partials, then
+  //    every thread reads the 32 warps' maxima)
+  int cmax = 0;
+  unsigned long long csum = 0;
   for (int b = tid; b < B; b += kThreads) {
     const int4 s = A.seq[b];
     const int n = tiles_of(L, s.z, s.w);
-    long long c = 0;
-    for (int t = 0; t < n; ++t) c += cost_of(L, p.causal, s.z, s.w, t);
+    const long long c = total_cost(L, p.causal, s.z, s.w, n);
     A.ntile[b] = n;
-    A.bucket[b] = (int)min(c, (long long)0x7fffffff);  // total cost for now
-    cmax = max(cmax, c);
-    csum += c;
+    const int ci = (int)min(c, (long long)0x7fffffff);
+    A.bucket[b] = ci;  // total cost for now
+    cmax = max(cmax, ci);
+    csum += (unsigned long long)c;
   }
-  if (tid == 0) sh.ctot = 0;
-  // block max
   for (int o = 16; o > 0; o >>= 1) cmax = max(cmax, __shfl_xor_sync(0xffffffffu, cmax, o));
-  if (tid == 0) sh.red = 0;
-  __syncthreads();
-  if (lane == 0) atomicMax(&sh.red, (int)min(cmax, (long long)0x7fffffff));
   for (int o = 16; o > 0; o >>= 1) csum += __shfl_xor_sync(0xffffffffu, csum, o);
-  if (lane == 0) atomicAdd(&sh.ctot, (unsigned long long)csum);
+  if (lane == 0) {
+    sh.wmax[warp] = cmax;
+    sh.wsum[warp] = csum;
+  }
   for (int c = tid; c < kBuckets; c += kThreads) { sh.hist[c] = 0; sh.run[c] = 0; }
   for (int i = tid; i < kWarps * (kBuckets + 1); i += kThreads) (&sh.wcount[0][0])[i] = 0;
   __syncthreads();
-  const long long top = sh.red;
+  int top = 0;
+  for (int w = 0; w < kWarps; ++w) top = max(top, sh.wmax[w]);
 
   // 2. cost buckets (relative to the heaviest sequence) and their histogram; one atomic
   //    per bucket and warp (equal costs are common: fixed-size blocks all share one)
@@ -157,8 +186,13 @@ __device__ void build_list(const Problem& p, const ListSpec& L, const Arrays& A,
     const int b = base + tid;
     int k = -1;
     if (b < B) {
-      const long long c = A.bucket[b];
-      k = top > 0 ? (int)(c * (kBuckets - 1) / top) : 0;
+      const int c = A.bucket[b];  // 0 <= c <= top
+      if (top <= 0)
+        k = 0;
+      else if (top < (1 << 24))  // c (kBuckets - 1) fits 32 bits
+        k = (int)((unsigned)c * (unsigned)(kBuckets - 1) / (unsigned)top);
+      else
+        k = (int)((long long)c * (kBuckets - 1) / top);
       A.bucket[b] = k;
     }
     const unsigned peers = __match_any_sync(0xffffffffu, k);
@@ -183,7 +217,25 @@ __device__ void build_list(const Problem& p, const ListSpec& L, const Arrays& A,
   __syncthreads();
 
   // 4. stable counting sort of the sequences by bucket -> order[]
-  for (int base = 0; base < B; base += kThreads) {
+  if (B <= kThreads) {
+    // one round: a sequence's place in its bucket is the number of same-bucket sequences
+    // in earlier lanes of its warp plus those in earlier warps, summed directly from the
+    // per-warp counts (zeroed in step 1)
+    const int b = tid;
+    const bool valid = b < B;
+    const int c = valid ? A.bucket[b] : -1;
+    const unsigned peers = __match_any_sync(0xffffffffu, c);
+    const int rank = __popc(peers & ((1u << lane) - 1u));
+    if (valid && rank == 0) sh.wcount[warp][c] = __popc(peers);
+    __syncthreads();
+    if (valid) {
+      int before = 0;
+      for (int w = 0; w < warp; ++w) before += sh.wcount[w][c];
+      A.order[sh.start[c] + before + rank] = b;
+    }
+    __syncthreads();
+  }
+  for (int base = 0; B > kThreads && base < B; base += kThreads) {
     const int b = base + tid;
     const bool valid = b < B;
     const int c = valid ? A.bucket[b] : -1;
@@ -226,51 +278,53 @@ __device__ void build_list(const Problem& p, const ListSpec& L, const Arrays& A,
     __syncthreads();
   }
 
-  // 6. write the items (unit u = sequence tile, item u * H + h).  A warp takes 32
-  //    consecutive units, one per lane: the lane finds its unit's sequence by a binary
-  //    search of the units' prefix first[] (sequences without units are skipped) and forms
-  //    the unit's fields.  The warp then writes the 32 units' items in order, lane l of a
-  //    round writing the round's item l with its unit's fields fetched by shuffles, so the
-  //    warp's 32-byte stores are consecutive and each unit costs one search, not H.
+  // 6. write the items (unit u = sequence tile, item u * H + h) of this slice's units.  A
+  //    warp takes 32 consecutive units, one per lane: the lane finds its unit's sequence by
+  //    a binary search of the units' prefix first[] (sequences without units are skipped)
+  //    and forms the unit's two 16-byte halves.  The warp then writes the units' items in
+  //    order, 16 per store instruction: lane l stores half l & 1 of item l >> 1 with the
+  //    fields fetched from the unit's lane by shuffles, so each instruction fills 512
+  //    contiguous bytes.  One search per unit, not per item.
   //    Item counts stay below 2^31 (checked on the host), so the indices are 32-bit.
   const int n_units = carry, H = p.heads;
-  for (int u0 = warp * 32; u0 < n_units; u0 += kThreads) {
+  const int u_lo = (int)((long long)n_units * slice / slices);
+  const int u_hi = (int)((long long)n_units * (slice + 1) / slices);
+  const int half = lane & 1;
+  for (int u0 = u_lo + warp * 32; u0 < u_hi; u0 += kThreads) {
     const int u = u0 + lane;
-    int fb = 0, ft = 0, fc = 0;
-    int4 fs = make_int4(0, 0, 0, 0);
-    if (u < n_units) {
+    int4 fa = make_int4(0, 0, 0, 0);  // (b, -, tile, cost)
+    int4 fs = make_int4(0, 0, 0, 0);  // (q0, k0, lq, lk)
+    if (u < u_hi) {
       int lo = 0, hi = B - 1;  // the last r with first[r] <= u
       while (lo < hi) {
         const int mid = (lo + hi + 1) >> 1;
         if (A.first[mid] <= u) lo = mid; else hi = mid - 1;
       }
-      fb = A.order[lo];
-      fs = A.seq[fb];
-      ft = tile_at(L, p.causal, A.ntile[fb], u - A.first[lo]);
-      fc = cost_of(L, p.causal, fs.z, fs.w, ft);
+      const int b = A.order[lo];
+      fs = A.seq[b];
+      const int t = tile_at(L, p.causal, A.ntile[b], u - A.first[lo]);
+      fa = make_int4(b, 0, t, cost_of(L, p.causal, fs.z, fs.w, t));
     }
-    const int n = min(32, n_units - u0) * H;  // items of this warp's units
-    WorkItem* dst = list + (int64_t)u0 * H;
-    for (int e0 = 0; e0 < n; e0 += 32) {  // uniform over the warp: every lane shuffles
-      const int e = e0 + lane, src = min(e, n - 1) / H;
-      WorkItem w;
-      w.b = __shfl_sync(0xffffffffu, fb, src);
-      w.h = e - src * H;
-      w.tile = __shfl_sync(0xffffffffu, ft, src);
-      w.cost = __shfl_sync(0xffffffffu, fc, src);
-      w.q0 = __shfl_sync(0xffffffffu, fs.x, src);
-      w.k0 = __shfl_sync(0xffffffffu, fs.y, src);
-      w.lq = __shfl_sync(0xffffffffu, fs.z, src);
-      w.lk = __shfl_sync(0xffffffffu, fs.w, src);
-      if (e < n) dst[e] = w;
+    const int n = min(32, u_hi - u0) * H;  // items of this warp's units
+    int4* dst = reinterpret_cast<int4*>(list + (int64_t)u0 * H);
+    for (int e0 = 0; e0 < n; e0 += 16) {  // uniform over the warp: every lane shuffles
+      const int e = e0 + (lane >> 1), src = min(e, n - 1) / H;
+      const int a0 = __shfl_sync(0xffffffffu, fa.x, src), a2 = __shfl_sync(0xffffffffu, fa.z, src);
+      const int a3 = __shfl_sync(0xffffffffu, fa.w, src), s0 = __shfl_sync(0xffffffffu, fs.x, src);
+      const int s1 = __shfl_sync(0xffffffffu, fs.y, src), s2 = __shfl_sync(0xffffffffu, fs.z, src);
+      const int s3 = __shfl_sync(0xffffffffu, fs.w, src);
+      const int4 v = half ? make_int4(s0, s1, s2, s3) : make_int4(a0, e - src * H, a2, a3);
+      if (e < n) dst[2 * e + half] = v;
     }
   }
   const int n_items = n_units * H;
-  if (tid == 0) {
+  if (tid == 0 && slice == 0) {
     *n_out = n_items;
     // claim counters of the kernels that walk this list: 0 (taken from), or -1 (fixed
     // assignment)
-    const int init = sh.ctot >= (unsigned long long)kClaimMinMeanCost * (unsigned long long)carry ? 0 : -1;
+    unsigned long long ctot = 0;  // total cost of the list's units
+    for (int w = 0; w < kWarps; ++w) ctot += sh.wsum[w];
+    const int init = ctot >= (unsigned long long)kClaimMinMeanCost * (unsigned long long)carry ? 0 : -1;
     *claim0 = init;
     if (claim1) *claim1 = init;
   }
@@ -279,14 +333,16 @@ __device__ void build_list(const Problem& p, const ListSpec& L, const Arrays& A,
 
 __global__ void __launch_bounds__(kThreads, 1)
 schedule_kernel(Problem p, Workspace ws, ListSpec lq_spec, ListSpec lk_spec, int build_q,
-                int build_k, int self_attention) {
+                int build_k, int self_attention, int split, int slices) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   SchedShared& sh = *reinterpret_cast<SchedShared*>(smem_raw);
   const int tid = threadIdx.x;
   const int B = (int)p.batch;
   Arrays A;
   if (B <= kCacheB) {
-    A = Arrays{sh.seq, sh.ntile, sh.bucket, sh.order, sh.first};
+    int4* seq = reinterpret_cast<int4*>(smem_raw + kSeqArraysOff);
+    int* ints = reinterpret_cast<int*>(seq + B);
+    A = Arrays{seq, ints, ints + B, ints + 2 * B, ints + 3 * B};
   } else {
     A = Arrays{ws.seq, ws.seq_ints, ws.seq_ints + (B + 1), ws.seq_ints + 2 * (B + 1),
                ws.seq_ints + 3 * (B + 1)};
@@ -310,7 +366,7 @@ schedule_kernel(Problem p, Workspace ws, ListSpec lq_spec, ListSpec lk_spec, int
   }
   bad = __syncthreads_or(bad);
   if (bad) {
-    if (tid == 0) {
+    if (tid == 0 && blockIdx.x == 0) {
       ws.hdr->status = JFA_ERR_BAD_OFFSETS;
       ws.hdr->n_q = 0;
       ws.hdr->n_k = 0;
@@ -318,36 +374,65 @@ schedule_kernel(Problem p, Workspace ws, ListSpec lq_spec, ListSpec lk_spec, int
     }
     return;
   }
-  // With two CTAs (both lists wanted, per-sequence arrays in each CTA's shared memory),
-  // CTA 0 builds the q-list and CTA 1 the k-list; both validated the same offsets.
-  const bool split = gridDim.x == 2;
-  if (!split || blockIdx.x == 0) {
+  // With split (both lists wanted, per-sequence arrays in each CTA's shared memory),
+  // even CTAs build the q-list and odd ones the k-list; both validated the same offsets.
+  // The CTAs of one list are its slices.
+  const int which = split ? (int)(blockIdx.x & 1) : -1;
+  const int slice = split ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
+  if (which != 1) {
     if (build_q)
-      build_list(p, lq_spec, A, ws.list_q, &ws.hdr->n_q, &ws.hdr->claim[kClaimFwd], &ws.hdr->claim[kClaimDq], sh);
-    else if (tid == 0)
+      build_list(p, lq_spec, A, ws.list_q, &ws.hdr->n_q, &ws.hdr->claim[kClaimFwd], &ws.hdr->claim[kClaimDq], sh,
+                 slice, slices);
+    else if (tid == 0 && slice == 0)
       ws.hdr->n_q = 0;
   }
-  if (!split || blockIdx.x == 1) {
+  if (which != 0) {
     if (build_k)
-      build_list(p, lk_spec, A, ws.list_k, &ws.hdr->n_k, &ws.hdr->claim[kClaimDkdv], nullptr, sh);
-    else if (tid == 0)
+      build_list(p, lk_spec, A, ws.list_k, &ws.hdr->n_k, &ws.hdr->claim[kClaimDkdv], nullptr, sh, slice, slices);
+    else if (tid == 0 && slice == 0)
       ws.hdr->n_k = 0;
   }
-  if (tid == 0) ws.hdr->status = JFA_OK;
+  if (tid == 0 && blockIdx.x == 0) ws.hdr->status = JFA_OK;
 }
 
 }  // namespace
 
+int log2_exact(int x) {  // log2 of a power of two, else -1
+  if (x <= 0 || (x & (x - 1)) != 0) return -1;
+  int k = 0;
+  while ((1 << k) < x) ++k;
+  return k;
+}
+
+// Items one CTA writes when a list is cut into slices: fewer would leave most of the
+// launch to the steps every slice repeats.
+constexpr int64_t kItemsPerSlice = 1024;
+constexpr int kMaxSlices = 32;
+
 cudaError_t launch_schedule(const Problem& p, const Workspace& ws, const SchedConfig& c,
                             cudaStream_t s) {
-  ListSpec lq{false, c.q_rows, c.q_keys_step};
-  ListSpec lk{true, c.k_keys, c.k_rows_step};
-  const int smem = (int)sizeof(SchedShared);
-  cudaError_t e = kernel_setup((const void*)schedule_kernel, kThreads, smem);
+  ListSpec lq{false, c.q_rows, c.q_keys_step, log2_exact(c.q_rows), log2_exact(c.q_keys_step)};
+  ListSpec lk{true, c.k_keys, c.k_rows_step, log2_exact(c.k_keys), log2_exact(c.k_rows_step)};
+  if (lq.tile_shift < 0 || lq.step_shift < 0 || lk.tile_shift < 0 || lk.step_shift < 0)
+    return cudaErrorInvalidValue;  // every kernel family's tiles and steps are powers of two
+  cudaError_t e = kernel_setup((const void*)schedule_kernel, kThreads, sched_smem_bytes(kCacheB));
   if (e != cudaSuccess) return e;
+  const bool in_smem = p.batch <= kCacheB;  // else the arrays live in the workspace, one CTA
+  const size_t smem = sched_smem_bytes(in_smem ? (int)p.batch : 0);
   // both lists from two CTAs at once when each CTA can keep its own per-sequence arrays
-  const int grid = (c.build_q && c.build_k && p.batch <= kCacheB) ? 2 : 1;
-  schedule_kernel<<<grid, kThreads, smem, s>>>(p, ws, lq, lk, c.build_q, c.build_k, c.self_attention);
+  const int split = (c.build_q && c.build_k && in_smem) ? 1 : 0;
+  // slices: from a bound on the larger list's items, H (rows / tile + B)
+  int slices = 1;
+  if (in_smem) {
+    int64_t units = 0;
+    if (c.build_q) units = std::max<int64_t>(units, p.total_q / c.q_rows + p.batch);
+    if (c.build_k) units = std::max<int64_t>(units, p.total_k / c.k_keys + p.batch);
+    const int64_t items = units * p.heads;
+    slices = (int)std::min<int64_t>(kMaxSlices, std::max<int64_t>(1, items / kItemsPerSlice));
+  }
+  const int grid = (split ? 2 : 1) * slices;
+  schedule_kernel<<<grid, kThreads, smem, s>>>(p, ws, lq, lk, c.build_q, c.build_k, c.self_attention, split,
+                                               slices);
   return cudaGetLastError();
 }
 

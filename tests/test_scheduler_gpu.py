@@ -105,3 +105,34 @@ def test_large_batch_many_rounds(nseq):
     st, got_q, _ = read_lists(ws, len(lq), int(oq[-1]), int(oq[-1]), H)
     assert st == 0
     assert got_q == with_rows(expected(list(lq), list(lq), H, 128, 128, True, False), lq, lq)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_lists_written_by_many_slices(causal):
+    """A batch whose lists are large enough to be written by several CTAs, each taking a
+    share of the units after computing the whole order itself; the lists must be exactly
+    those of the rule, both from a planned build (q- and k-list at once) and from the
+    forward's own build (q-list alone)."""
+    import jagged_attention_recsys_gb300 as jfa
+
+    rng = np.random.default_rng(21)
+    lq = rng.integers(0, 700, 1500)
+    lq[7] = 0
+    H = 8
+    w = workloads.Workload("s", 0, H, 64, 64, causal, 0, torch.bfloat16, False)
+    batch = workloads.make_batch(w, lq, seed=21, device="cuda")
+    oq = torch.as_tensor(batch["offs_q"], device="cuda")
+    T = int(oq[-1])
+    assert H * (T // 128 + len(lq)) >= 8 * 4096  # several slices per list
+    want_q = with_rows(expected(list(lq), list(lq), H, 128, 128, causal, False), lq, lq)
+    want_k = with_rows(expected(list(lq), list(lq), H, 128, 128, causal, True), lq, lq)
+    ws = jfa.jfa_plan(batch["q"], batch["k"], batch["v"], oq, causal=causal)
+    st, got_q, got_k = read_lists(ws, len(lq), T, T, H)
+    assert st == 0
+    assert got_q == want_q
+    assert got_k == want_k
+    ws2 = jfa.workspace(jfa.params_for(batch["q"], batch["k"], batch["v"], oq, causal=causal))
+    jfa.jfa_fwd(batch["q"], batch["k"], batch["v"], oq, causal=causal, ws=ws2)
+    st, got_q, _ = read_lists(ws2, len(lq), T, T, H)
+    assert st == 0
+    assert got_q == want_q
