@@ -36,8 +36,11 @@ import workloads  # noqa: E402
 METRIC = "useful (unpadded) attention TFLOP/s fwd+bwd on 1 GB300; % of dense BF16 peak"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 L2_FLUSH_BYTES = 256 << 20
-KERNEL_SOURCES = {"fwd": "tc_fwd.cu", "bwd_dkdv": "tc_bwd.cu", "bwd_dq": "tc_bwd.cu",
-                  "bwd_d": "tc_bwd.cu", "schedule": "sched.cu"}
+# the sources each kernel is compiled from (its file and the headers it includes)
+_TC_HEADERS = ("tc.h", "tc_host.h", "tc_ptx.cuh", "feed.cuh", "internal.h")
+KERNEL_SOURCES = {"fwd": ("tc_fwd.cu",) + _TC_HEADERS, "bwd_dkdv": ("tc_bwd.cu",) + _TC_HEADERS,
+                  "bwd_dq": ("tc_bwd.cu",) + _TC_HEADERS, "bwd_d": ("tc_bwd.cu",) + _TC_HEADERS,
+                  "schedule": ("sched.cu", "internal.h")}
 
 
 def log(*a):
@@ -120,12 +123,16 @@ def kernel_flops_bytes(w, lq, lk, tq, tk):
     }
 
 
-def file_sha(name):
-    p = os.path.join(ROOT, "jagged_attention_recsys_gb300", "csrc", name)
-    try:
-        return hashlib.sha256(open(p, "rb").read()).hexdigest()[:16]
-    except OSError:
-        return None
+def file_sha(names):
+    """Hash of the named kernel sources, concatenated in order (None if one is missing)."""
+    h = hashlib.sha256()
+    for name in names:
+        p = os.path.join(ROOT, "jagged_attention_recsys_gb300", "csrc", name)
+        try:
+            h.update(open(p, "rb").read())
+        except OSError:
+            return None
+    return h.hexdigest()[:16]
 
 
 def measured_traffic(kind, workload):
@@ -135,7 +142,7 @@ def measured_traffic(kind, workload):
         ent = d[workload][kind]
     except Exception:
         return None
-    if ent.get("source_sha") != file_sha(KERNEL_SOURCES.get(kind, "")):
+    if ent.get("source_sha") != file_sha(KERNEL_SOURCES.get(kind, ())):
         return None
     return ent.get("dram_bytes_per_launch")
 
