@@ -147,12 +147,58 @@ def measured_traffic(kind, workload):
     return ent.get("dram_bytes_per_launch")
 
 
-class ClockSampler:
-    """nvidia-smi clocks and throttle reasons, sampled every 50 ms in the background.
+class _Nvml:
+    """Read-only NVML queries through ctypes (the driver's libnvidia-ml): SM clock, its
+    maximum, and the active clock-event (throttle) reasons of one GPU."""
+    # clock-event reason bits (nvml.h)
+    BITS = {"sw_power_cap": 0x4, "hw_slowdown": 0x8, "sw_thermal_slowdown": 0x20,
+            "hw_thermal_slowdown": 0x40}
 
-    Each line is stamped with the host time it arrived; the summary covers the lines
-    that arrived inside the marked window (``mark_start`` / ``mark_end``), or, when
-    the window is shorter than the sampling period, the nearest line on each side.
+    def __init__(self, cuda_index):
+        import ctypes
+        lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if lib.nvmlInit_v2() != 0:
+            raise RuntimeError("nvmlInit failed")
+        self.lib, self.c = lib, ctypes
+        self.h = ctypes.c_void_p()
+        try:  # the CUDA device's PCI address, so that the NVML and CUDA numberings may differ
+            pr = torch.cuda.get_device_properties(cuda_index)
+            bus = b"%08x:%02x:%02x.0" % (pr.pci_domain_id, pr.pci_bus_id, pr.pci_device_id)
+            rc = lib.nvmlDeviceGetHandleByPciBusId_v2(ctypes.c_char_p(bus), ctypes.byref(self.h))
+        except Exception:
+            rc = -1
+        if rc != 0 and lib.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(cuda_index),
+                                                          ctypes.byref(self.h)) != 0:
+            raise RuntimeError("no NVML handle")
+        self.max_mhz = self._clock(lib.nvmlDeviceGetMaxClockInfo)
+
+    def _clock(self, fn):
+        v = self.c.c_uint()
+        if fn(self.h, self.c.c_uint(1), self.c.byref(v)) != 0:  # NVML_CLOCK_SM
+            raise RuntimeError("clock query failed")
+        return float(v.value)
+
+    def sample(self):
+        r = self.c.c_ulonglong()
+        fn = getattr(self.lib, "nvmlDeviceGetCurrentClocksEventReasons", None)
+        if fn is None:  # the older name of the same query
+            fn = self.lib.nvmlDeviceGetCurrentClocksThrottleReasons
+        if fn(self.h, self.c.byref(r)) != 0:
+            raise RuntimeError("reason query failed")
+        flags = ["Active" if r.value & b else "Not Active" for b in
+                 (self.BITS["hw_slowdown"], self.BITS["hw_thermal_slowdown"],
+                  self.BITS["sw_thermal_slowdown"], self.BITS["sw_power_cap"])]
+        return "%s, %s, %s" % (self._clock(self.lib.nvmlDeviceGetClockInfo), self.max_mhz,
+                               ", ".join(flags))
+
+
+class ClockSampler:
+    """SM clocks and throttle reasons, sampled in the background: through NVML every
+    10 ms where the driver's library loads, else from nvidia-smi every 50 ms.
+
+    Each sample is stamped with the host time it was taken; the summary covers the
+    samples inside the marked window (``mark_start`` / ``mark_end``), or, when the window
+    is shorter than the sampling period, the nearest sample on each side.
     """
     FIELDS = ("clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,"
               "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
@@ -161,17 +207,37 @@ class ClockSampler:
 
     def __init__(self, device_index):
         self.proc = None
+        self.nvml = None
+        self.stop = False
         self.dev = device_index
         self.stamped = []
         self.t0 = self.t1 = None
+        self.source = None
 
     def _reader(self):
         for line in self.proc.stdout:
             if line.strip():
                 self.stamped.append((time.time(), line))
 
+    def _poller(self):
+        while not self.stop:
+            try:
+                self.stamped.append((time.time(), self.nvml.sample()))
+            except Exception:
+                return
+            time.sleep(0.01)
+
     def __enter__(self):
         import threading
+        try:
+            self.nvml = _Nvml(self.dev)
+            self.nvml.sample()
+            self.thread = threading.Thread(target=self._poller, daemon=True)
+            self.thread.start()
+            self.source = "NVML every 10 ms"
+            return self
+        except Exception:
+            self.nvml = None
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.dev), "--query-gpu=" + self.FIELDS,
@@ -182,6 +248,7 @@ class ClockSampler:
             deadline = time.time() + 3.0  # let the sampler come up before the timed region
             while not self.stamped and time.time() < deadline:
                 time.sleep(0.01)
+            self.source = "nvidia-smi every 50 ms"
         except Exception:
             self.proc = None
         return self
@@ -191,13 +258,16 @@ class ClockSampler:
 
     def mark_end(self):
         self.t1 = time.time()
-        if self.proc is not None:  # one more sample after the window
+        if self.proc is not None or self.nvml is not None:  # one more sample after the window
             n = len(self.stamped)
             deadline = time.time() + 0.5
             while len(self.stamped) == n and time.time() < deadline:
                 time.sleep(0.01)
 
     def __exit__(self, *exc):
+        self.stop = True
+        if self.nvml is not None:
+            self.thread.join(timeout=2)
         if self.proc is not None:
             self.proc.terminate()
             try:
@@ -234,7 +304,7 @@ class ClockSampler:
                     reasons.add(n)
         return {"sm_mhz": statistics.median(r[1] for r in inside),
                 "sm_max_mhz": max(r[2] for r in inside), "samples": len(inside),
-                "window": where, "reasons": sorted(reasons)}
+                "window": where, "reasons": sorted(reasons), "source": self.source}
 
 
 # ----------------------------------------------------------------------------- our arm

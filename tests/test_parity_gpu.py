@@ -434,10 +434,12 @@ def test_full_size_block_rope_workload():
 
 
 # ----------------------------------------------------------------------------- CUDA graphs
+@pytest.mark.parametrize("planned", [False, True])
 @pytest.mark.parametrize("name", ["d64", "gdpa"])
-def test_cuda_graph_replay_matches_separate_calls(name):
+def test_cuda_graph_replay_matches_separate_calls(name, planned):
     """The library's calls capture into a CUDA graph (nothing synchronises with the host),
-    and a replay gives the same outputs, bit for bit, as the calls made one by one."""
+    and a replay gives the same outputs, bit for bit, as the calls made one by one; with
+    ``planned``, the captured step is a plan and the planned calls."""
     import jagged_attention_recsys_gb300 as jfa
 
     w = workloads.WORKLOADS[name]
@@ -452,14 +454,17 @@ def test_cuda_graph_replay_matches_separate_calls(name):
                 dq=torch.empty_like(q), dk=torch.empty_like(k), dv=torch.empty_like(v))
 
     def step():
+        if planned:
+            jfa.jfa_plan(q, k, v, oq, causal=w.causal, ws=ws)
         if w.act == workloads.ACT_SILU_OVER_LEN:
-            jfa.jfa_gdpa_fwd(q, k, v, oq, causal=w.causal, o=outs["o"], ws=ws)
+            jfa.jfa_gdpa_fwd(q, k, v, oq, causal=w.causal, o=outs["o"], ws=ws, planned=planned)
             jfa.jfa_gdpa_bwd(q, k, v, do, oq, causal=w.causal, dq=outs["dq"], dk=outs["dk"],
-                             dv=outs["dv"], ws=ws)
+                             dv=outs["dv"], ws=ws, planned=planned)
         else:
-            jfa.jfa_fwd(q, k, v, oq, causal=w.causal, o=outs["o"], lse=outs["lse"], ws=ws)
+            jfa.jfa_fwd(q, k, v, oq, causal=w.causal, o=outs["o"], lse=outs["lse"], ws=ws,
+                        planned=planned)
             jfa.jfa_bwd(q, k, v, outs["o"], outs["lse"], do, oq, causal=w.causal, dq=outs["dq"],
-                        dk=outs["dk"], dv=outs["dv"], ws=ws)
+                        dk=outs["dk"], dv=outs["dv"], ws=ws, planned=planned)
 
     side = torch.cuda.Stream()
     side.wait_stream(torch.cuda.current_stream())

@@ -132,3 +132,45 @@ def test_planned_call_without_workspace_is_refused():
     oq = torch.as_tensor(b["offs_q"], device="cuda")
     with pytest.raises(ValueError):
         jfa.jfa_fwd(b["q"], b["k"], b["v"], oq, planned=True)
+
+
+@pytest.mark.parametrize("name", ["d64", "causal", "cross", "gdpa", "block", "block_rope"])
+def test_full_size_bench_step_matches_unplanned_calls(name):
+    """The step bench.py times (one plan, then the planned forward and backward calls), on
+    the full-size workload, gives the outputs of calls that each build their own lists, bit
+    for bit; those are the calls the whole-batch oracle tests check."""
+    import bench
+
+    w = workloads.WORKLOADS[name]
+    lq, lk = workloads.lengths(w.name, seed=0)
+    b = workloads.make_batch(w, lq, lk, seed=0, device="cuda")
+    d = dict(q=b["q"], k=b["k"], v=b["v"], do=b["do"],
+             oq=torch.as_tensor(b["offs_q"], device="cuda"),
+             ok=torch.as_tensor(b["offs_k"], device="cuda"))
+    q, k, v, do, oq, ok = d["q"], d["k"], d["v"], d["do"], d["oq"], d["ok"]
+    d["o"] = torch.empty(q.shape[0], q.shape[1], v.shape[2], dtype=q.dtype, device="cuda")
+    d["lse"] = torch.empty(q.shape[0], q.shape[1], dtype=torch.float32, device="cuda")
+    d["dq"], d["dk"], d["dv"] = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    p = jfa.params_for(q, k, v, oq, w.scale, w.causal)
+    ws = jfa.block_workspace(p) if w.block else jfa.workspace(p)
+    bench.gpu_step_fn(jfa, w, d, ws)()
+    torch.cuda.synchronize()
+    assert jfa.jfa_status_check(ws) == jfa.JFA_OK
+    sc, c = w.scale, w.causal
+    if w.block:
+        o, lse = jfa.jfa_block_fwd(q, k, v, oq, scale=sc, causal=c, rope=w.rope)
+        g = jfa.jfa_block_bwd(q, k, v, o, lse, do, oq, scale=sc, causal=c, rope=w.rope)
+        ref = [o, lse, *g]
+    elif w.act == GD:
+        o = jfa.jfa_gdpa_fwd(q, k, v, oq, ok, scale=sc, causal=c)
+        ref = [o, None, *jfa.jfa_gdpa_bwd(q, k, v, do, oq, ok, scale=sc, causal=c)]
+    elif w.cross:
+        o, lse = jfa.jfa_cross_fwd(q, k, v, oq, ok, scale=sc)
+        ref = [o, lse, *jfa.jfa_cross_bwd(q, k, v, o, lse, do, oq, ok, scale=sc)]
+    else:
+        o, lse = jfa.jfa_fwd(q, k, v, oq, scale=sc, causal=c)
+        ref = [o, lse, *jfa.jfa_bwd(q, k, v, o, lse, do, oq, scale=sc, causal=c)]
+    torch.cuda.synchronize()
+    for nm, x in zip(("o", "lse", "dq", "dk", "dv"), ref):
+        if x is not None:
+            assert torch.equal(x, d[nm]), (name, nm)
