@@ -307,11 +307,11 @@ tc_dkdv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
     // Q / dO stages and the accumulators are released by both issuers
     for (int s = 0; s < NQ; ++s) {
       mbar_init(bar(KV_QFULL + s), 1);
-      mbar_init(bar(KV_QEMPTY + s), 2);
+      mbar_init(bar(KV_QEMPTY + s), 1);  // dK's commit (see the issuers)
     }
     for (int s = 0; s < NO; ++s) {
       mbar_init(bar(KV_OFULL + s), 1);
-      mbar_init(bar(KV_OEMPTY + s), 2);
+      mbar_init(bar(KV_OEMPTY + s), 1);  // dV's commit
       mbar_init(bar(KV_RSFULL + s), 32);
     }
     for (int s = 0; s < 2; ++s) {
@@ -471,8 +471,12 @@ tc_dkdv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
     // ------------------------------------------------------------ MMA issuers
     // An MMA issue occupies the issuing thread for most of the MMA's duration and
     // the tensor pipe queues only a few, so the products come from two threads.
-    // Each commit covers only its own thread's MMAs; resources used by both chains
-    // (Q / dO stages, the accumulators) take one commit from each.
+    // Each commit covers only its own thread's MMAs.  The accumulators, read by both
+    // chains, take one commit from each.  A Q stage is read by S^T(g) (issuer A) and
+    // dK(g) (issuer B), a dO stage by dP^T(g) (B) and dV(g) (A); each is released by
+    // the later product's commit alone: dK(g) is issued only after the compute warps
+    // formed dS^T(g), which they do after loading S^T(g) (so S^T(g) has completed), and
+    // dV(g) likewise after dP^T(g).
     {  // the whole warp runs the issuer loop; one elected lane issues
       const bool chain_p = warp == 1;
       constexpr uint32_t idesc_dv = idesc_bf16(TILE, DV, 0, 1);
@@ -506,7 +510,6 @@ tc_dkdv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
           mma_bf16(d_tm, da + off, db + off, idesc, kk > 0 ? 1u : 0u);
         }
         mma_commit(bar((chain_p ? KV_SFULL : KV_DPFULL) + b));
-        mma_commit(bar((chain_p ? KV_QEMPTY : KV_OEMPTY) + st));
         if (c.last()) mma_commit(bar(chain_p ? KV_KEMPTY : KV_VEMPTY));  // last use of this tile
         return true;
       };

@@ -252,11 +252,19 @@ def fwd_roles(costs, NQB, NK, NV, softmax, seed, feed=False, late_epilogue=False
 
 
 # ----------------------------------------------------------------------------- dK/dV
-def dkdv_roles(costs, NQ, NO, softmax, seed, feed=False):
+def dkdv_roles(costs, NQ, NO, softmax, seed, feed=False, stage_release_by_score=False):
+    """stage_release_by_score: a planted mistake; the Q and dO stages are released by the
+    score products (S^T, dP^T) instead of the gradient products that read them later."""
     G = 2 if softmax else 4  # compute warpgroups
     spec = [("KFULL", 1), ("KEMPTY", 1), ("VFULL", 1), ("VEMPTY", 1)]
-    spec += [(("QFULL", s), 1) for s in range(NQ)] + [(("QEMPTY", s), 2) for s in range(NQ)]
-    spec += [(("OFULL", s), 1) for s in range(NO)] + [(("OEMPTY", s), 2) for s in range(NO)]
+    # A Q stage is read by S^T(g) (issuer A) and dK(g) (issuer B), a dO stage by dP^T(g)
+    # (B) and dV(g) (A).  Each is released by one commit, after the later product: dK(g)
+    # is issued only once dS^T(g) exists, which the compute warps form after S^T(g) has
+    # completed, and likewise dV(g) after dP^T(g).  `done` records each product's
+    # completion (at its commit), and the producers check it before refilling a stage.
+    spec += [(("QFULL", s), 1) for s in range(NQ)] + [(("QEMPTY", s), 1) for s in range(NQ)]
+    spec += [(("OFULL", s), 1) for s in range(NO)] + [(("OEMPTY", s), 1) for s in range(NO)]
+    done = set()  # (product, step)
     spec += [(("RSFULL", s), 1) for s in range(NO)]
     for s in range(2):
         spec += [(("SFULL", s), 1), (("SEMPTY", s), G), (("DPFULL", s), 1), (("PDSFULL", s), G),
@@ -276,6 +284,8 @@ def dkdv_roles(costs, NQ, NO, softmax, seed, feed=False):
             for _ in range(n):
                 st = q % NQ
                 yield W(("QEMPTY", st), ((q // NQ) & 1) ^ 1)
+                if q >= NQ:  # the stage's previous readers have completed
+                    assert ("S", q - NQ) in done and ("dK", q - NQ) in done, ("Q stage", q)
                 yield A(("QFULL", st))
                 q += 1
 
@@ -288,6 +298,8 @@ def dkdv_roles(costs, NQ, NO, softmax, seed, feed=False):
             for _ in range(n):
                 so = q % NO
                 yield W(("OEMPTY", so), ((q // NO) & 1) ^ 1)
+                if q >= NO:
+                    assert ("dP", q - NO) in done and ("dV", q - NO) in done, ("dO stage", q)
                 yield A(("OFULL", so))
                 yield A(("RSFULL", so))
                 q += 1
@@ -306,8 +318,10 @@ def dkdv_roles(costs, NQ, NO, softmax, seed, feed=False):
                 yield W(("KDONE", b), ((c["g"] >> 1) & 1) ^ 1)
             else:
                 yield W(("SEMPTY", b), (c["g"] >> 1) & 1)
+            done.add(("S" if chain_p else "dP", c["g"]))
             yield A(("SFULL" if chain_p else "DPFULL", b))
-            yield A(("QEMPTY" if chain_p else "OEMPTY", st))
+            if stage_release_by_score:
+                yield A(("QEMPTY" if chain_p else "OEMPTY", st))
             if c["last"]:
                 yield A("KEMPTY" if chain_p else "VEMPTY")
                 yield ("take", c["kv"] + 1, "cs")  # the leading cursor moves on
@@ -327,11 +341,14 @@ def dkdv_roles(costs, NQ, NO, softmax, seed, feed=False):
             yield W(("PDSFULL", b), (cg["g"] >> 1) & 1)
             if cg["j"] == 0:
                 yield W("ACCEMPTY", (a_it & 1) ^ 1)
+            done.add(("dV" if chain_p else "dK", cg["g"]))
             if chain_p:
-                yield A(("OEMPTY", cg["g"] % NO))
+                if not stage_release_by_score:
+                    yield A(("OEMPTY", cg["g"] % NO))
             else:
                 yield A(("KDONE", b))
-                yield A(("QEMPTY", cg["g"] % NQ))
+                if not stage_release_by_score:
+                    yield A(("QEMPTY", cg["g"] % NQ))
             if cg["last"]:
                 yield A("ACCFULL")
                 a_it += 1
@@ -603,3 +620,17 @@ def test_model_finds_a_planted_race():
         roles, bars = dq_roles(item_costs(seed), 2, 2, 6, 4, single_ds_barrier=True)
         found += run(roles, bars, seed) is not None
     assert found > 0
+
+
+def test_model_finds_a_stage_released_before_its_last_reader():
+    """The Q and dO stages of dK/dV are released by one commit each, after the gradient
+    product that reads them last.  Released instead by the score products, a producer can
+    refill a stage that dK or dV still reads; the model's hazard check must catch it."""
+    caught = 0
+    for seed in SEEDS:
+        roles, bars = dkdv_roles(item_costs(seed), 3, 2, False, seed, stage_release_by_score=True)
+        try:
+            run(roles, bars, seed)
+        except AssertionError:
+            caught += 1
+    assert caught > 0
