@@ -70,3 +70,32 @@ def test_claimed_lists_are_bitwise_deterministic_and_match_the_oracle():
         for name in ("o", "dq", "dk", "dv"):
             assert torch.equal(ref[name], got[name]), name
     whole_batch_check(w, b, ref, seqs=[0, 4, 5], strict_o=False)
+
+
+def test_softmax_cross_over_long_keys_keeps_the_fixed_order():
+    """Softmax cross-attention over long key sequences: the scheduler marks the q-list
+    (many steps per item) for claiming, but the softmax kernels are compiled without the
+    claimer and walk it in the fixed order, leaving the counters as planned; repeated
+    planned calls give the same results bit for bit, and they match the oracle."""
+    rng = np.random.default_rng(8)
+    lq = rng.integers(1, 64, 400)
+    lk = rng.integers(1500, 4096, 400)
+    w = workloads.Workload("feedx", 0, 2, 128, 64, False, workloads.ACT_SOFTMAX, torch.bfloat16, True)
+    b = workloads.make_batch(w, lq, lk, seed=8, device="cuda")
+    oq = torch.as_tensor(b["offs_q"], device="cuda")
+    ok = torch.as_tensor(b["offs_k"], device="cuda")
+    ws = jfa.jfa_plan(b["q"], b["k"], b["v"], oq, ok)
+    status, n_q, n_k, c_fwd, c_dkdv, c_dq = _header(ws)
+    assert status == 0 and c_fwd == 0 and c_dq == 0  # marked for claiming
+    ref = None
+    for _ in range(3):
+        o, lse = jfa.jfa_cross_fwd(b["q"], b["k"], b["v"], oq, ok, ws=ws, planned=True)
+        g = jfa.jfa_cross_bwd(b["q"], b["k"], b["v"], o, lse, b["do"], oq, ok, ws=ws, planned=True)
+        torch.cuda.synchronize()
+        assert _header(ws)[3:6] == [0, c_dkdv, 0]
+        got = dict(o=o, lse=lse, dq=g[0], dk=g[1], dv=g[2])
+        if ref is None:
+            ref = got
+        for name in got:
+            assert torch.equal(ref[name], got[name]), name
+    whole_batch_check(w, b, ref, seqs=[0, 1, 399], strict_o=True)
