@@ -744,12 +744,12 @@ tc_dkdv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
 #pragma unroll
         for (int c = 0; c < HC; c += 2) {
           const float2 d = make_float2(dp[c], dp[c + 1]);
-          float2 ds;
-          if (ACT == kActSoftmax)
-            ds = fmul2(unpack_bf16(pk[c / 2]), fadd2(d, *reinterpret_cast<const float2*>(rs + KSTEP + c)));
-          else
-            ds = fmul2(d, unpack_bf16(fk[c / 2]));
-          dk2[c / 2] = pack_bf16(ds.x, ds.y);
+          if (ACT == kActSoftmax) {
+            const float2 ds = fmul2(unpack_bf16(pk[c / 2]), fadd2(d, *reinterpret_cast<const float2*>(rs + KSTEP + c)));
+            dk2[c / 2] = pack_bf16(ds.x, ds.y);
+          } else {  // dP^T rounded to bf16, times the bf16 factor, rounded once
+            dk2[c / 2] = mul_bf16x2(pack_bf16(d.x, d.y), fk[c / 2]);
+          }
         }
         // P^T then dS^T over this group's own, already loaded columns
         if constexpr (HC == 64) {
@@ -1346,9 +1346,12 @@ tc_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
 #pragma unroll
         for (int c = 0; c < HC; c += 2) {
           const float2 d = make_float2(dp[c], dp[c + 1]);
-          const float2 ds = ACT == kActSoftmax ? fmul2(unpack_bf16(fk[c / 2]), fadd2(d, nd))
-                                               : fmul2(d, unpack_bf16(fk[c / 2]));
-          dk2[c / 2] = pack_bf16(ds.x, ds.y);
+          if (ACT == kActSoftmax) {
+            const float2 ds = fmul2(unpack_bf16(fk[c / 2]), fadd2(d, nd));
+            dk2[c / 2] = pack_bf16(ds.x, ds.y);
+          } else {  // dP rounded to bf16, times the bf16 factor, rounded once
+            dk2[c / 2] = mul_bf16x2(pack_bf16(d.x, d.y), fk[c / 2]);
+          }
         }
         // dS over this group's own S columns (already loaded above)
         if constexpr (HC == 64)

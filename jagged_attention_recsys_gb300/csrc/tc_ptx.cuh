@@ -312,6 +312,13 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
   return r;
 }
+// Elementwise product of two packed bf16 pairs, rounded once to bf16 (a fused multiply-add
+// with -0 as the addend, so a product of +0 stays +0).
+__device__ __forceinline__ uint32_t mul_bf16x2(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(0x80008000u));
+  return r;
+}
 // 32-byte global store (dst must be 32-byte aligned)
 __device__ __forceinline__ void st_global_v8(void* dst, const uint32_t* r) {
   asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(dst), "r"(r[0]),
