@@ -164,6 +164,11 @@ enum : uint32_t {
 };
 static_assert(8 * KV_COUNT + 8 <= 640, "mbarriers, TMEM slot and abort flag in front of the item ring");
 
+// bf16 pair (low, high) of a packed word to two floats, exactly
+__device__ __forceinline__ float2 unpack_bf16(uint32_t u) {
+  return make_float2(__uint_as_float(u << 16), __uint_as_float(u & 0xffff0000u));
+}
+
 // Walks the steps of a CTA's items in order (items without steps are skipped):
 // item w, local step j, global step g, Q/dO stage counter q, item counter kv.  The
 // items come from the CTA's feed; `arrive` marks the cursor that releases each feed
@@ -741,7 +746,12 @@ tc_dkdv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
           const float2 d = make_float2(dp[c], dp[c + 1]);
           if (ACT == kActSoftmax) {  // dP^T - D in fp32, rounded to bf16, times the bf16 P^T
             const float2 t = fadd2(d, *reinterpret_cast<const float2*>(rs + KSTEP + c));
-            dk2[c / 2] = mul_bf16x2(pack_bf16(t.x, t.y), pk[c / 2]);
+            if constexpr (ROPE) {  // measured faster in fp32 here (register allocation)
+              const float2 ds = fmul2(unpack_bf16(pk[c / 2]), t);
+              dk2[c / 2] = pack_bf16(ds.x, ds.y);
+            } else {
+              dk2[c / 2] = mul_bf16x2(pack_bf16(t.x, t.y), pk[c / 2]);
+            }
           } else {  // dP^T rounded to bf16, times the bf16 factor, rounded once
             dk2[c / 2] = mul_bf16x2(pack_bf16(d.x, d.y), fk[c / 2]);
           }
@@ -1343,7 +1353,12 @@ tc_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
           const float2 d = make_float2(dp[c], dp[c + 1]);
           if (ACT == kActSoftmax) {  // dP - D in fp32, rounded to bf16, times the bf16 P
             const float2 t = fadd2(d, nd);
-            dk2[c / 2] = mul_bf16x2(pack_bf16(t.x, t.y), fk[c / 2]);
+            if constexpr (ROPE) {  // measured faster in fp32 here (register allocation)
+              const float2 ds = fmul2(unpack_bf16(fk[c / 2]), t);
+              dk2[c / 2] = pack_bf16(ds.x, ds.y);
+            } else {
+              dk2[c / 2] = mul_bf16x2(pack_bf16(t.x, t.y), fk[c / 2]);
+            }
           } else {  // dP rounded to bf16, times the bf16 factor, rounded once
             dk2[c / 2] = mul_bf16x2(pack_bf16(d.x, d.y), fk[c / 2]);
           }
