@@ -621,7 +621,8 @@ tc_dkdv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
                 dv + pend_krow * DV + (grp & 1) * (DV / 2), 1.f);
         else
           drain(std::integral_constant<int, DQK / 2>{}, tmem + lane_base + T_DK + (grp & 1) * (DQK / 2),
-                dk + pend_krow * DQK + (grp & 1) * (DQK / 2), p.scale);
+                dk + pend_krow * DQK + (grp & 1) * (DQK / 2),
+                ACT == kActSoftmax ? p.scale : 0.5f * p.scale);  // SiLU/L: dS^T was doubled
       } else {
         // half grp of dK and half grp of dV
         float x[DQK / 2], y[DV / 2];
@@ -672,7 +673,6 @@ tc_dkdv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
         break;
       }
       const float inv_len = 1.0f / (float)max(Lq, 1);
-      const float2 hl = make_float2(0.5f * inv_len, 0.5f * inv_len);
       const float2 il = make_float2(inv_len, inv_len);
       const int qs0 = CAUSAL ? key0 / KSTEP : 0;
       for (int step = 0; step < n; ++step, ++q_it, ++s_it) {
@@ -724,11 +724,14 @@ tc_dkdv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
             const float2 e = ffma2(x, cc, *reinterpret_cast<const float2*>(rs + c));
             pv = make_float2(ex2(e.x), ex2(e.y));
           } else {
-            // u = s c, h = u/2, t = tanh h: P = h (1+t)/L, SiLU'(u)/L = (1+t)/(2L) (1 + h - h t)
+            // u = s c, h = u/2, t = tanh h: P = h (1+t)/L, SiLU'(u)/L = (1+t)/(2L) (1 + h - h t).
+            // The factor formed here is twice SiLU'(u)/L, sharing (1+t)/L with P; dS^T and dK
+            // come out doubled, exactly, and the dK epilogue halves its scale.
             const float2 hh = fmul2(x, hc);
             const float2 t = make_float2(tanh_approx(hh.x), tanh_approx(hh.y));
-            pv = fmul2(hh, ffma2(t, il, il));
-            const float2 f = fmul2(ffma2(t, hl, hl), ffma2(make_float2(-hh.x, -hh.y), t, fadd2(hh, one)));
+            const float2 ti = ffma2(t, il, il);
+            pv = fmul2(hh, ti);
+            const float2 f = fmul2(ti, ffma2(make_float2(-hh.x, -hh.y), t, fadd2(hh, one)));
             fk[c / 2] = pack_bf16(f.x, f.y);
           }
           pk[c / 2] = pack_bf16(pv.x, pv.y);
