@@ -137,3 +137,73 @@ def test_default_workload_is_gdpa():
 
     src = open(os.path.join(ROOT, "bench.py")).read()
     assert 'ap.add_argument("--workload", default="gdpa"' in src
+
+
+def _bench_module():
+    import importlib.util
+    spec = importlib.util.spec_from_file_location("bench_under_test", os.path.join(ROOT, "bench.py"))
+    mod = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mod)
+    return mod
+
+
+def test_traffic_is_reported_only_while_the_kernel_sources_are_unchanged(monkeypatch):
+    b = _bench_module()
+    stored = json.load(open(os.path.join(ROOT, "profiles", "traffic.json")))["gdpa"]["bwd_dkdv"]
+    # the committed capture names the hash of every source the dK/dV kernel is built from
+    assert stored["source_sha"] == b.file_sha(b.KERNEL_SOURCES["bwd_dkdv"])
+    assert b.measured_traffic("bwd_dkdv", "gdpa") == stored["dram_bytes_per_launch"]
+    # a change to any of them (here: one more file in the list) voids the figure
+    monkeypatch.setitem(b.KERNEL_SOURCES, "bwd_dkdv", b.KERNEL_SOURCES["bwd_dkdv"] + ("sched.cu",))
+    assert b.measured_traffic("bwd_dkdv", "gdpa") is None
+    assert b.measured_traffic("fwd", "no_such_workload") is None
+    assert b.file_sha(("no_such_file.cu",)) is None
+
+
+def test_clock_summary_inside_and_around_the_window():
+    b = _bench_module()
+    c = b.ClockSampler(0)
+    na, ac = "Not Active", "Active"
+    c.stamped = [(0.9, "2070, 2070, %s, %s, %s, %s" % (na, na, na, na)),
+                 (1.1, "1900, 2070, %s, %s, %s, %s" % (na, na, na, ac)),
+                 (1.2, "1950, 2070, %s, %s, %s, %s" % (na, na, na, na)),
+                 (1.3, "2000, 2070, %s, %s, %s, %s" % (na, na, na, na)),
+                 (1.6, "2070, 2070, %s, %s, %s, %s" % (na, na, na, na))]
+    c.t0, c.t1, c.source = 1.0, 1.5, "test"
+    s = c.summary()
+    assert s["samples"] == 3 and s["sm_mhz"] == 1950 and s["sm_max_mhz"] == 2070
+    assert s["reasons"] == ["sw_power_cap"] and s["window"] == "during the timed region"
+    c.t0, c.t1 = 1.31, 1.35  # shorter than the sampling period: the nearest sample each side
+    s = c.summary()
+    assert s["samples"] == 2 and s["sm_mhz"] == (2000 + 2070) / 2
+    assert s["window"].startswith("nearest samples around")
+
+
+class _Recorder:
+    """Stands in for the binding: records the calls a step makes, in order."""
+
+    def __init__(self):
+        self.calls = []
+
+    def __getattr__(self, name):
+        def call(*a, **kw):
+            self.calls.append((name, kw.get("planned", False)))
+        return call
+
+
+def test_bench_step_is_one_plan_then_planned_calls():
+    import workloads
+
+    b = _bench_module()
+    d = {n: None for n in ("q", "k", "v", "do", "oq", "ok", "o", "lse", "dq", "dk", "dv")}
+    for name, plan, calls in (("gdpa", "jfa_plan", ("jfa_gdpa_fwd", "jfa_gdpa_bwd")),
+                              ("d64", "jfa_plan", ("jfa_fwd", "jfa_bwd")),
+                              ("cross", "jfa_plan", ("jfa_cross_fwd", "jfa_cross_bwd")),
+                              ("block", "jfa_block_plan", ("jfa_block_fwd", "jfa_block_bwd")),
+                              ("block_rope", "jfa_block_plan", ("jfa_block_fwd", "jfa_block_bwd"))):
+        rec = _Recorder()
+        b.gpu_step_fn(rec, workloads.WORKLOADS[name], d, ws=None)()
+        assert rec.calls == [(plan, False), (calls[0], True), (calls[1], True)], name
+    rec = _Recorder()  # the pooled calls take no plan
+    b.gpu_step_fn(rec, workloads.WORKLOADS["pooled"], d, ws=None)()
+    assert rec.calls == [("jfa_pooled_fwd", False), ("jfa_pooled_bwd", False)]
