@@ -64,8 +64,6 @@ __host__ __device__ constexpr size_t sched_smem_bytes(int cap) {
 }
 static_assert(sched_smem_bytes(kCacheB) <= 232448, "scheduler arrays within one CTA's shared memory");
 
-__device__ __forceinline__ int cdiv(int a, int b) { return (a + b - 1) / b; }
-
 // Inclusive block-wide scan of one int per thread.
 __device__ int block_inclusive_scan(int x, int* warp_tot) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
